@@ -1,0 +1,287 @@
+"""CPU oracle for the Beam MoE sublayer -- TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, FP64 NumPy restatement of what the layer computes. Only the
+tests, the package's smoke check and the benchmark's CPU-baseline leg may use
+it; the product path never imports it. It shares no code with the CUDA path.
+
+Sources (release pages about the model, cited by title and section):
+  [P1] "Reflection 发布 Beam 501B 开源模型，支持 1M tokens 上下文"
+       sections 专家混合模型 (experts, router), 残差流 (residual stream,
+       FP32 steps, pre/post norm).
+  [P3] tech.fxxz.com article on the Beam release, sections 混合专家系统 and
+       残差流设计 (a machine-translated copy of [P1]).
+  [P4] "Welcome Beam: a 501B open model you can own, customize, and scale"
+       (English excerpt: layer counts, experts, residual step weights).
+  [P5] "Reflection 放出 501B 的 Beam 权重：四套精度、滑动窗口和一场榜单落差"
+       section "config.json 里还有六处能直接抄的细节" (n_group 8,
+       topk_group 4, norm_topk_prob true, routed_scaling_factor 2.5).
+
+Readings where the pages leave a step open (each is also listed in the
+design notes):
+  * scaling: the combine weights are multiplied by 2.5 ([P1] 专家混合模型,
+    [P5] routed_scaling_factor); [P3] "缩小为 2.5" is a garbled translation.
+  * normalisation divides by the sum of the 8 selected sigmoid scores, with
+    no epsilon.
+  * a router-logit bias, when given, is added before the sigmoid, so it
+    changes selection and weights alike.
+  * ties: lower expert index first, lower group index first.
+  * decisions (group ranking, expert ranking) are taken on FP32 scores, the
+    router's precision on the pages ([P1] 残差流: the router runs in FP32);
+    the group score is the FP32 sum of the two largest FP32 scores.
+  * SwiGLU: silu(x W_g^T) * (x W_u^T), then W_d.
+  * RMSNorm: v / sqrt(mean(v^2) + eps) * gain, eps = 1e-6, plain
+    multiplicative gain.
+  * post-norm applies to the combined MoE output before the 1/sqrt(k) weight.
+  * the pre-norm output is rounded to BF16, the activation dtype the expert
+    matmuls consume.
+
+Everything is FP64 except the FP32 rounding of the router scores (above) and
+the BF16 rounding of the pre-norm output.
+
+Every function has a pin in tests/test_oracle_pins.py that checks it against
+something other than itself (closed forms, hand-worked examples, brute force
+and library routines).
+"""
+from __future__ import annotations
+
+import math
+from typing import Callable, Optional, Tuple
+
+import numpy as np
+
+F64 = np.float64
+F32 = np.float32
+
+
+# ----------------------------------------------------------------------------
+# elementwise helpers
+# ----------------------------------------------------------------------------
+def bf16_round(a) -> np.ndarray:
+    """Round to the nearest BF16 value (ties to even); returns float32 values.
+
+    BF16 keeps the top 16 bits of an IEEE float32. Finite inputs only.
+    """
+    u = np.ascontiguousarray(np.asarray(a, dtype=F32)).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)).astype(np.uint32)
+    return r.view(F32)
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    """Logistic function 1 / (1 + e^-z), FP64."""
+    z = np.asarray(z, dtype=F64)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """z * sigmoid(z), FP64."""
+    z = np.asarray(z, dtype=F64)
+    return z * sigmoid(z)
+
+
+def rms_norm(v: np.ndarray, gain: Optional[np.ndarray] = None,
+             eps: float = 1e-6) -> np.ndarray:
+    """Row-wise RMSNorm: v / sqrt(mean(v^2) + eps) * gain ([P1] 残差流: every
+    sublayer is normalised before and after)."""
+    v = np.asarray(v, dtype=F64)
+    ms = np.mean(v * v, axis=-1, keepdims=True)
+    out = v / np.sqrt(ms + eps)
+    if gain is not None:
+        out = out * np.asarray(gain, dtype=F64)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# router ([P1] 专家混合模型; [P5] config fields)
+# ----------------------------------------------------------------------------
+def router_scores(x: np.ndarray, w_router: np.ndarray,
+                  bias: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Sigmoid scores for every expert.
+
+    logit[t,e] = sum_j x[t,j] * w_router[e,j] (+ bias[e]); s = sigmoid(logit).
+    Returns (s64 [T,E] FP64, s32 [T,E] FP32 rounding of s64).
+    """
+    x = np.asarray(x, dtype=F64)
+    w = np.asarray(w_router, dtype=F64)
+    logits = x @ w.T
+    if bias is not None:
+        logits = logits + np.asarray(bias, dtype=F64)[None, :]
+    s64 = sigmoid(logits)
+    return s64, s64.astype(F32)
+
+
+def group_scores(s32: np.ndarray, n_group: int) -> np.ndarray:
+    """Score of each group: FP32 sum of its two largest FP32 scores
+    (of its only score when a group has one expert)."""
+    T, E = s32.shape
+    gsize = E // n_group
+    sg = np.asarray(s32, dtype=F32).reshape(T, n_group, gsize)
+    srt = -np.sort(-sg, axis=-1)           # descending within each group
+    if gsize == 1:
+        return srt[..., 0].copy()
+    return (srt[..., 0] + srt[..., 1]).astype(F32)   # float32 addition
+
+
+def _rank_desc(values: np.ndarray) -> np.ndarray:
+    """Indices sorting one row by value descending, ties by lower index."""
+    idx = np.arange(values.shape[-1])
+    return np.lexsort((idx, -values.astype(F64)))
+
+
+def group_limited_topk(s32: np.ndarray, n_group: int, topk_group: int,
+                       top_k: int) -> dict:
+    """Group-limited selection ([P1] 专家混合模型).
+
+    1. split the E experts into n_group consecutive groups;
+    2. rank the groups by the sum of their two best scores, keep topk_group;
+    3. among the experts of the kept groups, take the top_k best scores.
+    Output order: descending score, ties by lower expert index.
+
+    Returns dict with
+      idx         [T, top_k] int32 selected experts in output order
+      kept        [T, topk_group] int32 kept groups in rank order
+      gscore      [T, n_group] float32 group scores
+      group_margin  [T] float64: 4th-best minus 5th-best group score (inf if
+                    every group is kept)
+      topk_margin   [T] float64: k-th selected minus best unselected
+                    candidate score (inf if no candidate is left out)
+    """
+    s32 = np.asarray(s32, dtype=F32)
+    T, E = s32.shape
+    assert E % n_group == 0
+    gsize = E // n_group
+    assert 1 <= topk_group <= n_group and 1 <= top_k <= topk_group * gsize
+    gs = group_scores(s32, n_group)
+    idx = np.empty((T, top_k), dtype=np.int32)
+    kept = np.empty((T, topk_group), dtype=np.int32)
+    gmar = np.full(T, np.inf)
+    kmar = np.full(T, np.inf)
+    for t in range(T):
+        gorder = _rank_desc(gs[t])
+        kept[t] = gorder[:topk_group]
+        if topk_group < n_group:
+            gmar[t] = float(gs[t, gorder[topk_group - 1]]) - float(gs[t, gorder[topk_group]])
+        cand = np.concatenate([np.arange(g * gsize, (g + 1) * gsize)
+                               for g in sorted(kept[t])])
+        corder = cand[_rank_desc(s32[t, cand])]
+        idx[t] = corder[:top_k]
+        if len(corder) > top_k:
+            kmar[t] = float(s32[t, corder[top_k - 1]]) - float(s32[t, corder[top_k]])
+    return dict(idx=idx, kept=kept, gscore=gs, group_margin=gmar,
+                topk_margin=kmar)
+
+
+def combine_weights(s: np.ndarray, idx: np.ndarray, scale: float) -> np.ndarray:
+    """w[t,j] = scale * s[t, idx[t,j]] / sum_i s[t, idx[t,i]]  ([P1] 专家混合模型:
+    normalised router weights, multiplied by 2.5; [P5] norm_topk_prob,
+    routed_scaling_factor)."""
+    s = np.asarray(s, dtype=F64)
+    sel = np.take_along_axis(s, np.asarray(idx, dtype=np.int64), axis=1)
+    return scale * sel / sel.sum(axis=1, keepdims=True)
+
+
+def route(x, w_router, bias, n_group, topk_group, top_k, scale) -> dict:
+    """Scores, group-limited selection and combine weights for every token."""
+    s64, s32 = router_scores(x, w_router, bias)
+    sel = group_limited_topk(s32, n_group, topk_group, top_k)
+    sel["weights"] = combine_weights(s64, sel["idx"], scale)
+    sel["s64"] = s64
+    sel["s32"] = s32
+    return sel
+
+
+def near_ties(sel: dict, margin: float = 1e-5) -> np.ndarray:
+    """Tokens whose group or top-k boundary is closer than `margin` in FP32
+    score: another correct FP32 evaluation may pick the other side there."""
+    return (sel["group_margin"] < margin) | (sel["topk_margin"] < margin)
+
+
+# ----------------------------------------------------------------------------
+# permutation (token -> expert order)
+# ----------------------------------------------------------------------------
+def permutation(idx: np.ndarray, E: int) -> dict:
+    """Token-expert pairs grouped by expert, stable in pair order p = t*k + j.
+
+    Returns counts [E], offsets [E+1], row_pair [T*k] (the pair at each row of
+    the expert-ordered layout).
+    """
+    flat = np.asarray(idx, dtype=np.int64).ravel()
+    row_pair = np.argsort(flat, kind="stable").astype(np.int64)
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    return dict(counts=counts, offsets=offsets, row_pair=row_pair)
+
+
+# ----------------------------------------------------------------------------
+# experts ([P1] 专家混合模型: each expert a SwiGLU MLP; [P1] 残差流: SwiGLU
+# product in FP32 -- the oracle keeps FP64)
+# ----------------------------------------------------------------------------
+def swiglu_expert(x_rows: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray,
+                  w_down: np.ndarray) -> np.ndarray:
+    """y = (silu(x W_g^T) * (x W_u^T)) W_d^T for rows x [n,H];
+    w_gate, w_up [I,H]; w_down [H,I]."""
+    x = np.asarray(x_rows, dtype=F64)
+    g = x @ np.asarray(w_gate, dtype=F64).T
+    u = x @ np.asarray(w_up, dtype=F64).T
+    a = silu(g) * u
+    return a @ np.asarray(w_down, dtype=F64).T
+
+
+def moe_combine(x: np.ndarray, idx: np.ndarray, weights: np.ndarray,
+                get_expert: Callable[[int], tuple]) -> np.ndarray:
+    """out[t] = sum_j weights[t,j] * f_{idx[t,j]}(x[t]), expert by expert
+    ([P1] 专家混合模型: expert outputs combined with the normalised weights)."""
+    x = np.asarray(x, dtype=F64)
+    T = x.shape[0]
+    out = np.zeros((T, x.shape[1]), dtype=F64)
+    idx = np.asarray(idx)
+    for e in np.unique(idx):
+        tok, slot = np.nonzero(idx == e)
+        wg, wu, wd = get_expert(int(e))
+        y = swiglu_expert(x[tok], wg, wu, wd)
+        out[tok] += weights[tok, slot][:, None] * y
+    return out
+
+
+# ----------------------------------------------------------------------------
+# residual stream ([P1] 残差流; [P4] residual paragraph)
+# ----------------------------------------------------------------------------
+def residual_coeffs(k: int) -> Tuple[float, float]:
+    """(sqrt((k-1)/k), 1/sqrt(k)): keep weight and add weight at step k."""
+    if k < 2:
+        raise ValueError("residual step k must be >= 2 (the embedding is step 1)")
+    return math.sqrt((k - 1) / k), 1.0 / math.sqrt(k)
+
+
+def residual_step(h_prev, sub_out, k: int, gain=None, eps: float = 1e-6,
+                  apply_norm: bool = True) -> np.ndarray:
+    """h_k = sqrt((k-1)/k) h_{k-1} + (1/sqrt(k)) * n, n = RMSNorm(sub_out)
+    (or sub_out itself when apply_norm is False)."""
+    a, b = residual_coeffs(k)
+    n = rms_norm(sub_out, gain, eps) if apply_norm else np.asarray(sub_out, F64)
+    return a * np.asarray(h_prev, dtype=F64) + b * n
+
+
+# ----------------------------------------------------------------------------
+# the whole sublayer
+# ----------------------------------------------------------------------------
+def moe_forward(x_in, w_router, bias, get_expert, *, n_group=8, topk_group=4,
+                top_k=8, scale=2.5, eps=1e-6, pre_norm=False, pre_gain=None,
+                residual_k=0, post_gain=None, routing: Optional[dict] = None) -> dict:
+    """The MoE sublayer as the pages state it.
+
+    x_in: layer input [T,H] (h_{k-1} when pre_norm or residual_k >= 2).
+    get_expert(e) -> (w_gate [I,H], w_up [I,H], w_down [H,I]).
+    routing: optional dict with 'idx' and 'weights' to use instead of the
+    oracle's own routing (to compare experts and combine on near-tie tokens).
+    Returns dict(x, sel, out, h).
+    """
+    x_in = np.asarray(x_in, dtype=F64)
+    x = bf16_round(rms_norm(x_in, pre_gain, eps)).astype(F64) if pre_norm else x_in
+    sel = route(x, w_router, bias, n_group, topk_group, top_k, scale)
+    use = routing if routing is not None else sel
+    out = moe_combine(x, use["idx"], use["weights"], get_expert)
+    h = None
+    if residual_k:
+        h = residual_step(x_in, out, residual_k, post_gain, eps, True)
+    return dict(x=x, sel=sel, out=out, h=h)

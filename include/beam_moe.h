@@ -1,0 +1,191 @@
+/*
+ * beam_moe.h -- C ABI of the Beam MoE sublayer on one B300 (sm_103a).
+ *
+ * The operation, as the release pages state it:
+ *   [P1] "Reflection 发布 Beam 501B 开源模型，支持 1M tokens 上下文",
+ *        section 专家混合模型: sigmoid router over all experts, 8 groups of
+ *        32, keep the 4 groups with the best sum of their two top scores,
+ *        top-8 experts inside them, no shared expert, each expert a SwiGLU
+ *        MLP (intermediate 2560), outputs combined with the normalised
+ *        router weights multiplied by 2.5;
+ *        section 残差流: the embedding is step 1; step k keeps the stream
+ *        with weight sqrt((k-1)/k) and adds the sublayer output with weight
+ *        1/sqrt(k); every sublayer is normalised before and after; router,
+ *        SwiGLU product and normalisation run in FP32.
+ *   [P5] "Reflection 放出 501B 的 Beam 权重：四套精度、滑动窗口和一场榜单落差",
+ *        section "config.json 里还有六处能直接抄的细节": n_group 8,
+ *        topk_group 4, norm_topk_prob true, routed_scaling_factor 2.5; and
+ *        the FP32 router weight (the quantisers skip "mlp.gate").
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers owned by the caller (inputs, outputs
+ *     and workspace) unless stated otherwise. The library never allocates
+ *     device memory in these calls.
+ *   - Tensors are dense row-major. Weight matrices use the nn.Linear layout
+ *     [out_features, in_features]. Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *     enqueued asynchronously; nothing synchronises the host.
+ *   - Argument errors are reported synchronously through the return value
+ *     (nothing is enqueued then). Errors inside kernels (a bounded wait that
+ *     timed out) set a per-device flag read back by beam_status().
+ *   - beam_last_error_string() describes the last failure of the calling
+ *     host thread.
+ */
+#ifndef BEAM_MOE_H_
+#define BEAM_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BEAM_OK = 0,
+  BEAM_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, k < 2 */
+  BEAM_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels implement */
+  BEAM_ERR_WORKSPACE = 3,    /* workspace smaller than beam_moe_workspace_size() */
+  BEAM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+  BEAM_ERR_TIMEOUT = 5,      /* a device-side bounded wait gave up */
+  BEAM_ERR_DEVICE_FLAG = 6   /* another device-side error flag was set */
+} beam_status_t;
+
+/* beam_moe_params.flags */
+#define BEAM_FLAG_PRE_NORM 1      /* input is h_{k-1}; RMSNorm it (FP32) into BF16 x first */
+#define BEAM_FLAG_FP32_OUT 2      /* `out` is FP32 (only without the residual step) */
+#define BEAM_FLAG_RETURN_SCORES 4 /* beam_moe_route also writes the sigmoid scores */
+
+/* Shape and hyper-parameters of one MoE sublayer call.
+ *   T           tokens in the batch (0 is allowed: nothing is enqueued)
+ *   H           hidden size (5120 for Beam); multiple of 128
+ *   E           experts (256 for Beam); multiple of 32, at most 256
+ *   I           expert SwiGLU intermediate size (2560); multiple of 128
+ *   n_group     expert groups (8); E / n_group must be 32, or n_group must equal
+ *               topk_group (all groups kept: plain top-k)
+ *   topk_group  groups kept per token (4)
+ *   top_k       experts per token (8); 1..32 and <= topk_group * E / n_group
+ *   routed_scale  factor on the normalised weights (2.5)
+ *   rms_eps     RMSNorm epsilon (1e-6)
+ *   residual_k  0: no residual step (out = combined MoE output); >= 2: the
+ *               step index k of the scaled residual update; out = h_k
+ *   flags       BEAM_FLAG_* bits
+ */
+typedef struct {
+  int T, H, E, I, n_group, topk_group, top_k;
+  float routed_scale;
+  float rms_eps;
+  int residual_k;
+  int flags;
+} beam_moe_params;
+
+/* Bytes of device workspace that beam_moe_route / beam_moe_forward need for
+ * these parameters (0 when the parameters are invalid; see
+ * beam_last_error_string()). The same workspace may be reused by successive
+ * calls on one stream; calls that overlap in time need separate workspaces. */
+size_t beam_moe_workspace_size(const beam_moe_params* p);
+
+/* Router only ([P1] 专家混合模型; [P5] config fields).
+ *   x          [T,H] bf16: layer input (h_{k-1} when BEAM_FLAG_PRE_NORM)
+ *   w_router   [E,H] fp32 router weight
+ *   logit_bias [E] fp32 added to the logits before the sigmoid, or NULL
+ *   pre_gain   [H] fp32 gain of the pre-norm, or NULL (= 1); used only
+ *              with BEAM_FLAG_PRE_NORM
+ *   topk_idx   [T,top_k] int32 out: selected experts, by descending score,
+ *              ties to the lower expert index
+ *   topk_w     [T,top_k] fp32 out: routed_scale * s / (sum of the selected s)
+ *   scores     [T,E] fp32 out (sigmoid scores) when BEAM_FLAG_RETURN_SCORES,
+ *              else ignored (may be NULL)
+ * Scores are FP32: logits accumulate x (bf16 -> fp32) times w_router in FP32.
+ * Group score = FP32 sum of the group's two largest scores; groups rank by
+ * it (ties to the lower group index). */
+beam_status_t beam_moe_route(const beam_moe_params* p, const void* x,
+                             const float* w_router, const float* logit_bias,
+                             const float* pre_gain, int32_t* topk_idx, float* topk_w,
+                             float* scores, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* The whole MoE sublayer ([P1] 专家混合模型 and 残差流):
+ *   x = BEAM_FLAG_PRE_NORM ? bf16(RMSNorm(x_in) * pre_gain) : x_in
+ *   route x (as beam_moe_route)
+ *   y_e = (silu(x W_gate[e]^T) * (x W_up[e]^T)) W_down[e]^T for each selected
+ *         expert, BF16 operands, FP32 accumulation, SwiGLU product in FP32,
+ *         the intermediate rounded to BF16 before the down projection
+ *   o   = sum_j topk_w[t,j] * y_{topk_idx[t,j]}   (FP32)
+ *   out = residual_k >= 2 ? bf16(sqrt((k-1)/k) x_in + RMSNorm(o) * post_gain / sqrt(k))
+ *                         : o (bf16, or fp32 with BEAM_FLAG_FP32_OUT)
+ * Arguments:
+ *   x_in       [T,H] bf16
+ *   w_router   [E,H] fp32;  logit_bias [E] fp32 or NULL
+ *   w_gate     [E,I,H] bf16; w_up [E,I,H] bf16; w_down [E,H,I] bf16
+ *   pre_gain   [H] fp32 or NULL (= 1);  post_gain [H] fp32 or NULL (= 1)
+ *   out        [T,H] bf16 (fp32 with BEAM_FLAG_FP32_OUT); must not alias x_in
+ *   topk_idx, topk_w  optional outputs as in beam_moe_route (NULL: kept in the
+ *              workspace)
+ * Token-to-expert order inside the workspace is stable (by token, then slot).
+ * The FP32 combine uses atomic adds, so the last bits of `out` may vary from
+ * run to run; routing is deterministic. */
+beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in,
+                               const float* w_router, const float* logit_bias,
+                               const void* w_gate, const void* w_up, const void* w_down,
+                               const float* pre_gain, const float* post_gain, void* out,
+                               int32_t* topk_idx, float* topk_w, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* One scaled residual update ([P1] 残差流):
+ *   h_out = bf16( sqrt((k-1)/k) * h_prev + (1/sqrt(k)) * n ),
+ *   n = apply_norm ? RMSNorm(sub_out) * post_gain : sub_out   (FP32 math)
+ *   h_prev  [T,H] bf16;  sub_out [T,H] bf16, or fp32 when sub_out_is_fp32
+ *   post_gain [H] fp32 or NULL (= 1);  k >= 2 (the embedding is step 1)
+ *   h_out   [T,H] bf16; may alias h_prev (each element is read before it is
+ *           written by the same thread) but not sub_out.
+ * H must be a multiple of 8. */
+beam_status_t beam_residual_step(const void* h_prev, const void* sub_out, int T, int H,
+                                 int k, const float* post_gain, float eps, int apply_norm,
+                                 int sub_out_is_fp32, void* h_out, void* stream);
+
+/* Synchronises `stream`, then reads and clears the calling device's error
+ * flag: BEAM_OK, BEAM_ERR_TIMEOUT or BEAM_ERR_DEVICE_FLAG (or BEAM_ERR_CUDA
+ * if the synchronisation itself failed). */
+beam_status_t beam_status(void* stream);
+
+/* Human-readable description of the calling thread's last failure. The
+ * string stays valid until the next call on the same thread. */
+const char* beam_last_error_string(void);
+
+/* ---- diagnostics (tests and tooling) ---------------------------------- */
+
+/* Byte offsets of the internal buffers inside the forward workspace, in this
+ * order: 0 normalised x [T,H] bf16, 1 router partial logits, 2 topk_idx,
+ * 3 topk_w, 4 expert counts [E] int32, 5 expert offsets [E+1] int32,
+ * 6 row_token [T*top_k] int32, 7 row_weight [T*top_k] fp32, 8 permuted x
+ * [T*top_k,H] bf16, 9 SwiGLU activations [T*top_k,I] bf16, 10 FP32
+ * accumulator [T,H], 11 unit counts [4] int32, 12 per-block expert
+ * histograms, 13 per-block expert offsets, 14 gate/up work list, 15 down
+ * work list. Writes min(n, 16) entries and returns how many it wrote (0 on
+ * invalid parameters). */
+int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n);
+
+/* Launches one block whose single thread waits on a shared-memory barrier
+ * that nothing ever completes, with the same bounded wait the GEMM kernels
+ * use, giving up after `timeout_ns`. The device error flag then reads
+ * BEAM_ERR_TIMEOUT through beam_status(). Used to test the failure path
+ * without hanging or faulting the GPU. */
+beam_status_t beam_debug_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* Per-kernel timing. While enabled (on != 0), every kernel launch of this
+ * library is bracketed by two CUDA events recorded on its stream. */
+void beam_profile_enable(int on);
+
+/* Synchronises the recorded events and returns, per kernel name, the total
+ * elapsed milliseconds and the launch count since the last read; then
+ * clears the record. `names` receives the names separated by newlines (at
+ * most names_len bytes, NUL-terminated); total_ms and launches receive up to
+ * max_entries values in the same order. Returns the number of entries. */
+int beam_profile_read(char* names, size_t names_len, double* total_ms, int* launches,
+                      int max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BEAM_MOE_H_ */

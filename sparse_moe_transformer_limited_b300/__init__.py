@@ -1,0 +1,16 @@
+"""Beam MoE sublayer on one B300 (sm_103a): Python binding of libbeam_moe.so.
+
+The layer (router, group-limited top-8, normalised x2.5 weights, token
+permutation, SwiGLU experts, weighted combine, post-RMSNorm and the scaled
+residual update) runs in the library's CUDA kernels; this package only
+marshals torch tensors into the C ABI declared in include/beam_moe.h.
+"""
+from ._native import (BeamError, Params, make_params, workspace_size, workspace_layout,
+                      alloc_workspace, route, forward, residual_step, status, last_error,
+                      debug_wait_timeout, lib, LIB_PATH, EXPORTED, FLAG_PRE_NORM,
+                      FLAG_FP32_OUT, FLAG_RETURN_SCORES, profile_enable, profile_read)
+
+__all__ = ["BeamError", "Params", "make_params", "workspace_size", "workspace_layout",
+           "alloc_workspace", "route", "forward", "residual_step", "status", "last_error",
+           "debug_wait_timeout", "lib", "LIB_PATH", "EXPORTED", "FLAG_PRE_NORM",
+           "FLAG_FP32_OUT", "FLAG_RETURN_SCORES", "profile_enable", "profile_read"]

@@ -1,0 +1,211 @@
+"""ctypes binding of libbeam_moe.so (the C ABI in include/beam_moe.h).
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream; every step of the layer runs in the library's kernels.
+There is no fallback: if the library is missing or cannot load, importing
+the functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
+
+BEAM_OK = 0
+BEAM_ERR_INVALID_ARG = 1
+BEAM_ERR_UNSUPPORTED = 2
+BEAM_ERR_WORKSPACE = 3
+BEAM_ERR_CUDA = 4
+BEAM_ERR_TIMEOUT = 5
+BEAM_ERR_DEVICE_FLAG = 6
+
+FLAG_PRE_NORM = 1
+FLAG_FP32_OUT = 2
+FLAG_RETURN_SCORES = 4
+
+# names of the workspace buffers, in beam_moe_workspace_layout() order
+LAYOUT_NAMES = ("xn", "part", "topk_idx", "topk_w", "counts", "offsets", "row_token",
+                "row_weight", "xperm", "act", "acc", "n_units", "blk_hist", "blk_off",
+                "units_gu", "units_dn")
+
+# every symbol include/beam_moe.h declares
+EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_forward",
+            "beam_residual_step", "beam_status", "beam_last_error_string",
+            "beam_moe_workspace_layout", "beam_debug_wait_timeout", "beam_profile_enable",
+            "beam_profile_read")
+
+
+class BeamError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"beam status {code}: {msg}")
+        self.code = code
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int),
+                ("I", ctypes.c_int), ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("routed_scale", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("residual_k", ctypes.c_int),
+                ("flags", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library once; raise if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run "
+                              "`python -m sparse_moe_transformer_limited_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+        P = ctypes.POINTER(Params)
+        L.beam_moe_workspace_size.argtypes = [P]
+        L.beam_moe_workspace_size.restype = sz
+        L.beam_moe_workspace_layout.argtypes = [P, ctypes.POINTER(sz), i32]
+        L.beam_moe_workspace_layout.restype = i32
+        L.beam_moe_route.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.beam_moe_route.restype = i32
+        L.beam_moe_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.beam_moe_forward.restype = i32
+        L.beam_residual_step.argtypes = [vp, vp, i32, i32, i32, vp, f32, i32, i32, vp, vp]
+        L.beam_residual_step.restype = i32
+        L.beam_status.argtypes = [vp]
+        L.beam_status.restype = i32
+        L.beam_last_error_string.argtypes = []
+        L.beam_last_error_string.restype = ctypes.c_char_p
+        L.beam_debug_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.beam_debug_wait_timeout.restype = i32
+        L.beam_profile_enable.argtypes = [i32]
+        L.beam_profile_enable.restype = None
+        L.beam_profile_read.argtypes = [ctypes.c_char_p, sz, ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(i32), i32]
+        L.beam_profile_read.restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(code: int):
+    if code != BEAM_OK:
+        raise BeamError(code, lib().beam_last_error_string().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_params(T, H, E, I, n_group=8, topk_group=4, top_k=8, routed_scale=2.5,
+                rms_eps=1e-6, residual_k=0, flags=0) -> Params:
+    return Params(T, H, E, I, n_group, topk_group, top_k, routed_scale, rms_eps, residual_k,
+                  flags)
+
+
+def workspace_size(p: Params) -> int:
+    n = lib().beam_moe_workspace_size(ctypes.byref(p))
+    if n == 0:
+        raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
+    return int(n)
+
+
+def workspace_layout(p: Params) -> dict:
+    arr = (ctypes.c_size_t * len(LAYOUT_NAMES))()
+    n = lib().beam_moe_workspace_layout(ctypes.byref(p), arr, len(LAYOUT_NAMES))
+    if n == 0:
+        raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
+    return {LAYOUT_NAMES[i]: int(arr[i]) for i in range(n)}
+
+
+def alloc_workspace(p: Params, device="cuda") -> torch.Tensor:
+    return torch.empty(workspace_size(p), dtype=torch.uint8, device=device)
+
+
+def route(p: Params, x, w_router, bias=None, pre_gain=None, topk_idx=None, topk_w=None,
+          scores=None, workspace=None, stream=None):
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((p.T, p.top_k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((p.T, p.top_k), dtype=torch.float32, device=dev)
+    if scores is None and (p.flags & FLAG_RETURN_SCORES):
+        scores = torch.empty((p.T, p.E), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(p, dev)
+    _check(lib().beam_moe_route(ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(bias),
+                                _ptr(pre_gain), _ptr(topk_idx), _ptr(topk_w), _ptr(scores),
+                                _ptr(workspace), workspace.numel(), _stream(stream)))
+    return topk_idx, topk_w, scores
+
+
+def forward(p: Params, x, w_router, w_gate, w_up, w_down, bias=None, pre_gain=None,
+            post_gain=None, out=None, topk_idx=None, topk_w=None, workspace=None, stream=None):
+    dev = x.device
+    if out is None:
+        dt = torch.float32 if (p.flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((p.T, p.H), dtype=dt, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(p, dev)
+    _check(lib().beam_moe_forward(ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(bias),
+                                  _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(pre_gain),
+                                  _ptr(post_gain), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
+                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def residual_step(h_prev, sub_out, k, post_gain=None, eps=1e-6, apply_norm=True, out=None,
+                  stream=None):
+    T, H = h_prev.shape
+    if out is None:
+        out = torch.empty_like(h_prev)
+    _check(lib().beam_residual_step(_ptr(h_prev), _ptr(sub_out), T, H, k, _ptr(post_gain),
+                                    eps, int(bool(apply_norm)),
+                                    int(sub_out.dtype == torch.float32), _ptr(out),
+                                    _stream(stream)))
+    return out
+
+
+def status(stream=None) -> int:
+    """Synchronise the stream and read (and clear) the device error flag."""
+    code = lib().beam_status(_stream(stream))
+    return int(code)
+
+
+def last_error() -> str:
+    return lib().beam_last_error_string().decode()
+
+
+def debug_wait_timeout(timeout_ns: int, stream=None):
+    _check(lib().beam_debug_wait_timeout(ctypes.c_uint64(timeout_ns), _stream(stream)))
+
+
+def profile_enable(on: bool = True):
+    """Bracket every library kernel launch with CUDA events (on its stream)."""
+    lib().beam_profile_enable(1 if on else 0)
+
+
+def profile_read() -> dict:
+    """{kernel name: (total ms, launches)} since the last read; clears it."""
+    n_max = 64
+    names = ctypes.create_string_buffer(4096)
+    ms = (ctypes.c_double * n_max)()
+    cnt = (ctypes.c_int * n_max)()
+    n = lib().beam_profile_read(names, 4096, ms, cnt, n_max)
+    keys = names.value.decode().split("\n")[:n]
+    return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(keys)}

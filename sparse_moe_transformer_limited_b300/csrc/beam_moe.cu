@@ -1,0 +1,572 @@
+// Host side of the C ABI declared in include/beam_moe.h: argument checks,
+// workspace layout, TMA descriptors and kernel launches. Nothing here
+// allocates device memory; all buffers are the caller's.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "beam_moe.h"
+#include "kernels_gemm.cuh"
+#include "kernels_permute.cuh"
+#include "kernels_router.cuh"
+#include "kernels_rows.cuh"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+beam_status_t fail(beam_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+#define BEAM_CUDA_TRY(expr)                                                              \
+  do {                                                                                   \
+    cudaError_t e_ = (expr);                                                             \
+    if (e_ != cudaSuccess)                                                               \
+      return fail(BEAM_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));        \
+  } while (0)
+
+#define BEAM_LAUNCH_CHECK(what)                                                          \
+  do {                                                                                   \
+    cudaError_t e_ = cudaGetLastError();                                                 \
+    if (e_ != cudaSuccess)                                                               \
+      return fail(BEAM_ERR_CUDA, "launch of %s failed: %s", what, cudaGetErrorString(e_)); \
+  } while (0)
+
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+
+// ------------------------------------------------------------ profiling
+// When enabled, every launch is bracketed by two CUDA events recorded on the
+// launching stream; beam_profile_read() aggregates their elapsed times.
+struct ProfRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+struct ProfScope {
+  bool on = false;
+  ProfRec rec{};
+  cudaStream_t st;
+  ProfScope(const char* name, cudaStream_t s) : st(s) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (!g_prof_on) return;
+    rec.name = name;
+    rec.start = prof_event();
+    rec.stop = prof_event();
+    if (rec.start && rec.stop && cudaEventRecord(rec.start, st) == cudaSuccess) on = true;
+  }
+  ~ProfScope() {
+    if (!on) return;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (cudaEventRecord(rec.stop, st) == cudaSuccess) g_prof_recs.push_back(rec);
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ tiles
+// Token-tile width of the expert GEMMs, chosen from the mean tokens per
+// expert: narrow tiles when each expert sees a handful of tokens (decode),
+// wide tiles for prefill.
+int choose_nt(const beam_moe_params& p) {
+  const long long pairs = static_cast<long long>(p.T) * p.top_k;
+  return (pairs <= 24LL * p.E) ? 32 : 128;
+}
+
+// K-slices of the router logits GEMM: enough blocks to cover the SMs when T
+// is small. Must divide H / 32 and leave at least 64 columns per slice.
+int choose_router_ks(const beam_moe_params& p, int num_sms) {
+  const int tiles = ((p.T + beam::RL_BT - 1) / beam::RL_BT) * ((p.E + beam::RL_BE - 1) / beam::RL_BE);
+  const int want = (2 * num_sms + tiles - 1) / tiles;
+  const int nk = p.H / 32;
+  int best = 1;
+  for (int ks = 1; ks <= nk; ++ks)
+    if (nk % ks == 0 && ks <= want && (p.H / ks) >= 64) best = ks;
+  return best;
+}
+
+struct Layout {
+  size_t off[16];
+  size_t total;
+  int KS, NB, NT;
+  long long units_gu_max, units_dn_max;
+};
+
+enum {
+  L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_ACC,
+  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN
+};
+
+int sm_count() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
+  } else {
+    cudaGetLastError();
+  }
+  return n;
+}
+
+beam_status_t check_params(const beam_moe_params* p) {
+  if (p == nullptr) return fail(BEAM_ERR_INVALID_ARG, "params is NULL");
+  if (p->T < 0 || p->H <= 0 || p->E <= 0 || p->I <= 0)
+    return fail(BEAM_ERR_INVALID_ARG, "T=%d H=%d E=%d I=%d: sizes must be positive", p->T, p->H,
+                p->E, p->I);
+  if (p->T > (1 << 22)) return fail(BEAM_ERR_UNSUPPORTED, "T=%d exceeds 4194304", p->T);
+  if (p->H % 128 || p->I % 128)
+    return fail(BEAM_ERR_UNSUPPORTED, "H=%d and I=%d must be multiples of 128", p->H, p->I);
+  if (p->H > 65536 || p->I > 65536)
+    return fail(BEAM_ERR_UNSUPPORTED, "H and I must be at most 65536");
+  if (p->E % 32 || p->E > 256)
+    return fail(BEAM_ERR_UNSUPPORTED, "E=%d must be a multiple of 32 and at most 256", p->E);
+  if (p->n_group <= 0 || p->E % p->n_group)
+    return fail(BEAM_ERR_INVALID_ARG, "n_group=%d must divide E=%d", p->n_group, p->E);
+  if (p->topk_group <= 0 || p->topk_group > p->n_group)
+    return fail(BEAM_ERR_INVALID_ARG, "topk_group=%d must be in [1, n_group=%d]", p->topk_group,
+                p->n_group);
+  if (p->topk_group < p->n_group && p->E / p->n_group != 32)
+    return fail(BEAM_ERR_UNSUPPORTED, "group size E/n_group=%d: only groups of 32 are implemented",
+                p->E / p->n_group);
+  const int cand = p->topk_group * (p->E / p->n_group);
+  if (p->top_k <= 0 || p->top_k > 32 || p->top_k > cand)
+    return fail(BEAM_ERR_INVALID_ARG, "top_k=%d must be in [1, min(32, %d)]", p->top_k, cand);
+  if (!(p->routed_scale > 0.f) || !std::isfinite(p->routed_scale))
+    return fail(BEAM_ERR_INVALID_ARG, "routed_scale must be positive and finite");
+  if (!(p->rms_eps >= 0.f) || !std::isfinite(p->rms_eps))
+    return fail(BEAM_ERR_INVALID_ARG, "rms_eps must be >= 0 and finite");
+  if (p->residual_k == 1 || p->residual_k < 0)
+    return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", p->residual_k);
+  if (p->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_RETURN_SCORES))
+    return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  if ((p->flags & BEAM_FLAG_FP32_OUT) && p->residual_k >= 2)
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP32_OUT applies only without the residual step");
+  const long long pairs = static_cast<long long>(p->T) * p->top_k;
+  if (pairs > (1LL << 26)) return fail(BEAM_ERR_UNSUPPORTED, "T*top_k too large");
+  return BEAM_OK;
+}
+
+Layout make_layout(const beam_moe_params& p) {
+  Layout L{};
+  const int nsm = sm_count();
+  L.KS = choose_router_ks(p, nsm);
+  L.NB = (p.T + beam::PERM_TPB - 1) / beam::PERM_TPB;
+  L.NT = choose_nt(p);
+  const long long R = static_cast<long long>(p.T) * p.top_k;
+  const long long tiles = (R + L.NT - 1) / L.NT + p.E;
+  L.units_gu_max = tiles * (p.I / 128);
+  L.units_dn_max = tiles * (p.H / 128);
+  size_t sz[16];
+  sz[L_XN] = (p.flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p.T) * p.H * 2 : 0;
+  sz[L_PART] = static_cast<size_t>(L.KS) * p.T * p.E * 4;
+  sz[L_IDX] = static_cast<size_t>(R) * 4;
+  sz[L_W] = static_cast<size_t>(R) * 4;
+  sz[L_COUNTS] = static_cast<size_t>(p.E) * 4;
+  sz[L_OFFS] = static_cast<size_t>(p.E + 1) * 4;
+  sz[L_ROWTOK] = static_cast<size_t>(R) * 4;
+  sz[L_ROWW] = static_cast<size_t>(R) * 4;
+  sz[L_XPERM] = static_cast<size_t>(R) * p.H * 2;
+  sz[L_ACT] = static_cast<size_t>(R) * p.I * 2;
+  sz[L_ACC] = static_cast<size_t>(p.T) * p.H * 4;
+  sz[L_NUNITS] = 16;
+  sz[L_BLKHIST] = static_cast<size_t>(L.NB) * p.E * 4;
+  sz[L_BLKOFF] = static_cast<size_t>(L.NB) * p.E * 4;
+  sz[L_UGU] = static_cast<size_t>(L.units_gu_max) * 16;
+  sz[L_UDN] = static_cast<size_t>(L.units_dn_max) * 16;
+  size_t cur = 0;
+  for (int i = 0; i < 16; ++i) {
+    L.off[i] = cur;
+    cur = align_up(cur + sz[i], 1024);
+  }
+  L.total = cur;
+  return L;
+}
+
+// ------------------------------------------------------------- TMA maps
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                      const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                      const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                      CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled_t encode_fn() {
+  static PFN_encodeTiled_t fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled_t>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] -> TMA map with box {64 cols, box_rows}
+// and the 128-byte swizzle (one box row = 128 bytes).
+beam_status_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows) {
+  PFN_encodeTiled_t fn = encode_fn();
+  if (fn == nullptr) return fail(BEAM_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BEAM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llux%llu matrix",
+                static_cast<int>(r), static_cast<unsigned long long>(rows),
+                static_cast<unsigned long long>(cols));
+  return BEAM_OK;
+}
+
+// --------------------------------------------------------- GEMM launches
+template <int MODE, int NT, int STAGES>
+beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                          const beam::GemmArgs& args, cudaStream_t st) {
+  using C = beam::GemmCfg<MODE, NT, STAGES>;
+  auto kern = beam::expert_gemm_kernel<MODE, NT, STAGES>;
+  static bool attr_set = false;  // per template instance
+  if (!attr_set) {
+    BEAM_CUDA_TRY(
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
+    attr_set = true;
+  }
+  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down_combine", st);
+  kern<<<sm_count(), 192, C::SMEM_BYTES, st>>>(a0, a1, b, args);
+  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>" : "expert_gemm_kernel<down>");
+  return BEAM_OK;
+}
+
+beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const void* x_in,
+                            const float* w_router, const float* bias, const float* pre_gain,
+                            int32_t* idx, float* w, float* scores, float* acc_zero,
+                            uint8_t* ws, cudaStream_t st) {
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
+  if (p.flags & BEAM_FLAG_PRE_NORM) {
+    __nv_bfloat16* xn = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_XN]);
+    ProfScope ps("prenorm", st);
+    beam::prenorm_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(x, pre_gain, xn, p.T, p.H, p.rms_eps);
+    BEAM_LAUNCH_CHECK("prenorm_kernel");
+    x = xn;
+  }
+  float* part = reinterpret_cast<float*>(ws + L.off[L_PART]);
+  dim3 g1((p.T + beam::RL_BT - 1) / beam::RL_BT, (p.E + beam::RL_BE - 1) / beam::RL_BE, L.KS);
+  {
+    ProfScope ps("router_logits", st);
+    beam::router_logits_kernel<<<g1, 256, 0, st>>>(x, w_router, part, p.T, p.H, p.E, p.H / L.KS);
+  }
+  BEAM_LAUNCH_CHECK("router_logits_kernel");
+  const int nb = (p.T + 7) / 8;
+  ProfScope ps("router_select", st);
+#define BEAM_SEL(NI)                                                                          \
+  case NI:                                                                                    \
+    beam::router_select_kernel<NI><<<nb, 256, 0, st>>>(part, L.KS, bias, p.T, p.E, p.n_group, \
+                                                      p.topk_group, p.top_k, p.routed_scale, \
+                                                      idx, w, scores, acc_zero, p.H);         \
+    break;
+  switch (p.E / 32) {
+    BEAM_SEL(1) BEAM_SEL(2) BEAM_SEL(3) BEAM_SEL(4) BEAM_SEL(5) BEAM_SEL(6) BEAM_SEL(7)
+    BEAM_SEL(8)
+    default:
+      return fail(BEAM_ERR_UNSUPPORTED, "E=%d", p.E);
+  }
+#undef BEAM_SEL
+  BEAM_LAUNCH_CHECK("router_select_kernel");
+  return BEAM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* beam_last_error_string(void) { return t_last_error.c_str(); }
+
+size_t beam_moe_workspace_size(const beam_moe_params* p) {
+  if (check_params(p) != BEAM_OK) return 0;
+  return make_layout(*p).total;
+}
+
+int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n) {
+  if (check_params(p) != BEAM_OK || offsets == nullptr || n <= 0) return 0;
+  const Layout L = make_layout(*p);
+  const int m = n < 16 ? n : 16;
+  for (int i = 0; i < m; ++i) offsets[i] = L.off[i];
+  return m;
+}
+
+beam_status_t beam_moe_route(const beam_moe_params* p, const void* x, const float* w_router,
+                             const float* logit_bias, const float* pre_gain, int32_t* topk_idx,
+                             float* topk_w, float* scores, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_params(p);
+  if (s != BEAM_OK) return s;
+  if (p->T == 0) return BEAM_OK;
+  if (!x || !w_router || !topk_idx || !topk_w || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if ((p->flags & BEAM_FLAG_RETURN_SCORES) && !scores)
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_RETURN_SCORES needs a scores buffer");
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace) ||
+      (pre_gain && !aligned16(pre_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "x, w_router, pre_gain and workspace must be 16-byte aligned");
+  const Layout L = make_layout(*p);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+  return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
+                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr, nullptr,
+                       static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const float* w_router,
+                               const float* logit_bias, const void* w_gate, const void* w_up,
+                               const void* w_down, const float* pre_gain, const float* post_gain,
+                               void* out, int32_t* topk_idx, float* topk_w, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_params(p);
+  if (s != BEAM_OK) return s;
+  if (p->T == 0) return BEAM_OK;
+  if (!x_in || !w_router || !w_gate || !w_up || !w_down || !out || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  const void* ptrs[] = {x_in, w_router, w_gate, w_up, w_down, out, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
+  if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
+  if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
+  const Layout L = make_layout(*p);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int T = p->T, H = p->H, E = p->E, I = p->I, K = p->top_k;
+  const long long R = static_cast<long long>(T) * K;
+  int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.off[L_IDX]);
+  float* wts = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.off[L_W]);
+  const bool direct_fp32 = (p->flags & BEAM_FLAG_FP32_OUT) && p->residual_k == 0;
+  float* acc = direct_fp32 ? static_cast<float*>(out) : reinterpret_cast<float*>(ws + L.off[L_ACC]);
+
+  // 1. pre-norm (optional) + router, which also zeroes the FP32 accumulator
+  s = launch_router(*p, L, x_in, w_router, logit_bias, pre_gain, idx, wts, nullptr, acc, ws, st);
+  if (s != BEAM_OK) return s;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
+  if (p->flags & BEAM_FLAG_PRE_NORM) x = reinterpret_cast<const __nv_bfloat16*>(ws + L.off[L_XN]);
+
+  // 2. permutation and work lists
+  int* blk_hist = reinterpret_cast<int*>(ws + L.off[L_BLKHIST]);
+  int* blk_off = reinterpret_cast<int*>(ws + L.off[L_BLKOFF]);
+  int* counts = reinterpret_cast<int*>(ws + L.off[L_COUNTS]);
+  int* offs = reinterpret_cast<int*>(ws + L.off[L_OFFS]);
+  int* row_tok = reinterpret_cast<int*>(ws + L.off[L_ROWTOK]);
+  float* row_w = reinterpret_cast<float*>(ws + L.off[L_ROWW]);
+  __nv_bfloat16* xperm = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_XPERM]);
+  __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_ACT]);
+  int4* ugu = reinterpret_cast<int4*>(ws + L.off[L_UGU]);
+  int4* udn = reinterpret_cast<int4*>(ws + L.off[L_UDN]);
+  int* nunits = reinterpret_cast<int*>(ws + L.off[L_NUNITS]);
+
+  {
+    ProfScope ps("expert_hist", st);
+    beam::expert_block_hist_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(idx, T, K, E, blk_hist);
+  }
+  BEAM_LAUNCH_CHECK("expert_block_hist_kernel");
+  {
+    ProfScope ps("expert_scan_units", st);
+    beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs,
+                                                      ugu, udn, nunits, L.NT, I / 128, H / 128);
+  }
+  BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
+  const size_t scatter_smem = static_cast<size_t>(2) * beam::PERM_TPB * K * sizeof(int);
+  {
+    ProfScope ps("expert_scatter", st);
+    beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, scatter_smem, st>>>(
+        idx, wts, T, K, E, blk_off, x, H, row_tok, row_w, xperm);
+  }
+  BEAM_LAUNCH_CHECK("expert_scatter_kernel");
+
+  // 3. gate/up GEMM + SwiGLU, 4. down GEMM + weighted combine
+  CUtensorMap m_g, m_u, m_d, m_x, m_a;
+  if ((s = make_map(&m_g, w_gate, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
+  if ((s = make_map(&m_u, w_up, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
+  if ((s = make_map(&m_d, w_down, static_cast<uint64_t>(E) * H, I, 128)) != BEAM_OK) return s;
+  if ((s = make_map(&m_x, xperm, R, H, 16)) != BEAM_OK) return s;
+  if ((s = make_map(&m_a, act, R, I, 16)) != BEAM_OK) return s;
+
+  beam::GemmArgs ga{};
+  ga.units = ugu;
+  ga.n_units = nunits + 0;
+  ga.k_blocks = H / 64;
+  ga.a_rows_per_expert = I;
+  ga.act_out = act;
+  ga.act_ld = I;
+  ga.timeout_ns = kWaitTimeoutNs;
+  beam::GemmArgs gd{};
+  gd.units = udn;
+  gd.n_units = nunits + 1;
+  gd.k_blocks = I / 64;
+  gd.a_rows_per_expert = H;
+  gd.row_token = row_tok;
+  gd.row_weight = row_w;
+  gd.acc = acc;
+  gd.acc_ld = H;
+  gd.timeout_ns = kWaitTimeoutNs;
+  if (L.NT == 32) {
+    if ((s = launch_gemm<0, 32, 6>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+    if ((s = launch_gemm<1, 32, 10>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+  } else {
+    if ((s = launch_gemm<0, 128, 4>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+    if ((s = launch_gemm<1, 128, 6>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+  }
+
+  // 5. post-norm + scaled residual, or the BF16 output
+  if (!direct_fp32) {
+    const int resid = p->residual_k >= 2;
+    const float k = static_cast<float>(resid ? p->residual_k : 2);
+    const float a = resid ? std::sqrt((k - 1.f) / k) : 0.f;
+    const float b = resid ? 1.f / std::sqrt(k) : 1.f;
+    ProfScope ps("finalize_rows", st);
+    beam::finalize_rows_kernel<float><<<(T + 7) / 8, 256, 0, st>>>(
+        acc, static_cast<const __nv_bfloat16*>(x_in), post_gain,
+        static_cast<__nv_bfloat16*>(out), T, H, p->rms_eps, a, b, resid, 1);
+    BEAM_LAUNCH_CHECK("finalize_rows_kernel");
+  }
+  (void)counts;
+  (void)offs;
+  return BEAM_OK;
+}
+
+beam_status_t beam_residual_step(const void* h_prev, const void* sub_out, int T, int H, int k,
+                                 const float* post_gain, float eps, int apply_norm,
+                                 int sub_out_is_fp32, void* h_out, void* stream) {
+  if (T < 0 || H <= 0 || H % 8) return fail(BEAM_ERR_INVALID_ARG, "T=%d H=%d (H %% 8 == 0)", T, H);
+  if (k < 2) return fail(BEAM_ERR_INVALID_ARG, "k=%d: the residual step needs k >= 2", k);
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(BEAM_ERR_INVALID_ARG, "eps must be >= 0");
+  if (T == 0) return BEAM_OK;
+  if (!h_prev || !sub_out || !h_out) return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(h_prev) || !aligned16(sub_out) || !aligned16(h_out) ||
+      (post_gain && !aligned16(post_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (h_out == sub_out) return fail(BEAM_ERR_INVALID_ARG, "h_out must not alias sub_out");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const double a = std::sqrt((static_cast<double>(k) - 1.0) / k), b = 1.0 / std::sqrt(static_cast<double>(k));
+  ProfScope ps("residual_step", st);
+  if (sub_out_is_fp32)
+    beam::finalize_rows_kernel<float><<<(T + 7) / 8, 256, 0, st>>>(
+        static_cast<const float*>(sub_out), static_cast<const __nv_bfloat16*>(h_prev), post_gain,
+        static_cast<__nv_bfloat16*>(h_out), T, H, eps, static_cast<float>(a),
+        static_cast<float>(b), 1, apply_norm ? 1 : 0);
+  else
+    beam::finalize_rows_kernel<__nv_bfloat16><<<(T + 7) / 8, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(sub_out), static_cast<const __nv_bfloat16*>(h_prev),
+        post_gain, static_cast<__nv_bfloat16*>(h_out), T, H, eps, static_cast<float>(a),
+        static_cast<float>(b), 1, apply_norm ? 1 : 0);
+  BEAM_LAUNCH_CHECK("finalize_rows_kernel");
+  return BEAM_OK;
+}
+
+beam_status_t beam_status(void* stream) {
+  BEAM_CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int v = 0;
+  BEAM_CUDA_TRY(cudaMemcpyFromSymbol(&v, beam::g_beam_err, sizeof(int)));
+  if (v == 0) return BEAM_OK;
+  const int zero = 0;
+  BEAM_CUDA_TRY(cudaMemcpyToSymbol(beam::g_beam_err, &zero, sizeof(int)));
+  if (v & beam::DEV_ERR_TIMEOUT) return fail(BEAM_ERR_TIMEOUT, "a device-side wait timed out (flag 0x%x)", v);
+  return fail(BEAM_ERR_DEVICE_FLAG, "device error flag 0x%x", v);
+}
+
+void beam_profile_enable(int on) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+int beam_profile_read(char* names, size_t names_len, double* total_ms, int* launches,
+                      int max_entries) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    recs.swap(g_prof_recs);
+  }
+  std::map<std::string, std::pair<double, int>> agg;
+  for (const ProfRec& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, r.start, r.stop) == cudaSuccess) {
+      auto& a = agg[r.name];
+      a.first += ms;
+      a.second += 1;
+    } else {
+      cudaGetLastError();
+    }
+  }
+  {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    for (const ProfRec& r : recs) {
+      g_prof_pool.push_back(r.start);
+      g_prof_pool.push_back(r.stop);
+    }
+  }
+  int n = 0;
+  size_t used = 0;
+  if (names && names_len) names[0] = 0;
+  for (const auto& kv : agg) {
+    if (n >= max_entries) break;
+    const size_t need = kv.first.size() + 1;
+    if (names == nullptr || used + need >= names_len) break;
+    std::memcpy(names + used, kv.first.c_str(), kv.first.size());
+    names[used + kv.first.size()] = '\n';
+    used += need;
+    names[used] = 0;
+    if (total_ms) total_ms[n] = kv.second.first;
+    if (launches) launches[n] = kv.second.second;
+    ++n;
+  }
+  return n;
+}
+
+beam_status_t beam_debug_wait_timeout(uint64_t timeout_ns, void* stream) {
+  beam::debug_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns);
+  BEAM_LAUNCH_CHECK("debug_wait_kernel");
+  return BEAM_OK;
+}
+
+}  // extern "C"

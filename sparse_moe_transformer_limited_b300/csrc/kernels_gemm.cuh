@@ -1,0 +1,309 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA.
+//
+// Each expert of the layer is a SwiGLU MLP with hidden 5120 and intermediate
+// 2560 ("Reflection 发布 Beam 501B 开源模型，支持 1M tokens 上下文", section
+// 专家混合模型); its outputs are combined with the normalised router weights.
+// The SwiGLU product runs in FP32 (same page, section 残差流).
+//
+// Both GEMMs put the WEIGHTS in the MMA's M=128 operand and the tokens of one
+// expert in the N operand (16..NT columns), so one instruction shape serves
+// decode (2-3 tokens per expert) and prefill (hundreds):
+//   gate/up  (MODE 0): unit = (expert e, 128 intermediate rows m, token tile)
+//            D_g[i,t] = sum_h Wg[e, m*128+i, h] * Xp[t, h]  (TMEM cols [0,NT))
+//            D_u[i,t] = sum_h Wu[e, m*128+i, h] * Xp[t, h]  (TMEM cols [NT,2NT))
+//            epilogue: act[t, m*128+i] = bf16(silu(D_g) * D_u)   (FP32 math)
+//   down     (MODE 1): unit = (expert e, 128 hidden rows m, token tile)
+//            D[h,t] = sum_i Wd[e, m*128+h, i] * act[t, i]
+//            epilogue: acc[token(t), m*128+h] += weight(t) * D[h,t]  (FP32 red)
+//
+// Warp roles (192 threads, persistent, one CTA per SM):
+//   warp 0      TMA producer (one elected lane): fills a STAGES-deep smem ring
+//   warp 1      TMEM owner and MMA issuer (one elected lane)
+//   warps 2..5  epilogue: tcgen05.ld from TMEM lane quarter (warp % 4)
+// The accumulator is double-buffered in TMEM when it fits, so the epilogue of
+// one unit overlaps the main loop of the next.
+//
+// Every wait is bounded (global timer); on expiry the waiter raises a shared
+// abort flag and the device error word, every role drains and the CTA exits
+// normally after its in-flight TMA loads have landed.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace beam {
+
+__device__ int g_beam_err;  // per-device error word, read by beam_status()
+constexpr int DEV_ERR_TIMEOUT = 1;
+
+struct GemmArgs {
+  const int4* units;          // work list
+  const int* n_units;         // device count of units
+  int k_blocks;               // K / 64
+  int a_rows_per_expert;      // I (gate/up) or H (down)
+  __nv_bfloat16* act_out;     // MODE 0: [R, act_ld]
+  int act_ld;
+  const int* row_token;       // MODE 1
+  const float* row_weight;    // MODE 1
+  float* acc;                 // MODE 1: [T, acc_ld] FP32
+  int acc_ld;
+  unsigned long long timeout_ns;
+};
+
+__host__ __device__ constexpr int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int MODE, int NT, int STAGES>
+struct GemmCfg {
+  static constexpr int A_TILE = 128 * 128;  // 128 rows x 64 bf16
+  static constexpr int A_BYTES = (MODE == 0 ? 2 : 1) * A_TILE;
+  static constexpr int B_BYTES = NT * 128;  // NT rows x 64 bf16
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = (MODE == 0 ? 2 : 1) * NT;
+  static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS = pow2_at_least(NBUF * ACC_COLS);
+  static constexpr int BAR_BYTES = (2 * STAGES + 2 * NBUF + 1) * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "token tile");
+  static_assert(TMEM_COLS <= 512, "TMEM");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void gemm_fail(volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicOr(&g_beam_err, DEV_ERR_TIMEOUT);
+}
+
+template <int MODE, int NT, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                       const __grid_constant__ CUtensorMap tm_a1,
+                       const __grid_constant__ CUtensorMap tm_b, const GemmArgs args) {
+  using C = GemmCfg<MODE, NT, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + C::NBUF;
+  uint64_t* mma_done = tempty + C::NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < C::NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tm_a0);
+    if (MODE == 0) tma_prefetch_desc(&tm_a1);
+    tma_prefetch_desc(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_units = *args.n_units;
+  const uint64_t tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const int4 un = args.units[u];
+        const int nb16 = (un.z + 15) >> 4;
+        const uint32_t bytes = C::A_BYTES + nb16 * 2048;
+        const int arow = un.x * args.a_rows_per_expert + un.w * 128;
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            ok = false;
+            break;
+          }
+          uint8_t* sb = smem + stage * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sb, &tm_a0, &full[stage], kb * 64, arow, pol_w);
+          if (MODE == 0) tma_load_2d(sb + C::A_TILE, &tm_a1, &full[stage], kb * 64, arow, pol_w);
+          for (int j = 0; j < nb16; ++j)
+            tma_load_2d(sb + C::A_BYTES + j * 2048, &tm_b, &full[stage], kb * 64, un.y + j * 16,
+                        pol_x);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every load issued must have landed before the CTA may exit.
+      const int pending = issued < STAGES ? issued : STAGES;
+      for (int i = 0; i < pending; ++i) {
+        if (stage == 0) {
+          stage = STAGES - 1;
+          phase ^= 1u;
+        } else {
+          --stage;
+        }
+        const volatile int never = 0;
+        if (!mbar_wait_bounded(&full[stage], phase, tmo, &never)) gemm_fail(abort_flag);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++it) {
+        const int4 un = args.units[u];
+        const int buf = (C::NBUF == 1) ? 0 : (it & 1);
+        const uint32_t tpar = static_cast<uint32_t>((C::NBUF == 1) ? it : (it >> 1)) & 1u;
+        if (!mbar_wait_bounded(&tempty[buf], tpar ^ 1u, tmo, abort_flag)) {
+          gemm_fail(abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const int n16 = (un.z + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(128, n16);
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint64_t da0 = sdesc_k128(sa);
+          const uint64_t da1 = sdesc_k128(sa + C::A_TILE);
+          const uint64_t db = sdesc_k128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            mma_bf16_ss(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+            if (MODE == 0) mma_bf16_ss(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[buf]);
+      }
+      // Every MMA issued by this thread must complete before TMEM is freed.
+      mma_commit(mma_done);
+      const volatile int never = 0;
+      if (!mbar_wait_bounded(mma_done, 0, tmo, &never)) gemm_fail(abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int rloc = q * 32 + lane;
+    int it = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+      const int4 un = args.units[u];
+      const int buf = (C::NBUF == 1) ? 0 : (it & 1);
+      const uint32_t tpar = static_cast<uint32_t>((C::NBUF == 1) ? it : (it >> 1)) & 1u;
+      bool ready = false;
+      if (lane == 0) ready = mbar_wait_bounded(&tfull[buf], tpar, tmo, abort_flag);
+      ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+      if (!ready) {
+        if (lane == 0) gemm_fail(abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      const int nch = (un.z + 15) >> 4;
+      const int col = un.w * 128 + rloc;
+      for (int c = 0; c < nch; ++c) {
+        if (MODE == 0) {
+          float g[16], v[16];
+          tmem_ld16x2(tb + c * 16, tb + NT + c * 16, g, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c * 16 + j;
+            if (tok < un.z) {
+              const float a = g[j] / (1.0f + expf(-g[j])) * v[j];
+              args.act_out[static_cast<size_t>(un.y + tok) * args.act_ld + col] =
+                  __float2bfloat16_rn(a);
+            }
+          }
+        } else {
+          float d[16];
+          tmem_ld16(tb + c * 16, d);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c * 16 + j;
+            if (tok < un.z) {
+              const int r = un.y + tok;
+              const int t = args.row_token[r];
+              const float wgt = args.row_weight[r];
+              atomicAdd(args.acc + static_cast<size_t>(t) * args.acc_ld + col, wgt * d[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// A kernel that waits on a barrier nothing completes, with the bounded wait
+// above; used to test the timeout path without hanging the GPU.
+__global__ void debug_wait_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_bounded(&bar, 0, timeout_ns, &abort_flag)) atomicOr(&g_beam_err, DEV_ERR_TIMEOUT);
+  }
+}
+
+}  // namespace beam

@@ -1,0 +1,90 @@
+"""The C-ABI library loads without a GPU, exports every symbol the public
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_moe_transformer_limited_b300 as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "beam_moe.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(beam_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.lib()
+    names = _declared()
+    assert "beam_moe_forward" in names and len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_params_struct_matches_header():
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} beam_moe_params;", src, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b([A-Za-z_][A-Za-z_0-9]*)\s*[,;]", body)
+    assert fields == [f for f, _ in B.Params._fields_]
+
+
+def _p(**kw):
+    base = dict(T=64, H=5120, E=256, I=2560)
+    base.update(kw)
+    return B.make_params(**base)
+
+
+def test_workspace_size_and_layout():
+    p = _p()
+    n = B.workspace_size(p)
+    lay = B.workspace_layout(p)
+    assert list(lay) == list(B._native.LAYOUT_NAMES)
+    offs = list(lay.values())
+    assert offs == sorted(offs) and offs[-1] < n
+    assert all(o % 1024 == 0 for o in offs)
+    # the permuted copy of x and the SwiGLU buffer are sized for T*top_k rows
+    assert lay["act"] - lay["xperm"] >= 64 * 8 * 5120 * 2
+    big = B.workspace_size(_p(T=16384, flags=B.FLAG_PRE_NORM, residual_k=50))
+    assert big > 16384 * 8 * (5120 + 2560) * 2
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(residual_k=1), 1), (dict(residual_k=-3), 1), (dict(E=48, n_group=8), 2),
+    (dict(H=5000), 2), (dict(I=2500), 2), (dict(top_k=0), 1), (dict(top_k=33), 1),
+    (dict(topk_group=9), 1), (dict(n_group=3), 1), (dict(E=256, n_group=16), 2),
+    (dict(routed_scale=-1.0), 1), (dict(flags=64), 1),
+    (dict(flags=B.FLAG_FP32_OUT, residual_k=50), 1), (dict(T=-1), 1),
+])
+def test_invalid_params_rejected(kw, code):
+    p = _p(**kw)
+    assert B.lib().beam_moe_workspace_size(ctypes.byref(p)) == 0
+    r = B.lib().beam_moe_forward(ctypes.byref(p), *([None] * 12), 0, None)
+    assert r == code, B.last_error()
+    assert B.last_error()
+
+
+def test_null_pointers_rejected():
+    p = _p()
+    r = B.lib().beam_moe_forward(ctypes.byref(p), *([None] * 12), 0, None)
+    assert r == 1
+    r = B.lib().beam_moe_route(ctypes.byref(p), *([None] * 8), 0, None)
+    assert r == 1
+
+
+def test_residual_step_args_rejected():
+    lib = B.lib()
+    assert lib.beam_residual_step(None, None, 4, 5120, 1, None, 1e-6, 1, 0, None, None) == 1
+    assert lib.beam_residual_step(None, None, 4, 5121, 2, None, 1e-6, 1, 0, None, None) == 1
+    assert lib.beam_residual_step(None, None, 4, 5120, 2, None, 1e-6, 1, 0, None, None) == 1
+
+
+def test_empty_batch_is_a_no_op():
+    p = _p(T=0)
+    assert B.lib().beam_moe_forward(ctypes.byref(p), *([None] * 12), 0, None) == 0

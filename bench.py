@@ -1,0 +1,416 @@
+"""Benchmark of the Beam MoE sublayer on B300 GPUs.
+
+One step = one pass of the whole sublayer over one batch: pre-RMSNorm, FP32
+router with group-limited top-8, permutation, SwiGLU experts, weighted
+combine, post-RMSNorm and the scaled residual update at k=50. Inputs are
+synthetic (seeded; see beam_synth.py), weights random-init of the layer's
+shapes (20.1 GB of BF16 expert weights, larger than the 126 MB L2, so no L2
+flush is needed between steps).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|prefill|skew|long_prefill]
+                  [--impl ours|reference]
+
+Prints one JSON line on rank 0. With N > 1 (torchrun) every rank runs an
+independent replica on its own batch (weak scaling, no data-path
+collective); `value` is the tokens/s of all ranks over the slowest rank's
+time. `--impl reference` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import beam_synth as S  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at T=64 and T=8192; % of HBM or BF16 tensor roofline"
+RESIDUAL_K = 50
+LAUNCHES_PER_STEP = 9   # prenorm, router x2, hist, scan, scatter, 2 GEMMs, finalize
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "25", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ workload
+def _workload(name):
+    wl = S.WORKLOADS[name]
+    return wl
+
+
+def _describe(wl):
+    return (f"Beam MoE sublayer, {wl.name}: T={wl.T} tokens, hidden {wl.H}, {wl.E} experts "
+            f"(8 groups x 32, keep 4), top-{wl.top_k}, SwiGLU intermediate {wl.I}; "
+            f"pre-RMSNorm -> FP32 sigmoid router -> permute -> experts -> x2.5 weighted "
+            f"combine -> post-RMSNorm -> residual k={RESIDUAL_K}")
+
+
+def _algorithmic(wl, counts):
+    """Algorithmic bytes / FLOPs of the two expert GEMMs (what the method must
+    move and compute: each touched expert's weights once, the activations in
+    and out)."""
+    touched = int((counts > 0).sum())
+    R = wl.T * wl.top_k
+    gu_bytes = touched * 2 * wl.I * wl.H * 2 + R * wl.H * 2 + R * wl.I * 2
+    dn_bytes = touched * wl.H * wl.I * 2 + R * wl.I * 2 + wl.T * wl.H * 4
+    gu_flops = 2.0 * R * 2 * wl.I * wl.H
+    dn_flops = 2.0 * R * wl.I * wl.H
+    layer_bytes = touched * 3 * wl.I * wl.H * 2 + 2 * wl.T * wl.H * 2 + wl.E * wl.H * 4
+    return dict(touched=touched, gu_bytes=gu_bytes, dn_bytes=dn_bytes, gu_flops=gu_flops,
+                dn_flops=dn_flops, layer_bytes=layer_bytes,
+                layer_flops=gu_flops + dn_flops + 2.0 * wl.T * wl.H * wl.E)
+
+
+def _traffic_for(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    src = os.path.join(ROOT, "sparse_moe_transformer_limited_b300", "csrc", "kernels_gemm.cuh")
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    for r in rec.get("entries", []):
+        if r.get("kernel") == kernel and r.get("workload") == workload and r.get("src_sha") == sha:
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import sparse_moe_transformer_limited_b300 as B
+    B.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = _workload(args.config)
+    wl_rank = wl.replace(seed=wl.seed + 1000 * rank) if rank else wl
+    d = S.make_inputs(wl_rank, dev)
+    p = B.make_params(wl.T, wl.H, wl.E, wl.I, wl.n_group, wl.topk_group, wl.top_k,
+                      wl.routed_scale, wl.rms_eps, RESIDUAL_K, B.FLAG_PRE_NORM)
+    ws = B.alloc_workspace(p, dev)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
+                  bias=d["bias"], out=out, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    lay = B.workspace_layout(p)
+    counts = ws[lay["counts"]:lay["counts"] + wl.E * 4].view(torch.int32).cpu().numpy()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- device-timed region (inputs resident in HBM)
+    clocks = ClockSampler(local_rank)
+    barrier()
+    clocks.start()
+    B.profile_read()
+    B.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    B.profile_enable(False)
+    clk = clocks.stop()
+    prof = B.profile_read()
+    ms_total = e0.elapsed_time(e1)
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * wl.T * args.steps / (ms_total / 1e3)
+
+    # ---- end-to-end through the public API with host buffers
+    h_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    h_host.copy_(d["x"].cpu())
+    o_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(d["x"])
+
+    def e2e_step():
+        x_dev.copy_(h_host, non_blocking=True)
+        B.forward(p, x_dev, d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
+                  bias=d["bias"], out=out, workspace=ws)
+        o_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = world * wl.T * args.steps / float(te.item())
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+
+    alg = _algorithmic(wl, counts)
+    peaks = _peaks()
+    gu_ms = prof["expert_gemm_gateup_swiglu"][0] / prof["expert_gemm_gateup_swiglu"][1]
+    dn_ms = prof["expert_gemm_down_combine"][0] / prof["expert_gemm_down_combine"][1]
+    decode_like = wl.T * wl.top_k <= 24 * wl.E
+    kname = "expert_gemm_gateup_swiglu"
+    if decode_like:
+        achieved = alg["gu_bytes"] / (gu_ms / 1e3) / 1e9
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+                "peak_source": peaks["source"] + " hbm_gbs",
+                "traffic": _traffic_for(kname, wl.name),
+                "algorithmic_bytes_per_launch": alg["gu_bytes"], "launch_ms": round(gu_ms, 4)}
+    else:
+        achieved = alg["gu_flops"] / (gu_ms / 1e3) / 1e12
+        roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
+                "peak_source": peaks["source"] + " bf16_tflops (burst)",
+                "traffic": _traffic_for(kname, wl.name),
+                "algorithmic_flops_per_launch": alg["gu_flops"], "launch_ms": round(gu_ms, 4)}
+    layer = {"hbm_frac": round(alg["layer_bytes"] / (ms_step / 1e3) / 1e9 / peaks["hbm"], 4),
+             "tensor_frac": round(alg["layer_flops"] / (ms_step / 1e3) / 1e12 / peaks["bf16"], 4),
+             "touched_experts": alg["touched"], "max_tokens_per_expert": int(counts.max())}
+    kernels = {k: round(v[0] / v[1], 4) for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
+    return dict(value=value, ms_step=ms_step, e2e=e2e_value, clocks=clk, roofline=roof,
+                layer=layer, kernels_ms=kernels, wl=wl,
+                h2d=wl.T * wl.H * 2, d2h=wl.T * wl.H * 2)
+
+
+# ---------------------------------------------------------- oracle arm
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(wl, n_tokens, device):
+    """Stage the oracle (as it stands) on the first n_tokens of the batch and
+    return a callable that runs it once: pre-norm, routing, experts, combine,
+    post-norm and residual. Expert weights are copied to host memory here,
+    before any clock starts."""
+    import oracle as O
+    d = S.make_inputs(wl, device)
+    x = d["x"][:n_tokens].float().cpu().numpy()
+    wr = d["w_router"].float().cpu().numpy()
+    bias = None if d["bias"] is None else d["bias"].float().cpu().numpy()
+    xn = O.bf16_round(O.rms_norm(x.astype(np.float64), None, wl.rms_eps)).astype(np.float64)
+    sel = O.route(xn, wr, bias, wl.n_group, wl.topk_group, wl.top_k, wl.routed_scale)
+    weights = {int(e): tuple(d[k][int(e)].float().cpu().numpy()
+                             for k in ("w_gate", "w_up", "w_down"))
+               for e in np.unique(sel["idx"])}
+    del d
+
+    def run():
+        O.moe_forward(x, wr, bias, lambda e: weights[e], n_group=wl.n_group,
+                      topk_group=wl.topk_group, top_k=wl.top_k, scale=wl.routed_scale,
+                      eps=wl.rms_eps, pre_norm=True, residual_k=RESIDUAL_K)
+    return run, len(weights)
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, each step a bounded sample (2
+    tokens) of the same workload, on the host cores of rank 0 only."""
+    if rank != 0:
+        return None
+    wl = _workload(args.config)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    n_tok = 2
+    run, ne = oracle_sample(wl, n_tok, dev)
+    for _ in range(min(args.warmup, 1)):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    total = time.perf_counter() - t0
+    value = n_tok * args.steps / total
+    sample = (f"{n_tok} tokens of the {wl.name} batch per step (full sublayer path: pre-norm, "
+              f"routing, {wl.top_k} experts each ({ne} distinct), combine, post-norm, "
+              f"residual); weights staged on host before timing")
+    return dict(value=value, ms_step=1e3 * total / args.steps, cores=_blas_threads(),
+                sample=sample)
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the secondary T=8192 measurement")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1 and args.impl == "ours":
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    wl = _workload(args.config)
+    if args.impl == "reference":
+        r = run_reference(args, rank, world)
+        if r is None:
+            return
+        line = {"impl": "reference", "metric": METRIC, "value": round(r["value"], 4),
+                "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": _describe(wl), "T": wl.T, "seed": wl.seed},
+                "cpu_baseline": {"value": round(r["value"], 4), "unit": "tokens/s",
+                                 "cores": r["cores"], "kind": "oracle", "sample": r["sample"]},
+                "e2e": {"value": round(r["value"], 4), "unit": "tokens/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, rank, world, local_rank)
+    extra = {}
+    if rank == 0 and world == 1 and args.config == "decode" and not args.no_prefill:
+        a2 = argparse.Namespace(**vars(args))
+        a2.config = "prefill"
+        torch.cuda.empty_cache()
+        r2 = run_ours(a2, rank, world, local_rank)
+        extra = {"prefill_T8192": {"value": round(r2["value"], 1), "unit": "tokens/s",
+                                   "ms_per_step": round(r2["ms_step"], 4),
+                                   "e2e": round(r2["e2e"], 1), "roofline": r2["roofline"],
+                                   "layer": r2["layer"], "kernels_ms": r2["kernels_ms"],
+                                   "clocks": r2["clocks"]}}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        torch.cuda.empty_cache()
+        n_tok = 4
+        run, ne = oracle_sample(wl, n_tok, "cuda")
+        t0 = time.perf_counter()
+        run()
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(n_tok / dt, 4), "unit": "tokens/s", "cores": _blas_threads(),
+               "kind": "oracle",
+               "sample": f"{n_tok} tokens of the {wl.name} batch (full sublayer path, {ne} "
+                         f"experts), {dt:.1f} s of CPU work; weights staged on host before "
+                         f"timing"}
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": round(r["value"], 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": round(r["ms_step"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": _describe(wl), "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I,
+                       "top_k": wl.top_k, "seed": wl.seed,
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "no flush: 20.1 GB of expert weights per step exceed the 126 MB L2"},
+            "roofline": r["roofline"], "layer": r["layer"], "kernels_ms": r["kernels_ms"],
+            "clocks": r["clocks"],
+            "e2e": {"value": round(r["e2e"], 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "cpu_baseline": cpu}
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,138 @@
+"""GPU parity at the layer's full size (H=5120, E=256, I=2560, 20 GB of expert
+weights): routing of every token against the oracle, layer outputs on
+sampled tokens the oracle computes one by one, and the invariants that hold
+at any size. Includes the exact launch configuration the benchmark times
+(pre-norm, router, experts, post-norm, residual at k=50, T=64 and T=8192)."""
+import numpy as np
+import pytest
+import torch
+
+import beam_synth as S
+import oracle as O
+from _helpers import (OUT_REL_TOL, compare_routing, expert_getter, host, oracle_outputs,
+                      prenorm_ambiguous, rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import sparse_moe_transformer_limited_b300 as B
+    B.lib()
+    return B
+
+
+def _params(B, wl, flags=0, residual_k=0):
+    return B.make_params(wl.T, wl.H, wl.E, wl.I, wl.n_group, wl.topk_group, wl.top_k,
+                         wl.routed_scale, wl.rms_eps, residual_k, flags)
+
+
+def _forward(B, wl, d, flags=0, residual_k=0):
+    p = _params(B, wl, flags, residual_k)
+    ws = B.alloc_workspace(p)
+    idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device="cuda")
+    out = B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
+                    bias=d["bias"], topk_idx=idx, topk_w=w, workspace=ws)
+    assert B.status() == 0, B.last_error()
+    counts = ws[B.workspace_layout(p)["counts"]:][:wl.E * 4].view(torch.int32).cpu().numpy()
+    return out, idx.cpu().numpy(), w.cpu().numpy(), counts
+
+
+def _sample(T, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(T, size=min(n, T), replace=False))
+
+
+def _check(wl, d, out, gi, gw, sample, x64=None, h64=None, residual_k=0, clean=None):
+    """Routing of every (clean) token; outputs of the sampled tokens."""
+    if x64 is None:
+        x64 = host(d["x"]).astype(np.float64)
+    toks = np.arange(wl.T) if clean is None else clean
+    sel = O.route(x64[toks], host(d["w_router"]), host(d["bias"]), wl.n_group,
+                  wl.topk_group, wl.top_k, wl.routed_scale)
+    ties, chosen = compare_routing(sel, gi[toks], gw[toks], wl)
+    pos = {int(t): i for i, t in enumerate(toks)}
+    samp = np.array([t for t in sample if int(t) in pos])
+    rows = [chosen[pos[int(t)]] for t in samp]
+    o = oracle_outputs(x64[samp], rows, np.arange(len(samp)), expert_getter(d))
+    if residual_k:
+        want = O.residual_step(h64[samp], o, residual_k, None, wl.rms_eps, True)
+    else:
+        want = o
+    err = rel_err(host(out)[samp], want)
+    assert err <= OUT_REL_TOL, f"rel err {err}"
+    return int(ties.sum()), err
+
+
+def test_decode_layer_T64(B):
+    """Full Beam layer, decode regime: every token's output checked."""
+    wl = S.WORKLOADS["decode"]
+    d = S.make_inputs(wl, "cuda")
+    out, gi, gw, counts = _forward(B, wl, d, B.FLAG_FP32_OUT)
+    n_ties, err = _check(wl, d, out, gi, gw, np.arange(wl.T))
+    assert counts.sum() == wl.T * 8 and 180 <= (counts > 0).sum() <= 256
+    print(f"decode: near ties {n_ties}, rel err {err:.2e}, touched {(counts > 0).sum()}")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_bench_configuration(B, name):
+    """What the benchmark times: h_prev N(0,1) -> pre-norm -> MoE -> post-norm
+    -> residual k=50, at T=64 and T=8192."""
+    wl = S.WORKLOADS[name]
+    d = S.make_inputs(wl, "cuda")
+    hk, gi, gw, counts = _forward(B, wl, d, B.FLAG_PRE_NORM, 50)
+    h64 = host(d["x"]).astype(np.float64)
+    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
+    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
+    clean = np.nonzero(~amb.any(axis=1))[0]
+    assert len(clean) >= 0.8 * wl.T
+    sample = _sample(wl.T, 64 if wl.T <= 64 else 16, 1)
+    n_ties, err = _check(wl, d, hk, gi, gw, sample, x64=x64, h64=h64, residual_k=50,
+                         clean=clean)
+    print(f"{name}: clean {len(clean)}/{wl.T}, near ties {n_ties}, rel err {err:.2e}")
+
+
+def test_prefill_layer_T8192(B):
+    wl = S.WORKLOADS["prefill"]
+    d = S.make_inputs(wl, "cuda")
+    out, gi, gw, counts = _forward(B, wl, d, 0)
+    n_ties, err = _check(wl, d, out, gi, gw, _sample(wl.T, 16, 2))
+    assert counts.sum() == wl.T * 8 and (counts > 0).sum() == 256
+    # any-size invariants: weights sum to 2.5, all experts distinct per token
+    assert np.allclose(gw.sum(1), 2.5, atol=1e-5)
+    assert all(len(set(r)) == 8 for r in gi.tolist())
+    print(f"prefill: near ties {n_ties}, rel err {err:.2e}, max/expert {counts.max()}")
+
+
+def test_skewed_layer_T4096(B):
+    wl = S.WORKLOADS["skew"]
+    d = S.make_inputs(wl, "cuda")
+    out, gi, gw, counts = _forward(B, wl, d, 0)
+    hot = np.argsort(-counts)[:2]
+    # sample: a few tokens of the two hottest experts plus random tokens
+    hot_toks = np.nonzero(np.isin(gi, hot).any(axis=1))[0][:8]
+    sample = np.unique(np.concatenate([_sample(wl.T, 8, 3), hot_toks]))
+    n_ties, err = _check(wl, d, out, gi, gw, sample)
+    assert counts.max() > 1000 and (counts == 0).sum() > 0
+    print(f"skew: max {counts.max()}, median {np.median(counts)}, zero {(counts == 0).sum()}, "
+          f"near ties {n_ties}, rel err {err:.2e}")
+
+
+def test_long_prefill_residual_T16384(B):
+    wl = S.WORKLOADS["long_prefill"]
+    d = S.make_inputs(wl, "cuda")
+    hk, gi, gw, counts = _forward(B, wl, d, B.FLAG_PRE_NORM, wl.residual_k)
+    h64 = host(d["x"]).astype(np.float64)
+    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
+    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
+    clean = np.nonzero(~amb.any(axis=1))[0]
+    assert len(clean) >= 0.8 * wl.T
+    n_ties, err = _check(wl, d, hk, gi, gw, _sample(wl.T, 16, 4), x64=x64, h64=h64,
+                         residual_k=wl.residual_k, clean=clean)
+    # the stream keeps unit scale: h = a*h_prev + b*n with |n| RMS 1
+    rms = torch.sqrt(hk.float().pow(2).mean(1)).cpu().numpy()
+    assert np.all(np.abs(rms - 1.0) < 0.05)
+    print(f"long prefill: clean {len(clean)}/{wl.T}, near ties {n_ties}, rel err {err:.2e}")

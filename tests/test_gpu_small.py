@@ -198,7 +198,8 @@ def test_forward_permutation_stage(B):
         g = wg.astype(np.float64) @ xr
         u = wu.astype(np.float64) @ xr
         a = O.silu(g) * u
-        assert np.max(np.abs(act[r] - a)) <= 1e-2 * np.sqrt(np.mean(a * a)) + 1e-6
+        # BF16 rounding of the FP32 product (half an ulp) plus accumulation-order slack
+        assert np.all(np.abs(act[r] - a) <= bf16_ulp(a) + 1e-6)
 
 
 def test_forward_empty_batch(B):

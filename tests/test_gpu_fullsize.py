@@ -116,7 +116,10 @@ def test_skewed_layer_T4096(B):
     hot_toks = np.nonzero(np.isin(gi, hot).any(axis=1))[0][:8]
     sample = np.unique(np.concatenate([_sample(wl.T, 8, 3), hot_toks]))
     n_ties, err = _check(wl, d, out, gi, gw, sample)
-    assert counts.max() > 1000 and (counts == 0).sum() > 0
+    # Zipf-like load: hot experts take > 1000 tokens (about 9x the median);
+    # with this recipe no expert ends up empty (empty experts are covered by
+    # the small edge-case tests)
+    assert counts.max() > 1000 and counts.max() > 8 * np.median(counts)
     print(f"skew: max {counts.max()}, median {np.median(counts)}, zero {(counts == 0).sum()}, "
           f"near ties {n_ties}, rel err {err:.2e}")
 

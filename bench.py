@@ -327,6 +327,30 @@ def run_reference(args, rank, world):
                 sample=sample)
 
 
+# ------------------------------------------------------------ ncu cases
+def run_ncu_case(kind):
+    """A small case for profiler captures: the full layer path with the real
+    H=5120 / I=2560 shapes but 32 experts (one group, plain top-8), so the
+    expert weights take 2.5 GB -- more than the L2, little device memory.
+    kind 'decode': T=64 (16 tokens/expert, token tile 32);
+    kind 'prefill': T=2048 (512 tokens/expert, token tile 128).
+    Runs four forward calls (pre-norm + residual k=50) and exits."""
+    import sparse_moe_transformer_limited_b300 as B
+    T = 64 if kind == "decode" else 2048
+    wl = S.Workload("ncu_" + kind, T=T, E=32, n_group=1, topk_group=1, seed=7)
+    d = S.make_inputs(wl, "cuda")
+    p = B.make_params(wl.T, wl.H, wl.E, wl.I, wl.n_group, wl.topk_group, wl.top_k,
+                      wl.routed_scale, wl.rms_eps, RESIDUAL_K, B.FLAG_PRE_NORM)
+    ws = B.alloc_workspace(p)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    for _ in range(4):
+        B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], out=out,
+                  workspace=ws)
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    print(f"ncu case {kind}: ok")
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -338,7 +362,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the secondary T=8192 measurement")
+    ap.add_argument("--ncu-case", choices=["decode", "prefill"],
+                    help="run the small profiler case and exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

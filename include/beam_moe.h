@@ -153,6 +153,41 @@ beam_status_t beam_status(void* stream);
  * string stays valid until the next call on the same thread. */
 const char* beam_last_error_string(void);
 
+/* Router for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point: it is an interface
+ * choice of this library. Some programs that call the router cannot allocate:
+ * hosts that hand all of a GPU's memory to their own pool at start-up and
+ * forbid further cudaMalloc, and plug-ins inside such hosts that are given
+ * no allocator and no workspace. beam_moe_route needs a caller workspace;
+ * this variant needs none and allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library call). Its scratch -- the router's partial logits and,
+ * with BEAM_FLAG_PRE_NORM, the normalised x -- is a fixed array of
+ * BEAM_ROUTE_STATIC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Arguments, results and errors are those of beam_moe_route (same kernels,
+ * same K-slicing, so the results are identical), without the workspace.
+ * Scratch needed: KS*T*E*4 bytes (rounded up to 256) for the partial logits,
+ * where KS is the number of K-slices the router uses for this T (many for a
+ * few tokens, one for thousands), plus T*H*2 bytes with BEAM_FLAG_PRE_NORM.
+ * A call needing more returns BEAM_ERR_UNSUPPORTED with a message that gives
+ * the bytes needed; nothing is enqueued then. For the Beam shapes (H=5120,
+ * E=256, 148 SMs) that allows T <= 409 with pre-norm and T <= 8192 without.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture. All calls on a device share the one
+ * array and it keeps the last call's contents; every call writes each scratch
+ * byte it later reads, so nothing needs clearing between calls. Calls whose
+ * work overlaps on the GPU (other streams, other host threads) race on the
+ * array: the caller must order them. */
+#define BEAM_ROUTE_STATIC_SCRATCH_BYTES (8u << 20)
+beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
+                                    const float* w_router, const float* logit_bias,
+                                    const float* pre_gain, int32_t* topk_idx, float* topk_w,
+                                    float* scores, void* stream);
+
 /* ---- diagnostics (tests and tooling) ---------------------------------- */
 
 /* Byte offsets of the internal buffers inside the forward workspace, in this

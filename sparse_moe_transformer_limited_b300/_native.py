@@ -34,7 +34,8 @@ LAYOUT_NAMES = ("xn", "part", "topk_idx", "topk_w", "counts", "offsets", "row_to
                 "units_gu", "units_dn")
 
 # every symbol include/beam_moe.h declares
-EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_forward",
+EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static",
+            "beam_moe_forward",
             "beam_residual_step", "beam_status", "beam_last_error_string",
             "beam_moe_workspace_layout", "beam_debug_wait_timeout", "beam_profile_enable",
             "beam_profile_read")
@@ -73,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.beam_moe_workspace_layout.restype = i32
         L.beam_moe_route.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.beam_moe_route.restype = i32
+        L.beam_moe_route_static.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.beam_moe_route_static.restype = i32
         L.beam_moe_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.beam_moe_forward.restype = i32
         L.beam_residual_step.argtypes = [vp, vp, i32, i32, i32, vp, f32, i32, i32, vp, vp]
@@ -151,6 +154,23 @@ def route(p: Params, x, w_router, bias=None, pre_gain=None, topk_idx=None, topk_
     _check(lib().beam_moe_route(ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(bias),
                                 _ptr(pre_gain), _ptr(topk_idx), _ptr(topk_w), _ptr(scores),
                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+    return topk_idx, topk_w, scores
+
+
+def route_static(p: Params, x, w_router, bias=None, pre_gain=None, topk_idx=None,
+                 topk_w=None, scores=None, stream=None):
+    """beam_moe_route_static: the router with its scratch in a fixed array
+    inside the library (no workspace, no allocation by the library)."""
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((p.T, p.top_k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((p.T, p.top_k), dtype=torch.float32, device=dev)
+    if scores is None and (p.flags & FLAG_RETURN_SCORES):
+        scores = torch.empty((p.T, p.E), dtype=torch.float32, device=dev)
+    _check(lib().beam_moe_route_static(ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(bias),
+                                       _ptr(pre_gain), _ptr(topk_idx), _ptr(topk_w),
+                                       _ptr(scores), _stream(stream)))
     return topk_idx, topk_w, scores
 
 

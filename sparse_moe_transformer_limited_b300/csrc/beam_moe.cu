@@ -570,3 +570,77 @@ beam_status_t beam_debug_wait_timeout(uint64_t timeout_ns, void* stream) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Allocation-free router (beam_moe_route_static).
+//
+// Its scratch -- the router's partial logits and, with BEAM_FLAG_PRE_NORM,
+// the normalised x -- lives in this file-scope device array of
+// BEAM_ROUTE_STATIC_SCRATCH_BYTES bytes. Every device that loads the library
+// holds the array until the process exits. Host code must not pass the
+// array's name to a kernel (on the host it names a stand-in, not device
+// memory): the device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, and passed to the kernels.
+// ===========================================================================
+static __device__ __align__(256) unsigned char g_route_static_scratch[BEAM_ROUTE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_route_static_mu;
+void* g_route_static_addr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device (looked up on
+// the first call for that device, then cached).
+beam_status_t route_static_scratch(void** addr) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(BEAM_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(BEAM_ERR_UNSUPPORTED, "device ordinal %d is beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> g(g_route_static_mu);
+  if (g_route_static_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_route_static_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(BEAM_ERR_CUDA, "cudaGetSymbolAddress of the router scratch failed: %s",
+                  cudaGetErrorString(e));
+    g_route_static_addr[dev] = ptr;
+  }
+  *addr = g_route_static_addr[dev];
+  return BEAM_OK;
+}
+
+}  // namespace
+
+extern "C" beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
+                                               const float* w_router, const float* logit_bias,
+                                               const float* pre_gain, int32_t* topk_idx,
+                                               float* topk_w, float* scores, void* stream) {
+  beam_status_t s = check_params(p);
+  if (s != BEAM_OK) return s;
+  if (p->T == 0) return BEAM_OK;
+  if (!x || !w_router || !topk_idx || !topk_w)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if ((p->flags & BEAM_FLAG_RETURN_SCORES) && !scores)
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_RETURN_SCORES needs a scores buffer");
+  if (!aligned16(x) || !aligned16(w_router) || (pre_gain && !aligned16(pre_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "x, w_router and pre_gain must be 16-byte aligned");
+  // Same K-slicing as beam_moe_route, so both entry points give identical results.
+  Layout L{};
+  L.KS = choose_router_ks(*p, sm_count());
+  const size_t part = align_up(static_cast<size_t>(L.KS) * p->T * p->E * 4, 256);
+  const size_t xn = (p->flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p->T) * p->H * 2 : 0;
+  if (part + xn > BEAM_ROUTE_STATIC_SCRATCH_BYTES)
+    return fail(BEAM_ERR_UNSUPPORTED,
+                "T=%d needs %zu bytes of router scratch; the static scratch holds %zu bytes "
+                "(use beam_moe_route with a workspace for this size)",
+                p->T, part + xn, static_cast<size_t>(BEAM_ROUTE_STATIC_SCRATCH_BYTES));
+  void* base = nullptr;
+  if ((s = route_static_scratch(&base)) != BEAM_OK) return s;
+  L.off[L_PART] = 0;
+  L.off[L_XN] = part;
+  return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
+                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr, nullptr,
+                       static_cast<uint8_t*>(base), static_cast<cudaStream_t>(stream));
+}

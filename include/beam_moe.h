@@ -58,7 +58,7 @@ typedef enum {
 
 /* Shape and hyper-parameters of one MoE sublayer call.
  *   T           tokens in the batch (0 is allowed: nothing is enqueued)
- *   H           hidden size (5120 for Beam); multiple of 128
+ *   H           hidden size (5120 for Beam); multiple of 128, at most 8192
  *   E           experts (256 for Beam); multiple of 32, at most 256
  *   I           expert SwiGLU intermediate size (2560); multiple of 128
  *   n_group     expert groups (8); E / n_group must be 32, or n_group must equal
@@ -111,7 +111,8 @@ beam_status_t beam_moe_route(const beam_moe_params* p, const void* x,
  *   y_e = (silu(x W_gate[e]^T) * (x W_up[e]^T)) W_down[e]^T for each selected
  *         expert, BF16 operands, FP32 accumulation, SwiGLU product in FP32,
  *         the intermediate rounded to BF16 before the down projection
- *   o   = sum_j topk_w[t,j] * y_{topk_idx[t,j]}   (FP32)
+ *   o   = sum_j topk_w[t,j] * y_{topk_idx[t,j]}   (FP32 expert outputs, FP32 sum
+ *         in slot order)
  *   out = residual_k >= 2 ? bf16(sqrt((k-1)/k) x_in + RMSNorm(o) * post_gain / sqrt(k))
  *                         : o (bf16, or fp32 with BEAM_FLAG_FP32_OUT)
  * Arguments:
@@ -123,8 +124,7 @@ beam_status_t beam_moe_route(const beam_moe_params* p, const void* x,
  *   topk_idx, topk_w  optional outputs as in beam_moe_route (NULL: kept in the
  *              workspace)
  * Token-to-expert order inside the workspace is stable (by token, then slot).
- * The FP32 combine uses atomic adds, so the last bits of `out` may vary from
- * run to run; routing is deterministic. */
+ * Results are deterministic: the same inputs give bit-identical outputs. */
 beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in,
                                const float* w_router, const float* logit_bias,
                                const void* w_gate, const void* w_up, const void* w_down,
@@ -194,11 +194,11 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
  * order: 0 normalised x [T,H] bf16, 1 router partial logits, 2 topk_idx,
  * 3 topk_w, 4 expert counts [E] int32, 5 expert offsets [E+1] int32,
  * 6 row_token [T*top_k] int32, 7 row_weight [T*top_k] fp32, 8 permuted x
- * [T*top_k,H] bf16, 9 SwiGLU activations [T*top_k,I] bf16, 10 FP32
- * accumulator [T,H], 11 unit counts [4] int32, 12 per-block expert
- * histograms, 13 per-block expert offsets, 14 gate/up work list, 15 down
- * work list. Writes min(n, 16) entries and returns how many it wrote (0 on
- * invalid parameters). */
+ * [T*top_k,H] bf16, 9 SwiGLU activations [T*top_k,I] bf16, 10 per-pair
+ * expert outputs [T*top_k,H] fp32, 11 unit counts [4] int32, 12 per-block
+ * expert histograms, 13 per-block expert offsets, 14 gate/up work list,
+ * 15 down work list, 16 pair -> row map [T*top_k] int32. Writes min(n, 17)
+ * entries and returns how many it wrote (0 on invalid parameters). */
 int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n);
 
 /* Launches one block whose single thread waits on a shared-memory barrier

@@ -15,6 +15,7 @@
 
 #include "beam_moe.h"
 #include "kernels_gemm.cuh"
+#include "kernels_gemm_tm.cuh"
 #include "kernels_permute.cuh"
 #include "kernels_router.cuh"
 #include "kernels_rows.cuh"
@@ -98,13 +99,22 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ------------------------------------------------------------------ tiles
-// Token-tile width of the expert GEMMs, chosen from the mean tokens per
-// expert: narrow tiles when each expert sees a handful of tokens (decode),
-// wide tiles for prefill.
-int choose_nt(const beam_moe_params& p) {
+// Expert-GEMM path, chosen from the mean tokens per expert:
+//  few tokens per expert (decode): weights as the M=128 operand, token tiles
+//    of 32 (expert_gemm_kernel);
+//  many tokens (prefill): token-major two-CTA clusters sharing 256-row weight
+//    tiles, 256-row token groups (expert_gemm_tm_kernel; needs H % 256 == 0);
+//    otherwise weights as M with token tiles of 128.
+enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2 };
+
+GemmPath choose_path(const beam_moe_params& p) {
   const long long pairs = static_cast<long long>(p.T) * p.top_k;
-  return (pairs <= 24LL * p.E) ? 32 : 128;
+  if (pairs <= 24LL * p.E) return PATH_W32;
+  return (p.H % 256 == 0) ? PATH_TM : PATH_W128;
 }
+
+int path_nt(GemmPath g) { return g == PATH_W32 ? 32 : (g == PATH_W128 ? 128 : 256); }
+int path_mt_down(GemmPath g, int H) { return g == PATH_TM ? H / 256 : H / 128; }
 
 // K-slices of the router logits GEMM: enough blocks to cover the SMs when T
 // is small. Must divide H / 32 and leave at least 64 columns per slice.
@@ -118,16 +128,19 @@ int choose_router_ks(const beam_moe_params& p, int num_sms) {
   return best;
 }
 
+constexpr int kLayoutEntries = 17;
+
 struct Layout {
-  size_t off[16];
+  size_t off[kLayoutEntries];
   size_t total;
   int KS, NB, NT;
+  GemmPath path;
   long long units_gu_max, units_dn_max;
 };
 
 enum {
-  L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_ACC,
-  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN
+  L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_Y,
+  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW
 };
 
 int sm_count() {
@@ -148,8 +161,8 @@ beam_status_t check_params(const beam_moe_params* p) {
   if (p->T > (1 << 22)) return fail(BEAM_ERR_UNSUPPORTED, "T=%d exceeds 4194304", p->T);
   if (p->H % 128 || p->I % 128)
     return fail(BEAM_ERR_UNSUPPORTED, "H=%d and I=%d must be multiples of 128", p->H, p->I);
-  if (p->H > 65536 || p->I > 65536)
-    return fail(BEAM_ERR_UNSUPPORTED, "H and I must be at most 65536");
+  if (p->H > 8192 || p->I > 65536)
+    return fail(BEAM_ERR_UNSUPPORTED, "H must be at most 8192 and I at most 65536");
   if (p->E % 32 || p->E > 256)
     return fail(BEAM_ERR_UNSUPPORTED, "E=%d must be a multiple of 32 and at most 256", p->E);
   if (p->n_group <= 0 || p->E % p->n_group)
@@ -183,12 +196,13 @@ Layout make_layout(const beam_moe_params& p) {
   const int nsm = sm_count();
   L.KS = choose_router_ks(p, nsm);
   L.NB = (p.T + beam::PERM_TPB - 1) / beam::PERM_TPB;
-  L.NT = choose_nt(p);
+  L.path = choose_path(p);
+  L.NT = path_nt(L.path);
   const long long R = static_cast<long long>(p.T) * p.top_k;
   const long long tiles = (R + L.NT - 1) / L.NT + p.E;
   L.units_gu_max = tiles * (p.I / 128);
-  L.units_dn_max = tiles * (p.H / 128);
-  size_t sz[16];
+  L.units_dn_max = tiles * path_mt_down(L.path, p.H);
+  size_t sz[kLayoutEntries];
   sz[L_XN] = (p.flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p.T) * p.H * 2 : 0;
   sz[L_PART] = static_cast<size_t>(L.KS) * p.T * p.E * 4;
   sz[L_IDX] = static_cast<size_t>(R) * 4;
@@ -199,14 +213,15 @@ Layout make_layout(const beam_moe_params& p) {
   sz[L_ROWW] = static_cast<size_t>(R) * 4;
   sz[L_XPERM] = static_cast<size_t>(R) * p.H * 2;
   sz[L_ACT] = static_cast<size_t>(R) * p.I * 2;
-  sz[L_ACC] = static_cast<size_t>(p.T) * p.H * 4;
+  sz[L_Y] = static_cast<size_t>(R) * p.H * 4;
   sz[L_NUNITS] = 16;
   sz[L_BLKHIST] = static_cast<size_t>(L.NB) * p.E * 4;
   sz[L_BLKOFF] = static_cast<size_t>(L.NB) * p.E * 4;
   sz[L_UGU] = static_cast<size_t>(L.units_gu_max) * 16;
   sz[L_UDN] = static_cast<size_t>(L.units_dn_max) * 16;
+  sz[L_PAIRROW] = static_cast<size_t>(R) * 4;
   size_t cur = 0;
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < kLayoutEntries; ++i) {
     L.off[i] = cur;
     cur = align_up(cur + sz[i], 1024);
   }
@@ -269,9 +284,27 @@ beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CU
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
     attr_set = true;
   }
-  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down_combine", st);
+  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
   kern<<<sm_count(), 192, C::SMEM_BYTES, st>>>(a0, a1, b, args);
   BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>" : "expert_gemm_kernel<down>");
+  return BEAM_OK;
+}
+
+template <int MODE>
+beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& tok,
+                             const beam::TmArgs& args, cudaStream_t st) {
+  using C = beam::TmCfg;
+  auto kern = beam::expert_gemm_tm_kernel<MODE>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    BEAM_CUDA_TRY(
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
+    attr_set = true;
+  }
+  const int grid = (sm_count() / 2) * 2;
+  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(w0, w1, tok, args);
+  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_tm_kernel<gate/up>" : "expert_gemm_tm_kernel<down>");
   return BEAM_OK;
 }
 
@@ -327,7 +360,7 @@ size_t beam_moe_workspace_size(const beam_moe_params* p) {
 int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n) {
   if (check_params(p) != BEAM_OK || offsets == nullptr || n <= 0) return 0;
   const Layout L = make_layout(*p);
-  const int m = n < 16 ? n : 16;
+  const int m = n < kLayoutEntries ? n : kLayoutEntries;
   for (int i = 0; i < m; ++i) offsets[i] = L.off[i];
   return m;
 }
@@ -382,24 +415,25 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   const long long R = static_cast<long long>(T) * K;
   int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.off[L_IDX]);
   float* wts = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.off[L_W]);
-  const bool direct_fp32 = (p->flags & BEAM_FLAG_FP32_OUT) && p->residual_k == 0;
-  float* acc = direct_fp32 ? static_cast<float*>(out) : reinterpret_cast<float*>(ws + L.off[L_ACC]);
 
-  // 1. pre-norm (optional) + router, which also zeroes the FP32 accumulator
-  s = launch_router(*p, L, x_in, w_router, logit_bias, pre_gain, idx, wts, nullptr, acc, ws, st);
+  // 1. pre-norm (optional) + router
+  s = launch_router(*p, L, x_in, w_router, logit_bias, pre_gain, idx, wts, nullptr, nullptr, ws,
+                    st);
   if (s != BEAM_OK) return s;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
   if (p->flags & BEAM_FLAG_PRE_NORM) x = reinterpret_cast<const __nv_bfloat16*>(ws + L.off[L_XN]);
 
-  // 2. permutation and work lists
+  // 2. permutation, work lists and the expert-ordered copy of x
   int* blk_hist = reinterpret_cast<int*>(ws + L.off[L_BLKHIST]);
   int* blk_off = reinterpret_cast<int*>(ws + L.off[L_BLKOFF]);
   int* counts = reinterpret_cast<int*>(ws + L.off[L_COUNTS]);
   int* offs = reinterpret_cast<int*>(ws + L.off[L_OFFS]);
   int* row_tok = reinterpret_cast<int*>(ws + L.off[L_ROWTOK]);
   float* row_w = reinterpret_cast<float*>(ws + L.off[L_ROWW]);
+  int* pair_row = reinterpret_cast<int*>(ws + L.off[L_PAIRROW]);
   __nv_bfloat16* xperm = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_XPERM]);
   __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_ACT]);
+  float* y = reinterpret_cast<float*>(ws + L.off[L_Y]);
   int4* ugu = reinterpret_cast<int4*>(ws + L.off[L_UGU]);
   int4* udn = reinterpret_cast<int4*>(ws + L.off[L_UDN]);
   int* nunits = reinterpret_cast<int*>(ws + L.off[L_NUNITS]);
@@ -412,65 +446,94 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   {
     ProfScope ps("expert_scan_units", st);
     beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs,
-                                                      ugu, udn, nunits, L.NT, I / 128, H / 128);
+                                                      ugu, udn, nunits, L.NT, I / 128,
+                                                      path_mt_down(L.path, H));
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
-  const size_t scatter_smem = static_cast<size_t>(2) * beam::PERM_TPB * K * sizeof(int);
   {
     ProfScope ps("expert_scatter", st);
-    beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, scatter_smem, st>>>(
-        idx, wts, T, K, E, blk_off, x, H, row_tok, row_w, xperm);
+    beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(idx, wts, T, K, E, blk_off,
+                                                                     pair_row, row_tok, row_w);
   }
   BEAM_LAUNCH_CHECK("expert_scatter_kernel");
+  {
+    ProfScope ps("gather_rows", st);
+    beam::gather_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+        x, row_tok, static_cast<int>(R), H, xperm);
+  }
+  BEAM_LAUNCH_CHECK("gather_rows_kernel");
 
-  // 3. gate/up GEMM + SwiGLU, 4. down GEMM + weighted combine
+  // 3. gate/up GEMM + SwiGLU -> act, 4. down GEMM -> per-pair y
+  const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
   CUtensorMap m_g, m_u, m_d, m_x, m_a;
   if ((s = make_map(&m_g, w_gate, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
   if ((s = make_map(&m_u, w_up, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
   if ((s = make_map(&m_d, w_down, static_cast<uint64_t>(E) * H, I, 128)) != BEAM_OK) return s;
-  if ((s = make_map(&m_x, xperm, R, H, 16)) != BEAM_OK) return s;
-  if ((s = make_map(&m_a, act, R, I, 16)) != BEAM_OK) return s;
+  if ((s = make_map(&m_x, xperm, R, H, tok_box)) != BEAM_OK) return s;
+  if ((s = make_map(&m_a, act, R, I, tok_box)) != BEAM_OK) return s;
 
-  beam::GemmArgs ga{};
-  ga.units = ugu;
-  ga.n_units = nunits + 0;
-  ga.k_blocks = H / 64;
-  ga.a_rows_per_expert = I;
-  ga.act_out = act;
-  ga.act_ld = I;
-  ga.timeout_ns = kWaitTimeoutNs;
-  beam::GemmArgs gd{};
-  gd.units = udn;
-  gd.n_units = nunits + 1;
-  gd.k_blocks = I / 64;
-  gd.a_rows_per_expert = H;
-  gd.row_token = row_tok;
-  gd.row_weight = row_w;
-  gd.acc = acc;
-  gd.acc_ld = H;
-  gd.timeout_ns = kWaitTimeoutNs;
-  if (L.NT == 32) {
-    if ((s = launch_gemm<0, 32, 6>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
-    if ((s = launch_gemm<1, 32, 10>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+  if (L.path == PATH_TM) {
+    beam::TmArgs ta{};
+    ta.units = ugu;
+    ta.n_units = nunits + 0;
+    ta.k_blocks = H / 64;
+    ta.w_rows_per_expert = I;
+    ta.out = act;
+    ta.out_ld = I;
+    ta.timeout_ns = kWaitTimeoutNs;
+    beam::TmArgs td = ta;
+    td.units = udn;
+    td.n_units = nunits + 1;
+    td.k_blocks = I / 64;
+    td.w_rows_per_expert = H;
+    td.out = nullptr;
+    td.y = y;
+    td.out_ld = H;
+    if ((s = launch_gemm_tm<0>(m_g, m_u, m_x, ta, st)) != BEAM_OK) return s;
+    if ((s = launch_gemm_tm<1>(m_d, m_d, m_a, td, st)) != BEAM_OK) return s;
   } else {
-    if ((s = launch_gemm<0, 128, 4>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
-    if ((s = launch_gemm<1, 128, 6>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+    beam::GemmArgs ga{};
+    ga.units = ugu;
+    ga.n_units = nunits + 0;
+    ga.k_blocks = H / 64;
+    ga.a_rows_per_expert = I;
+    ga.out = act;
+    ga.out_ld = I;
+    ga.timeout_ns = kWaitTimeoutNs;
+    beam::GemmArgs gd = ga;
+    gd.units = udn;
+    gd.n_units = nunits + 1;
+    gd.k_blocks = I / 64;
+    gd.a_rows_per_expert = H;
+    gd.out = nullptr;
+    gd.y = y;
+    gd.out_ld = H;
+    if (L.path == PATH_W32) {
+      if ((s = launch_gemm<0, 32, 6>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+      if ((s = launch_gemm<1, 32, 10>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+    } else {
+      if ((s = launch_gemm<0, 128, 4>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+      if ((s = launch_gemm<1, 128, 6>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+    }
   }
 
-  // 5. post-norm + scaled residual, or the BF16 output
-  if (!direct_fp32) {
-    const int resid = p->residual_k >= 2;
-    const float k = static_cast<float>(resid ? p->residual_k : 2);
-    const float a = resid ? std::sqrt((k - 1.f) / k) : 0.f;
-    const float b = resid ? 1.f / std::sqrt(k) : 1.f;
-    ProfScope ps("finalize_rows", st);
-    beam::finalize_rows_kernel<float><<<(T + 7) / 8, 256, 0, st>>>(
-        acc, static_cast<const __nv_bfloat16*>(x_in), post_gain,
-        static_cast<__nv_bfloat16*>(out), T, H, p->rms_eps, a, b, resid, 1);
-    BEAM_LAUNCH_CHECK("finalize_rows_kernel");
+  // 5. weighted combine, then post-norm + scaled residual (or the output)
+  const int resid = p->residual_k >= 2;
+  const float kf = static_cast<float>(resid ? p->residual_k : 2);
+  const float a = resid ? std::sqrt((kf - 1.f) / kf) : 0.f;
+  const float b = resid ? 1.f / std::sqrt(kf) : 1.f;
+  {
+    ProfScope ps("combine_rows", st);
+    if (p->flags & BEAM_FLAG_FP32_OUT)
+      beam::combine_rows_kernel<true><<<T, beam::COMBINE_THREADS, 0, st>>>(
+          y, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
+          p->rms_eps, a, b, resid);
+    else
+      beam::combine_rows_kernel<false><<<T, beam::COMBINE_THREADS, 0, st>>>(
+          y, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
+          p->rms_eps, a, b, resid);
   }
-  (void)counts;
-  (void)offs;
+  BEAM_LAUNCH_CHECK("combine_rows_kernel");
   return BEAM_OK;
 }
 

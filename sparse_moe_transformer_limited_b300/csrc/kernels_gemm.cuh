@@ -15,7 +15,8 @@
 //            epilogue: act[t, m*128+i] = bf16(silu(D_g) * D_u)   (FP32 math)
 //   down     (MODE 1): unit = (expert e, 128 hidden rows m, token tile)
 //            D[h,t] = sum_i Wd[e, m*128+h, i] * act[t, i]
-//            epilogue: acc[token(t), m*128+h] += weight(t) * D[h,t]  (FP32 red)
+//            epilogue: y[t, m*128+h] = D[h,t] (FP32), the per-pair expert output
+//            (the row kernel combines the pairs of a token with its weights)
 //
 // Warp roles (192 threads, persistent, one CTA per SM):
 //   warp 0      TMA producer (one elected lane): fills a STAGES-deep smem ring
@@ -44,12 +45,9 @@ struct GemmArgs {
   const int* n_units;         // device count of units
   int k_blocks;               // K / 64
   int a_rows_per_expert;      // I (gate/up) or H (down)
-  __nv_bfloat16* act_out;     // MODE 0: [R, act_ld]
-  int act_ld;
-  const int* row_token;       // MODE 1
-  const float* row_weight;    // MODE 1
-  float* acc;                 // MODE 1: [T, acc_ld] FP32
-  int acc_ld;
+  __nv_bfloat16* out;         // MODE 0: act [R, I] bf16
+  float* y;                   // MODE 1: y [R, H] fp32
+  int out_ld;
   unsigned long long timeout_ns;
 };
 
@@ -257,7 +255,7 @@ __global__ void __launch_bounds__(192, 1)
             const int tok = c * 16 + j;
             if (tok < un.z) {
               const float a = g[j] / (1.0f + expf(-g[j])) * v[j];
-              args.act_out[static_cast<size_t>(un.y + tok) * args.act_ld + col] =
+              args.out[static_cast<size_t>(un.y + tok) * args.out_ld + col] =
                   __float2bfloat16_rn(a);
             }
           }
@@ -267,12 +265,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
-            if (tok < un.z) {
-              const int r = un.y + tok;
-              const int t = args.row_token[r];
-              const float wgt = args.row_weight[r];
-              atomicAdd(args.acc + static_cast<size_t>(t) * args.acc_ld + col, wgt * d[j]);
-            }
+            if (tok < un.z) args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = d[j];
           }
         }
       }

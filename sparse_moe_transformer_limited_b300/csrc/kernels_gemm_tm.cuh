@@ -1,0 +1,279 @@
+// Token-major grouped expert GEMMs for many tokens per expert (prefill),
+// on tcgen05 + TMEM, with TMA multicast of the weight tiles inside a
+// two-CTA cluster.
+//
+// The layer's experts ("Reflection 发布 Beam 501B 开源模型，支持 1M tokens 上下文",
+// section 专家混合模型): SwiGLU MLPs, hidden 5120, intermediate 2560, the
+// SwiGLU product in FP32 (section 残差流).
+//
+// A unit is (expert e, weight tile n, group of up to 256 consecutive rows of
+// the expert-ordered token layout). The two CTAs of a cluster take 128 rows
+// each (the MMA's M = 128) and share one 256-row weight tile (the MMA's
+// N = 256): CTA r loads half r of the weight tile and multicasts it into both
+// CTAs' shared memory, so each weight byte leaves L2 once per 256 tokens.
+//   gate/up (MODE 0): tile n = intermediate rows [128n, 128n+128) of W_g
+//            (half 0, TMEM columns 0..127) and of W_u (half 1, columns
+//            128..255); epilogue act[row, 128n + i] = bf16(silu(g_i) * u_i)
+//            with g_i and u_i read by the same thread (FP32 math).
+//   down    (MODE 1): tile n = hidden rows [256n, 256n+256) of W_d;
+//            epilogue y[row, 256n + j] = D[row, j] (FP32) -- the per-pair
+//            expert output, combined per token by the row kernel.
+//
+// Warp roles as in the weight-major kernel: warp 0 TMA producer, warp 1 TMEM
+// owner and MMA issuer, warps 2..5 epilogue (TMEM lane quarter = warp % 4).
+// A shared-memory stage may be refilled only when the MMAs of BOTH CTAs have
+// consumed it (the peer's multicast writes into this CTA's stage too), so each
+// MMA commit arrives on the `empty` barrier of both CTAs (count 2). All waits
+// are bounded; the CTAs of a cluster meet at a cluster barrier before TMEM is
+// freed and before exit, so no CTA leaves while its peer may still write
+// into it.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "kernels_gemm.cuh"
+#include "ptx.cuh"
+
+namespace beam {
+
+struct TmArgs {
+  const int4* units;        // {expert, first row, rows (<= 256), weight tile}
+  const int* n_units;
+  int k_blocks;             // K / 64
+  int w_rows_per_expert;    // I (gate/up) or H (down)
+  __nv_bfloat16* out;       // MODE 0: act [R, I] bf16
+  float* y;                 // MODE 1: y [R, H] fp32
+  int out_ld;
+  unsigned long long timeout_ns;
+};
+
+struct TmCfg {
+  static constexpr int BM = 128;                 // token rows per CTA
+  static constexpr int BN = 256;                 // weight rows per unit
+  static constexpr int STAGES = 4;
+  static constexpr int A_BYTES = BM * 128;       // 16 KB
+  static constexpr int B_BYTES = BN * 128;       // 32 KB
+  static constexpr int HALF_B = B_BYTES / 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = BN;
+  static constexpr int NBUF = 2;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int BAR_BYTES = (2 * STAGES + 2 * NBUF + 1) * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    expert_gemm_tm_kernel(const __grid_constant__ CUtensorMap tm_w0,
+                          const __grid_constant__ CUtensorMap tm_w1,
+                          const __grid_constant__ CUtensorMap tm_tok, const TmArgs args) {
+  using C = TmCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + C::NBUF;
+  uint64_t* mma_done = tempty + C::NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 2);
+    }
+    for (int b = 0; b < C::NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tm_w0);
+    if (MODE == 0) tma_prefetch_desc(&tm_w1);
+    tma_prefetch_desc(&tm_tok);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_units = *args.n_units;
+  const uint64_t tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      const CUtensorMap* wmap = (MODE == 0 && crank == 1) ? &tm_w1 : &tm_w0;
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = cid; ok && u < n_units; u += ncl) {
+        const int4 un = args.units[u];
+        const int tok_row = un.y + static_cast<int>(crank) * C::BM;
+        const int wrow = (MODE == 0) ? un.x * args.w_rows_per_expert + un.w * 128
+                                     : un.x * args.w_rows_per_expert + un.w * 256 +
+                                           static_cast<int>(crank) * 128;
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            ok = false;
+            break;
+          }
+          uint8_t* sb = smem + stage * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(sb, &tm_tok, &full[stage], kb * 64, tok_row, pol_x);
+          tma_load_2d_mc(sb + C::A_BYTES + static_cast<int>(crank) * C::HALF_B, wmap,
+                         &full[stage], kb * 64, wrow, static_cast<uint16_t>(0x3), pol_w);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      const int pending = issued < C::STAGES ? issued : C::STAGES;
+      for (int i = 0; i < pending; ++i) {
+        if (stage == 0) {
+          stage = C::STAGES - 1;
+          phase ^= 1u;
+        } else {
+          --stage;
+        }
+        const volatile int never = 0;
+        if (!mbar_wait_bounded(&full[stage], phase, tmo, &never)) gemm_fail(abort_flag);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, C::BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = cid; ok && u < n_units; u += ncl, ++it) {
+        const int buf = it & 1;
+        const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!mbar_wait_bounded(&tempty[buf], tpar ^ 1u, tmo, abort_flag)) {
+          gemm_fail(abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint64_t da = sdesc_k128(sa);
+          const uint64_t db = sdesc_k128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          mma_commit_mc(&empty[stage], static_cast<uint16_t>(0x3));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[buf]);
+      }
+      mma_commit(mma_done);
+      const volatile int never = 0;
+      if (!mbar_wait_bounded(mma_done, 0, tmo, &never)) gemm_fail(abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int rloc = q * 32 + lane;
+    int it = 0;
+    for (int u = cid; u < n_units; u += ncl, ++it) {
+      const int4 un = args.units[u];
+      const int buf = it & 1;
+      const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
+      bool ready = false;
+      if (lane == 0) ready = mbar_wait_bounded(&tfull[buf], tpar, tmo, abort_flag);
+      ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+      if (!ready) {
+        if (lane == 0) gemm_fail(abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      const int nv = un.z - static_cast<int>(crank) * C::BM;
+      const bool valid = rloc < nv;
+      const size_t row = static_cast<size_t>(un.y) + crank * C::BM + rloc;
+      if (MODE == 0) {
+        __nv_bfloat16* dst = args.out + row * args.out_ld + un.w * 128;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          float g[16], v[16];
+          tmem_ld16x2(tb + c * 16, tb + 128 + c * 16, g, v);
+          if (valid) {
+            uint4 pk[2];
+            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float a0 = g[2 * j] / (1.0f + expf(-g[2 * j])) * v[2 * j];
+              const float a1 = g[2 * j + 1] / (1.0f + expf(-g[2 * j + 1])) * v[2 * j + 1];
+              p2[j] = __floats2bfloat162_rn(a0, a1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
+            d4[0] = pk[0];
+            d4[1] = pk[1];
+          }
+        }
+      } else {
+        float* dst = args.y + row * args.out_ld + un.w * 256;
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          float d[16];
+          tmem_ld16(tb + c * 16, d);
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              d4[j] = make_float4(d[4 * j], d[4 * j + 1], d[4 * j + 2], d[4 * j + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // the peer no longer writes into this CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace beam

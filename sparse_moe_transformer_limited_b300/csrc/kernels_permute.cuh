@@ -1,6 +1,7 @@
 // Token -> expert permutation: per-block expert histograms, one scan that also
-// builds the expert-GEMM work lists, and a scatter that writes the
-// expert-ordered copy of x. The pages only say that each token runs 8 of the
+// builds the expert-GEMM work lists, a scatter that assigns every
+// token-expert pair its row, and a gather that writes the expert-ordered copy
+// of x. The pages only say that each token runs 8 of the
 // 256 experts ("Reflection 发布 Beam 501B 开源模型…", section 专家混合模型); grouping
 // the token-expert pairs by expert is what lets each expert's weights stream
 // once per token tile.
@@ -29,70 +30,85 @@ __global__ void __launch_bounds__(PERM_THREADS) expert_block_hist_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[blockIdx.x * E + e] = hist[e];
 }
 
+// Exclusive prefix sum over the 256 threads of a block; *total receives the
+// sum of all values. s_warp holds 8 ints of scratch.
+__device__ __forceinline__ int block_exclusive_scan256(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < 8 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < 8) s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int base = warp > 0 ? s_warp[warp - 1] : 0;
+  *total = s_warp[7];
+  __syncthreads();
+  return base + x - v;
+}
+
 // One block of 256 threads (thread = expert, E <= 256).
 //  counts[e], offsets[e] (exclusive scan, offsets[E] = T*top_k),
 //  blk_off[b][e] = first row of block b's pairs of expert e,
 //  work lists for the two expert GEMMs. A unit is int4 {expert, first row,
-//  rows (<= NT), weight row-tile}. Experts are ordered by token count
+//  rows (<= NT), weight tile}. Experts are ordered by token count
 //  (descending, ties to the lower index); inside an expert, units run
-//  row-tile-major so the token tiles sharing one weight tile are adjacent.
+//  weight-tile-major so the token tiles sharing one weight tile are adjacent.
 __global__ void __launch_bounds__(256) expert_scan_units_kernel(
     const int* __restrict__ blk_hist, int NB, int E, int* __restrict__ blk_off,
     int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ units_gu,
     int4* __restrict__ units_dn, int* __restrict__ n_units, int NT, int MT_gu, int MT_dn) {
   __shared__ int s_cnt[256];
-  __shared__ int s_off[257];
   __shared__ int s_order[256];
-  __shared__ int s_tbase[257];
+  __shared__ int s_warp[8];
   const int e = threadIdx.x;
   int c = 0;
   if (e < E)
     for (int b = 0; b < NB; ++b) c += blk_hist[b * E + e];
   s_cnt[e] = (e < E) ? c : 0;
-  __syncthreads();
-  if (e == 0) {
-    int run = 0;
-    for (int i = 0; i < E; ++i) {
-      s_off[i] = run;
-      run += s_cnt[i];
-    }
-    s_off[E] = run;
-  }
-  __syncthreads();
+  int total = 0;
+  const int off = block_exclusive_scan256(e < E ? c : 0, s_warp, &total);
   if (e < E) {
-    counts[e] = s_cnt[e];
-    offsets[e] = s_off[e];
-    if (e == 0) offsets[E] = s_off[E];
-    int run = s_off[e];
+    counts[e] = c;
+    offsets[e] = off;
+    if (e == 0) offsets[E] = total;
+    int run = off;
     for (int b = 0; b < NB; ++b) {
       blk_off[b * E + e] = run;
       run += blk_hist[b * E + e];
     }
     int rank = 0;
-    const int me = s_cnt[e];
-    for (int j = 0; j < E; ++j) rank += (s_cnt[j] > me) || (s_cnt[j] == me && j < e);
+    for (int j = 0; j < E; ++j) rank += (s_cnt[j] > c) || (s_cnt[j] == c && j < e);
     s_order[rank] = e;
   }
   __syncthreads();
+  // position p in the order holds expert ex; its token tiles start at tbase
+  const int ex = e < E ? s_order[e] : 0;
+  const int n = e < E ? s_cnt[ex] : 0;
+  const int nt = (n + NT - 1) / NT;
+  int ntiles = 0;
+  const int tb = block_exclusive_scan256(nt, s_warp, &ntiles);
   if (e == 0) {
-    int run = 0;
-    for (int p = 0; p < E; ++p) {
-      s_tbase[p] = run;
-      run += (s_cnt[s_order[p]] + NT - 1) / NT;
-    }
-    s_tbase[E] = run;
-    n_units[0] = run * MT_gu;
-    n_units[1] = run * MT_dn;
-    n_units[2] = run;
+    n_units[0] = ntiles * MT_gu;
+    n_units[1] = ntiles * MT_dn;
+    n_units[2] = ntiles;
     n_units[3] = 0;
   }
-  __syncthreads();
-  if (e < E) {
-    const int ex = s_order[e];
-    const int n = s_cnt[ex];
-    const int nt = (n + NT - 1) / NT;
-    const int tb = s_tbase[e];
-    const int r0 = s_off[ex];
+  if (e < E && nt > 0) {
+    // offsets of expert ex: recompute from the counts (exclusive scan value of ex)
+    int r0 = 0;
+    for (int j = 0; j < ex; ++j) r0 += s_cnt[j];
     for (int m = 0; m < MT_gu; ++m)
       for (int j = 0; j < nt; ++j)
         units_gu[static_cast<size_t>(tb) * MT_gu + m * nt + j] =
@@ -104,16 +120,13 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
   }
 }
 
-// Rows of this block's pairs, row_token / row_weight, and the expert-ordered
-// copy of x (one warp copies one row with 16-byte loads and stores).
+// Row of every pair of this block in the expert-ordered layout: pair_row[p],
+// and the inverse maps row_token / row_weight.
 __global__ void __launch_bounds__(PERM_THREADS) expert_scatter_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ wts, int T, int top_k, int E,
-    const int* __restrict__ blk_off, const __nv_bfloat16* __restrict__ x, int H,
-    int* __restrict__ row_token, float* __restrict__ row_weight,
-    __nv_bfloat16* __restrict__ xperm) {
-  extern __shared__ int sm[];
-  int* s_e = sm;
-  int* s_row = sm + PERM_TPB * top_k;
+    const int* __restrict__ blk_off, int* __restrict__ pair_row, int* __restrict__ row_token,
+    float* __restrict__ row_weight) {
+  __shared__ int s_e[PERM_TPB * 32];
   const int p0 = blockIdx.x * PERM_TPB * top_k;
   const int np = min(PERM_TPB * top_k, T * top_k - p0);
   for (int p = threadIdx.x; p < np; p += blockDim.x) s_e[p] = idx[p0 + p];
@@ -123,20 +136,25 @@ __global__ void __launch_bounds__(PERM_THREADS) expert_scatter_kernel(
     int r = 0;
     for (int q = 0; q < p; ++q) r += (s_e[q] == e);
     const int row = blk_off[blockIdx.x * E + e] + r;
-    s_row[p] = row;
+    pair_row[p0 + p] = row;
     row_token[row] = (p0 + p) / top_k;
     row_weight[row] = wts[p0 + p];
   }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = blockDim.x >> 5;
+}
+
+// xperm[row, :] = x[row_token[row], :], one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const int* __restrict__ row_token,
+                                                          int R, int H,
+                                                          __nv_bfloat16* __restrict__ xperm) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  const int t = row_token[row];
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+  uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<size_t>(row) * H);
   const int nc = H >> 3;
-  for (int p = warp; p < np; p += nw) {
-    const int t = (p0 + p) / top_k;
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
-    uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<size_t>(s_row[p]) * H);
-    for (int c = lane; c < nc; c += 32) dst[c] = src[c];
-  }
+  for (int c = lane; c < nc; c += 32) dst[c] = src[c];
 }
 
 }  // namespace beam

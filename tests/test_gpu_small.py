@@ -213,15 +213,62 @@ def test_forward_empty_batch(B):
     assert B.status() == 0
 
 
-def test_forward_run_to_run(B):
-    """Routing is bit-identical across runs; outputs differ at most in the
-    last bits (FP32 atomic combine order)."""
-    wl = S.WORKLOADS["tiny"]
-    d = S.make_inputs(wl, "cuda")
+@pytest.mark.parametrize("T,E,n_group", [(64, 256, 8), (1100, 32, 1)])
+def test_forward_run_to_run(B, T, E, n_group):
+    """Routing and outputs are bit-identical across runs (no atomics), on the
+    weight-major and the token-major GEMM paths."""
+    wl, d = S.make_custom(T=T, H=256, E=E, I=128, n_group=n_group, topk_group=min(4, n_group),
+                          top_k=8, seed=77, device="cuda")
     o1, i1, w1, *_ = _run_forward(B, wl, d, B.FLAG_FP32_OUT)
     o2, i2, w2, *_ = _run_forward(B, wl, d, B.FLAG_FP32_OUT)
     assert torch.equal(i1, i2) and torch.equal(w1, w2)
-    assert rel_err(host(o1), host(o2)) < 1e-5
+    assert torch.equal(o1, o2)
+
+
+# Token-major two-CTA path (many tokens per expert): E small enough that the
+# mean tokens per expert exceeds 24. Covers one and several 256-row groups
+# per expert, the second CTA of a cluster with no rows, several weight tiles
+# in both GEMMs and K loops longer than the shared-memory ring.
+@pytest.mark.parametrize("T,H,I,E,n_group,topk_group,top_k", [
+    (300, 256, 128, 32, 1, 1, 8),
+    (1100, 512, 256, 32, 1, 1, 8),
+    (700, 256, 256, 64, 2, 2, 6),
+    (1537, 768, 128, 64, 2, 2, 8),
+])
+def test_forward_token_major_path(B, T, H, I, E, n_group, topk_group, top_k):
+    wl, d = S.make_custom(T=T, H=H, E=E, I=I, n_group=n_group, topk_group=topk_group,
+                          top_k=top_k, seed=T + E, device="cuda")
+    _full_layer_check(B, wl, d)
+
+
+def test_forward_token_major_hot_group(B):
+    """1000 tokens all routed to experts 0..7 (four 256-row groups each, the
+    last one ragged) and 248 empty experts, on the token-major path."""
+    wl, d = S.make_custom(T=1000, H=256, E=256, I=128, n_group=8, topk_group=4, top_k=8,
+                          seed=5, device="cuda", router_mode="hot_group")
+    _full_layer_check(B, wl, d)
+
+
+def test_forward_token_major_residual(B):
+    """Token-major path with pre-norm, post-norm and the residual at k=9."""
+    wl = S.Workload("tm_resid", T=900, H=512, E=32, I=128, n_group=1, topk_group=1, seed=6,
+                    wr_std=0.05, pre_norm=True, residual_k=9)
+    d = S.make_inputs(wl, "cuda")
+    p = _params(B, wl, B.FLAG_PRE_NORM, 9)
+    idx = torch.empty((wl.T, 8), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, 8), dtype=torch.float32, device="cuda")
+    hk = B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
+                   topk_idx=idx, topk_w=w)
+    assert B.status() == 0
+    h = host(d["x"]).astype(np.float64)
+    amb = prenorm_ambiguous(h, None, wl.rms_eps)
+    xo = O.bf16_round(O.rms_norm(h, None, wl.rms_eps)).astype(np.float64)
+    clean = np.nonzero(~amb.any(axis=1))[0]
+    sel = O.route(xo[clean], host(d["w_router"]), None, 1, 1, 8, 2.5)
+    _, chosen = compare_routing(sel, idx.cpu().numpy()[clean], w.cpu().numpy()[clean], wl)
+    o = oracle_outputs(xo[clean], chosen, np.arange(len(clean)), expert_getter(d))
+    want = O.residual_step(h[clean], o, 9, None, wl.rms_eps, True)
+    assert rel_err(host(hk)[clean], want) <= OUT_REL_TOL
 
 
 # ---------------------------------------------------------------- residual

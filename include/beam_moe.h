@@ -96,7 +96,9 @@ size_t beam_moe_workspace_size(const beam_moe_params* p);
  *   topk_w     [T,top_k] fp32 out: routed_scale * s / (sum of the selected s)
  *   scores     [T,E] fp32 out (sigmoid scores) when BEAM_FLAG_RETURN_SCORES,
  *              else ignored (may be NULL)
- * Scores are FP32: logits accumulate x (bf16 -> fp32) times w_router in FP32.
+ * Scores are FP32: logits accumulate x (bf16 -> fp32) times w_router in FP32
+ * (for T >= 512 and E % 128 == 0 on the tensor cores, with w_router split
+ * exactly into three BF16 pieces so every product is exact in FP32).
  * Group score = FP32 sum of the group's two largest scores; groups rank by
  * it (ties to the lower group index). */
 beam_status_t beam_moe_route(const beam_moe_params* p, const void* x,
@@ -170,10 +172,12 @@ const char* beam_last_error_string(void);
  * same K-slicing, so the results are identical), without the workspace.
  * Scratch needed: KS*T*E*4 bytes (rounded up to 256) for the partial logits,
  * where KS is the number of K-slices the router uses for this T (many for a
- * few tokens, one for thousands), plus T*H*2 bytes with BEAM_FLAG_PRE_NORM.
- * A call needing more returns BEAM_ERR_UNSUPPORTED with a message that gives
- * the bytes needed; nothing is enqueued then. For the Beam shapes (H=5120,
- * E=256, 148 SMs) that allows T <= 409 with pre-norm and T <= 8192 without.
+ * few tokens, one for thousands), plus T*H*2 bytes with BEAM_FLAG_PRE_NORM,
+ * plus E*3H*2 bytes for the split router weight when the router runs on the
+ * tensor cores (T >= 512). A call needing more returns BEAM_ERR_UNSUPPORTED
+ * with a message that gives the bytes needed; nothing is enqueued then. For
+ * the Beam shapes (H=5120, E=256, 148 SMs) that allows T <= 409 with
+ * pre-norm and T <= 512 without.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
@@ -197,8 +201,10 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
  * [T*top_k,H] bf16, 9 SwiGLU activations [T*top_k,I] bf16, 10 per-pair
  * expert outputs [T*top_k,H] fp32, 11 unit counts [4] int32, 12 per-block
  * expert histograms, 13 per-block expert offsets, 14 gate/up work list,
- * 15 down work list, 16 pair -> row map [T*top_k] int32. Writes min(n, 17)
- * entries and returns how many it wrote (0 on invalid parameters). */
+ * 15 down work list, 16 pair -> row map [T*top_k] int32, 17 the router
+ * weight split into three BF16 pieces [E, 3H] (tensor-core router only).
+ * Writes min(n, 18) entries and returns how many it wrote (0 on invalid
+ * parameters). */
 int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n);
 
 /* Launches one block whose single thread waits on a shared-memory barrier

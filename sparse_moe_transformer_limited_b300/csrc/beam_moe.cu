@@ -116,9 +116,15 @@ GemmPath choose_path(const beam_moe_params& p) {
 int path_nt(GemmPath g) { return g == PATH_W32 ? 32 : (g == PATH_W128 ? 128 : 256); }
 int path_mt_down(GemmPath g, int H) { return g == PATH_TM ? H / 256 : H / 128; }
 
+// Router logits path: the tensor cores (exact three-way BF16 split of the
+// FP32 weight, FP32 accumulation) once there are enough tokens to fill the
+// GPU, else the FP32 SIMT kernel with K-slices.
+bool router_on_tensor_cores(const beam_moe_params& p) { return p.T >= 512 && p.E % 128 == 0; }
+
 // K-slices of the router logits GEMM: enough blocks to cover the SMs when T
 // is small. Must divide H / 32 and leave at least 64 columns per slice.
 int choose_router_ks(const beam_moe_params& p, int num_sms) {
+  if (router_on_tensor_cores(p)) return 1;
   const int tiles = ((p.T + beam::RL_BT - 1) / beam::RL_BT) * ((p.E + beam::RL_BE - 1) / beam::RL_BE);
   const int want = (2 * num_sms + tiles - 1) / tiles;
   const int nk = p.H / 32;
@@ -128,7 +134,7 @@ int choose_router_ks(const beam_moe_params& p, int num_sms) {
   return best;
 }
 
-constexpr int kLayoutEntries = 17;
+constexpr int kLayoutEntries = 18;
 
 struct Layout {
   size_t off[kLayoutEntries];
@@ -140,7 +146,7 @@ struct Layout {
 
 enum {
   L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_Y,
-  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW
+  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW, L_WR3
 };
 
 int sm_count() {
@@ -200,8 +206,16 @@ Layout make_layout(const beam_moe_params& p) {
   L.NT = path_nt(L.path);
   const long long R = static_cast<long long>(p.T) * p.top_k;
   const long long tiles = (R + L.NT - 1) / L.NT + p.E;
-  L.units_gu_max = tiles * (p.I / 128);
-  L.units_dn_max = tiles * path_mt_down(L.path, p.H);
+  if (L.path == PATH_TM) {
+    // cluster units (two int4 each): at most MT per 256-row group plus MT/2+1
+    // tail units per expert
+    const long long groups = (R + 255) / 256 + p.E;
+    L.units_gu_max = 2 * (groups * (p.I / 128) + static_cast<long long>(p.E) * (p.I / 256 + 1));
+    L.units_dn_max = 2 * (groups * (p.H / 256) + static_cast<long long>(p.E) * (p.H / 512 + 1));
+  } else {
+    L.units_gu_max = tiles * (p.I / 128);
+    L.units_dn_max = tiles * path_mt_down(L.path, p.H);
+  }
   size_t sz[kLayoutEntries];
   sz[L_XN] = (p.flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p.T) * p.H * 2 : 0;
   sz[L_PART] = static_cast<size_t>(L.KS) * p.T * p.E * 4;
@@ -220,6 +234,7 @@ Layout make_layout(const beam_moe_params& p) {
   sz[L_UGU] = static_cast<size_t>(L.units_gu_max) * 16;
   sz[L_UDN] = static_cast<size_t>(L.units_dn_max) * 16;
   sz[L_PAIRROW] = static_cast<size_t>(R) * 4;
+  sz[L_WR3] = router_on_tensor_cores(p) ? static_cast<size_t>(p.E) * 3 * p.H * 2 : 0;
   size_t cur = 0;
   for (int i = 0; i < kLayoutEntries; ++i) {
     L.off[i] = cur;
@@ -284,9 +299,12 @@ beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CU
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
     attr_set = true;
   }
-  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
+  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu"
+                         : (MODE == 1 ? "expert_gemm_down" : "router_logits_tc"),
+               st);
   kern<<<sm_count(), 192, C::SMEM_BYTES, st>>>(a0, a1, b, args);
-  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>" : "expert_gemm_kernel<down>");
+  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>"
+                              : (MODE == 1 ? "expert_gemm_kernel<down>" : "expert_gemm_kernel<router>"));
   return BEAM_OK;
 }
 
@@ -321,12 +339,38 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
     x = xn;
   }
   float* part = reinterpret_cast<float*>(ws + L.off[L_PART]);
-  dim3 g1((p.T + beam::RL_BT - 1) / beam::RL_BT, (p.E + beam::RL_BE - 1) / beam::RL_BE, L.KS);
-  {
-    ProfScope ps("router_logits", st);
-    beam::router_logits_kernel<<<g1, 256, 0, st>>>(x, w_router, part, p.T, p.H, p.E, p.H / L.KS);
+  if (router_on_tensor_cores(p)) {
+    // logits [T, E] = [x, x, x] . [W1 | W2 | W3]^T on the tensor cores
+    __nv_bfloat16* w3 = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_WR3]);
+    {
+      ProfScope ps("router_split", st);
+      beam::router_split_kernel<<<2 * sm_count(), 256, 0, st>>>(w_router, p.E, p.H, w3);
+    }
+    BEAM_LAUNCH_CHECK("router_split_kernel");
+    CUtensorMap m_w, m_x;
+    beam_status_t s;
+    if ((s = make_map(&m_w, w3, static_cast<uint64_t>(p.E), static_cast<uint64_t>(3) * p.H,
+                      128)) != BEAM_OK)
+      return s;
+    if ((s = make_map(&m_x, x, static_cast<uint64_t>(p.T), p.H, 16)) != BEAM_OK) return s;
+    beam::GemmArgs ga{};
+    ga.k_blocks = 3 * p.H / 64;
+    ga.b_k_wrap = p.H / 64;
+    ga.rows_total = p.T;
+    ga.m_tiles = p.E / 128;
+    ga.y = part;
+    ga.out_ld = p.E;
+    ga.timeout_ns = kWaitTimeoutNs;
+    if ((s = launch_gemm<2, 128, 6>(m_w, m_w, m_x, ga, st)) != BEAM_OK) return s;
+  } else {
+    dim3 g1((p.T + beam::RL_BT - 1) / beam::RL_BT, (p.E + beam::RL_BE - 1) / beam::RL_BE, L.KS);
+    {
+      ProfScope ps("router_logits", st);
+      beam::router_logits_kernel<<<g1, 256, 0, st>>>(x, w_router, part, p.T, p.H, p.E,
+                                                     p.H / L.KS);
+    }
+    BEAM_LAUNCH_CHECK("router_logits_kernel");
   }
-  BEAM_LAUNCH_CHECK("router_logits_kernel");
   const int nb = (p.T + 7) / 8;
   ProfScope ps("router_select", st);
 #define BEAM_SEL(NI)                                                                          \
@@ -445,9 +489,14 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   BEAM_LAUNCH_CHECK("expert_block_hist_kernel");
   {
     ProfScope ps("expert_scan_units", st);
-    beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs,
-                                                      ugu, udn, nunits, L.NT, I / 128,
-                                                      path_mt_down(L.path, H));
+    if (L.path == PATH_TM)
+      beam::expert_scan_units_tm_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts,
+                                                           offs, ugu, udn, nunits, I / 128,
+                                                           H / 256);
+    else
+      beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs,
+                                                        ugu, udn, nunits, L.NT, I / 128,
+                                                        path_mt_down(L.path, H));
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
   {
@@ -693,16 +742,20 @@ extern "C" beam_status_t beam_moe_route_static(const beam_moe_params* p, const v
   Layout L{};
   L.KS = choose_router_ks(*p, sm_count());
   const size_t part = align_up(static_cast<size_t>(L.KS) * p->T * p->E * 4, 256);
-  const size_t xn = (p->flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p->T) * p->H * 2 : 0;
-  if (part + xn > BEAM_ROUTE_STATIC_SCRATCH_BYTES)
+  const size_t xn = align_up(
+      (p->flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p->T) * p->H * 2 : 0, 256);
+  const size_t wr3 =
+      router_on_tensor_cores(*p) ? static_cast<size_t>(p->E) * 3 * p->H * 2 : 0;
+  if (part + xn + wr3 > BEAM_ROUTE_STATIC_SCRATCH_BYTES)
     return fail(BEAM_ERR_UNSUPPORTED,
                 "T=%d needs %zu bytes of router scratch; the static scratch holds %zu bytes "
                 "(use beam_moe_route with a workspace for this size)",
-                p->T, part + xn, static_cast<size_t>(BEAM_ROUTE_STATIC_SCRATCH_BYTES));
+                p->T, part + xn + wr3, static_cast<size_t>(BEAM_ROUTE_STATIC_SCRATCH_BYTES));
   void* base = nullptr;
   if ((s = route_static_scratch(&base)) != BEAM_OK) return s;
   L.off[L_PART] = 0;
   L.off[L_XN] = part;
+  L.off[L_WR3] = part + xn;
   return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
                        (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr, nullptr,
                        static_cast<uint8_t*>(base), static_cast<cudaStream_t>(stream));

@@ -6,11 +6,14 @@
 // section 专家混合模型): SwiGLU MLPs, hidden 5120, intermediate 2560, the
 // SwiGLU product in FP32 (section 残差流).
 //
-// A unit is (expert e, weight tile n, group of up to 256 consecutive rows of
-// the expert-ordered token layout). The two CTAs of a cluster take 128 rows
-// each (the MMA's M = 128) and share one 256-row weight tile (the MMA's
-// N = 256): CTA r loads half r of the weight tile and multicasts it into both
-// CTAs' shared memory, so each weight byte leaves L2 once per 256 tokens.
+// A cluster unit is two sub-units, one per CTA, each (expert e, weight tile
+// n, up to 128 consecutive rows of the expert-ordered token layout = the
+// MMA's M). The weight tile has 256 rows (the MMA's N). In a PAIR unit both
+// CTAs work on the same tile (rows [0,128) and [128,256) of a 256-row group):
+// CTA r loads half r of the weight tile and multicasts it into both CTAs'
+// shared memory, so each weight byte leaves L2 once per 256 tokens. In a SOLO
+// unit (an expert's last <= 128 rows) each CTA works on its own tile and
+// loads both halves itself.
 //   gate/up (MODE 0): tile n = intermediate rows [128n, 128n+128) of W_g
 //            (half 0, TMEM columns 0..127) and of W_u (half 1, columns
 //            128..255); epilogue act[row, 128n + i] = bf16(silu(g_i) * u_i)
@@ -33,12 +36,13 @@
 #include <cstdint>
 
 #include "kernels_gemm.cuh"
+#include "kernels_permute.cuh"
 #include "ptx.cuh"
 
 namespace beam {
 
 struct TmArgs {
-  const int4* units;        // {expert, first row, rows (<= 256), weight tile}
+  const int4* units;        // 2 per cluster unit: {expert, first row, rows, tile | TM_PAIR}
   const int* n_units;
   int k_blocks;             // K / 64
   int w_rows_per_expert;    // I (gate/up) or H (down)
@@ -120,17 +124,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
-      const CUtensorMap* wmap = (MODE == 0 && crank == 1) ? &tm_w1 : &tm_w0;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
       for (int u = cid; ok && u < n_units; u += ncl) {
-        const int4 un = args.units[u];
-        const int tok_row = un.y + static_cast<int>(crank) * C::BM;
-        const int wrow = (MODE == 0) ? un.x * args.w_rows_per_expert + un.w * 128
-                                     : un.x * args.w_rows_per_expert + un.w * 256 +
-                                           static_cast<int>(crank) * 128;
+        const int4 un = args.units[2 * u + crank];
+        const bool pair = (un.w & TM_PAIR) != 0;
+        const int nt = un.w & 0xFFFF;
+        // weight rows of half 0 and half 1 of the 256-row tile
+        const int wr0 = (MODE == 0) ? un.x * args.w_rows_per_expert + nt * 128
+                                    : un.x * args.w_rows_per_expert + nt * 256;
+        const int wr1 = (MODE == 0) ? wr0 : wr0 + 128;
+        const CUtensorMap* wm1 = (MODE == 0) ? &tm_w1 : &tm_w0;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
             gemm_fail(abort_flag);
@@ -139,9 +145,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           }
           uint8_t* sb = smem + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sb, &tm_tok, &full[stage], kb * 64, tok_row, pol_x);
-          tma_load_2d_mc(sb + C::A_BYTES + static_cast<int>(crank) * C::HALF_B, wmap,
-                         &full[stage], kb * 64, wrow, static_cast<uint16_t>(0x3), pol_w);
+          tma_load_2d(sb, &tm_tok, &full[stage], kb * 64, un.y, pol_x);
+          if (pair) {
+            if (crank == 0)
+              tma_load_2d_mc(sb + C::A_BYTES, &tm_w0, &full[stage], kb * 64, wr0,
+                             static_cast<uint16_t>(0x3), pol_w);
+            else
+              tma_load_2d_mc(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kb * 64, wr1,
+                             static_cast<uint16_t>(0x3), pol_w);
+          } else {
+            tma_load_2d(sb + C::A_BYTES, &tm_w0, &full[stage], kb * 64, wr0, pol_w);
+            tma_load_2d(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kb * 64, wr1, pol_w);
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -212,7 +227,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const int rloc = q * 32 + lane;
     int it = 0;
     for (int u = cid; u < n_units; u += ncl, ++it) {
-      const int4 un = args.units[u];
+      const int4 un = args.units[2 * u + crank];
+      const int nt = un.w & 0xFFFF;
       const int buf = it & 1;
       const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
       bool ready = false;
@@ -225,11 +241,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS) +
                           (static_cast<uint32_t>(q * 32) << 16);
-      const int nv = un.z - static_cast<int>(crank) * C::BM;
-      const bool valid = rloc < nv;
-      const size_t row = static_cast<size_t>(un.y) + crank * C::BM + rloc;
+      const bool valid = rloc < un.z;
+      const size_t row = static_cast<size_t>(un.y) + rloc;
       if (MODE == 0) {
-        __nv_bfloat16* dst = args.out + row * args.out_ld + un.w * 128;
+        __nv_bfloat16* dst = args.out + row * args.out_ld + nt * 128;
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           float g[16], v[16];
@@ -239,8 +254,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float a0 = g[2 * j] / (1.0f + expf(-g[2 * j])) * v[2 * j];
-              const float a1 = g[2 * j + 1] / (1.0f + expf(-g[2 * j + 1])) * v[2 * j + 1];
+              const float a0 = __fdividef(g[2 * j], 1.0f + __expf(-g[2 * j])) * v[2 * j];
+              const float a1 =
+                  __fdividef(g[2 * j + 1], 1.0f + __expf(-g[2 * j + 1])) * v[2 * j + 1];
               p2[j] = __floats2bfloat162_rn(a0, a1);
             }
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
@@ -249,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           }
         }
       } else {
-        float* dst = args.y + row * args.out_ld + un.w * 256;
+        float* dst = args.y + row * args.out_ld + nt * 256;
 #pragma unroll 1
         for (int c = 0; c < 16; ++c) {
           float d[16];

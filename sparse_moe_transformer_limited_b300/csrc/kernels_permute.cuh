@@ -120,6 +120,93 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
   }
 }
 
+// Work lists of the token-major two-CTA GEMMs. A cluster unit is two int4
+// sub-units, one per CTA: {expert, first row, rows (<= 128), weight tile |
+// TM_PAIR}. An expert's rows go in 256-row groups, each a PAIR unit (both
+// CTAs on the same weight tile, 128 rows each, the tile multicast); a last
+// remainder of at most 128 rows becomes SOLO sub-units -- one per weight
+// tile, two tiles per cluster unit, each CTA loading its own weights -- so a
+// tail costs one 128-row MMA tile instead of a 256-row group. Units of one
+// expert are contiguous, tiles in ascending order; experts by token count,
+// descending. A sub-unit with 0 rows repeats a valid tile and stores nothing.
+constexpr int TM_PAIR = 0x40000000;
+
+__device__ __forceinline__ int tm_units_for(int n, int MT) {
+  const int q = n >> 8, rem = n & 255;
+  const int pairs = q + (rem > 128 ? 1 : 0);
+  const int tail = (rem > 0 && rem <= 128) ? 1 : 0;
+  return MT * pairs + tail * ((MT + 1) >> 1);
+}
+
+__device__ void tm_write_units(int4* units, int base, int ex, int r0, int n, int MT) {
+  const int q = n >> 8, rem = n & 255;
+  const int pairs = q + (rem > 128 ? 1 : 0);
+  const int tail = (rem > 0 && rem <= 128) ? rem : 0;
+  int u = base;
+  for (int m = 0; m < MT; m += 2) {
+    for (int mm = m; mm < min(m + 2, MT); ++mm)
+      for (int g = 0; g < pairs; ++g) {
+        const int gr = r0 + 256 * g, gn = n - 256 * g;
+        units[2 * u] = make_int4(ex, gr, min(128, gn), mm | TM_PAIR);
+        units[2 * u + 1] = make_int4(ex, gr + 128, max(0, min(128, gn - 128)), mm | TM_PAIR);
+        ++u;
+      }
+    if (tail) {
+      const int tr = r0 + 256 * q;
+      units[2 * u] = make_int4(ex, tr, tail, m);
+      units[2 * u + 1] = (m + 1 < MT) ? make_int4(ex, tr, tail, m + 1) : make_int4(ex, tr, 0, m);
+      ++u;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) expert_scan_units_tm_kernel(
+    const int* __restrict__ blk_hist, int NB, int E, int* __restrict__ blk_off,
+    int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ units_gu,
+    int4* __restrict__ units_dn, int* __restrict__ n_units, int MT_gu, int MT_dn) {
+  __shared__ int s_cnt[256];
+  __shared__ int s_order[256];
+  __shared__ int s_warp[8];
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E)
+    for (int b = 0; b < NB; ++b) c += blk_hist[b * E + e];
+  s_cnt[e] = (e < E) ? c : 0;
+  int total = 0;
+  const int off = block_exclusive_scan256(e < E ? c : 0, s_warp, &total);
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = off;
+    if (e == 0) offsets[E] = total;
+    int run = off;
+    for (int b = 0; b < NB; ++b) {
+      blk_off[b * E + e] = run;
+      run += blk_hist[b * E + e];
+    }
+    int rank = 0;
+    for (int j = 0; j < E; ++j) rank += (s_cnt[j] > c) || (s_cnt[j] == c && j < e);
+    s_order[rank] = e;
+  }
+  __syncthreads();
+  const int ex = e < E ? s_order[e] : 0;
+  const int n = e < E ? s_cnt[ex] : 0;
+  int r0 = 0;
+  for (int j = 0; j < ex; ++j) r0 += s_cnt[j];
+  int tot_gu = 0, tot_dn = 0;
+  const int b_gu = block_exclusive_scan256(n > 0 ? tm_units_for(n, MT_gu) : 0, s_warp, &tot_gu);
+  const int b_dn = block_exclusive_scan256(n > 0 ? tm_units_for(n, MT_dn) : 0, s_warp, &tot_dn);
+  if (e == 0) {
+    n_units[0] = tot_gu;
+    n_units[1] = tot_dn;
+    n_units[2] = 0;
+    n_units[3] = 0;
+  }
+  if (e < E && n > 0) {
+    tm_write_units(units_gu, b_gu, ex, r0, n, MT_gu);
+    tm_write_units(units_dn, b_dn, ex, r0, n, MT_dn);
+  }
+}
+
 // Row of every pair of this block in the expert-ordered layout: pair_row[p],
 // and the inverse maps row_token / row_weight.
 __global__ void __launch_bounds__(PERM_THREADS) expert_scatter_kernel(

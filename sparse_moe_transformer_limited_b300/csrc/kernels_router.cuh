@@ -104,6 +104,32 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
 }
 
 // ---------------------------------------------------------------------------
+// Exact three-way BF16 split of the FP32 router weight for the tensor-core
+// logits GEMM: w = w1 + w2 + w3 with w1 = bf16(w), w2 = bf16(w - w1),
+// w3 = bf16(w - w1 - w2) (each difference is exact in FP32). Output
+// [E, 3H]: columns [0,H) hold w1, [H,2H) w2, [2H,3H) w3.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ w, int E,
+                                                           int H,
+                                                           __nv_bfloat16* __restrict__ w3cat) {
+  const size_t n = static_cast<size_t>(E) * H;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t e = i / H, j = i - e * H;
+    const float v = w[i];
+    const __nv_bfloat16 a = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(a);
+    const __nv_bfloat16 b = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(b);
+    const __nv_bfloat16 c = __float2bfloat16_rn(r2);
+    __nv_bfloat16* row = w3cat + e * 3 * H;
+    row[j] = a;
+    row[H + j] = b;
+    row[2 * H + j] = c;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // selection: one warp per token. Lane l holds experts e = 32*i + l for
 // i < NI = E/32, so with groups of 32 experts group g is register column g and
 // a group's top-2 is two warp max-reductions.
@@ -126,10 +152,22 @@ __global__ void __launch_bounds__(256) router_select_kernel(
 
   float s[NI];
 #pragma unroll
+  for (int i = 0; i < NI; ++i) s[i] = 0.f;
+  // K-slice partial sums, in slice order; the loads of all NI columns of a
+  // slice are independent, which hides their latency
+#pragma unroll 4
+  for (int k = 0; k < KS; ++k) {
+    const float* pk = part + (static_cast<size_t>(k) * T + t) * E + lane;
+    float v[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) v[i] = pk[i * 32];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) s[i] += v[i];
+  }
+#pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = i * 32 + lane;
-    float l = 0.f;
-    for (int k = 0; k < KS; ++k) l += part[(static_cast<size_t>(k) * T + t) * E + e];
+    float l = s[i];
     if (bias != nullptr) l += bias[e];
     s[i] = 1.0f / (1.0f + expf(-l));
     if (scores_out != nullptr) scores_out[static_cast<size_t>(t) * E + e] = s[i];

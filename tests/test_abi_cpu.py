@@ -47,7 +47,7 @@ def test_workspace_size_and_layout():
     lay = B.workspace_layout(p)
     assert list(lay) == list(B._native.LAYOUT_NAMES)
     offs = list(lay.values())
-    assert offs == sorted(offs) and offs[-1] < n
+    assert offs == sorted(offs) and offs[-1] <= n
     assert all(o % 1024 == 0 for o in offs)
     # the permuted copy of x and the SwiGLU buffer are sized for T*top_k rows
     assert lay["act"] - lay["xperm"] >= 64 * 8 * 5120 * 2

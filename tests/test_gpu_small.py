@@ -75,6 +75,21 @@ def test_route_tiny_bitexact(B):
     assert np.allclose(w.cpu().numpy().sum(1), 2.5, atol=1e-5)
 
 
+@pytest.mark.parametrize("T,H,mode", [(512, 256, "random"), (700, 384, "random"),
+                                      (1031, 256, "dup_rows")])
+def test_route_tensor_core_path(B, T, H, mode):
+    """T >= 512 with E = 256: logits on the tensor cores with the exact
+    three-way BF16 split of the FP32 router weight."""
+    wl, d = S.make_custom(T=T, H=H, E=256, I=128, n_group=8, topk_group=4, top_k=8,
+                          seed=T, device="cuda", router_mode=mode)
+    p = _params(B, wl, B.FLAG_RETURN_SCORES)
+    idx, w, sc = B.route(p, d["x"], d["w_router"], bias=d["bias"])
+    assert B.status() == 0
+    x, sel = _oracle_sel(wl, d)
+    assert np.max(np.abs(host(sc) - sel["s64"])) < 2e-6
+    compare_routing(sel, idx.cpu().numpy(), w.cpu().numpy(), wl)
+
+
 def test_route_deterministic(B):
     wl = S.WORKLOADS["tiny"].replace(T=300, seed=5)
     d = S.make_inputs(wl, "cuda")

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -16,6 +17,7 @@
 #include "beam_moe.h"
 #include "kernels_gemm.cuh"
 #include "kernels_gemm_tm.cuh"
+#include "kernels_gemm_2sm.cuh"
 #include "kernels_permute.cuh"
 #include "kernels_router.cuh"
 #include "kernels_rows.cuh"
@@ -102,19 +104,30 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Expert-GEMM path, chosen from the mean tokens per expert:
 //  few tokens per expert (decode): weights as the M=128 operand, token tiles
 //    of 32 (expert_gemm_kernel);
-//  many tokens (prefill): token-major two-CTA clusters sharing 256-row weight
-//    tiles, 256-row token groups (expert_gemm_tm_kernel; needs H % 256 == 0);
-//    otherwise weights as M with token tiles of 128.
-enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2 };
+//  many tokens (prefill, H % 256 == 0): PATH_MIXED -- gate/up on the
+//    token-major two-CTA multicast kernel (expert_gemm_tm_kernel, whose
+//    token-major epilogue writes the SwiGLU output in 32-byte vectors), down
+//    on the 2-SM pair kernel (expert_gemm_pair_kernel); PATH_TM and
+//    PATH_PAIR run both GEMMs on one kernel (BEAM_PREFILL_GEMM=tm|pair);
+//  otherwise weights as M with token tiles of 128.
+enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2, PATH_PAIR = 3, PATH_MIXED = 4 };
 
 GemmPath choose_path(const beam_moe_params& p) {
   const long long pairs = static_cast<long long>(p.T) * p.top_k;
   if (pairs <= 24LL * p.E) return PATH_W32;
-  return (p.H % 256 == 0) ? PATH_TM : PATH_W128;
+  if (p.H % 256 == 0) {
+    const char* v = std::getenv("BEAM_PREFILL_GEMM");
+    if (v != nullptr && std::strcmp(v, "tm") == 0) return PATH_TM;
+    if (v != nullptr && std::strcmp(v, "pair") == 0) return PATH_PAIR;
+    return PATH_MIXED;
+  }
+  return PATH_W128;
 }
 
 int path_nt(GemmPath g) { return g == PATH_W32 ? 32 : (g == PATH_W128 ? 128 : 256); }
-int path_mt_down(GemmPath g, int H) { return g == PATH_TM ? H / 256 : H / 128; }
+int path_mt_down(GemmPath g, int H) {
+  return (g == PATH_TM || g == PATH_PAIR || g == PATH_MIXED) ? H / 256 : H / 128;
+}
 
 // Router logits path: the tensor cores (exact three-way BF16 split of the
 // FP32 weight, FP32 accumulation) once there are enough tokens to fill the
@@ -206,7 +219,14 @@ Layout make_layout(const beam_moe_params& p) {
   L.NT = path_nt(L.path);
   const long long R = static_cast<long long>(p.T) * p.top_k;
   const long long tiles = (R + L.NT - 1) / L.NT + p.E;
-  if (L.path == PATH_TM) {
+  if (L.path == PATH_PAIR || L.path == PATH_MIXED) {
+    const long long groups = (R + 255) / 256 + p.E;
+    // (the mixed path's gate/up list holds tm cluster units: two int4 each)
+    L.units_gu_max = L.path == PATH_MIXED
+                         ? 2 * (groups * (p.I / 128) + static_cast<long long>(p.E) * (p.I / 256 + 1))
+                         : groups * (p.I / 128);
+    L.units_dn_max = groups * (p.H / 256);
+  } else if (L.path == PATH_TM) {
     // cluster units (two int4 each): at most MT per 256-row group plus MT/2+1
     // tail units per expert
     const long long groups = (R + 255) / 256 + p.E;
@@ -305,6 +325,25 @@ beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   kern<<<sm_count(), 192, C::SMEM_BYTES, st>>>(a0, a1, b, args);
   BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>"
                               : (MODE == 1 ? "expert_gemm_kernel<down>" : "expert_gemm_kernel<router>"));
+  return BEAM_OK;
+}
+
+template <int MODE>
+beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& tok,
+                               const CUtensorMap& tok64, const beam::PairArgs& args,
+                               cudaStream_t st) {
+  using C = beam::PairCfg;
+  auto kern = beam::expert_gemm_pair_kernel<MODE>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    BEAM_CUDA_TRY(
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
+    attr_set = true;
+  }
+  const int grid = (sm_count() / 2) * 2;
+  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(a0, a1, tok, tok64, args);
+  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_pair_kernel<gate/up>" : "expert_gemm_pair_kernel<down>");
   return BEAM_OK;
 }
 
@@ -489,10 +528,18 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   BEAM_LAUNCH_CHECK("expert_block_hist_kernel");
   {
     ProfScope ps("expert_scan_units", st);
-    if (L.path == PATH_TM)
-      beam::expert_scan_units_tm_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts,
-                                                           offs, ugu, udn, nunits, I / 128,
-                                                           H / 256);
+    if (L.path == PATH_PAIR)
+      beam::expert_scan_units_prefill_kernel<beam::LIST_PAIR, beam::LIST_PAIR>
+          <<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
+                              H / 256);
+    else if (L.path == PATH_MIXED)
+      beam::expert_scan_units_prefill_kernel<beam::LIST_TM, beam::LIST_PAIR>
+          <<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
+                              H / 256);
+    else if (L.path == PATH_TM)
+      beam::expert_scan_units_prefill_kernel<beam::LIST_TM, beam::LIST_TM>
+          <<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
+                              H / 256);
     else
       beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs,
                                                         ugu, udn, nunits, L.NT, I / 128,
@@ -514,14 +561,54 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
 
   // 3. gate/up GEMM + SwiGLU -> act, 4. down GEMM -> per-pair y
   const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
+  const uint32_t gu_box = L.path == PATH_PAIR ? 64 : 128;
   CUtensorMap m_g, m_u, m_d, m_x, m_a;
-  if ((s = make_map(&m_g, w_gate, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
-  if ((s = make_map(&m_u, w_up, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
+  if ((s = make_map(&m_g, w_gate, static_cast<uint64_t>(E) * I, H, gu_box)) != BEAM_OK) return s;
+  if ((s = make_map(&m_u, w_up, static_cast<uint64_t>(E) * I, H, gu_box)) != BEAM_OK) return s;
   if ((s = make_map(&m_d, w_down, static_cast<uint64_t>(E) * H, I, 128)) != BEAM_OK) return s;
   if ((s = make_map(&m_x, xperm, R, H, tok_box)) != BEAM_OK) return s;
   if ((s = make_map(&m_a, act, R, I, tok_box)) != BEAM_OK) return s;
 
-  if (L.path == PATH_TM) {
+  if (L.path == PATH_PAIR || L.path == PATH_MIXED) {
+    beam::PairArgs pa{};
+    pa.units = ugu;
+    pa.n_units = nunits + 0;
+    pa.k_blocks = H / 64;
+    pa.w_rows_per_expert = I;
+    pa.act = act;
+    pa.out_ld = I;
+    pa.timeout_ns = kWaitTimeoutNs;
+    beam::PairArgs pd = pa;
+    pd.units = udn;
+    pd.n_units = nunits + 1;
+    pd.k_blocks = I / 64;
+    pd.w_rows_per_expert = H;
+    pd.act = nullptr;
+    pd.y = y;
+    pd.out_ld = H;
+    CUtensorMap m_x64, m_a64;
+    if ((s = make_map(&m_x64, xperm, R, H, 64)) != BEAM_OK) return s;
+    if ((s = make_map(&m_a64, act, R, I, 64)) != BEAM_OK) return s;
+    if (L.path == PATH_MIXED) {
+      // gate/up on the token-major multicast kernel (128-row boxes)
+      CUtensorMap m_g128, m_u128, m_x128;
+      if ((s = make_map(&m_g128, w_gate, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
+      if ((s = make_map(&m_u128, w_up, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
+      if ((s = make_map(&m_x128, xperm, R, H, 128)) != BEAM_OK) return s;
+      beam::TmArgs ta{};
+      ta.units = ugu;
+      ta.n_units = nunits + 0;
+      ta.k_blocks = H / 64;
+      ta.w_rows_per_expert = I;
+      ta.out = act;
+      ta.out_ld = I;
+      ta.timeout_ns = kWaitTimeoutNs;
+      if ((s = launch_gemm_tm<0>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK) return s;
+    } else {
+      if ((s = launch_gemm_pair<0>(m_g, m_u, m_x, m_x64, pa, st)) != BEAM_OK) return s;
+    }
+    if ((s = launch_gemm_pair<1>(m_d, m_d, m_a, m_a64, pd, st)) != BEAM_OK) return s;
+  } else if (L.path == PATH_TM) {
     beam::TmArgs ta{};
     ta.units = ugu;
     ta.n_units = nunits + 0;

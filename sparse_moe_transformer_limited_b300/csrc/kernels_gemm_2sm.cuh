@@ -1,0 +1,339 @@
+// Pair (2-SM) grouped expert GEMMs for prefill: tcgen05.mma.cta_group::2 on a
+// two-CTA cluster, weights as the MMA's M = 256 operand (128 rows in each
+// CTA), the tokens of one expert as N (32..256, N/2 rows in each CTA).
+//
+// The layer's experts ("Reflection 发布 Beam 501B 开源模型，支持 1M tokens 上下文",
+// section 专家混合模型): SwiGLU MLPs, hidden 5120, intermediate 2560, the
+// SwiGLU product in FP32 (section 残差流).
+//
+// Each CTA holds only its half of both operands, so one K-block is 32 KB of
+// shared memory per CTA (six stages fit) and each SM's shared memory serves
+// half of the MMA's operand reads. A unit is (expert e, weight tile m, a
+// group of at most 256 tokens of e); an expert's tokens are split into
+// balanced groups and N is the group size rounded up to 32, so a ragged group
+// costs MMA time in proportion to its tokens.
+//   gate/up (MODE 0): tile m = intermediate rows i0 = 128m .. +127. CTA r
+//            holds W_g rows i0+64r .. +63 (A rows 0..63) and W_u rows
+//            i0+64r .. +63 (A rows 64..127); TMEM lanes 0..63 = gate,
+//            64..127 = up. The warps holding up values pass them through
+//            shared memory to the warps holding the gate values of the same
+//            rows, which write act[t, i] = bf16(silu(g) * u) (FP32 math).
+//   down    (MODE 1): tile m = hidden rows h0 = 256m .. +255, CTA r holds
+//            rows h0+128r .. +127; y[t, h] = D (FP32), the per-pair expert
+//            output, combined per token by the row kernel.
+//
+// Roles per CTA (192 threads): warp 0 TMA producer; warp 1 TMEM allocation
+// (both CTAs) and, in the even CTA only, the MMA issuer; warps 2..5 epilogue.
+// Both CTAs' TMA loads count their bytes on the even CTA's `full` barrier;
+// the MMA commits arrive on the `empty` and `tmem_full` barriers of both
+// CTAs; both CTAs' epilogues release an accumulator on the even CTA's
+// `tmem_empty` barrier (count 8). All waits are bounded; the CTAs meet at a
+// cluster barrier before TMEM is freed and before exit.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "kernels_gemm.cuh"
+#include "ptx.cuh"
+
+namespace beam {
+
+struct PairArgs {
+  const int4* units;        // {expert, first row, tokens (<= 256), weight tile}
+  const int* n_units;
+  int k_blocks;             // K / 64
+  int w_rows_per_expert;    // I (gate/up) or H (down)
+  __nv_bfloat16* act;       // MODE 0: [R, I]
+  float* y;                 // MODE 1: [R, H]
+  int out_ld;
+  unsigned long long timeout_ns;
+};
+
+struct PairCfg {
+  static constexpr int STAGES = 6;
+  static constexpr int A_BYTES = 128 * 128;      // this CTA's 128 weight rows x 64
+  static constexpr int B_BYTES = 128 * 128;      // up to 128 token rows x 64
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = 256;           // N <= 256
+  static constexpr int NBUF = 2;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int XCHG_BYTES = 2 * 2 * 32 * 16 * 4;  // 2 warp pairs x 2 buffers
+  static constexpr int BAR_BYTES = (2 * STAGES + 2 * NBUF + 1) * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCHG_BYTES + BAR_BYTES;
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also ANDs a predicate over its participants.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                            const __grid_constant__ CUtensorMap tm_a1,
+                            const __grid_constant__ CUtensorMap tm_tok,
+                            const __grid_constant__ CUtensorMap tm_tok64, const PairArgs args) {
+  using C = PairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* xchg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::XCHG_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + C::NBUF;
+  uint64_t* mma_done = tempty + C::NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < C::NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tm_a0);
+    if (MODE == 0) tma_prefetch_desc(&tm_a1);
+    tma_prefetch_desc(&tm_tok);
+    tma_prefetch_desc(&tm_tok64);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers and TMEM of both CTAs ready
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_units = *args.n_units;
+  const uint64_t tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = cid; ok && u < n_units; u += ncl) {
+        const int4 un = args.units[u];
+        const int N = (un.z + 31) & ~31;
+        const int rows = N >> 1;             // token rows of this CTA (multiple of 16)
+        const int n64 = rows >> 6;           // 64-row boxes, then 16-row boxes
+        const int n16 = (rows & 63) >> 4;
+        const uint32_t cta_bytes = C::A_BYTES + rows * 128;
+        const int tok0 = un.y + static_cast<int>(crank) * (N >> 1);
+        const int wrow = (MODE == 0)
+                             ? un.x * args.w_rows_per_expert + un.w * 128 + static_cast<int>(crank) * 64
+                             : un.x * args.w_rows_per_expert + un.w * 256 + static_cast<int>(crank) * 128;
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            ok = false;
+            break;
+          }
+          uint8_t* sb = smem + stage * C::STAGE_BYTES;
+          const uint32_t fbar = mapa_shared(&full[stage], 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * cta_bytes);
+          if (MODE == 0) {
+            tma_load_2d_pair(sb, &tm_a0, fbar, kb * 64, wrow, pol_w);
+            tma_load_2d_pair(sb + C::A_BYTES / 2, &tm_a1, fbar, kb * 64, wrow, pol_w);
+          } else {
+            tma_load_2d_pair(sb, &tm_a0, fbar, kb * 64, wrow, pol_w);
+          }
+          for (int j = 0; j < n64; ++j)
+            tma_load_2d_pair(sb + C::A_BYTES + j * 8192, &tm_tok64, fbar, kb * 64, tok0 + j * 64,
+                             pol_x);
+          for (int j = 0; j < n16; ++j)
+            tma_load_2d_pair(sb + C::A_BYTES + n64 * 8192 + j * 2048, &tm_tok, fbar, kb * 64,
+                             tok0 + n64 * 64 + j * 16, pol_x);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // The leader drains its full barriers (both CTAs' bytes land there);
+      // the follower's loads complete on the leader's barriers, which the
+      // leader's drain and the final cluster barrier cover.
+      if (leader) {
+        const int pending = issued < C::STAGES ? issued : C::STAGES;
+        for (int i = 0; i < pending; ++i) {
+          if (stage == 0) {
+            stage = C::STAGES - 1;
+            phase ^= 1u;
+          } else {
+            --stage;
+          }
+          const volatile int never = 0;
+          if (!mbar_wait_bounded(&full[stage], phase, tmo, &never)) gemm_fail(abort_flag);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = cid; ok && u < n_units; u += ncl, ++it) {
+        const int4 un = args.units[u];
+        const int N = (un.z + 31) & ~31;
+        const uint32_t idesc = idesc_bf16_f32(256, N);
+        const int buf = it & 1;
+        const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!mbar_wait_bounded(&tempty[buf], tpar ^ 1u, tmo, abort_flag)) {
+          gemm_fail(abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint64_t da = sdesc_k128(sa);
+          const uint64_t db = sdesc_k128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss_pair(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          mma_commit_pair_mc(&empty[stage], static_cast<uint16_t>(0x3));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(&tfull[buf], static_cast<uint16_t>(0x3));
+      }
+      mma_commit_pair_mc(mma_done, static_cast<uint16_t>(0x1));
+      const volatile int never = 0;
+      if (!mbar_wait_bounded(mma_done, 0, tmo, &never)) gemm_fail(abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter
+    int it = 0;
+    for (int u = cid; u < n_units; u += ncl, ++it) {
+      const int4 un = args.units[u];
+      const int buf = it & 1;
+      const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
+      bool ready = false;
+      if (lane == 0) ready = mbar_wait_bounded(&tfull[buf], tpar, tmo, abort_flag);
+      ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+      // gate/up: the two warps that exchange values through shared memory
+      // leave together, so neither waits alone at their named barrier
+      if (MODE == 0) ready = named_bar_and(1 + (q & 1), 64, ready);
+      if (!ready) {
+        if (lane == 0) gemm_fail(abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      const int nch = (un.z + 15) >> 4;
+      if (MODE == 0) {
+        // lanes 0..63 (q 0,1) gate, 64..127 (q 2,3) up of intermediate rows
+        // i = i0 + 64*crank + 32*(q & 1) + lane. Per chunk of 16 tokens the
+        // gate warp hands g of tokens 8..15 to its up partner and receives u
+        // of tokens 0..7, so each of the two computes and stores 8 tokens.
+        const int pairid = q & 1;
+        const bool is_gate = q < 2;
+        const int i = un.w * 128 + static_cast<int>(crank) * 64 + pairid * 32 + lane;
+        float* xb = xchg + pairid * (2 * 32 * 16);
+        const int tbase = is_gate ? 0 : 8;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          float v[16];
+          tmem_ld16(tb + c * 16, v);
+          // slot layout per lane: [0..7] u of tokens 0..7 (from up), [8..15] g of tokens 8..15
+          float* slot = xb + (c & 1) * (32 * 16) + lane * 16;
+          if (is_gate) {
+            *reinterpret_cast<float4*>(slot + 8) = make_float4(v[8], v[9], v[10], v[11]);
+            *reinterpret_cast<float4*>(slot + 12) = make_float4(v[12], v[13], v[14], v[15]);
+          } else {
+            *reinterpret_cast<float4*>(slot + 0) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(slot + 4) = make_float4(v[4], v[5], v[6], v[7]);
+          }
+          named_bar_sync(1 + pairid, 64);
+          const float4 o0 = *reinterpret_cast<const float4*>(slot + (is_gate ? 0 : 8));
+          const float4 o1 = *reinterpret_cast<const float4*>(slot + (is_gate ? 4 : 12));
+          const float other[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int tok = c * 16 + tbase + j;
+            if (tok < un.z) {
+              const float g = is_gate ? v[j] : other[j];
+              const float uu = is_gate ? other[j] : v[8 + j];
+              const float a = __fdividef(g, 1.0f + __expf(-g)) * uu;
+              args.act[static_cast<size_t>(un.y + tok) * args.out_ld + i] = __float2bfloat16_rn(a);
+            }
+          }
+        }
+      } else {
+        const int h = un.w * 256 + static_cast<int>(crank) * 128 + q * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          float d[16];
+          tmem_ld16(tb + c * 16, d);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c * 16 + j;
+            // per-pair outputs are read once, by the row kernel: stream them past L2
+            if (tok < un.z) __stcs(args.y + static_cast<size_t>(un.y + tok) * args.out_ld + h, d[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs done: no more loads, MMAs or arrivals into either
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace beam

@@ -274,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              d4[j] = make_float4(d[4 * j], d[4 * j + 1], d[4 * j + 2], d[4 * j + 3]);
+              __stcs(d4 + j, make_float4(d[4 * j], d[4 * j + 1], d[4 * j + 2], d[4 * j + 3]));
           }
         }
       }

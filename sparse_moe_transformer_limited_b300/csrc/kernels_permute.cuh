@@ -160,7 +160,45 @@ __device__ void tm_write_units(int4* units, int base, int ex, int r0, int n, int
   }
 }
 
-__global__ void __launch_bounds__(256) expert_scan_units_tm_kernel(
+// Work lists of the pair (2-SM) GEMMs: an expert's n tokens are split into
+// g = ceil(n / 256) balanced groups; a unit is {expert, first row, group
+// size, weight tile}. Units of one expert are contiguous, weight-tile-major
+// (the groups sharing a weight tile are adjacent); experts by token count,
+// descending.
+__device__ void pair_write_units(int4* units, int base, int ex, int r0, int n, int MT) {
+  const int g = (n + 255) >> 8;
+  const int q = n / g, extra = n - q * g;
+  int u = base;
+  for (int m = 0; m < MT; ++m) {
+    int start = 0;
+    for (int gi = 0; gi < g; ++gi) {
+      const int sz = q + (gi < extra ? 1 : 0);
+      units[u++] = make_int4(ex, r0 + start, sz, m);
+      start += sz;
+    }
+  }
+}
+
+// Work lists for prefill: each GEMM's list in the format of the kernel that
+// runs it (LIST_TM: two-CTA multicast cluster units; LIST_PAIR: 2-SM pair
+// units). Also writes counts, offsets and the per-block row offsets.
+constexpr int LIST_TM = 0;
+constexpr int LIST_PAIR = 1;
+
+template <int KIND>
+__device__ __forceinline__ int list_units_for(int n, int MT) {
+  return KIND == LIST_TM ? tm_units_for(n, MT) : ((n + 255) >> 8) * MT;
+}
+template <int KIND>
+__device__ __forceinline__ void list_write(int4* units, int base, int ex, int r0, int n, int MT) {
+  if (KIND == LIST_TM)
+    tm_write_units(units, base, ex, r0, n, MT);
+  else
+    pair_write_units(units, base, ex, r0, n, MT);
+}
+
+template <int GU_KIND, int DN_KIND>
+__global__ void __launch_bounds__(256) expert_scan_units_prefill_kernel(
     const int* __restrict__ blk_hist, int NB, int E, int* __restrict__ blk_off,
     int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ units_gu,
     int4* __restrict__ units_dn, int* __restrict__ n_units, int MT_gu, int MT_dn) {
@@ -193,8 +231,10 @@ __global__ void __launch_bounds__(256) expert_scan_units_tm_kernel(
   int r0 = 0;
   for (int j = 0; j < ex; ++j) r0 += s_cnt[j];
   int tot_gu = 0, tot_dn = 0;
-  const int b_gu = block_exclusive_scan256(n > 0 ? tm_units_for(n, MT_gu) : 0, s_warp, &tot_gu);
-  const int b_dn = block_exclusive_scan256(n > 0 ? tm_units_for(n, MT_dn) : 0, s_warp, &tot_dn);
+  const int b_gu = block_exclusive_scan256(n > 0 ? list_units_for<GU_KIND>(n, MT_gu) : 0, s_warp,
+                                           &tot_gu);
+  const int b_dn = block_exclusive_scan256(n > 0 ? list_units_for<DN_KIND>(n, MT_dn) : 0, s_warp,
+                                           &tot_dn);
   if (e == 0) {
     n_units[0] = tot_gu;
     n_units[1] = tot_dn;
@@ -202,8 +242,8 @@ __global__ void __launch_bounds__(256) expert_scan_units_tm_kernel(
     n_units[3] = 0;
   }
   if (e < E && n > 0) {
-    tm_write_units(units_gu, b_gu, ex, r0, n, MT_gu);
-    tm_write_units(units_dn, b_dn, ex, r0, n, MT_dn);
+    list_write<GU_KIND>(units_gu, b_gu, ex, r0, n, MT_gu);
+    list_write<DN_KIND>(units_dn, b_dn, ex, r0, n, MT_dn);
   }
 }
 

@@ -244,21 +244,33 @@ def test_forward_run_to_run(B, T, E, n_group):
 # mean tokens per expert exceeds 24. Covers one and several 256-row groups
 # per expert, the second CTA of a cluster with no rows, several weight tiles
 # in both GEMMs and K loops longer than the shared-memory ring.
+@pytest.fixture(params=["mixed", "pair", "tm"])
+def prefill_gemm(request, monkeypatch):
+    """The prefill GEMM kernels: by default gate/up on the two-CTA multicast
+    kernel and down on the 2-SM pair kernel; BEAM_PREFILL_GEMM=pair or tm runs
+    both GEMMs on one of them."""
+    if request.param == "mixed":
+        monkeypatch.delenv("BEAM_PREFILL_GEMM", raising=False)
+    else:
+        monkeypatch.setenv("BEAM_PREFILL_GEMM", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("T,H,I,E,n_group,topk_group,top_k", [
     (300, 256, 128, 32, 1, 1, 8),
     (1100, 512, 256, 32, 1, 1, 8),
     (700, 256, 256, 64, 2, 2, 6),
     (1537, 768, 128, 64, 2, 2, 8),
 ])
-def test_forward_token_major_path(B, T, H, I, E, n_group, topk_group, top_k):
+def test_forward_token_major_path(B, prefill_gemm, T, H, I, E, n_group, topk_group, top_k):
     wl, d = S.make_custom(T=T, H=H, E=E, I=I, n_group=n_group, topk_group=topk_group,
                           top_k=top_k, seed=T + E, device="cuda")
     _full_layer_check(B, wl, d)
 
 
-def test_forward_token_major_hot_group(B):
-    """1000 tokens all routed to experts 0..7 (four 256-row groups each, the
-    last one ragged) and 248 empty experts, on the token-major path."""
+def test_forward_token_major_hot_group(B, prefill_gemm):
+    """1000 tokens all routed to experts 0..7 (four groups of 250 each) and
+    248 empty experts, on the prefill GEMM paths."""
     wl, d = S.make_custom(T=1000, H=256, E=256, I=128, n_group=8, topk_group=4, top_k=8,
                           seed=5, device="cuda", router_mode="hot_group")
     _full_layer_check(B, wl, d)

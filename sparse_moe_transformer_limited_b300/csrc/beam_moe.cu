@@ -367,7 +367,7 @@ beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const
 
 beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const void* x_in,
                             const float* w_router, const float* bias, const float* pre_gain,
-                            int32_t* idx, float* w, float* scores, float* acc_zero,
+                            int32_t* idx, float* w, float* scores,
                             uint8_t* ws, cudaStream_t st) {
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
   if (p.flags & BEAM_FLAG_PRE_NORM) {
@@ -410,13 +410,14 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
     }
     BEAM_LAUNCH_CHECK("router_logits_kernel");
   }
-  const int nb = (p.T + 7) / 8;
+  const int tpb = p.T <= 512 ? 1 : beam::SEL_TOKENS;
+  const int nb = (p.T + tpb - 1) / tpb;
   ProfScope ps("router_select", st);
 #define BEAM_SEL(NI)                                                                          \
   case NI:                                                                                    \
     beam::router_select_kernel<NI><<<nb, 256, 0, st>>>(part, L.KS, bias, p.T, p.E, p.n_group, \
                                                       p.topk_group, p.top_k, p.routed_scale, \
-                                                      idx, w, scores, acc_zero, p.H);         \
+                                                      idx, w, scores, tpb);                   \
     break;
   switch (p.E / 32) {
     BEAM_SEL(1) BEAM_SEL(2) BEAM_SEL(3) BEAM_SEL(4) BEAM_SEL(5) BEAM_SEL(6) BEAM_SEL(7)
@@ -467,7 +468,7 @@ beam_status_t beam_moe_route(const beam_moe_params* p, const void* x, const floa
     return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
                 workspace_bytes, L.total);
   return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
-                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr, nullptr,
+                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr,
                        static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
@@ -500,8 +501,7 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   float* wts = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.off[L_W]);
 
   // 1. pre-norm (optional) + router
-  s = launch_router(*p, L, x_in, w_router, logit_bias, pre_gain, idx, wts, nullptr, nullptr, ws,
-                    st);
+  s = launch_router(*p, L, x_in, w_router, logit_bias, pre_gain, idx, wts, nullptr, ws, st);
   if (s != BEAM_OK) return s;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
   if (p->flags & BEAM_FLAG_PRE_NORM) x = reinterpret_cast<const __nv_bfloat16*>(ws + L.off[L_XN]);
@@ -542,7 +542,7 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
                               H / 256);
     else
       beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs,
-                                                        ugu, udn, nunits, L.NT, I / 128,
+                                                        ugu, nunits, L.NT, I / 128,
                                                         path_mt_down(L.path, H));
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
@@ -629,16 +629,17 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
     if ((s = launch_gemm_tm<1>(m_d, m_d, m_a, td, st)) != BEAM_OK) return s;
   } else {
     beam::GemmArgs ga{};
-    ga.units = ugu;
+    ga.units = ugu;  // token tiles, shared by both GEMMs
     ga.n_units = nunits + 0;
+    ga.m_tiles = I / 128;
     ga.k_blocks = H / 64;
     ga.a_rows_per_expert = I;
     ga.out = act;
     ga.out_ld = I;
     ga.timeout_ns = kWaitTimeoutNs;
     beam::GemmArgs gd = ga;
-    gd.units = udn;
     gd.n_units = nunits + 1;
+    gd.m_tiles = H / 128;
     gd.k_blocks = I / 64;
     gd.a_rows_per_expert = H;
     gd.out = nullptr;
@@ -844,6 +845,6 @@ extern "C" beam_status_t beam_moe_route_static(const beam_moe_params* p, const v
   L.off[L_XN] = part;
   L.off[L_WR3] = part + xn;
   return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
-                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr, nullptr,
+                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr,
                        static_cast<uint8_t*>(base), static_cast<cudaStream_t>(stream));
 }

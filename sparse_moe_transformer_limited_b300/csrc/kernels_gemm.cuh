@@ -48,7 +48,7 @@ __device__ int g_beam_err;  // per-device error word, read by beam_status()
 constexpr int DEV_ERR_TIMEOUT = 1;
 
 struct GemmArgs {
-  const int4* units;          // work list
+  const int4* units;          // token tiles {expert, first row, rows, 0} (MODE 0/1)
   const int* n_units;         // device count of units
   int k_blocks;               // K / 64
   int a_rows_per_expert;      // I (gate/up) or H (down)
@@ -57,20 +57,21 @@ struct GemmArgs {
   int out_ld;
   int b_k_wrap;               // k-blocks after which the B coordinate wraps (MODE 2: H/64)
   int rows_total;             // MODE 2: T (units are generated, not read)
-  int m_tiles;                // MODE 2: E / 128
+  int m_tiles;                // weight row-tiles per unit list (I/128, H/128, E/128)
   unsigned long long timeout_ns;
 };
 
-// Unit u of a GEMM: read from the work list, or (MODE 2, no list) generated:
-// m-tile u % m_tiles, token tile u / m_tiles.
+// Unit u of a GEMM: token tile u / m_tiles (from the tile list, or for the
+// router generated from T) and weight row-tile u % m_tiles.
 template <int MODE, int NT>
 __device__ __forceinline__ int4 gemm_unit(const GemmArgs& a, int u) {
+  const int m = u % a.m_tiles, j = u / a.m_tiles;
   if (MODE == 2) {
-    const int m = u % a.m_tiles, j = u / a.m_tiles;
     const int r0 = j * NT;
     return make_int4(0, r0, min(NT, a.rows_total - r0), m);
   }
-  return a.units[u];
+  const int4 t = a.units[j];
+  return make_int4(t.x, t.y, t.z, m);
 }
 
 __host__ __device__ constexpr int pow2_at_least(int v) {

@@ -61,15 +61,17 @@ __device__ __forceinline__ int block_exclusive_scan256(int v, int* s_warp, int* 
 // One block of 256 threads (thread = expert, E <= 256).
 //  counts[e], offsets[e] (exclusive scan, offsets[E] = T*top_k),
 //  blk_off[b][e] = first row of block b's pairs of expert e,
-//  work lists for the two expert GEMMs. A unit is int4 {expert, first row,
-//  rows (<= NT), weight tile}. Experts are ordered by token count
-//  (descending, ties to the lower index); inside an expert, units run
-//  weight-tile-major so the token tiles sharing one weight tile are adjacent.
+//  and the token-tile list of the weight-major GEMMs: tiles[k] = {expert,
+//  first row, rows (<= NT), 0}, experts ordered by token count (descending,
+//  ties to the lower index). The GEMMs expand unit u into tile u / MT and
+//  weight row-tile u % MT, so a few hundred tiles describe all units.
+//  n_units = {tiles * MT_gu, tiles * MT_dn, tiles, 0}.
 __global__ void __launch_bounds__(256) expert_scan_units_kernel(
     const int* __restrict__ blk_hist, int NB, int E, int* __restrict__ blk_off,
-    int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ units_gu,
-    int4* __restrict__ units_dn, int* __restrict__ n_units, int NT, int MT_gu, int MT_dn) {
+    int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ tiles,
+    int* __restrict__ n_units, int NT, int MT_gu, int MT_dn) {
   __shared__ int s_cnt[256];
+  __shared__ int s_off[256];
   __shared__ int s_order[256];
   __shared__ int s_warp[8];
   const int e = threadIdx.x;
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
   s_cnt[e] = (e < E) ? c : 0;
   int total = 0;
   const int off = block_exclusive_scan256(e < E ? c : 0, s_warp, &total);
+  s_off[e] = off;
   if (e < E) {
     counts[e] = c;
     offsets[e] = off;
@@ -93,7 +96,6 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
     s_order[rank] = e;
   }
   __syncthreads();
-  // position p in the order holds expert ex; its token tiles start at tbase
   const int ex = e < E ? s_order[e] : 0;
   const int n = e < E ? s_cnt[ex] : 0;
   const int nt = (n + NT - 1) / NT;
@@ -105,19 +107,8 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
     n_units[2] = ntiles;
     n_units[3] = 0;
   }
-  if (e < E && nt > 0) {
-    // offsets of expert ex: recompute from the counts (exclusive scan value of ex)
-    int r0 = 0;
-    for (int j = 0; j < ex; ++j) r0 += s_cnt[j];
-    for (int m = 0; m < MT_gu; ++m)
-      for (int j = 0; j < nt; ++j)
-        units_gu[static_cast<size_t>(tb) * MT_gu + m * nt + j] =
-            make_int4(ex, r0 + j * NT, min(NT, n - j * NT), m);
-    for (int m = 0; m < MT_dn; ++m)
-      for (int j = 0; j < nt; ++j)
-        units_dn[static_cast<size_t>(tb) * MT_dn + m * nt + j] =
-            make_int4(ex, r0 + j * NT, min(NT, n - j * NT), m);
-  }
+  const int r0 = s_off[ex];
+  for (int j = 0; j < nt; ++j) tiles[tb + j] = make_int4(ex, r0 + j * NT, min(NT, n - j * NT), 0);
 }
 
 // Work lists of the token-major two-CTA GEMMs. A cluster unit is two int4

@@ -140,38 +140,43 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// One block of 256 threads handles `tpb` (1..8) tokens: first all threads
+// sum the K-slice partial logits of the block's (token, expert) pairs
+// (coalesced over experts, slices summed in slice order) and apply bias and
+// sigmoid into shared memory; then warp w selects for token tpb*blockIdx + w.
+// Few tokens (many K-slices): one token per block, so the sums spread over
+// many SMs; many tokens: 8 per block.
+constexpr int SEL_TOKENS = 8;
+
 template <int NI>
 __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ part, int KS, const float* __restrict__ bias, int T, int E,
     int n_group, int topk_group, int top_k, float scale, int32_t* __restrict__ idx_out,
-    float* __restrict__ w_out, float* __restrict__ scores_out, float* __restrict__ acc_zero,
-    int H) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    float* __restrict__ w_out, float* __restrict__ scores_out, int tpb) {
+  __shared__ float s_sc[SEL_TOKENS][NI * 32];
+  const int t0 = blockIdx.x * tpb;
+  for (int q = threadIdx.x; q < tpb * E; q += blockDim.x) {
+    const int tl = q / E, e = q - tl * E;
+    const int tt = t0 + tl;
+    if (tt >= T) continue;
+    const float* pk = part + static_cast<size_t>(tt) * E + e;
+    const size_t kstride = static_cast<size_t>(T) * E;
+    float l = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < KS; ++k) l += pk[k * kstride];
+    if (bias != nullptr) l += bias[e];
+    const float sv = 1.0f / (1.0f + expf(-l));
+    s_sc[tl][e] = sv;
+    if (scores_out != nullptr) scores_out[static_cast<size_t>(tt) * E + e] = sv;
+  }
+  __syncthreads();
+  const int t = t0 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  if ((threadIdx.x >> 5) >= tpb || t >= T) return;
 
   float s[NI];
 #pragma unroll
-  for (int i = 0; i < NI; ++i) s[i] = 0.f;
-  // K-slice partial sums, in slice order; the loads of all NI columns of a
-  // slice are independent, which hides their latency
-#pragma unroll 4
-  for (int k = 0; k < KS; ++k) {
-    const float* pk = part + (static_cast<size_t>(k) * T + t) * E + lane;
-    float v[NI];
-#pragma unroll
-    for (int i = 0; i < NI; ++i) v[i] = pk[i * 32];
-#pragma unroll
-    for (int i = 0; i < NI; ++i) s[i] += v[i];
-  }
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int e = i * 32 + lane;
-    float l = s[i];
-    if (bias != nullptr) l += bias[e];
-    s[i] = 1.0f / (1.0f + expf(-l));
-    if (scores_out != nullptr) scores_out[static_cast<size_t>(t) * E + e] = s[i];
-  }
+  for (int i = 0; i < NI; ++i) s[i] = s_sc[threadIdx.x >> 5][i * 32 + lane];
 
   // groups: keep topk_group of n_group (n_group == NI here unless all are kept)
   bool kept[NI];
@@ -241,11 +246,6 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   if (lane < top_k) {
     idx_out[static_cast<size_t>(t) * top_k + lane] = my_e;
     w_out[static_cast<size_t>(t) * top_k + lane] = scale * my_s / sum;
-  }
-  if (acc_zero != nullptr) {
-    float4* row = reinterpret_cast<float4*>(acc_zero + static_cast<size_t>(t) * H);
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = lane; q < (H >> 2); q += 32) row[q] = z;
   }
 }
 

@@ -268,6 +268,15 @@ def test_forward_token_major_path(B, prefill_gemm, T, H, I, E, n_group, topk_gro
     _full_layer_check(B, wl, d)
 
 
+@pytest.mark.parametrize("T,H", [(700, 384), (1500, 640)])
+def test_forward_weight_major_wide_tiles(B, T, H):
+    """Many tokens per expert with H not a multiple of 256: the weight-major
+    GEMMs with 128-token tiles (several tiles per expert)."""
+    wl, d = S.make_custom(T=T, H=H, E=32, I=128, n_group=1, topk_group=1, top_k=8,
+                          seed=T, device="cuda")
+    _full_layer_check(B, wl, d)
+
+
 def test_forward_token_major_hot_group(B, prefill_gemm):
     """1000 tokens all routed to experts 0..7 (four groups of 250 each) and
     248 empty experts, on the prefill GEMM paths."""

@@ -110,6 +110,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# --------------------------------------------------------------- ranks
+def combine_ranks(ms_total: float, e2e_s: float, world: int, device) -> tuple:
+    """Slowest rank's device time and end-to-end time (each rank ran its own
+    batch; the job finishes when the slowest rank does)."""
+    if world <= 1:
+        return ms_total, e2e_s
+    t = torch.tensor([ms_total, e2e_s], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t[0].item()), float(t[1].item())
+
+
+def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, seconds: float) -> float:
+    """Tokens/s of the whole job: all ranks' tokens over the slowest time."""
+    return world * tokens_per_rank * steps / seconds
+
+
 # ------------------------------------------------------------ workload
 def _workload(name):
     wl = S.WORKLOADS[name]
@@ -149,12 +165,16 @@ def _traffic_for(kernel, workload):
             rec = json.load(f)
     except Exception:
         return None
-    src = os.path.join(ROOT, "sparse_moe_transformer_limited_b300", "csrc", "kernels_gemm.cuh")
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
     for r in rec.get("entries", []):
-        if r.get("kernel") == kernel and r.get("workload") == workload and r.get("src_sha") == sha:
-            return r.get("dram_bytes_per_launch")
+        if r.get("kernel") != kernel or r.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, "sparse_moe_transformer_limited_b300", "csrc", r["src_file"])
+        try:
+            with open(src, "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        except OSError:
+            return None
+        return r.get("dram_bytes_per_launch") if r.get("src_sha") == sha else None
     return None
 
 
@@ -208,12 +228,6 @@ def run_ours(args, rank, world, local_rank):
     ms_total = e0.elapsed_time(e1)
     if B.status() != 0:
         raise RuntimeError(B.last_error())
-    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_total = float(t.item())
-    ms_step = ms_total / args.steps
-    value = world * wl.T * args.steps / (ms_total / 1e3)
 
     # ---- end-to-end through the public API with host buffers
     h_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
@@ -235,12 +249,12 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     barrier()
     e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = world * wl.T * args.steps / float(te.item())
     if B.status() != 0:
         raise RuntimeError(B.last_error())
+    ms_total, e2e_s = combine_ranks(ms_total, e2e_s, world, dev)
+    ms_step = ms_total / args.steps
+    value = weak_scaling_value(world, wl.T, args.steps, ms_total / 1e3)
+    e2e_value = weak_scaling_value(world, wl.T, args.steps, e2e_s)
 
     alg = _algorithmic(wl, counts)
     peaks = _peaks()

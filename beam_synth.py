@@ -165,3 +165,17 @@ def residual_inputs(T: int, H: int, seed: int, device="cpu"):
     h = torch.randn((T, H), generator=g).to(torch.bfloat16)
     o = torch.randn((T, H), generator=g).to(torch.bfloat16)
     return h.to(device), o.to(device)
+
+
+def dense_inputs(T: int, H: int, I: int, seed: int, device="cpu"):
+    """Dense SwiGLU MLP inputs: x BF16 N(0,1); w_gate, w_up [I,H] and w_down
+    [H,I] FP32 N(0, 0.02) rounded to BF16. Small sizes are drawn on the CPU."""
+    dev = torch.device(device)
+    small = (3 * I * H + T * H) < (1 << 26)
+    gen_dev = "cpu" if small or dev.type == "cpu" else dev
+    g = _gen(gen_dev, seed)
+    w_gate = _randn_bf16((I, H), 0.02, g, gen_dev)
+    w_up = _randn_bf16((I, H), 0.02, g, gen_dev)
+    w_down = _randn_bf16((H, I), 0.02, g, gen_dev)
+    x = _randn_bf16((T, H), 1.0, g, gen_dev, max(1, min(T, (1 << 26) // H)))
+    return tuple(t.to(dev) for t in (x, w_gate, w_up, w_down))

@@ -18,6 +18,7 @@ time. `--impl reference` times the CPU oracle on a bounded sample instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -286,6 +287,74 @@ def run_ours(args, rank, world, local_rank):
                 h2d=wl.T * wl.H * 2, d2h=wl.T * wl.H * 2)
 
 
+# ------------------------------------------------------- dense MLP arm
+# The dense SwiGLU MLP of the first layers. Its intermediate size is not on
+# the pages; 12288 (2.4 x hidden) stands in for it. Layer 0's MLP is residual
+# step k = 3 (the embedding is step 1, layer 0's attention step 2).
+DENSE = {"dense_prefill": dict(T=8192, H=5120, I=12288, seed=5),
+         "dense_decode": dict(T=64, H=5120, I=12288, seed=6)}
+DENSE_K = 3
+
+
+def run_dense(args, rank, world, local_rank, name):
+    import sparse_moe_transformer_limited_b300 as B
+    B.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = DENSE[name]
+    T, H, I = cfg["T"], cfg["H"], cfg["I"]
+    x, wg, wu, wd = S.dense_inputs(T, H, I, cfg["seed"] + 1000 * rank, dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    n = B.lib().beam_dense_workspace_size(ctypes.byref(B.DenseParams(T, H, I, 1e-6, DENSE_K,
+                                                                     B.FLAG_PRE_NORM)))
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+
+    def step():
+        B.dense_forward(T, H, I, x, wg, wu, wd, residual_k=DENSE_K, flags=B.FLAG_PRE_NORM,
+                        out=out, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    B.profile_read()
+    B.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    B.profile_enable(False)
+    clk = clocks.stop()
+    prof = B.profile_read()
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks = _peaks()
+    gu_ms = prof["expert_gemm_gateup_swiglu"][0] / prof["expert_gemm_gateup_swiglu"][1]
+    flops = 2.0 * T * 3 * H * I
+    wbytes = 3 * H * I * 2 + 2 * T * H * 2
+    if T <= 24:
+        bound, ach, peak, unit = "hbm", 2 * I * H * 2 / (gu_ms / 1e3) / 1e9, peaks["hbm"], "GB/s"
+    else:
+        bound, ach, peak, unit = ("tensor", 2.0 * T * 2 * I * H / (gu_ms / 1e3) / 1e12,
+                                  peaks["bf16"], "TFLOP/s")
+    return {"workload": f"dense SwiGLU MLP sublayer T={T}, hidden {H}, intermediate {I} "
+                        f"(stand-in size), pre-norm + residual k={DENSE_K}",
+            "value": round(T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "layer_tflops": round(flops / (ms / 1e3) / 1e12, 1),
+            "layer_hbm_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
+            "roofline": {"kernel": "expert_gemm_gateup_swiglu", "bound": bound,
+                         "achieved": round(ach, 1), "peak": peak, "unit": unit,
+                         "frac": round(ach / peak, 4), "launch_ms": round(gu_ms, 4)},
+            "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in prof.items()}, "clocks": clk}
+
+
 # ---------------------------------------------------------- oracle arm
 def _blas_threads():
     try:
@@ -373,7 +442,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--config", default="decode", choices=sorted(S.WORKLOADS) + sorted(DENSE))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
@@ -392,6 +461,11 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
+    if args.config in DENSE:
+        r = run_dense(args, rank, world, local_rank, args.config)
+        if rank == 0:
+            print(json.dumps(dict(metric=METRIC, n_gpus=world, steps=args.steps, **r)), flush=True)
+        return
     wl = _workload(args.config)
     if args.impl == "reference":
         r = run_reference(args, rank, world)
@@ -417,7 +491,10 @@ def main():
         a2.config = "prefill"
         torch.cuda.empty_cache()
         r2 = run_ours(a2, rank, world, local_rank)
-        extra = {"prefill_T8192": {"value": round(r2["value"], 1), "unit": "tokens/s",
+        torch.cuda.empty_cache()
+        extra_dense = run_dense(a2, rank, world, local_rank, "dense_prefill")
+        extra = {"dense_mlp_T8192": extra_dense,
+                 "prefill_T8192": {"value": round(r2["value"], 1), "unit": "tokens/s",
                                    "ms_per_step": round(r2["ms_step"], 4),
                                    "e2e": round(r2["e2e"], 1), "roofline": r2["roofline"],
                                    "layer": r2["layer"], "kernels_ms": r2["kernels_ms"],

@@ -134,6 +134,38 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in,
                                int32_t* topk_idx, float* topk_w, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* Dense SwiGLU MLP sublayer of the first layers ([P1] 专家混合模型: the first 3
+ * of the 52 layers use a dense SwiGLU MLP instead of the experts; 残差流: normalised
+ * before and after, scaled residual). The pages do not give its intermediate
+ * size, so I is a parameter.
+ *   T, H, I     tokens, hidden (multiple of 128, at most 8192), intermediate
+ *               (multiple of 128)
+ *   rms_eps, residual_k, flags  as in beam_moe_params (flags: PRE_NORM,
+ *               FP32_OUT)
+ */
+typedef struct {
+  int T, H, I;
+  float rms_eps;
+  int residual_k;
+  int flags;
+} beam_dense_params;
+
+/* Workspace bytes for beam_dense_mlp_forward (0 on invalid parameters). */
+size_t beam_dense_workspace_size(const beam_dense_params* p);
+
+/*   x = BEAM_FLAG_PRE_NORM ? bf16(RMSNorm(x_in) * pre_gain) : x_in
+ *   y = (silu(x W_gate^T) * (x W_up^T)) W_down^T  (BF16 operands, FP32
+ *       accumulation, SwiGLU product in FP32 rounded to BF16)
+ *   out = residual_k >= 2 ? bf16(sqrt((k-1)/k) x_in + RMSNorm(y) * post_gain / sqrt(k))
+ *                         : y (bf16, or fp32 with BEAM_FLAG_FP32_OUT)
+ *   x_in [T,H] bf16; w_gate, w_up [I,H] bf16; w_down [H,I] bf16;
+ *   pre_gain, post_gain [H] fp32 or NULL; out [T,H]. Runs on the same expert
+ *   GEMM kernels as beam_moe_forward, as one expert that every token uses. */
+beam_status_t beam_dense_mlp_forward(const beam_dense_params* p, const void* x_in,
+                                     const void* w_gate, const void* w_up, const void* w_down,
+                                     const float* pre_gain, const float* post_gain, void* out,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* One scaled residual update ([P1] 残差流):
  *   h_out = bf16( sqrt((k-1)/k) * h_prev + (1/sqrt(k)) * n ),
  *   n = apply_norm ? RMSNorm(sub_out) * post_gain : sub_out   (FP32 math)

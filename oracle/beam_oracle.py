@@ -263,6 +263,22 @@ def residual_step(h_prev, sub_out, k: int, gain=None, eps: float = 1e-6,
 
 
 # ----------------------------------------------------------------------------
+# dense SwiGLU MLP of the first layers ([P1] 专家混合模型: the first 3 layers use
+# a dense SwiGLU MLP; [P1] 残差流: normalised before and after, scaled residual)
+# ----------------------------------------------------------------------------
+def dense_mlp_forward(x_in, w_gate, w_up, w_down, *, eps=1e-6, pre_norm=False,
+                      pre_gain=None, residual_k=0, post_gain=None) -> dict:
+    """x = pre_norm ? bf16(RMSNorm(x_in)) : x_in; y = SwiGLU MLP of x;
+    h = residual step at k (when residual_k >= 2). w_gate, w_up [I,H];
+    w_down [H,I]; the intermediate size I is a parameter (not on the pages)."""
+    x_in = np.asarray(x_in, dtype=F64)
+    x = bf16_round(rms_norm(x_in, pre_gain, eps)).astype(F64) if pre_norm else x_in
+    y = swiglu_expert(x, w_gate, w_up, w_down)
+    h = residual_step(x_in, y, residual_k, post_gain, eps, True) if residual_k else None
+    return dict(x=x, out=y, h=h)
+
+
+# ----------------------------------------------------------------------------
 # the whole sublayer
 # ----------------------------------------------------------------------------
 def moe_forward(x_in, w_router, bias, get_expert, *, n_group=8, topk_group=4,

@@ -6,11 +6,11 @@ residual update) runs in the library's CUDA kernels; this package only
 marshals torch tensors into the C ABI declared in include/beam_moe.h.
 """
 from ._native import (BeamError, Params, make_params, workspace_size, workspace_layout,
-                      alloc_workspace, route, route_static, forward, residual_step, status, last_error,
+                      alloc_workspace, route, route_static, forward, dense_forward, DenseParams, residual_step, status, last_error,
                       debug_wait_timeout, lib, LIB_PATH, EXPORTED, FLAG_PRE_NORM,
                       FLAG_FP32_OUT, FLAG_RETURN_SCORES, profile_enable, profile_read)
 
 __all__ = ["BeamError", "Params", "make_params", "workspace_size", "workspace_layout",
-           "alloc_workspace", "route", "route_static", "forward", "residual_step", "status", "last_error",
+           "alloc_workspace", "route", "route_static", "forward", "dense_forward", "DenseParams", "residual_step", "status", "last_error",
            "debug_wait_timeout", "lib", "LIB_PATH", "EXPORTED", "FLAG_PRE_NORM",
            "FLAG_FP32_OUT", "FLAG_RETURN_SCORES", "profile_enable", "profile_read"]

@@ -35,7 +35,7 @@ LAYOUT_NAMES = ("xn", "part", "topk_idx", "topk_w", "counts", "offsets", "row_to
 
 # every symbol include/beam_moe.h declares
 EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static",
-            "beam_moe_forward",
+            "beam_moe_forward", "beam_dense_workspace_size", "beam_dense_mlp_forward",
             "beam_residual_step", "beam_status", "beam_last_error_string",
             "beam_moe_workspace_layout", "beam_debug_wait_timeout", "beam_profile_enable",
             "beam_profile_read")
@@ -51,6 +51,12 @@ class Params(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int),
                 ("I", ctypes.c_int), ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("routed_scale", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("residual_k", ctypes.c_int),
+                ("flags", ctypes.c_int)]
+
+
+class DenseParams(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("rms_eps", ctypes.c_float), ("residual_k", ctypes.c_int),
                 ("flags", ctypes.c_int)]
 
@@ -78,6 +84,11 @@ def lib() -> ctypes.CDLL:
         L.beam_moe_route_static.restype = i32
         L.beam_moe_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.beam_moe_forward.restype = i32
+        D = ctypes.POINTER(DenseParams)
+        L.beam_dense_workspace_size.argtypes = [D]
+        L.beam_dense_workspace_size.restype = sz
+        L.beam_dense_mlp_forward.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.beam_dense_mlp_forward.restype = i32
         L.beam_residual_step.argtypes = [vp, vp, i32, i32, i32, vp, f32, i32, i32, vp, vp]
         L.beam_residual_step.restype = i32
         L.beam_status.argtypes = [vp]
@@ -186,6 +197,24 @@ def forward(p: Params, x, w_router, w_gate, w_up, w_down, bias=None, pre_gain=No
                                   _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(pre_gain),
                                   _ptr(post_gain), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
                                   _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def dense_forward(T, H, I, x, w_gate, w_up, w_down, pre_gain=None, post_gain=None,
+                  rms_eps=1e-6, residual_k=0, flags=0, out=None, workspace=None, stream=None):
+    """beam_dense_mlp_forward: the dense SwiGLU MLP sublayer."""
+    p = DenseParams(T, H, I, rms_eps, residual_k, flags)
+    if out is None:
+        dt = torch.float32 if (flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((T, H), dtype=dt, device=x.device)
+    if workspace is None:
+        n = lib().beam_dense_workspace_size(ctypes.byref(p))
+        if n == 0:
+            raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    _check(lib().beam_dense_mlp_forward(ctypes.byref(p), _ptr(x), _ptr(w_gate), _ptr(w_up),
+                                        _ptr(w_down), _ptr(pre_gain), _ptr(post_gain), _ptr(out),
+                                        _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

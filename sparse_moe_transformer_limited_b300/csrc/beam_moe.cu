@@ -430,82 +430,20 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
   return BEAM_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* beam_last_error_string(void) { return t_last_error.c_str(); }
-
-size_t beam_moe_workspace_size(const beam_moe_params* p) {
-  if (check_params(p) != BEAM_OK) return 0;
-  return make_layout(*p).total;
-}
-
-int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n) {
-  if (check_params(p) != BEAM_OK || offsets == nullptr || n <= 0) return 0;
-  const Layout L = make_layout(*p);
-  const int m = n < kLayoutEntries ? n : kLayoutEntries;
-  for (int i = 0; i < m; ++i) offsets[i] = L.off[i];
-  return m;
-}
-
-beam_status_t beam_moe_route(const beam_moe_params* p, const void* x, const float* w_router,
-                             const float* logit_bias, const float* pre_gain, int32_t* topk_idx,
-                             float* topk_w, float* scores, void* workspace,
-                             size_t workspace_bytes, void* stream) {
-  beam_status_t s = check_params(p);
-  if (s != BEAM_OK) return s;
-  if (p->T == 0) return BEAM_OK;
-  if (!x || !w_router || !topk_idx || !topk_w || !workspace)
-    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
-  if ((p->flags & BEAM_FLAG_RETURN_SCORES) && !scores)
-    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_RETURN_SCORES needs a scores buffer");
-  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace) ||
-      (pre_gain && !aligned16(pre_gain)))
-    return fail(BEAM_ERR_INVALID_ARG, "x, w_router, pre_gain and workspace must be 16-byte aligned");
-  const Layout L = make_layout(*p);
-  if (workspace_bytes < L.total)
-    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
-                workspace_bytes, L.total);
-  return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
-                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr,
-                       static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
-}
-
-beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const float* w_router,
-                               const float* logit_bias, const void* w_gate, const void* w_up,
-                               const void* w_down, const float* pre_gain, const float* post_gain,
-                               void* out, int32_t* topk_idx, float* topk_w, void* workspace,
-                               size_t workspace_bytes, void* stream) {
-  beam_status_t s = check_params(p);
-  if (s != BEAM_OK) return s;
-  if (p->T == 0) return BEAM_OK;
-  if (!x_in || !w_router || !w_gate || !w_up || !w_down || !out || !workspace)
-    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
-  const void* ptrs[] = {x_in, w_router, w_gate, w_up, w_down, out, workspace};
-  for (const void* q : ptrs)
-    if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
-  if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
-    return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
-  if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
-  const Layout L = make_layout(*p);
-  if (workspace_bytes < L.total)
-    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
-                workspace_bytes, L.total);
-
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+// Steps 2-5 of the sublayer, given the routing (idx, wts): permutation and
+// work lists, the expert GEMMs, then the weighted combine with post-norm and
+// residual. With dense = true there is one expert that every token uses with
+// weight 1 (the dense SwiGLU MLP): the permutation is the identity, set up by
+// dense_setup_kernel, and the GEMMs read x in place.
+beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const void* x_in,
+                          const __nv_bfloat16* x, const int32_t* idx, float* wts,
+                          const void* w_gate, const void* w_up, const void* w_down,
+                          const float* post_gain, void* out, uint8_t* ws, cudaStream_t st,
+                          bool dense) {
+  const beam_moe_params* p = &prm;
+  beam_status_t s = BEAM_OK;
   const int T = p->T, H = p->H, E = p->E, I = p->I, K = p->top_k;
   const long long R = static_cast<long long>(T) * K;
-  int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.off[L_IDX]);
-  float* wts = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.off[L_W]);
-
-  // 1. pre-norm (optional) + router
-  s = launch_router(*p, L, x_in, w_router, logit_bias, pre_gain, idx, wts, nullptr, ws, st);
-  if (s != BEAM_OK) return s;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
-  if (p->flags & BEAM_FLAG_PRE_NORM) x = reinterpret_cast<const __nv_bfloat16*>(ws + L.off[L_XN]);
-
   // 2. permutation, work lists and the expert-ordered copy of x
   int* blk_hist = reinterpret_cast<int*>(ws + L.off[L_BLKHIST]);
   int* blk_off = reinterpret_cast<int*>(ws + L.off[L_BLKOFF]);
@@ -521,7 +459,12 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   int4* udn = reinterpret_cast<int4*>(ws + L.off[L_UDN]);
   int* nunits = reinterpret_cast<int*>(ws + L.off[L_NUNITS]);
 
-  {
+  const int NB = dense ? 1 : L.NB;
+  if (dense) {
+    ProfScope ps("dense_setup", st);
+    beam::dense_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, blk_hist, pair_row, row_tok,
+                                                              row_w, wts);
+  } else {
     ProfScope ps("expert_hist", st);
     beam::expert_block_hist_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(idx, T, K, E, blk_hist);
   }
@@ -530,34 +473,38 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
     ProfScope ps("expert_scan_units", st);
     if (L.path == PATH_PAIR)
       beam::expert_scan_units_prefill_kernel<beam::LIST_PAIR, beam::LIST_PAIR>
-          <<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
+          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
                               H / 256);
     else if (L.path == PATH_MIXED)
       beam::expert_scan_units_prefill_kernel<beam::LIST_TM, beam::LIST_PAIR>
-          <<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
+          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
                               H / 256);
     else if (L.path == PATH_TM)
       beam::expert_scan_units_prefill_kernel<beam::LIST_TM, beam::LIST_TM>
-          <<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
+          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
                               H / 256);
     else
-      beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, E, blk_off, counts, offs,
+      beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs,
                                                         ugu, nunits, L.NT, I / 128,
                                                         path_mt_down(L.path, H));
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
-  {
-    ProfScope ps("expert_scatter", st);
-    beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(idx, wts, T, K, E, blk_off,
-                                                                     pair_row, row_tok, row_w);
+  if (dense) {
+    xperm = const_cast<__nv_bfloat16*>(x);  // identity permutation: read x in place
+  } else {
+    {
+      ProfScope ps("expert_scatter", st);
+      beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(
+          idx, wts, T, K, E, blk_off, pair_row, row_tok, row_w);
+    }
+    BEAM_LAUNCH_CHECK("expert_scatter_kernel");
+    {
+      ProfScope ps("gather_rows", st);
+      beam::gather_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+          x, row_tok, static_cast<int>(R), H, xperm);
+    }
+    BEAM_LAUNCH_CHECK("gather_rows_kernel");
   }
-  BEAM_LAUNCH_CHECK("expert_scatter_kernel");
-  {
-    ProfScope ps("gather_rows", st);
-    beam::gather_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
-        x, row_tok, static_cast<int>(R), H, xperm);
-  }
-  BEAM_LAUNCH_CHECK("gather_rows_kernel");
 
   // 3. gate/up GEMM + SwiGLU -> act, 4. down GEMM -> per-pair y
   const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
@@ -672,6 +619,172 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   }
   BEAM_LAUNCH_CHECK("combine_rows_kernel");
   return BEAM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* beam_last_error_string(void) { return t_last_error.c_str(); }
+
+size_t beam_moe_workspace_size(const beam_moe_params* p) {
+  if (check_params(p) != BEAM_OK) return 0;
+  return make_layout(*p).total;
+}
+
+int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n) {
+  if (check_params(p) != BEAM_OK || offsets == nullptr || n <= 0) return 0;
+  const Layout L = make_layout(*p);
+  const int m = n < kLayoutEntries ? n : kLayoutEntries;
+  for (int i = 0; i < m; ++i) offsets[i] = L.off[i];
+  return m;
+}
+
+beam_status_t beam_moe_route(const beam_moe_params* p, const void* x, const float* w_router,
+                             const float* logit_bias, const float* pre_gain, int32_t* topk_idx,
+                             float* topk_w, float* scores, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_params(p);
+  if (s != BEAM_OK) return s;
+  if (p->T == 0) return BEAM_OK;
+  if (!x || !w_router || !topk_idx || !topk_w || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if ((p->flags & BEAM_FLAG_RETURN_SCORES) && !scores)
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_RETURN_SCORES needs a scores buffer");
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace) ||
+      (pre_gain && !aligned16(pre_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "x, w_router, pre_gain and workspace must be 16-byte aligned");
+  const Layout L = make_layout(*p);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+  return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
+                       (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr,
+                       static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const float* w_router,
+                               const float* logit_bias, const void* w_gate, const void* w_up,
+                               const void* w_down, const float* pre_gain, const float* post_gain,
+                               void* out, int32_t* topk_idx, float* topk_w, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_params(p);
+  if (s != BEAM_OK) return s;
+  if (p->T == 0) return BEAM_OK;
+  if (!x_in || !w_router || !w_gate || !w_up || !w_down || !out || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  const void* ptrs[] = {x_in, w_router, w_gate, w_up, w_down, out, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
+  if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
+  if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
+  const Layout L = make_layout(*p);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int T = p->T, H = p->H, E = p->E, I = p->I, K = p->top_k;
+  const long long R = static_cast<long long>(T) * K;
+  int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.off[L_IDX]);
+  float* wts = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.off[L_W]);
+
+  // 1. pre-norm (optional) + router
+  s = launch_router(*p, L, x_in, w_router, logit_bias, pre_gain, idx, wts, nullptr, ws, st);
+  if (s != BEAM_OK) return s;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
+  if (p->flags & BEAM_FLAG_PRE_NORM) x = reinterpret_cast<const __nv_bfloat16*>(ws + L.off[L_XN]);
+
+  // 2-5. permutation, expert GEMMs, combine and the residual
+  return run_experts(*p, L, x_in, x, idx, wts, w_gate, w_up, w_down, post_gain, out, ws, st,
+                     false);
+}
+
+// ------------------------------------------------------------- dense MLP
+namespace {
+
+beam_status_t check_dense(const beam_dense_params* d) {
+  if (d == nullptr) return fail(BEAM_ERR_INVALID_ARG, "params is NULL");
+  if (d->T < 0 || d->H <= 0 || d->I <= 0)
+    return fail(BEAM_ERR_INVALID_ARG, "T=%d H=%d I=%d: sizes must be positive", d->T, d->H, d->I);
+  if (d->T > (1 << 22)) return fail(BEAM_ERR_UNSUPPORTED, "T=%d exceeds 4194304", d->T);
+  if (d->H % 128 || d->I % 128)
+    return fail(BEAM_ERR_UNSUPPORTED, "H=%d and I=%d must be multiples of 128", d->H, d->I);
+  if (d->H > 8192 || d->I > 65536)
+    return fail(BEAM_ERR_UNSUPPORTED, "H must be at most 8192 and I at most 65536");
+  if (!(d->rms_eps >= 0.f) || !std::isfinite(d->rms_eps))
+    return fail(BEAM_ERR_INVALID_ARG, "rms_eps must be >= 0 and finite");
+  if (d->residual_k == 1 || d->residual_k < 0)
+    return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", d->residual_k);
+  if (d->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT))
+    return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
+  if ((d->flags & BEAM_FLAG_FP32_OUT) && d->residual_k >= 2)
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP32_OUT applies only without the residual step");
+  return BEAM_OK;
+}
+
+// The dense MLP runs as a one-expert sublayer: E = 1, top_k = 1, weight 1.
+beam_moe_params dense_as_moe(const beam_dense_params& d) {
+  beam_moe_params m{};
+  m.T = d.T;
+  m.H = d.H;
+  m.E = 1;
+  m.I = d.I;
+  m.n_group = 1;
+  m.topk_group = 1;
+  m.top_k = 1;
+  m.routed_scale = 1.f;
+  m.rms_eps = d.rms_eps;
+  m.residual_k = d.residual_k;
+  m.flags = d.flags;
+  return m;
+}
+
+}  // namespace
+
+size_t beam_dense_workspace_size(const beam_dense_params* d) {
+  if (check_dense(d) != BEAM_OK) return 0;
+  return make_layout(dense_as_moe(*d)).total;
+}
+
+beam_status_t beam_dense_mlp_forward(const beam_dense_params* d, const void* x_in,
+                                     const void* w_gate, const void* w_up, const void* w_down,
+                                     const float* pre_gain, const float* post_gain, void* out,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_dense(d);
+  if (s != BEAM_OK) return s;
+  if (d->T == 0) return BEAM_OK;
+  if (!x_in || !w_gate || !w_up || !w_down || !out || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  const void* ptrs[] = {x_in, w_gate, w_up, w_down, out, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
+  if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
+  if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
+  const beam_moe_params mp = dense_as_moe(*d);
+  const Layout L = make_layout(mp);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
+  if (d->flags & BEAM_FLAG_PRE_NORM) {
+    __nv_bfloat16* xn = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_XN]);
+    {
+      ProfScope ps("prenorm", st);
+      beam::prenorm_kernel<<<(d->T + 7) / 8, 256, 0, st>>>(x, pre_gain, xn, d->T, d->H,
+                                                           d->rms_eps);
+    }
+    BEAM_LAUNCH_CHECK("prenorm_kernel");
+    x = xn;
+  }
+  float* wts = reinterpret_cast<float*>(ws + L.off[L_W]);
+  return run_experts(mp, L, x_in, x, nullptr, wts, w_gate, w_up, w_down, post_gain, out, ws, st,
+                     true);
 }
 
 beam_status_t beam_residual_step(const void* h_prev, const void* sub_out, int T, int H, int k,

@@ -260,6 +260,23 @@ __global__ void __launch_bounds__(PERM_THREADS) expert_scatter_kernel(
   }
 }
 
+// Identity routing for the dense SwiGLU MLP (one expert that every token uses
+// with weight 1): the histogram of the single block and the maps.
+__global__ void __launch_bounds__(256) dense_setup_kernel(int T, int* __restrict__ blk_hist,
+                                                          int* __restrict__ pair_row,
+                                                          int* __restrict__ row_token,
+                                                          float* __restrict__ row_weight,
+                                                          float* __restrict__ w) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t == 0) blk_hist[0] = T;
+  if (t < T) {
+    pair_row[t] = t;
+    row_token[t] = t;
+    row_weight[t] = 1.f;
+    w[t] = 1.f;
+  }
+}
+
 // xperm[row, :] = x[row_token[row], :], one warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
                                                           const int* __restrict__ row_token,

@@ -35,6 +35,25 @@ def test_params_struct_matches_header():
     assert fields == [f for f, _ in B.Params._fields_]
 
 
+def test_dense_params_struct_matches_header():
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct \{([^{}]*)\} beam_dense_params;", src).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b([A-Za-z_][A-Za-z_0-9]*)\s*[,;]", body)
+    assert fields == [f for f, _ in B.DenseParams._fields_]
+
+
+@pytest.mark.parametrize("T,H,I,k,flags,code", [
+    (8, 5120, 2500, 0, 0, 2), (8, 5000, 2560, 0, 0, 2), (8, 5120, 2560, 1, 0, 1),
+    (8, 5120, 2560, 50, 2, 1), (-1, 5120, 2560, 0, 0, 1), (8, 5120, 2560, 0, 4, 1),
+])
+def test_dense_invalid_params_rejected(T, H, I, k, flags, code):
+    p = B.DenseParams(T, H, I, 1e-6, k, flags)
+    assert B.lib().beam_dense_workspace_size(ctypes.byref(p)) == 0
+    r = B.lib().beam_dense_mlp_forward(ctypes.byref(p), *([None] * 8), 0, None)
+    assert r == code, B.last_error()
+
+
 def _p(**kw):
     base = dict(T=64, H=5120, E=256, I=2560)
     base.update(kw)

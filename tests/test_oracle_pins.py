@@ -362,3 +362,32 @@ def test_layer_shape_facts():
     active = k * L * per_expert + (total - experts_all)
     assert round(active / 1e9, 1) == f["active_params_billions"]["value"]
     assert f["dense_layers"]["value"] + L == f["num_layers"]["value"]
+
+
+# --------------------------------------------------------------------------
+# dense SwiGLU MLP of the first layers
+# --------------------------------------------------------------------------
+def test_dense_mlp_closed_form():
+    """H=2, I=1 by hand (as the expert case): x=[1,2], g=2, u=0.75."""
+    x = np.array([[1.0, 2.0]])
+    r = O.dense_mlp_forward(x, np.array([[1.0, 0.5]]), np.array([[0.25, 0.25]]),
+                            np.array([[1.0], [-2.0]]))
+    a = 2.0 / (1.0 + math.exp(-2.0)) * 0.75
+    assert np.allclose(r["out"], [[a, -2.0 * a]], atol=1e-15)
+    assert r["h"] is None
+
+
+def test_dense_mlp_is_one_expert_with_unit_weight():
+    """The dense MLP equals the expert combine with a single expert that every
+    token uses with weight 1 (a separate code path: moe_combine)."""
+    rng = np.random.default_rng(12)
+    T, H, I = 9, 32, 24
+    x = rng.normal(size=(T, H))
+    wg, wu, wd = rng.normal(size=(I, H)) * .1, rng.normal(size=(I, H)) * .1, rng.normal(size=(H, I)) * .1
+    d = O.dense_mlp_forward(x, wg, wu, wd)
+    m = O.moe_combine(x, np.zeros((T, 1), np.int64), np.ones((T, 1)), lambda e: (wg, wu, wd))
+    assert np.allclose(d["out"], m, rtol=1e-13, atol=1e-15)
+    h = O.dense_mlp_forward(x, wg, wu, wd, residual_k=7, pre_norm=True)
+    xn = O.bf16_round(O.rms_norm(x)).astype(np.float64)
+    want = math.sqrt(6 / 7) * x + O.rms_norm(O.swiglu_expert(xn, wg, wu, wd)) / math.sqrt(7)
+    assert np.allclose(h["h"], want, atol=1e-12)

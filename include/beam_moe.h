@@ -97,7 +97,7 @@ size_t beam_moe_workspace_size(const beam_moe_params* p);
  *   scores     [T,E] fp32 out (sigmoid scores) when BEAM_FLAG_RETURN_SCORES,
  *              else ignored (may be NULL)
  * Scores are FP32: logits accumulate x (bf16 -> fp32) times w_router in FP32
- * (for T >= 512 and E % 128 == 0 on the tensor cores, with w_router split
+ * (for T >= 512 and E == 256 on the tensor cores, with w_router split
  * exactly into three BF16 pieces so every product is exact in FP32).
  * Group score = FP32 sum of the group's two largest scores; groups rank by
  * it (ties to the lower group index). */
@@ -205,11 +205,11 @@ const char* beam_last_error_string(void);
  * Scratch needed: KS*T*E*4 bytes (rounded up to 256) for the partial logits,
  * where KS is the number of K-slices the router uses for this T (many for a
  * few tokens, one for thousands), plus T*H*2 bytes with BEAM_FLAG_PRE_NORM,
- * plus E*3H*2 bytes for the split router weight when the router runs on the
- * tensor cores (T >= 512). A call needing more returns BEAM_ERR_UNSUPPORTED
- * with a message that gives the bytes needed; nothing is enqueued then. For
- * the Beam shapes (H=5120, E=256, 148 SMs) that allows T <= 409 with
- * pre-norm and T <= 512 without.
+ * plus E*3H*2 bytes for the split router weight and its work list when the
+ * router runs on the tensor cores (T >= 512). A call needing more returns
+ * BEAM_ERR_UNSUPPORTED with a message that gives the bytes needed; nothing is
+ * enqueued then. For the Beam shapes (H=5120, E=256, 148 SMs) that allows
+ * T <= 409 with pre-norm and T <= 511 without.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
@@ -234,9 +234,9 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
  * expert outputs [T*top_k,H] fp32, 11 unit counts [4] int32, 12 per-block
  * expert histograms, 13 per-block expert offsets, 14 gate/up work list,
  * 15 down work list, 16 pair -> row map [T*top_k] int32, 17 the router
- * weight split into three BF16 pieces [E, 3H] (tensor-core router only).
- * Writes min(n, 18) entries and returns how many it wrote (0 on invalid
- * parameters). */
+ * weight split into three BF16 pieces [E, 3H] and 18 the router GEMM's work
+ * list (tensor-core router only). Writes min(n, 19) entries and returns how
+ * many it wrote (0 on invalid parameters). */
 int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n);
 
 /* Launches one block whose single thread waits on a shared-memory barrier

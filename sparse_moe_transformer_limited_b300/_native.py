@@ -31,7 +31,7 @@ FLAG_RETURN_SCORES = 4
 # names of the workspace buffers, in beam_moe_workspace_layout() order
 LAYOUT_NAMES = ("xn", "part", "topk_idx", "topk_w", "counts", "offsets", "row_token",
                 "row_weight", "xperm", "act", "y", "n_units", "blk_hist", "blk_off",
-                "units_gu", "units_dn", "pair_row", "router_w3")
+                "units_gu", "units_dn", "pair_row", "router_w3", "router_units")
 
 # every symbol include/beam_moe.h declares
 EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static",

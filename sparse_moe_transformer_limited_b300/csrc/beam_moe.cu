@@ -132,12 +132,13 @@ int path_mt_down(GemmPath g, int H) {
 // Router logits path: the tensor cores (exact three-way BF16 split of the
 // FP32 weight, FP32 accumulation) once there are enough tokens to fill the
 // GPU, else the FP32 SIMT kernel with K-slices.
-bool router_on_tensor_cores(const beam_moe_params& p) { return p.T >= 512 && p.E % 128 == 0; }
+bool router_on_tensor_cores(const beam_moe_params& p) { return p.T >= 512 && p.E == 256; }
+constexpr int kRouterKSplit = 2;  // K-slices of the tensor-core router GEMM
 
 // K-slices of the router logits GEMM: enough blocks to cover the SMs when T
 // is small. Must divide H / 32 and leave at least 64 columns per slice.
 int choose_router_ks(const beam_moe_params& p, int num_sms) {
-  if (router_on_tensor_cores(p)) return 1;
+  if (router_on_tensor_cores(p)) return kRouterKSplit;
   const int tiles = ((p.T + beam::RL_BT - 1) / beam::RL_BT) * ((p.E + beam::RL_BE - 1) / beam::RL_BE);
   const int want = (2 * num_sms + tiles - 1) / tiles;
   const int nk = p.H / 32;
@@ -147,7 +148,7 @@ int choose_router_ks(const beam_moe_params& p, int num_sms) {
   return best;
 }
 
-constexpr int kLayoutEntries = 18;
+constexpr int kLayoutEntries = 19;
 
 struct Layout {
   size_t off[kLayoutEntries];
@@ -159,8 +160,13 @@ struct Layout {
 
 enum {
   L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_Y,
-  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW, L_WR3
+  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW, L_WR3, L_RUNITS
 };
+
+// Bytes of the router's unit list and count (tensor-core router only).
+size_t router_units_bytes(const beam_moe_params& p) {
+  return static_cast<size_t>(kRouterKSplit) * ((p.T + 255) / 256) * 16 + 16;
+}
 
 int sm_count() {
   int dev = 0, n = 148;
@@ -255,6 +261,7 @@ Layout make_layout(const beam_moe_params& p) {
   sz[L_UDN] = static_cast<size_t>(L.units_dn_max) * 16;
   sz[L_PAIRROW] = static_cast<size_t>(R) * 4;
   sz[L_WR3] = router_on_tensor_cores(p) ? static_cast<size_t>(p.E) * 3 * p.H * 2 : 0;
+  sz[L_RUNITS] = router_on_tensor_cores(p) ? router_units_bytes(p) : 0;
   size_t cur = 0;
   for (int i = 0; i < kLayoutEntries; ++i) {
     L.off[i] = cur;
@@ -319,19 +326,16 @@ beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CU
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
     attr_set = true;
   }
-  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu"
-                         : (MODE == 1 ? "expert_gemm_down" : "router_logits_tc"),
-               st);
+  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
   kern<<<sm_count(), 192, C::SMEM_BYTES, st>>>(a0, a1, b, args);
-  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>"
-                              : (MODE == 1 ? "expert_gemm_kernel<down>" : "expert_gemm_kernel<router>"));
+  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>" : "expert_gemm_kernel<down>");
   return BEAM_OK;
 }
 
 template <int MODE>
 beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& tok,
                                const CUtensorMap& tok64, const beam::PairArgs& args,
-                               cudaStream_t st) {
+                               cudaStream_t st, const char* prof_name = nullptr) {
   using C = beam::PairCfg;
   auto kern = beam::expert_gemm_pair_kernel<MODE>;
   static bool attr_set = false;
@@ -341,7 +345,8 @@ beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, con
     attr_set = true;
   }
   const int grid = (sm_count() / 2) * 2;
-  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
+  ProfScope ps(prof_name ? prof_name : (MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down"),
+               st);
   kern<<<grid, 192, C::SMEM_BYTES, st>>>(a0, a1, tok, tok64, args);
   BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_pair_kernel<gate/up>" : "expert_gemm_pair_kernel<down>");
   return BEAM_OK;
@@ -379,28 +384,38 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
   }
   float* part = reinterpret_cast<float*>(ws + L.off[L_PART]);
   if (router_on_tensor_cores(p)) {
-    // logits [T, E] = [x, x, x] . [W1 | W2 | W3]^T on the tensor cores
+    // logits [T, E] = [x, x, x] . [W1 | W2 | W3]^T on the tensor cores: the
+    // 2-SM pair kernel with the 256 experts as M, tokens as N, K split in
+    // kRouterKSplit slices (summed by the select kernel)
     __nv_bfloat16* w3 = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_WR3]);
+    int4* runits = reinterpret_cast<int4*>(ws + L.off[L_RUNITS]);
+    int* rcount = reinterpret_cast<int*>(ws + L.off[L_RUNITS] + router_units_bytes(p) - 16);
     {
       ProfScope ps("router_split", st);
-      beam::router_split_kernel<<<2 * sm_count(), 256, 0, st>>>(w_router, p.E, p.H, w3);
+      beam::router_split_kernel<<<2 * sm_count(), 256, 0, st>>>(w_router, p.E, p.H, w3, p.T,
+                                                                kRouterKSplit, runits, rcount);
     }
     BEAM_LAUNCH_CHECK("router_split_kernel");
-    CUtensorMap m_w, m_x;
+    CUtensorMap m_w, m_x, m_x64;
     beam_status_t s;
     if ((s = make_map(&m_w, w3, static_cast<uint64_t>(p.E), static_cast<uint64_t>(3) * p.H,
                       128)) != BEAM_OK)
       return s;
     if ((s = make_map(&m_x, x, static_cast<uint64_t>(p.T), p.H, 16)) != BEAM_OK) return s;
-    beam::GemmArgs ga{};
-    ga.k_blocks = 3 * p.H / 64;
-    ga.b_k_wrap = p.H / 64;
-    ga.rows_total = p.T;
-    ga.m_tiles = p.E / 128;
-    ga.y = part;
-    ga.out_ld = p.E;
-    ga.timeout_ns = kWaitTimeoutNs;
-    if ((s = launch_gemm<2, 128, 6>(m_w, m_w, m_x, ga, st)) != BEAM_OK) return s;
+    if ((s = make_map(&m_x64, x, static_cast<uint64_t>(p.T), p.H, 64)) != BEAM_OK) return s;
+    beam::PairArgs ra{};
+    ra.units = runits;
+    ra.n_units = rcount;
+    ra.k_blocks = 3 * p.H / 64 / kRouterKSplit;
+    ra.w_rows_per_expert = 0;
+    ra.y = part;
+    ra.out_ld = p.E;
+    ra.k_split = kRouterKSplit;
+    ra.b_k_wrap = p.H / 64;
+    ra.y_split = static_cast<size_t>(p.T) * p.E;
+    ra.timeout_ns = kWaitTimeoutNs;
+    if ((s = launch_gemm_pair<1>(m_w, m_w, m_x, m_x64, ra, st, "router_logits_tc")) != BEAM_OK)
+      return s;
   } else {
     dim3 g1((p.T + beam::RL_BT - 1) / beam::RL_BT, (p.E + beam::RL_BE - 1) / beam::RL_BE, L.KS);
     {
@@ -947,16 +962,18 @@ extern "C" beam_status_t beam_moe_route_static(const beam_moe_params* p, const v
       (p->flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p->T) * p->H * 2 : 0, 256);
   const size_t wr3 =
       router_on_tensor_cores(*p) ? static_cast<size_t>(p->E) * 3 * p->H * 2 : 0;
-  if (part + xn + wr3 > BEAM_ROUTE_STATIC_SCRATCH_BYTES)
+  const size_t ru = router_on_tensor_cores(*p) ? align_up(router_units_bytes(*p), 256) : 0;
+  if (part + xn + wr3 + ru > BEAM_ROUTE_STATIC_SCRATCH_BYTES)
     return fail(BEAM_ERR_UNSUPPORTED,
                 "T=%d needs %zu bytes of router scratch; the static scratch holds %zu bytes "
                 "(use beam_moe_route with a workspace for this size)",
-                p->T, part + xn + wr3, static_cast<size_t>(BEAM_ROUTE_STATIC_SCRATCH_BYTES));
+                p->T, part + xn + wr3 + ru, static_cast<size_t>(BEAM_ROUTE_STATIC_SCRATCH_BYTES));
   void* base = nullptr;
   if ((s = route_static_scratch(&base)) != BEAM_OK) return s;
   L.off[L_PART] = 0;
   L.off[L_XN] = part;
   L.off[L_WR3] = part + xn;
+  L.off[L_RUNITS] = part + xn + wr3;
   return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
                        (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr,
                        static_cast<uint8_t*>(base), static_cast<cudaStream_t>(stream));

@@ -17,13 +17,6 @@
 //            D[h,t] = sum_i Wd[e, m*128+h, i] * act[t, i]
 //            epilogue: y[t, m*128+h] = D[h,t] (FP32), the per-pair expert output
 //            (the row kernel combines the pairs of a token with its weights)
-//   router   (MODE 2): the FP32 router logits on the tensor cores. The FP32
-//            router weight is split exactly into three BF16 pieces,
-//            W = W1 + W2 + W3, stored side by side as W3cat [E, 3H]; x is BF16,
-//            so every product x*Wi is exact in FP32 and
-//            logit[t, e] = sum over the 3H columns of W3cat[e, :] * [x, x, x][t, :]
-//            accumulates in FP32 in TMEM. unit = (128 experts m, token tile);
-//            epilogue logits[t, m*128+e] = D[e, t].
 //
 // Warp roles (192 threads, persistent, one CTA per SM):
 //   warp 0      TMA producer (one elected lane): fills a STAGES-deep smem ring
@@ -53,23 +46,17 @@ struct GemmArgs {
   int k_blocks;               // K / 64
   int a_rows_per_expert;      // I (gate/up) or H (down)
   __nv_bfloat16* out;         // MODE 0: act [R, I] bf16
-  float* y;                   // MODE 1: y [R, H] fp32; MODE 2: logits [T, E] fp32
+  float* y;                   // MODE 1: y [R, H] fp32
   int out_ld;
-  int b_k_wrap;               // k-blocks after which the B coordinate wraps (MODE 2: H/64)
-  int rows_total;             // MODE 2: T (units are generated, not read)
-  int m_tiles;                // weight row-tiles per unit list (I/128, H/128, E/128)
+  int m_tiles;                // weight row-tiles per token tile (I/128 or H/128)
   unsigned long long timeout_ns;
 };
 
-// Unit u of a GEMM: token tile u / m_tiles (from the tile list, or for the
-// router generated from T) and weight row-tile u % m_tiles.
+// Unit u of a GEMM: token tile u / m_tiles of the tile list and weight
+// row-tile u % m_tiles.
 template <int MODE, int NT>
 __device__ __forceinline__ int4 gemm_unit(const GemmArgs& a, int u) {
   const int m = u % a.m_tiles, j = u / a.m_tiles;
-  if (MODE == 2) {
-    const int r0 = j * NT;
-    return make_int4(0, r0, min(NT, a.rows_total - r0), m);
-  }
   const int4 t = a.units[j];
   return make_int4(t.x, t.y, t.z, m);
 }
@@ -82,7 +69,7 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
 
 template <int MODE, int NT, int STAGES>
 struct GemmCfg {
-  static_assert(MODE >= 0 && MODE <= 2, "mode");
+  static_assert(MODE == 0 || MODE == 1, "mode");
   static constexpr int A_TILE = 128 * 128;  // 128 rows x 64 bf16
   static constexpr int A_BYTES = (MODE == 0 ? 2 : 1) * A_TILE;
   static constexpr int B_BYTES = NT * 128;  // NT rows x 64 bf16
@@ -147,8 +134,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int n_units = (MODE == 2) ? args.m_tiles * ((args.rows_total + NT - 1) / NT)
-                                  : *args.n_units;
+  const int n_units = *args.n_units;
   const uint64_t tmo = args.timeout_ns;
 
   if (warp == 0) {
@@ -175,9 +161,8 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sb, &tm_a0, &full[stage], kb * 64, arow, pol_w);
           if (MODE == 0) tma_load_2d(sb + C::A_TILE, &tm_a1, &full[stage], kb * 64, arow, pol_w);
-          const int kb_b = (MODE == 2) ? kb % args.b_k_wrap : kb;
           for (int j = 0; j < nb16; ++j)
-            tma_load_2d(sb + C::A_BYTES + j * 2048, &tm_b, &full[stage], kb_b * 64, un.y + j * 16,
+            tma_load_2d(sb + C::A_BYTES + j * 2048, &tm_b, &full[stage], kb * 64, un.y + j * 16,
                         pol_x);
           ++issued;
           if (++stage == STAGES) {

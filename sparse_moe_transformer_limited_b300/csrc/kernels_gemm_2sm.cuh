@@ -40,13 +40,19 @@
 namespace beam {
 
 struct PairArgs {
-  const int4* units;        // {expert, first row, tokens (<= 256), weight tile}
+  const int4* units;        // {expert | K-split, first row, tokens (<= 256), weight tile}
   const int* n_units;
-  int k_blocks;             // K / 64
+  int k_blocks;             // K-blocks (of 64) per unit
   int w_rows_per_expert;    // I (gate/up) or H (down)
   __nv_bfloat16* act;       // MODE 0: [R, I]
   float* y;                 // MODE 1: [R, H]
   int out_ld;
+  // K-split (router logits): unit.x is the split index ks; the unit covers
+  // K-blocks [ks*k_blocks, (ks+1)*k_blocks) of A, B's K-block is the A
+  // K-block modulo b_k_wrap (0: no wrap), and the output is y + ks*y_split.
+  int k_split;              // 0: no split (unit.x is the expert)
+  int b_k_wrap;
+  size_t y_split;
   unsigned long long timeout_ns;
 };
 
@@ -153,10 +159,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const int n16 = (rows & 63) >> 4;
         const uint32_t cta_bytes = C::A_BYTES + rows * 128;
         const int tok0 = un.y + static_cast<int>(crank) * (N >> 1);
+        const int expert = args.k_split ? 0 : un.x;
+        const int kb0 = args.k_split ? un.x * args.k_blocks : 0;
         const int wrow = (MODE == 0)
-                             ? un.x * args.w_rows_per_expert + un.w * 128 + static_cast<int>(crank) * 64
-                             : un.x * args.w_rows_per_expert + un.w * 256 + static_cast<int>(crank) * 128;
-        for (int kb = 0; kb < args.k_blocks; ++kb) {
+                             ? expert * args.w_rows_per_expert + un.w * 128 + static_cast<int>(crank) * 64
+                             : expert * args.w_rows_per_expert + un.w * 256 + static_cast<int>(crank) * 128;
+        for (int kbl = 0; kbl < args.k_blocks; ++kbl) {
+          const int kb = kb0 + kbl;
+          const int kbb = args.b_k_wrap ? kb % args.b_k_wrap : kb;
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
             gemm_fail(abort_flag);
             ok = false;
@@ -172,10 +182,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             tma_load_2d_pair(sb, &tm_a0, fbar, kb * 64, wrow, pol_w);
           }
           for (int j = 0; j < n64; ++j)
-            tma_load_2d_pair(sb + C::A_BYTES + j * 8192, &tm_tok64, fbar, kb * 64, tok0 + j * 64,
+            tma_load_2d_pair(sb + C::A_BYTES + j * 8192, &tm_tok64, fbar, kbb * 64, tok0 + j * 64,
                              pol_x);
           for (int j = 0; j < n16; ++j)
-            tma_load_2d_pair(sb + C::A_BYTES + n64 * 8192 + j * 2048, &tm_tok, fbar, kb * 64,
+            tma_load_2d_pair(sb + C::A_BYTES + n64 * 8192 + j * 2048, &tm_tok, fbar, kbb * 64,
                              tok0 + n64 * 64 + j * 16, pol_x);
           ++issued;
           if (++stage == C::STAGES) {
@@ -310,6 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
       } else {
         const int h = un.w * 256 + static_cast<int>(crank) * 128 + q * 32 + lane;
+        float* ybase = args.k_split ? args.y + static_cast<size_t>(un.x) * args.y_split : args.y;
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
           float d[16];
@@ -318,7 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
             // per-pair outputs are read once, by the row kernel: stream them past L2
-            if (tok < un.z) __stcs(args.y + static_cast<size_t>(un.y + tok) * args.out_ld + h, d[j]);
+            if (tok < un.z) __stcs(ybase + static_cast<size_t>(un.y + tok) * args.out_ld + h, d[j]);
           }
         }
       }

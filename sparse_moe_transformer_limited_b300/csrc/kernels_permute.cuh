@@ -30,6 +30,39 @@ __global__ void __launch_bounds__(PERM_THREADS) expert_block_hist_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[blockIdx.x * E + e] = hist[e];
 }
 
+// Sum over the NB per-block histograms of expert e, and (second pass) the
+// running offsets blk_off[b][e]; loads are issued eight at a time so their
+// latencies overlap.
+__device__ __forceinline__ int hist_total(const int* __restrict__ blk_hist, int NB, int E, int e) {
+  int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int b = 0;
+  for (; b + 8 <= NB; b += 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] += blk_hist[(b + j) * E + e];
+  }
+  for (; b < NB; ++b) acc[0] += blk_hist[b * E + e];
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+}
+__device__ __forceinline__ void hist_offsets(const int* __restrict__ blk_hist, int NB, int E,
+                                             int e, int start, int* __restrict__ blk_off) {
+  int run = start;
+  int b = 0;
+  for (; b + 8 <= NB; b += 8) {
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = blk_hist[(b + j) * E + e];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      blk_off[(b + j) * E + e] = run;
+      run += v[j];
+    }
+  }
+  for (; b < NB; ++b) {
+    blk_off[b * E + e] = run;
+    run += blk_hist[b * E + e];
+  }
+}
+
 // Exclusive prefix sum over the 256 threads of a block; *total receives the
 // sum of all values. s_warp holds 8 ints of scratch.
 __device__ __forceinline__ int block_exclusive_scan256(int v, int* s_warp, int* total) {
@@ -75,9 +108,7 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
   __shared__ int s_order[256];
   __shared__ int s_warp[8];
   const int e = threadIdx.x;
-  int c = 0;
-  if (e < E)
-    for (int b = 0; b < NB; ++b) c += blk_hist[b * E + e];
+  const int c = e < E ? hist_total(blk_hist, NB, E, e) : 0;
   s_cnt[e] = (e < E) ? c : 0;
   int total = 0;
   const int off = block_exclusive_scan256(e < E ? c : 0, s_warp, &total);
@@ -86,11 +117,7 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
     counts[e] = c;
     offsets[e] = off;
     if (e == 0) offsets[E] = total;
-    int run = off;
-    for (int b = 0; b < NB; ++b) {
-      blk_off[b * E + e] = run;
-      run += blk_hist[b * E + e];
-    }
+    hist_offsets(blk_hist, NB, E, e, off, blk_off);
     int rank = 0;
     for (int j = 0; j < E; ++j) rank += (s_cnt[j] > c) || (s_cnt[j] == c && j < e);
     s_order[rank] = e;
@@ -129,45 +156,50 @@ __device__ __forceinline__ int tm_units_for(int n, int MT) {
   return MT * pairs + tail * ((MT + 1) >> 1);
 }
 
-__device__ void tm_write_units(int4* units, int base, int ex, int r0, int n, int MT) {
+// Unit l (0-based, within one expert's contiguous run) of each list format,
+// computed directly, so all threads of a block can write any expert's units.
+// tm: per pair of weight tiles (m, m+1): `pairs` PAIR units for m, `pairs`
+// for m+1, then one SOLO unit for the tail (when there is one); a last odd
+// tile has `pairs` PAIR units and the tail.
+__device__ __forceinline__ void tm_unit_at(int l, int ex, int r0, int n, int MT, int4* out2) {
   const int q = n >> 8, rem = n & 255;
   const int pairs = q + (rem > 128 ? 1 : 0);
   const int tail = (rem > 0 && rem <= 128) ? rem : 0;
-  int u = base;
-  for (int m = 0; m < MT; m += 2) {
-    for (int mm = m; mm < min(m + 2, MT); ++mm)
-      for (int g = 0; g < pairs; ++g) {
-        const int gr = r0 + 256 * g, gn = n - 256 * g;
-        units[2 * u] = make_int4(ex, gr, min(128, gn), mm | TM_PAIR);
-        units[2 * u + 1] = make_int4(ex, gr + 128, max(0, min(128, gn - 128)), mm | TM_PAIR);
-        ++u;
-      }
-    if (tail) {
-      const int tr = r0 + 256 * q;
-      units[2 * u] = make_int4(ex, tr, tail, m);
-      units[2 * u + 1] = (m + 1 < MT) ? make_int4(ex, tr, tail, m + 1) : make_int4(ex, tr, 0, m);
-      ++u;
-    }
+  const int per = 2 * pairs + (tail ? 1 : 0);
+  const int nfull = MT >> 1;
+  int b, r, mm;
+  if (l < nfull * per) {
+    b = l / per;
+    r = l - b * per;
+    mm = 2;
+  } else {
+    b = nfull;
+    r = l - nfull * per;
+    mm = 1;
+  }
+  const int m = 2 * b;
+  if (r < pairs * mm) {
+    const int mo = r / pairs, g = r - mo * pairs;
+    const int gr = r0 + 256 * g, gn = n - 256 * g;
+    out2[0] = make_int4(ex, gr, min(128, gn), (m + mo) | TM_PAIR);
+    out2[1] = make_int4(ex, gr + 128, max(0, min(128, gn - 128)), (m + mo) | TM_PAIR);
+  } else {
+    const int tr = r0 + 256 * q;
+    out2[0] = make_int4(ex, tr, tail, m);
+    out2[1] = (m + 1 < MT) ? make_int4(ex, tr, tail, m + 1) : make_int4(ex, tr, 0, m);
   }
 }
 
-// Work lists of the pair (2-SM) GEMMs: an expert's n tokens are split into
-// g = ceil(n / 256) balanced groups; a unit is {expert, first row, group
-// size, weight tile}. Units of one expert are contiguous, weight-tile-major
-// (the groups sharing a weight tile are adjacent); experts by token count,
-// descending.
-__device__ void pair_write_units(int4* units, int base, int ex, int r0, int n, int MT) {
+// pair (2-SM) lists: an expert's n tokens are split into g = ceil(n / 256)
+// balanced groups; a unit is {expert, first row, group size, weight tile},
+// weight-tile-major (the groups sharing a tile are adjacent): unit l is
+// weight tile m = l / g, group l % g.
+__device__ __forceinline__ int4 pair_unit_at(int l, int ex, int r0, int n, int MT) {
   const int g = (n + 255) >> 8;
   const int q = n / g, extra = n - q * g;
-  int u = base;
-  for (int m = 0; m < MT; ++m) {
-    int start = 0;
-    for (int gi = 0; gi < g; ++gi) {
-      const int sz = q + (gi < extra ? 1 : 0);
-      units[u++] = make_int4(ex, r0 + start, sz, m);
-      start += sz;
-    }
-  }
+  const int m = l / g, gi = l - m * g;
+  const int start = gi * q + min(gi, extra);
+  return make_int4(ex, r0 + start, q + (gi < extra ? 1 : 0), m);
 }
 
 // Work lists for prefill: each GEMM's list in the format of the kernel that
@@ -180,12 +212,17 @@ template <int KIND>
 __device__ __forceinline__ int list_units_for(int n, int MT) {
   return KIND == LIST_TM ? tm_units_for(n, MT) : ((n + 255) >> 8) * MT;
 }
+// Unit u of a list = unit l of expert run (ex, r0, n).
 template <int KIND>
-__device__ __forceinline__ void list_write(int4* units, int base, int ex, int r0, int n, int MT) {
-  if (KIND == LIST_TM)
-    tm_write_units(units, base, ex, r0, n, MT);
-  else
-    pair_write_units(units, base, ex, r0, n, MT);
+__device__ __forceinline__ void list_unit(int4* units, int u, int l, int ex, int r0, int n, int MT) {
+  if (KIND == LIST_TM) {
+    int4 two[2];
+    tm_unit_at(l, ex, r0, n, MT, two);
+    units[2 * u] = two[0];
+    units[2 * u + 1] = two[1];
+  } else {
+    units[u] = pair_unit_at(l, ex, r0, n, MT);
+  }
 }
 
 template <int GU_KIND, int DN_KIND>
@@ -197,9 +234,7 @@ __global__ void __launch_bounds__(256) expert_scan_units_prefill_kernel(
   __shared__ int s_order[256];
   __shared__ int s_warp[8];
   const int e = threadIdx.x;
-  int c = 0;
-  if (e < E)
-    for (int b = 0; b < NB; ++b) c += blk_hist[b * E + e];
+  const int c = e < E ? hist_total(blk_hist, NB, E, e) : 0;
   s_cnt[e] = (e < E) ? c : 0;
   int total = 0;
   const int off = block_exclusive_scan256(e < E ? c : 0, s_warp, &total);
@@ -207,11 +242,7 @@ __global__ void __launch_bounds__(256) expert_scan_units_prefill_kernel(
     counts[e] = c;
     offsets[e] = off;
     if (e == 0) offsets[E] = total;
-    int run = off;
-    for (int b = 0; b < NB; ++b) {
-      blk_off[b * E + e] = run;
-      run += blk_hist[b * E + e];
-    }
+    hist_offsets(blk_hist, NB, E, e, off, blk_off);
     int rank = 0;
     for (int j = 0; j < E; ++j) rank += (s_cnt[j] > c) || (s_cnt[j] == c && j < e);
     s_order[rank] = e;
@@ -232,9 +263,34 @@ __global__ void __launch_bounds__(256) expert_scan_units_prefill_kernel(
     n_units[2] = 0;
     n_units[3] = 0;
   }
-  if (e < E && n > 0) {
-    list_write<GU_KIND>(units_gu, b_gu, ex, r0, n, MT_gu);
-    list_write<DN_KIND>(units_dn, b_dn, ex, r0, n, MT_dn);
+  // Cooperative writes: unit u belongs to the sorted position p whose base is
+  // the largest <= u (binary search over the bases in shared memory).
+  __shared__ int s_bgu[257], s_bdn[257], s_ex[256], s_r0[256], s_n[256];
+  s_bgu[e] = b_gu;
+  s_bdn[e] = b_dn;
+  s_ex[e] = ex;
+  s_r0[e] = r0;
+  s_n[e] = n;
+  if (e == 0) {
+    s_bgu[256] = tot_gu;
+    s_bdn[256] = tot_dn;
+  }
+  __syncthreads();
+  for (int u = e; u < tot_gu; u += blockDim.x) {
+    int lo = 0, hi = 255;  // last position with base <= u (positions with 0 units share bases)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_bgu[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    list_unit<GU_KIND>(units_gu, u, u - s_bgu[lo], s_ex[lo], s_r0[lo], s_n[lo], MT_gu);
+  }
+  for (int u = e; u < tot_dn; u += blockDim.x) {
+    int lo = 0, hi = 255;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_bdn[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    list_unit<DN_KIND>(units_dn, u, u - s_bdn[lo], s_ex[lo], s_r0[lo], s_n[lo], MT_dn);
   }
 }
 

@@ -109,9 +109,23 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
 // w3 = bf16(w - w1 - w2) (each difference is exact in FP32). Output
 // [E, 3H]: columns [0,H) hold w1, [H,2H) w2, [2H,3H) w3.
 // ---------------------------------------------------------------------------
+// Also writes the work list of the pair-kernel logits GEMM: units
+// {K-split ks, first token, tokens (<= 256), 0}, split-major (the groups
+// sharing a K-slice of the weight are adjacent), and their count.
 __global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ w, int E,
                                                            int H,
-                                                           __nv_bfloat16* __restrict__ w3cat) {
+                                                           __nv_bfloat16* __restrict__ w3cat,
+                                                           int T, int k_split,
+                                                           int4* __restrict__ units,
+                                                           int* __restrict__ n_units) {
+  const int ngroups = (T + 255) / 256;
+  if (blockIdx.x == 0) {
+    for (int u = threadIdx.x; u < k_split * ngroups; u += blockDim.x) {
+      const int ks = u / ngroups, j = u - ks * ngroups;
+      units[u] = make_int4(ks, 256 * j, min(256, T - 256 * j), 0);
+    }
+    if (threadIdx.x == 0) *n_units = k_split * ngroups;
+  }
   const size_t n = static_cast<size_t>(E) * H;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {

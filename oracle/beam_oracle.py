@@ -301,3 +301,127 @@ def moe_forward(x_in, w_router, bias, get_expert, *, n_group=8, topk_group=4,
     if residual_k:
         h = residual_step(x_in, out, residual_k, post_gain, eps, True)
     return dict(x=x, sel=sel, out=out, h=h)
+
+
+# ----------------------------------------------------------------------------
+# FP8 expert weights ([P5] section 四套权重的账，自己算一遍: the FP8 checkpoint
+# stores every linear weight except lm_head, the embedding and the router
+# ("mlp.gate") as F8_E4M3 and is a dynamic FP8 quantisation; [P1] 专家混合模型:
+# an FP8 checkpoint exists beside the BF16 one).
+#
+# Readings where the pages leave the format open:
+#   * element type E4M3 in the OCP "E4M3FN" form: 4 exponent bits (bias 7),
+#     3 mantissa bits, subnormals, largest finite value 448, no infinities;
+#     conversion rounds to nearest, ties to even, and saturates at +-448.
+#   * weights: one FP32 scale per output row (static, from the row's absolute
+#     maximum); activations: one FP32 scale per token row, computed at run
+#     time from that row ("dynamic"). The same row quantiser serves both:
+#       amax = max_j |v_j|;  scale = fp32(amax / 448);  inv = fp32(448 / amax)
+#       code_j = E4M3(fp32(v_j * inv))       (scale = inv = 1 for a zero row)
+#     and a row is dequantised as E4M3 value * scale.
+#   * the expert input x is the BF16 pre-norm output, quantised per token;
+#     the SwiGLU output A is rounded to BF16 (the activation dtype) and then
+#     quantised per token-expert pair, before the down projection.
+#   * the router stays unquantised (FP32 weight, FP32 scores).
+# ----------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest E4M3 value (ties to even) of each finite input, saturating at
+    +-448; returned as float64. Spacing is 2^(e-3) in the binade [2^e, 2^(e+1))
+    for e >= -6 and 2^-9 below 2^-6 (subnormals)."""
+    v = np.asarray(v, dtype=F64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                     # a = m * 2^ex, m in [0.5, 1)
+    e = np.maximum(ex - 1, -6)              # binade exponent, subnormals share -6
+    q = np.ldexp(1.0, e - 3)                # spacing of the grid there
+    r = np.round(a / q) * q                 # np.round: halves go to even
+    r = np.where(a == 0, 0.0, r)
+    r = np.minimum(r, E4M3_MAX)
+    return np.copysign(r, v)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Byte codes (sign | exponent << 3 | mantissa) of values already on the
+    E4M3 grid (|v| <= 448)."""
+    v = np.asarray(v, dtype=F64)
+    a = np.abs(v)
+    sign = np.signbit(v).astype(np.uint8) << np.uint8(7)
+    _, ex = np.frexp(a)
+    e_unb = ex - 1
+    normal = a >= 2.0 ** -6
+    m_norm = np.where(normal, a / np.ldexp(1.0, np.where(normal, e_unb, 0)) - 1.0, 0.0) * 8.0
+    m_sub = a / 2.0 ** -9
+    mant = np.where(normal, m_norm, m_sub)
+    expo = np.where(normal, e_unb + 7, 0)
+    assert np.all(mant == np.round(mant)) and np.all((mant >= 0) & (mant <= 7)), "value off the E4M3 grid"
+    assert np.all((expo >= 0) & (expo <= 15)), "value out of E4M3 range"
+    return sign | (expo.astype(np.uint8) << np.uint8(3)) | mant.astype(np.uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of E4M3 byte codes as float64 (NaN for S.1111.111)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return s * val
+
+
+def quantize_rows_e4m3(a) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-row E4M3 quantisation with an FP32 scale (reading above).
+
+    a: [R, K] FP32-representable values (BF16 weights or activations).
+    Returns (codes [R, K] uint8, scale [R] float32)."""
+    a32 = np.asarray(a, dtype=F32)
+    amax = np.max(np.abs(a32), axis=-1)
+    nz = amax > 0
+    safe = np.where(nz, amax, F32(1.0)).astype(F32)
+    scale = np.where(nz, safe / F32(E4M3_MAX), F32(1.0)).astype(F32)   # IEEE FP32 division
+    inv = np.where(nz, F32(E4M3_MAX) / safe, F32(1.0)).astype(F32)
+    v = (a32 * inv[..., None]).astype(F32)                             # one FP32 rounding
+    return e4m3_encode(e4m3_round(v)), scale
+
+
+def dequantize_rows_e4m3(codes, scale) -> np.ndarray:
+    """E4M3 value * row scale, FP64."""
+    return e4m3_decode(codes) * np.asarray(scale, dtype=F64)[..., None]
+
+
+def swiglu_expert_fp8(x_rows, gate_q, up_q, down_q) -> np.ndarray:
+    """One expert on FP8 weights: x rows (BF16 values) are quantised per row,
+    g = x W_g^T and u = x W_u^T on the dequantised operands (FP64),
+    a = bf16(silu(g) * u) quantised per row, y = a W_d^T (FP64).
+    gate_q, up_q: (codes [I,H], scale [I]); down_q: (codes [H,I], scale [H])."""
+    qx, sx = quantize_rows_e4m3(x_rows)
+    xd = dequantize_rows_e4m3(qx, sx)
+    g = xd @ dequantize_rows_e4m3(*gate_q).T
+    u = xd @ dequantize_rows_e4m3(*up_q).T
+    a = bf16_round(silu(g) * u)
+    qa, sa = quantize_rows_e4m3(a)
+    return dequantize_rows_e4m3(qa, sa) @ dequantize_rows_e4m3(*down_q).T
+
+
+def moe_forward_fp8(x_in, w_router, bias, get_expert_q, *, n_group=8, topk_group=4,
+                    top_k=8, scale=2.5, eps=1e-6, pre_norm=False, pre_gain=None,
+                    residual_k=0, post_gain=None, routing: Optional[dict] = None) -> dict:
+    """The MoE sublayer with FP8 expert weights: routing as in moe_forward
+    (unquantised router), each selected expert through swiglu_expert_fp8,
+    combine, post-norm and residual as in moe_forward.
+    get_expert_q(e) -> (gate_q, up_q, down_q), each (codes, row scales)."""
+    x_in = np.asarray(x_in, dtype=F64)
+    x = bf16_round(rms_norm(x_in, pre_gain, eps)).astype(F64) if pre_norm else x_in
+    sel = route(x, w_router, bias, n_group, topk_group, top_k, scale)
+    use = routing if routing is not None else sel
+    idx = np.asarray(use["idx"])
+    T = x.shape[0]
+    out = np.zeros((T, x.shape[1]), dtype=F64)
+    for e in np.unique(idx):
+        tok, slot = np.nonzero(idx == e)
+        y = swiglu_expert_fp8(x[tok], *get_expert_q(int(e)))
+        out[tok] += np.asarray(use["weights"], dtype=F64)[tok, slot][:, None] * y
+    h = residual_step(x_in, out, residual_k, post_gain, eps, True) if residual_k else None
+    return dict(x=x, sel=sel, out=out, h=h)

@@ -1,0 +1,153 @@
+"""Pins for the oracle's FP8 (E4M3) expert-weight path, each against
+something other than the oracle itself: torch's float8_e4m3fn type (an
+independent implementation of the same format), hand-derived grid values and
+ties, a hand-computed one-expert case whose operands are exactly
+representable, and properties of the format. No GPU needed.
+"""
+import math
+
+import numpy as np
+import torch
+
+import oracle as O
+
+
+def test_decode_all_codes_matches_torch():
+    c = np.arange(256, dtype=np.uint8)
+    got = O.e4m3_decode(c)
+    ref = torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.isnan(got).sum() == 2                      # 0x7F and 0xFF only
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert O.e4m3_decode(np.uint8(0x7E)) == 448.0        # largest finite
+    assert O.e4m3_decode(np.uint8(0x01)) == 2.0 ** -9    # smallest subnormal
+    assert O.e4m3_decode(np.uint8(0x08)) == 2.0 ** -6    # smallest normal
+    assert O.e4m3_decode(np.uint8(0x38)) == 1.0          # exponent field 7 = bias
+
+
+def test_encode_round_trips_every_finite_code():
+    c = np.arange(256, dtype=np.uint8)
+    v = O.e4m3_decode(c)
+    ok = ~np.isnan(v)
+    assert np.array_equal(O.e4m3_encode(v[ok]), c[ok])   # includes -0.0 -> 0x80
+
+
+def test_round_matches_torch_in_range():
+    g = torch.Generator().manual_seed(3)
+    v = torch.randn(200000, generator=g) * torch.exp(torch.empty(200000).uniform_(-14, 6, generator=g))
+    v = v.clamp(-448, 448)
+    ref = v.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3_round(v.numpy()), ref)
+
+
+def test_round_ties_go_to_even_at_every_midpoint():
+    grid = O.e4m3_decode(np.arange(0x00, 0x7F, dtype=np.uint8))   # 0 .. 448, ascending
+    mids = (grid[:-1] + grid[1:]) / 2                             # exact in float32
+    got = O.e4m3_round(mids.astype(np.float32))
+    ref = torch.from_numpy(mids.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(got, ref)
+    codes = O.e4m3_encode(got)
+    assert np.all((codes & 1) == 0)                               # even mantissa
+
+
+def test_round_hand_values():
+    cases = {
+        2.0 ** -10: 0.0,              # half the smallest subnormal: tie to 0
+        3 * 2.0 ** -10: 2.0 ** -8,    # between 1 and 2 units of 2^-9: tie to 2
+        1.0625: 1.0,                  # between 1 and 1.125: tie to mantissa 0
+        1.1875: 1.25,                 # between 1.125 and 1.25: tie to mantissa 2
+        240.0: 240.0,                 # 1.875 * 2^7, exact
+        447.0: 448.0,
+        460.0: 448.0,
+        500.0: 448.0,                 # saturates (torch's conversion gives NaN here)
+        1e6: 448.0,
+        -1e6: -448.0,
+        -0.3: -0.3125,                # 1.25 * 2^-2
+    }
+    for v, want in cases.items():
+        assert O.e4m3_round(np.float32(v)) == want, v
+
+
+def test_quantize_rows_against_torch_steps():
+    # the same definition carried out with torch's FP32 arithmetic and its
+    # float8 conversion (clamped first: torch maps overflow to NaN)
+    g = torch.Generator().manual_seed(5)
+    a = (torch.randn(64, 320, generator=g) * torch.exp(torch.randn(64, 1, generator=g) * 3))
+    a = a.to(torch.bfloat16).float()
+    a[7] = 0.0
+    codes, scale = O.quantize_rows_e4m3(a.numpy())
+    amax = a.abs().amax(dim=1)
+    nz = amax > 0
+    inv = torch.where(nz, torch.tensor(448.0) / torch.where(nz, amax, torch.ones_like(amax)), torch.ones_like(amax))
+    sc = torch.where(nz, amax / torch.tensor(448.0), torch.ones_like(amax))
+    q = (a * inv[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn)
+    assert np.array_equal(codes, q.view(torch.uint8).numpy())
+    assert np.array_equal(scale, sc.numpy())
+    assert np.all(codes[7] == 0) and scale[7] == 1.0
+
+
+def test_quantize_rows_properties():
+    g = np.random.default_rng(11)
+    a = (g.standard_normal((32, 512)) * 0.02).astype(np.float32)
+    codes, scale = O.quantize_rows_e4m3(a)
+    vals = O.e4m3_decode(codes)
+    # the row's largest magnitude lands on +-448
+    j = np.argmax(np.abs(a), axis=1)
+    assert np.all(np.abs(vals[np.arange(32), j]) == 448.0)
+    # dequantised within half a grid step: relative 2^-4 for normal values,
+    # absolute 2^-10 * scale in the subnormal range
+    deq = O.dequantize_rows_e4m3(codes, scale)
+    err = np.abs(deq - a)
+    bound = np.maximum(np.abs(a) * 2.0 ** -4, scale[:, None].astype(np.float64) * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(err <= bound)
+    assert np.all(np.sign(deq) * np.sign(a) >= 0)
+
+
+def test_fp8_expert_hand_case():
+    # H = 2, I = 1; every operand is exact in E4M3 with power-of-two scales
+    x = np.array([[0.5, 1.75]])                 # amax 1.75: inv 256, codes 128, 448
+    wg = np.array([[0.875, -0.4375]])           # amax 0.875: inv 512, codes 448, -224
+    wu = np.array([[1.75, 0.875]])              # inv 256: codes 448, 224
+    wd = np.array([[0.875], [1.75]])            # one element per row: code 448
+    qg, qu, qd = (O.quantize_rows_e4m3(w) for w in (wg, wu, wd))
+    assert np.array_equal(O.dequantize_rows_e4m3(*qg), wg)
+    assert np.array_equal(O.dequantize_rows_e4m3(*qd), wd)
+    y = O.swiglu_expert_fp8(x, qg, qu, qd)
+    g = 0.5 * 0.875 - 1.75 * 0.4375             # -0.328125
+    u = 0.5 * 1.75 + 1.75 * 0.875               # 2.40625
+    a = g / (1 + math.exp(-g)) * u
+    a_bf16 = float(torch.tensor(a, dtype=torch.float32).to(torch.bfloat16).float())
+    # A has one element: it quantises to -448 with scale fp32(|a|/448)
+    want = a_bf16 * np.array([0.875, 1.75])
+    assert np.allclose(y[0], want, rtol=2 ** -22, atol=0)
+    assert not np.allclose(y[0], a * np.array([0.875, 1.75]), rtol=1e-4, atol=0)   # BF16 step matters
+
+
+def test_fp8_forward_close_to_bf16_forward():
+    # FP8 weights and activations stay within E4M3's relative precision of
+    # the unquantised sublayer (a wrong scale or operand would be far off)
+    g = np.random.default_rng(2)
+    T, H, I, E = 12, 256, 128, 32
+    x = O.bf16_round(g.standard_normal((T, H))).astype(np.float64)
+    wr = g.standard_normal((E, H)) * 0.05
+    W = [(O.bf16_round(g.standard_normal((I, H)) * 0.02).astype(np.float64),
+          O.bf16_round(g.standard_normal((I, H)) * 0.02).astype(np.float64),
+          O.bf16_round(g.standard_normal((H, I)) * 0.02).astype(np.float64)) for _ in range(E)]
+    Q = [tuple(O.quantize_rows_e4m3(w) for w in ws) for ws in W]
+    kw = dict(n_group=4, topk_group=2, top_k=4, scale=2.5)
+    ref = O.moe_forward(x, wr, None, lambda e: W[e], **kw)
+    got = O.moe_forward_fp8(x, wr, None, lambda e: Q[e], **kw)
+    assert np.array_equal(ref["sel"]["idx"], got["sel"]["idx"])      # router unquantised
+    rel = np.sqrt(np.mean((got["out"] - ref["out"]) ** 2)) / np.sqrt(np.mean(ref["out"] ** 2))
+    assert 0.005 < rel < 0.08, rel
+
+
+def test_fp8_checkpoint_counts():
+    # [P5] 四套权重的账: F8_E4M3 + BF16 + F32 counts of the FP8 checkpoint sum
+    # to the model's parameter total, and every routed-expert weight
+    # (49 layers x 256 experts x 3 x 5120 x 2560) fits in the F8 share
+    f8, bf16, f32 = 499_646_464_000, 1_556_910_528, 64_237_824
+    assert f8 + bf16 + f32 == 501_267_612_352
+    experts = 49 * 256 * 3 * 5120 * 2560
+    assert experts == 493_250_150_400 and experts < f8

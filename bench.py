@@ -38,7 +38,6 @@ import beam_synth as S  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at T=64 and T=8192; % of HBM or BF16 tensor roofline"
 RESIDUAL_K = 50
-LAUNCHES_PER_STEP = 10  # prenorm, router x2, hist, scan, scatter, gather, 2 GEMMs, combine
 
 
 def _peaks():
@@ -140,18 +139,21 @@ def _describe(wl):
             f"combine -> post-RMSNorm -> residual k={RESIDUAL_K}")
 
 
-def _algorithmic(wl, counts):
+def _algorithmic(wl, counts, fp8=False):
     """Algorithmic bytes / FLOPs (what the method must move and compute): each
-    touched expert's weights once plus the layer's BF16 input or output; the
-    intermediates (permuted x, SwiGLU activations, per-pair outputs) are not
-    counted."""
+    touched expert's weights once (BF16, or E4M3 codes plus one FP32 scale per
+    row) plus the layer's BF16 input or output; the intermediates (permuted
+    x, SwiGLU activations, per-pair outputs) are not counted."""
     touched = int((counts > 0).sum())
     R = wl.T * wl.top_k
-    gu_bytes = touched * 2 * wl.I * wl.H * 2 + wl.T * wl.H * 2
-    dn_bytes = touched * wl.H * wl.I * 2 + wl.T * wl.H * 2
+    eb = 1 if fp8 else 2
+    sc = 4 if fp8 else 0
+    gu_bytes = touched * 2 * wl.I * (wl.H * eb + sc) + wl.T * wl.H * 2
+    dn_bytes = touched * wl.H * (wl.I * eb + sc) + wl.T * wl.H * 2
     gu_flops = 2.0 * R * 2 * wl.I * wl.H
     dn_flops = 2.0 * R * wl.I * wl.H
-    layer_bytes = touched * 3 * wl.I * wl.H * 2 + 2 * wl.T * wl.H * 2 + wl.E * wl.H * 4
+    layer_bytes = (touched * (3 * wl.I * wl.H * eb + (2 * wl.I + wl.H) * sc)
+                   + 2 * wl.T * wl.H * 2 + wl.E * wl.H * 4)
     return dict(touched=touched, gu_bytes=gu_bytes, dn_bytes=dn_bytes, gu_flops=gu_flops,
                 dn_flops=dn_flops, layer_bytes=layer_bytes,
                 layer_flops=gu_flops + dn_flops + 2.0 * wl.T * wl.H * wl.E)
@@ -180,7 +182,9 @@ def _traffic_for(kernel, workload):
 
 
 # ------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
+def run_ours(args, rank, world, local_rank, fp8=False):
+    """The sublayer with BF16 expert weights, or (fp8) E4M3 expert weights
+    quantised once on the device before any timing."""
     import sparse_moe_transformer_limited_b300 as B
     B.lib()
     dev = torch.device("cuda", local_rank)
@@ -188,15 +192,28 @@ def run_ours(args, rank, world, local_rank):
     wl = _workload(args.config)
     wl_rank = wl.replace(seed=wl.seed + 1000 * rank) if rank else wl
     d = S.make_inputs(wl_rank, dev)
+    flags = B.FLAG_PRE_NORM | (B.FLAG_FP8_EXPERTS if fp8 else 0)
     p = B.make_params(wl.T, wl.H, wl.E, wl.I, wl.n_group, wl.topk_group, wl.top_k,
-                      wl.routed_scale, wl.rms_eps, RESIDUAL_K, B.FLAG_PRE_NORM)
+                      wl.routed_scale, wl.rms_eps, RESIDUAL_K, flags)
     ws = B.alloc_workspace(p, dev)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if fp8:
+        q = tuple(B.quantize_e4m3_rows(d[k]) for k in ("w_gate", "w_up", "w_down"))
+        for k in ("w_gate", "w_up", "w_down"):
+            d[k] = None
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+
+    def fwd(x_in):
+        if fp8:
+            B.forward_fp8(p, x_in, d["w_router"], *q, bias=d["bias"], out=out, workspace=ws)
+        else:
+            B.forward(p, x_in, d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
+                      bias=d["bias"], out=out, workspace=ws)
 
     def step():
-        B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
-                  bias=d["bias"], out=out, workspace=ws)
+        fwd(d["x"])
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -238,8 +255,7 @@ def run_ours(args, rank, world, local_rank):
 
     def e2e_step():
         x_dev.copy_(h_host, non_blocking=True)
-        B.forward(p, x_dev, d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
-                  bias=d["bias"], out=out, workspace=ws)
+        fwd(x_dev)
         o_host.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -257,8 +273,13 @@ def run_ours(args, rank, world, local_rank):
     value = weak_scaling_value(world, wl.T, args.steps, ms_total / 1e3)
     e2e_value = weak_scaling_value(world, wl.T, args.steps, e2e_s)
 
-    alg = _algorithmic(wl, counts)
+    alg = _algorithmic(wl, counts, fp8)
     peaks = _peaks()
+    if fp8:
+        # E4M3 contraction: the measured BF16 peaks times the nominal
+        # FP8 / BF16 dense ratio (4.5 / 2.25 PFLOP/s)
+        peaks = dict(peaks, bf16=2 * peaks["bf16"], bf16_sustained=2 * peaks["bf16_sustained"],
+                     tensor_note=" x 2 (nominal FP8/BF16 dense ratio)")
     gu_ms = prof["expert_gemm_gateup_swiglu"][0] / prof["expert_gemm_gateup_swiglu"][1]
     dn_ms = prof["expert_gemm_down"][0] / prof["expert_gemm_down"][1]
     decode_like = wl.T * wl.top_k <= 24 * wl.E
@@ -274,7 +295,8 @@ def run_ours(args, rank, world, local_rank):
         achieved = alg["gu_flops"] / (gu_ms / 1e3) / 1e12
         roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
-                "peak_source": peaks["source"] + " bf16_tflops (burst)",
+                "peak_source": peaks["source"] + " bf16_tflops (burst)" + peaks.get("tensor_note", ""),
+                "dtype": "e4m3" if fp8 else "bf16",
                 "frac_of_sustained": round(achieved / peaks["bf16_sustained"], 4),
                 "traffic": _traffic_for(kname, wl.name),
                 "algorithmic_flops_per_launch": alg["gu_flops"], "launch_ms": round(gu_ms, 4)}
@@ -282,8 +304,9 @@ def run_ours(args, rank, world, local_rank):
              "tensor_frac": round(alg["layer_flops"] / (ms_step / 1e3) / 1e12 / peaks["bf16"], 4),
              "touched_experts": alg["touched"], "max_tokens_per_expert": int(counts.max())}
     kernels = {k: round(v[0] / v[1], 4) for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
+    launches = sum(v[1] for v in prof.values())   # the library's launches in the timed region
     return dict(value=value, ms_step=ms_step, e2e=e2e_value, clocks=clk, roofline=roof,
-                layer=layer, kernels_ms=kernels, wl=wl,
+                layer=layer, kernels_ms=kernels, wl=wl, launches=launches,
                 h2d=wl.T * wl.H * 2, d2h=wl.T * wl.H * 2)
 
 
@@ -413,24 +436,30 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------ ncu cases
-def run_ncu_case(kind):
+def run_ncu_case(kind, fp8=False):
     """A small case for profiler captures: the full layer path with the real
     H=5120 / I=2560 shapes but 32 experts (one group, plain top-8), so the
     expert weights take 2.5 GB -- more than the L2, little device memory.
     kind 'decode': T=64 (16 tokens/expert, token tile 32);
     kind 'prefill': T=2048 (512 tokens/expert, token tile 128).
-    Runs four forward calls (pre-norm + residual k=50) and exits."""
+    Runs four forward calls (pre-norm + residual k=50) and exits; fp8: with
+    E4M3 expert weights (quantised first)."""
     import sparse_moe_transformer_limited_b300 as B
     T = 64 if kind == "decode" else 2048
     wl = S.Workload("ncu_" + kind, T=T, E=32, n_group=1, topk_group=1, seed=7)
     d = S.make_inputs(wl, "cuda")
+    flags = B.FLAG_PRE_NORM | (B.FLAG_FP8_EXPERTS if fp8 else 0)
     p = B.make_params(wl.T, wl.H, wl.E, wl.I, wl.n_group, wl.topk_group, wl.top_k,
-                      wl.routed_scale, wl.rms_eps, RESIDUAL_K, B.FLAG_PRE_NORM)
+                      wl.routed_scale, wl.rms_eps, RESIDUAL_K, flags)
     ws = B.alloc_workspace(p)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    q = tuple(B.quantize_e4m3_rows(d[k]) for k in ("w_gate", "w_up", "w_down")) if fp8 else None
     for _ in range(4):
-        B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], out=out,
-                  workspace=ws)
+        if fp8:
+            B.forward_fp8(p, d["x"], d["w_router"], *q, out=out, workspace=ws)
+        else:
+            B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], out=out,
+                      workspace=ws)
     if B.status() != 0:
         raise RuntimeError(B.last_error())
     print(f"ncu case {kind}: ok")
@@ -444,6 +473,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="decode", choices=sorted(S.WORKLOADS) + sorted(DENSE))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--experts", default="bf16", choices=["bf16", "fp8"],
+                    help="expert weight type of the timed sublayer (fp8: E4M3 + row scales)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the secondary T=8192 measurement")
@@ -451,7 +482,7 @@ def main():
                     help="run the small profiler case and exit")
     args = ap.parse_args()
     if args.ncu_case:
-        run_ncu_case(args.ncu_case)
+        run_ncu_case(args.ncu_case, args.experts == "fp8")
         return
 
     rank = int(os.environ.get("RANK", 0))
@@ -484,7 +515,8 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
-    r = run_ours(args, rank, world, local_rank)
+    fp8 = args.experts == "fp8"
+    r = run_ours(args, rank, world, local_rank, fp8)
     extra = {}
     if rank == 0 and world == 1 and args.config == "decode" and not args.no_prefill:
         a2 = argparse.Namespace(**vars(args))
@@ -493,12 +525,20 @@ def main():
         r2 = run_ours(a2, rank, world, local_rank)
         torch.cuda.empty_cache()
         extra_dense = run_dense(a2, rank, world, local_rank, "dense_prefill")
-        extra = {"dense_mlp_T8192": extra_dense,
-                 "prefill_T8192": {"value": round(r2["value"], 1), "unit": "tokens/s",
-                                   "ms_per_step": round(r2["ms_step"], 4),
-                                   "e2e": round(r2["e2e"], 1), "roofline": r2["roofline"],
-                                   "layer": r2["layer"], "kernels_ms": r2["kernels_ms"],
-                                   "clocks": r2["clocks"]}}
+        def summary(rr):
+            return {"value": round(rr["value"], 1), "unit": "tokens/s",
+                    "ms_per_step": round(rr["ms_step"], 4), "e2e": round(rr["e2e"], 1),
+                    "roofline": rr["roofline"], "layer": rr["layer"],
+                    "kernels_ms": rr["kernels_ms"], "clocks": rr["clocks"]}
+        extra = {"dense_mlp_T8192": extra_dense, "prefill_T8192": summary(r2)}
+        if not fp8:
+            # the same sublayers with E4M3 expert weights (secondary lines)
+            torch.cuda.empty_cache()
+            a3 = argparse.Namespace(**vars(args))
+            extra["fp8_experts_T64"] = summary(run_ours(a3, rank, world, local_rank, True))
+            torch.cuda.empty_cache()
+            extra["fp8_experts_T8192"] = summary(run_ours(a2, rank, world, local_rank, True))
+            torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         torch.cuda.empty_cache()
@@ -517,7 +557,8 @@ def main():
     line = {"metric": METRIC, "value": round(r["value"], 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": round(r["ms_step"], 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "data": "synthetic",
             "config": {"workload": _describe(wl), "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I,
                        "top_k": wl.top_k, "seed": wl.seed,
                        "parallelism": "replicas" if world > 1 else "single GPU",
@@ -526,7 +567,7 @@ def main():
             "clocks": r["clocks"],
             "e2e": {"value": round(r["e2e"], 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "gpu_launches": r["launches"],
             "cpu_baseline": cpu}
     line.update(extra)
     print(json.dumps(line), flush=True)

@@ -55,6 +55,9 @@ typedef enum {
 #define BEAM_FLAG_PRE_NORM 1      /* input is h_{k-1}; RMSNorm it (FP32) into BF16 x first */
 #define BEAM_FLAG_FP32_OUT 2      /* `out` is FP32 (only without the residual step) */
 #define BEAM_FLAG_RETURN_SCORES 4 /* beam_moe_route also writes the sigmoid scores */
+#define BEAM_FLAG_FP8_EXPERTS 8   /* workspace also holds the E4M3 activations of the
+                                     FP8 expert path (beam_moe_forward_fp8 and
+                                     beam_dense_mlp_forward_fp8 require this bit) */
 
 /* Shape and hyper-parameters of one MoE sublayer call.
  *   T           tokens in the batch (0 is allowed: nothing is enqueued)
@@ -141,7 +144,7 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in,
  *   T, H, I     tokens, hidden (multiple of 128, at most 8192), intermediate
  *               (multiple of 128)
  *   rms_eps, residual_k, flags  as in beam_moe_params (flags: PRE_NORM,
- *               FP32_OUT)
+ *               FP32_OUT, FP8_EXPERTS)
  */
 typedef struct {
   int T, H, I;
@@ -152,6 +155,12 @@ typedef struct {
 
 /* Workspace bytes for beam_dense_mlp_forward (0 on invalid parameters). */
 size_t beam_dense_workspace_size(const beam_dense_params* p);
+
+/* Byte offsets of the dense MLP's workspace buffers, in the order and with
+ * the meaning of beam_moe_workspace_layout (one expert, top_k = 1). Writes
+ * min(n, 22) entries and returns how many it wrote (0 on invalid
+ * parameters). Diagnostic. */
+int beam_dense_workspace_layout(const beam_dense_params* p, size_t* offsets, int n);
 
 /*   x = BEAM_FLAG_PRE_NORM ? bf16(RMSNorm(x_in) * pre_gain) : x_in
  *   y = (silu(x W_gate^T) * (x W_up^T)) W_down^T  (BF16 operands, FP32
@@ -165,6 +174,66 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_params* p, const void* x_i
                                      const void* w_gate, const void* w_up, const void* w_down,
                                      const float* pre_gain, const float* post_gain, void* out,
                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * FP8 (E4M3) expert weights.
+ * [P5] section 四套权重的账，自己算一遍: the FP8 checkpoint stores every linear
+ * weight except lm_head, the embedding and the router ("mlp.gate") as
+ * F8_E4M3, a dynamic FP8 quantisation; [P1] 专家混合模型 lists the FP8
+ * checkpoint beside the BF16 one. The pages fix neither the scale
+ * granularity nor the rounding; this library takes one FP32 scale per row:
+ *   amax = max_j |v_j|;  scale = amax / 448;  inv = 448 / amax  (FP32 IEEE
+ *   division; scale = inv = 1 for an all-zero row)
+ *   code_j = E4M3(v_j * inv)  (FP32 product, round to nearest even, saturate
+ *                              at +-448; E4M3 = OCP E4M3FN: bias 7,
+ *                              subnormals, no infinities)
+ * and dequantises a row as E4M3 value * scale. Weights carry one scale per
+ * output row (static); activations are quantised per row at run time.
+ * ------------------------------------------------------------------------- */
+
+/* Row quantiser: q[r,:] = E4M3 codes of src[r,:], scale[r] as above.
+ *   src    [rows, K] bf16 (device);  q [rows, K] uint8 out;  scale [rows] fp32 out
+ *   K      multiple of 16; rows >= 0 (0: nothing is enqueued)
+ * Used once to quantise expert weights: for W_gate / W_up [E,I,H] call it
+ * with rows = E*I, K = H; for W_down [E,H,I] with rows = E*H, K = I. */
+beam_status_t beam_quantize_e4m3_rows(const void* src, long long rows, int K, void* q,
+                                      float* scale, void* stream);
+
+/* The MoE sublayer with E4M3 expert weights. As beam_moe_forward except:
+ *   x (BF16, after the optional pre-norm) is quantised per token;
+ *   g = (sx q_x) . (s_g q_g)^T, u likewise, on the E4M3 tensor cores with FP32
+ *   accumulation, the scales applied to the FP32 accumulators;
+ *   A = bf16(silu(g) * u) is quantised per (token, expert) row;
+ *   y_e = (sa q_A) . (s_d q_d)^T; combine, post-norm and residual as in
+ *   beam_moe_forward. The router is unquantised (FP32 weight, FP32 scores).
+ * Arguments as beam_moe_forward, with each expert weight given as codes and
+ * row scales:
+ *   wq_gate, wq_up [E,I,H] uint8;  ws_gate, ws_up [E*I] fp32
+ *   wq_down [E,H,I] uint8;         ws_down [E*H] fp32
+ * p->flags must include BEAM_FLAG_FP8_EXPERTS (and the workspace must be
+ * sized with it). */
+beam_status_t beam_moe_forward_fp8(const beam_moe_params* p, const void* x_in,
+                                   const float* w_router, const float* logit_bias,
+                                   const void* wq_gate, const float* ws_gate,
+                                   const void* wq_up, const float* ws_up,
+                                   const void* wq_down, const float* ws_down,
+                                   const float* pre_gain, const float* post_gain, void* out,
+                                   int32_t* topk_idx, float* topk_w, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* The dense SwiGLU MLP with E4M3 weights (the FP8 checkpoint quantises the
+ * dense layers too): as beam_dense_mlp_forward with x quantised per token
+ * and A per token, as in beam_moe_forward_fp8.
+ *   wq_gate, wq_up [I,H] uint8, ws_gate, ws_up [I] fp32;
+ *   wq_down [H,I] uint8, ws_down [H] fp32.
+ * p->flags must include BEAM_FLAG_FP8_EXPERTS. */
+beam_status_t beam_dense_mlp_forward_fp8(const beam_dense_params* p, const void* x_in,
+                                         const void* wq_gate, const float* ws_gate,
+                                         const void* wq_up, const float* ws_up,
+                                         const void* wq_down, const float* ws_down,
+                                         const float* pre_gain, const float* post_gain,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream);
 
 /* One scaled residual update ([P1] 残差流):
  *   h_out = bf16( sqrt((k-1)/k) * h_prev + (1/sqrt(k)) * n ),
@@ -234,9 +303,12 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
  * expert outputs [T*top_k,H] fp32, 11 unit counts [4] int32, 12 per-block
  * expert histograms, 13 per-block expert offsets, 14 gate/up work list,
  * 15 down work list, 16 pair -> row map [T*top_k] int32, 17 the router
- * weight split into three BF16 pieces [E, 3H] and 18 the router GEMM's work
- * list (tensor-core router only). Writes min(n, 19) entries and returns how
- * many it wrote (0 on invalid parameters). */
+ * weight split into three BF16 pieces [E, 3H], 18 the router GEMM's work
+ * list (tensor-core router only), and with BEAM_FLAG_FP8_EXPERTS: 19 per-row
+ * scales of the quantised x [T*top_k] fp32 (the quantised x itself occupies
+ * entry 8), 20 E4M3 activations [T*top_k,I] uint8, 21 their row scales
+ * [T*top_k] fp32. Writes min(n, 22) entries and returns how many it wrote
+ * (0 on invalid parameters). */
 int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n);
 
 /* Launches one block whose single thread waits on a shared-memory barrier

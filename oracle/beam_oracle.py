@@ -360,15 +360,25 @@ def e4m3_encode(v) -> np.ndarray:
     return sign | (expo.astype(np.uint8) << np.uint8(3)) | mant.astype(np.uint8)
 
 
-def e4m3_decode(codes) -> np.ndarray:
-    """Values of E4M3 byte codes as float64 (NaN for S.1111.111)."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+def _e4m3_value(c: np.ndarray) -> np.ndarray:
+    """Value of each E4M3 byte code (int64 array): sign bit 7, exponent bits
+    3..6 (bias 7; 0 = subnormal, m * 2^-9), mantissa bits 0..2; S.1111.111
+    is NaN."""
     s = np.where(c & 0x80, -1.0, 1.0)
     e = (c >> 3) & 0xF
     m = c & 0x7
     val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
     val = np.where((e == 15) & (m == 7), np.nan, val)
     return s * val
+
+
+_E4M3_TABLE = _e4m3_value(np.arange(256, dtype=np.int64))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of E4M3 byte codes as float64 (NaN for S.1111.111), looked up
+    in the table of all 256 codes' values."""
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
 def quantize_rows_e4m3(a) -> Tuple[np.ndarray, np.ndarray]:
@@ -391,18 +401,40 @@ def dequantize_rows_e4m3(codes, scale) -> np.ndarray:
     return e4m3_decode(codes) * np.asarray(scale, dtype=F64)[..., None]
 
 
-def swiglu_expert_fp8(x_rows, gate_q, up_q, down_q) -> np.ndarray:
-    """One expert on FP8 weights: x rows (BF16 values) are quantised per row,
-    g = x W_g^T and u = x W_u^T on the dequantised operands (FP64),
-    a = bf16(silu(g) * u) quantised per row, y = a W_d^T (FP64).
-    gate_q, up_q: (codes [I,H], scale [I]); down_q: (codes [H,I], scale [H])."""
+def swiglu_act_fp8(x_rows, gate_q, up_q) -> np.ndarray:
+    """SwiGLU activation of an FP8 expert before its BF16 rounding: x rows
+    (BF16 values) quantised per row, g = x W_g^T and u = x W_u^T on the
+    dequantised operands, a = silu(g) * u (FP64).
+    gate_q, up_q: (codes [I,H], scale [I])."""
     qx, sx = quantize_rows_e4m3(x_rows)
     xd = dequantize_rows_e4m3(qx, sx)
     g = xd @ dequantize_rows_e4m3(*gate_q).T
     u = xd @ dequantize_rows_e4m3(*up_q).T
-    a = bf16_round(silu(g) * u)
+    return silu(g) * u
+
+
+def swiglu_expert_fp8(x_rows, gate_q, up_q, down_q) -> np.ndarray:
+    """One expert on FP8 weights: a = swiglu_act_fp8, rounded to BF16 and
+    quantised per row, then y = a W_d^T on the dequantised operands (FP64).
+    down_q: (codes [H,I], scale [H])."""
+    a = bf16_round(swiglu_act_fp8(x_rows, gate_q, up_q))
     qa, sa = quantize_rows_e4m3(a)
     return dequantize_rows_e4m3(qa, sa) @ dequantize_rows_e4m3(*down_q).T
+
+
+def moe_combine_fp8(x: np.ndarray, idx: np.ndarray, weights: np.ndarray,
+                    get_expert_q: Callable[[int], tuple]) -> np.ndarray:
+    """out[t] = sum_j weights[t,j] * f8_{idx[t,j]}(x[t]) with the FP8 experts
+    (swiglu_expert_fp8), expert by expert."""
+    x = np.asarray(x, dtype=F64)
+    out = np.zeros((x.shape[0], x.shape[1]), dtype=F64)
+    idx = np.asarray(idx)
+    weights = np.asarray(weights, dtype=F64)
+    for e in np.unique(idx):
+        tok, slot = np.nonzero(idx == e)
+        y = swiglu_expert_fp8(x[tok], *get_expert_q(int(e)))
+        out[tok] += weights[tok, slot][:, None] * y
+    return out
 
 
 def moe_forward_fp8(x_in, w_router, bias, get_expert_q, *, n_group=8, topk_group=4,
@@ -416,12 +448,6 @@ def moe_forward_fp8(x_in, w_router, bias, get_expert_q, *, n_group=8, topk_group
     x = bf16_round(rms_norm(x_in, pre_gain, eps)).astype(F64) if pre_norm else x_in
     sel = route(x, w_router, bias, n_group, topk_group, top_k, scale)
     use = routing if routing is not None else sel
-    idx = np.asarray(use["idx"])
-    T = x.shape[0]
-    out = np.zeros((T, x.shape[1]), dtype=F64)
-    for e in np.unique(idx):
-        tok, slot = np.nonzero(idx == e)
-        y = swiglu_expert_fp8(x[tok], *get_expert_q(int(e)))
-        out[tok] += np.asarray(use["weights"], dtype=F64)[tok, slot][:, None] * y
+    out = moe_combine_fp8(x, use["idx"], use["weights"], get_expert_q)
     h = residual_step(x_in, out, residual_k, post_gain, eps, True) if residual_k else None
     return dict(x=x, sel=sel, out=out, h=h)

@@ -27,18 +27,21 @@ BEAM_ERR_DEVICE_FLAG = 6
 FLAG_PRE_NORM = 1
 FLAG_FP32_OUT = 2
 FLAG_RETURN_SCORES = 4
+FLAG_FP8_EXPERTS = 8
 
 # names of the workspace buffers, in beam_moe_workspace_layout() order
 LAYOUT_NAMES = ("xn", "part", "topk_idx", "topk_w", "counts", "offsets", "row_token",
                 "row_weight", "xperm", "act", "y", "n_units", "blk_hist", "blk_off",
-                "units_gu", "units_dn", "pair_row", "router_w3", "router_units")
+                "units_gu", "units_dn", "pair_row", "router_w3", "router_units",
+                "x_scale", "act_q", "act_scale")
 
 # every symbol include/beam_moe.h declares
 EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static",
             "beam_moe_forward", "beam_dense_workspace_size", "beam_dense_mlp_forward",
             "beam_residual_step", "beam_status", "beam_last_error_string",
             "beam_moe_workspace_layout", "beam_debug_wait_timeout", "beam_profile_enable",
-            "beam_profile_read")
+            "beam_profile_read", "beam_quantize_e4m3_rows", "beam_moe_forward_fp8",
+            "beam_dense_mlp_forward_fp8", "beam_dense_workspace_layout")
 
 
 class BeamError(RuntimeError):
@@ -87,8 +90,16 @@ def lib() -> ctypes.CDLL:
         D = ctypes.POINTER(DenseParams)
         L.beam_dense_workspace_size.argtypes = [D]
         L.beam_dense_workspace_size.restype = sz
+        L.beam_dense_workspace_layout.argtypes = [D, ctypes.POINTER(sz), i32]
+        L.beam_dense_workspace_layout.restype = i32
         L.beam_dense_mlp_forward.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.beam_dense_mlp_forward.restype = i32
+        L.beam_quantize_e4m3_rows.argtypes = [vp, ctypes.c_longlong, i32, vp, vp, vp]
+        L.beam_quantize_e4m3_rows.restype = i32
+        L.beam_moe_forward_fp8.argtypes = [P] + [vp] * 15 + [sz, vp]
+        L.beam_moe_forward_fp8.restype = i32
+        L.beam_dense_mlp_forward_fp8.argtypes = [D] + [vp] * 11 + [sz, vp]
+        L.beam_dense_mlp_forward_fp8.restype = i32
         L.beam_residual_step.argtypes = [vp, vp, i32, i32, i32, vp, f32, i32, i32, vp, vp]
         L.beam_residual_step.restype = i32
         L.beam_status.argtypes = [vp]
@@ -142,6 +153,21 @@ def workspace_size(p: Params) -> int:
 def workspace_layout(p: Params) -> dict:
     arr = (ctypes.c_size_t * len(LAYOUT_NAMES))()
     n = lib().beam_moe_workspace_layout(ctypes.byref(p), arr, len(LAYOUT_NAMES))
+    if n == 0:
+        raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
+    return {LAYOUT_NAMES[i]: int(arr[i]) for i in range(n)}
+
+
+def dense_workspace_size(p: DenseParams) -> int:
+    n = lib().beam_dense_workspace_size(ctypes.byref(p))
+    if n == 0:
+        raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
+    return int(n)
+
+
+def dense_workspace_layout(p: DenseParams) -> dict:
+    arr = (ctypes.c_size_t * len(LAYOUT_NAMES))()
+    n = lib().beam_dense_workspace_layout(ctypes.byref(p), arr, len(LAYOUT_NAMES))
     if n == 0:
         raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
     return {LAYOUT_NAMES[i]: int(arr[i]) for i in range(n)}
@@ -208,13 +234,58 @@ def dense_forward(T, H, I, x, w_gate, w_up, w_down, pre_gain=None, post_gain=Non
         dt = torch.float32 if (flags & FLAG_FP32_OUT) else torch.bfloat16
         out = torch.empty((T, H), dtype=dt, device=x.device)
     if workspace is None:
-        n = lib().beam_dense_workspace_size(ctypes.byref(p))
-        if n == 0:
-            raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
-        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(dense_workspace_size(p), dtype=torch.uint8, device=x.device)
     _check(lib().beam_dense_mlp_forward(ctypes.byref(p), _ptr(x), _ptr(w_gate), _ptr(w_up),
                                         _ptr(w_down), _ptr(pre_gain), _ptr(post_gain), _ptr(out),
                                         _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def quantize_e4m3_rows(w, stream=None):
+    """beam_quantize_e4m3_rows over the last dimension of a bf16 tensor:
+    returns (codes uint8 of w's shape, row scales fp32 of w.shape[:-1])."""
+    K = w.shape[-1]
+    rows = w.numel() // K if K else 0
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _check(lib().beam_quantize_e4m3_rows(_ptr(w), rows, K, _ptr(q), _ptr(sc), _stream(stream)))
+    return q, sc
+
+
+def forward_fp8(p: Params, x, w_router, gate_q, up_q, down_q, bias=None, pre_gain=None,
+                post_gain=None, out=None, topk_idx=None, topk_w=None, workspace=None,
+                stream=None):
+    """beam_moe_forward_fp8; gate_q, up_q, down_q are (codes, row scales)
+    pairs as quantize_e4m3_rows returns them. p.flags must hold
+    FLAG_FP8_EXPERTS."""
+    dev = x.device
+    if out is None:
+        dt = torch.float32 if (p.flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((p.T, p.H), dtype=dt, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(p, dev)
+    _check(lib().beam_moe_forward_fp8(
+        ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(gate_q[0]), _ptr(gate_q[1]),
+        _ptr(up_q[0]), _ptr(up_q[1]), _ptr(down_q[0]), _ptr(down_q[1]), _ptr(pre_gain),
+        _ptr(post_gain), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return out
+
+
+def dense_forward_fp8(T, H, I, x, gate_q, up_q, down_q, pre_gain=None, post_gain=None,
+                      rms_eps=1e-6, residual_k=0, flags=FLAG_FP8_EXPERTS, out=None,
+                      workspace=None, stream=None):
+    """beam_dense_mlp_forward_fp8; weights as (codes, row scales) pairs."""
+    p = DenseParams(T, H, I, rms_eps, residual_k, flags)
+    if out is None:
+        dt = torch.float32 if (flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((T, H), dtype=dt, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(dense_workspace_size(p), dtype=torch.uint8, device=x.device)
+    _check(lib().beam_dense_mlp_forward_fp8(
+        ctypes.byref(p), _ptr(x), _ptr(gate_q[0]), _ptr(gate_q[1]), _ptr(up_q[0]),
+        _ptr(up_q[1]), _ptr(down_q[0]), _ptr(down_q[1]), _ptr(pre_gain), _ptr(post_gain),
+        _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

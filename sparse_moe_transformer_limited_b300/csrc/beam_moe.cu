@@ -19,6 +19,7 @@
 #include "kernels_gemm_tm.cuh"
 #include "kernels_gemm_2sm.cuh"
 #include "kernels_permute.cuh"
+#include "kernels_quant.cuh"
 #include "kernels_router.cuh"
 #include "kernels_rows.cuh"
 
@@ -148,7 +149,7 @@ int choose_router_ks(const beam_moe_params& p, int num_sms) {
   return best;
 }
 
-constexpr int kLayoutEntries = 19;
+constexpr int kLayoutEntries = 22;
 
 struct Layout {
   size_t off[kLayoutEntries];
@@ -160,7 +161,8 @@ struct Layout {
 
 enum {
   L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_Y,
-  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW, L_WR3, L_RUNITS
+  L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW, L_WR3, L_RUNITS,
+  L_XSCALE, L_ACTQ, L_ASCALE
 };
 
 // Bytes of the router's unit list and count (tensor-core router only).
@@ -207,7 +209,8 @@ beam_status_t check_params(const beam_moe_params* p) {
     return fail(BEAM_ERR_INVALID_ARG, "rms_eps must be >= 0 and finite");
   if (p->residual_k == 1 || p->residual_k < 0)
     return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", p->residual_k);
-  if (p->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_RETURN_SCORES))
+  if (p->flags &
+      ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_RETURN_SCORES | BEAM_FLAG_FP8_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
   if ((p->flags & BEAM_FLAG_FP32_OUT) && p->residual_k >= 2)
     return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP32_OUT applies only without the residual step");
@@ -262,6 +265,10 @@ Layout make_layout(const beam_moe_params& p) {
   sz[L_PAIRROW] = static_cast<size_t>(R) * 4;
   sz[L_WR3] = router_on_tensor_cores(p) ? static_cast<size_t>(p.E) * 3 * p.H * 2 : 0;
   sz[L_RUNITS] = router_on_tensor_cores(p) ? router_units_bytes(p) : 0;
+  const bool f8 = (p.flags & BEAM_FLAG_FP8_EXPERTS) != 0;
+  sz[L_XSCALE] = f8 ? static_cast<size_t>(R) * 4 : 0;
+  sz[L_ACTQ] = f8 ? static_cast<size_t>(R) * p.I : 0;
+  sz[L_ASCALE] = f8 ? static_cast<size_t>(R) * 4 : 0;
   size_t cur = 0;
   for (int i = 0; i < kLayoutEntries; ++i) {
     L.off[i] = cur;
@@ -294,17 +301,19 @@ PFN_encodeTiled_t encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] -> TMA map with box {64 cols, box_rows}
-// and the 128-byte swizzle (one box row = 128 bytes).
+// Row-major matrix [rows, cols] of bf16 (f8 = false) or one-byte E4M3 codes
+// (f8 = true) -> TMA map with a box of one 128-byte row segment (64 bf16 or
+// 128 codes) x box_rows rows and the 128-byte swizzle.
 beam_status_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                       uint32_t box_rows) {
+                       uint32_t box_rows, bool f8 = false) {
   PFN_encodeTiled_t fn = encode_fn();
   if (fn == nullptr) return fail(BEAM_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t strides[1] = {cols * (f8 ? 1 : 2)};
+  cuuint32_t box[2] = {f8 ? 128u : 64u, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -315,11 +324,11 @@ beam_status_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 }
 
 // --------------------------------------------------------- GEMM launches
-template <int MODE, int NT, int STAGES>
+template <int MODE, int NT, int STAGES, bool F8>
 beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                           const beam::GemmArgs& args, cudaStream_t st) {
   using C = beam::GemmCfg<MODE, NT, STAGES>;
-  auto kern = beam::expert_gemm_kernel<MODE, NT, STAGES>;
+  auto kern = beam::expert_gemm_kernel<MODE, NT, STAGES, F8>;
   static bool attr_set = false;  // per template instance
   if (!attr_set) {
     BEAM_CUDA_TRY(
@@ -332,12 +341,12 @@ beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   return BEAM_OK;
 }
 
-template <int MODE>
+template <int MODE, bool F8>
 beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& tok,
                                const CUtensorMap& tok64, const beam::PairArgs& args,
                                cudaStream_t st, const char* prof_name = nullptr) {
   using C = beam::PairCfg;
-  auto kern = beam::expert_gemm_pair_kernel<MODE>;
+  auto kern = beam::expert_gemm_pair_kernel<MODE, F8>;
   static bool attr_set = false;
   if (!attr_set) {
     BEAM_CUDA_TRY(
@@ -352,11 +361,11 @@ beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, con
   return BEAM_OK;
 }
 
-template <int MODE>
+template <int MODE, bool F8>
 beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& tok,
                              const beam::TmArgs& args, cudaStream_t st) {
   using C = beam::TmCfg;
-  auto kern = beam::expert_gemm_tm_kernel<MODE>;
+  auto kern = beam::expert_gemm_tm_kernel<MODE, F8>;
   static bool attr_set = false;
   if (!attr_set) {
     BEAM_CUDA_TRY(
@@ -414,7 +423,7 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
     ra.b_k_wrap = p.H / 64;
     ra.y_split = static_cast<size_t>(p.T) * p.E;
     ra.timeout_ns = kWaitTimeoutNs;
-    if ((s = launch_gemm_pair<1>(m_w, m_w, m_x, m_x64, ra, st, "router_logits_tc")) != BEAM_OK)
+    if ((s = launch_gemm_pair<1, false>(m_w, m_w, m_x, m_x64, ra, st, "router_logits_tc")) != BEAM_OK)
       return s;
   } else {
     dim3 g1((p.T + beam::RL_BT - 1) / beam::RL_BT, (p.E + beam::RL_BE - 1) / beam::RL_BE, L.KS);
@@ -445,6 +454,166 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
   return BEAM_OK;
 }
 
+// The expert weights of one call: BF16 matrices, or E4M3 codes with one FP32
+// scale per output row.
+struct ExpertWeights {
+  const void* gate;
+  const void* up;
+  const void* down;
+  const float* s_gate;  // E4M3 only
+  const float* s_up;
+  const float* s_down;
+  bool f8;
+};
+
+// Steps 3-4: gate/up GEMM + SwiGLU into act (bf16), then the down GEMM into
+// the per-pair FP32 outputs y. F8: the expert-ordered x (xop) and the
+// weights are E4M3 with row scales; act is quantised per row into aq before
+// the down GEMM.
+template <bool F8>
+beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
+                                  const ExpertWeights& w, const void* xop, const float* xscale,
+                                  __nv_bfloat16* act, uint8_t* aq, float* ascale, float* y,
+                                  int4* ugu, int4* udn, int* nunits, long long R,
+                                  cudaStream_t st) {
+  beam_status_t s = BEAM_OK;
+  const int H = prm.H, E = prm.E, I = prm.I;
+  const int KB = beam::KBlock<F8>::ELEMS;
+  // operand of the down GEMM: the bf16 act, or its E4M3 codes
+  const void* aop = F8 ? static_cast<const void*>(aq) : static_cast<const void*>(act);
+  const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
+  const uint32_t gu_box = L.path == PATH_PAIR ? 64 : 128;
+  CUtensorMap m_g, m_u, m_d, m_x, m_a;
+  if ((s = make_map(&m_g, w.gate, static_cast<uint64_t>(E) * I, H, gu_box, F8)) != BEAM_OK) return s;
+  if ((s = make_map(&m_u, w.up, static_cast<uint64_t>(E) * I, H, gu_box, F8)) != BEAM_OK) return s;
+  if ((s = make_map(&m_d, w.down, static_cast<uint64_t>(E) * H, I, 128, F8)) != BEAM_OK) return s;
+  if ((s = make_map(&m_x, xop, R, H, tok_box, F8)) != BEAM_OK) return s;
+  if ((s = make_map(&m_a, aop, R, I, tok_box, F8)) != BEAM_OK) return s;
+
+  // E4M3: SwiGLU output -> per-row codes and scales (between the two GEMMs)
+  auto quant_act = [&]() -> beam_status_t {
+    if (!F8) return BEAM_OK;
+    {
+      ProfScope ps("quant_act", st);
+      beam::quant_rows_e4m3_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+          act, nullptr, R, I, aq, ascale);
+    }
+    BEAM_LAUNCH_CHECK("quant_rows_e4m3_kernel<act>");
+    return BEAM_OK;
+  };
+
+  if (L.path == PATH_PAIR || L.path == PATH_MIXED) {
+    beam::PairArgs pa{};
+    pa.units = ugu;
+    pa.n_units = nunits + 0;
+    pa.k_blocks = H / KB;
+    pa.w_rows_per_expert = I;
+    pa.act = act;
+    pa.out_ld = I;
+    pa.timeout_ns = kWaitTimeoutNs;
+    pa.row_scale = xscale;
+    pa.w_scale0 = w.s_gate;
+    pa.w_scale1 = w.s_up;
+    beam::PairArgs pd = pa;
+    pd.units = udn;
+    pd.n_units = nunits + 1;
+    pd.k_blocks = I / KB;
+    pd.w_rows_per_expert = H;
+    pd.act = nullptr;
+    pd.y = y;
+    pd.out_ld = H;
+    pd.row_scale = ascale;
+    pd.w_scale0 = w.s_down;
+    pd.w_scale1 = nullptr;
+    CUtensorMap m_x64, m_a64;
+    if ((s = make_map(&m_x64, xop, R, H, 64, F8)) != BEAM_OK) return s;
+    if ((s = make_map(&m_a64, aop, R, I, 64, F8)) != BEAM_OK) return s;
+    if (L.path == PATH_MIXED) {
+      // gate/up on the token-major multicast kernel (128-row boxes)
+      CUtensorMap m_g128, m_u128, m_x128;
+      if ((s = make_map(&m_g128, w.gate, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
+      if ((s = make_map(&m_u128, w.up, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
+      if ((s = make_map(&m_x128, xop, R, H, 128, F8)) != BEAM_OK) return s;
+      beam::TmArgs ta{};
+      ta.units = ugu;
+      ta.n_units = nunits + 0;
+      ta.k_blocks = H / KB;
+      ta.w_rows_per_expert = I;
+      ta.out = act;
+      ta.out_ld = I;
+      ta.timeout_ns = kWaitTimeoutNs;
+      ta.row_scale = xscale;
+      ta.w_scale0 = w.s_gate;
+      ta.w_scale1 = w.s_up;
+      if ((s = launch_gemm_tm<0, F8>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK) return s;
+    } else {
+      if ((s = launch_gemm_pair<0, F8>(m_g, m_u, m_x, m_x64, pa, st)) != BEAM_OK) return s;
+    }
+    if ((s = quant_act()) != BEAM_OK) return s;
+    if ((s = launch_gemm_pair<1, F8>(m_d, m_d, m_a, m_a64, pd, st)) != BEAM_OK) return s;
+  } else if (L.path == PATH_TM) {
+    beam::TmArgs ta{};
+    ta.units = ugu;
+    ta.n_units = nunits + 0;
+    ta.k_blocks = H / KB;
+    ta.w_rows_per_expert = I;
+    ta.out = act;
+    ta.out_ld = I;
+    ta.timeout_ns = kWaitTimeoutNs;
+    ta.row_scale = xscale;
+    ta.w_scale0 = w.s_gate;
+    ta.w_scale1 = w.s_up;
+    beam::TmArgs td = ta;
+    td.units = udn;
+    td.n_units = nunits + 1;
+    td.k_blocks = I / KB;
+    td.w_rows_per_expert = H;
+    td.out = nullptr;
+    td.y = y;
+    td.out_ld = H;
+    td.row_scale = ascale;
+    td.w_scale0 = w.s_down;
+    td.w_scale1 = nullptr;
+    if ((s = launch_gemm_tm<0, F8>(m_g, m_u, m_x, ta, st)) != BEAM_OK) return s;
+    if ((s = quant_act()) != BEAM_OK) return s;
+    if ((s = launch_gemm_tm<1, F8>(m_d, m_d, m_a, td, st)) != BEAM_OK) return s;
+  } else {
+    beam::GemmArgs ga{};
+    ga.units = ugu;  // token tiles, shared by both GEMMs
+    ga.n_units = nunits + 0;
+    ga.m_tiles = I / 128;
+    ga.k_blocks = H / KB;
+    ga.a_rows_per_expert = I;
+    ga.out = act;
+    ga.out_ld = I;
+    ga.timeout_ns = kWaitTimeoutNs;
+    ga.row_scale = xscale;
+    ga.w_scale0 = w.s_gate;
+    ga.w_scale1 = w.s_up;
+    beam::GemmArgs gd = ga;
+    gd.n_units = nunits + 1;
+    gd.m_tiles = H / 128;
+    gd.k_blocks = I / KB;
+    gd.a_rows_per_expert = H;
+    gd.out = nullptr;
+    gd.y = y;
+    gd.out_ld = H;
+    gd.row_scale = ascale;
+    gd.w_scale0 = w.s_down;
+    gd.w_scale1 = nullptr;
+    if (L.path == PATH_W32) {
+      if ((s = launch_gemm<0, 32, 6, F8>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+      if ((s = quant_act()) != BEAM_OK) return s;
+      if ((s = launch_gemm<1, 32, 10, F8>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+    } else {
+      if ((s = launch_gemm<0, 128, 4, F8>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+      if ((s = quant_act()) != BEAM_OK) return s;
+      if ((s = launch_gemm<1, 128, 6, F8>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+    }
+  }
+  return BEAM_OK;
+}
+
 // Steps 2-5 of the sublayer, given the routing (idx, wts): permutation and
 // work lists, the expert GEMMs, then the weighted combine with post-norm and
 // residual. With dense = true there is one expert that every token uses with
@@ -452,9 +621,8 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
 // dense_setup_kernel, and the GEMMs read x in place.
 beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const void* x_in,
                           const __nv_bfloat16* x, const int32_t* idx, float* wts,
-                          const void* w_gate, const void* w_up, const void* w_down,
-                          const float* post_gain, void* out, uint8_t* ws, cudaStream_t st,
-                          bool dense) {
+                          const ExpertWeights& w, const float* post_gain, void* out, uint8_t* ws,
+                          cudaStream_t st, bool dense) {
   const beam_moe_params* p = &prm;
   beam_status_t s = BEAM_OK;
   const int T = p->T, H = p->H, E = p->E, I = p->I, K = p->top_k;
@@ -473,6 +641,10 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   int4* ugu = reinterpret_cast<int4*>(ws + L.off[L_UGU]);
   int4* udn = reinterpret_cast<int4*>(ws + L.off[L_UDN]);
   int* nunits = reinterpret_cast<int*>(ws + L.off[L_NUNITS]);
+  // E4M3 path: x codes (in the permuted-x region) and the activations' codes
+  float* xscale = w.f8 ? reinterpret_cast<float*>(ws + L.off[L_XSCALE]) : nullptr;
+  uint8_t* actq = w.f8 ? ws + L.off[L_ACTQ] : nullptr;
+  float* ascale = w.f8 ? reinterpret_cast<float*>(ws + L.off[L_ASCALE]) : nullptr;
 
   const int NB = dense ? 1 : L.NB;
   if (dense) {
@@ -504,7 +676,21 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
                                                         path_mt_down(L.path, H));
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
-  if (dense) {
+  if (w.f8) {
+    // quantise x per token, gathered into expert order (identity when dense)
+    if (!dense) {
+      ProfScope ps("expert_scatter", st);
+      beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(
+          idx, wts, T, K, E, blk_off, pair_row, row_tok, row_w);
+    }
+    BEAM_LAUNCH_CHECK("expert_scatter_kernel");
+    {
+      ProfScope ps("quant_x", st);
+      beam::quant_rows_e4m3_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+          x, dense ? nullptr : row_tok, R, H, ws + L.off[L_XPERM], xscale);
+    }
+    BEAM_LAUNCH_CHECK("quant_rows_e4m3_kernel<x>");
+  } else if (dense) {
     xperm = const_cast<__nv_bfloat16*>(x);  // identity permutation: read x in place
   } else {
     {
@@ -522,99 +708,14 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   }
 
   // 3. gate/up GEMM + SwiGLU -> act, 4. down GEMM -> per-pair y
-  const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
-  const uint32_t gu_box = L.path == PATH_PAIR ? 64 : 128;
-  CUtensorMap m_g, m_u, m_d, m_x, m_a;
-  if ((s = make_map(&m_g, w_gate, static_cast<uint64_t>(E) * I, H, gu_box)) != BEAM_OK) return s;
-  if ((s = make_map(&m_u, w_up, static_cast<uint64_t>(E) * I, H, gu_box)) != BEAM_OK) return s;
-  if ((s = make_map(&m_d, w_down, static_cast<uint64_t>(E) * H, I, 128)) != BEAM_OK) return s;
-  if ((s = make_map(&m_x, xperm, R, H, tok_box)) != BEAM_OK) return s;
-  if ((s = make_map(&m_a, act, R, I, tok_box)) != BEAM_OK) return s;
-
-  if (L.path == PATH_PAIR || L.path == PATH_MIXED) {
-    beam::PairArgs pa{};
-    pa.units = ugu;
-    pa.n_units = nunits + 0;
-    pa.k_blocks = H / 64;
-    pa.w_rows_per_expert = I;
-    pa.act = act;
-    pa.out_ld = I;
-    pa.timeout_ns = kWaitTimeoutNs;
-    beam::PairArgs pd = pa;
-    pd.units = udn;
-    pd.n_units = nunits + 1;
-    pd.k_blocks = I / 64;
-    pd.w_rows_per_expert = H;
-    pd.act = nullptr;
-    pd.y = y;
-    pd.out_ld = H;
-    CUtensorMap m_x64, m_a64;
-    if ((s = make_map(&m_x64, xperm, R, H, 64)) != BEAM_OK) return s;
-    if ((s = make_map(&m_a64, act, R, I, 64)) != BEAM_OK) return s;
-    if (L.path == PATH_MIXED) {
-      // gate/up on the token-major multicast kernel (128-row boxes)
-      CUtensorMap m_g128, m_u128, m_x128;
-      if ((s = make_map(&m_g128, w_gate, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
-      if ((s = make_map(&m_u128, w_up, static_cast<uint64_t>(E) * I, H, 128)) != BEAM_OK) return s;
-      if ((s = make_map(&m_x128, xperm, R, H, 128)) != BEAM_OK) return s;
-      beam::TmArgs ta{};
-      ta.units = ugu;
-      ta.n_units = nunits + 0;
-      ta.k_blocks = H / 64;
-      ta.w_rows_per_expert = I;
-      ta.out = act;
-      ta.out_ld = I;
-      ta.timeout_ns = kWaitTimeoutNs;
-      if ((s = launch_gemm_tm<0>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK) return s;
-    } else {
-      if ((s = launch_gemm_pair<0>(m_g, m_u, m_x, m_x64, pa, st)) != BEAM_OK) return s;
-    }
-    if ((s = launch_gemm_pair<1>(m_d, m_d, m_a, m_a64, pd, st)) != BEAM_OK) return s;
-  } else if (L.path == PATH_TM) {
-    beam::TmArgs ta{};
-    ta.units = ugu;
-    ta.n_units = nunits + 0;
-    ta.k_blocks = H / 64;
-    ta.w_rows_per_expert = I;
-    ta.out = act;
-    ta.out_ld = I;
-    ta.timeout_ns = kWaitTimeoutNs;
-    beam::TmArgs td = ta;
-    td.units = udn;
-    td.n_units = nunits + 1;
-    td.k_blocks = I / 64;
-    td.w_rows_per_expert = H;
-    td.out = nullptr;
-    td.y = y;
-    td.out_ld = H;
-    if ((s = launch_gemm_tm<0>(m_g, m_u, m_x, ta, st)) != BEAM_OK) return s;
-    if ((s = launch_gemm_tm<1>(m_d, m_d, m_a, td, st)) != BEAM_OK) return s;
+  if (w.f8) {
+    s = launch_expert_gemms<true>(*p, L, w, xperm, xscale, act, actq, ascale, y, ugu, udn, nunits,
+                                  R, st);
   } else {
-    beam::GemmArgs ga{};
-    ga.units = ugu;  // token tiles, shared by both GEMMs
-    ga.n_units = nunits + 0;
-    ga.m_tiles = I / 128;
-    ga.k_blocks = H / 64;
-    ga.a_rows_per_expert = I;
-    ga.out = act;
-    ga.out_ld = I;
-    ga.timeout_ns = kWaitTimeoutNs;
-    beam::GemmArgs gd = ga;
-    gd.n_units = nunits + 1;
-    gd.m_tiles = H / 128;
-    gd.k_blocks = I / 64;
-    gd.a_rows_per_expert = H;
-    gd.out = nullptr;
-    gd.y = y;
-    gd.out_ld = H;
-    if (L.path == PATH_W32) {
-      if ((s = launch_gemm<0, 32, 6>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
-      if ((s = launch_gemm<1, 32, 10>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
-    } else {
-      if ((s = launch_gemm<0, 128, 4>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
-      if ((s = launch_gemm<1, 128, 6>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
-    }
+    s = launch_expert_gemms<false>(*p, L, w, xperm, nullptr, act, nullptr, nullptr, y, ugu, udn,
+                                   nunits, R, st);
   }
+  if (s != BEAM_OK) return s;
 
   // 5. weighted combine, then post-norm + scaled residual (or the output)
   const int resid = p->residual_k >= 2;
@@ -678,19 +779,31 @@ beam_status_t beam_moe_route(const beam_moe_params* p, const void* x, const floa
                        static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
-beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const float* w_router,
-                               const float* logit_bias, const void* w_gate, const void* w_up,
-                               const void* w_down, const float* pre_gain, const float* post_gain,
-                               void* out, int32_t* topk_idx, float* topk_w, void* workspace,
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the BF16 and E4M3 forward entry points, then steps 1-5.
+beam_status_t moe_forward_impl(const beam_moe_params* p, const void* x_in, const float* w_router,
+                               const float* logit_bias, const ExpertWeights& w,
+                               const float* pre_gain, const float* post_gain, void* out,
+                               int32_t* topk_idx, float* topk_w, void* workspace,
                                size_t workspace_bytes, void* stream) {
   beam_status_t s = check_params(p);
   if (s != BEAM_OK) return s;
+  if (w.f8 && !(p->flags & BEAM_FLAG_FP8_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG,
+                "the E4M3 path needs BEAM_FLAG_FP8_EXPERTS in flags (and a workspace sized with it)");
   if (p->T == 0) return BEAM_OK;
-  if (!x_in || !w_router || !w_gate || !w_up || !w_down || !out || !workspace)
+  if (!x_in || !w_router || !w.gate || !w.up || !w.down || !out || !workspace)
     return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
-  const void* ptrs[] = {x_in, w_router, w_gate, w_up, w_down, out, workspace};
+  if (w.f8 && (!w.s_gate || !w.s_up || !w.s_down))
+    return fail(BEAM_ERR_INVALID_ARG, "the E4M3 weights need their row scales");
+  const void* ptrs[] = {x_in, w_router, w.gate, w.up, w.down, out, workspace};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
+  if (w.f8 && (!aligned16(w.s_gate) || !aligned16(w.s_up) || !aligned16(w.s_down)))
+    return fail(BEAM_ERR_INVALID_ARG, "weight scales must be 16-byte aligned");
   if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
     return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
   if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
@@ -701,8 +814,6 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int T = p->T, H = p->H, E = p->E, I = p->I, K = p->top_k;
-  const long long R = static_cast<long long>(T) * K;
   int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.off[L_IDX]);
   float* wts = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.off[L_W]);
 
@@ -713,8 +824,51 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
   if (p->flags & BEAM_FLAG_PRE_NORM) x = reinterpret_cast<const __nv_bfloat16*>(ws + L.off[L_XN]);
 
   // 2-5. permutation, expert GEMMs, combine and the residual
-  return run_experts(*p, L, x_in, x, idx, wts, w_gate, w_up, w_down, post_gain, out, ws, st,
-                     false);
+  return run_experts(*p, L, x_in, x, idx, wts, w, post_gain, out, ws, st, false);
+}
+
+}  // namespace
+
+extern "C" {
+
+beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const float* w_router,
+                               const float* logit_bias, const void* w_gate, const void* w_up,
+                               const void* w_down, const float* pre_gain, const float* post_gain,
+                               void* out, int32_t* topk_idx, float* topk_w, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  const ExpertWeights w{w_gate, w_up, w_down, nullptr, nullptr, nullptr, false};
+  return moe_forward_impl(p, x_in, w_router, logit_bias, w, pre_gain, post_gain, out, topk_idx,
+                          topk_w, workspace, workspace_bytes, stream);
+}
+
+beam_status_t beam_moe_forward_fp8(const beam_moe_params* p, const void* x_in,
+                                   const float* w_router, const float* logit_bias,
+                                   const void* wq_gate, const float* ws_gate, const void* wq_up,
+                                   const float* ws_up, const void* wq_down, const float* ws_down,
+                                   const float* pre_gain, const float* post_gain, void* out,
+                                   int32_t* topk_idx, float* topk_w, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  const ExpertWeights w{wq_gate, wq_up, wq_down, ws_gate, ws_up, ws_down, true};
+  return moe_forward_impl(p, x_in, w_router, logit_bias, w, pre_gain, post_gain, out, topk_idx,
+                          topk_w, workspace, workspace_bytes, stream);
+}
+
+beam_status_t beam_quantize_e4m3_rows(const void* src, long long rows, int K, void* q,
+                                      float* scale, void* stream) {
+  if (rows < 0 || K <= 0 || K % 16)
+    return fail(BEAM_ERR_INVALID_ARG, "rows=%lld K=%d: rows >= 0 and K a positive multiple of 16",
+                rows, K);
+  if (rows > (1LL << 34)) return fail(BEAM_ERR_UNSUPPORTED, "rows=%lld is too large", rows);
+  if (rows == 0) return BEAM_OK;
+  if (!src || !q || !scale) return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(src) || !aligned16(q) || !aligned16(scale))
+    return fail(BEAM_ERR_INVALID_ARG, "src, q and scale must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps("quant_rows", st);
+  beam::quant_rows_e4m3_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(src), nullptr, rows, K, static_cast<uint8_t*>(q), scale);
+  BEAM_LAUNCH_CHECK("quant_rows_e4m3_kernel");
+  return BEAM_OK;
 }
 
 // ------------------------------------------------------------- dense MLP
@@ -733,7 +887,7 @@ beam_status_t check_dense(const beam_dense_params* d) {
     return fail(BEAM_ERR_INVALID_ARG, "rms_eps must be >= 0 and finite");
   if (d->residual_k == 1 || d->residual_k < 0)
     return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", d->residual_k);
-  if (d->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT))
+  if (d->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_FP8_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
   if ((d->flags & BEAM_FLAG_FP32_OUT) && d->residual_k >= 2)
     return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP32_OUT applies only without the residual step");
@@ -764,18 +918,37 @@ size_t beam_dense_workspace_size(const beam_dense_params* d) {
   return make_layout(dense_as_moe(*d)).total;
 }
 
-beam_status_t beam_dense_mlp_forward(const beam_dense_params* d, const void* x_in,
-                                     const void* w_gate, const void* w_up, const void* w_down,
-                                     const float* pre_gain, const float* post_gain, void* out,
-                                     void* workspace, size_t workspace_bytes, void* stream) {
+int beam_dense_workspace_layout(const beam_dense_params* d, size_t* offsets, int n) {
+  if (check_dense(d) != BEAM_OK || offsets == nullptr || n <= 0) return 0;
+  const Layout L = make_layout(dense_as_moe(*d));
+  const int m = n < kLayoutEntries ? n : kLayoutEntries;
+  for (int i = 0; i < m; ++i) offsets[i] = L.off[i];
+  return m;
+}
+
+}  // extern "C"
+
+namespace {
+
+beam_status_t dense_forward_impl(const beam_dense_params* d, const void* x_in,
+                                 const ExpertWeights& w, const float* pre_gain,
+                                 const float* post_gain, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
   beam_status_t s = check_dense(d);
   if (s != BEAM_OK) return s;
+  if (w.f8 && !(d->flags & BEAM_FLAG_FP8_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG,
+                "the E4M3 path needs BEAM_FLAG_FP8_EXPERTS in flags (and a workspace sized with it)");
   if (d->T == 0) return BEAM_OK;
-  if (!x_in || !w_gate || !w_up || !w_down || !out || !workspace)
+  if (!x_in || !w.gate || !w.up || !w.down || !out || !workspace)
     return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
-  const void* ptrs[] = {x_in, w_gate, w_up, w_down, out, workspace};
+  if (w.f8 && (!w.s_gate || !w.s_up || !w.s_down))
+    return fail(BEAM_ERR_INVALID_ARG, "the E4M3 weights need their row scales");
+  const void* ptrs[] = {x_in, w.gate, w.up, w.down, out, workspace};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
+  if (w.f8 && (!aligned16(w.s_gate) || !aligned16(w.s_up) || !aligned16(w.s_down)))
+    return fail(BEAM_ERR_INVALID_ARG, "weight scales must be 16-byte aligned");
   if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
     return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
   if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
@@ -798,8 +971,32 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_params* d, const void* x_i
     x = xn;
   }
   float* wts = reinterpret_cast<float*>(ws + L.off[L_W]);
-  return run_experts(mp, L, x_in, x, nullptr, wts, w_gate, w_up, w_down, post_gain, out, ws, st,
-                     true);
+  return run_experts(mp, L, x_in, x, nullptr, wts, w, post_gain, out, ws, st, true);
+}
+
+}  // namespace
+
+extern "C" {
+
+beam_status_t beam_dense_mlp_forward(const beam_dense_params* d, const void* x_in,
+                                     const void* w_gate, const void* w_up, const void* w_down,
+                                     const float* pre_gain, const float* post_gain, void* out,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  const ExpertWeights w{w_gate, w_up, w_down, nullptr, nullptr, nullptr, false};
+  return dense_forward_impl(d, x_in, w, pre_gain, post_gain, out, workspace, workspace_bytes,
+                            stream);
+}
+
+beam_status_t beam_dense_mlp_forward_fp8(const beam_dense_params* d, const void* x_in,
+                                         const void* wq_gate, const float* ws_gate,
+                                         const void* wq_up, const float* ws_up,
+                                         const void* wq_down, const float* ws_down,
+                                         const float* pre_gain, const float* post_gain,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  const ExpertWeights w{wq_gate, wq_up, wq_down, ws_gate, ws_up, ws_down, true};
+  return dense_forward_impl(d, x_in, w, pre_gain, post_gain, out, workspace, workspace_bytes,
+                            stream);
 }
 
 beam_status_t beam_residual_step(const void* h_prev, const void* sub_out, int T, int H, int k,

@@ -43,13 +43,19 @@ constexpr int DEV_ERR_TIMEOUT = 1;
 struct GemmArgs {
   const int4* units;          // token tiles {expert, first row, rows, 0} (MODE 0/1)
   const int* n_units;         // device count of units
-  int k_blocks;               // K / 64
+  int k_blocks;               // K / 64 (BF16) or K / 128 (E4M3): 128-byte K-blocks
   int a_rows_per_expert;      // I (gate/up) or H (down)
   __nv_bfloat16* out;         // MODE 0: act [R, I] bf16
   float* y;                   // MODE 1: y [R, H] fp32
   int out_ld;
   int m_tiles;                // weight row-tiles per token tile (I/128 or H/128)
   unsigned long long timeout_ns;
+  // E4M3 operands only: per token-row scale of the B operand (x or act) and
+  // per weight-row scales (gate and up for MODE 0, down for MODE 1), indexed
+  // expert * a_rows_per_expert + row
+  const float* row_scale;
+  const float* w_scale0;
+  const float* w_scale1;
 };
 
 // Unit u of a GEMM: token tile u / m_tiles of the tile list and weight
@@ -70,9 +76,9 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
 template <int MODE, int NT, int STAGES>
 struct GemmCfg {
   static_assert(MODE == 0 || MODE == 1, "mode");
-  static constexpr int A_TILE = 128 * 128;  // 128 rows x 64 bf16
+  static constexpr int A_TILE = 128 * 128;  // 128 rows x 128 bytes (64 bf16 or 128 e4m3)
   static constexpr int A_BYTES = (MODE == 0 ? 2 : 1) * A_TILE;
-  static constexpr int B_BYTES = NT * 128;  // NT rows x 64 bf16
+  static constexpr int B_BYTES = NT * 128;  // NT rows x 128 bytes
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int ACC_COLS = (MODE == 0 ? 2 : 1) * NT;
   static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
@@ -89,7 +95,9 @@ __device__ __forceinline__ void gemm_fail(volatile int* abort_flag) {
   atomicOr(&g_beam_err, DEV_ERR_TIMEOUT);
 }
 
-template <int MODE, int NT, int STAGES>
+// F8: both operands E4M3 (K-blocks of 128 elements, kind::f8f6f4) and the
+// epilogue applies the row and weight scales; else BF16 (K-blocks of 64).
+template <int MODE, int NT, int STAGES, bool F8>
 __global__ void __launch_bounds__(192, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                        const __grid_constant__ CUtensorMap tm_a1,
@@ -159,10 +167,11 @@ __global__ void __launch_bounds__(192, 1)
           }
           uint8_t* sb = smem + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sb, &tm_a0, &full[stage], kb * 64, arow, pol_w);
-          if (MODE == 0) tma_load_2d(sb + C::A_TILE, &tm_a1, &full[stage], kb * 64, arow, pol_w);
+          const int kx = kb * KBlock<F8>::ELEMS;
+          tma_load_2d(sb, &tm_a0, &full[stage], kx, arow, pol_w);
+          if (MODE == 0) tma_load_2d(sb + C::A_TILE, &tm_a1, &full[stage], kx, arow, pol_w);
           for (int j = 0; j < nb16; ++j)
-            tma_load_2d(sb + C::A_BYTES + j * 2048, &tm_b, &full[stage], kb * 64, un.y + j * 16,
+            tma_load_2d(sb + C::A_BYTES + j * 2048, &tm_b, &full[stage], kx, un.y + j * 16,
                         pol_x);
           ++issued;
           if (++stage == STAGES) {
@@ -202,7 +211,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_after();
         const int n16 = (un.z + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(128, n16);
+        const uint32_t idesc = idesc_f32acc<F8>(128, n16);
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, tmo, abort_flag)) {
@@ -218,8 +227,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-            mma_bf16_ss(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
-            if (MODE == 0) mma_bf16_ss(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+            mma_ss<F8>(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+            if (MODE == 0) mma_ss<F8>(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, accum);
           }
           mma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -257,6 +266,12 @@ __global__ void __launch_bounds__(192, 1)
                           (static_cast<uint32_t>(q * 32) << 16);
       const int nch = (un.z + 15) >> 4;
       const int col = un.w * 128 + rloc;
+      float ws0 = 1.f, ws1 = 1.f;
+      if (F8) {
+        const size_t wi = static_cast<size_t>(un.x) * args.a_rows_per_expert + col;
+        ws0 = args.w_scale0[wi];
+        if (MODE == 0) ws1 = args.w_scale1[wi];
+      }
       for (int c = 0; c < nch; ++c) {
         if (MODE == 0) {
           float g[16], v[16];
@@ -265,7 +280,13 @@ __global__ void __launch_bounds__(192, 1)
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
             if (tok < un.z) {
-              const float a = g[j] / (1.0f + expf(-g[j])) * v[j];
+              float gj = g[j], uj = v[j];
+              if (F8) {
+                const float sx = args.row_scale[un.y + tok];
+                gj *= ws0 * sx;
+                uj *= ws1 * sx;
+              }
+              const float a = gj / (1.0f + expf(-gj)) * uj;
               args.out[static_cast<size_t>(un.y + tok) * args.out_ld + col] =
                   __float2bfloat16_rn(a);
             }
@@ -276,7 +297,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
-            if (tok < un.z) args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = d[j];
+            if (tok < un.z) {
+              float yv = d[j];
+              if (F8) yv *= ws0 * args.row_scale[un.y + tok];
+              args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = yv;
+            }
           }
         }
       }

@@ -42,7 +42,7 @@ namespace beam {
 struct PairArgs {
   const int4* units;        // {expert | K-split, first row, tokens (<= 256), weight tile}
   const int* n_units;
-  int k_blocks;             // K-blocks (of 64) per unit
+  int k_blocks;             // 128-byte K-blocks per unit (64 BF16 or 128 E4M3 elements)
   int w_rows_per_expert;    // I (gate/up) or H (down)
   __nv_bfloat16* act;       // MODE 0: [R, I]
   float* y;                 // MODE 1: [R, H]
@@ -54,6 +54,11 @@ struct PairArgs {
   int b_k_wrap;
   size_t y_split;
   unsigned long long timeout_ns;
+  // E4M3 operands only: per token-row scale and per weight-row scales (gate
+  // and up for MODE 0, down for MODE 1), indexed expert * w_rows_per_expert + row
+  const float* row_scale;
+  const float* w_scale0;
+  const float* w_scale1;
 };
 
 struct PairCfg {
@@ -87,7 +92,9 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
   return r != 0;
 }
 
-template <int MODE>
+// F8: E4M3 operands (K-blocks of 128 elements, kind::f8f6f4) with the scales
+// applied in the epilogue; else BF16 (K-blocks of 64).
+template <int MODE, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0,
                             const __grid_constant__ CUtensorMap tm_a1,
@@ -175,17 +182,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           uint8_t* sb = smem + stage * C::STAGE_BYTES;
           const uint32_t fbar = mapa_shared(&full[stage], 0);
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * cta_bytes);
+          const int kx = kb * KBlock<F8>::ELEMS, kbx = kbb * KBlock<F8>::ELEMS;
           if (MODE == 0) {
-            tma_load_2d_pair(sb, &tm_a0, fbar, kb * 64, wrow, pol_w);
-            tma_load_2d_pair(sb + C::A_BYTES / 2, &tm_a1, fbar, kb * 64, wrow, pol_w);
+            tma_load_2d_pair(sb, &tm_a0, fbar, kx, wrow, pol_w);
+            tma_load_2d_pair(sb + C::A_BYTES / 2, &tm_a1, fbar, kx, wrow, pol_w);
           } else {
-            tma_load_2d_pair(sb, &tm_a0, fbar, kb * 64, wrow, pol_w);
+            tma_load_2d_pair(sb, &tm_a0, fbar, kx, wrow, pol_w);
           }
           for (int j = 0; j < n64; ++j)
-            tma_load_2d_pair(sb + C::A_BYTES + j * 8192, &tm_tok64, fbar, kbb * 64, tok0 + j * 64,
+            tma_load_2d_pair(sb + C::A_BYTES + j * 8192, &tm_tok64, fbar, kbx, tok0 + j * 64,
                              pol_x);
           for (int j = 0; j < n16; ++j)
-            tma_load_2d_pair(sb + C::A_BYTES + n64 * 8192 + j * 2048, &tm_tok, fbar, kbb * 64,
+            tma_load_2d_pair(sb + C::A_BYTES + n64 * 8192 + j * 2048, &tm_tok, fbar, kbx,
                              tok0 + n64 * 64 + j * 16, pol_x);
           ++issued;
           if (++stage == C::STAGES) {
@@ -222,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       for (int u = cid; ok && u < n_units; u += ncl, ++it) {
         const int4 un = args.units[u];
         const int N = (un.z + 31) & ~31;
-        const uint32_t idesc = idesc_bf16_f32(256, N);
+        const uint32_t idesc = idesc_f32acc<F8>(256, N);
         const int buf = it & 1;
         const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait_bounded(&tempty[buf], tpar ^ 1u, tmo, abort_flag)) {
@@ -243,7 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint64_t db = sdesc_k128(sa + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss_pair(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_ss_pair<F8>(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           mma_commit_pair_mc(&empty[stage], static_cast<uint16_t>(0x3));
           if (++stage == C::STAGES) {
             stage = 0;
@@ -290,6 +298,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const int i = un.w * 128 + static_cast<int>(crank) * 64 + pairid * 32 + lane;
         float* xb = xchg + pairid * (2 * 32 * 16);
         const int tbase = is_gate ? 0 : 8;
+        float sg = 1.f, su = 1.f;
+        if (F8) {
+          const size_t wi = static_cast<size_t>(un.x) * args.w_rows_per_expert + i;
+          sg = args.w_scale0[wi];
+          su = args.w_scale1[wi];
+        }
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
           float v[16];
@@ -311,8 +325,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           for (int j = 0; j < 8; ++j) {
             const int tok = c * 16 + tbase + j;
             if (tok < un.z) {
-              const float g = is_gate ? v[j] : other[j];
-              const float uu = is_gate ? other[j] : v[8 + j];
+              float g = is_gate ? v[j] : other[j];
+              float uu = is_gate ? other[j] : v[8 + j];
+              if (F8) {
+                const float sx = args.row_scale[un.y + tok];
+                g *= sg * sx;
+                uu *= su * sx;
+              }
               const float a = __fdividef(g, 1.0f + __expf(-g)) * uu;
               args.act[static_cast<size_t>(un.y + tok) * args.out_ld + i] = __float2bfloat16_rn(a);
             }
@@ -321,6 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       } else {
         const int h = un.w * 256 + static_cast<int>(crank) * 128 + q * 32 + lane;
         float* ybase = args.k_split ? args.y + static_cast<size_t>(un.x) * args.y_split : args.y;
+        const float sd = F8 ? args.w_scale0[static_cast<size_t>(un.x) * args.w_rows_per_expert + h] : 1.f;
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
           float d[16];
@@ -329,7 +349,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
             // per-pair outputs are read once, by the row kernel: stream them past L2
-            if (tok < un.z) __stcs(ybase + static_cast<size_t>(un.y + tok) * args.out_ld + h, d[j]);
+            if (tok < un.z) {
+              const float yv = F8 ? d[j] * (sd * args.row_scale[un.y + tok]) : d[j];
+              __stcs(ybase + static_cast<size_t>(un.y + tok) * args.out_ld + h, yv);
+            }
           }
         }
       }

@@ -44,12 +44,17 @@ namespace beam {
 struct TmArgs {
   const int4* units;        // 2 per cluster unit: {expert, first row, rows, tile | TM_PAIR}
   const int* n_units;
-  int k_blocks;             // K / 64
+  int k_blocks;             // 128-byte K-blocks: K / 64 (BF16) or K / 128 (E4M3)
   int w_rows_per_expert;    // I (gate/up) or H (down)
   __nv_bfloat16* out;       // MODE 0: act [R, I] bf16
   float* y;                 // MODE 1: y [R, H] fp32
   int out_ld;
   unsigned long long timeout_ns;
+  // E4M3 operands only: per token-row scale and per weight-row scales (gate
+  // and up for MODE 0, down for MODE 1), indexed expert * w_rows_per_expert + row
+  const float* row_scale;
+  const float* w_scale0;
+  const float* w_scale1;
 };
 
 struct TmCfg {
@@ -68,7 +73,9 @@ struct TmCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-template <int MODE>
+// F8: E4M3 operands (K-blocks of 128 elements, kind::f8f6f4) with the scales
+// applied in the epilogue; else BF16 (K-blocks of 64).
+template <int MODE, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     expert_gemm_tm_kernel(const __grid_constant__ CUtensorMap tm_w0,
                           const __grid_constant__ CUtensorMap tm_w1,
@@ -145,17 +152,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           }
           uint8_t* sb = smem + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sb, &tm_tok, &full[stage], kb * 64, un.y, pol_x);
+          const int kx = kb * KBlock<F8>::ELEMS;
+          tma_load_2d(sb, &tm_tok, &full[stage], kx, un.y, pol_x);
           if (pair) {
             if (crank == 0)
-              tma_load_2d_mc(sb + C::A_BYTES, &tm_w0, &full[stage], kb * 64, wr0,
+              tma_load_2d_mc(sb + C::A_BYTES, &tm_w0, &full[stage], kx, wr0,
                              static_cast<uint16_t>(0x3), pol_w);
             else
-              tma_load_2d_mc(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kb * 64, wr1,
+              tma_load_2d_mc(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kx, wr1,
                              static_cast<uint16_t>(0x3), pol_w);
           } else {
-            tma_load_2d(sb + C::A_BYTES, &tm_w0, &full[stage], kb * 64, wr0, pol_w);
-            tma_load_2d(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kb * 64, wr1, pol_w);
+            tma_load_2d(sb + C::A_BYTES, &tm_w0, &full[stage], kx, wr0, pol_w);
+            tma_load_2d(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kx, wr1, pol_w);
           }
           ++issued;
           if (++stage == C::STAGES) {
@@ -180,7 +188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, C::BN);
+      const uint32_t idesc = idesc_f32acc<F8>(128, C::BN);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -206,7 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint64_t db = sdesc_k128(sa + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_ss<F8>(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           mma_commit_mc(&empty[stage], static_cast<uint16_t>(0x3));
           if (++stage == C::STAGES) {
             stage = 0;
@@ -243,12 +251,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                           (static_cast<uint32_t>(q * 32) << 16);
       const bool valid = rloc < un.z;
       const size_t row = static_cast<size_t>(un.y) + rloc;
+      const float sx = (F8 && valid) ? args.row_scale[row] : 1.f;
       if (MODE == 0) {
         __nv_bfloat16* dst = args.out + row * args.out_ld + nt * 128;
+        const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 128;
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           float g[16], v[16];
           tmem_ld16x2(tb + c * 16, tb + 128 + c * 16, g, v);
+          if (F8) {
+            // weight-row scales of these 16 columns (the same for every lane)
+            const float4* sg4 = reinterpret_cast<const float4*>(args.w_scale0 + wi0 + c * 16);
+            const float4* su4 = reinterpret_cast<const float4*>(args.w_scale1 + wi0 + c * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float4 a = __ldg(sg4 + j), b = __ldg(su4 + j);
+              g[4 * j] *= a.x * sx; g[4 * j + 1] *= a.y * sx; g[4 * j + 2] *= a.z * sx; g[4 * j + 3] *= a.w * sx;
+              v[4 * j] *= b.x * sx; v[4 * j + 1] *= b.y * sx; v[4 * j + 2] *= b.z * sx; v[4 * j + 3] *= b.w * sx;
+            }
+          }
           if (valid) {
             uint4 pk[2];
             __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
@@ -266,10 +287,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
       } else {
         float* dst = args.y + row * args.out_ld + nt * 256;
+        const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 256;
 #pragma unroll 1
         for (int c = 0; c < 16; ++c) {
           float d[16];
           tmem_ld16(tb + c * 16, d);
+          if (F8) {
+            const float4* sd4 = reinterpret_cast<const float4*>(args.w_scale0 + wi0 + c * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float4 a = __ldg(sd4 + j);
+              d[4 * j] *= a.x * sx; d[4 * j + 1] *= a.y * sx; d[4 * j + 2] *= a.z * sx; d[4 * j + 3] *= a.w * sx;
+            }
+          }
           if (valid) {
             float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
 #pragma unroll

@@ -201,6 +201,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with E4M3 inputs: D=F32 [4,6)=1,
+// A and B format E4M3 = 0 in [7,10) and [10,13), both K-major, N>>3 at
+// [17,23), M>>4 at [24,29). One instruction consumes K = 32 elements (32
+// bytes of each operand row, the same bytes as K = 16 for BF16).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T on E4M3 operands, FP32 accumulation.
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_e4m3_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by a single thread.
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
@@ -290,5 +318,32 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va
     vb[i] = __uint_as_float(b[i]);
   }
 }
+
+// Element-type dispatch for the GEMM kernels: F8 = E4M3 operands (K-blocks of
+// 128 elements), else BF16 (K-blocks of 64); both are 128-byte rows.
+template <bool F8>
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N) {
+  return F8 ? idesc_e4m3_f32(M, N) : idesc_bf16_f32(M, N);
+}
+template <bool F8>
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  if (F8)
+    mma_e4m3_ss(d, a, b, idesc, acc);
+  else
+    mma_bf16_ss(d, a, b, idesc, acc);
+}
+template <bool F8>
+__device__ __forceinline__ void mma_ss_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  if (F8)
+    mma_e4m3_ss_pair(d, a, b, idesc, acc);
+  else
+    mma_bf16_ss_pair(d, a, b, idesc, acc);
+}
+template <bool F8>
+struct KBlock {
+  static constexpr int ELEMS = F8 ? 128 : 64;  // elements per 128-byte K-block row
+};
 
 }  // namespace beam

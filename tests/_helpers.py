@@ -117,6 +117,138 @@ def oracle_outputs(x64, chosen_rows, tokens, get_expert):
     return O.moe_combine(x64[tokens], idx, w, get_expert)
 
 
+def expert_getter_fp8(gq, uq, dq):
+    """Oracle access to E4M3 expert weights: ((codes, scales) x 3) per expert,
+    copied from the device tensors the quantiser wrote."""
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache[e] = tuple((q[0][e].cpu().numpy(), q[1][e].cpu().numpy()) for q in (gq, uq, dq))
+            if len(cache) > 48:
+                cache.pop(next(iter(cache)))
+        return cache[e]
+    return get
+
+
+def _bf16_grid_between(lo, hi):
+    """BF16 values in [lo, hi] for 0 <= lo <= hi (both BF16 values)."""
+    b0 = int(np.float32(lo).view(np.uint32)) >> 16
+    b1 = int(np.float32(hi).view(np.uint32)) >> 16
+    assert b1 - b0 <= 4096, "interval too wide"
+    bits = (np.arange(b0, b1 + 1, dtype=np.uint32) << np.uint32(16))
+    return bits.view(np.float32).astype(np.float64)
+
+
+def check_act_codes_fp8(a64, gpu_codes, gpu_scale, rel=1e-5, row_abs=1e-5):
+    """Validate the GPU's E4M3 codes and row scales of SwiGLU rows a64 [n, I]
+    (FP64, before rounding) against the oracle's quantiser.
+
+    The GPU's FP32 value of each element lies within m = rel*|a| +
+    row_abs*max|a_row| of a64 (its FP32 accumulation and SwiGLU err far less).
+    BF16 rounding, the FP32 product with the row's 448/amax and the E4M3
+    rounding are all monotone, so a correct code lies between the codes of
+    the interval's two ends; the row maximum lies between the largest lower
+    and upper ends, and the GPU's scale must be amax/448 (FP32) for a BF16
+    value amax there. Returns (checked mask [n] (all rows), codes, scale):
+    the validated GPU codes and scales, each of them an oracle-admitted
+    result."""
+    a64 = np.asarray(a64, dtype=np.float64)
+    gpu_codes = np.asarray(gpu_codes)
+    gpu_scale = np.asarray(gpu_scale, dtype=np.float32)
+    n = a64.shape[0]
+    m = rel * np.abs(a64) + row_abs * np.max(np.abs(a64), axis=1, keepdims=True)
+    lo_v = O.bf16_round(a64 - m).astype(np.float64)
+    hi_v = O.bf16_round(a64 + m).astype(np.float64)
+    absmin = np.where(lo_v > 0, lo_v, np.where(hi_v < 0, -hi_v, 0.0))
+    absmax = np.maximum(np.abs(lo_v), np.abs(hi_v))
+    amax_lo, amax_hi = absmin.max(axis=1), absmax.max(axis=1)
+    inv = np.empty(n, dtype=np.float32)
+    f448 = np.float32(O.E4M3_MAX)
+    for r in range(n):
+        if amax_hi[r] == 0:
+            assert gpu_scale[r] == 1.0, f"row {r}: zero row with scale {gpu_scale[r]}"
+            inv[r] = 1.0
+            continue
+        cands = _bf16_grid_between(amax_lo[r], amax_hi[r])
+        cands = cands[cands > 0].astype(np.float32)
+        hit = cands[(cands / f448).astype(np.float32) == gpu_scale[r]]
+        assert len(hit) >= 1, (f"row {r}: scale {gpu_scale[r]} is amax/448 for no amax in "
+                               f"[{amax_lo[r]}, {amax_hi[r]}]")
+        inv[r] = np.float32(f448 / hit[0])
+    inv2 = inv[:, None]
+    c_lo = O.e4m3_round((lo_v.astype(np.float32) * inv2).astype(np.float32))
+    c_hi = O.e4m3_round((hi_v.astype(np.float32) * inv2).astype(np.float32))
+    gv = O.e4m3_decode(gpu_codes)
+    ok = (gv >= c_lo) & (gv <= c_hi)
+    if not ok.all():
+        r, j = map(int, np.argwhere(~ok)[0])
+        raise AssertionError(
+            f"{(~ok).sum()} act codes outside the oracle's interval; first at row {r} "
+            f"col {j}: a64={a64[r, j]!r} code value {gv[r, j]!r} not in "
+            f"[{c_lo[r, j]!r}, {c_hi[r, j]!r}] (scale {gpu_scale[r]!r})")
+    return np.ones(n, dtype=bool), gpu_codes, gpu_scale
+
+
+def oracle_outputs_fp8_checked(x64, gpu_idx, weight_of, get_expert_q, act_rows, E,
+                               tokens=None):
+    """Oracle FP8 combine for `tokens` (default: all), with each pair row's
+    SwiGLU codes and scale validated against the GPU's
+    (check_act_codes_fp8). Rows are in the expert order the permutation of
+    gpu_idx gives (stable by token, slot); act_rows(rows) returns the GPU's
+    (codes [n, I], scales [n]) of those rows; weight_of(t, e) is the oracle's
+    combine weight. Returns (out [len(tokens), H], all-checked mask)."""
+    gpu_idx = np.asarray(gpu_idx)
+    T, K = gpu_idx.shape
+    perm = O.permutation(gpu_idx, E)
+    row_of_pair = np.empty(T * K, dtype=np.int64)
+    row_of_pair[perm["row_pair"]] = np.arange(T * K)
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    pos = {int(t): i for i, t in enumerate(toks)}
+    pairs = (toks[:, None] * K + np.arange(K)[None, :]).ravel()
+    experts = gpu_idx.ravel()[pairs]
+    out = np.zeros((len(toks), x64.shape[1]))
+    for e in np.unique(experts):
+        pe = pairs[experts == e]
+        rows, tk = row_of_pair[pe], pe // K
+        gq, uq, dq = get_expert_q(int(e))
+        a64 = O.swiglu_act_fp8(x64[tk], gq, uq)
+        codes_g, scale_g = act_rows(rows)
+        _, codes, scale = check_act_codes_fp8(a64, codes_g, scale_g)
+        y = O.dequantize_rows_e4m3(codes, scale) @ O.dequantize_rows_e4m3(*dq).T
+        for i, t in enumerate(tk):
+            out[pos[int(t)]] += weight_of(int(t), int(e)) * y[i]
+    return out, np.ones(len(toks), dtype=bool)
+
+
+def act_rows_reader(ws, lay, I):
+    """act_rows callable for oracle_outputs_fp8_checked: copies the GPU's
+    E4M3 SwiGLU rows and their scales out of the workspace."""
+    def read(rows):
+        rows = np.asarray(rows, dtype=np.int64)
+        codes = np.stack([ws[lay["act_q"] + r * I:lay["act_q"] + (r + 1) * I].cpu().numpy()
+                          for r in rows])
+        sc = ws[lay["act_scale"]:lay["act_scale"] + (int(rows.max()) + 1) * 4]
+        sc = sc.view(torch.float32).cpu().numpy()[rows]
+        return codes, sc
+    return read
+
+
+def weights_from_chosen(chosen, tokens=None):
+    """weight_of(t, e) from compare_routing's chosen selections (listed in
+    the order of `tokens`, default 0..T-1)."""
+    toks = range(len(chosen)) if tokens is None else tokens
+    maps = {int(t): dict(zip(c[0].tolist(), c[1].tolist())) for t, c in zip(toks, chosen)}
+    return lambda t, e: maps[t][e]
+
+
+def oracle_outputs_fp8(x64, chosen_rows, tokens, get_expert_q):
+    """Oracle FP8 combine for the given tokens using the selections."""
+    idx = np.stack([chosen_rows[i][0] for i in range(len(tokens))])
+    w = np.stack([chosen_rows[i][1] for i in range(len(tokens))])
+    return O.moe_combine_fp8(x64[tokens], idx, w, get_expert_q)
+
+
 def rel_err(got, want):
     want = np.asarray(want, dtype=np.float64)
     got = np.asarray(got, dtype=np.float64)

@@ -107,3 +107,30 @@ def test_residual_step_args_rejected():
 def test_empty_batch_is_a_no_op():
     p = _p(T=0)
     assert B.lib().beam_moe_forward(ctypes.byref(p), *([None] * 12), 0, None) == 0
+
+
+def test_fp8_workspace_holds_e4m3_buffers():
+    plain = B.workspace_layout(_p())
+    f8 = B.workspace_layout(_p(flags=B.FLAG_FP8_EXPERTS))
+    assert plain["act_q"] == plain["act_scale"]          # absent without the flag
+    assert f8["act_scale"] - f8["act_q"] >= 64 * 8 * 2560  # one code per activation
+    assert f8["act_q"] - f8["x_scale"] >= 64 * 8 * 4       # one scale per pair row
+    assert B.workspace_size(_p(flags=B.FLAG_FP8_EXPERTS)) > B.workspace_size(_p())
+
+
+def test_fp8_entry_points_reject_bad_args():
+    lib = B.lib()
+    p = _p()                                   # FLAG_FP8_EXPERTS missing
+    assert lib.beam_moe_forward_fp8(ctypes.byref(p), *([None] * 15), 0, None) == 1
+    assert "FP8_EXPERTS" in B.last_error()
+    p = _p(flags=B.FLAG_FP8_EXPERTS)           # pointers missing
+    assert lib.beam_moe_forward_fp8(ctypes.byref(p), *([None] * 15), 0, None) == 1
+    p = _p(T=0, flags=B.FLAG_FP8_EXPERTS)
+    assert lib.beam_moe_forward_fp8(ctypes.byref(p), *([None] * 15), 0, None) == 0
+    d = B.DenseParams(8, 5120, 2560, 1e-6, 0, 0)
+    assert lib.beam_dense_mlp_forward_fp8(ctypes.byref(d), *([None] * 11), 0, None) == 1
+    # the quantiser wants K a positive multiple of 16 and rows >= 0
+    assert lib.beam_quantize_e4m3_rows(None, 4, 10, None, None, None) == 1
+    assert lib.beam_quantize_e4m3_rows(None, -1, 16, None, None, None) == 1
+    assert lib.beam_quantize_e4m3_rows(None, 0, 16, None, None, None) == 0
+    assert lib.beam_quantize_e4m3_rows(None, 4, 16, None, None, None) == 1

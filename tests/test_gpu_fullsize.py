@@ -9,8 +9,9 @@ import torch
 
 import beam_synth as S
 import oracle as O
-from _helpers import (OUT_REL_TOL, compare_routing, expert_getter, host, oracle_outputs,
-                      prenorm_ambiguous, rel_err)
+from _helpers import (OUT_REL_TOL, act_rows_reader, compare_routing, expert_getter,
+                      expert_getter_fp8, host, oracle_outputs, oracle_outputs_fp8_checked,
+                      prenorm_ambiguous, rel_err, weights_from_chosen)
 
 pytestmark = pytest.mark.gpu
 
@@ -139,3 +140,50 @@ def test_long_prefill_residual_T16384(B):
     rms = torch.sqrt(hk.float().pow(2).mean(1)).cpu().numpy()
     assert np.all(np.abs(rms - 1.0) < 0.05)
     print(f"long prefill: clean {len(clean)}/{wl.T}, near ties {n_ties}, rel err {err:.2e}")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_bench_configuration_fp8(B, name):
+    """The E4M3 expert path as the benchmark times it (pre-norm, FP8
+    experts, post-norm, residual k=50): the weight quantiser bit-exact on
+    sampled rows, routing of every clean token, and sampled tokens' outputs
+    with each of their SwiGLU rows' codes validated."""
+    wl = S.WORKLOADS[name]
+    d = S.make_inputs(wl, "cuda")
+    q = tuple(B.quantize_e4m3_rows(d[k]) for k in ("w_gate", "w_up", "w_down"))
+    assert B.status() == 0, B.last_error()
+    rows = _sample(wl.E * wl.I, 64, 9)
+    wg = d["w_gate"].view(-1, wl.H)[torch.as_tensor(rows, device="cuda")].float().cpu().numpy()
+    want_c, want_s = O.quantize_rows_e4m3(wg)
+    assert np.array_equal(q[0][0].view(-1, wl.H)[torch.as_tensor(rows, device="cuda")].cpu().numpy(),
+                          want_c)
+    assert np.array_equal(q[0][1].view(-1)[torch.as_tensor(rows, device="cuda")].cpu().numpy(),
+                          want_s)
+    for k in ("w_gate", "w_up", "w_down"):
+        d[k] = None
+    torch.cuda.empty_cache()
+    p = _params(B, wl, B.FLAG_PRE_NORM | B.FLAG_FP8_EXPERTS, 50)
+    ws = B.alloc_workspace(p)
+    idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device="cuda")
+    hk = B.forward_fp8(p, d["x"], d["w_router"], *q, bias=d["bias"], topk_idx=idx, topk_w=w,
+                       workspace=ws)
+    assert B.status() == 0, B.last_error()
+    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+    h64 = host(d["x"]).astype(np.float64)
+    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
+    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
+    clean = np.nonzero(~amb.any(axis=1))[0]
+    assert len(clean) >= 0.8 * wl.T
+    sel = O.route(x64[clean], host(d["w_router"]), None, wl.n_group, wl.topk_group, wl.top_k,
+                  wl.routed_scale)
+    ties, chosen = compare_routing(sel, gi[clean], gw[clean], wl)
+    sample = np.intersect1d(_sample(wl.T, 16, 5), clean)
+    o, _ = oracle_outputs_fp8_checked(x64, gi, weights_from_chosen(chosen, clean),
+                                      expert_getter_fp8(*q),
+                                      act_rows_reader(ws, B.workspace_layout(p), wl.I), wl.E,
+                                      tokens=sample)
+    want = O.residual_step(h64[sample], o, 50, None, wl.rms_eps, True)
+    err = rel_err(host(hk)[sample], want)
+    assert err <= OUT_REL_TOL, f"rel err {err}"
+    print(f"{name} fp8: clean {len(clean)}/{wl.T}, near ties {int(ties.sum())}, rel err {err:.2e}")

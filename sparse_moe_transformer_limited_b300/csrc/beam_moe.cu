@@ -522,7 +522,7 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     pd.act = nullptr;
     pd.y = y;
     pd.out_ld = H;
-    pd.row_scale = ascale;
+    pd.row_scale = nullptr;  // the activation row scales are applied by the combine
     pd.w_scale0 = w.s_down;
     pd.w_scale1 = nullptr;
     CUtensorMap m_x64, m_a64;
@@ -571,7 +571,7 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     td.out = nullptr;
     td.y = y;
     td.out_ld = H;
-    td.row_scale = ascale;
+    td.row_scale = nullptr;  // the activation row scales are applied by the combine
     td.w_scale0 = w.s_down;
     td.w_scale1 = nullptr;
     if ((s = launch_gemm_tm<0, F8>(m_g, m_u, m_x, ta, st)) != BEAM_OK) return s;
@@ -598,7 +598,7 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     gd.out = nullptr;
     gd.y = y;
     gd.out_ld = H;
-    gd.row_scale = ascale;
+    gd.row_scale = nullptr;  // the activation row scales are applied by the combine
     gd.w_scale0 = w.s_down;
     gd.w_scale1 = nullptr;
     if (L.path == PATH_W32) {
@@ -726,11 +726,11 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     ProfScope ps("combine_rows", st);
     if (p->flags & BEAM_FLAG_FP32_OUT)
       beam::combine_rows_kernel<true><<<T, beam::COMBINE_THREADS, 0, st>>>(
-          y, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
+          y, ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
           p->rms_eps, a, b, resid);
     else
       beam::combine_rows_kernel<false><<<T, beam::COMBINE_THREADS, 0, st>>>(
-          y, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
+          y, ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
           p->rms_eps, a, b, resid);
   }
   BEAM_LAUNCH_CHECK("combine_rows_kernel");

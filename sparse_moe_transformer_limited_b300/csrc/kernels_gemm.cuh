@@ -50,9 +50,10 @@ struct GemmArgs {
   int out_ld;
   int m_tiles;                // weight row-tiles per token tile (I/128 or H/128)
   unsigned long long timeout_ns;
-  // E4M3 operands only: per token-row scale of the B operand (x or act) and
-  // per weight-row scales (gate and up for MODE 0, down for MODE 1), indexed
-  // expert * a_rows_per_expert + row
+  // E4M3 operands only: per token-row scale of x (MODE 0; in MODE 1 the
+  // activation row scale is a factor of the whole output row, applied by the
+  // combine) and per weight-row scales (gate and up for MODE 0, down for
+  // MODE 1), indexed expert * a_rows_per_expert + row
   const float* row_scale;
   const float* w_scale0;
   const float* w_scale1;
@@ -297,11 +298,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
-            if (tok < un.z) {
-              float yv = d[j];
-              if (F8) yv *= ws0 * args.row_scale[un.y + tok];
-              args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = yv;
-            }
+            if (tok < un.z)
+              args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = F8 ? d[j] * ws0 : d[j];
           }
         }
       }

@@ -54,8 +54,9 @@ struct PairArgs {
   int b_k_wrap;
   size_t y_split;
   unsigned long long timeout_ns;
-  // E4M3 operands only: per token-row scale and per weight-row scales (gate
-  // and up for MODE 0, down for MODE 1), indexed expert * w_rows_per_expert + row
+  // E4M3 operands only: per token-row scale (MODE 0; MODE 1 leaves the
+  // activation row scale to the combine) and per weight-row scales (gate and
+  // up for MODE 0, down for MODE 1), indexed expert * w_rows_per_expert + row
   const float* row_scale;
   const float* w_scale0;
   const float* w_scale1;
@@ -340,19 +341,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       } else {
         const int h = un.w * 256 + static_cast<int>(crank) * 128 + q * 32 + lane;
         float* ybase = args.k_split ? args.y + static_cast<size_t>(un.x) * args.y_split : args.y;
+        // E4M3: the weight-row scale here; the activation row scale is a
+        // factor of the whole output row and is applied by the combine
         const float sd = F8 ? args.w_scale0[static_cast<size_t>(un.x) * args.w_rows_per_expert + h] : 1.f;
+        float* yrow = ybase + static_cast<size_t>(un.y) * args.out_ld + h;
+        // 32 accumulator columns (tokens) per TMEM wait; the second half may
+        // lie past N but stays inside this accumulator's 256 columns
 #pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
-          float d[16];
-          tmem_ld16(tb + c * 16, d);
+        for (int c = 0; c < nch; c += 2) {
+          float d[16], e[16];
+          tmem_ld16x2(tb + c * 16, tb + c * 16 + 16, d, e);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
             // per-pair outputs are read once, by the row kernel: stream them past L2
-            if (tok < un.z) {
-              const float yv = F8 ? d[j] * (sd * args.row_scale[un.y + tok]) : d[j];
-              __stcs(ybase + static_cast<size_t>(un.y + tok) * args.out_ld + h, yv);
-            }
+            if (tok < un.z) __stcs(yrow + static_cast<size_t>(tok) * args.out_ld, F8 ? d[j] * sd : d[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c * 16 + 16 + j;
+            if (tok < un.z) __stcs(yrow + static_cast<size_t>(tok) * args.out_ld, F8 ? e[j] * sd : e[j]);
           }
         }
       }

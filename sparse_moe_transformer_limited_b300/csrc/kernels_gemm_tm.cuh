@@ -50,8 +50,9 @@ struct TmArgs {
   float* y;                 // MODE 1: y [R, H] fp32
   int out_ld;
   unsigned long long timeout_ns;
-  // E4M3 operands only: per token-row scale and per weight-row scales (gate
-  // and up for MODE 0, down for MODE 1), indexed expert * w_rows_per_expert + row
+  // E4M3 operands only: per token-row scale (MODE 0; MODE 1 leaves the
+  // activation row scale to the combine) and per weight-row scales (gate and
+  // up for MODE 0, down for MODE 1), indexed expert * w_rows_per_expert + row
   const float* row_scale;
   const float* w_scale0;
   const float* w_scale1;
@@ -251,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                           (static_cast<uint32_t>(q * 32) << 16);
       const bool valid = rloc < un.z;
       const size_t row = static_cast<size_t>(un.y) + rloc;
-      const float sx = (F8 && valid) ? args.row_scale[row] : 1.f;
+      const float sx = (F8 && MODE == 0 && valid) ? args.row_scale[row] : 1.f;
       if (MODE == 0) {
         __nv_bfloat16* dst = args.out + row * args.out_ld + nt * 128;
         const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 128;
@@ -297,7 +298,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float4 a = __ldg(sd4 + j);
-              d[4 * j] *= a.x * sx; d[4 * j + 1] *= a.y * sx; d[4 * j + 2] *= a.z * sx; d[4 * j + 3] *= a.w * sx;
+              d[4 * j] *= a.x; d[4 * j + 1] *= a.y; d[4 * j + 2] *= a.z; d[4 * j + 3] *= a.w;
             }
           }
           if (valid) {

@@ -138,7 +138,9 @@ __global__ void __launch_bounds__(256) finalize_rows_kernel(
 // post-norm + scaled residual ("Reflection 发布 Beam 501B 开源模型…", section
 // 专家混合模型: expert outputs combined with the normalised router weights;
 // section 残差流: normalise after the sublayer, then h_k = a*h_{k-1} + b*n):
-//   o[t,:] = sum_j w[t,j] * y[pair_row[t,j], :]   (y FP32; FP32 sum, slot order)
+//   o[t,:] = sum_j w[t,j] * s[r] * y[r, :], r = pair_row[t,j]   (y FP32; FP32
+//            sum, slot order; s = the per-row scale of y, or 1 when y_scale
+//            is NULL -- the E4M3 path's activation row scales)
 //   resid:  out = bf16( a * h_prev + b * RMSNorm(o) * gain )
 //   else:   out = o  (bf16, or fp32 when OUT_F32)
 // One block of 128 threads per token; each thread keeps up to 8 chunks of 8
@@ -148,7 +150,7 @@ constexpr int COMBINE_MAX_CHUNKS = 8;
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_rows_kernel(
-    const float* __restrict__ y, const int* __restrict__ pair_row,
+    const float* __restrict__ y, const float* __restrict__ y_scale, const int* __restrict__ pair_row,
     const float* __restrict__ topk_w, int top_k, const __nv_bfloat16* __restrict__ h_prev,
     const float* __restrict__ gain, void* __restrict__ out, int H, float eps, float a, float b,
     int resid) {
@@ -158,8 +160,10 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_rows_kernel(
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   if (tid < top_k) {
-    s_row[tid] = pair_row[static_cast<size_t>(t) * top_k + tid];
-    s_w[tid] = topk_w[static_cast<size_t>(t) * top_k + tid];
+    const int r = pair_row[static_cast<size_t>(t) * top_k + tid];
+    s_row[tid] = r;
+    const float wt = topk_w[static_cast<size_t>(t) * top_k + tid];
+    s_w[tid] = y_scale != nullptr ? wt * y_scale[r] : wt;
   }
   __syncthreads();
   const int nc = H >> 3;

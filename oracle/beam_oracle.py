@@ -451,3 +451,154 @@ def moe_forward_fp8(x_in, w_router, bias, get_expert_q, *, n_group=8, topk_group
     out = moe_combine_fp8(x, use["idx"], use["weights"], get_expert_q)
     h = residual_step(x_in, out, residual_k, post_gain, eps, True) if residual_k else None
     return dict(x=x, sel=sel, out=out, h=h)
+
+
+# ----------------------------------------------------------------------------
+# NVFP4 expert weights ([P5] section 四套权重的账，自己算一遍: the NVFP4
+# checkpoint packs every routed-expert weight as two 4-bit values per byte
+# (U8 count = half the expert parameters) and keeps the rest in BF16; its
+# section 上手前的五个坑: NVFP4 is packed by modelopt and runs on the FP4
+# tensor-core path of Blackwell; [P1] 专家混合模型: NVFP4 stores most
+# parameters in 4 bits for Blackwell GPUs).
+#
+# Readings where the pages leave the format open:
+#   * element type E2M1: sign bit 3, exponent bits 1..2 (bias 1), mantissa
+#     bit 0, values 0, 0.5, 1, 1.5, 2, 3, 4, 6; round to nearest, ties to
+#     even, saturate at +-6; two per byte, the even element in the low nibble.
+#   * 16 consecutive elements along K share a block scale stored as E4M3
+#     (one byte); a second FP32 scale covers a group of rows: one expert
+#     matrix for weights (static), one row for activations (dynamic, run
+#     time). Supporting arithmetic: the NVFP4 checkpoint's disk size
+#     (293.63 GB) equals its listed U8 + BF16 + F32 bytes (262.79 GB) plus one
+#     byte per 16 routed-expert weights (30.83 GB) to within 0.02 GB.
+#   * quantiser, in FP32 with IEEE division, for a group with largest
+#     magnitude amax (g = 1 for an all-zero group) and each 16-block b:
+#       g   = amax / 2688                      (2688 = 6 * 448)
+#       s_b = E4M3(amax_b / (6 * g))           (block scale, <= 448)
+#       q_i = E2M1(v_i * (1 / (s_b * g)))      (q = 0 where s_b = 0)
+#     and an element is dequantised as E2M1 value * s_b * g.
+#   * x (BF16, after the optional pre-norm) is quantised per token; the
+#     SwiGLU output A is rounded to BF16 and quantised per (token, expert)
+#     row, as for FP8; the router stays FP32.
+# ----------------------------------------------------------------------------
+E2M1_MAX = 6.0
+NVFP4_BLOCK = 16
+
+
+def e2m1_round(v) -> np.ndarray:
+    """Nearest E2M1 value (ties to even mantissa), saturating at +-6; float64.
+    Grid spacing 0.5 below 2, 1 in [2, 4), 2 in [4, 6]."""
+    v = np.asarray(v, dtype=F64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)
+    e = np.clip(ex - 1, 0, 2)                 # binade [2^e, 2^(e+1)); 0.5-steps below 2
+    q = np.ldexp(1.0, e - 1)                  # spacing: 0.5, 1, 2
+    r = np.round(a / q) * q                   # np.round: halves go to even
+    r = np.minimum(np.where(a == 0, 0.0, r), E2M1_MAX)
+    return np.copysign(r, v)
+
+
+_E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """4-bit codes (sign << 3 | magnitude index) of values on the E2M1 grid."""
+    v = np.asarray(v, dtype=F64)
+    mag = np.abs(v)
+    idx = np.searchsorted(_E2M1_VALUES, mag)
+    assert np.all(_E2M1_VALUES[np.minimum(idx, 7)] == mag), "value off the E2M1 grid"
+    return (np.signbit(v).astype(np.uint8) << np.uint8(3)) | idx.astype(np.uint8)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Values of 4-bit E2M1 codes: exponent field e (bits 1..2), mantissa m
+    (bit 0): e = 0 gives m * 0.5, else (1 + m/2) * 2^(e-1)."""
+    c = np.asarray(codes, dtype=np.int64) & 0xF
+    e = (c >> 1) & 0x3
+    m = c & 0x1
+    val = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.ldexp(1.0, e - 1))
+    return np.where(c & 0x8, -val, val)
+
+
+def pack_e2m1(codes) -> np.ndarray:
+    """[..., K] 4-bit codes -> [..., K/2] bytes, the even element in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def unpack_e2m1(packed) -> np.ndarray:
+    """[..., K/2] bytes -> [..., K] 4-bit codes."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def quantize_nvfp4(a, rows_per_group: int):
+    """NVFP4 quantisation (reading above) of rows a [R, K] (K % 16 == 0)
+    whose consecutive groups of rows_per_group rows share the FP32 scale.
+    Returns (packed codes [R, K/2] uint8, block scales [R, K/16] uint8 E4M3
+    codes, group scales [R / rows_per_group] float32)."""
+    a32 = np.asarray(a, dtype=F32)
+    R, K = a32.shape
+    assert K % NVFP4_BLOCK == 0 and R % rows_per_group == 0
+    G = R // rows_per_group
+    amax = np.max(np.abs(a32).reshape(G, -1), axis=1)
+    g = np.where(amax > 0, amax / F32(2688.0), F32(1.0)).astype(F32)
+    g_row = np.repeat(g, rows_per_group)
+    blocks = a32.reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)
+    amax_b = np.max(np.abs(blocks), axis=2)
+    six_g = (F32(6.0) * g_row).astype(F32)
+    sb_val = e4m3_round((amax_b / six_g[:, None]).astype(F32))
+    sb_code = e4m3_encode(sb_val)
+    denom = (sb_val.astype(F32) * g_row[:, None]).astype(F32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(sb_val > 0, F32(1.0) / np.where(sb_val > 0, denom, F32(1.0)),
+                       F32(0.0)).astype(F32)
+    v = (blocks * inv[:, :, None]).astype(F32)
+    codes = e2m1_encode(e2m1_round(v)).reshape(R, K)
+    return pack_e2m1(codes), sb_code, g
+
+
+def dequantize_nvfp4(packed, block_scales, group_scales, rows_per_group: int) -> np.ndarray:
+    """E2M1 value * E4M3 block scale * FP32 group scale, FP64 [R, K]."""
+    vals = e2m1_decode(unpack_e2m1(packed))
+    R, K = vals.shape
+    sb = e4m3_decode(block_scales)
+    g = np.repeat(np.asarray(group_scales, dtype=F64), rows_per_group)
+    return (vals.reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK) * sb[:, :, None]
+            * g[:, None, None]).reshape(R, K)
+
+
+def swiglu_act_nvfp4(x_rows, gate_q, up_q) -> np.ndarray:
+    """SwiGLU activation of an NVFP4 expert before its BF16 rounding: x rows
+    quantised per row (NVFP4, group = one row), g and u on the dequantised
+    operands, a = silu(g) * u (FP64). gate_q, up_q: (packed [I,H/2], block
+    scales [I,H/16], group scale [1]) of one expert matrix."""
+    xd = dequantize_nvfp4(*quantize_nvfp4(x_rows, 1), 1)
+    I = gate_q[0].shape[0]
+    g = xd @ dequantize_nvfp4(*gate_q, I).T
+    u = xd @ dequantize_nvfp4(*up_q, I).T
+    return silu(g) * u
+
+
+def swiglu_expert_nvfp4(x_rows, gate_q, up_q, down_q) -> np.ndarray:
+    """One NVFP4 expert: a = swiglu_act_nvfp4 rounded to BF16, quantised per
+    row (NVFP4), y = a W_d^T on the dequantised operands (FP64)."""
+    a = bf16_round(swiglu_act_nvfp4(x_rows, gate_q, up_q))
+    ad = dequantize_nvfp4(*quantize_nvfp4(a, 1), 1)
+    H = down_q[0].shape[0]
+    return ad @ dequantize_nvfp4(*down_q, H).T
+
+
+def moe_combine_nvfp4(x, idx, weights, get_expert_q) -> np.ndarray:
+    """out[t] = sum_j weights[t,j] * f4_{idx[t,j]}(x[t]) (swiglu_expert_nvfp4)."""
+    x = np.asarray(x, dtype=F64)
+    out = np.zeros((x.shape[0], x.shape[1]), dtype=F64)
+    idx = np.asarray(idx)
+    weights = np.asarray(weights, dtype=F64)
+    for e in np.unique(idx):
+        tok, slot = np.nonzero(idx == e)
+        out[tok] += weights[tok, slot][:, None] * swiglu_expert_nvfp4(x[tok], *get_expert_q(int(e)))
+    return out

@@ -58,6 +58,9 @@ typedef enum {
 #define BEAM_FLAG_FP8_EXPERTS 8   /* workspace also holds the E4M3 activations of the
                                      FP8 expert path (beam_moe_forward_fp8 and
                                      beam_dense_mlp_forward_fp8 require this bit) */
+#define BEAM_FLAG_NVFP4_EXPERTS 16 /* workspace laid out for the NVFP4 expert path
+                                      (beam_*_forward_nvfp4 require this bit; it
+                                      excludes BEAM_FLAG_FP8_EXPERTS) */
 
 /* Shape and hyper-parameters of one MoE sublayer call.
  *   T           tokens in the batch (0 is allowed: nothing is enqueued)
@@ -158,7 +161,7 @@ size_t beam_dense_workspace_size(const beam_dense_params* p);
 
 /* Byte offsets of the dense MLP's workspace buffers, in the order and with
  * the meaning of beam_moe_workspace_layout (one expert, top_k = 1). Writes
- * min(n, 22) entries and returns how many it wrote (0 on invalid
+ * min(n, 24) entries and returns how many it wrote (0 on invalid
  * parameters). Diagnostic. */
 int beam_dense_workspace_layout(const beam_dense_params* p, size_t* offsets, int n);
 
@@ -235,6 +238,67 @@ beam_status_t beam_dense_mlp_forward_fp8(const beam_dense_params* p, const void*
                                          void* out, void* workspace, size_t workspace_bytes,
                                          void* stream);
 
+/* ---------------------------------------------------------------------------
+ * NVFP4 expert weights.
+ * [P5] section 四套权重的账，自己算一遍: the NVFP4 checkpoint packs every
+ * routed-expert weight as two 4-bit values per byte (its U8 count is half
+ * the expert parameters) and keeps the rest in BF16; section 上手前的五个坑:
+ * NVFP4 is packed by modelopt and runs on the FP4 tensor-core path. The
+ * pages fix neither block size nor scale types; this library reads them as:
+ *   elements E2M1 (0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives), two per byte,
+ *   the even element in the low nibble; one E4M3 block scale per 16
+ *   elements along K; one FP32 scale per group of rows (an expert matrix
+ *   for weights, one row for activations). In FP32 with IEEE division:
+ *     g = amax_group / 2688;  s_b = E4M3(amax_b / (6 g));
+ *     q_i = E2M1(v_i * (1 / (s_b g)))   (round to nearest even, saturating;
+ *                                        q = 0 where s_b = 0)
+ *   and v is dequantised as E2M1(q) * s_b * g.
+ * Block-scale layout ("SF groups"): one 512-byte group per 128-row tile and
+ * K = 64 step, group index (r / 128) * (K / 64) + k / 64, byte
+ * (r % 32) * 16 + ((r % 128) / 32) * 4 + (k % 64) / 16. A matrix of R rows
+ * (R a multiple of 128) and K columns has R * K / 16 bytes of scales.
+ * ------------------------------------------------------------------------- */
+
+/* NVFP4 quantiser: rows x K bf16 (device) -> codes [rows, K/2] uint8, block
+ * scales [rows * K / 16] uint8 in the SF-group layout above, group scales
+ * [rows / rows_per_group] fp32. rows must be a multiple of 128 and of
+ * rows_per_group, K a multiple of 64. Expert weights: W_gate / W_up [E,I,H]
+ * with rows = E*I, K = H, rows_per_group = I (one scale per expert matrix);
+ * W_down [E,H,I] with rows = E*H, K = I, rows_per_group = H. */
+beam_status_t beam_quantize_nvfp4(const void* src, long long rows, int K, int rows_per_group,
+                                  void* codes, void* block_scales, float* group_scales,
+                                  void* stream);
+
+/* The MoE sublayer with NVFP4 expert weights: as beam_moe_forward_fp8 with
+ * E4M3 replaced by NVFP4 -- x quantised per token, the BF16 SwiGLU output per
+ * (token, expert) row, the FP4 tensor cores (kind::mxf4nvf4 with the E4M3
+ * block scales) accumulating in FP32, group scales applied to the FP32
+ * accumulators. Each expert weight is (codes, block scales, per-expert FP32
+ * scale) as beam_quantize_nvfp4 writes them:
+ *   wq_gate, wq_up [E,I,H/2] uint8; wsf_gate, wsf_up [E*I*H/16] uint8;
+ *   wg_gate, wg_up [E] fp32; wq_down [E,H,I/2]; wsf_down [E*H*I/16];
+ *   wg_down [E]. H and I must be multiples of 256; p->flags must include
+ * BEAM_FLAG_NVFP4_EXPERTS. */
+beam_status_t beam_moe_forward_nvfp4(const beam_moe_params* p, const void* x_in,
+                                     const float* w_router, const float* logit_bias,
+                                     const void* wq_gate, const void* wsf_gate, const float* wg_gate,
+                                     const void* wq_up, const void* wsf_up, const float* wg_up,
+                                     const void* wq_down, const void* wsf_down, const float* wg_down,
+                                     const float* pre_gain, const float* post_gain, void* out,
+                                     int32_t* topk_idx, float* topk_w, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/* The dense SwiGLU MLP with NVFP4 weights (one expert: the group scales are
+ * one float each). p->flags must include BEAM_FLAG_NVFP4_EXPERTS. */
+beam_status_t beam_dense_mlp_forward_nvfp4(const beam_dense_params* p, const void* x_in,
+                                           const void* wq_gate, const void* wsf_gate,
+                                           const float* wg_gate, const void* wq_up,
+                                           const void* wsf_up, const float* wg_up,
+                                           const void* wq_down, const void* wsf_down,
+                                           const float* wg_down, const float* pre_gain,
+                                           const float* post_gain, void* out, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
 /* One scaled residual update ([P1] 残差流):
  *   h_out = bf16( sqrt((k-1)/k) * h_prev + (1/sqrt(k)) * n ),
  *   n = apply_norm ? RMSNorm(sub_out) * post_gain : sub_out   (FP32 math)
@@ -304,11 +368,18 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
  * expert histograms, 13 per-block expert offsets, 14 gate/up work list,
  * 15 down work list, 16 pair -> row map [T*top_k] int32, 17 the router
  * weight split into three BF16 pieces [E, 3H], 18 the router GEMM's work
- * list (tensor-core router only), and with BEAM_FLAG_FP8_EXPERTS: 19 per-row
- * scales of the quantised x [T*top_k] fp32 (the quantised x itself occupies
- * entry 8), 20 E4M3 activations [T*top_k,I] uint8, 21 their row scales
- * [T*top_k] fp32. Writes min(n, 22) entries and returns how many it wrote
- * (0 on invalid parameters). */
+ * list (tensor-core router only), and with BEAM_FLAG_FP8_EXPERTS or
+ * BEAM_FLAG_NVFP4_EXPERTS: 19 scales of the quantised x [rows] fp32 (the
+ * quantised x itself occupies entry 8), 20 E4M3 / NVFP4 activation codes,
+ * 21 their row scales [rows] fp32; with BEAM_FLAG_NVFP4_EXPERTS also 22 the
+ * block scales of x and 23 those of the activations (the SF-group layout
+ * with token tiles of 32 or 128 rows -- the GEMM's token tile -- in place
+ * of 128-row weight tiles: group (r / tile) * (K / 64) + k / 64, byte
+ * (r % 32) * 16 + ((r % tile) / 32) * 4 + (k % 64) / 16).
+ * Row-indexed buffers (6-10, 19-23) hold rows = T*top_k rows, or with NVFP4
+ * every expert's rows padded to the token tile (32 or 128). Writes
+ * min(n, 24) entries and returns how many it wrote (0 on invalid
+ * parameters). */
 int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n);
 
 /* Launches one block whose single thread waits on a shared-memory barrier

@@ -28,12 +28,13 @@ FLAG_PRE_NORM = 1
 FLAG_FP32_OUT = 2
 FLAG_RETURN_SCORES = 4
 FLAG_FP8_EXPERTS = 8
+FLAG_NVFP4_EXPERTS = 16
 
 # names of the workspace buffers, in beam_moe_workspace_layout() order
 LAYOUT_NAMES = ("xn", "part", "topk_idx", "topk_w", "counts", "offsets", "row_token",
                 "row_weight", "xperm", "act", "y", "n_units", "blk_hist", "blk_off",
                 "units_gu", "units_dn", "pair_row", "router_w3", "router_units",
-                "x_scale", "act_q", "act_scale")
+                "x_scale", "act_q", "act_scale", "x_sf", "act_sf")
 
 # every symbol include/beam_moe.h declares
 EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static",
@@ -41,7 +42,8 @@ EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static"
             "beam_residual_step", "beam_status", "beam_last_error_string",
             "beam_moe_workspace_layout", "beam_debug_wait_timeout", "beam_profile_enable",
             "beam_profile_read", "beam_quantize_e4m3_rows", "beam_moe_forward_fp8",
-            "beam_dense_mlp_forward_fp8", "beam_dense_workspace_layout")
+            "beam_dense_mlp_forward_fp8", "beam_dense_workspace_layout",
+            "beam_quantize_nvfp4", "beam_moe_forward_nvfp4", "beam_dense_mlp_forward_nvfp4")
 
 
 class BeamError(RuntimeError):
@@ -100,6 +102,12 @@ def lib() -> ctypes.CDLL:
         L.beam_moe_forward_fp8.restype = i32
         L.beam_dense_mlp_forward_fp8.argtypes = [D] + [vp] * 11 + [sz, vp]
         L.beam_dense_mlp_forward_fp8.restype = i32
+        L.beam_quantize_nvfp4.argtypes = [vp, ctypes.c_longlong, i32, i32, vp, vp, vp, vp]
+        L.beam_quantize_nvfp4.restype = i32
+        L.beam_moe_forward_nvfp4.argtypes = [P] + [vp] * 18 + [sz, vp]
+        L.beam_moe_forward_nvfp4.restype = i32
+        L.beam_dense_mlp_forward_nvfp4.argtypes = [D] + [vp] * 14 + [sz, vp]
+        L.beam_dense_mlp_forward_nvfp4.restype = i32
         L.beam_residual_step.argtypes = [vp, vp, i32, i32, i32, vp, f32, i32, i32, vp, vp]
         L.beam_residual_step.restype = i32
         L.beam_status.argtypes = [vp]
@@ -286,6 +294,62 @@ def dense_forward_fp8(T, H, I, x, gate_q, up_q, down_q, pre_gain=None, post_gain
         ctypes.byref(p), _ptr(x), _ptr(gate_q[0]), _ptr(gate_q[1]), _ptr(up_q[0]),
         _ptr(up_q[1]), _ptr(down_q[0]), _ptr(down_q[1]), _ptr(pre_gain), _ptr(post_gain),
         _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def quantize_nvfp4(w, rows_per_group=None, stream=None):
+    """beam_quantize_nvfp4 over the last dimension of a bf16 tensor whose
+    leading dimensions flatten to a multiple of 128 rows. rows_per_group
+    defaults to the second-to-last dimension (one scale per matrix of a
+    [E, N, K] expert tensor). Returns (codes uint8 [..., K/2], block scales
+    uint8 [rows * K / 16] in the SF-group layout, group scales fp32)."""
+    K = w.shape[-1]
+    rows = w.numel() // K
+    if rows_per_group is None:
+        rows_per_group = w.shape[-2] if w.dim() >= 2 else rows
+    codes = torch.empty(w.shape[:-1] + (K // 2,), dtype=torch.uint8, device=w.device)
+    sf = torch.empty(rows * K // 16, dtype=torch.uint8, device=w.device)
+    g = torch.empty(rows // rows_per_group, dtype=torch.float32, device=w.device)
+    _check(lib().beam_quantize_nvfp4(_ptr(w), rows, K, rows_per_group, _ptr(codes), _ptr(sf),
+                                     _ptr(g), _stream(stream)))
+    return codes, sf, g
+
+
+def forward_nvfp4(p: Params, x, w_router, gate_q, up_q, down_q, bias=None, pre_gain=None,
+                  post_gain=None, out=None, topk_idx=None, topk_w=None, workspace=None,
+                  stream=None):
+    """beam_moe_forward_nvfp4; gate_q, up_q, down_q are (codes, block scales,
+    group scales) as quantize_nvfp4 returns them. p.flags must hold
+    FLAG_NVFP4_EXPERTS."""
+    dev = x.device
+    if out is None:
+        dt = torch.float32 if (p.flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((p.T, p.H), dtype=dt, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(p, dev)
+    _check(lib().beam_moe_forward_nvfp4(
+        ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(bias),
+        *[_ptr(t) for q in (gate_q, up_q, down_q) for t in q],
+        _ptr(pre_gain), _ptr(post_gain), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def dense_forward_nvfp4(T, H, I, x, gate_q, up_q, down_q, pre_gain=None, post_gain=None,
+                        rms_eps=1e-6, residual_k=0, flags=FLAG_NVFP4_EXPERTS, out=None,
+                        workspace=None, stream=None):
+    """beam_dense_mlp_forward_nvfp4; weights as (codes, block scales, group
+    scales) triples."""
+    p = DenseParams(T, H, I, rms_eps, residual_k, flags)
+    if out is None:
+        dt = torch.float32 if (flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((T, H), dtype=dt, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(dense_workspace_size(p), dtype=torch.uint8, device=x.device)
+    _check(lib().beam_dense_mlp_forward_nvfp4(
+        ctypes.byref(p), _ptr(x), *[_ptr(t) for q in (gate_q, up_q, down_q) for t in q],
+        _ptr(pre_gain), _ptr(post_gain), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
     return out
 
 

@@ -116,6 +116,8 @@ enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2, PATH_PAIR = 3, PATH_MI
 GemmPath choose_path(const beam_moe_params& p) {
   const long long pairs = static_cast<long long>(p.T) * p.top_k;
   if (pairs <= 24LL * p.E) return PATH_W32;
+  // NVFP4 runs on the weight-major kernels (128-token tiles when many tokens)
+  if (p.flags & BEAM_FLAG_NVFP4_EXPERTS) return PATH_W128;
   if (p.H % 256 == 0) {
     const char* v = std::getenv("BEAM_PREFILL_GEMM");
     if (v != nullptr && std::strcmp(v, "tm") == 0) return PATH_TM;
@@ -149,10 +151,15 @@ int choose_router_ks(const beam_moe_params& p, int num_sms) {
   return best;
 }
 
-constexpr int kLayoutEntries = 22;
+constexpr int kLayoutEntries = 24;
 
 struct Layout {
   size_t off[kLayoutEntries];
+  // rows of the expert-ordered layout: T * top_k, or with NVFP4 experts every
+  // expert's rows padded to a multiple of `pad` (the token tile), so each
+  // tile starts at a multiple of 32 inside its 128-row block-scale tile
+  long long rows;
+  int pad;
   size_t total;
   int KS, NB, NT;
   GemmPath path;
@@ -162,7 +169,7 @@ struct Layout {
 enum {
   L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_Y,
   L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW, L_WR3, L_RUNITS,
-  L_XSCALE, L_ACTQ, L_ASCALE
+  L_XSCALE, L_ACTQ, L_ASCALE, L_XSF, L_ASF
 };
 
 // Bytes of the router's unit list and count (tensor-core router only).
@@ -209,9 +216,14 @@ beam_status_t check_params(const beam_moe_params* p) {
     return fail(BEAM_ERR_INVALID_ARG, "rms_eps must be >= 0 and finite");
   if (p->residual_k == 1 || p->residual_k < 0)
     return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", p->residual_k);
-  if (p->flags &
-      ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_RETURN_SCORES | BEAM_FLAG_FP8_EXPERTS))
+  if (p->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_RETURN_SCORES |
+                   BEAM_FLAG_FP8_EXPERTS | BEAM_FLAG_NVFP4_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  if ((p->flags & BEAM_FLAG_FP8_EXPERTS) && (p->flags & BEAM_FLAG_NVFP4_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP8_EXPERTS and BEAM_FLAG_NVFP4_EXPERTS exclude each other");
+  if ((p->flags & BEAM_FLAG_NVFP4_EXPERTS) && (p->H % 256 || p->I % 256))
+    return fail(BEAM_ERR_UNSUPPORTED, "NVFP4 experts need H=%d and I=%d to be multiples of 256",
+                p->H, p->I);
   if ((p->flags & BEAM_FLAG_FP32_OUT) && p->residual_k >= 2)
     return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP32_OUT applies only without the residual step");
   const long long pairs = static_cast<long long>(p->T) * p->top_k;
@@ -227,6 +239,10 @@ Layout make_layout(const beam_moe_params& p) {
   L.path = choose_path(p);
   L.NT = path_nt(L.path);
   const long long R = static_cast<long long>(p.T) * p.top_k;
+  const bool f4 = (p.flags & BEAM_FLAG_NVFP4_EXPERTS) != 0;
+  L.pad = f4 ? (L.path == PATH_W32 ? 32 : 128) : 1;
+  L.rows = f4 ? (R + (L.pad - 1) * std::min<long long>(p.E, R) + 127) / 128 * 128 : R;
+  const long long Rr = L.rows;
   const long long tiles = (R + L.NT - 1) / L.NT + p.E;
   if (L.path == PATH_PAIR || L.path == PATH_MIXED) {
     const long long groups = (R + 255) / 256 + p.E;
@@ -252,11 +268,11 @@ Layout make_layout(const beam_moe_params& p) {
   sz[L_W] = static_cast<size_t>(R) * 4;
   sz[L_COUNTS] = static_cast<size_t>(p.E) * 4;
   sz[L_OFFS] = static_cast<size_t>(p.E + 1) * 4;
-  sz[L_ROWTOK] = static_cast<size_t>(R) * 4;
-  sz[L_ROWW] = static_cast<size_t>(R) * 4;
-  sz[L_XPERM] = static_cast<size_t>(R) * p.H * 2;
-  sz[L_ACT] = static_cast<size_t>(R) * p.I * 2;
-  sz[L_Y] = static_cast<size_t>(R) * p.H * 4;
+  sz[L_ROWTOK] = static_cast<size_t>(Rr) * 4;
+  sz[L_ROWW] = static_cast<size_t>(Rr) * 4;
+  sz[L_XPERM] = static_cast<size_t>(Rr) * p.H * 2;
+  sz[L_ACT] = static_cast<size_t>(Rr) * p.I * 2;
+  sz[L_Y] = static_cast<size_t>(Rr) * p.H * 4;
   sz[L_NUNITS] = 16;
   sz[L_BLKHIST] = static_cast<size_t>(L.NB) * p.E * 4;
   sz[L_BLKOFF] = static_cast<size_t>(L.NB) * p.E * 4;
@@ -266,9 +282,12 @@ Layout make_layout(const beam_moe_params& p) {
   sz[L_WR3] = router_on_tensor_cores(p) ? static_cast<size_t>(p.E) * 3 * p.H * 2 : 0;
   sz[L_RUNITS] = router_on_tensor_cores(p) ? router_units_bytes(p) : 0;
   const bool f8 = (p.flags & BEAM_FLAG_FP8_EXPERTS) != 0;
-  sz[L_XSCALE] = f8 ? static_cast<size_t>(R) * 4 : 0;
-  sz[L_ACTQ] = f8 ? static_cast<size_t>(R) * p.I : 0;
-  sz[L_ASCALE] = f8 ? static_cast<size_t>(R) * 4 : 0;
+  sz[L_XSCALE] = (f8 || f4) ? static_cast<size_t>(Rr) * 4 : 0;
+  sz[L_ACTQ] = f8 ? static_cast<size_t>(Rr) * p.I : (f4 ? static_cast<size_t>(Rr) * p.I / 2 : 0);
+  sz[L_ASCALE] = (f8 || f4) ? static_cast<size_t>(Rr) * 4 : 0;
+  // token block scales: 512-byte groups per (token tile of L.pad rows, K = 64 step)
+  sz[L_XSF] = f4 ? static_cast<size_t>(Rr / L.pad) * (p.H / 64) * 512 : 0;
+  sz[L_ASF] = f4 ? static_cast<size_t>(Rr / L.pad) * (p.I / 64) * 512 : 0;
   size_t cur = 0;
   for (int i = 0; i < kLayoutEntries; ++i) {
     L.off[i] = cur;
@@ -324,11 +343,11 @@ beam_status_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 }
 
 // --------------------------------------------------------- GEMM launches
-template <int MODE, int NT, int STAGES, bool F8>
+template <int MODE, int NT, int STAGES, int KIND>
 beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                           const beam::GemmArgs& args, cudaStream_t st) {
-  using C = beam::GemmCfg<MODE, NT, STAGES>;
-  auto kern = beam::expert_gemm_kernel<MODE, NT, STAGES, F8>;
+  using C = beam::GemmCfg<MODE, NT, STAGES, KIND>;
+  auto kern = beam::expert_gemm_kernel<MODE, NT, STAGES, KIND>;
   static bool attr_set = false;  // per template instance
   if (!attr_set) {
     BEAM_CUDA_TRY(
@@ -454,51 +473,74 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
   return BEAM_OK;
 }
 
-// The expert weights of one call: BF16 matrices, or E4M3 codes with one FP32
-// scale per output row.
+// The expert weights of one call: BF16 matrices; E4M3 codes with one FP32
+// scale per output row; or NVFP4 codes with block scales (SF groups) and one
+// FP32 scale per expert matrix.
 struct ExpertWeights {
   const void* gate;
   const void* up;
   const void* down;
-  const float* s_gate;  // E4M3 only
+  const float* s_gate;  // E4M3: per row; NVFP4: per expert
   const float* s_up;
   const float* s_down;
-  bool f8;
+  const void* sf_gate;  // NVFP4 block scales
+  const void* sf_up;
+  const void* sf_down;
+  int kind;             // beam::KIND_*
+};
+
+// Quantised activations of the E4M3 / NVFP4 paths (workspace buffers).
+struct QuantBufs {
+  const float* xscale;   // per-row scale of the quantised x
+  const uint8_t* xsf;    // NVFP4 block scales of x
+  uint8_t* aq;           // codes of the SwiGLU output
+  float* ascale;         // its per-row scale
+  uint8_t* asf;          // NVFP4 block scales
+  const int* row_valid;  // NVFP4: row_token (< 0 on padding rows)
+  const int* rows_dev;   // NVFP4: device count of rows (offsets[E])
 };
 
 // Steps 3-4: gate/up GEMM + SwiGLU into act (bf16), then the down GEMM into
-// the per-pair FP32 outputs y. F8: the expert-ordered x (xop) and the
-// weights are E4M3 with row scales; act is quantised per row into aq before
-// the down GEMM.
-template <bool F8>
+// the per-pair FP32 outputs y. E4M3 / NVFP4: the expert-ordered x (xop) and
+// the weights are quantised; act is quantised per row (into q.aq) before
+// the down GEMM. NVFP4 runs on the weight-major kernels only.
+template <int KIND>
 beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
-                                  const ExpertWeights& w, const void* xop, const float* xscale,
-                                  __nv_bfloat16* act, uint8_t* aq, float* ascale, float* y,
-                                  int4* ugu, int4* udn, int* nunits, long long R,
-                                  cudaStream_t st) {
+                                  const ExpertWeights& w, const void* xop, const QuantBufs& q,
+                                  __nv_bfloat16* act, float* y, int4* ugu, int4* udn, int* nunits,
+                                  long long R, cudaStream_t st) {
+  constexpr bool F8 = KIND == beam::KIND_E4M3;
+  constexpr bool F4 = KIND == beam::KIND_NVFP4;
   beam_status_t s = BEAM_OK;
   const int H = prm.H, E = prm.E, I = prm.I;
-  const int KB = beam::KBlock<F8>::ELEMS;
-  // operand of the down GEMM: the bf16 act, or its E4M3 codes
-  const void* aop = F8 ? static_cast<const void*>(aq) : static_cast<const void*>(act);
+  const int KB = beam::KBlock<KIND>::ELEMS;
+  if (F4 && L.path != PATH_W32 && L.path != PATH_W128)
+    return fail(BEAM_ERR_UNSUPPORTED, "NVFP4 experts run on the weight-major GEMM kernels only");
+  const bool bytes = F8 || F4;     // TMA maps over one-byte elements (codes)
+  const int hc = F4 ? H / 2 : H;   // row length of the code matrices, in map elements
+  const int ic = F4 ? I / 2 : I;
+  // operand of the down GEMM: the bf16 act, or its codes
+  const void* aop = (F8 || F4) ? static_cast<const void*>(q.aq) : static_cast<const void*>(act);
   const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
   const uint32_t gu_box = L.path == PATH_PAIR ? 64 : 128;
   CUtensorMap m_g, m_u, m_d, m_x, m_a;
-  if ((s = make_map(&m_g, w.gate, static_cast<uint64_t>(E) * I, H, gu_box, F8)) != BEAM_OK) return s;
-  if ((s = make_map(&m_u, w.up, static_cast<uint64_t>(E) * I, H, gu_box, F8)) != BEAM_OK) return s;
-  if ((s = make_map(&m_d, w.down, static_cast<uint64_t>(E) * H, I, 128, F8)) != BEAM_OK) return s;
-  if ((s = make_map(&m_x, xop, R, H, tok_box, F8)) != BEAM_OK) return s;
-  if ((s = make_map(&m_a, aop, R, I, tok_box, F8)) != BEAM_OK) return s;
+  if ((s = make_map(&m_g, w.gate, static_cast<uint64_t>(E) * I, hc, gu_box, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_u, w.up, static_cast<uint64_t>(E) * I, hc, gu_box, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_d, w.down, static_cast<uint64_t>(E) * H, ic, 128, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_x, xop, R, hc, tok_box, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_a, aop, R, ic, tok_box, bytes)) != BEAM_OK) return s;
 
-  // E4M3: SwiGLU output -> per-row codes and scales (between the two GEMMs)
+  // SwiGLU output -> per-row codes and scales (between the two GEMMs)
   auto quant_act = [&]() -> beam_status_t {
-    if (!F8) return BEAM_OK;
-    {
-      ProfScope ps("quant_act", st);
+    if (!F8 && !F4) return BEAM_OK;
+    ProfScope ps("quant_act", st);
+    if (F8)
       beam::quant_rows_e4m3_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
-          act, nullptr, R, I, aq, ascale);
-    }
-    BEAM_LAUNCH_CHECK("quant_rows_e4m3_kernel<act>");
+          act, nullptr, R, I, q.aq, q.ascale);
+    else
+      beam::quant_rows_nvfp4_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+          act, nullptr, q.row_valid, R, q.rows_dev, I, 1, nullptr, q.aq, q.asf, q.ascale, L.pad);
+    BEAM_LAUNCH_CHECK("quant_rows_*_kernel<act>");
     return BEAM_OK;
   };
 
@@ -511,7 +553,7 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     pa.act = act;
     pa.out_ld = I;
     pa.timeout_ns = kWaitTimeoutNs;
-    pa.row_scale = xscale;
+    pa.row_scale = q.xscale;
     pa.w_scale0 = w.s_gate;
     pa.w_scale1 = w.s_up;
     beam::PairArgs pd = pa;
@@ -542,7 +584,7 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
       ta.out = act;
       ta.out_ld = I;
       ta.timeout_ns = kWaitTimeoutNs;
-      ta.row_scale = xscale;
+      ta.row_scale = q.xscale;
       ta.w_scale0 = w.s_gate;
       ta.w_scale1 = w.s_up;
       if ((s = launch_gemm_tm<0, F8>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK) return s;
@@ -560,7 +602,7 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     ta.out = act;
     ta.out_ld = I;
     ta.timeout_ns = kWaitTimeoutNs;
-    ta.row_scale = xscale;
+    ta.row_scale = q.xscale;
     ta.w_scale0 = w.s_gate;
     ta.w_scale1 = w.s_up;
     beam::TmArgs td = ta;
@@ -587,9 +629,12 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     ga.out = act;
     ga.out_ld = I;
     ga.timeout_ns = kWaitTimeoutNs;
-    ga.row_scale = xscale;
+    ga.row_scale = q.xscale;
     ga.w_scale0 = w.s_gate;
     ga.w_scale1 = w.s_up;
+    ga.a_sf0 = static_cast<const uint8_t*>(w.sf_gate);
+    ga.a_sf1 = static_cast<const uint8_t*>(w.sf_up);
+    ga.b_sf = q.xsf;
     beam::GemmArgs gd = ga;
     gd.n_units = nunits + 1;
     gd.m_tiles = H / 128;
@@ -601,14 +646,19 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     gd.row_scale = nullptr;  // the activation row scales are applied by the combine
     gd.w_scale0 = w.s_down;
     gd.w_scale1 = nullptr;
+    gd.a_sf0 = static_cast<const uint8_t*>(w.sf_down);
+    gd.a_sf1 = nullptr;
+    gd.b_sf = q.asf;
+    // stage counts: NVFP4 stages also carry the K-block's block scales
+    constexpr int S_GU32 = F4 ? 5 : 6, S_DN32 = F4 ? 9 : 10;
     if (L.path == PATH_W32) {
-      if ((s = launch_gemm<0, 32, 6, F8>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+      if ((s = launch_gemm<0, 32, S_GU32, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
       if ((s = quant_act()) != BEAM_OK) return s;
-      if ((s = launch_gemm<1, 32, 10, F8>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+      if ((s = launch_gemm<1, 32, S_DN32, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
     } else {
-      if ((s = launch_gemm<0, 128, 4, F8>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+      if ((s = launch_gemm<0, 128, 4, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
       if ((s = quant_act()) != BEAM_OK) return s;
-      if ((s = launch_gemm<1, 128, 6, F8>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
+      if ((s = launch_gemm<1, 128, 6, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
     }
   }
   return BEAM_OK;
@@ -641,10 +691,20 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   int4* ugu = reinterpret_cast<int4*>(ws + L.off[L_UGU]);
   int4* udn = reinterpret_cast<int4*>(ws + L.off[L_UDN]);
   int* nunits = reinterpret_cast<int*>(ws + L.off[L_NUNITS]);
-  // E4M3 path: x codes (in the permuted-x region) and the activations' codes
-  float* xscale = w.f8 ? reinterpret_cast<float*>(ws + L.off[L_XSCALE]) : nullptr;
-  uint8_t* actq = w.f8 ? ws + L.off[L_ACTQ] : nullptr;
-  float* ascale = w.f8 ? reinterpret_cast<float*>(ws + L.off[L_ASCALE]) : nullptr;
+  // E4M3 / NVFP4 paths: x codes (in the permuted-x region), the activations'
+  // codes, their scales
+  const bool quant = w.kind != beam::KIND_BF16;
+  const bool f4 = w.kind == beam::KIND_NVFP4;
+  QuantBufs qb{};
+  qb.xscale = quant ? reinterpret_cast<float*>(ws + L.off[L_XSCALE]) : nullptr;
+  qb.xsf = f4 ? ws + L.off[L_XSF] : nullptr;
+  qb.aq = quant ? ws + L.off[L_ACTQ] : nullptr;
+  qb.ascale = quant ? reinterpret_cast<float*>(ws + L.off[L_ASCALE]) : nullptr;
+  qb.asf = f4 ? ws + L.off[L_ASF] : nullptr;
+  qb.row_valid = row_tok;
+  qb.rows_dev = offs + E;
+  // rows of the expert-ordered layout (NVFP4: padded, bounded by L.rows)
+  const long long Rl = f4 ? L.rows : R;
 
   const int NB = dense ? 1 : L.NB;
   if (dense) {
@@ -673,10 +733,10 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     else
       beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs,
                                                         ugu, nunits, L.NT, I / 128,
-                                                        path_mt_down(L.path, H));
+                                                        path_mt_down(L.path, H), L.pad, row_tok);
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
-  if (w.f8) {
+  if (quant) {
     // quantise x per token, gathered into expert order (identity when dense)
     if (!dense) {
       ProfScope ps("expert_scatter", st);
@@ -686,10 +746,15 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     BEAM_LAUNCH_CHECK("expert_scatter_kernel");
     {
       ProfScope ps("quant_x", st);
-      beam::quant_rows_e4m3_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
-          x, dense ? nullptr : row_tok, R, H, ws + L.off[L_XPERM], xscale);
+      if (f4)
+        beam::quant_rows_nvfp4_kernel<<<static_cast<unsigned>((Rl + 7) / 8), 256, 0, st>>>(
+            x, dense ? nullptr : row_tok, row_tok, Rl, offs + E, H, 1, nullptr,
+            ws + L.off[L_XPERM], ws + L.off[L_XSF], const_cast<float*>(qb.xscale), L.pad);
+      else
+        beam::quant_rows_e4m3_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+            x, dense ? nullptr : row_tok, R, H, ws + L.off[L_XPERM], const_cast<float*>(qb.xscale));
     }
-    BEAM_LAUNCH_CHECK("quant_rows_e4m3_kernel<x>");
+    BEAM_LAUNCH_CHECK("quant_rows_*_kernel<x>");
   } else if (dense) {
     xperm = const_cast<__nv_bfloat16*>(x);  // identity permutation: read x in place
   } else {
@@ -708,13 +773,12 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   }
 
   // 3. gate/up GEMM + SwiGLU -> act, 4. down GEMM -> per-pair y
-  if (w.f8) {
-    s = launch_expert_gemms<true>(*p, L, w, xperm, xscale, act, actq, ascale, y, ugu, udn, nunits,
-                                  R, st);
-  } else {
-    s = launch_expert_gemms<false>(*p, L, w, xperm, nullptr, act, nullptr, nullptr, y, ugu, udn,
-                                   nunits, R, st);
-  }
+  if (w.kind == beam::KIND_NVFP4)
+    s = launch_expert_gemms<beam::KIND_NVFP4>(*p, L, w, xperm, qb, act, y, ugu, udn, nunits, Rl, st);
+  else if (w.kind == beam::KIND_E4M3)
+    s = launch_expert_gemms<beam::KIND_E4M3>(*p, L, w, xperm, qb, act, y, ugu, udn, nunits, R, st);
+  else
+    s = launch_expert_gemms<beam::KIND_BF16>(*p, L, w, xperm, qb, act, y, ugu, udn, nunits, R, st);
   if (s != BEAM_OK) return s;
 
   // 5. weighted combine, then post-norm + scaled residual (or the output)
@@ -726,11 +790,11 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     ProfScope ps("combine_rows", st);
     if (p->flags & BEAM_FLAG_FP32_OUT)
       beam::combine_rows_kernel<true><<<T, beam::COMBINE_THREADS, 0, st>>>(
-          y, ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
+          y, qb.ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
           p->rms_eps, a, b, resid);
     else
       beam::combine_rows_kernel<false><<<T, beam::COMBINE_THREADS, 0, st>>>(
-          y, ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
+          y, qb.ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
           p->rms_eps, a, b, resid);
   }
   BEAM_LAUNCH_CHECK("combine_rows_kernel");
@@ -791,19 +855,28 @@ beam_status_t moe_forward_impl(const beam_moe_params* p, const void* x_in, const
                                size_t workspace_bytes, void* stream) {
   beam_status_t s = check_params(p);
   if (s != BEAM_OK) return s;
-  if (w.f8 && !(p->flags & BEAM_FLAG_FP8_EXPERTS))
+  if (w.kind == beam::KIND_E4M3 && !(p->flags & BEAM_FLAG_FP8_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG,
                 "the E4M3 path needs BEAM_FLAG_FP8_EXPERTS in flags (and a workspace sized with it)");
+  if (w.kind == beam::KIND_NVFP4 && !(p->flags & BEAM_FLAG_NVFP4_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG,
+                "the NVFP4 path needs BEAM_FLAG_NVFP4_EXPERTS in flags (and a workspace sized with it)");
+  if (w.kind != beam::KIND_NVFP4 && (p->flags & BEAM_FLAG_NVFP4_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_NVFP4_EXPERTS is for the NVFP4 entry points");
   if (p->T == 0) return BEAM_OK;
   if (!x_in || !w_router || !w.gate || !w.up || !w.down || !out || !workspace)
     return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (w.f8 && (!w.s_gate || !w.s_up || !w.s_down))
-    return fail(BEAM_ERR_INVALID_ARG, "the E4M3 weights need their row scales");
+  if (w.kind != beam::KIND_BF16 && (!w.s_gate || !w.s_up || !w.s_down))
+    return fail(BEAM_ERR_INVALID_ARG, "the quantised weights need their scales");
+  if (w.kind == beam::KIND_NVFP4 && (!w.sf_gate || !w.sf_up || !w.sf_down))
+    return fail(BEAM_ERR_INVALID_ARG, "the NVFP4 weights need their block scales");
   const void* ptrs[] = {x_in, w_router, w.gate, w.up, w.down, out, workspace};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
-  if (w.f8 && (!aligned16(w.s_gate) || !aligned16(w.s_up) || !aligned16(w.s_down)))
+  if (w.kind != beam::KIND_BF16 && (!aligned16(w.s_gate) || !aligned16(w.s_up) || !aligned16(w.s_down)))
     return fail(BEAM_ERR_INVALID_ARG, "weight scales must be 16-byte aligned");
+  if (w.kind == beam::KIND_NVFP4 && (!aligned16(w.sf_gate) || !aligned16(w.sf_up) || !aligned16(w.sf_down)))
+    return fail(BEAM_ERR_INVALID_ARG, "block scales must be 16-byte aligned");
   if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
     return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
   if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
@@ -836,7 +909,8 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in, const
                                const void* w_down, const float* pre_gain, const float* post_gain,
                                void* out, int32_t* topk_idx, float* topk_w, void* workspace,
                                size_t workspace_bytes, void* stream) {
-  const ExpertWeights w{w_gate, w_up, w_down, nullptr, nullptr, nullptr, false};
+  const ExpertWeights w{w_gate, w_up, w_down, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, nullptr, beam::KIND_BF16};
   return moe_forward_impl(p, x_in, w_router, logit_bias, w, pre_gain, post_gain, out, topk_idx,
                           topk_w, workspace, workspace_bytes, stream);
 }
@@ -848,9 +922,58 @@ beam_status_t beam_moe_forward_fp8(const beam_moe_params* p, const void* x_in,
                                    const float* pre_gain, const float* post_gain, void* out,
                                    int32_t* topk_idx, float* topk_w, void* workspace,
                                    size_t workspace_bytes, void* stream) {
-  const ExpertWeights w{wq_gate, wq_up, wq_down, ws_gate, ws_up, ws_down, true};
+  const ExpertWeights w{wq_gate, wq_up, wq_down, ws_gate, ws_up, ws_down,
+                        nullptr, nullptr, nullptr, beam::KIND_E4M3};
   return moe_forward_impl(p, x_in, w_router, logit_bias, w, pre_gain, post_gain, out, topk_idx,
                           topk_w, workspace, workspace_bytes, stream);
+}
+
+beam_status_t beam_moe_forward_nvfp4(const beam_moe_params* p, const void* x_in,
+                                     const float* w_router, const float* logit_bias,
+                                     const void* wq_gate, const void* wsf_gate, const float* wg_gate,
+                                     const void* wq_up, const void* wsf_up, const float* wg_up,
+                                     const void* wq_down, const void* wsf_down, const float* wg_down,
+                                     const float* pre_gain, const float* post_gain, void* out,
+                                     int32_t* topk_idx, float* topk_w, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  const ExpertWeights w{wq_gate, wq_up, wq_down, wg_gate, wg_up, wg_down,
+                        wsf_gate, wsf_up, wsf_down, beam::KIND_NVFP4};
+  return moe_forward_impl(p, x_in, w_router, logit_bias, w, pre_gain, post_gain, out, topk_idx,
+                          topk_w, workspace, workspace_bytes, stream);
+}
+
+beam_status_t beam_quantize_nvfp4(const void* src, long long rows, int K, int rows_per_group,
+                                  void* codes, void* block_scales, float* group_scales,
+                                  void* stream) {
+  if (rows < 0 || rows % 128 || K <= 0 || K % 64 || rows_per_group <= 0 ||
+      (rows > 0 && rows % rows_per_group))
+    return fail(BEAM_ERR_INVALID_ARG,
+                "rows=%lld K=%d rows_per_group=%d: rows a multiple of 128 and of rows_per_group, "
+                "K a positive multiple of 64", rows, K, rows_per_group);
+  if (rows > (1LL << 34)) return fail(BEAM_ERR_UNSUPPORTED, "rows=%lld is too large", rows);
+  if (rows == 0) return BEAM_OK;
+  if (!src || !codes || !block_scales || !group_scales)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(src) || !aligned16(codes) || !aligned16(block_scales) || !aligned16(group_scales))
+    return fail(BEAM_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long groups = rows / rows_per_group;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(src);
+  unsigned* gmax = reinterpret_cast<unsigned*>(group_scales);
+  ProfScope ps("quant_nvfp4", st);
+  // group maxima (as float bits, in the output array), quantise, then g
+  BEAM_CUDA_TRY(cudaMemsetAsync(gmax, 0, static_cast<size_t>(groups) * 4, st));
+  beam::group_amax_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(x, rows, K,
+                                                                                rows_per_group, gmax);
+  BEAM_LAUNCH_CHECK("group_amax_kernel");
+  beam::quant_rows_nvfp4_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+      x, nullptr, nullptr, rows, nullptr, K, rows_per_group, gmax,
+      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(block_scales), nullptr, 128);
+  BEAM_LAUNCH_CHECK("quant_rows_nvfp4_kernel");
+  beam::nvfp4_group_scale_kernel<<<static_cast<unsigned>((groups + 255) / 256), 256, 0, st>>>(
+      group_scales, groups);
+  BEAM_LAUNCH_CHECK("nvfp4_group_scale_kernel");
+  return BEAM_OK;
 }
 
 beam_status_t beam_quantize_e4m3_rows(const void* src, long long rows, int K, void* q,
@@ -887,8 +1010,14 @@ beam_status_t check_dense(const beam_dense_params* d) {
     return fail(BEAM_ERR_INVALID_ARG, "rms_eps must be >= 0 and finite");
   if (d->residual_k == 1 || d->residual_k < 0)
     return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", d->residual_k);
-  if (d->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_FP8_EXPERTS))
+  if (d->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_FP8_EXPERTS |
+                   BEAM_FLAG_NVFP4_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
+  if ((d->flags & BEAM_FLAG_FP8_EXPERTS) && (d->flags & BEAM_FLAG_NVFP4_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP8_EXPERTS and BEAM_FLAG_NVFP4_EXPERTS exclude each other");
+  if ((d->flags & BEAM_FLAG_NVFP4_EXPERTS) && (d->H % 256 || d->I % 256))
+    return fail(BEAM_ERR_UNSUPPORTED, "NVFP4 weights need H=%d and I=%d to be multiples of 256",
+                d->H, d->I);
   if ((d->flags & BEAM_FLAG_FP32_OUT) && d->residual_k >= 2)
     return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP32_OUT applies only without the residual step");
   return BEAM_OK;
@@ -936,19 +1065,28 @@ beam_status_t dense_forward_impl(const beam_dense_params* d, const void* x_in,
                                  size_t workspace_bytes, void* stream) {
   beam_status_t s = check_dense(d);
   if (s != BEAM_OK) return s;
-  if (w.f8 && !(d->flags & BEAM_FLAG_FP8_EXPERTS))
+  if (w.kind == beam::KIND_E4M3 && !(d->flags & BEAM_FLAG_FP8_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG,
                 "the E4M3 path needs BEAM_FLAG_FP8_EXPERTS in flags (and a workspace sized with it)");
+  if (w.kind == beam::KIND_NVFP4 && !(d->flags & BEAM_FLAG_NVFP4_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG,
+                "the NVFP4 path needs BEAM_FLAG_NVFP4_EXPERTS in flags (and a workspace sized with it)");
+  if (w.kind != beam::KIND_NVFP4 && (d->flags & BEAM_FLAG_NVFP4_EXPERTS))
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_NVFP4_EXPERTS is for the NVFP4 entry points");
   if (d->T == 0) return BEAM_OK;
   if (!x_in || !w.gate || !w.up || !w.down || !out || !workspace)
     return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (w.f8 && (!w.s_gate || !w.s_up || !w.s_down))
-    return fail(BEAM_ERR_INVALID_ARG, "the E4M3 weights need their row scales");
+  if (w.kind != beam::KIND_BF16 && (!w.s_gate || !w.s_up || !w.s_down))
+    return fail(BEAM_ERR_INVALID_ARG, "the quantised weights need their scales");
+  if (w.kind == beam::KIND_NVFP4 && (!w.sf_gate || !w.sf_up || !w.sf_down))
+    return fail(BEAM_ERR_INVALID_ARG, "the NVFP4 weights need their block scales");
   const void* ptrs[] = {x_in, w.gate, w.up, w.down, out, workspace};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
-  if (w.f8 && (!aligned16(w.s_gate) || !aligned16(w.s_up) || !aligned16(w.s_down)))
+  if (w.kind != beam::KIND_BF16 && (!aligned16(w.s_gate) || !aligned16(w.s_up) || !aligned16(w.s_down)))
     return fail(BEAM_ERR_INVALID_ARG, "weight scales must be 16-byte aligned");
+  if (w.kind == beam::KIND_NVFP4 && (!aligned16(w.sf_gate) || !aligned16(w.sf_up) || !aligned16(w.sf_down)))
+    return fail(BEAM_ERR_INVALID_ARG, "block scales must be 16-byte aligned");
   if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
     return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
   if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
@@ -982,7 +1120,8 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_params* d, const void* x_i
                                      const void* w_gate, const void* w_up, const void* w_down,
                                      const float* pre_gain, const float* post_gain, void* out,
                                      void* workspace, size_t workspace_bytes, void* stream) {
-  const ExpertWeights w{w_gate, w_up, w_down, nullptr, nullptr, nullptr, false};
+  const ExpertWeights w{w_gate, w_up, w_down, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, nullptr, beam::KIND_BF16};
   return dense_forward_impl(d, x_in, w, pre_gain, post_gain, out, workspace, workspace_bytes,
                             stream);
 }
@@ -994,7 +1133,22 @@ beam_status_t beam_dense_mlp_forward_fp8(const beam_dense_params* d, const void*
                                          const float* pre_gain, const float* post_gain,
                                          void* out, void* workspace, size_t workspace_bytes,
                                          void* stream) {
-  const ExpertWeights w{wq_gate, wq_up, wq_down, ws_gate, ws_up, ws_down, true};
+  const ExpertWeights w{wq_gate, wq_up, wq_down, ws_gate, ws_up, ws_down,
+                        nullptr, nullptr, nullptr, beam::KIND_E4M3};
+  return dense_forward_impl(d, x_in, w, pre_gain, post_gain, out, workspace, workspace_bytes,
+                            stream);
+}
+
+beam_status_t beam_dense_mlp_forward_nvfp4(const beam_dense_params* d, const void* x_in,
+                                           const void* wq_gate, const void* wsf_gate,
+                                           const float* wg_gate, const void* wq_up,
+                                           const void* wsf_up, const float* wg_up,
+                                           const void* wq_down, const void* wsf_down,
+                                           const float* wg_down, const float* pre_gain,
+                                           const float* post_gain, void* out, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  const ExpertWeights w{wq_gate, wq_up, wq_down, wg_gate, wg_up, wg_down,
+                        wsf_gate, wsf_up, wsf_down, beam::KIND_NVFP4};
   return dense_forward_impl(d, x_in, w, pre_gain, post_gain, out, workspace, workspace_bytes,
                             stream);
 }
@@ -1035,6 +1189,8 @@ beam_status_t beam_status(void* stream) {
   if (v == 0) return BEAM_OK;
   const int zero = 0;
   BEAM_CUDA_TRY(cudaMemcpyToSymbol(beam::g_beam_err, &zero, sizeof(int)));
+  if (v & beam::DEV_ERR_ALIGN)
+    return fail(BEAM_ERR_DEVICE_FLAG, "a device-side copy address was misaligned and skipped (flag 0x%x)", v);
   if (v & beam::DEV_ERR_TIMEOUT) return fail(BEAM_ERR_TIMEOUT, "a device-side wait timed out (flag 0x%x)", v);
   return fail(BEAM_ERR_DEVICE_FLAG, "device error flag 0x%x", v);
 }

@@ -39,6 +39,7 @@ namespace beam {
 
 __device__ int g_beam_err;  // per-device error word, read by beam_status()
 constexpr int DEV_ERR_TIMEOUT = 1;
+constexpr int DEV_ERR_ALIGN = 2;  // a bulk copy address was not 16-byte aligned (copy skipped)
 
 struct GemmArgs {
   const int4* units;          // token tiles {expert, first row, rows, 0} (MODE 0/1)
@@ -50,13 +51,20 @@ struct GemmArgs {
   int out_ld;
   int m_tiles;                // weight row-tiles per token tile (I/128 or H/128)
   unsigned long long timeout_ns;
-  // E4M3 operands only: per token-row scale of x (MODE 0; in MODE 1 the
-  // activation row scale is a factor of the whole output row, applied by the
-  // combine) and per weight-row scales (gate and up for MODE 0, down for
-  // MODE 1), indexed expert * a_rows_per_expert + row
+  // E4M3 and NVFP4 operands: FP32 scale of each token row of x (MODE 0; in
+  // MODE 1 the activation row scale is a factor of the whole output row,
+  // applied by the combine), and the weight scales (gate and up for MODE 0,
+  // down for MODE 1): E4M3 one per weight row, indexed expert *
+  // a_rows_per_expert + row; NVFP4 one per expert matrix, indexed by expert.
   const float* row_scale;
   const float* w_scale0;
   const float* w_scale1;
+  // NVFP4 only: 512-byte block-scale groups (one K = 64 step of a row tile),
+  // [rows / tile][K / 64][512], of the weights (gate / up or down; tile 128)
+  // and of the expert-ordered token rows (tile NT)
+  const uint8_t* a_sf0;
+  const uint8_t* a_sf1;
+  const uint8_t* b_sf;
 };
 
 // Unit u of a GEMM: token tile u / m_tiles of the tile list and weight
@@ -74,20 +82,31 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int MODE, int NT, int STAGES>
+template <int MODE, int NT, int STAGES, int KIND = KIND_BF16>
 struct GemmCfg {
   static_assert(MODE == 0 || MODE == 1, "mode");
-  static constexpr int A_TILE = 128 * 128;  // 128 rows x 128 bytes (64 bf16 or 128 e4m3)
+  static constexpr int A_TILE = 128 * 128;  // 128 rows x 128 bytes (64 bf16, 128 e4m3, 256 e2m1)
   static constexpr int A_BYTES = (MODE == 0 ? 2 : 1) * A_TILE;
   static constexpr int B_BYTES = NT * 128;  // NT rows x 128 bytes
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // NVFP4: per stage the block scales of the K-block (four 512-byte groups
+  // per operand matrix) follow the operand tiles
+  static constexpr int SF_A_BYTES = KIND == KIND_NVFP4 ? (MODE == 0 ? 2 : 1) * 2048 : 0;
+  static constexpr int SF_B_BYTES = KIND == KIND_NVFP4 ? 2048 : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_A_BYTES + SF_B_BYTES;
   static constexpr int ACC_COLS = (MODE == 0 ? 2 : 1) * NT;
-  static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int TMEM_COLS = pow2_at_least(NBUF * ACC_COLS);
+  // NVFP4: each stage has its own TMEM columns for the scales it copies in
+  // (four columns per group), after the accumulators
+  static constexpr int SF_COLS = KIND == KIND_NVFP4 ? 4 * 4 * (MODE == 0 ? 3 : 2) : 0;
+  static constexpr int SF_B_COL = KIND == KIND_NVFP4 ? 16 * (MODE == 0 ? 2 : 1) : 0;
+  static constexpr int NBUF = (2 * ACC_COLS + STAGES * SF_COLS <= 512) ? 2 : 1;
+  static constexpr int SF_TMEM_BASE = NBUF * ACC_COLS;
+  static constexpr int TMEM_COLS =
+      KIND == KIND_NVFP4 ? 512 : pow2_at_least(NBUF * ACC_COLS);
   static constexpr int BAR_BYTES = (2 * STAGES + 2 * NBUF + 1) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "token tile");
-  static_assert(TMEM_COLS <= 512, "TMEM");
+  static_assert(NBUF * ACC_COLS + STAGES * SF_COLS <= 512 && TMEM_COLS <= 512, "TMEM");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -96,14 +115,19 @@ __device__ __forceinline__ void gemm_fail(volatile int* abort_flag) {
   atomicOr(&g_beam_err, DEV_ERR_TIMEOUT);
 }
 
-// F8: both operands E4M3 (K-blocks of 128 elements, kind::f8f6f4) and the
-// epilogue applies the row and weight scales; else BF16 (K-blocks of 64).
-template <int MODE, int NT, int STAGES, bool F8>
+// KIND_E4M3: both operands E4M3 (K-blocks of 128 elements, kind::f8f6f4);
+// KIND_NVFP4: both packed E2M1 (K-blocks of 256 elements) with E4M3 scales
+// per 16 elements copied from shared memory into TMEM by the MMA thread
+// (kind::mxf4nvf4 block_scale); the epilogue applies the row and weight
+// scales. KIND_BF16: K-blocks of 64.
+template <int MODE, int NT, int STAGES, int KIND>
 __global__ void __launch_bounds__(192, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                        const __grid_constant__ CUtensorMap tm_a1,
                        const __grid_constant__ CUtensorMap tm_b, const GemmArgs args) {
-  using C = GemmCfg<MODE, NT, STAGES>;
+  using C = GemmCfg<MODE, NT, STAGES, KIND>;
+  constexpr bool F8 = KIND == KIND_E4M3;
+  constexpr bool F4 = KIND == KIND_NVFP4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -158,7 +182,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
         const int4 un = gemm_unit<MODE, NT>(args, u);
         const int nb16 = (un.z + 15) >> 4;
-        const uint32_t bytes = C::A_BYTES + nb16 * 2048;
+        const uint32_t bytes = C::A_BYTES + nb16 * 2048 + C::SF_A_BYTES + C::SF_B_BYTES;
         const int arow = un.x * args.a_rows_per_expert + un.w * 128;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
@@ -168,12 +192,33 @@ __global__ void __launch_bounds__(192, 1)
           }
           uint8_t* sb = smem + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          const int kx = kb * KBlock<F8>::ELEMS;
+          // inner TMA coordinate in elements of the map: bf16 / e4m3 / bytes of e2m1 pairs
+          const int kx = kb * (F4 ? 128 : KBlock<KIND>::ELEMS);
           tma_load_2d(sb, &tm_a0, &full[stage], kx, arow, pol_w);
           if (MODE == 0) tma_load_2d(sb + C::A_TILE, &tm_a1, &full[stage], kx, arow, pol_w);
           for (int j = 0; j < nb16; ++j)
             tma_load_2d(sb + C::A_BYTES + j * 2048, &tm_b, &full[stage], kx, un.y + j * 16,
                         pol_x);
+          if (F4) {
+            // the K-block's four scale groups of the weight tile and of the
+            // 128-row token tile holding this unit's rows
+            const size_t ksteps = static_cast<size_t>(args.k_blocks) * 4;
+            const size_t a_off = ((static_cast<size_t>(arow) >> 7) * ksteps + 4 * kb) * 512;
+            const size_t b_off = (static_cast<size_t>(un.y / NT) * ksteps + 4 * kb) * 512;
+            uint8_t* sf = sb + C::A_BYTES + C::B_BYTES;
+            const uint8_t* src0 = args.a_sf0 + a_off;
+            const uint8_t* src1 = MODE == 0 ? args.a_sf1 + a_off : src0;
+            const uint8_t* srcb = args.b_sf + b_off;
+            if (((reinterpret_cast<uintptr_t>(src0) | reinterpret_cast<uintptr_t>(src1) |
+                  reinterpret_cast<uintptr_t>(srcb)) & 15) != 0) {
+              // never issue a misaligned bulk copy: flag it; the stage's wait then times out
+              atomicOr(&g_beam_err, DEV_ERR_ALIGN);
+            } else {
+              bulk_load(sf, src0, 2048, &full[stage], pol_w);
+              if (MODE == 0) bulk_load(sf + 2048, src1, 2048, &full[stage], pol_w);
+              bulk_load(sf + C::SF_A_BYTES, srcb, 2048, &full[stage], pol_x);
+            }
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -211,8 +256,10 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
-        const int n16 = (un.z + 15) & ~15;
-        const uint32_t idesc = idesc_f32acc<F8>(128, n16);
+        // N: the unit's tokens rounded up to 16 (NVFP4: to 32; the token
+        // tile's scale groups start at column 0 of the unit's TMEM slot)
+        const int n16 = F4 ? ((un.z + 31) & ~31) : ((un.z + 15) & ~15);
+        const uint32_t idesc = F4 ? idesc_nvf4(128, n16) : idesc_f32acc<F8>(128, n16);
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, tmo, abort_flag)) {
@@ -225,11 +272,32 @@ __global__ void __launch_bounds__(192, 1)
           const uint64_t da0 = sdesc_k128(sa);
           const uint64_t da1 = sdesc_k128(sa + C::A_TILE);
           const uint64_t db = sdesc_k128(sa + C::A_BYTES);
+          if (F4) {
+            // scales into this stage's TMEM columns, then the four K = 64 MMAs
+            // (tcgen05 operations of one thread execute in issue order)
+            const uint32_t slot = tmem_base + static_cast<uint32_t>(C::SF_TMEM_BASE + stage * C::SF_COLS);
+            const uint32_t sf = sa + C::A_BYTES + C::B_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-            mma_ss<F8>(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
-            if (MODE == 0) mma_ss<F8>(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+            for (int kk = 0; kk < 4; ++kk) {
+              tmem_cp_sf512(slot + 4 * kk, sdesc_sf512(sf + kk * 512));
+              if (MODE == 0) tmem_cp_sf512(slot + 16 + 4 * kk, sdesc_sf512(sf + 2048 + kk * 512));
+              tmem_cp_sf512(slot + C::SF_B_COL + 4 * kk, sdesc_sf512(sf + C::SF_A_BYTES + kk * 512));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+              const uint32_t sfb = slot + C::SF_B_COL + 4 * kk;
+              mma_nvf4_ss(d0, da0 + 2 * kk, db + 2 * kk, idesc, slot + 4 * kk, sfb, accum);
+              if (MODE == 0)
+                mma_nvf4_ss(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, slot + 16 + 4 * kk, sfb, accum);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+              mma_ss<F8>(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+              if (MODE == 0) mma_ss<F8>(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -268,8 +336,9 @@ __global__ void __launch_bounds__(192, 1)
       const int nch = (un.z + 15) >> 4;
       const int col = un.w * 128 + rloc;
       float ws0 = 1.f, ws1 = 1.f;
-      if (F8) {
-        const size_t wi = static_cast<size_t>(un.x) * args.a_rows_per_expert + col;
+      if (F8 || F4) {
+        const size_t wi = F8 ? static_cast<size_t>(un.x) * args.a_rows_per_expert + col
+                             : static_cast<size_t>(un.x);
         ws0 = args.w_scale0[wi];
         if (MODE == 0) ws1 = args.w_scale1[wi];
       }
@@ -282,7 +351,7 @@ __global__ void __launch_bounds__(192, 1)
             const int tok = c * 16 + j;
             if (tok < un.z) {
               float gj = g[j], uj = v[j];
-              if (F8) {
+              if (F8 || F4) {
                 const float sx = args.row_scale[un.y + tok];
                 gj *= ws0 * sx;
                 uj *= ws1 * sx;
@@ -299,7 +368,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
             if (tok < un.z)
-              args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = F8 ? d[j] * ws0 : d[j];
+              args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = (F8 || F4) ? d[j] * ws0 : d[j];
           }
         }
       }

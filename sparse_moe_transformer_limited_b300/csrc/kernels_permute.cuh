@@ -99,10 +99,14 @@ __device__ __forceinline__ int block_exclusive_scan256(int v, int* s_warp, int* 
 //  ties to the lower index). The GEMMs expand unit u into tile u / MT and
 //  weight row-tile u % MT, so a few hundred tiles describe all units.
 //  n_units = {tiles * MT_gu, tiles * MT_dn, tiles, 0}.
+// With pad > 1 every expert's rows start at a multiple of `pad` (its row
+// range is padded to a multiple of pad; offsets[E] is the padded total) and
+// the padding rows get row_token = -1.
 __global__ void __launch_bounds__(256) expert_scan_units_kernel(
     const int* __restrict__ blk_hist, int NB, int E, int* __restrict__ blk_off,
     int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ tiles,
-    int* __restrict__ n_units, int NT, int MT_gu, int MT_dn) {
+    int* __restrict__ n_units, int NT, int MT_gu, int MT_dn, int pad,
+    int* __restrict__ row_token) {
   __shared__ int s_cnt[256];
   __shared__ int s_off[256];
   __shared__ int s_order[256];
@@ -111,13 +115,15 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
   const int c = e < E ? hist_total(blk_hist, NB, E, e) : 0;
   s_cnt[e] = (e < E) ? c : 0;
   int total = 0;
-  const int off = block_exclusive_scan256(e < E ? c : 0, s_warp, &total);
+  const int cpad = (c + pad - 1) / pad * pad;
+  const int off = block_exclusive_scan256(e < E ? cpad : 0, s_warp, &total);
   s_off[e] = off;
   if (e < E) {
     counts[e] = c;
     offsets[e] = off;
     if (e == 0) offsets[E] = total;
     hist_offsets(blk_hist, NB, E, e, off, blk_off);
+    for (int r = off + c; r < off + cpad; ++r) row_token[r] = -1;
     int rank = 0;
     for (int j = 0; j < E; ++j) rank += (s_cnt[j] > c) || (s_cnt[j] == c && j < e);
     s_order[rank] = e;

@@ -319,6 +319,56 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va
   }
 }
 
+// ------------------------------------------------------- NVFP4 (block scaled)
+// Instruction descriptor, kind::mxf4nvf4 with block scales: A and B format
+// E2M1 = 1 in [7,10) and [10,13), scale factor type UE4M3 = 0 (bit 23), both
+// scale-factor IDs 0 ([4,6) and [29,31)), K-major, N>>3 at [17,23), M>>4 at
+// [24,29). One instruction consumes K = 64 elements (32 bytes of each row).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D (+)= A * B^T on packed E2M1 operands with one UE4M3 scale per 16
+// elements of K for each row of A and of B, read from TMEM: A's scales at
+// sfa (row m: lane m, column sfa + m/32, byte = block), B's at sfb (row n:
+// lane n % 32 of every lane quarter, column sfb + n/32). FP32 accumulation.
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Shared-memory descriptor of one 512-byte scale-factor block: 32 rows of 16
+// bytes, no swizzle (8-row core matrices 128 bytes apart). 16-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_sf512(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+// Copy one 512-byte scale-factor block into TMEM: smem row r (16 bytes) goes
+// to lane r of every lane quarter, columns taddr .. taddr+3. With the block
+// laid out as byte (r % 32) * 16 + ((r % 128) / 32) * 4 + blk for row r of a
+// 128-row tile and 16-element block blk of one K = 64 step, the four columns
+// are exactly what mma_nvf4_ss reads for A (M = 128) or for B (N <= 128).
+__device__ __forceinline__ void tmem_cp_sf512(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Non-tensor bulk copy global -> shared (16-byte aligned, size a multiple of
+// 16), completion counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Element-type dispatch for the GEMM kernels: F8 = E4M3 operands (K-blocks of
 // 128 elements), else BF16 (K-blocks of 64); both are 128-byte rows.
 template <bool F8>
@@ -341,9 +391,12 @@ __device__ __forceinline__ void mma_ss_pair(uint32_t d, uint64_t a, uint64_t b, 
   else
     mma_bf16_ss_pair(d, a, b, idesc, acc);
 }
-template <bool F8>
+// Operand element kinds of the expert GEMMs; a K-block is one 128-byte row
+// segment: 64 BF16, 128 E4M3 or 256 E2M1 elements.
+constexpr int KIND_BF16 = 0, KIND_E4M3 = 1, KIND_NVFP4 = 2;
+template <int KIND>
 struct KBlock {
-  static constexpr int ELEMS = F8 ? 128 : 64;  // elements per 128-byte K-block row
+  static constexpr int ELEMS = 64 << KIND;  // elements per 128-byte K-block row
 };
 
 }  // namespace beam

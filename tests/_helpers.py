@@ -272,3 +272,152 @@ def prenorm_ambiguous(h64, gain, eps, rel=4e-7):
     ulp = bf16_ulp(lo)
     mid = lo + np.sign(v - lo) * ulp / 2
     return (v != lo) & (np.abs(v - mid) <= rel * np.abs(v))
+
+
+# ---------------------------------------------------------------- NVFP4
+def sf_index(r, b, K, tile=128):
+    """Byte of row r, 16-element block b in the library's SF-group layout
+    (512-byte groups per row tile of `tile` rows and K = 64 step)."""
+    return ((r // tile) * (K // 64) + b // 4) * 512 + (r % 32) * 16 + ((r % tile) // 32) * 4 + b % 4
+
+
+def sf_groups_to_plain(sf, rows, K, tile=128):
+    """Block scales from the SF-group layout to a plain [rows, K/16] array;
+    `sf` starts at a tile boundary."""
+    sf = np.asarray(sf)
+    r = np.arange(rows)[:, None]
+    b = np.arange(K // 16)[None, :]
+    return sf[sf_index(r, b, K, tile)]
+
+
+def expert_getter_nvfp4(gq, uq, dq):
+    """Oracle access to NVFP4 expert weights quantised by the library:
+    per expert ((codes, plain block scales, group scale) x 3)."""
+    cache = {}
+
+    def one(q, e):
+        codes, sf, g = q
+        n, kh = codes.shape[1], codes.shape[2]
+        K = 2 * kh
+        start = e * n * K // 16
+        sfe = sf[start:start + n * K // 16].cpu().numpy()
+        return (codes[e].cpu().numpy(), sf_groups_to_plain(sfe, n, K), g[e:e + 1].cpu().numpy())
+
+    def get(e):
+        if e not in cache:
+            cache[e] = tuple(one(q, e) for q in (gq, uq, dq))
+            if len(cache) > 48:
+                cache.pop(next(iter(cache)))
+        return cache[e]
+    return get
+
+
+def check_act_codes_nvfp4(a64, gpu_codes, gpu_sf, gpu_g, rel=1e-5, row_abs=1e-5):
+    """Validate the GPU's NVFP4 quantisation of SwiGLU rows a64 [n, I] (FP64,
+    before rounding): per-row scale, block scales and codes. As for E4M3,
+    each element's GPU FP32 value lies within m = rel*|a| + row_abs*max|a_row|
+    of a64; BF16 rounding, the block and row maxima, the E4M3 block scale and
+    the E2M1 code are monotone in it, so every GPU decision must lie between
+    the decisions taken at the interval's two ends (given the GPU's own
+    scales for the later steps). Returns (codes, plain block scales, row
+    scales) validated."""
+    a64 = np.asarray(a64, dtype=np.float64)
+    n, I = a64.shape
+    m = rel * np.abs(a64) + row_abs * np.max(np.abs(a64), axis=1, keepdims=True)
+    lo_v = O.bf16_round(a64 - m).astype(np.float64)
+    hi_v = O.bf16_round(a64 + m).astype(np.float64)
+    absmin = np.where(lo_v > 0, lo_v, np.where(hi_v < 0, -hi_v, 0.0))
+    absmax = np.maximum(np.abs(lo_v), np.abs(hi_v))
+    g = np.asarray(gpu_g, dtype=np.float32)
+    f2688 = np.float32(2688.0)
+    for r in range(n):
+        lo_a, hi_a = absmin[r].max(), absmax[r].max()
+        if hi_a == 0:
+            assert g[r] == 1.0
+            continue
+        cands = _bf16_grid_between(lo_a, hi_a)
+        cands = cands[cands > 0].astype(np.float32)
+        assert ((cands / f2688).astype(np.float32) == g[r]).any(), \
+            f"row {r}: scale {g[r]} is amax/2688 for no amax in [{lo_a}, {hi_a}]"
+    six_g = (np.float32(6.0) * g).astype(np.float32)[:, None]
+    bmin = absmin.reshape(n, I // 16, 16).max(axis=2)
+    bmax = absmax.reshape(n, I // 16, 16).max(axis=2)
+    s_lo = O.e4m3_round((bmin.astype(np.float32) / six_g).astype(np.float32))
+    s_hi = O.e4m3_round((bmax.astype(np.float32) / six_g).astype(np.float32))
+    sbv = O.e4m3_decode(np.asarray(gpu_sf))
+    ok_s = (sbv >= s_lo) & (sbv <= s_hi)
+    assert ok_s.all(), f"{(~ok_s).sum()} block scales outside the oracle's interval"
+    denom = (sbv.astype(np.float32) * g[:, None]).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(sbv > 0, np.float32(1.0) / np.where(sbv > 0, denom, np.float32(1.0)),
+                       np.float32(0.0)).astype(np.float32)
+    inv_e = np.repeat(inv, 16, axis=1)
+    c_lo = O.e2m1_round((lo_v.astype(np.float32) * inv_e).astype(np.float32))
+    c_hi = O.e2m1_round((hi_v.astype(np.float32) * inv_e).astype(np.float32))
+    gv = O.e2m1_decode(O.unpack_e2m1(np.asarray(gpu_codes)))
+    ok = (gv >= c_lo) & (gv <= c_hi)
+    if not ok.all():
+        r, j = map(int, np.argwhere(~ok)[0])
+        raise AssertionError(f"{(~ok).sum()} act codes outside the oracle's interval; first at "
+                             f"row {r} col {j}: a64={a64[r, j]!r} code value {gv[r, j]} not in "
+                             f"[{c_lo[r, j]}, {c_hi[r, j]}]")
+    return np.asarray(gpu_codes), np.asarray(gpu_sf), g
+
+
+def nvfp4_pad(T, top_k, E):
+    """Token-tile padding of the NVFP4 expert-ordered layout (32 rows on the
+    decode tiles, 128 when there are many tokens per expert)."""
+    return 32 if T * top_k <= 24 * E else 128
+
+
+def oracle_outputs_nvfp4_checked(x64, gpu_idx, weight_of, get_expert_q, act_rows, E, pad,
+                                 tokens=None):
+    """Oracle NVFP4 combine for `tokens`, with each pair row's SwiGLU
+    quantisation validated (check_act_codes_nvfp4). Rows are in the
+    library's padded expert order: expert e's rows start at the sum of the
+    earlier experts' counts each rounded up to `pad`, in pair order.
+    act_rows(rows) -> (codes [n, I/2], plain block scales [n, I/16],
+    row scales [n])."""
+    gpu_idx = np.asarray(gpu_idx)
+    T, K = gpu_idx.shape
+    perm = O.permutation(gpu_idx, E)
+    counts = perm["counts"]
+    padded = (counts + pad - 1) // pad * pad
+    poff = np.concatenate([[0], np.cumsum(padded)])
+    row_of_pair = np.empty(T * K, dtype=np.int64)
+    for e in np.nonzero(counts)[0]:
+        pr = perm["row_pair"][perm["offsets"][e]:perm["offsets"][e + 1]]
+        row_of_pair[pr] = poff[e] + np.arange(len(pr))
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    pos = {int(t): i for i, t in enumerate(toks)}
+    pairs = (toks[:, None] * K + np.arange(K)[None, :]).ravel()
+    experts = gpu_idx.ravel()[pairs]
+    out = np.zeros((len(toks), x64.shape[1]))
+    for e in np.unique(experts):
+        pe = pairs[experts == e]
+        rows, tk = row_of_pair[pe], pe // K
+        gq, uq, dq = get_expert_q(int(e))
+        a64 = O.swiglu_act_nvfp4(x64[tk], gq, uq)
+        codes_g, sf_g, g_g = act_rows(rows)
+        codes, sf, g = check_act_codes_nvfp4(a64, codes_g, sf_g, g_g)
+        H = dq[0].shape[0]
+        y = O.dequantize_nvfp4(codes, sf, g, 1) @ O.dequantize_nvfp4(*dq, H).T
+        for i, t in enumerate(tk):
+            out[pos[int(t)]] += weight_of(int(t), int(e)) * y[i]
+    return out
+
+
+def act_rows_reader_nvfp4(ws, lay, I, tile):
+    """act_rows callable for oracle_outputs_nvfp4_checked: the GPU's NVFP4
+    SwiGLU codes, block scales (token tiles of `tile` rows) and row scales
+    from the workspace."""
+    def read(rows):
+        rows = np.asarray(rows, dtype=np.int64)
+        tiles = int(rows.max()) // tile + 1
+        sf_all = ws[lay["act_sf"]:lay["act_sf"] + tiles * (I // 64) * 512].cpu().numpy()
+        g_all = ws[lay["act_scale"]:lay["act_scale"] + tiles * tile * 4].view(torch.float32).cpu().numpy()
+        codes = np.stack([ws[lay["act_q"] + r * (I // 2):lay["act_q"] + (r + 1) * (I // 2)].cpu().numpy()
+                          for r in rows])
+        idx = sf_index(rows[:, None], np.arange(I // 16)[None, :], I, tile)
+        return codes, sf_all[idx], g_all[rows]
+    return read

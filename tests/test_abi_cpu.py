@@ -134,3 +134,28 @@ def test_fp8_entry_points_reject_bad_args():
     assert lib.beam_quantize_e4m3_rows(None, -1, 16, None, None, None) == 1
     assert lib.beam_quantize_e4m3_rows(None, 0, 16, None, None, None) == 0
     assert lib.beam_quantize_e4m3_rows(None, 4, 16, None, None, None) == 1
+
+
+def test_nvfp4_entry_points_reject_bad_args():
+    lib = B.lib()
+    p = _p()                                   # FLAG_NVFP4_EXPERTS missing
+    assert lib.beam_moe_forward_nvfp4(ctypes.byref(p), *([None] * 18), 0, None) == 1
+    p = _p(flags=B.FLAG_NVFP4_EXPERTS | B.FLAG_FP8_EXPERTS)
+    assert B.lib().beam_moe_workspace_size(ctypes.byref(p)) == 0
+    p = _p(I=2560 + 128, flags=B.FLAG_NVFP4_EXPERTS)   # I % 256 != 0
+    assert lib.beam_moe_forward_nvfp4(ctypes.byref(p), *([None] * 18), 0, None) == 2
+    p = _p(T=0, flags=B.FLAG_NVFP4_EXPERTS)
+    assert lib.beam_moe_forward_nvfp4(ctypes.byref(p), *([None] * 18), 0, None) == 0
+    # the quantiser wants rows a multiple of 128 and of rows_per_group, K of 64
+    assert lib.beam_quantize_nvfp4(None, 100, 64, 1, None, None, None, None) == 1
+    assert lib.beam_quantize_nvfp4(None, 128, 48, 1, None, None, None, None) == 1
+    assert lib.beam_quantize_nvfp4(None, 256, 64, 100, None, None, None, None) == 1
+    assert lib.beam_quantize_nvfp4(None, 0, 64, 1, None, None, None, None) == 0
+
+
+def test_nvfp4_workspace_pads_expert_rows():
+    f4 = B.workspace_layout(_p(flags=B.FLAG_NVFP4_EXPERTS))
+    plain = B.workspace_layout(_p())
+    # T=64, top-8: up to 256 experts each padded to 32 rows -> far more rows
+    assert f4["act"] - f4["xperm"] > plain["act"] - plain["xperm"]
+    assert f4["act_sf"] > f4["x_sf"] > f4["act_scale"]

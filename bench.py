@@ -139,20 +139,27 @@ def _describe(wl):
             f"combine -> post-RMSNorm -> residual k={RESIDUAL_K}")
 
 
-def _algorithmic(wl, counts, fp8=False):
+# bytes per weight element and per weight row, by expert weight type:
+# BF16; E4M3 codes + one FP32 scale per row; NVFP4 packed codes + one E4M3
+# block scale per 16 elements (the per-matrix FP32 scale is negligible)
+WEIGHT_BYTES = {"bf16": (2.0, 0), "fp8": (1.0, 4), "nvfp4": (0.5 + 1.0 / 16, 0)}
+# nominal dense tensor rate relative to BF16 (2.25 / 4.5 / 13.5 PFLOP/s)
+TENSOR_RATIO = {"bf16": 1, "fp8": 2, "nvfp4": 6}
+
+
+def _algorithmic(wl, counts, kind="bf16"):
     """Algorithmic bytes / FLOPs (what the method must move and compute): each
-    touched expert's weights once (BF16, or E4M3 codes plus one FP32 scale per
-    row) plus the layer's BF16 input or output; the intermediates (permuted
-    x, SwiGLU activations, per-pair outputs) are not counted."""
+    touched expert's weights once (WEIGHT_BYTES) plus the layer's BF16 input
+    or output; the intermediates (permuted x, SwiGLU activations, per-pair
+    outputs) are not counted."""
     touched = int((counts > 0).sum())
     R = wl.T * wl.top_k
-    eb = 1 if fp8 else 2
-    sc = 4 if fp8 else 0
-    gu_bytes = touched * 2 * wl.I * (wl.H * eb + sc) + wl.T * wl.H * 2
-    dn_bytes = touched * wl.H * (wl.I * eb + sc) + wl.T * wl.H * 2
+    eb, sc = WEIGHT_BYTES[kind]
+    gu_bytes = int(touched * 2 * wl.I * (wl.H * eb + sc)) + wl.T * wl.H * 2
+    dn_bytes = int(touched * wl.H * (wl.I * eb + sc)) + wl.T * wl.H * 2
     gu_flops = 2.0 * R * 2 * wl.I * wl.H
     dn_flops = 2.0 * R * wl.I * wl.H
-    layer_bytes = (touched * (3 * wl.I * wl.H * eb + (2 * wl.I + wl.H) * sc)
+    layer_bytes = (int(touched * (3 * wl.I * wl.H * eb + (2 * wl.I + wl.H) * sc))
                    + 2 * wl.T * wl.H * 2 + wl.E * wl.H * 4)
     return dict(touched=touched, gu_bytes=gu_bytes, dn_bytes=dn_bytes, gu_flops=gu_flops,
                 dn_flops=dn_flops, layer_bytes=layer_bytes,
@@ -182,9 +189,10 @@ def _traffic_for(kernel, workload):
 
 
 # ------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank, fp8=False):
-    """The sublayer with BF16 expert weights, or (fp8) E4M3 expert weights
+def run_ours(args, rank, world, local_rank, kind="bf16"):
+    """The sublayer with BF16 expert weights, or E4M3 / NVFP4 expert weights
     quantised once on the device before any timing."""
+    fp8, f4 = kind == "fp8", kind == "nvfp4"
     import sparse_moe_transformer_limited_b300 as B
     B.lib()
     dev = torch.device("cuda", local_rank)
@@ -192,14 +200,16 @@ def run_ours(args, rank, world, local_rank, fp8=False):
     wl = _workload(args.config)
     wl_rank = wl.replace(seed=wl.seed + 1000 * rank) if rank else wl
     d = S.make_inputs(wl_rank, dev)
-    flags = B.FLAG_PRE_NORM | (B.FLAG_FP8_EXPERTS if fp8 else 0)
+    flags = (B.FLAG_PRE_NORM | (B.FLAG_FP8_EXPERTS if fp8 else 0)
+             | (B.FLAG_NVFP4_EXPERTS if f4 else 0))
     p = B.make_params(wl.T, wl.H, wl.E, wl.I, wl.n_group, wl.topk_group, wl.top_k,
                       wl.routed_scale, wl.rms_eps, RESIDUAL_K, flags)
     ws = B.alloc_workspace(p, dev)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-    if fp8:
-        q = tuple(B.quantize_e4m3_rows(d[k]) for k in ("w_gate", "w_up", "w_down"))
+    if fp8 or f4:
+        quant = B.quantize_e4m3_rows if fp8 else B.quantize_nvfp4
+        q = tuple(quant(d[k]) for k in ("w_gate", "w_up", "w_down"))
         for k in ("w_gate", "w_up", "w_down"):
             d[k] = None
         torch.cuda.synchronize(dev)
@@ -208,6 +218,8 @@ def run_ours(args, rank, world, local_rank, fp8=False):
     def fwd(x_in):
         if fp8:
             B.forward_fp8(p, x_in, d["w_router"], *q, bias=d["bias"], out=out, workspace=ws)
+        elif f4:
+            B.forward_nvfp4(p, x_in, d["w_router"], *q, bias=d["bias"], out=out, workspace=ws)
         else:
             B.forward(p, x_in, d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
                       bias=d["bias"], out=out, workspace=ws)
@@ -273,13 +285,14 @@ def run_ours(args, rank, world, local_rank, fp8=False):
     value = weak_scaling_value(world, wl.T, args.steps, ms_total / 1e3)
     e2e_value = weak_scaling_value(world, wl.T, args.steps, e2e_s)
 
-    alg = _algorithmic(wl, counts, fp8)
+    alg = _algorithmic(wl, counts, kind)
     peaks = _peaks()
-    if fp8:
-        # E4M3 contraction: the measured BF16 peaks times the nominal
-        # FP8 / BF16 dense ratio (4.5 / 2.25 PFLOP/s)
-        peaks = dict(peaks, bf16=2 * peaks["bf16"], bf16_sustained=2 * peaks["bf16_sustained"],
-                     tensor_note=" x 2 (nominal FP8/BF16 dense ratio)")
+    if kind != "bf16":
+        # E4M3 / NVFP4 contraction: the measured BF16 peaks times the nominal
+        # dense ratio to BF16 (4.5 / 2.25 and 13.5 / 2.25 PFLOP/s)
+        rt = TENSOR_RATIO[kind]
+        peaks = dict(peaks, bf16=rt * peaks["bf16"], bf16_sustained=rt * peaks["bf16_sustained"],
+                     tensor_note=f" x {rt} (nominal {kind}/BF16 dense ratio)")
     gu_ms = prof["expert_gemm_gateup_swiglu"][0] / prof["expert_gemm_gateup_swiglu"][1]
     dn_ms = prof["expert_gemm_down"][0] / prof["expert_gemm_down"][1]
     decode_like = wl.T * wl.top_k <= 24 * wl.E
@@ -296,7 +309,7 @@ def run_ours(args, rank, world, local_rank, fp8=False):
         roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
                 "peak_source": peaks["source"] + " bf16_tflops (burst)" + peaks.get("tensor_note", ""),
-                "dtype": "e4m3" if fp8 else "bf16",
+                "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[kind],
                 "frac_of_sustained": round(achieved / peaks["bf16_sustained"], 4),
                 "traffic": _traffic_for(kname, wl.name),
                 "algorithmic_flops_per_launch": alg["gu_flops"], "launch_ms": round(gu_ms, 4)}
@@ -436,27 +449,32 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------ ncu cases
-def run_ncu_case(kind, fp8=False):
+def run_ncu_case(kind, experts="bf16"):
     """A small case for profiler captures: the full layer path with the real
     H=5120 / I=2560 shapes but 32 experts (one group, plain top-8), so the
     expert weights take 2.5 GB -- more than the L2, little device memory.
     kind 'decode': T=64 (16 tokens/expert, token tile 32);
     kind 'prefill': T=2048 (512 tokens/expert, token tile 128).
-    Runs four forward calls (pre-norm + residual k=50) and exits; fp8: with
-    E4M3 expert weights (quantised first)."""
+    Runs four forward calls (pre-norm + residual k=50) and exits; with
+    experts fp8 / nvfp4 the expert weights are quantised first."""
     import sparse_moe_transformer_limited_b300 as B
     T = 64 if kind == "decode" else 2048
     wl = S.Workload("ncu_" + kind, T=T, E=32, n_group=1, topk_group=1, seed=7)
     d = S.make_inputs(wl, "cuda")
-    flags = B.FLAG_PRE_NORM | (B.FLAG_FP8_EXPERTS if fp8 else 0)
+    fp8, f4 = experts == "fp8", experts == "nvfp4"
+    flags = (B.FLAG_PRE_NORM | (B.FLAG_FP8_EXPERTS if fp8 else 0)
+             | (B.FLAG_NVFP4_EXPERTS if f4 else 0))
     p = B.make_params(wl.T, wl.H, wl.E, wl.I, wl.n_group, wl.topk_group, wl.top_k,
                       wl.routed_scale, wl.rms_eps, RESIDUAL_K, flags)
     ws = B.alloc_workspace(p)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
-    q = tuple(B.quantize_e4m3_rows(d[k]) for k in ("w_gate", "w_up", "w_down")) if fp8 else None
+    quant = B.quantize_e4m3_rows if fp8 else B.quantize_nvfp4
+    q = tuple(quant(d[k]) for k in ("w_gate", "w_up", "w_down")) if (fp8 or f4) else None
     for _ in range(4):
         if fp8:
             B.forward_fp8(p, d["x"], d["w_router"], *q, out=out, workspace=ws)
+        elif f4:
+            B.forward_nvfp4(p, d["x"], d["w_router"], *q, out=out, workspace=ws)
         else:
             B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], out=out,
                       workspace=ws)
@@ -473,8 +491,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="decode", choices=sorted(S.WORKLOADS) + sorted(DENSE))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--experts", default="bf16", choices=["bf16", "fp8"],
-                    help="expert weight type of the timed sublayer (fp8: E4M3 + row scales)")
+    ap.add_argument("--experts", default="bf16", choices=["bf16", "fp8", "nvfp4"],
+                    help="expert weight type of the timed sublayer (fp8: E4M3 + row scales; "
+                         "nvfp4: E2M1 + E4M3 block scales + FP32 matrix scales)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the secondary T=8192 measurement")
@@ -482,7 +501,7 @@ def main():
                     help="run the small profiler case and exit")
     args = ap.parse_args()
     if args.ncu_case:
-        run_ncu_case(args.ncu_case, args.experts == "fp8")
+        run_ncu_case(args.ncu_case, args.experts)
         return
 
     rank = int(os.environ.get("RANK", 0))
@@ -515,8 +534,8 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
-    fp8 = args.experts == "fp8"
-    r = run_ours(args, rank, world, local_rank, fp8)
+    kind = args.experts
+    r = run_ours(args, rank, world, local_rank, kind)
     extra = {}
     if rank == 0 and world == 1 and args.config == "decode" and not args.no_prefill:
         a2 = argparse.Namespace(**vars(args))
@@ -531,13 +550,14 @@ def main():
                     "roofline": rr["roofline"], "layer": rr["layer"],
                     "kernels_ms": rr["kernels_ms"], "clocks": rr["clocks"]}
         extra = {"dense_mlp_T8192": extra_dense, "prefill_T8192": summary(r2)}
-        if not fp8:
-            # the same sublayers with E4M3 expert weights (secondary lines)
-            torch.cuda.empty_cache()
+        if kind == "bf16":
+            # the same sublayers with E4M3 and NVFP4 expert weights (secondary lines)
             a3 = argparse.Namespace(**vars(args))
-            extra["fp8_experts_T64"] = summary(run_ours(a3, rank, world, local_rank, True))
-            torch.cuda.empty_cache()
-            extra["fp8_experts_T8192"] = summary(run_ours(a2, rank, world, local_rank, True))
+            for k2 in ("fp8", "nvfp4"):
+                torch.cuda.empty_cache()
+                extra[f"{k2}_experts_T64"] = summary(run_ours(a3, rank, world, local_rank, k2))
+                torch.cuda.empty_cache()
+                extra[f"{k2}_experts_T8192"] = summary(run_ours(a2, rank, world, local_rank, k2))
             torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -557,7 +577,8 @@ def main():
     line = {"metric": METRIC, "value": round(r["value"], 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": round(r["ms_step"], 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[kind],
             "data": "synthetic",
             "config": {"workload": _describe(wl), "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I,
                        "top_k": wl.top_k, "seed": wl.seed,

@@ -9,9 +9,10 @@ import torch
 
 import beam_synth as S
 import oracle as O
-from _helpers import (OUT_REL_TOL, act_rows_reader, compare_routing, expert_getter,
-                      expert_getter_fp8, host, oracle_outputs, oracle_outputs_fp8_checked,
-                      prenorm_ambiguous, rel_err, weights_from_chosen)
+from _helpers import (OUT_REL_TOL, act_rows_reader, act_rows_reader_nvfp4, compare_routing,
+                      expert_getter, expert_getter_fp8, expert_getter_nvfp4, host, nvfp4_pad,
+                      oracle_outputs, oracle_outputs_fp8_checked, oracle_outputs_nvfp4_checked,
+                      prenorm_ambiguous, rel_err, sf_groups_to_plain, weights_from_chosen)
 
 pytestmark = pytest.mark.gpu
 
@@ -187,3 +188,50 @@ def test_bench_configuration_fp8(B, name):
     err = rel_err(host(hk)[sample], want)
     assert err <= OUT_REL_TOL, f"rel err {err}"
     print(f"{name} fp8: clean {len(clean)}/{wl.T}, near ties {int(ties.sum())}, rel err {err:.2e}")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_bench_configuration_nvfp4(B, name):
+    """The NVFP4 expert path as the benchmark times it: one expert matrix's
+    quantisation exact against the oracle, routing of every clean token,
+    sampled tokens' outputs with each SwiGLU row's quantisation validated."""
+    wl = S.WORKLOADS[name]
+    d = S.make_inputs(wl, "cuda")
+    q = tuple(B.quantize_nvfp4(d[k]) for k in ("w_gate", "w_up", "w_down"))
+    assert B.status() == 0, B.last_error()
+    w0 = d["w_gate"][3].float().cpu().numpy()
+    pk, sb, g = O.quantize_nvfp4(w0, wl.I)
+    got = q[0][0][3].cpu().numpy()
+    assert np.array_equal(O.e2m1_decode(O.unpack_e2m1(got)), O.e2m1_decode(O.unpack_e2m1(pk)))
+    n = wl.I * wl.H // 16
+    assert np.array_equal(sf_groups_to_plain(q[0][1][3 * n:4 * n].cpu().numpy(), wl.I, wl.H), sb)
+    assert q[0][2][3].item() == g[0]
+    for k in ("w_gate", "w_up", "w_down"):
+        d[k] = None
+    torch.cuda.empty_cache()
+    p = _params(B, wl, B.FLAG_PRE_NORM | B.FLAG_NVFP4_EXPERTS, 50)
+    ws = B.alloc_workspace(p)
+    idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device="cuda")
+    hk = B.forward_nvfp4(p, d["x"], d["w_router"], *q, bias=d["bias"], topk_idx=idx, topk_w=w,
+                         workspace=ws)
+    assert B.status() == 0, B.last_error()
+    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+    h64 = host(d["x"]).astype(np.float64)
+    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
+    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
+    clean = np.nonzero(~amb.any(axis=1))[0]
+    assert len(clean) >= 0.8 * wl.T
+    sel = O.route(x64[clean], host(d["w_router"]), None, wl.n_group, wl.topk_group, wl.top_k,
+                  wl.routed_scale)
+    ties, chosen = compare_routing(sel, gi[clean], gw[clean], wl)
+    sample = np.intersect1d(_sample(wl.T, 12, 6), clean)
+    pad = nvfp4_pad(wl.T, wl.top_k, wl.E)
+    o = oracle_outputs_nvfp4_checked(x64, gi, weights_from_chosen(chosen, clean),
+                                     expert_getter_nvfp4(*q),
+                                     act_rows_reader_nvfp4(ws, B.workspace_layout(p), wl.I, pad),
+                                     wl.E, pad, tokens=sample)
+    want = O.residual_step(h64[sample], o, 50, None, wl.rms_eps, True)
+    err = rel_err(host(hk)[sample], want)
+    assert err <= OUT_REL_TOL, f"rel err {err}"
+    print(f"{name} nvfp4: clean {len(clean)}/{wl.T}, near ties {int(ties.sum())}, rel err {err:.2e}")

@@ -302,7 +302,7 @@ def run_ours(args, rank, world, local_rank, kind="bf16"):
         roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                 "peak_source": peaks["source"] + " hbm_gbs",
-                "traffic": _traffic_for(kname, wl.name),
+                "traffic": _traffic_for(kname, wl.name if kind == "bf16" else f"{wl.name}_{kind}"),
                 "algorithmic_bytes_per_launch": alg["gu_bytes"], "launch_ms": round(gu_ms, 4)}
     else:
         achieved = alg["gu_flops"] / (gu_ms / 1e3) / 1e12
@@ -311,7 +311,7 @@ def run_ours(args, rank, world, local_rank, kind="bf16"):
                 "peak_source": peaks["source"] + " bf16_tflops (burst)" + peaks.get("tensor_note", ""),
                 "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[kind],
                 "frac_of_sustained": round(achieved / peaks["bf16_sustained"], 4),
-                "traffic": _traffic_for(kname, wl.name),
+                "traffic": _traffic_for(kname, wl.name if kind == "bf16" else f"{wl.name}_{kind}"),
                 "algorithmic_flops_per_launch": alg["gu_flops"], "launch_ms": round(gu_ms, 4)}
     layer = {"hbm_frac": round(alg["layer_bytes"] / (ms_step / 1e3) / 1e9 / peaks["hbm"], 4),
              "tensor_frac": round(alg["layer_flops"] / (ms_step / 1e3) / 1e12 / peaks["bf16"], 4),

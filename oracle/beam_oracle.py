@@ -602,3 +602,108 @@ def moe_combine_nvfp4(x, idx, weights, get_expert_q) -> np.ndarray:
         tok, slot = np.nonzero(idx == e)
         out[tok] += weights[tok, slot][:, None] * swiglu_expert_nvfp4(x[tok], *get_expert_q(int(e)))
     return out
+
+
+# ----------------------------------------------------------------------------
+# attention sublayer ([P1] section 注意力: 52 decoder layers, hidden 5120;
+# sliding-window attention over the last 512 tokens, every sixth layer and
+# the last attend to the full context; sliding layers use RoPE, global
+# layers none but multiply each query by (1 + (pos + 1) / 2048) ** 0.1;
+# grouped-query attention with 48 query heads and 8 key/value heads, RMSNorm
+# on queries and keys; a learned sigmoid gate computed from the layer input
+# scales every channel of every head before the output projection.
+# [P1] 残差流: normalised before and after, the scaled residual step; RoPE and
+# the query scaling run in FP32. [P5] config.json: head_dim 128,
+# sliding_window 512, rope_theta 10000 on the sliding layers.)
+#
+# Readings where the pages leave a step open:
+#   * the window holds the current token and the 511 before it (key j is seen
+#     by query i when 0 <= i - j < 512); attention is causal;
+#   * softmax scale 1/sqrt(head_dim);
+#   * q_norm / k_norm: RMSNorm over the 128 channels of each head with a
+#     128-wide gain shared by the heads (eps 1e-6), applied before RoPE;
+#   * RoPE: rotate-half form over all 128 channels, frequency
+#     theta^(-2i/128) for channel pairs (i, i + 64), position = token index;
+#   * the global query scale multiplies the normalised query (pos = token
+#     index, 0-based);
+#   * query head h uses key/value head h // 6;
+#   * the gate is sigmoid(x W_g^T), x the pre-normed layer input, one value
+#     per (head, channel);
+#   * projections have no bias; Q, K, V and the gate come from one fused
+#     weight [W_q; W_k; W_v; W_g] of (48 + 8 + 8 + 48) * 128 rows;
+#   * Q, K, V enter the attention rounded to BF16 (the activation dtype) and
+#     the gated attention output is rounded to BF16 before the output
+#     projection.
+# ----------------------------------------------------------------------------
+def rope_rotate(v, pos, theta: float = 10000.0) -> np.ndarray:
+    """RoPE, rotate-half form, on the last dimension (size d) of v [..., T, d]
+    for positions pos [T] (FP64)."""
+    v = np.asarray(v, dtype=F64)
+    d = v.shape[-1]
+    half = d // 2
+    inv_freq = theta ** (-np.arange(half, dtype=F64) * 2.0 / d)
+    ang = np.asarray(pos, dtype=F64)[:, None] * inv_freq[None, :]
+    cos, sin = np.cos(ang), np.sin(ang)
+    x1, x2 = v[..., :half], v[..., half:]
+    return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
+
+
+def global_query_scale(pos) -> np.ndarray:
+    """(1 + (pos + 1) / 2048) ** 0.1 per position (FP64)."""
+    return (1.0 + (np.asarray(pos, dtype=F64) + 1.0) / 2048.0) ** 0.1
+
+
+def attention_core(q, k, v, window: int) -> np.ndarray:
+    """softmax(q k^T / sqrt(d) + mask) v per head with the causal (and, when
+    window > 0, sliding-window) mask; q [nq, T, d], k and v [nkv, T, d],
+    query head h reads key/value head h // (nq // nkv). FP64."""
+    q, k, v = (np.asarray(a, dtype=F64) for a in (q, k, v))
+    nq, T, d = q.shape
+    group = nq // k.shape[0]
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    allowed = j <= i
+    if window > 0:
+        allowed &= (i - j) < window
+    out = np.empty_like(q)
+    for h in range(nq):
+        s = q[h] @ k[h // group].T / math.sqrt(d)
+        s = np.where(allowed, s, -np.inf)
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        out[h] = (p / p.sum(axis=1, keepdims=True)) @ v[h // group]
+    return out
+
+
+def attention_forward(h_in, w_qkvg, w_o, q_gain, k_gain, *, n_q=48, n_kv=8, head_dim=128,
+                      window=512, rope_theta=10000.0, eps=1e-6, pre_gain=None,
+                      residual_k=0, post_gain=None) -> dict:
+    """The attention sublayer for one sequence of T tokens at positions 0..T-1.
+
+    h_in [T, H] (h_{k-1}); w_qkvg [(n_q + 2 n_kv + n_q) * head_dim, H];
+    w_o [H, n_q * head_dim]; q_gain, k_gain [head_dim]. window > 0: sliding
+    layer with RoPE; window == 0: global layer with the query scale.
+    Returns dict(x, q, k, v, gate, attn (gated, BF16-rounded), out, h)."""
+    h_in = np.asarray(h_in, dtype=F64)
+    T, H = h_in.shape
+    x = bf16_round(rms_norm(h_in, pre_gain, eps)).astype(F64)
+    proj = x @ np.asarray(w_qkvg, dtype=F64).T
+    dq, dkv = n_q * head_dim, n_kv * head_dim
+    q = proj[:, :dq].reshape(T, n_q, head_dim).transpose(1, 0, 2)
+    k = proj[:, dq:dq + dkv].reshape(T, n_kv, head_dim).transpose(1, 0, 2)
+    v = proj[:, dq + dkv:dq + 2 * dkv].reshape(T, n_kv, head_dim).transpose(1, 0, 2)
+    gate = sigmoid(proj[:, dq + 2 * dkv:])                      # [T, n_q * head_dim]
+    q = rms_norm(q, q_gain, eps)
+    k = rms_norm(k, k_gain, eps)
+    pos = np.arange(T)
+    if window > 0:
+        q = rope_rotate(q, pos, rope_theta)
+        k = rope_rotate(k, pos, rope_theta)
+    else:
+        q = q * global_query_scale(pos)[None, :, None]
+    q, k, v = (bf16_round(a).astype(F64) for a in (q, k, v))
+    o = attention_core(q, k, v, window)                          # [n_q, T, d]
+    attn = bf16_round(o.transpose(1, 0, 2).reshape(T, dq) * gate).astype(F64)
+    out = attn @ np.asarray(w_o, dtype=F64).T
+    hk = residual_step(h_in, out, residual_k, post_gain, eps, True) if residual_k else None
+    return dict(x=x, q=q, k=k, v=v, gate=gate, attn=attn, out=out, h=hk)

@@ -1,0 +1,119 @@
+"""Pins for the oracle's attention sublayer, each against something other
+than the oracle: closed forms of RoPE and the global query scale, a
+brute-force per-query loop, special cases (window 1, equal scores), a
+one-hot check of the query-to-key/value head mapping, and torch's
+scaled_dot_product_attention. No GPU needed."""
+import math
+
+import numpy as np
+import torch
+
+import oracle as O
+
+
+def test_rope_closed_forms():
+    # d = 2: the pair (x, y) turns by pos * theta^0 = pos radians
+    v = np.array([[[1.0, 0.0]]] * 3).reshape(1, 3, 2)
+    out = O.rope_rotate(v, np.array([0, 1, 2]))
+    assert np.allclose(out[0], [[1, 0], [math.cos(1), math.sin(1)], [math.cos(2), math.sin(2)]])
+    rng = np.random.default_rng(0)
+    q, k = rng.standard_normal((2, 1, 5, 128))
+    # norms of the (i, i + 64) pairs are kept
+    rq = O.rope_rotate(q, np.arange(5))
+    assert np.allclose(q[..., :64] ** 2 + q[..., 64:] ** 2, rq[..., :64] ** 2 + rq[..., 64:] ** 2)
+    # position 0 is the identity; dot products depend only on the position difference
+    assert np.allclose(rq[0, 0], q[0, 0])
+    a = (O.rope_rotate(q, np.array([3, 3, 3, 3, 3]))[0, 0] @ O.rope_rotate(k, np.array([1] * 5))[0, 0])
+    b = (O.rope_rotate(q, np.array([10] * 5))[0, 0] @ O.rope_rotate(k, np.array([8] * 5))[0, 0])
+    assert np.isclose(a, b)
+    # channel pair i turns with frequency 10000^(-2i/128): pair 32 at position 1
+    e = np.zeros((1, 1, 128)); e[0, 0, 32] = 1.0
+    r = O.rope_rotate(e, np.array([1]))[0, 0]
+    ang = 10000.0 ** (-64 / 128)
+    assert np.isclose(r[32], math.cos(ang)) and np.isclose(r[96], math.sin(ang))
+
+
+def test_global_query_scale_closed_form():
+    assert O.global_query_scale(np.array([-1.0]))[0] == 1.0
+    assert np.isclose(O.global_query_scale(np.array([2047.0]))[0], 2.0 ** 0.1)
+    assert np.isclose(O.global_query_scale(np.array([6143.0]))[0], 4.0 ** 0.1)
+
+
+def _brute(q, k, v, window):
+    nq, T, d = q.shape
+    g = nq // k.shape[0]
+    out = np.zeros_like(q)
+    for h in range(nq):
+        for i in range(T):
+            keys = [j for j in range(T) if j <= i and (window == 0 or i - j < window)]
+            s = np.array([q[h, i] @ k[h // g, j] / math.sqrt(d) for j in keys])
+            w = np.exp(s - s.max())
+            w /= w.sum()
+            out[h, i] = sum(wj * v[h // g, j] for wj, j in zip(w, keys))
+    return out
+
+
+def test_core_brute_force_and_special_cases():
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((4, 9, 8))
+    k = rng.standard_normal((2, 9, 8))
+    v = rng.standard_normal((2, 9, 8))
+    for window in (0, 1, 3, 100):
+        assert np.allclose(O.attention_core(q, k, v, window), _brute(q, k, v, window))
+    # window 1: every query sees only itself
+    o = O.attention_core(q, k, v, 1)
+    assert np.allclose(o[0], v[0]) and np.allclose(o[3], v[1])
+    # equal scores: the mean of the visible values (causal prefix / last w)
+    z = np.zeros_like(q)
+    o = O.attention_core(z, k, v, 0)
+    assert np.allclose(o[0, 4], v[0, :5].mean(axis=0))
+    o = O.attention_core(z, k, v, 3)
+    assert np.allclose(o[2, 6], v[1, 4:7].mean(axis=0))
+
+
+def test_query_head_to_kv_head_mapping():
+    T, d = 5, 4
+    q = np.random.default_rng(2).standard_normal((48, T, d))
+    k = np.zeros((8, T, d))
+    v = np.zeros((8, T, d))
+    v[3] = 1.0                                   # only key/value head 3 carries ones
+    o = O.attention_core(q, k, v, 0)
+    ones = np.array([np.allclose(o[h], 1.0) for h in range(48)])
+    assert ones.sum() == 6 and np.all(ones[18:24])   # query heads 18..23 = 3 * 6 .. 3 * 6 + 5
+
+
+def test_core_matches_torch_sdpa():
+    g = torch.Generator().manual_seed(3)
+    q = torch.randn(1, 12, 40, 32, generator=g, dtype=torch.float64)
+    k = torch.randn(1, 2, 40, 32, generator=g, dtype=torch.float64)
+    v = torch.randn(1, 2, 40, 32, generator=g, dtype=torch.float64)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, enable_gqa=True)
+    got = O.attention_core(q[0].numpy(), k[0].numpy(), v[0].numpy(), 0)
+    assert np.allclose(got, ref[0].numpy(), atol=1e-12)
+    i = torch.arange(40)[:, None]
+    j = torch.arange(40)[None, :]
+    mask = (j <= i) & (i - j < 7)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, enable_gqa=True)
+    assert np.allclose(O.attention_core(q[0].numpy(), k[0].numpy(), v[0].numpy(), 7), ref[0].numpy(),
+                       atol=1e-12)
+
+
+def test_forward_gate_and_layout():
+    """Zero gate weights give a gate of 1/2 everywhere; the fused weight's
+    row blocks are read as [W_q; W_k; W_v; W_g]."""
+    rng = np.random.default_rng(4)
+    T, H, nq, nkv, d = 12, 64, 6, 2, 16
+    w = rng.standard_normal(((nq + 2 * nkv + nq) * d, H)) * 0.1
+    w[(nq + 2 * nkv) * d:] = 0.0
+    wo = np.eye(H, nq * d)
+    r = O.attention_forward(rng.standard_normal((T, H)), w, wo, np.ones(d), np.ones(d), n_q=nq,
+                            n_kv=nkv, head_dim=d, window=4)
+    assert np.allclose(r["gate"], 0.5)
+    o = O.attention_core(r["q"], r["k"], r["v"], 4).transpose(1, 0, 2).reshape(T, nq * d)
+    assert np.allclose(r["attn"], O.bf16_round(0.5 * o), rtol=0, atol=0)
+    # K rows come right after the query rows: a zero K block gives equal scores
+    w2 = w.copy()
+    w2[nq * d:(nq + nkv) * d] = 0.0
+    r2 = O.attention_forward(np.ones((T, H)), w2, wo, np.ones(d), np.ones(d), n_q=nq, n_kv=nkv,
+                             head_dim=d, window=0)
+    assert np.allclose(r2["k"], 0.0)

@@ -179,3 +179,22 @@ def dense_inputs(T: int, H: int, I: int, seed: int, device="cpu"):
     w_down = _randn_bf16((H, I), 0.02, g, gen_dev)
     x = _randn_bf16((T, H), 1.0, g, gen_dev, max(1, min(T, (1 << 26) // H)))
     return tuple(t.to(dev) for t in (x, w_gate, w_up, w_down))
+
+
+def attn_inputs(T: int, H: int, n_q: int, n_kv: int, seed: int, device="cpu", head_dim=128):
+    """Attention sublayer inputs: h BF16 N(0,1) [T,H]; the fused weight
+    [W_q; W_k; W_v; W_g] [(2 n_q + 2 n_kv) * head_dim, H] and W_o
+    [H, n_q * head_dim], FP32 N(0, 0.02) rounded to BF16; q/k RMSNorm gains
+    1 + 0.1 N(0,1) (FP32). Small sizes are drawn on the CPU."""
+    dev = torch.device(device)
+    rows = (2 * n_q + 2 * n_kv) * head_dim
+    small = (rows * H + H * n_q * head_dim + T * H) < (1 << 26)
+    gen_dev = "cpu" if small or dev.type == "cpu" else dev
+    g = _gen(gen_dev, seed)
+    w_qkvg = _randn_bf16((rows, H), 0.02, g, gen_dev)
+    w_o = _randn_bf16((H, n_q * head_dim), 0.02, g, gen_dev)
+    x = _randn_bf16((T, H), 1.0, g, gen_dev, max(1, min(T, (1 << 26) // H)))
+    q_gain = 1.0 + 0.1 * torch.randn(head_dim, generator=g, device=gen_dev)
+    k_gain = 1.0 + 0.1 * torch.randn(head_dim, generator=g, device=gen_dev)
+    return dict(x=x.to(dev), w_qkvg=w_qkvg.to(dev), w_o=w_o.to(dev), q_gain=q_gain.to(dev),
+                k_gain=k_gain.to(dev))

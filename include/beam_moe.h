@@ -299,6 +299,64 @@ beam_status_t beam_dense_mlp_forward_nvfp4(const beam_dense_params* p, const voi
                                            const float* post_gain, void* out, void* workspace,
                                            size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Attention sublayer ([P1] section 注意力: 52 layers, hidden 5120; sliding
+ * window of 512 tokens on most layers with RoPE, full context on every sixth
+ * layer and the last with each query multiplied by (1 + (pos+1)/2048)^0.1;
+ * grouped-query attention, 48 query heads and 8 key/value heads, RMSNorm on
+ * queries and keys; a sigmoid gate computed from the layer input scales every
+ * head channel before the output projection. [P1] 残差流: normalised before
+ * and after, the scaled residual step, RoPE and the query scaling in FP32.
+ * [P5] config.json: head_dim 128, sliding_window 512, rope_theta 10000.)
+ * One sequence of T tokens at positions 0..T-1 (prefill):
+ *   x      = PRE_NORM ? bf16(RMSNorm(h_in) * pre_gain) : h_in
+ *   [q|k|v|g] = x W_qkvg^T   (FP32 accumulation)
+ *   q, k   = RMSNorm over each head's 128 channels * q_gain / k_gain (FP32),
+ *            then RoPE (rotate-half, theta^(-2i/128), window > 0) or, for
+ *            window == 0, q *= (1 + (t+1)/2048)^0.1; q, k, v rounded to BF16
+ *   o_h    = softmax(q_h k_{h/(nq/nkv)}^T / sqrt(128) + mask) v_{h/(nq/nkv)},
+ *            mask: causal, and 0 <= i - j < window when window > 0
+ *   a      = bf16(o * sigmoid(g))   (per head and channel)
+ *   y      = a W_o^T                (FP32)
+ *   out    = residual_k >= 2 ? bf16(sqrt((k-1)/k) h_in + RMSNorm(y) * post_gain / sqrt(k))
+ *                            : y (bf16, or fp32 with BEAM_FLAG_FP32_OUT)
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int T;            /* tokens of the sequence (>= 0) */
+  int H;            /* hidden size (5120); multiple of 256, at most 8192 */
+  int n_q, n_kv;    /* query / key-value heads (48 / 8); n_q % n_kv == 0, n_q + n_kv even */
+  int head_dim;     /* 128 (the only supported value) */
+  int window;       /* sliding window (512), or 0 for a global layer */
+  float rope_theta; /* 10000 */
+  float rms_eps;    /* 1e-6 */
+  int residual_k;   /* 0 (no residual) or the step k >= 2 */
+  int flags;        /* BEAM_FLAG_PRE_NORM, BEAM_FLAG_FP32_OUT */
+} beam_attn_params;
+
+/* Workspace bytes for beam_attention_forward (0 on invalid parameters). */
+size_t beam_attention_workspace_size(const beam_attn_params* p);
+
+/* Byte offsets of the attention workspace buffers (diagnostic): 0 pre-normed
+ * x [T,H] bf16, 1 fused projection [T,(2nq+2nkv)*128] fp32, 2 Q [nq][Tp][128]
+ * bf16, 3 K [nkv][Tp][128] bf16, 4 V transposed [nkv][128][Tp] bf16, 5 gate
+ * [T][nq*128] fp32, 6 gated attention output [T][nq*128] bf16, 7 output
+ * projection [T,H] fp32, 8-10 GEMM work lists and counts; Tp = T rounded up
+ * to 128. Writes min(n, 11) entries and returns how many it wrote. */
+int beam_attention_workspace_layout(const beam_attn_params* p, size_t* offsets, int n);
+
+/* Arguments (device pointers, 16-byte aligned):
+ *   h_in    [T,H] bf16
+ *   w_qkvg  [(2 n_q + 2 n_kv) * 128, H] bf16: rows W_q (n_q*128), W_k, W_v
+ *           (n_kv*128 each), W_g (n_q*128)
+ *   w_o     [H, n_q * 128] bf16
+ *   q_gain, k_gain [128] fp32 or NULL (= 1); pre_gain, post_gain [H] fp32 or NULL
+ *   out     [T,H] bf16 (fp32 with BEAM_FLAG_FP32_OUT); must not alias h_in */
+beam_status_t beam_attention_forward(const beam_attn_params* p, const void* h_in,
+                                     const void* w_qkvg, const void* w_o, const float* q_gain,
+                                     const float* k_gain, const float* pre_gain,
+                                     const float* post_gain, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* One scaled residual update ([P1] 残差流):
  *   h_out = bf16( sqrt((k-1)/k) * h_prev + (1/sqrt(k)) * n ),
  *   n = apply_norm ? RMSNorm(sub_out) * post_gain : sub_out   (FP32 math)

@@ -653,14 +653,16 @@ def global_query_scale(pos) -> np.ndarray:
     return (1.0 + (np.asarray(pos, dtype=F64) + 1.0) / 2048.0) ** 0.1
 
 
-def attention_core(q, k, v, window: int) -> np.ndarray:
+def attention_core(q, k, v, window: int, q_pos=None) -> np.ndarray:
     """softmax(q k^T / sqrt(d) + mask) v per head with the causal (and, when
-    window > 0, sliding-window) mask; q [nq, T, d], k and v [nkv, T, d],
-    query head h reads key/value head h // (nq // nkv). FP64."""
+    window > 0, sliding-window) mask; q [nq, Tq, d] at positions q_pos
+    (default 0..Tq-1), k and v [nkv, T, d] at positions 0..T-1; query head h
+    reads key/value head h // (nq // nkv). FP64."""
     q, k, v = (np.asarray(a, dtype=F64) for a in (q, k, v))
-    nq, T, d = q.shape
+    nq, Tq, d = q.shape
+    T = k.shape[1]
     group = nq // k.shape[0]
-    i = np.arange(T)[:, None]
+    i = (np.arange(Tq) if q_pos is None else np.asarray(q_pos))[:, None]
     j = np.arange(T)[None, :]
     allowed = j <= i
     if window > 0:
@@ -676,34 +678,40 @@ def attention_core(q, k, v, window: int) -> np.ndarray:
 
 
 def attention_forward(h_in, w_qkvg, w_o, q_gain, k_gain, *, n_q=48, n_kv=8, head_dim=128,
-                      window=512, rope_theta=10000.0, eps=1e-6, pre_gain=None,
-                      residual_k=0, post_gain=None) -> dict:
+                      window=512, rope_theta=10000.0, eps=1e-6, pre_norm=True, pre_gain=None,
+                      residual_k=0, post_gain=None, query_rows=None) -> dict:
     """The attention sublayer for one sequence of T tokens at positions 0..T-1.
 
-    h_in [T, H] (h_{k-1}); w_qkvg [(n_q + 2 n_kv + n_q) * head_dim, H];
-    w_o [H, n_q * head_dim]; q_gain, k_gain [head_dim]. window > 0: sliding
-    layer with RoPE; window == 0: global layer with the query scale.
-    Returns dict(x, q, k, v, gate, attn (gated, BF16-rounded), out, h)."""
+    h_in [T, H] (h_{k-1}; used as x itself when pre_norm is False);
+    w_qkvg [(n_q + 2 n_kv + n_q) * head_dim, H]; w_o [H, n_q * head_dim];
+    q_gain, k_gain [head_dim]. window > 0: sliding layer with RoPE;
+    window == 0: global layer with the query scale. query_rows: compute the
+    outputs of these token rows only (keys and values of every token).
+    Returns dict(x, q, k, v, gate, attn (gated, BF16-rounded), out, h) over
+    the output rows."""
     h_in = np.asarray(h_in, dtype=F64)
     T, H = h_in.shape
-    x = bf16_round(rms_norm(h_in, pre_gain, eps)).astype(F64)
-    proj = x @ np.asarray(w_qkvg, dtype=F64).T
+    rows = np.arange(T) if query_rows is None else np.asarray(query_rows)
+    x = bf16_round(rms_norm(h_in, pre_gain, eps)).astype(F64) if pre_norm else h_in
+    w = np.asarray(w_qkvg, dtype=F64)
     dq, dkv = n_q * head_dim, n_kv * head_dim
-    q = proj[:, :dq].reshape(T, n_q, head_dim).transpose(1, 0, 2)
-    k = proj[:, dq:dq + dkv].reshape(T, n_kv, head_dim).transpose(1, 0, 2)
-    v = proj[:, dq + dkv:dq + 2 * dkv].reshape(T, n_kv, head_dim).transpose(1, 0, 2)
-    gate = sigmoid(proj[:, dq + 2 * dkv:])                      # [T, n_q * head_dim]
+    qg = x[rows] @ np.concatenate([w[:dq], w[dq + 2 * dkv:]]).T          # q and gate rows
+    kv = x @ w[dq:dq + 2 * dkv].T
+    q = qg[:, :dq].reshape(len(rows), n_q, head_dim).transpose(1, 0, 2)
+    k = kv[:, :dkv].reshape(T, n_kv, head_dim).transpose(1, 0, 2)
+    v = kv[:, dkv:].reshape(T, n_kv, head_dim).transpose(1, 0, 2)
+    gate = sigmoid(qg[:, dq:])                                  # [rows, n_q * head_dim]
     q = rms_norm(q, q_gain, eps)
     k = rms_norm(k, k_gain, eps)
-    pos = np.arange(T)
     if window > 0:
-        q = rope_rotate(q, pos, rope_theta)
-        k = rope_rotate(k, pos, rope_theta)
+        q = rope_rotate(q, rows, rope_theta)
+        k = rope_rotate(k, np.arange(T), rope_theta)
     else:
-        q = q * global_query_scale(pos)[None, :, None]
+        q = q * global_query_scale(rows)[None, :, None]
     q, k, v = (bf16_round(a).astype(F64) for a in (q, k, v))
-    o = attention_core(q, k, v, window)                          # [n_q, T, d]
-    attn = bf16_round(o.transpose(1, 0, 2).reshape(T, dq) * gate).astype(F64)
+    o = attention_core(q, k, v, window, q_pos=rows)              # [n_q, rows, d]
+    attn = bf16_round(o.transpose(1, 0, 2).reshape(len(rows), dq) * gate).astype(F64)
     out = attn @ np.asarray(w_o, dtype=F64).T
-    hk = residual_step(h_in, out, residual_k, post_gain, eps, True) if residual_k else None
+    hk = (residual_step(h_in[rows], out, residual_k, post_gain, eps, True)
+          if residual_k else None)
     return dict(x=x, q=q, k=k, v=v, gate=gate, attn=attn, out=out, h=hk)

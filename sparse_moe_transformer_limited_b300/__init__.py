@@ -2,7 +2,8 @@
 
 The layer (router, group-limited top-8, normalised x2.5 weights, token
 permutation, SwiGLU experts, weighted combine, post-RMSNorm and the scaled
-residual update; BF16, E4M3 or NVFP4 expert weights) runs in the library's CUDA kernels; this package only
+residual update; BF16, E4M3 or NVFP4 expert weights), the dense MLP and the
+attention sublayer runs in the library's CUDA kernels; this package only
 marshals torch tensors into the C ABI declared in include/beam_moe.h.
 """
 from ._native import (BeamError, Params, make_params, workspace_size, workspace_layout,
@@ -11,7 +12,9 @@ from ._native import (BeamError, Params, make_params, workspace_size, workspace_
                       FLAG_FP32_OUT, FLAG_RETURN_SCORES, FLAG_FP8_EXPERTS, profile_enable,
                       profile_read, quantize_e4m3_rows, forward_fp8, dense_forward_fp8,
                       dense_workspace_size, dense_workspace_layout, FLAG_NVFP4_EXPERTS,
-                      quantize_nvfp4, forward_nvfp4, dense_forward_nvfp4)
+                      quantize_nvfp4, forward_nvfp4, dense_forward_nvfp4, AttnParams,
+                      make_attn_params, attention_workspace_size, attention_forward,
+                      attention_workspace_layout)
 
 __all__ = ["BeamError", "Params", "make_params", "workspace_size", "workspace_layout",
            "alloc_workspace", "route", "route_static", "forward", "dense_forward", "DenseParams", "residual_step", "status", "last_error",
@@ -19,4 +22,6 @@ __all__ = ["BeamError", "Params", "make_params", "workspace_size", "workspace_la
            "FLAG_FP32_OUT", "FLAG_RETURN_SCORES", "FLAG_FP8_EXPERTS", "profile_enable",
            "profile_read", "quantize_e4m3_rows", "forward_fp8", "dense_forward_fp8",
            "dense_workspace_size", "dense_workspace_layout", "FLAG_NVFP4_EXPERTS",
-           "quantize_nvfp4", "forward_nvfp4", "dense_forward_nvfp4"]
+           "quantize_nvfp4", "forward_nvfp4", "dense_forward_nvfp4", "AttnParams",
+           "make_attn_params", "attention_workspace_size", "attention_forward",
+           "attention_workspace_layout"]

@@ -43,7 +43,9 @@ EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static"
             "beam_moe_workspace_layout", "beam_debug_wait_timeout", "beam_profile_enable",
             "beam_profile_read", "beam_quantize_e4m3_rows", "beam_moe_forward_fp8",
             "beam_dense_mlp_forward_fp8", "beam_dense_workspace_layout",
-            "beam_quantize_nvfp4", "beam_moe_forward_nvfp4", "beam_dense_mlp_forward_nvfp4")
+            "beam_quantize_nvfp4", "beam_moe_forward_nvfp4", "beam_dense_mlp_forward_nvfp4",
+            "beam_attention_workspace_size", "beam_attention_forward",
+            "beam_attention_workspace_layout")
 
 
 class BeamError(RuntimeError):
@@ -64,6 +66,13 @@ class DenseParams(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("rms_eps", ctypes.c_float), ("residual_k", ctypes.c_int),
                 ("flags", ctypes.c_int)]
+
+
+class AttnParams(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("n_q", ctypes.c_int),
+                ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int), ("window", ctypes.c_int),
+                ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("residual_k", ctypes.c_int), ("flags", ctypes.c_int)]
 
 
 _lib = None
@@ -108,6 +117,13 @@ def lib() -> ctypes.CDLL:
         L.beam_moe_forward_nvfp4.restype = i32
         L.beam_dense_mlp_forward_nvfp4.argtypes = [D] + [vp] * 14 + [sz, vp]
         L.beam_dense_mlp_forward_nvfp4.restype = i32
+        A = ctypes.POINTER(AttnParams)
+        L.beam_attention_workspace_size.argtypes = [A]
+        L.beam_attention_workspace_size.restype = sz
+        L.beam_attention_workspace_layout.argtypes = [A, ctypes.POINTER(sz), i32]
+        L.beam_attention_workspace_layout.restype = i32
+        L.beam_attention_forward.argtypes = [A] + [vp] * 9 + [sz, vp]
+        L.beam_attention_forward.restype = i32
         L.beam_residual_step.argtypes = [vp, vp, i32, i32, i32, vp, f32, i32, i32, vp, vp]
         L.beam_residual_step.restype = i32
         L.beam_status.argtypes = [vp]
@@ -350,6 +366,45 @@ def dense_forward_nvfp4(T, H, I, x, gate_q, up_q, down_q, pre_gain=None, post_ga
         ctypes.byref(p), _ptr(x), *[_ptr(t) for q in (gate_q, up_q, down_q) for t in q],
         _ptr(pre_gain), _ptr(post_gain), _ptr(out), _ptr(workspace), workspace.numel(),
         _stream(stream)))
+    return out
+
+
+def make_attn_params(T, H=5120, n_q=48, n_kv=8, head_dim=128, window=512, rope_theta=10000.0,
+                     rms_eps=1e-6, residual_k=0, flags=0) -> AttnParams:
+    return AttnParams(T, H, n_q, n_kv, head_dim, window, rope_theta, rms_eps, residual_k, flags)
+
+
+def attention_workspace_size(p: AttnParams) -> int:
+    n = lib().beam_attention_workspace_size(ctypes.byref(p))
+    if n == 0:
+        raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
+    return int(n)
+
+
+ATTN_LAYOUT_NAMES = ("x", "proj", "q", "k", "vt", "gate", "attn", "y", "units_qkvg", "units_o",
+                     "n_units")
+
+
+def attention_workspace_layout(p: AttnParams) -> dict:
+    arr = (ctypes.c_size_t * len(ATTN_LAYOUT_NAMES))()
+    n = lib().beam_attention_workspace_layout(ctypes.byref(p), arr, len(ATTN_LAYOUT_NAMES))
+    if n == 0:
+        raise BeamError(BEAM_ERR_INVALID_ARG, lib().beam_last_error_string().decode())
+    return {ATTN_LAYOUT_NAMES[i]: int(arr[i]) for i in range(n)}
+
+
+def attention_forward(p: AttnParams, h, w_qkvg, w_o, q_gain=None, k_gain=None, pre_gain=None,
+                      post_gain=None, out=None, workspace=None, stream=None):
+    """beam_attention_forward: the attention sublayer over one sequence."""
+    if out is None:
+        dt = torch.float32 if (p.flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((p.T, p.H), dtype=dt, device=h.device)
+    if workspace is None:
+        workspace = torch.empty(attention_workspace_size(p), dtype=torch.uint8, device=h.device)
+    _check(lib().beam_attention_forward(ctypes.byref(p), _ptr(h), _ptr(w_qkvg), _ptr(w_o),
+                                        _ptr(q_gain), _ptr(k_gain), _ptr(pre_gain),
+                                        _ptr(post_gain), _ptr(out), _ptr(workspace),
+                                        workspace.numel(), _stream(stream)))
     return out
 
 

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "beam_moe.h"
+#include "kernels_attn.cuh"
 #include "kernels_gemm.cuh"
 #include "kernels_gemm_tm.cuh"
 #include "kernels_gemm_2sm.cuh"
@@ -1251,6 +1252,220 @@ beam_status_t beam_debug_wait_timeout(uint64_t timeout_ns, void* stream) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Attention sublayer (beam_attention_forward).
+// ===========================================================================
+namespace {
+
+enum { A_XN = 0, A_PROJ, A_Q, A_K, A_VT, A_GATE, A_ATT, A_Y, A_U1, A_U2, A_NU, kAttnEntries };
+
+struct AttnLayout {
+  size_t off[kAttnEntries];
+  size_t total;
+  int Tp, N1, MT1, MT2, groups;
+};
+
+beam_status_t check_attn(const beam_attn_params* p) {
+  if (p == nullptr) return fail(BEAM_ERR_INVALID_ARG, "params is NULL");
+  if (p->T < 0 || p->H <= 0 || p->n_q <= 0 || p->n_kv <= 0)
+    return fail(BEAM_ERR_INVALID_ARG, "T=%d H=%d n_q=%d n_kv=%d", p->T, p->H, p->n_q, p->n_kv);
+  if (p->T > (1 << 20)) return fail(BEAM_ERR_UNSUPPORTED, "T=%d exceeds 1048576", p->T);
+  if (p->head_dim != beam::ATT_D) return fail(BEAM_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (p->H % 256 || p->H > 8192) return fail(BEAM_ERR_UNSUPPORTED, "H=%d: a multiple of 256, at most 8192", p->H);
+  if (p->n_q % p->n_kv || (p->n_q + p->n_kv) % 2 || p->n_q > 128)
+    return fail(BEAM_ERR_UNSUPPORTED, "n_q=%d, n_kv=%d: n_q a multiple of n_kv, n_q + n_kv even, n_q <= 128",
+                p->n_q, p->n_kv);
+  if (p->window < 0) return fail(BEAM_ERR_INVALID_ARG, "window=%d must be >= 0", p->window);
+  if (!(p->rope_theta > 0.f) || !std::isfinite(p->rope_theta))
+    return fail(BEAM_ERR_INVALID_ARG, "rope_theta must be positive");
+  if (!(p->rms_eps >= 0.f) || !std::isfinite(p->rms_eps)) return fail(BEAM_ERR_INVALID_ARG, "rms_eps");
+  if (p->residual_k == 1 || p->residual_k < 0)
+    return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", p->residual_k);
+  if (p->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT))
+    return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  if ((p->flags & BEAM_FLAG_FP32_OUT) && p->residual_k >= 2)
+    return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP32_OUT applies only without the residual step");
+  return BEAM_OK;
+}
+
+AttnLayout attn_layout(const beam_attn_params& p) {
+  AttnLayout L{};
+  const size_t T = static_cast<size_t>(p.T);
+  L.Tp = (p.T + beam::ATT_BQ - 1) / beam::ATT_BQ * beam::ATT_BQ;
+  L.N1 = (2 * p.n_q + 2 * p.n_kv) * beam::ATT_D;
+  L.MT1 = L.N1 / 256;
+  L.MT2 = p.H / 256;
+  L.groups = (p.T + 255) / 256;
+  const size_t dq = static_cast<size_t>(p.n_q) * beam::ATT_D;
+  size_t sz[kAttnEntries];
+  sz[A_XN] = (p.flags & BEAM_FLAG_PRE_NORM) ? T * p.H * 2 : 0;
+  sz[A_PROJ] = T * L.N1 * 4;
+  sz[A_Q] = static_cast<size_t>(p.n_q) * L.Tp * beam::ATT_D * 2;
+  sz[A_K] = static_cast<size_t>(p.n_kv) * L.Tp * beam::ATT_D * 2;
+  sz[A_VT] = static_cast<size_t>(p.n_kv) * beam::ATT_D * L.Tp * 2;
+  sz[A_GATE] = T * dq * 4;
+  sz[A_ATT] = T * dq * 2;
+  sz[A_Y] = T * p.H * 4;
+  sz[A_U1] = static_cast<size_t>(L.MT1) * L.groups * 16;
+  sz[A_U2] = static_cast<size_t>(L.MT2) * L.groups * 16;
+  sz[A_NU] = 16;
+  size_t cur = 0;
+  for (int i = 0; i < kAttnEntries; ++i) {
+    L.off[i] = cur;
+    cur = align_up(cur + sz[i], 1024);
+  }
+  L.total = cur;
+  return L;
+}
+
+// y [n, N] (FP32) = x [n, K] W [N, K]^T on the 2-SM pair kernel (one expert).
+beam_status_t dense_linear(const void* x, const void* w, int n, int N, int K, float* y,
+                           const int4* units, const int* n_units, cudaStream_t st,
+                           const char* prof_name) {
+  beam_status_t s;
+  CUtensorMap m_w, m_x, m_x64;
+  if ((s = make_map(&m_w, w, static_cast<uint64_t>(N), K, 128)) != BEAM_OK) return s;
+  if ((s = make_map(&m_x, x, static_cast<uint64_t>(n), K, 16)) != BEAM_OK) return s;
+  if ((s = make_map(&m_x64, x, static_cast<uint64_t>(n), K, 64)) != BEAM_OK) return s;
+  beam::PairArgs a{};
+  a.units = units;
+  a.n_units = n_units;
+  a.k_blocks = K / 64;
+  a.w_rows_per_expert = N;
+  a.y = y;
+  a.out_ld = N;
+  a.timeout_ns = kWaitTimeoutNs;
+  return launch_gemm_pair<1, false>(m_w, m_w, m_x, m_x64, a, st, prof_name);
+}
+
+}  // namespace
+
+extern "C" size_t beam_attention_workspace_size(const beam_attn_params* p) {
+  if (check_attn(p) != BEAM_OK) return 0;
+  return attn_layout(*p).total;
+}
+
+extern "C" int beam_attention_workspace_layout(const beam_attn_params* p, size_t* offsets, int n) {
+  if (check_attn(p) != BEAM_OK || offsets == nullptr || n <= 0) return 0;
+  const AttnLayout L = attn_layout(*p);
+  const int m = n < kAttnEntries ? n : kAttnEntries;
+  for (int i = 0; i < m; ++i) offsets[i] = L.off[i];
+  return m;
+}
+
+extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const void* h_in,
+                                                const void* w_qkvg, const void* w_o,
+                                                const float* q_gain, const float* k_gain,
+                                                const float* pre_gain, const float* post_gain,
+                                                void* out, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_attn(p);
+  if (s != BEAM_OK) return s;
+  if (p->T == 0) return BEAM_OK;
+  if (!h_in || !w_qkvg || !w_o || !out || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  const void* ptrs[] = {h_in, w_qkvg, w_o, out, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
+  const void* opt[] = {q_gain, k_gain, pre_gain, post_gain};
+  for (const void* q : opt)
+    if (q && !aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
+  if (out == h_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias h_in");
+  const AttnLayout L = attn_layout(*p);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int T = p->T, H = p->H, nq = p->n_q, nkv = p->n_kv;
+  const int dq = nq * beam::ATT_D;
+
+  // 1. pre-norm
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(h_in);
+  if (p->flags & BEAM_FLAG_PRE_NORM) {
+    __nv_bfloat16* xn = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_XN]);
+    {
+      ProfScope ps("prenorm", st);
+      beam::prenorm_kernel<<<(T + 7) / 8, 256, 0, st>>>(x, pre_gain, xn, T, H, p->rms_eps);
+    }
+    BEAM_LAUNCH_CHECK("prenorm_kernel");
+    x = xn;
+  }
+  // 2. work lists of the two dense GEMMs, then the fused Q/K/V/gate projection
+  int4* u1 = reinterpret_cast<int4*>(ws + L.off[A_U1]);
+  int4* u2 = reinterpret_cast<int4*>(ws + L.off[A_U2]);
+  int* nu = reinterpret_cast<int*>(ws + L.off[A_NU]);
+  beam::linear_units_kernel<<<4, 256, 0, st>>>(T, L.MT1, u1, nu + 0);
+  beam::linear_units_kernel<<<4, 256, 0, st>>>(T, L.MT2, u2, nu + 1);
+  BEAM_LAUNCH_CHECK("linear_units_kernel");
+  float* proj = reinterpret_cast<float*>(ws + L.off[A_PROJ]);
+  if ((s = dense_linear(x, w_qkvg, T, L.N1, H, proj, u1, nu + 0, st, "attn_qkvg_proj")) != BEAM_OK)
+    return s;
+  // 3. QK-norm, RoPE / query scale, V transposed, gate; V^T padding keys zeroed
+  __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_Q]);
+  __nv_bfloat16* k = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_K]);
+  __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_VT]);
+  float* gate = reinterpret_cast<float*>(ws + L.off[A_GATE]);
+  if (L.Tp > T)
+    BEAM_CUDA_TRY(cudaMemset2DAsync(vt + T, static_cast<size_t>(L.Tp) * 2, 0,
+                                    static_cast<size_t>(L.Tp - T) * 2,
+                                    static_cast<size_t>(nkv) * beam::ATT_D, st));
+  {
+    ProfScope ps("attn_prep", st);
+    dim3 grid(T, (2 * nq + 2 * nkv + 7) / 8);
+    beam::attn_prep_kernel<<<grid, 256, 0, st>>>(proj, T, L.Tp, nq, nkv, q_gain, k_gain,
+                                                 p->rms_eps, p->window, p->rope_theta, q, k, vt,
+                                                 gate);
+  }
+  BEAM_LAUNCH_CHECK("attn_prep_kernel");
+  // 4. attention, gated, BF16
+  __nv_bfloat16* att = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_ATT]);
+  {
+    CUtensorMap m_q, m_k, m_vt;
+    if ((s = make_map(&m_q, q, static_cast<uint64_t>(nq) * L.Tp, beam::ATT_D, 128)) != BEAM_OK) return s;
+    if ((s = make_map(&m_k, k, static_cast<uint64_t>(nkv) * L.Tp, beam::ATT_D, 128)) != BEAM_OK) return s;
+    if ((s = make_map(&m_vt, vt, static_cast<uint64_t>(nkv) * beam::ATT_D, L.Tp, 128)) != BEAM_OK) return s;
+    beam::AttnArgs aa{};
+    aa.T = T;
+    aa.Tp = L.Tp;
+    aa.nq = nq;
+    aa.nkv = nkv;
+    aa.window = p->window;
+    aa.scale = 1.0f / std::sqrt(static_cast<float>(beam::ATT_D));
+    aa.gate = gate;
+    aa.out = att;
+    aa.timeout_ns = kWaitTimeoutNs;
+    static bool attr_set = false;
+    if (!attr_set) {
+      BEAM_CUDA_TRY(cudaFuncSetAttribute(beam::flash_attn_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         beam::AttnCfg::SMEM_BYTES));
+      attr_set = true;
+    }
+    ProfScope ps("flash_attn", st);
+    beam::flash_attn_kernel<<<dim3(L.Tp / beam::ATT_BQ, nq), 192, beam::AttnCfg::SMEM_BYTES, st>>>(
+        m_q, m_k, m_vt, aa);
+  }
+  BEAM_LAUNCH_CHECK("flash_attn_kernel");
+  // 5. output projection (FP32; straight into `out` with BEAM_FLAG_FP32_OUT)
+  const bool resid = p->residual_k >= 2;
+  float* y = (p->flags & BEAM_FLAG_FP32_OUT) ? static_cast<float*>(out)
+                                             : reinterpret_cast<float*>(ws + L.off[A_Y]);
+  if ((s = dense_linear(att, w_o, T, H, dq, y, u2, nu + 1, st, "attn_out_proj")) != BEAM_OK) return s;
+  // 6. post-norm + scaled residual, or the BF16 output
+  if (!(p->flags & BEAM_FLAG_FP32_OUT)) {
+    const float kf = static_cast<float>(resid ? p->residual_k : 2);
+    const float a = resid ? std::sqrt((kf - 1.f) / kf) : 0.f;
+    const float b = resid ? 1.f / std::sqrt(kf) : 1.f;
+    ProfScope ps("attn_finalize", st);
+    beam::finalize_rows_kernel<float><<<(T + 7) / 8, 256, 0, st>>>(
+        y, static_cast<const __nv_bfloat16*>(h_in), post_gain, static_cast<__nv_bfloat16*>(out), T,
+        H, p->rms_eps, a, b, resid ? 1 : 0, resid ? 1 : 0);
+    BEAM_LAUNCH_CHECK("finalize_rows_kernel");
+  }
+  return BEAM_OK;
+}
 
 // ===========================================================================
 // Allocation-free router (beam_moe_route_static).

@@ -159,3 +159,30 @@ def test_nvfp4_workspace_pads_expert_rows():
     # T=64, top-8: up to 256 experts each padded to 32 rows -> far more rows
     assert f4["act"] - f4["xperm"] > plain["act"] - plain["xperm"]
     assert f4["act_sf"] > f4["x_sf"] > f4["act_scale"]
+
+
+def test_attn_params_struct_matches_header():
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct \{([^{}]*)\} beam_attn_params;", src).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b([A-Za-z_][A-Za-z_0-9]*)\s*[,;]", body)
+    assert fields == [f for f, _ in B.AttnParams._fields_]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=64), 2), (dict(H=5000), 2), (dict(n_q=48, n_kv=5), 2), (dict(n_q=7, n_kv=2), 2),
+    (dict(window=-1), 1), (dict(residual_k=1), 1), (dict(flags=64), 1),
+    (dict(flags=2, residual_k=50), 1), (dict(T=-1), 1),
+])
+def test_attn_invalid_params_rejected(kw, code):
+    base = dict(T=64)
+    base.update(kw)
+    p = B.make_attn_params(**base)
+    assert B.lib().beam_attention_workspace_size(ctypes.byref(p)) == 0
+    assert B.lib().beam_attention_forward(ctypes.byref(p), *([None] * 9), 0, None) == code
+
+
+def test_attn_workspace_and_empty_sequence():
+    assert B.attention_workspace_size(B.make_attn_params(T=8192)) > 8192 * 14336 * 4
+    p = B.make_attn_params(T=0)
+    assert B.lib().beam_attention_forward(ctypes.byref(p), *([None] * 9), 0, None) == 0

@@ -117,3 +117,19 @@ def test_forward_gate_and_layout():
     r2 = O.attention_forward(np.ones((T, H)), w2, wo, np.ones(d), np.ones(d), n_q=nq, n_kv=nkv,
                              head_dim=d, window=0)
     assert np.allclose(r2["k"], 0.0)
+
+
+def test_forward_query_row_subset_equals_full():
+    rng = np.random.default_rng(5)
+    T, H, nq, nkv, d = 30, 64, 4, 2, 16
+    w = rng.standard_normal(((nq + 2 * nkv + nq) * d, H)) * 0.1
+    wo = rng.standard_normal((H, nq * d)) * 0.1
+    h = rng.standard_normal((T, H))
+    for window in (0, 7):
+        full = O.attention_forward(h, w, wo, np.ones(d), np.ones(d), n_q=nq, n_kv=nkv,
+                                   head_dim=d, window=window, residual_k=5)
+        rows = np.array([0, 3, 17, 29])
+        sub = O.attention_forward(h, w, wo, np.ones(d), np.ones(d), n_q=nq, n_kv=nkv,
+                                  head_dim=d, window=window, residual_k=5, query_rows=rows)
+        assert np.allclose(sub["out"], full["out"][rows], rtol=1e-12, atol=1e-12)
+        assert np.allclose(sub["h"], full["h"][rows], rtol=1e-12, atol=1e-12)

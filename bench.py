@@ -391,6 +391,77 @@ def run_dense(args, rank, world, local_rank, name):
             "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in prof.items()}, "clocks": clk}
 
 
+# ------------------------------------------------------- attention arm
+# The attention sublayer over one sequence of 8192 tokens (hidden 5120, 48
+# query / 8 key-value heads of 128, pre-norm, post-norm and residual): a
+# sliding-window layer (window 512, RoPE; layer 4, residual step k = 10) and a
+# global layer (layer 5, k = 12).
+ATTN = {"attn_swa": dict(T=8192, window=512, k=10, seed=12),
+        "attn_global": dict(T=8192, window=0, k=12, seed=13)}
+
+
+def run_attn(args, rank, world, local_rank, name):
+    import sparse_moe_transformer_limited_b300 as B
+    B.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = ATTN[name]
+    T, H, nq, nkv, D = cfg["T"], 5120, 48, 8, 128
+    d = S.attn_inputs(T, H, nq, nkv, cfg["seed"] + 1000 * rank, dev)
+    p = B.make_attn_params(T, H, nq, nkv, D, cfg["window"], 10000.0, 1e-6, cfg["k"],
+                           B.FLAG_PRE_NORM)
+    ws = torch.empty(B.attention_workspace_size(p), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        B.attention_forward(p, d["x"], d["w_qkvg"], d["w_o"], d["q_gain"], d["k_gain"], out=out,
+                            workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    B.profile_read()
+    B.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    steps = max(1, args.steps // 2)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    B.profile_enable(False)
+    clk = clocks.stop()
+    prof = B.profile_read()
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    ms = e0.elapsed_time(e1) / steps
+    w = cfg["window"]
+    pairs = sum(min(i + 1, w) for i in range(T)) if w else T * (T + 1) // 2
+    attn_flops = 4.0 * nq * D * pairs                        # Q K^T and P V over visible pairs
+    proj_flops = 2.0 * T * H * (2 * nq + 2 * nkv) * D + 2.0 * T * nq * D * H
+    peaks = _peaks()
+    k_ms = {k: v[0] / v[1] for k, v in prof.items()}
+    top = "flash_attn" if k_ms.get("flash_attn", 0) > k_ms.get("attn_qkvg_proj", 0) else "attn_qkvg_proj"
+    top_flops = attn_flops if top == "flash_attn" else 2.0 * T * H * (2 * nq + 2 * nkv) * D
+    ach = top_flops / (k_ms[top] / 1e3) / 1e12
+    return {"workload": f"attention sublayer, one sequence of T={T}, hidden {H}, {nq}/{nkv} heads x "
+                        f"{D}, {'sliding window ' + str(w) + ' + RoPE' if w else 'global + query scale'}, "
+                        f"pre-norm, post-norm, residual k={cfg['k']}",
+            "value": round(T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "layer_tflops": round((attn_flops + proj_flops) / (ms / 1e3) / 1e12, 1),
+            "roofline": {"kernel": top, "bound": "tensor", "achieved": round(ach, 1),
+                         "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(ach / peaks["bf16"], 4),
+                         "algorithmic_flops_per_launch": top_flops, "launch_ms": round(k_ms[top], 4),
+                         "peak_source": peaks["source"] + " bf16_tflops (burst)"},
+            "kernels_ms": {k: round(v, 4) for k, v in sorted(k_ms.items(), key=lambda kv: -kv[1])},
+            "clocks": clk}
+
+
 # ---------------------------------------------------------- oracle arm
 def _blas_threads():
     try:
@@ -489,7 +560,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode", choices=sorted(S.WORKLOADS) + sorted(DENSE))
+    ap.add_argument("--config", default="decode",
+                    choices=sorted(S.WORKLOADS) + sorted(DENSE) + sorted(ATTN))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--experts", default="bf16", choices=["bf16", "fp8", "nvfp4"],
                     help="expert weight type of the timed sublayer (fp8: E4M3 + row scales; "
@@ -511,8 +583,9 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
-    if args.config in DENSE:
-        r = run_dense(args, rank, world, local_rank, args.config)
+    if args.config in DENSE or args.config in ATTN:
+        fn = run_dense if args.config in DENSE else run_attn
+        r = fn(args, rank, world, local_rank, args.config)
         if rank == 0:
             print(json.dumps(dict(metric=METRIC, n_gpus=world, steps=args.steps, **r)), flush=True)
         return
@@ -550,6 +623,9 @@ def main():
                     "roofline": rr["roofline"], "layer": rr["layer"],
                     "kernels_ms": rr["kernels_ms"], "clocks": rr["clocks"]}
         extra = {"dense_mlp_T8192": extra_dense, "prefill_T8192": summary(r2)}
+        for an in ("attn_swa", "attn_global"):
+            torch.cuda.empty_cache()
+            extra[f"attention_{an[5:]}_T8192"] = run_attn(a2, rank, world, local_rank, an)
         if kind == "bf16":
             # the same sublayers with E4M3 and NVFP4 expert weights (secondary lines)
             a3 = argparse.Namespace(**vars(args))

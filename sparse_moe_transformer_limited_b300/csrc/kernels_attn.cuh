@@ -113,17 +113,24 @@ __global__ void linear_units_kernel(int n, int MT, int4* __restrict__ units, int
 
 // ---------------------------------------------------------------------------
 // Flash attention on tcgen05, one CTA per (query tile of 128 rows, query
-// head). Warp 0: TMA producer (Q once, then K and V^T tiles of 128 keys into
-// a two-stage ring). Warp 1: TMEM owner and MMA issuer: S_j = Q K_j^T into
-// one of two TMEM S buffers, then O += P_j V_j into TMEM once P_j is ready.
-// Warps 2..5 (thread = query row = TMEM lane): per tile read S, mask, online
-// softmax in FP32 (running max m and sum l), rescale the O row in TMEM when
-// m grows, write P (BF16) into shared memory in the MMA's 128-byte-swizzled
-// K-major layout; at the end O / l times the gate, BF16, to `out`.
+// head). Warp 0: TMA producer -- lane 0 loads Q once and then K tiles of 128
+// keys into a three-stage ring (a stage is freed as soon as its S has been
+// computed), lane 1 loads V^T tiles into a two-stage ring (freed after P V).
+// Warp 1: TMEM owner and MMA issuer: S_0 and S_1 up front into two TMEM S
+// buffers; then per tile j: O += P_j V_j as soon as P_j is ready, then
+// S_{j+2} into the buffer S_j leaves. Warps 2..5 (thread = query row = TMEM
+// lane): per tile read the S row, mask, online softmax in FP32 with a lazy
+// reference: the row maximum m moves (and the O row in TMEM is rescaled)
+// only when a tile's maximum exceeds m by more than ATT_TAU, so P <= e^TAU;
+// the exponentials are computed before waiting for the previous P V; P is
+// written as BF16 into the 128-byte-swizzled K-major tile the MMA reads. At
+// the end O / l times the gate, BF16, to `out`.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384).
 // All waits are bounded; on expiry the error word is set and every role
-// leaves after in-flight copies and MMAs have completed.
+// leaves after its in-flight copies and MMAs have completed.
 // ---------------------------------------------------------------------------
+constexpr float ATT_TAU = 8.0f;
+
 struct AttnArgs {
   int T, Tp, nq, nkv, window;
   float scale;                 // 1 / sqrt(head_dim)
@@ -137,9 +144,10 @@ struct AttnCfg {
   static constexpr int K_BYTES = ATT_BK * ATT_D * 2;     // 32 KB
   static constexpr int V_BYTES = ATT_D * ATT_BK * 2;     // 32 KB (V^T: 128 channels x 128 keys)
   static constexpr int P_BYTES = ATT_BQ * ATT_BK * 2;    // 32 KB
-  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-  static constexpr int BAR_BYTES = 16 * 8 + 16;
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + 2 * STAGE_BYTES + P_BYTES + BAR_BYTES;
+  static constexpr int K_STAGES = 3, V_STAGES = 2;
+  static constexpr int BAR_BYTES = 20 * 8 + 16;
+  static constexpr int SMEM_BYTES =
+      1024 + Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES + P_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -160,17 +168,20 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + C::Q_BYTES;                    // stage s: K at s*STAGE, V^T after
-  uint8_t* sP = sKV + 2 * C::STAGE_BYTES;
+  uint8_t* sK = sQ + C::Q_BYTES;
+  uint8_t* sV = sK + C::K_STAGES * C::K_BYTES;
+  uint8_t* sP = sV + C::V_STAGES * C::V_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + C::P_BYTES);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;       // [2]
-  uint64_t* kv_empty = bars + 3;      // [2]
-  uint64_t* s_full = bars + 5;        // [2]
-  uint64_t* p_full = bars + 7;
-  uint64_t* o_done = bars + 8;
-  uint64_t* mma_done = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* k_full = bars + 1;        // [3]
+  uint64_t* k_empty = bars + 4;       // [3]
+  uint64_t* v_full = bars + 7;        // [2]
+  uint64_t* v_empty = bars + 9;       // [2]
+  uint64_t* s_full = bars + 11;       // [2]
+  uint64_t* p_full = bars + 13;
+  uint64_t* o_done = bars + 14;
+  uint64_t* mma_done = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -185,11 +196,16 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-      mbar_init(&s_full[s], 1);
+    for (int s = 0; s < C::K_STAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
+    for (int s = 0; s < C::V_STAGES; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
@@ -210,35 +226,44 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ producers
+    if (lane < 2) {
       const uint64_t pol = l2_policy_evict_last();
-      const int qrow = h * args.Tp + qt * ATT_BQ;
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      tma_load_2d(sQ, &tm_q, q_full, 0, qrow, pol);
-      tma_load_2d(sQ + C::Q_BYTES / 2, &tm_q, q_full, 64, qrow, pol);
+      const volatile int never = 0;
+      if (lane == 0) {
+        const int qrow = h * args.Tp + qt * ATT_BQ;
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+        tma_load_2d(sQ, &tm_q, q_full, 0, qrow, pol);
+        tma_load_2d(sQ + C::Q_BYTES / 2, &tm_q, q_full, 64, qrow, pol);
+      }
+      // lane 0: K tiles (3 stages); lane 1: V^T tiles (2 stages)
+      const int NS = lane == 0 ? C::K_STAGES : C::V_STAGES;
+      uint64_t* full = lane == 0 ? k_full : v_full;
+      uint64_t* empty = lane == 0 ? k_empty : v_empty;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait_bounded(&kv_empty[s], ((j >> 1) & 1) ^ 1u, tmo, abort_flag)) {
+        const int s = j % NS;
+        if (!mbar_wait_bounded(&empty[s], ((j / NS) & 1) ^ 1u, tmo, abort_flag)) {
           gemm_fail(abort_flag);
           break;
         }
-        uint8_t* st = sKV + s * C::STAGE_BYTES;
         const int k0 = (j0 + j) * ATT_BK;
-        mbar_arrive_expect_tx(&kv_full[s], C::STAGE_BYTES);
-        tma_load_2d(st, &tm_k, &kv_full[s], 0, g * args.Tp + k0, pol);
-        tma_load_2d(st + C::K_BYTES / 2, &tm_k, &kv_full[s], 64, g * args.Tp + k0, pol);
-        tma_load_2d(st + C::K_BYTES, &tm_vt, &kv_full[s], k0, g * ATT_D, pol);
-        tma_load_2d(st + C::K_BYTES + C::V_BYTES / 2, &tm_vt, &kv_full[s], k0 + 64, g * ATT_D, pol);
+        mbar_arrive_expect_tx(&full[s], C::K_BYTES);
+        if (lane == 0) {
+          uint8_t* st = sK + s * C::K_BYTES;
+          tma_load_2d(st, &tm_k, &full[s], 0, g * args.Tp + k0, pol);
+          tma_load_2d(st + C::K_BYTES / 2, &tm_k, &full[s], 64, g * args.Tp + k0, pol);
+        } else {
+          uint8_t* st = sV + s * C::V_BYTES;
+          tma_load_2d(st, &tm_vt, &full[s], k0, g * ATT_D, pol);
+          tma_load_2d(st + C::V_BYTES / 2, &tm_vt, &full[s], k0 + 64, g * ATT_D, pol);
+        }
         ++issued;
       }
       // every load must land before the CTA exits
-      const volatile int never = 0;
-      if (!mbar_wait_bounded(q_full, 0, tmo, &never)) gemm_fail(abort_flag);
-      for (int j = issued - 2; j < issued; ++j)
-        if (j >= 0 && !mbar_wait_bounded(&kv_full[j & 1], (j >> 1) & 1, tmo, &never))
-          gemm_fail(abort_flag);
+      if (lane == 0 && !mbar_wait_bounded(q_full, 0, tmo, &never)) gemm_fail(abort_flag);
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        if (!mbar_wait_bounded(&full[j % NS], (j / NS) & 1, tmo, &never)) gemm_fail(abort_flag);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -253,40 +278,43 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t dp = sdesc_k128(smem_u32(sP));
       const uint64_t dp1 = sdesc_k128(smem_u32(sP + C::P_BYTES / 2));
       auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!mbar_wait_bounded(&kv_full[s], (j >> 1) & 1, tmo, abort_flag)) return false;
+        const int ks = j % C::K_STAGES;
+        if (!mbar_wait_bounded(&k_full[ks], (j / C::K_STAGES) & 1, tmo, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t base = smem_u32(sKV + s * C::STAGE_BYTES);
+        const uint32_t base = smem_u32(sK + ks * C::K_BYTES);
         const uint64_t dk = sdesc_k128(base), dk1 = sdesc_k128(base + C::K_BYTES / 2);
-        const uint32_t dS = tmem_base + static_cast<uint32_t>(s * 128);
+        const uint32_t dS = tmem_base + static_cast<uint32_t>((j & 1) * 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dS, dq + 2 * kk, dk + 2 * kk, idesc, kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dS, dq1 + 2 * kk, dk1 + 2 * kk, idesc, 1u);
-        mma_commit(&s_full[s]);
+        mma_commit(&s_full[j & 1]);
+        mma_commit(&k_empty[ks]);
         return true;
       };
       if (ok && ntiles > 0) ok = issue_s(0);
+      if (ok && ntiles > 1) ok = issue_s(1);
       for (int j = 0; ok && j < ntiles; ++j) {
-        // S_{j+1} overlaps the softmax of tile j (its buffer was read by the
-        // softmax of tile j-1, which signalled p_full before this point)
-        if (j + 1 < ntiles && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait_bounded(p_full, j & 1, tmo, abort_flag)) {
+        const int vs = j % C::V_STAGES;
+        if (!mbar_wait_bounded(p_full, j & 1, tmo, abort_flag) ||
+            !mbar_wait_bounded(&v_full[vs], (j / C::V_STAGES) & 1, tmo, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t base = smem_u32(sKV + (j & 1) * C::STAGE_BYTES);
-        const uint64_t dv = sdesc_k128(base + C::K_BYTES), dv1 = sdesc_k128(base + C::K_BYTES + C::V_BYTES / 2);
+        const uint32_t base = smem_u32(sV + vs * C::V_BYTES);
+        const uint64_t dv = sdesc_k128(base), dv1 = sdesc_k128(base + C::V_BYTES / 2);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, dp + 2 * kk, dv + 2 * kk, idesc, (j | kk) != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, dp1 + 2 * kk, dv1 + 2 * kk, idesc, 1u);
         mma_commit(o_done);
-        mma_commit(&kv_empty[j & 1]);
+        mma_commit(&v_empty[vs]);
+        // S_{j+2} into the buffer the softmax of tile j has finished reading
+        if (j + 2 < ntiles && !issue_s(j + 2)) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) gemm_fail(abort_flag);
       mma_commit(mma_done);
@@ -302,8 +330,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lanebits = static_cast<uint32_t>(q * 32) << 16;
     const float NEG = -1e30f;
     float m = NEG, l = 0.f;
-    // softmax scale; global layers' query scale is already in q
-    const float sc = args.scale;
+    const float sc = args.scale;            // global layers' query scale is already in q
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j & 1;
@@ -317,27 +344,38 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int k0 = (j0 + j) * ATT_BK;
       float sv[ATT_BK];
+      tmem_ld128(tmem_base + lanebits + s * 128, sv);
+      // visible keys: kj <= qi, kj < T and (window) qi - kj < window, i.e.
+      // kj in [lo, hi]; reductions in eight independent partials (one warp per
+      // scheduler: long dependency chains would stall it)
+      const int hi = min(qi, args.T - 1);
+      const int lo = args.window > 0 ? qi - args.window + 1 : 0;
+      float mp[8];
 #pragma unroll
-      for (int c = 0; c < ATT_BK; c += 32) {
-        float a[16], b[16];
-        tmem_ld16x2(tmem_base + lanebits + s * 128 + c, tmem_base + lanebits + s * 128 + c + 16, a, b);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          sv[c + i] = a[i];
-          sv[c + 16 + i] = b[i];
-        }
-      }
-      float mt = NEG;
+      for (int i = 0; i < 8; ++i) mp[i] = NEG;
 #pragma unroll
       for (int c = 0; c < ATT_BK; ++c) {
         const int kj = k0 + c;
-        const bool vis = kj <= qi && kj < args.T && (args.window == 0 || qi - kj < args.window);
-        sv[c] = vis ? sv[c] * sc : -INFINITY;
-        mt = fmaxf(mt, sv[c]);
+        sv[c] = (kj >= lo && kj <= hi) ? sv[c] * sc : -INFINITY;
+        mp[c & 7] = fmaxf(mp[c & 7], sv[c]);
       }
-      const float mn = fmaxf(m, mt);
+      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      // lazy reference: move m only when this tile exceeds it by more than TAU
+      const float mn = mt > m + ATT_TAU ? mt : m;
       const float alpha = __expf(m - mn);
-      // the O row may be rescaled only after the previous P V has completed
+      float sp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sp[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < ATT_BK; ++c) {
+        sv[c] = __expf(sv[c] - mn);
+        sp[c & 7] += sv[c];
+      }
+      const float ps = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      l = l * alpha + ps;
+      m = mn;
+      // O may be rescaled and P overwritten only after the previous P V
       if (j > 0) {
         bool od = false;
         if (lane == 0) od = mbar_wait_bounded(o_done, (j - 1) & 1, tmo, abort_flag);
@@ -359,28 +397,20 @@ __global__ void __launch_bounds__(192, 1)
           tmem_wait_st();
         }
       }
-      float ps = 0.f;
       // P row, BF16, into the swizzled K-major tile: key c of row `row` sits
       // in 64-key block c/64, 16-byte chunk (c%64)/8 ^ (row%8)
 #pragma unroll
       for (int c8 = 0; c8 < ATT_BK / 8; ++c8) {
-        float p8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p8[i] = __expf(sv[c8 * 8 + i] - mn);
-          ps += p8[i];
-        }
         uint4 pk;
         __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p2[i] = __floats2bfloat162_rn(p8[2 * i], p8[2 * i + 1]);
+        for (int i = 0; i < 4; ++i)
+          p2[i] = __floats2bfloat162_rn(sv[c8 * 8 + 2 * i], sv[c8 * 8 + 2 * i + 1]);
         const int kb = c8 >> 3, chunk = c8 & 7;
         uint8_t* dst = sP + kb * (C::P_BYTES / 2) + (row >> 3) * 1024 + (row & 7) * 128 +
                        ((chunk ^ (row & 7)) << 4);
         *reinterpret_cast<uint4*>(dst) = pk;
       }
-      l = l * alpha + ps;
-      m = mn;
       // P (generic-proxy stores) and the O rescale visible to the MMA
       fence_proxy_async_smem();
       tc_fence_before();
@@ -407,11 +437,18 @@ __global__ void __launch_bounds__(192, 1)
         float o[16];
         tmem_ld16(tmem_base + lanebits + 256 + c, o);
         if (valid) {
+          float gt[16];
+          const float4* g4 = reinterpret_cast<const float4*>(gr + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 t4 = g4[i];
+            gt[4 * i] = t4.x; gt[4 * i + 1] = t4.y; gt[4 * i + 2] = t4.z; gt[4 * i + 3] = t4.w;
+          }
           uint4 pk[2];
           __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            p2[i] = __floats2bfloat162_rn(o[2 * i] * inv_l * gr[c + 2 * i], o[2 * i + 1] * inv_l * gr[c + 2 * i + 1]);
+            p2[i] = __floats2bfloat162_rn(o[2 * i] * inv_l * gt[2 * i], o[2 * i + 1] * inv_l * gt[2 * i + 1]);
           uint4* d4 = reinterpret_cast<uint4*>(orow + c);
           d4[0] = pk[0];
           d4[1] = pk[1];

@@ -1417,6 +1417,8 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
     beam::attn_prep_kernel<<<grid, 256, 0, st>>>(proj, T, L.Tp, nq, nkv, q_gain, k_gain,
                                                  p->rms_eps, p->window, p->rope_theta, q, k, vt,
                                                  gate);
+    beam::attn_vt_kernel<<<dim3((T + 31) / 32, (nkv + 3) / 4), 128, 0, st>>>(proj, T, L.Tp, nq,
+                                                                             nkv, vt);
   }
   BEAM_LAUNCH_CHECK("attn_prep_kernel");
   // 4. attention, gated, BF16

@@ -7,8 +7,9 @@
 // projection; section 残差流: RoPE and the query scaling in FP32). Head
 // dimension 128 ("config.json" of the release, head_dim).
 //
-//   attn_prep_kernel       QK-RMSNorm, RoPE or query scale, V transposed,
-//                          gate sigmoid, from the FP32 fused projection
+//   attn_prep_kernel       QK-RMSNorm, RoPE or query scale, gate sigmoid,
+//                          from the FP32 fused projection
+//   attn_vt_kernel         V transposed (keys contiguous)
 //   linear_units_kernel    work list of a dense GEMM on the 2-SM pair kernel
 //   flash_attn_kernel      softmax(Q K^T / sqrt(128) + mask) V per head on
 //                          tcgen05 (S and O accumulate in TMEM), times the gate
@@ -35,8 +36,8 @@ constexpr int ATT_BK = 128;      // keys per tile (S's N, P V's K)
 // weight [W_q; W_k; W_v; W_g]).
 //   q[h][t][:] = bf16(rope_or_scale(RMSNorm(q) * q_gain))   [nq][Tp][128]
 //   k[g][t][:] = bf16(rope(RMSNorm(k) * k_gain))            [nkv][Tp][128]
-//   vt[g][c][t] = bf16(v[t][g][c])                          [nkv][128][Tp]
 //   gate[t][h*128 + c] = sigmoid(.)  (FP32)                 [T][nq*128]
+// (value slots are written by attn_vt_kernel)
 // window > 0: RoPE (theta) on q and k; window == 0: q *= (1 + (t+1)/2048)^0.1.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) attn_prep_kernel(
@@ -59,13 +60,7 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(
     for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = 1.0f / (1.0f + expf(-v[i]));
     return;
   }
-  if (slot >= nq + nkv) {      // value: transposed, keys contiguous
-    const int g = slot - nq - nkv;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      vt[(static_cast<size_t>(g) * ATT_D + lane + 32 * i) * Tp + t] = __float2bfloat16_rn(v[i]);
-    return;
-  }
+  if (slot >= nq + nkv) return;  // values: attn_vt_kernel
   const bool is_q = slot < nq;
   // RMSNorm over the head's 128 channels (FP32), gain per channel
   float ss = 0.f;
@@ -98,6 +93,29 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(
                             : k + (static_cast<size_t>(slot - nq) * Tp + t) * ATT_D;
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = __float2bfloat16_rn(v[i]);
+}
+
+// V transposed, keys contiguous: vt[g][c][t] = bf16(v[t][g][c]). One lane
+// per token, a warp per 32 consecutive tokens of one key/value head, so the
+// stores of a channel row are 64 contiguous bytes.
+__global__ void __launch_bounds__(128) attn_vt_kernel(const float* __restrict__ proj, int T, int Tp,
+                                                      int nq, int nkv,
+                                                      __nv_bfloat16* __restrict__ vt) {
+  const int t = blockIdx.x * 32 + (threadIdx.x & 31);
+  const int g = blockIdx.y * 4 + (threadIdx.x >> 5);
+  if (g >= nkv || t >= T) return;
+  const int nslots = 2 * nq + 2 * nkv;
+  const float4* src = reinterpret_cast<const float4*>(
+      proj + static_cast<size_t>(t) * nslots * ATT_D + static_cast<size_t>(nq + nkv + g) * ATT_D);
+  __nv_bfloat16* dst = vt + static_cast<size_t>(g) * ATT_D * Tp + t;
+#pragma unroll 4
+  for (int c4 = 0; c4 < ATT_D / 4; ++c4) {
+    const float4 f = src[c4];
+    dst[static_cast<size_t>(4 * c4) * Tp] = __float2bfloat16_rn(f.x);
+    dst[static_cast<size_t>(4 * c4 + 1) * Tp] = __float2bfloat16_rn(f.y);
+    dst[static_cast<size_t>(4 * c4 + 2) * Tp] = __float2bfloat16_rn(f.z);
+    dst[static_cast<size_t>(4 * c4 + 3) * Tp] = __float2bfloat16_rn(f.w);
+  }
 }
 
 // Work list of one dense GEMM (one "expert" of n rows) on the 2-SM pair

@@ -1446,7 +1446,8 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
       attr_set = true;
     }
     ProfScope ps("flash_attn", st);
-    beam::flash_attn_kernel<<<dim3(L.Tp / beam::ATT_BQ, nq), 192, beam::AttnCfg::SMEM_BYTES, st>>>(
+    beam::flash_attn_kernel<<<dim3(L.Tp / beam::ATT_BQ, nq), beam::ATT_THREADS,
+                              beam::AttnCfg::SMEM_BYTES, st>>>(
         m_q, m_k, m_vt, aa);
   }
   BEAM_LAUNCH_CHECK("flash_attn_kernel");

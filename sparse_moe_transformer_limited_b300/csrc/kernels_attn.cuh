@@ -131,23 +131,30 @@ __global__ void linear_units_kernel(int n, int MT, int4* __restrict__ units, int
 
 // ---------------------------------------------------------------------------
 // Flash attention on tcgen05, one CTA per (query tile of 128 rows, query
-// head). Warp 0: TMA producer -- lane 0 loads Q once and then K tiles of 128
-// keys into a three-stage ring (a stage is freed as soon as its S has been
-// computed), lane 1 loads V^T tiles into a two-stage ring (freed after P V).
-// Warp 1: TMEM owner and MMA issuer: S_0 and S_1 up front into two TMEM S
-// buffers; then per tile j: O += P_j V_j as soon as P_j is ready, then
-// S_{j+2} into the buffer S_j leaves. Warps 2..5 (thread = query row = TMEM
-// lane): per tile read the S row, mask, online softmax in FP32 with a lazy
-// reference: the row maximum m moves (and the O row in TMEM is rescaled)
-// only when a tile's maximum exceeds m by more than ATT_TAU, so P <= e^TAU;
-// the exponentials are computed before waiting for the previous P V; P is
-// written as BF16 into the 128-byte-swizzled K-major tile the MMA reads. At
-// the end O / l times the gate, BF16, to `out`.
+// head), 10 warps. Warp 0: TMA producer -- lane 0 loads Q once and then K
+// tiles of 128 keys into a three-stage ring (a stage is freed as soon as its
+// S has been computed), lane 1 loads V^T tiles into a two-stage ring (freed
+// after P V). Warp 1: TMEM owner and MMA issuer: S_0 and S_1 up front into
+// two TMEM S buffers; then per tile j: S_{j+2} as soon as S_j has been read
+// out, O += P_j V_j as soon as P_j is written. Warps 2..9: two warps per
+// 32-row TMEM lane quarter, one for keys [0, 64) of the tile and one for keys
+// [64, 128) (and the matching halves of O); thread = (query row, half). Per
+// tile: read the half row of S, mask (boundary tiles only), row maximum over
+// both halves (exchanged through shared memory), online softmax in base 2
+// with a lazy reference: m moves (and the O row is rescaled) only when a
+// tile's maximum exceeds it by more than ATT_TAU2, so P <= 2^TAU2; P goes as
+// BF16 into the 128-byte-swizzled K-major tile the MMA reads. At the end
+// O / l times the gate, BF16, to `out`.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384).
 // All waits are bounded; on expiry the error word is set and every role
-// leaves after its in-flight copies and MMAs have completed.
+// leaves after its in-flight copies and MMAs have completed. The two warps of
+// a lane quarter meet at named barriers the same number of times whatever
+// happens (no early exit from the tile loop), so those barriers cannot hang.
 // ---------------------------------------------------------------------------
-constexpr float ATT_TAU = 8.0f;
+constexpr float ATT_TAU2 = 8.0f;        // lazy-rescale threshold, base-2 units
+constexpr float ATT_LOG2E = 1.4426950408889634f;
+constexpr int ATT_SOFTMAX_WARPS = 8;
+constexpr int ATT_THREADS = 32 * (2 + ATT_SOFTMAX_WARPS);
 
 struct AttnArgs {
   int T, Tp, nq, nkv, window;
@@ -163,9 +170,10 @@ struct AttnCfg {
   static constexpr int V_BYTES = ATT_D * ATT_BK * 2;     // 32 KB (V^T: 128 channels x 128 keys)
   static constexpr int P_BYTES = ATT_BQ * ATT_BK * 2;    // 32 KB
   static constexpr int K_STAGES = 3, V_STAGES = 2;
+  static constexpr int XCH_BYTES = 2 * ATT_BQ * 4;       // per (half, row): one float
   static constexpr int BAR_BYTES = 20 * 8 + 16;
-  static constexpr int SMEM_BYTES =
-      1024 + Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES + P_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES +
+                                    P_BYTES + XCH_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -178,7 +186,38 @@ __device__ __forceinline__ void attn_key_tiles(int qt, int T, int window, int* j
   *j1 = qlast / ATT_BK + 1;
 }
 
-__global__ void __launch_bounds__(192, 1)
+// Packed FP32 pair arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// 2^x (hardware approximation, flushes subnormal results)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __launch_bounds__(ATT_THREADS, 1)
     flash_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_vt, const AttnArgs args) {
   using C = AttnCfg;
@@ -189,17 +228,19 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sK = sQ + C::Q_BYTES;
   uint8_t* sV = sK + C::K_STAGES * C::K_BYTES;
   uint8_t* sP = sV + C::V_STAGES * C::V_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + C::P_BYTES);
+  float* xch = reinterpret_cast<float*>(sP + C::P_BYTES);   // [2 halves][128 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + C::P_BYTES + C::XCH_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;        // [3]
   uint64_t* k_empty = bars + 4;       // [3]
   uint64_t* v_full = bars + 7;        // [2]
   uint64_t* v_empty = bars + 9;       // [2]
   uint64_t* s_full = bars + 11;       // [2]
-  uint64_t* p_full = bars + 13;
-  uint64_t* o_done = bars + 14;
-  uint64_t* mma_done = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* s_free = bars + 13;       // [2]
+  uint64_t* p_full = bars + 15;
+  uint64_t* o_done = bars + 16;
+  uint64_t* mma_done = bars + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -222,9 +263,11 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], ATT_SOFTMAX_WARPS);
+    }
+    mbar_init(p_full, ATT_SOFTMAX_WARPS);
     mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -313,6 +356,18 @@ __global__ void __launch_bounds__(192, 1)
       if (ok && ntiles > 0) ok = issue_s(0);
       if (ok && ntiles > 1) ok = issue_s(1);
       for (int j = 0; ok && j < ntiles; ++j) {
+        // S_{j+2} into the buffer S_j leaves, as soon as S_j has been read out
+        if (j + 2 < ntiles) {
+          if (!mbar_wait_bounded(&s_free[j & 1], (j >> 1) & 1, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!issue_s(j + 2)) {
+            ok = false;
+            break;
+          }
+        }
         const int vs = j % C::V_STAGES;
         if (!mbar_wait_bounded(p_full, j & 1, tmo, abort_flag) ||
             !mbar_wait_bounded(&v_full[vs], (j / C::V_STAGES) & 1, tmo, abort_flag)) {
@@ -328,11 +383,6 @@ __global__ void __launch_bounds__(192, 1)
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, dp1 + 2 * kk, dv1 + 2 * kk, idesc, 1u);
         mma_commit(o_done);
         mma_commit(&v_empty[vs]);
-        // S_{j+2} into the buffer the softmax of tile j has finished reading
-        if (j + 2 < ntiles && !issue_s(j + 2)) {
-          ok = false;
-          break;
-        }
       }
       if (!ok) gemm_fail(abort_flag);
       mma_commit(mma_done);
@@ -343,91 +393,113 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int q = warp & 3;                 // TMEM lane quarter
+    const int half = (warp - 2) >> 2;       // keys / O columns [64 half, 64 half + 64)
     const int row = q * 32 + lane;          // query row within the tile
     const int qi = qt * ATT_BQ + row;       // query index
     const uint32_t lanebits = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half * 64);
+    const int bar_id = 1 + q;               // named barrier of this lane quarter's two warps
     const float NEG = -1e30f;
-    float m = NEG, l = 0.f;
-    const float sc = args.scale;            // global layers' query scale is already in q
+    float m = NEG, l = 0.f;                 // base-2 units; l over this half's keys
+    // global layers' query scale is already in q; logits to base 2 in one FMA
+    const float c2 = args.scale * ATT_LOG2E;
+    const uint64_t cc = f2_pack(c2, c2);
+    const int hi = min(qi, args.T - 1);     // visible keys of row qi: [lo, hi]
+    const int lo = args.window > 0 ? qi - args.window + 1 : 0;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j & 1;
-      bool ready = false;
-      if (lane == 0) ready = mbar_wait_bounded(&s_full[s], (j >> 1) & 1, tmo, abort_flag);
-      ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-      if (!ready) {
-        ok = false;
-        break;
+      if (ok) {
+        bool ready = false;
+        if (lane == 0) ready = mbar_wait_bounded(&s_full[s], (j >> 1) & 1, tmo, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
       }
-      tc_fence_after();
-      const int k0 = (j0 + j) * ATT_BK;
-      float sv[ATT_BK];
-      tmem_ld128(tmem_base + lanebits + s * 128, sv);
-      // visible keys: kj <= qi, kj < T and (window) qi - kj < window, i.e.
-      // kj in [lo, hi]; reductions in eight independent partials (one warp per
-      // scheduler: long dependency chains would stall it)
-      const int hi = min(qi, args.T - 1);
-      const int lo = args.window > 0 ? qi - args.window + 1 : 0;
-      float mp[8];
+      float sv[64];
+      float mt = -INFINITY;
+      if (ok) {
+        tc_fence_after();
+        tmem_ld64(tmem_base + lanebits + s * 128 + col0, sv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[s]);
+        const int k0 = (j0 + j) * ATT_BK + half * 64;
+        if (__any_sync(0xffffffffu, k0 < lo || k0 + 63 > hi)) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mp[i] = NEG;
+          for (int c = 0; c < 64; ++c) {
+            const int kj = k0 + c;
+            sv[c] = (kj >= lo && kj <= hi) ? sv[c] : -INFINITY;
+          }
+        }
+        // raw maximum in eight independent partials (one warp per scheduler
+        // pair: long dependency chains would stall it)
+        float mp[8];
 #pragma unroll
-      for (int c = 0; c < ATT_BK; ++c) {
-        const int kj = k0 + c;
-        sv[c] = (kj >= lo && kj <= hi) ? sv[c] * sc : -INFINITY;
-        mp[c & 7] = fmaxf(mp[c & 7], sv[c]);
+        for (int i = 0; i < 8; ++i) mp[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
+#pragma unroll
+        for (int c = 24; c < 64; c += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mp[i] = fmax3(mp[i], sv[c + i], sv[c + 8 + i]);
+        }
+        mt = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * c2;
       }
-      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      // lazy reference: move m only when this tile exceeds it by more than TAU
-      const float mn = mt > m + ATT_TAU ? mt : m;
-      const float alpha = __expf(m - mn);
-      float sp[8];
+      // tile maximum over both halves of the row (-inf from a failed half)
+      xch[half * ATT_BQ + row] = mt;
+      named_bar_sync(bar_id, 64);
+      mt = fmaxf(mt, xch[(half ^ 1) * ATT_BQ + row]);
+      named_bar_sync(bar_id, 64);
+      if (!ok) continue;
+      // lazy reference: move m only when this tile exceeds it by more than TAU2
+      const float mn = mt > m + ATT_TAU2 ? mt : m;
+      const float alpha = ex2_approx(m - mn);
+      const uint64_t nm = f2_pack(-mn, -mn);
+      uint64_t sp[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sp[i] = 0.f;
-#pragma unroll
-      for (int c = 0; c < ATT_BK; ++c) {
-        sv[c] = __expf(sv[c] - mn);
-        sp[c & 7] += sv[c];
+      for (int c = 0; c < 64; c += 2) {
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), cc, nm), a, b);
+        sv[c] = ex2_approx(a);
+        sv[c + 1] = ex2_approx(b);
+        sp[(c >> 1) & 3] = f2_add(sp[(c >> 1) & 3], f2_pack(sv[c], sv[c + 1]));
       }
-      const float ps = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      float ps = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a, b;
+        f2_unpack(sp[i], a, b);
+        ps += a + b;
+      }
       l = l * alpha + ps;
       m = mn;
       // O may be rescaled and P overwritten only after the previous P V
       if (j > 0) {
         bool od = false;
         if (lane == 0) od = mbar_wait_bounded(o_done, (j - 1) & 1, tmo, abort_flag);
-        od = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
-        if (!od) {
-          ok = false;
-          break;
-        }
+        ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
+        if (!ok) continue;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < ATT_D; c += 16) {
+          for (int c = 0; c < 64; c += 16) {
             float o[16];
-            tmem_ld16(tmem_base + lanebits + 256 + c, o);
+            tmem_ld16(tmem_base + lanebits + 256 + col0 + c, o);
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tmem_st16(tmem_base + lanebits + 256 + c, o);
+            tmem_st16(tmem_base + lanebits + 256 + col0 + c, o);
           }
           tmem_wait_st();
         }
       }
-      // P row, BF16, into the swizzled K-major tile: key c of row `row` sits
-      // in 64-key block c/64, 16-byte chunk (c%64)/8 ^ (row%8)
+      // P half row, BF16, into the swizzled K-major tile: key c of row `row`
+      // sits in 64-key block c/64, 16-byte chunk (c%64)/8 ^ (row%8)
+      uint8_t* prow = sP + half * (C::P_BYTES / 2) + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < ATT_BK / 8; ++c8) {
+      for (int chunk = 0; chunk < 8; ++chunk) {
         uint4 pk;
         __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          p2[i] = __floats2bfloat162_rn(sv[c8 * 8 + 2 * i], sv[c8 * 8 + 2 * i + 1]);
-        const int kb = c8 >> 3, chunk = c8 & 7;
-        uint8_t* dst = sP + kb * (C::P_BYTES / 2) + (row >> 3) * 1024 + (row & 7) * 128 +
-                       ((chunk ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = pk;
+          p2[i] = __floats2bfloat162_rn(sv[chunk * 8 + 2 * i], sv[chunk * 8 + 2 * i + 1]);
+        *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = pk;
       }
       // P (generic-proxy stores) and the O rescale visible to the MMA
       fence_proxy_async_smem();
@@ -435,25 +507,28 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // final: O / l times the gate, BF16
-    bool od = ok;
+    // final: O / l times the gate, BF16; l summed over both halves
     if (ok && ntiles > 0) {
+      bool od = false;
       if (lane == 0) od = mbar_wait_bounded(o_done, (ntiles - 1) & 1, tmo, abort_flag);
-      od = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
+      ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
     }
-    if (!od) {
+    xch[half * ATT_BQ + row] = l;
+    named_bar_sync(bar_id, 64);
+    const float lt = l + xch[(half ^ 1) * ATT_BQ + row];
+    if (!ok) {
       if (lane == 0) gemm_fail(abort_flag);
     } else {
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
       const bool valid = qi < args.T;
       const size_t ld = static_cast<size_t>(args.nq) * ATT_D;
-      const float* gr = args.gate + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D;
-      __nv_bfloat16* orow = args.out + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D;
+      const float* gr = args.gate + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
+      __nv_bfloat16* orow = args.out + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
 #pragma unroll 1
-      for (int c = 0; c < ATT_D; c += 16) {
+      for (int c = 0; c < 64; c += 16) {
         float o[16];
-        tmem_ld16(tmem_base + lanebits + 256 + c, o);
+        tmem_ld16(tmem_base + lanebits + 256 + col0 + c, o);
         if (valid) {
           float gt[16];
           const float4* g4 = reinterpret_cast<const float4*>(gr + c);

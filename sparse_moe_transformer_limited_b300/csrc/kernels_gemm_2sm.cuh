@@ -76,9 +76,6 @@ struct PairCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 // Named barrier that also ANDs a predicate over its participants.
 __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
   uint32_t r;

@@ -117,8 +117,12 @@ enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2, PATH_PAIR = 3, PATH_MI
 GemmPath choose_path(const beam_moe_params& p) {
   const long long pairs = static_cast<long long>(p.T) * p.top_k;
   if (pairs <= 24LL * p.E) return PATH_W32;
-  // NVFP4 runs on the weight-major kernels (128-token tiles when many tokens)
-  if (p.flags & BEAM_FLAG_NVFP4_EXPERTS) return PATH_W128;
+  // NVFP4 with many tokens: both GEMMs on the token-major kernel
+  if (p.flags & BEAM_FLAG_NVFP4_EXPERTS) {
+    const char* v = std::getenv("BEAM_PREFILL_GEMM");
+    if (p.H % 256 == 0 && !(v != nullptr && std::strcmp(v, "w128") == 0)) return PATH_TM;
+    return PATH_W128;
+  }
   if (p.H % 256 == 0) {
     const char* v = std::getenv("BEAM_PREFILL_GEMM");
     if (v != nullptr && std::strcmp(v, "tm") == 0) return PATH_TM;
@@ -381,11 +385,11 @@ beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, con
   return BEAM_OK;
 }
 
-template <int MODE, bool F8>
+template <int MODE, int KIND>
 beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& tok,
                              const beam::TmArgs& args, cudaStream_t st) {
-  using C = beam::TmCfg;
-  auto kern = beam::expert_gemm_tm_kernel<MODE, F8>;
+  using C = beam::TmCfg<KIND>;
+  auto kern = beam::expert_gemm_tm_kernel<MODE, KIND>;
   static bool attr_set = false;
   if (!attr_set) {
     BEAM_CUDA_TRY(
@@ -394,7 +398,7 @@ beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const
   }
   const int grid = (sm_count() / 2) * 2;
   ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(w0, w1, tok, args);
+  kern<<<grid, beam::TM_THREADS, C::SMEM_BYTES, st>>>(w0, w1, tok, args);
   BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_tm_kernel<gate/up>" : "expert_gemm_tm_kernel<down>");
   return BEAM_OK;
 }
@@ -515,8 +519,8 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
   beam_status_t s = BEAM_OK;
   const int H = prm.H, E = prm.E, I = prm.I;
   const int KB = beam::KBlock<KIND>::ELEMS;
-  if (F4 && L.path != PATH_W32 && L.path != PATH_W128)
-    return fail(BEAM_ERR_UNSUPPORTED, "NVFP4 experts run on the weight-major GEMM kernels only");
+  if (F4 && L.path != PATH_W32 && L.path != PATH_W128 && L.path != PATH_TM)
+    return fail(BEAM_ERR_UNSUPPORTED, "NVFP4 experts run on the weight-major or token-major kernels");
   const bool bytes = F8 || F4;     // TMA maps over one-byte elements (codes)
   const int hc = F4 ? H / 2 : H;   // row length of the code matrices, in map elements
   const int ic = F4 ? I / 2 : I;
@@ -588,7 +592,8 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
       ta.row_scale = q.xscale;
       ta.w_scale0 = w.s_gate;
       ta.w_scale1 = w.s_up;
-      if ((s = launch_gemm_tm<0, F8>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK) return s;
+      if ((s = launch_gemm_tm<0, F8 ? beam::KIND_E4M3 : beam::KIND_BF16>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK)
+        return s;
     } else {
       if ((s = launch_gemm_pair<0, F8>(m_g, m_u, m_x, m_x64, pa, st)) != BEAM_OK) return s;
     }
@@ -606,6 +611,9 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     ta.row_scale = q.xscale;
     ta.w_scale0 = w.s_gate;
     ta.w_scale1 = w.s_up;
+    ta.a_sf = q.xsf;
+    ta.w_sf0 = static_cast<const uint8_t*>(w.sf_gate);
+    ta.w_sf1 = static_cast<const uint8_t*>(w.sf_up);
     beam::TmArgs td = ta;
     td.units = udn;
     td.n_units = nunits + 1;
@@ -617,9 +625,12 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     td.row_scale = nullptr;  // the activation row scales are applied by the combine
     td.w_scale0 = w.s_down;
     td.w_scale1 = nullptr;
-    if ((s = launch_gemm_tm<0, F8>(m_g, m_u, m_x, ta, st)) != BEAM_OK) return s;
+    td.a_sf = q.asf;
+    td.w_sf0 = static_cast<const uint8_t*>(w.sf_down);
+    td.w_sf1 = nullptr;
+    if ((s = launch_gemm_tm<0, KIND>(m_g, m_u, m_x, ta, st)) != BEAM_OK) return s;
     if ((s = quant_act()) != BEAM_OK) return s;
-    if ((s = launch_gemm_tm<1, F8>(m_d, m_d, m_a, td, st)) != BEAM_OK) return s;
+    if ((s = launch_gemm_tm<1, KIND>(m_d, m_d, m_a, td, st)) != BEAM_OK) return s;
   } else {
     beam::GemmArgs ga{};
     ga.units = ugu;  // token tiles, shared by both GEMMs
@@ -730,7 +741,7 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     else if (L.path == PATH_TM)
       beam::expert_scan_units_prefill_kernel<beam::LIST_TM, beam::LIST_TM>
           <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
-                              H / 256);
+                              H / 256, L.pad, row_tok);
     else
       beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs,
                                                         ugu, nunits, L.NT, I / 128,

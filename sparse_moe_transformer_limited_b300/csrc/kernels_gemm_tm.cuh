@@ -22,8 +22,17 @@
 //            epilogue y[row, 256n + j] = D[row, j] (FP32) -- the per-pair
 //            expert output, combined per token by the row kernel.
 //
+// NVFP4 (E2M1 codes with E4M3 scales per 16 elements, "NVFP4 版" section):
+// a K-block is 256 elements (128 bytes per row); each stage also carries the
+// K-block's scale groups -- four 512-byte groups of the 128-row token tile
+// and eight of the two 128-row weight halves -- which the MMA thread copies
+// into the stage's own TMEM columns (tcgen05.cp) before the block-scaled
+// MMAs. TMEM then holds one accumulator (256 columns) and the scale columns
+// of every stage (48 each), so the epilogue does not overlap the next unit.
+//
 // Warp roles as in the weight-major kernel: warp 0 TMA producer, warp 1 TMEM
-// owner and MMA issuer, warps 2..5 epilogue (TMEM lane quarter = warp % 4).
+// owner and MMA issuer, warps 2..9 epilogue: two warps per TMEM lane quarter
+// (warp % 4), one per half of the accumulator's columns.
 // A shared-memory stage may be refilled only when the MMAs of BOTH CTAs have
 // consumed it (the peer's multicast writes into this CTA's stage too), so each
 // MMA commit arrives on the `empty` barrier of both CTAs (count 2). All waits
@@ -44,7 +53,7 @@ namespace beam {
 struct TmArgs {
   const int4* units;        // 2 per cluster unit: {expert, first row, rows, tile | TM_PAIR}
   const int* n_units;
-  int k_blocks;             // 128-byte K-blocks: K / 64 (BF16) or K / 128 (E4M3)
+  int k_blocks;             // 128-byte K-blocks: K / 64 (BF16), K / 128 (E4M3), K / 256 (NVFP4)
   int w_rows_per_expert;    // I (gate/up) or H (down)
   __nv_bfloat16* out;       // MODE 0: act [R, I] bf16
   float* y;                 // MODE 1: y [R, H] fp32
@@ -56,32 +65,54 @@ struct TmArgs {
   const float* row_scale;
   const float* w_scale0;
   const float* w_scale1;
+  // NVFP4: the same roles with one group scale per expert for the weights
+  // (w_scale0/1 indexed by expert) and per token row (row_scale), plus the
+  // 512-byte block-scale groups: token tiles of 128 rows (a_sf) and weight
+  // tiles of 128 rows (w_sf0: gate or down, w_sf1: up), group (tile, K = 64
+  // step) at byte (tile * K / 64 + step) * 512
+  const uint8_t* a_sf;
+  const uint8_t* w_sf0;
+  const uint8_t* w_sf1;
 };
 
+template <int KIND>
 struct TmCfg {
+  static constexpr bool F4 = KIND == KIND_NVFP4;
   static constexpr int BM = 128;                 // token rows per CTA
   static constexpr int BN = 256;                 // weight rows per unit
   static constexpr int STAGES = 4;
   static constexpr int A_BYTES = BM * 128;       // 16 KB
   static constexpr int B_BYTES = BN * 128;       // 32 KB
   static constexpr int HALF_B = B_BYTES / 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SF_A_BYTES = F4 ? 4 * 512 : 0;        // [K step][512]
+  static constexpr int SF_B_BYTES = F4 ? 2 * 4 * 512 : 0;    // [weight half][K step][512]
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_A_BYTES + SF_B_BYTES;
   static constexpr int ACC_COLS = BN;
-  static constexpr int NBUF = 2;
+  static constexpr int NBUF = F4 ? 1 : 2;
+  // per stage: A scales 4 columns per K step, B scales 8 (8-aligned)
+  static constexpr int SF_COLS = F4 ? 48 : 0;
+  static constexpr int SF_B_COL = 16;
+  static constexpr int SF_TMEM_BASE = NBUF * ACC_COLS;
   static constexpr int TMEM_COLS = 512;
+  static_assert(NBUF * ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "TMEM");
   static constexpr int BAR_BYTES = (2 * STAGES + 2 * NBUF + 1) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// F8: E4M3 operands (K-blocks of 128 elements, kind::f8f6f4) with the scales
-// applied in the epilogue; else BF16 (K-blocks of 64).
-template <int MODE, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+// KIND_E4M3: E4M3 operands (K-blocks of 128 elements, kind::f8f6f4) with the
+// scales applied in the epilogue; KIND_NVFP4: block-scaled E2M1 (K-blocks of
+// 256, kind::mxf4nvf4) with the group scales in the epilogue; else BF16.
+constexpr int TM_THREADS = 320;
+
+template <int MODE, int KIND>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
     expert_gemm_tm_kernel(const __grid_constant__ CUtensorMap tm_w0,
                           const __grid_constant__ CUtensorMap tm_w1,
                           const __grid_constant__ CUtensorMap tm_tok, const TmArgs args) {
-  using C = TmCfg;
+  using C = TmCfg<KIND>;
+  constexpr bool F8 = KIND == KIND_E4M3;
+  constexpr bool F4 = KIND == KIND_NVFP4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -106,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
     for (int b = 0; b < C::NBUF; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], 8);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -153,7 +184,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           }
           uint8_t* sb = smem + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          const int kx = kb * KBlock<F8>::ELEMS;
+          // inner TMA coordinate in map elements: bf16 / e4m3 / bytes of e2m1 pairs
+          const int kx = kb * (F4 ? 128 : KBlock<KIND>::ELEMS);
           tma_load_2d(sb, &tm_tok, &full[stage], kx, un.y, pol_x);
           if (pair) {
             if (crank == 0)
@@ -165,6 +197,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           } else {
             tma_load_2d(sb + C::A_BYTES, &tm_w0, &full[stage], kx, wr0, pol_w);
             tma_load_2d(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kx, wr1, pol_w);
+          }
+          if (F4) {
+            // this K-block's scale groups: token tile un.y / 128, weight tiles
+            // of the two halves (each CTA loads all of them itself)
+            const size_t ksteps = static_cast<size_t>(args.k_blocks) * 4;
+            uint8_t* sf = sb + C::A_BYTES + C::B_BYTES;
+            const uint8_t* srca = args.a_sf + ((static_cast<size_t>(un.y) >> 7) * ksteps + 4 * kb) * 512;
+            const uint8_t* srcb0 = args.w_sf0 + ((static_cast<size_t>(wr0) >> 7) * ksteps + 4 * kb) * 512;
+            const uint8_t* srcb1 = (MODE == 0 ? args.w_sf1 : args.w_sf0) +
+                                   ((static_cast<size_t>(wr1) >> 7) * ksteps + 4 * kb) * 512;
+            if (((reinterpret_cast<uintptr_t>(srca) | reinterpret_cast<uintptr_t>(srcb0) |
+                  reinterpret_cast<uintptr_t>(srcb1)) & 15) != 0 || (un.y & 127) != 0) {
+              // never issue a misaligned copy: flag it; the stage's wait then times out
+              atomicOr(&g_beam_err, DEV_ERR_ALIGN);
+            } else {
+              bulk_load(sf, srca, 2048, &full[stage], pol_x);
+              bulk_load(sf + C::SF_A_BYTES, srcb0, 2048, &full[stage], pol_w);
+              bulk_load(sf + C::SF_A_BYTES + 2048, srcb1, 2048, &full[stage], pol_w);
+            }
           }
           ++issued;
           if (++stage == C::STAGES) {
@@ -189,14 +240,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f32acc<F8>(128, C::BN);
+      const uint32_t idesc = F4 ? idesc_nvf4(128, C::BN) : idesc_f32acc<F8>(128, C::BN);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
       for (int u = cid; ok && u < n_units; u += ncl, ++it) {
-        const int buf = it & 1;
-        const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
+        const int buf = (C::NBUF == 1) ? 0 : (it & 1);
+        const uint32_t tpar = static_cast<uint32_t>((C::NBUF == 1) ? it : (it >> 1)) & 1u;
         if (!mbar_wait_bounded(&tempty[buf], tpar ^ 1u, tmo, abort_flag)) {
           gemm_fail(abort_flag);
           break;
@@ -213,9 +264,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint64_t da = sdesc_k128(sa);
           const uint64_t db = sdesc_k128(sa + C::A_BYTES);
+          if (F4) {
+            // scales into this stage's TMEM columns, then the four K = 64 MMAs
+            // (tcgen05 operations of one thread execute in issue order; a
+            // stage's columns are rewritten only after its MMAs completed,
+            // which the refill of the stage implies)
+            const uint32_t slot = tmem_base + static_cast<uint32_t>(C::SF_TMEM_BASE + stage * C::SF_COLS);
+            const uint32_t sf = sa + C::A_BYTES + C::B_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss<F8>(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              tmem_cp_sf512(slot + 4 * kk, sdesc_sf512(sf + kk * 512));
+              tmem_cp_sf512(slot + C::SF_B_COL + 8 * kk, sdesc_sf512(sf + C::SF_A_BYTES + kk * 512));
+              tmem_cp_sf512(slot + C::SF_B_COL + 8 * kk + 4,
+                            sdesc_sf512(sf + C::SF_A_BYTES + 2048 + kk * 512));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_nvf4_ss(d0, da + 2 * kk, db + 2 * kk, idesc, slot + 4 * kk,
+                          slot + C::SF_B_COL + 8 * kk, (kb | kk) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss<F8>(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
           mma_commit_mc(&empty[stage], static_cast<uint16_t>(0x3));
           if (++stage == C::STAGES) {
             stage = 0;
@@ -233,13 +304,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;   // accumulator columns of this warp
     const int rloc = q * 32 + lane;
     int it = 0;
     for (int u = cid; u < n_units; u += ncl, ++it) {
       const int4 un = args.units[2 * u + crank];
       const int nt = un.w & 0xFFFF;
-      const int buf = it & 1;
-      const uint32_t tpar = static_cast<uint32_t>(it >> 1) & 1u;
+      const int buf = (C::NBUF == 1) ? 0 : (it & 1);
+      const uint32_t tpar = static_cast<uint32_t>((C::NBUF == 1) ? it : (it >> 1)) & 1u;
       bool ready = false;
       if (lane == 0) ready = mbar_wait_bounded(&tfull[buf], tpar, tmo, abort_flag);
       ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
@@ -252,14 +324,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                           (static_cast<uint32_t>(q * 32) << 16);
       const bool valid = rloc < un.z;
       const size_t row = static_cast<size_t>(un.y) + rloc;
-      const float sx = (F8 && MODE == 0 && valid) ? args.row_scale[row] : 1.f;
+      const float sx = ((F8 || F4) && MODE == 0 && valid) ? args.row_scale[row] : 1.f;
+      // NVFP4: one group scale per expert and weight matrix
+      const float es0 = F4 ? args.w_scale0[un.x] : 1.f;
+      const float es1 = (F4 && MODE == 0) ? args.w_scale1[un.x] : 1.f;
+      // The warp's whole accumulator slice (128 columns) into registers, then
+      // the accumulator is released at once: the next unit's MMAs overlap the
+      // math and the stores below.
+      float acc[128];
       if (MODE == 0) {
-        __nv_bfloat16* dst = args.out + row * args.out_ld + nt * 128;
-        const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 128;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          float g[16], v[16];
-          tmem_ld16x2(tb + c * 16, tb + 128 + c * 16, g, v);
+        float* g = acc;
+        float* v = acc + 64;
+        tmem_ld64(tb + 64 * half, *reinterpret_cast<float(*)[64]>(g));
+        tmem_ld64(tb + 128 + 64 * half, *reinterpret_cast<float(*)[64]>(v));
+      } else {
+        tmem_ld128(tb + 128 * half, acc);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (MODE == 0) {
+        // gate columns 64 half + [0, 64) in acc[0..63], up in acc[64..127]
+        __nv_bfloat16* dst = args.out + row * args.out_ld + nt * 128 + 64 * half;
+        const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 128 + 64 * half;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float* g = acc + c * 16;
+          float* v = acc + 64 + c * 16;
           if (F8) {
             // weight-row scales of these 16 columns (the same for every lane)
             const float4* sg4 = reinterpret_cast<const float4*>(args.w_scale0 + wi0 + c * 16);
@@ -269,6 +360,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
               const float4 a = __ldg(sg4 + j), b = __ldg(su4 + j);
               g[4 * j] *= a.x * sx; g[4 * j + 1] *= a.y * sx; g[4 * j + 2] *= a.z * sx; g[4 * j + 3] *= a.w * sx;
               v[4 * j] *= b.x * sx; v[4 * j + 1] *= b.y * sx; v[4 * j + 2] *= b.z * sx; v[4 * j + 3] *= b.w * sx;
+            }
+          }
+          if (F4) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              g[j] *= es0 * sx;
+              v[j] *= es1 * sx;
             }
           }
           if (valid) {
@@ -287,12 +385,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           }
         }
       } else {
-        float* dst = args.y + row * args.out_ld + nt * 256;
-        const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 256;
-#pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
-          float d[16];
-          tmem_ld16(tb + c * 16, d);
+        float* dst = args.y + row * args.out_ld + nt * 256 + 128 * half;
+        const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 256 + 128 * half;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float* d = acc + c * 16;
           if (F8) {
             const float4* sd4 = reinterpret_cast<const float4*>(args.w_scale0 + wi0 + c * 16);
 #pragma unroll
@@ -300,6 +397,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
               const float4 a = __ldg(sd4 + j);
               d[4 * j] *= a.x; d[4 * j + 1] *= a.y; d[4 * j + 2] *= a.z; d[4 * j + 3] *= a.w;
             }
+          }
+          if (F4) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) d[j] *= es0;
           }
           if (valid) {
             float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
@@ -309,9 +410,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
     }
   }
 

@@ -235,20 +235,28 @@ template <int GU_KIND, int DN_KIND>
 __global__ void __launch_bounds__(256) expert_scan_units_prefill_kernel(
     const int* __restrict__ blk_hist, int NB, int E, int* __restrict__ blk_off,
     int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ units_gu,
-    int4* __restrict__ units_dn, int* __restrict__ n_units, int MT_gu, int MT_dn) {
+    int4* __restrict__ units_dn, int* __restrict__ n_units, int MT_gu, int MT_dn, int pad = 1,
+    int* __restrict__ row_token = nullptr) {
   __shared__ int s_cnt[256];
+  __shared__ int s_pad[256];
   __shared__ int s_order[256];
   __shared__ int s_warp[8];
   const int e = threadIdx.x;
   const int c = e < E ? hist_total(blk_hist, NB, E, e) : 0;
   s_cnt[e] = (e < E) ? c : 0;
+  // pad > 1: every expert's rows start at a multiple of pad; the padding rows
+  // get row_token = -1
+  const int cpad = (c + pad - 1) / pad * pad;
+  s_pad[e] = (e < E) ? cpad : 0;
   int total = 0;
-  const int off = block_exclusive_scan256(e < E ? c : 0, s_warp, &total);
+  const int off = block_exclusive_scan256(e < E ? cpad : 0, s_warp, &total);
   if (e < E) {
     counts[e] = c;
     offsets[e] = off;
     if (e == 0) offsets[E] = total;
     hist_offsets(blk_hist, NB, E, e, off, blk_off);
+    if (pad > 1)
+      for (int r = off + c; r < off + cpad; ++r) row_token[r] = -1;
     int rank = 0;
     for (int j = 0; j < E; ++j) rank += (s_cnt[j] > c) || (s_cnt[j] == c && j < e);
     s_order[rank] = e;
@@ -257,7 +265,7 @@ __global__ void __launch_bounds__(256) expert_scan_units_prefill_kernel(
   const int ex = e < E ? s_order[e] : 0;
   const int n = e < E ? s_cnt[ex] : 0;
   int r0 = 0;
-  for (int j = 0; j < ex; ++j) r0 += s_cnt[j];
+  for (int j = 0; j < ex; ++j) r0 += s_pad[j];
   int tot_gu = 0, tot_dn = 0;
   const int b_gu = block_exclusive_scan256(n > 0 ? list_units_for<GU_KIND>(n, MT_gu) : 0, s_warp,
                                            &tot_gu);

@@ -144,11 +144,31 @@ def test_nvfp4_forward_routing_edge_cases(B, mode):
     _layer_check(B, wl, d)
 
 
+@pytest.fixture(params=["tm", "w128"])
+def nvfp4_prefill_gemm(request, monkeypatch):
+    """Many tokens per expert: the token-major two-CTA kernel (default) or,
+    with BEAM_PREFILL_GEMM=w128, the weight-major kernel with 128-token tiles."""
+    if request.param == "tm":
+        monkeypatch.delenv("BEAM_PREFILL_GEMM", raising=False)
+    else:
+        monkeypatch.setenv("BEAM_PREFILL_GEMM", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("T,H,I", [(700, 256, 256), (1100, 512, 256), (1537, 768, 512)])
-def test_nvfp4_forward_128_token_tiles(B, T, H, I):
-    """Many tokens per expert: 128-token tiles, expert rows padded to 128."""
+def test_nvfp4_forward_128_token_tiles(B, T, H, I, nvfp4_prefill_gemm):
+    """Many tokens per expert: expert rows padded to 128, 128-row token tiles."""
     wl, d = S.make_custom(T=T, H=H, E=32, I=I, n_group=1, topk_group=1, top_k=8,
                           seed=T + 3, device="cuda")
+    _layer_check(B, wl, d)
+
+
+@pytest.mark.parametrize("mode", ["hot_expert", "hot_group"])
+def test_nvfp4_prefill_routing_edge_cases(B, mode, nvfp4_prefill_gemm):
+    """Token-major tiles under skewed routing: one expert with most rows
+    (many 256-row groups and a tail) and experts with a handful of rows."""
+    wl, d = S.make_custom(T=1200, H=256, E=32, I=256, n_group=1, topk_group=1, top_k=8,
+                          seed=57, device="cuda", router_mode=mode)
     _layer_check(B, wl, d)
 
 

@@ -623,6 +623,12 @@ def main():
                     "roofline": rr["roofline"], "layer": rr["layer"],
                     "kernels_ms": rr["kernels_ms"], "clocks": rr["clocks"]}
         extra = {"dense_mlp_T8192": extra_dense, "prefill_T8192": summary(r2)}
+        # the skewed-routing and long-prefill-with-residual workloads
+        for cfg, key in (("skew", "skew_T4096"), ("long_prefill", "long_prefill_T16384")):
+            a4 = argparse.Namespace(**vars(args))
+            a4.config = cfg
+            torch.cuda.empty_cache()
+            extra[key] = summary(run_ours(a4, rank, world, local_rank))
         for an in ("attn_swa", "attn_global"):
             torch.cuda.empty_cache()
             extra[f"attention_{an[5:]}_T8192"] = run_attn(a2, rank, world, local_rank, an)

@@ -133,19 +133,22 @@ __global__ void linear_units_kernel(int n, int MT, int4* __restrict__ units, int
 // Flash attention on tcgen05, one CTA per (query tile of 128 rows, query
 // head), 10 warps. Warp 0: TMA producer -- lane 0 loads Q once and then K
 // tiles of 128 keys into a three-stage ring (a stage is freed as soon as its
-// S has been computed), lane 1 loads V^T tiles into a two-stage ring (freed
+// S has been computed), lane 1 loads V^T tiles into a three-stage ring (freed
 // after P V). Warp 1: TMEM owner and MMA issuer: S_0 and S_1 up front into
-// two TMEM S buffers; then per tile j: S_{j+2} as soon as S_j has been read
-// out, O += P_j V_j as soon as P_j is written. Warps 2..9: two warps per
+// two TMEM S buffers; then per tile j: O += P_j V_j as soon as P_j is
+// written, with P_j read from TMEM (the MMA's A operand), then S_{j+2} into
+// the same buffer (one thread's MMAs execute in issue order, so S_{j+2}
+// overwrites P_j only after P_j V_j has read it). Warps 2..9: two warps per
 // 32-row TMEM lane quarter, one for keys [0, 64) of the tile and one for keys
 // [64, 128) (and the matching halves of O); thread = (query row, half). Per
 // tile: read the half row of S, mask (boundary tiles only), row maximum over
 // both halves (exchanged through shared memory), online softmax in base 2
 // with a lazy reference: m moves (and the O row is rescaled) only when a
 // tile's maximum exceeds it by more than ATT_TAU2, so P <= 2^TAU2; P goes as
-// BF16 into the 128-byte-swizzled K-major tile the MMA reads. At the end
+// BF16 pairs over the first 64 columns of its own S buffer (both warps of a
+// lane quarter have read their S halves before either writes P). At the end
 // O / l times the gate, BF16, to `out`.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384).
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O [256,384).
 // All waits are bounded; on expiry the error word is set and every role
 // leaves after its in-flight copies and MMAs have completed. The two warps of
 // a lane quarter meet at named barriers the same number of times whatever
@@ -168,12 +171,11 @@ struct AttnCfg {
   static constexpr int Q_BYTES = ATT_BQ * ATT_D * 2;     // 32 KB: two 64-channel blocks
   static constexpr int K_BYTES = ATT_BK * ATT_D * 2;     // 32 KB
   static constexpr int V_BYTES = ATT_D * ATT_BK * 2;     // 32 KB (V^T: 128 channels x 128 keys)
-  static constexpr int P_BYTES = ATT_BQ * ATT_BK * 2;    // 32 KB
   static constexpr int K_STAGES = 3, V_STAGES = 2;
-  static constexpr int XCH_BYTES = 2 * ATT_BQ * 4;       // per (half, row): one float
+  static constexpr int XCH_BYTES = 2 * 2 * ATT_BQ * 4;   // per (tile parity, half, row): one float
   static constexpr int BAR_BYTES = 20 * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES +
-                                    P_BYTES + XCH_BYTES + BAR_BYTES;
+                                    XCH_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -227,16 +229,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::Q_BYTES;
   uint8_t* sV = sK + C::K_STAGES * C::K_BYTES;
-  uint8_t* sP = sV + C::V_STAGES * C::V_BYTES;
-  float* xch = reinterpret_cast<float*>(sP + C::P_BYTES);   // [2 halves][128 rows]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + C::P_BYTES + C::XCH_BYTES);
+  float* xch = reinterpret_cast<float*>(sV + C::V_STAGES * C::V_BYTES);  // [parity][half][row]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::V_STAGES * C::V_BYTES + C::XCH_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;        // [3]
   uint64_t* k_empty = bars + 4;       // [3]
   uint64_t* v_full = bars + 7;        // [2]
-  uint64_t* v_empty = bars + 9;       // [2]
-  uint64_t* s_full = bars + 11;       // [2]
-  uint64_t* s_free = bars + 13;       // [2]
+  uint64_t* v_empty = bars + 10;      // [2]
+  uint64_t* s_full = bars + 13;       // [2]
   uint64_t* p_full = bars + 15;
   uint64_t* o_done = bars + 16;
   uint64_t* mma_done = bars + 17;
@@ -263,10 +263,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], ATT_SOFTMAX_WARPS);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(&s_full[s], 1);
     mbar_init(p_full, ATT_SOFTMAX_WARPS);
     mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
@@ -297,7 +294,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         tma_load_2d(sQ, &tm_q, q_full, 0, qrow, pol);
         tma_load_2d(sQ + C::Q_BYTES / 2, &tm_q, q_full, 64, qrow, pol);
       }
-      // lane 0: K tiles (3 stages); lane 1: V^T tiles (2 stages)
+      // lane 0: K tiles (three stages); lane 1: V^T tiles (two stages)
       const int NS = lane == 0 ? C::K_STAGES : C::V_STAGES;
       uint64_t* full = lane == 0 ? k_full : v_full;
       uint64_t* empty = lane == 0 ? k_empty : v_empty;
@@ -336,8 +333,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       tc_fence_after();
       const uint64_t dq = sdesc_k128(smem_u32(sQ));
       const uint64_t dq1 = sdesc_k128(smem_u32(sQ + C::Q_BYTES / 2));
-      const uint64_t dp = sdesc_k128(smem_u32(sP));
-      const uint64_t dp1 = sdesc_k128(smem_u32(sP + C::P_BYTES / 2));
       auto issue_s = [&](int j) -> bool {
         const int ks = j % C::K_STAGES;
         if (!mbar_wait_bounded(&k_full[ks], (j / C::K_STAGES) & 1, tmo, abort_flag)) return false;
@@ -356,18 +351,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (ok && ntiles > 0) ok = issue_s(0);
       if (ok && ntiles > 1) ok = issue_s(1);
       for (int j = 0; ok && j < ntiles; ++j) {
-        // S_{j+2} into the buffer S_j leaves, as soon as S_j has been read out
-        if (j + 2 < ntiles) {
-          if (!mbar_wait_bounded(&s_free[j & 1], (j >> 1) & 1, tmo, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (!issue_s(j + 2)) {
-            ok = false;
-            break;
-          }
-        }
         const int vs = j % C::V_STAGES;
         if (!mbar_wait_bounded(p_full, j & 1, tmo, abort_flag) ||
             !mbar_wait_bounded(&v_full[vs], (j / C::V_STAGES) & 1, tmo, abort_flag)) {
@@ -375,14 +358,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           break;
         }
         tc_fence_after();
+        // O += P_j V_j: P_j from TMEM (keys 16kk.. in columns 8kk..), V_j^T from
+        // shared memory (two 64-key blocks)
+        const uint32_t dP = tmem_base + static_cast<uint32_t>((j & 1) * 128);
         const uint32_t base = smem_u32(sV + vs * C::V_BYTES);
         const uint64_t dv = sdesc_k128(base), dv1 = sdesc_k128(base + C::V_BYTES / 2);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, dp + 2 * kk, dv + 2 * kk, idesc, (j | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16_ts(dO, dP + 8 * kk, dv + 2 * kk, idesc, (j | kk) != 0);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, dp1 + 2 * kk, dv1 + 2 * kk, idesc, 1u);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16_ts(dO, dP + 32 + 8 * kk, dv1 + 2 * kk, idesc, 1u);
         mma_commit(o_done);
         mma_commit(&v_empty[vs]);
+        // S_{j+2} into the buffer P_j occupies, after P_j V_j in issue order
+        if (j + 2 < ntiles && !issue_s(j + 2)) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) gemm_fail(abort_flag);
       mma_commit(mma_done);
@@ -419,9 +410,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (ok) {
         tc_fence_after();
         tmem_ld64(tmem_base + lanebits + s * 128 + col0, sv);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[s]);
         const int k0 = (j0 + j) * ATT_BK + half * 64;
         if (__any_sync(0xffffffffu, k0 < lo || k0 + 63 > hi)) {
 #pragma unroll
@@ -442,11 +430,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         mt = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * c2;
       }
-      // tile maximum over both halves of the row (-inf from a failed half)
-      xch[half * ATT_BQ + row] = mt;
+      // tile maximum over both halves of the row (-inf from a failed half),
+      // through slots of this tile's parity: the partner's next write to them
+      // (tile j + 2) comes after the barrier of tile j + 1, which this warp
+      // reaches only after reading. The barrier also orders both warps' S
+      // reads before either P write.
+      float* xs = xch + s * 2 * ATT_BQ;
+      xs[half * ATT_BQ + row] = mt;
+      tc_fence_before();
       named_bar_sync(bar_id, 64);
-      mt = fmaxf(mt, xch[(half ^ 1) * ATT_BQ + row]);
-      named_bar_sync(bar_id, 64);
+      tc_fence_after();
+      mt = fmaxf(mt, xs[(half ^ 1) * ATT_BQ + row]);
       if (!ok) continue;
       // lazy reference: move m only when this tile exceeds it by more than TAU2
       const float mn = mt > m + ATT_TAU2 ? mt : m;
@@ -470,52 +464,53 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       l = l * alpha + ps;
       m = mn;
-      // O may be rescaled and P overwritten only after the previous P V
-      if (j > 0) {
+      // the O row is rescaled only after the previous P V has completed. (At
+      // tile j every P V before j - 1 has completed -- S_j was issued after
+      // P_{j-2} V_{j-2} -- so this parity wait is exact even when earlier
+      // tiles skipped it.)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         bool od = false;
         if (lane == 0) od = mbar_wait_bounded(o_done, (j - 1) & 1, tmo, abort_flag);
         ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
         if (!ok) continue;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < 64; c += 16) {
-            float o[16];
-            tmem_ld16(tmem_base + lanebits + 256 + col0 + c, o);
+        for (int c = 0; c < 64; c += 16) {
+          float o[16];
+          tmem_ld16(tmem_base + lanebits + 256 + col0 + c, o);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tmem_st16(tmem_base + lanebits + 256 + col0 + c, o);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 16; ++i) o[i] *= alpha;
+          tmem_st16(tmem_base + lanebits + 256 + col0 + c, o);
         }
       }
-      // P half row, BF16, into the swizzled K-major tile: key c of row `row`
-      // sits in 64-key block c/64, 16-byte chunk (c%64)/8 ^ (row%8)
-      uint8_t* prow = sP + half * (C::P_BYTES / 2) + (row >> 3) * 1024 + (row & 7) * 128;
+      // P half row as BF16 pairs (key 2i in the low half) into columns
+      // [32 half, 32 half + 32) of this tile's S buffer
+      uint32_t pk[32];
 #pragma unroll
-      for (int chunk = 0; chunk < 8; ++chunk) {
-        uint4 pk;
-        __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          p2[i] = __floats2bfloat162_rn(sv[chunk * 8 + 2 * i], sv[chunk * 8 + 2 * i + 1]);
-        *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = pk;
+      for (int i = 0; i < 32; ++i) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(sv[2 * i], sv[2 * i + 1]);
+        pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      // P (generic-proxy stores) and the O rescale visible to the MMA
-      fence_proxy_async_smem();
+      tmem_st32(tmem_base + lanebits + s * 128 + half * 32, pk);
+      tmem_wait_st();
+      // P and the O rescale visible to the MMA
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // final: O / l times the gate, BF16; l summed over both halves
+    // final: O / l times the gate, BF16; l summed over both halves. Every
+    // MMA has completed once mma_done (committed after the last one) has.
     if (ok && ntiles > 0) {
       bool od = false;
-      if (lane == 0) od = mbar_wait_bounded(o_done, (ntiles - 1) & 1, tmo, abort_flag);
+      if (lane == 0) od = mbar_wait_bounded(mma_done, 0, tmo, abort_flag);
       ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
     }
-    xch[half * ATT_BQ + row] = l;
+    // (the last tile's exchange used parity (ntiles - 1) & 1; these slots
+    // were last read at tile ntiles - 2, before that tile's barrier)
+    float* xl = xch + (ntiles & 1) * 2 * ATT_BQ;
+    xl[half * ATT_BQ + row] = l;
     named_bar_sync(bar_id, 64);
-    const float lt = l + xch[(half ^ 1) * ATT_BQ + row];
+    const float lt = l + xl[(half ^ 1) * ATT_BQ + row];
     if (!ok) {
       if (lane == 0) gemm_fail(abort_flag);
     } else {

@@ -131,33 +131,40 @@ __global__ void linear_units_kernel(int n, int MT, int4* __restrict__ units, int
 
 // ---------------------------------------------------------------------------
 // Flash attention on tcgen05, one CTA per (query tile of 128 rows, query
-// head), 10 warps. Warp 0: TMA producer -- lane 0 loads Q once and then K
-// tiles of 128 keys into a three-stage ring (a stage is freed as soon as its
-// S has been computed), lane 1 loads V^T tiles into a three-stage ring (freed
-// after P V). Warp 1: TMEM owner and MMA issuer: S_0 and S_1 up front into
-// two TMEM S buffers; then per tile j: O += P_j V_j as soon as P_j is
-// written, with P_j read from TMEM (the MMA's A operand), then S_{j+2} into
-// the same buffer (one thread's MMAs execute in issue order, so S_{j+2}
-// overwrites P_j only after P_j V_j has read it). Warps 2..9: two warps per
-// 32-row TMEM lane quarter, one for keys [0, 64) of the tile and one for keys
-// [64, 128) (and the matching halves of O); thread = (query row, half). Per
-// tile: read the half row of S, mask (boundary tiles only), row maximum over
-// both halves (exchanged through shared memory), online softmax in base 2
-// with a lazy reference: m moves (and the O row is rescaled) only when a
-// tile's maximum exceeds it by more than ATT_TAU2, so P <= 2^TAU2; P goes as
-// BF16 pairs over the first 64 columns of its own S buffer (both warps of a
-// lane quarter have read their S halves before either writes P). At the end
-// O / l times the gate, BF16, to `out`.
-// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O [256,384).
+// head). Warp 0: TMA producer of Q (once) and of K tiles of 128 keys into a
+// three-stage ring (a stage is freed as soon as its S has been computed);
+// the last warp: TMA producer of V^T tiles into a two-stage ring (freed after
+// P V). Warp 1: TMEM owner and MMA issuer: S_0, S_1 and S_2 up front into
+// three TMEM S buffers; then per tile j: O += P_j V_j as soon as P_j is
+// written, with P_j read from TMEM (the MMA's A operand), then S_{j+3} into
+// the same buffer (one thread's MMAs execute in issue order, so S_{j+3}
+// overwrites P_j only after P_j V_j has read it); the S of the next two
+// tiles is thus computed while a tile's softmax runs. Warps 2..: ATT_PARTS warps
+// per 32-row TMEM lane quarter, each for ATT_KW consecutive keys of the tile
+// (and the matching columns of O); thread = (query row, part). Per tile: read
+// the part of the S row, mask (boundary tiles only), row maximum over all
+// parts (exchanged through shared memory), online softmax in base 2 with a
+// lazy reference: m moves (and the O row is rescaled) only when a tile's
+// maximum exceeds it by more than ATT_TAU2, so P <= 2^TAU2; P goes as BF16
+// pairs over the first 64 columns of its own S buffer (every warp of a lane
+// quarter has read its part of S before any writes P). At the end O / l
+// times the gate, BF16, to `out`.
+// TMEM columns: S/P buffers [0,128), [128,256), [256,384); O [384,512).
 // All waits are bounded; on expiry the error word is set and every role
 // leaves after its in-flight copies and MMAs have completed. The two warps of
 // a lane quarter meet at named barriers the same number of times whatever
 // happens (no early exit from the tile loop), so those barriers cannot hang.
 // ---------------------------------------------------------------------------
 constexpr float ATT_TAU2 = 8.0f;        // lazy-rescale threshold, base-2 units
+constexpr int ATT_SBUF = 3;             // S / P buffers in TMEM
+constexpr uint32_t ATT_O_COL = ATT_SBUF * 128;
 constexpr float ATT_LOG2E = 1.4426950408889634f;
-constexpr int ATT_SOFTMAX_WARPS = 8;
-constexpr int ATT_THREADS = 32 * (2 + ATT_SOFTMAX_WARPS);
+constexpr int ATT_PARTS = 2;                      // softmax warps per TMEM lane quarter
+constexpr int ATT_KW = ATT_BK / ATT_PARTS;        // keys (and O columns) per softmax warp
+constexpr int ATT_SOFTMAX_WARPS = 4 * ATT_PARTS;
+static_assert(ATT_KW == 32 || ATT_KW == 64, "softmax split");
+constexpr int ATT_VWARP = 2 + ATT_SOFTMAX_WARPS;   // the V^T producer warp (the last)
+constexpr int ATT_THREADS = 32 * (3 + ATT_SOFTMAX_WARPS);
 
 struct AttnArgs {
   int T, Tp, nq, nkv, window;
@@ -172,8 +179,8 @@ struct AttnCfg {
   static constexpr int K_BYTES = ATT_BK * ATT_D * 2;     // 32 KB
   static constexpr int V_BYTES = ATT_D * ATT_BK * 2;     // 32 KB (V^T: 128 channels x 128 keys)
   static constexpr int K_STAGES = 3, V_STAGES = 2;
-  static constexpr int XCH_BYTES = 2 * 2 * ATT_BQ * 4;   // per (tile parity, half, row): one float
-  static constexpr int BAR_BYTES = 20 * 8 + 16;
+  static constexpr int XCH_BYTES = 2 * ATT_PARTS * ATT_BQ * 4;  // per (tile parity, part, row): one float
+  static constexpr int BAR_BYTES = 24 * 8;
   static constexpr int SMEM_BYTES = 1024 + Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES +
                                     XCH_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -219,6 +226,29 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// A softmax warp's part of the S row (ATT_KW columns) from TMEM.
+__device__ __forceinline__ void attn_ld_part(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
+__device__ __forceinline__ void attn_ld_part(uint32_t taddr, float (&v)[64]) { tmem_ld64(taddr, v); }
+// The same part of the P row as BF16 pairs (key 2i in the low half) into TMEM.
+__device__ __forceinline__ void attn_st_p(uint32_t taddr, const float (&p)[32]) {
+  float pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(p[2 * i], p[2 * i + 1]);
+    pk[i] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&b2));
+  }
+  tmem_st16(taddr, pk);
+}
+__device__ __forceinline__ void attn_st_p(uint32_t taddr, const float (&p)[64]) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(p[2 * i], p[2 * i + 1]);
+    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  tmem_st32(taddr, pk);
+}
+
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     flash_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_vt, const AttnArgs args) {
@@ -229,18 +259,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::Q_BYTES;
   uint8_t* sV = sK + C::K_STAGES * C::K_BYTES;
-  float* xch = reinterpret_cast<float*>(sV + C::V_STAGES * C::V_BYTES);  // [parity][half][row]
+  float* xch = reinterpret_cast<float*>(sV + C::V_STAGES * C::V_BYTES);  // [parity][part][row]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::V_STAGES * C::V_BYTES + C::XCH_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;        // [3]
   uint64_t* k_empty = bars + 4;       // [3]
   uint64_t* v_full = bars + 7;        // [2]
   uint64_t* v_empty = bars + 10;      // [2]
-  uint64_t* s_full = bars + 13;       // [2]
-  uint64_t* p_full = bars + 15;
-  uint64_t* o_done = bars + 16;
-  uint64_t* mma_done = bars + 17;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  // Per S buffer b: s_full[b] / p_full[b] complete once per tile j with
+  // j % 3 == b. Neither can run two phases ahead of its waiter: S_{j+3} is
+  // issued only after P_j (whose softmax waited on S_j) has been consumed.
+  uint64_t* s_full = bars + 12;       // [3]
+  uint64_t* p_full = bars + 15;       // [3]
+  uint64_t* o_done = bars + 18;       // [2]: P_j V_j done, tiles of parity j & 1
+  uint64_t* mma_done = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -263,9 +296,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&s_full[s], 1);
-    mbar_init(p_full, ATT_SOFTMAX_WARPS);
-    mbar_init(o_done, 1);
+    for (int s = 0; s < ATT_SBUF; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], ATT_SOFTMAX_WARPS);
+    }
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -283,21 +319,23 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == ATT_VWARP) {
     // ------------------------------------------------------------ producers
-    if (lane < 2) {
+    // (one warp each, so neither producer's waits hold the other back)
+    const bool kp = warp == 0;              // Q and K tiles; else V^T tiles
+    if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
       const volatile int never = 0;
-      if (lane == 0) {
+      if (kp) {
         const int qrow = h * args.Tp + qt * ATT_BQ;
         mbar_arrive_expect_tx(q_full, C::Q_BYTES);
         tma_load_2d(sQ, &tm_q, q_full, 0, qrow, pol);
         tma_load_2d(sQ + C::Q_BYTES / 2, &tm_q, q_full, 64, qrow, pol);
       }
-      // lane 0: K tiles (three stages); lane 1: V^T tiles (two stages)
-      const int NS = lane == 0 ? C::K_STAGES : C::V_STAGES;
-      uint64_t* full = lane == 0 ? k_full : v_full;
-      uint64_t* empty = lane == 0 ? k_empty : v_empty;
+      // K tiles (three stages) or V^T tiles (two stages)
+      const int NS = kp ? C::K_STAGES : C::V_STAGES;
+      uint64_t* full = kp ? k_full : v_full;
+      uint64_t* empty = kp ? k_empty : v_empty;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % NS;
@@ -307,7 +345,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         const int k0 = (j0 + j) * ATT_BK;
         mbar_arrive_expect_tx(&full[s], C::K_BYTES);
-        if (lane == 0) {
+        if (kp) {
           uint8_t* st = sK + s * C::K_BYTES;
           tma_load_2d(st, &tm_k, &full[s], 0, g * args.Tp + k0, pol);
           tma_load_2d(st + C::K_BYTES / 2, &tm_k, &full[s], 64, g * args.Tp + k0, pol);
@@ -319,7 +357,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         ++issued;
       }
       // every load must land before the CTA exits
-      if (lane == 0 && !mbar_wait_bounded(q_full, 0, tmo, &never)) gemm_fail(abort_flag);
+      if (kp && !mbar_wait_bounded(q_full, 0, tmo, &never)) gemm_fail(abort_flag);
       for (int j = max(0, issued - NS); j < issued; ++j)
         if (!mbar_wait_bounded(&full[j % NS], (j / NS) & 1, tmo, &never)) gemm_fail(abort_flag);
     }
@@ -328,7 +366,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
-      const uint32_t dO = tmem_base + 256;
+      const uint32_t dO = tmem_base + ATT_O_COL;
       bool ok = mbar_wait_bounded(q_full, 0, tmo, abort_flag);
       tc_fence_after();
       const uint64_t dq = sdesc_k128(smem_u32(sQ));
@@ -339,20 +377,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         tc_fence_after();
         const uint32_t base = smem_u32(sK + ks * C::K_BYTES);
         const uint64_t dk = sdesc_k128(base), dk1 = sdesc_k128(base + C::K_BYTES / 2);
-        const uint32_t dS = tmem_base + static_cast<uint32_t>((j & 1) * 128);
+        const uint32_t dS = tmem_base + static_cast<uint32_t>((j % ATT_SBUF) * 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dS, dq + 2 * kk, dk + 2 * kk, idesc, kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dS, dq1 + 2 * kk, dk1 + 2 * kk, idesc, 1u);
-        mma_commit(&s_full[j & 1]);
+        mma_commit(&s_full[j % ATT_SBUF]);
         mma_commit(&k_empty[ks]);
         return true;
       };
-      if (ok && ntiles > 0) ok = issue_s(0);
-      if (ok && ntiles > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < ATT_SBUF && j < ntiles; ++j) ok = issue_s(j);
       for (int j = 0; ok && j < ntiles; ++j) {
         const int vs = j % C::V_STAGES;
-        if (!mbar_wait_bounded(p_full, j & 1, tmo, abort_flag) ||
+        if (!mbar_wait_bounded(&p_full[j % ATT_SBUF], (j / ATT_SBUF) & 1, tmo, abort_flag) ||
             !mbar_wait_bounded(&v_full[vs], (j / C::V_STAGES) & 1, tmo, abort_flag)) {
           ok = false;
           break;
@@ -360,17 +397,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         tc_fence_after();
         // O += P_j V_j: P_j from TMEM (keys 16kk.. in columns 8kk..), V_j^T from
         // shared memory (two 64-key blocks)
-        const uint32_t dP = tmem_base + static_cast<uint32_t>((j & 1) * 128);
+        const uint32_t dP = tmem_base + static_cast<uint32_t>((j % ATT_SBUF) * 128);
         const uint32_t base = smem_u32(sV + vs * C::V_BYTES);
         const uint64_t dv = sdesc_k128(base), dv1 = sdesc_k128(base + C::V_BYTES / 2);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ts(dO, dP + 8 * kk, dv + 2 * kk, idesc, (j | kk) != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ts(dO, dP + 32 + 8 * kk, dv1 + 2 * kk, idesc, 1u);
-        mma_commit(o_done);
+        mma_commit(&o_done[j & 1]);
         mma_commit(&v_empty[vs]);
-        // S_{j+2} into the buffer P_j occupies, after P_j V_j in issue order
-        if (j + 2 < ntiles && !issue_s(j + 2)) {
+        // S_{j+3} into the buffer P_j occupies, after P_j V_j in issue order
+        if (j + ATT_SBUF < ntiles && !issue_s(j + ATT_SBUF)) {
           ok = false;
           break;
         }
@@ -384,14 +421,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int q = warp & 3;                 // TMEM lane quarter
-    const int half = (warp - 2) >> 2;       // keys / O columns [64 half, 64 half + 64)
+    const int part = (warp - 2) >> 2;       // keys / O columns [KW part, KW part + KW)
     const int row = q * 32 + lane;          // query row within the tile
     const int qi = qt * ATT_BQ + row;       // query index
     const uint32_t lanebits = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(half * 64);
-    const int bar_id = 1 + q;               // named barrier of this lane quarter's two warps
+    const uint32_t col0 = static_cast<uint32_t>(part * ATT_KW);
+    const int bar_id = 1 + q;               // named barrier of this lane quarter's warps
     const float NEG = -1e30f;
-    float m = NEG, l = 0.f;                 // base-2 units; l over this half's keys
+    float m = NEG, l = 0.f;                 // base-2 units; l over this part's keys
     // global layers' query scale is already in q; logits to base 2 in one FMA
     const float c2 = args.scale * ATT_LOG2E;
     const uint64_t cc = f2_pack(c2, c2);
@@ -399,48 +436,50 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const int lo = args.window > 0 ? qi - args.window + 1 : 0;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
+      const int s = j & 1;                  // exchange slots
+      const int sb = j % ATT_SBUF;          // S / P buffer
       if (ok) {
         bool ready = false;
-        if (lane == 0) ready = mbar_wait_bounded(&s_full[s], (j >> 1) & 1, tmo, abort_flag);
+        if (lane == 0) ready = mbar_wait_bounded(&s_full[sb], (j / ATT_SBUF) & 1, tmo, abort_flag);
         ok = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
       }
-      float sv[64];
+      float sv[ATT_KW];
       float mt = -INFINITY;
       if (ok) {
         tc_fence_after();
-        tmem_ld64(tmem_base + lanebits + s * 128 + col0, sv);
-        const int k0 = (j0 + j) * ATT_BK + half * 64;
-        if (__any_sync(0xffffffffu, k0 < lo || k0 + 63 > hi)) {
+        attn_ld_part(tmem_base + lanebits + sb * 128 + col0, sv);
+        const int k0 = (j0 + j) * ATT_BK + part * ATT_KW;
+        if (__any_sync(0xffffffffu, k0 < lo || k0 + ATT_KW - 1 > hi)) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < ATT_KW; ++c) {
             const int kj = k0 + c;
             sv[c] = (kj >= lo && kj <= hi) ? sv[c] : -INFINITY;
           }
         }
-        // raw maximum in eight independent partials (one warp per scheduler
-        // pair: long dependency chains would stall it)
+        // raw maximum in eight independent partials (long dependency chains
+        // would stall the scheduler)
         float mp[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
+        for (int i = 0; i < 8; ++i) mp[i] = fmaxf(sv[i], sv[8 + i]);
 #pragma unroll
-        for (int c = 24; c < 64; c += 16) {
+        for (int c = 16; c < ATT_KW; c += 16) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) mp[i] = fmax3(mp[i], sv[c + i], sv[c + 8 + i]);
         }
         mt = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * c2;
       }
-      // tile maximum over both halves of the row (-inf from a failed half),
-      // through slots of this tile's parity: the partner's next write to them
+      // tile maximum over all parts of the row (-inf from a failed part),
+      // through slots of this tile's parity: a partner's next write to them
       // (tile j + 2) comes after the barrier of tile j + 1, which this warp
-      // reaches only after reading. The barrier also orders both warps' S
-      // reads before either P write.
-      float* xs = xch + s * 2 * ATT_BQ;
-      xs[half * ATT_BQ + row] = mt;
+      // reaches only after reading. The barrier also orders every warp's S
+      // reads before any P write.
+      float* xs = xch + s * ATT_PARTS * ATT_BQ;
+      xs[part * ATT_BQ + row] = mt;
       tc_fence_before();
-      named_bar_sync(bar_id, 64);
+      named_bar_sync(bar_id, 32 * ATT_PARTS);
       tc_fence_after();
-      mt = fmaxf(mt, xs[(half ^ 1) * ATT_BQ + row]);
+#pragma unroll
+      for (int o = 1; o < ATT_PARTS; ++o) mt = fmaxf(mt, xs[((part + o) % ATT_PARTS) * ATT_BQ + row]);
       if (!ok) continue;
       // lazy reference: move m only when this tile exceeds it by more than TAU2
       const float mn = mt > m + ATT_TAU2 ? mt : m;
@@ -448,7 +487,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const uint64_t nm = f2_pack(-mn, -mn);
       uint64_t sp[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < ATT_KW; c += 2) {
         float a, b;
         f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), cc, nm), a, b);
         sv[c] = ex2_approx(a);
@@ -464,41 +503,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       l = l * alpha + ps;
       m = mn;
-      // the O row is rescaled only after the previous P V has completed. (At
-      // tile j every P V before j - 1 has completed -- S_j was issued after
-      // P_{j-2} V_{j-2} -- so this parity wait is exact even when earlier
-      // tiles skipped it.)
+      // the O row is rescaled only after the previous P V has completed.
+      // o_done[b] completes once per tile of parity b. At tile j every P V
+      // up to j - 3 has completed (S_j was issued after P_{j-3} V_{j-3}) and
+      // P_{j+1} V_{j+1} cannot have, so the phase of P_{j-1} V_{j-1} is the
+      // current or the last one of o_done[(j-1)&1]: the parity wait is exact
+      // even when earlier tiles skipped it.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         bool od = false;
-        if (lane == 0) od = mbar_wait_bounded(o_done, (j - 1) & 1, tmo, abort_flag);
+        if (lane == 0)
+          od = mbar_wait_bounded(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, tmo, abort_flag);
         ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
         if (!ok) continue;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < ATT_KW; c += 16) {
           float o[16];
-          tmem_ld16(tmem_base + lanebits + 256 + col0 + c, o);
+          tmem_ld16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] *= alpha;
-          tmem_st16(tmem_base + lanebits + 256 + col0 + c, o);
+          tmem_st16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
         }
       }
-      // P half row as BF16 pairs (key 2i in the low half) into columns
-      // [32 half, 32 half + 32) of this tile's S buffer
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(sv[2 * i], sv[2 * i + 1]);
-        pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-      }
-      tmem_st32(tmem_base + lanebits + s * 128 + half * 32, pk);
+      // this part of the P row as BF16 pairs (key 2i in the low half) into
+      // columns [KW/2 part, KW/2 part + KW/2) of this tile's S buffer
+      attn_st_p(tmem_base + lanebits + sb * 128 + part * (ATT_KW / 2), sv);
       tmem_wait_st();
       // P and the O rescale visible to the MMA
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[sb]);
     }
-    // final: O / l times the gate, BF16; l summed over both halves. Every
+    // final: O / l times the gate, BF16; l summed over all parts. Every
     // MMA has completed once mma_done (committed after the last one) has.
     if (ok && ntiles > 0) {
       bool od = false;
@@ -507,10 +543,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     // (the last tile's exchange used parity (ntiles - 1) & 1; these slots
     // were last read at tile ntiles - 2, before that tile's barrier)
-    float* xl = xch + (ntiles & 1) * 2 * ATT_BQ;
-    xl[half * ATT_BQ + row] = l;
-    named_bar_sync(bar_id, 64);
-    const float lt = l + xl[(half ^ 1) * ATT_BQ + row];
+    float* xl = xch + (ntiles & 1) * ATT_PARTS * ATT_BQ;
+    xl[part * ATT_BQ + row] = l;
+    named_bar_sync(bar_id, 32 * ATT_PARTS);
+    float lt = l;
+#pragma unroll
+    for (int o = 1; o < ATT_PARTS; ++o) lt += xl[((part + o) % ATT_PARTS) * ATT_BQ + row];
     if (!ok) {
       if (lane == 0) gemm_fail(abort_flag);
     } else {
@@ -521,9 +559,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const float* gr = args.gate + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
       __nv_bfloat16* orow = args.out + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
 #pragma unroll 1
-      for (int c = 0; c < 64; c += 16) {
+      for (int c = 0; c < ATT_KW; c += 16) {
         float o[16];
-        tmem_ld16(tmem_base + lanebits + 256 + col0 + c, o);
+        tmem_ld16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
         if (valid) {
           float gt[16];
           const float4* g4 = reinterpret_cast<const float4*>(gr + c);

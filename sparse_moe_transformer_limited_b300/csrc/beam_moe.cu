@@ -11,6 +11,8 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <string>
 #include <vector>
 
@@ -180,6 +182,21 @@ enum {
 // Bytes of the router's unit list and count (tensor-core router only).
 size_t router_units_bytes(const beam_moe_params& p) {
   return static_cast<size_t>(kRouterKSplit) * ((p.T + 255) / 256) * 16 + 16;
+}
+
+// Opt kernel `fn` into `bytes` of dynamic shared memory on the current
+// device. The attribute belongs to the (kernel, device) pair, so it is set
+// once per pair, under a lock (launches may come from several host threads).
+beam_status_t ensure_smem(const void* fn, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  BEAM_CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({fn, dev}) != 0) return BEAM_OK;
+  BEAM_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  done.insert({fn, dev});
+  return BEAM_OK;
 }
 
 int sm_count() {
@@ -353,12 +370,8 @@ beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CU
                           const beam::GemmArgs& args, cudaStream_t st) {
   using C = beam::GemmCfg<MODE, NT, STAGES, KIND>;
   auto kern = beam::expert_gemm_kernel<MODE, NT, STAGES, KIND>;
-  static bool attr_set = false;  // per template instance
-  if (!attr_set) {
-    BEAM_CUDA_TRY(
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
-    attr_set = true;
-  }
+  beam_status_t sa = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  if (sa != BEAM_OK) return sa;
   ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
   kern<<<sm_count(), 192, C::SMEM_BYTES, st>>>(a0, a1, b, args);
   BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_kernel<gate/up>" : "expert_gemm_kernel<down>");
@@ -371,12 +384,8 @@ beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, con
                                cudaStream_t st, const char* prof_name = nullptr) {
   using C = beam::PairCfg;
   auto kern = beam::expert_gemm_pair_kernel<MODE, F8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    BEAM_CUDA_TRY(
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
-    attr_set = true;
-  }
+  beam_status_t sa = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  if (sa != BEAM_OK) return sa;
   const int grid = (sm_count() / 2) * 2;
   ProfScope ps(prof_name ? prof_name : (MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down"),
                st);
@@ -390,12 +399,8 @@ beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const
                              const beam::TmArgs& args, cudaStream_t st) {
   using C = beam::TmCfg<KIND>;
   auto kern = beam::expert_gemm_tm_kernel<MODE, KIND>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    BEAM_CUDA_TRY(
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
-    attr_set = true;
-  }
+  beam_status_t sa = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  if (sa != BEAM_OK) return sa;
   const int grid = (sm_count() / 2) * 2;
   ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
   kern<<<grid, beam::TM_THREADS, C::SMEM_BYTES, st>>>(w0, w1, tok, args);
@@ -1449,13 +1454,9 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
     aa.gate = gate;
     aa.out = att;
     aa.timeout_ns = kWaitTimeoutNs;
-    static bool attr_set = false;
-    if (!attr_set) {
-      BEAM_CUDA_TRY(cudaFuncSetAttribute(beam::flash_attn_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         beam::AttnCfg::SMEM_BYTES));
-      attr_set = true;
-    }
+    if ((s = ensure_smem(reinterpret_cast<const void*>(beam::flash_attn_kernel),
+                         beam::AttnCfg::SMEM_BYTES)) != BEAM_OK)
+      return s;
     ProfScope ps("flash_attn", st);
     beam::flash_attn_kernel<<<dim3(L.Tp / beam::ATT_BQ, nq), beam::ATT_THREADS,
                               beam::AttnCfg::SMEM_BYTES, st>>>(

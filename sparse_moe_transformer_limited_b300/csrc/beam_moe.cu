@@ -20,6 +20,7 @@
 #include "kernels_attn.cuh"
 #include "kernels_gemm.cuh"
 #include "kernels_gemm_tm.cuh"
+#include "kernels_gemm_tm2.cuh"
 #include "kernels_gemm_2sm.cuh"
 #include "kernels_permute.cuh"
 #include "kernels_quant.cuh"
@@ -113,8 +114,12 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 //    token-major epilogue writes the SwiGLU output in 32-byte vectors), down
 //    on the 2-SM pair kernel (expert_gemm_pair_kernel); PATH_TM and
 //    PATH_PAIR run both GEMMs on one kernel (BEAM_PREFILL_GEMM=tm|pair);
+//    PATH_TM2 runs gate/up on the 256-row token-major kernel
+//    (expert_gemm_tm2_kernel) and down on the pair kernel
+//    (BEAM_PREFILL_GEMM=tm2);
 //  otherwise weights as M with token tiles of 128.
-enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2, PATH_PAIR = 3, PATH_MIXED = 4 };
+enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2, PATH_PAIR = 3, PATH_MIXED = 4,
+                PATH_TM2 = 5 };
 
 GemmPath choose_path(const beam_moe_params& p) {
   const long long pairs = static_cast<long long>(p.T) * p.top_k;
@@ -129,6 +134,7 @@ GemmPath choose_path(const beam_moe_params& p) {
     const char* v = std::getenv("BEAM_PREFILL_GEMM");
     if (v != nullptr && std::strcmp(v, "tm") == 0) return PATH_TM;
     if (v != nullptr && std::strcmp(v, "pair") == 0) return PATH_PAIR;
+    if (v != nullptr && std::strcmp(v, "tm2") == 0) return PATH_TM2;
     return PATH_MIXED;
   }
   return PATH_W128;
@@ -136,7 +142,7 @@ GemmPath choose_path(const beam_moe_params& p) {
 
 int path_nt(GemmPath g) { return g == PATH_W32 ? 32 : (g == PATH_W128 ? 128 : 256); }
 int path_mt_down(GemmPath g, int H) {
-  return (g == PATH_TM || g == PATH_PAIR || g == PATH_MIXED) ? H / 256 : H / 128;
+  return (g == PATH_TM || g == PATH_PAIR || g == PATH_MIXED || g == PATH_TM2) ? H / 256 : H / 128;
 }
 
 // Router logits path: the tensor cores (exact three-way BF16 split of the
@@ -266,7 +272,7 @@ Layout make_layout(const beam_moe_params& p) {
   L.rows = f4 ? (R + (L.pad - 1) * std::min<long long>(p.E, R) + 127) / 128 * 128 : R;
   const long long Rr = L.rows;
   const long long tiles = (R + L.NT - 1) / L.NT + p.E;
-  if (L.path == PATH_PAIR || L.path == PATH_MIXED) {
+  if (L.path == PATH_PAIR || L.path == PATH_MIXED || L.path == PATH_TM2) {
     const long long groups = (R + 255) / 256 + p.E;
     // (the mixed path's gate/up list holds tm cluster units: two int4 each)
     L.units_gu_max = L.path == PATH_MIXED
@@ -405,6 +411,19 @@ beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const
   ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
   kern<<<grid, beam::TM_THREADS, C::SMEM_BYTES, st>>>(w0, w1, tok, args);
   BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_tm_kernel<gate/up>" : "expert_gemm_tm_kernel<down>");
+  return BEAM_OK;
+}
+
+template <int KIND>
+beam_status_t launch_gemm_tm2(const CUtensorMap& wg, const CUtensorMap& wu, const CUtensorMap& tok,
+                              const beam::Tm2Args& args, cudaStream_t st) {
+  using C = beam::Tm2Cfg<KIND>;
+  auto kern = beam::expert_gemm_tm2_kernel<KIND>;
+  beam_status_t sa = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  if (sa != BEAM_OK) return sa;
+  ProfScope ps("expert_gemm_gateup_swiglu", st);
+  kern<<<sm_count(), beam::TM2_THREADS, C::SMEM_BYTES, st>>>(wg, wu, tok, args);
+  BEAM_LAUNCH_CHECK("expert_gemm_tm2_kernel<gate/up>");
   return BEAM_OK;
 }
 
@@ -554,7 +573,7 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     return BEAM_OK;
   };
 
-  if (L.path == PATH_PAIR || L.path == PATH_MIXED) {
+  if (L.path == PATH_PAIR || L.path == PATH_MIXED || L.path == PATH_TM2) {
     beam::PairArgs pa{};
     pa.units = ugu;
     pa.n_units = nunits + 0;
@@ -580,7 +599,26 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     CUtensorMap m_x64, m_a64;
     if ((s = make_map(&m_x64, xop, R, H, 64, F8)) != BEAM_OK) return s;
     if ((s = make_map(&m_a64, aop, R, I, 64, F8)) != BEAM_OK) return s;
-    if (L.path == PATH_MIXED) {
+    if (L.path == PATH_TM2) {
+      // gate/up on the 256-row token-major kernel (128-row boxes)
+      CUtensorMap m_g128, m_u128, m_x128;
+      if ((s = make_map(&m_g128, w.gate, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
+      if ((s = make_map(&m_u128, w.up, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
+      if ((s = make_map(&m_x128, xop, R, H, 128, F8)) != BEAM_OK) return s;
+      beam::Tm2Args ta{};
+      ta.units = ugu;
+      ta.n_units = nunits + 0;
+      ta.k_blocks = H / KB;
+      ta.w_rows_per_expert = I;
+      ta.out = act;
+      ta.out_ld = I;
+      ta.timeout_ns = kWaitTimeoutNs;
+      ta.row_scale = q.xscale;
+      ta.w_scale0 = w.s_gate;
+      ta.w_scale1 = w.s_up;
+      if ((s = launch_gemm_tm2<F8 ? beam::KIND_E4M3 : beam::KIND_BF16>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK)
+        return s;
+    } else if (L.path == PATH_MIXED) {
       // gate/up on the token-major multicast kernel (128-row boxes)
       CUtensorMap m_g128, m_u128, m_x128;
       if ((s = make_map(&m_g128, w.gate, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
@@ -737,6 +775,10 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     ProfScope ps("expert_scan_units", st);
     if (L.path == PATH_PAIR)
       beam::expert_scan_units_prefill_kernel<beam::LIST_PAIR, beam::LIST_PAIR>
+          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
+                              H / 256);
+    else if (L.path == PATH_TM2)
+      beam::expert_scan_units_prefill_kernel<beam::LIST_TM2, beam::LIST_PAIR>
           <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
                               H / 256);
     else if (L.path == PATH_MIXED)

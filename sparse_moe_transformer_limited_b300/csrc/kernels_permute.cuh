@@ -208,11 +208,23 @@ __device__ __forceinline__ int4 pair_unit_at(int l, int ex, int r0, int n, int M
   return make_int4(ex, r0 + start, q + (gi < extra ? 1 : 0), m);
 }
 
+// 256-row token-major lists: an expert's n rows go in groups of 256 from its
+// first row (the last group holds the remainder); a unit is {expert, first
+// row, group rows, weight tile}, weight-tile-major (the groups sharing a tile
+// are adjacent): unit l is tile l / g, group l % g, g = ceil(n / 256).
+__device__ __forceinline__ int4 tm2_unit_at(int l, int ex, int r0, int n, int MT) {
+  const int g = (n + 255) >> 8;
+  const int m = l / g, gi = l - m * g;
+  return make_int4(ex, r0 + 256 * gi, min(256, n - 256 * gi), m);
+}
+
 // Work lists for prefill: each GEMM's list in the format of the kernel that
 // runs it (LIST_TM: two-CTA multicast cluster units; LIST_PAIR: 2-SM pair
-// units). Also writes counts, offsets and the per-block row offsets.
+// units; LIST_TM2: 256-row token-major units). Also writes counts, offsets
+// and the per-block row offsets.
 constexpr int LIST_TM = 0;
 constexpr int LIST_PAIR = 1;
+constexpr int LIST_TM2 = 2;
 
 template <int KIND>
 __device__ __forceinline__ int list_units_for(int n, int MT) {
@@ -226,6 +238,8 @@ __device__ __forceinline__ void list_unit(int4* units, int u, int l, int ex, int
     tm_unit_at(l, ex, r0, n, MT, two);
     units[2 * u] = two[0];
     units[2 * u + 1] = two[1];
+  } else if (KIND == LIST_TM2) {
+    units[u] = tm2_unit_at(l, ex, r0, n, MT);
   } else {
     units[u] = pair_unit_at(l, ex, r0, n, MT);
   }

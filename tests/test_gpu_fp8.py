@@ -134,7 +134,7 @@ def test_fp8_forward_routing_edge_cases(B, mode):
     _layer_check(B, wl, d)
 
 
-@pytest.fixture(params=["mixed", "pair", "tm"])
+@pytest.fixture(params=["mixed", "pair", "tm", "tm2"])
 def prefill_gemm(request, monkeypatch):
     """The prefill GEMM kernels (as in the BF16 tests): mixed = gate/up on
     the two-CTA multicast kernel, down on the 2-SM pair kernel."""

@@ -244,11 +244,12 @@ def test_forward_run_to_run(B, T, E, n_group):
 # mean tokens per expert exceeds 24. Covers one and several 256-row groups
 # per expert, the second CTA of a cluster with no rows, several weight tiles
 # in both GEMMs and K loops longer than the shared-memory ring.
-@pytest.fixture(params=["mixed", "pair", "tm"])
+@pytest.fixture(params=["mixed", "pair", "tm", "tm2"])
 def prefill_gemm(request, monkeypatch):
     """The prefill GEMM kernels: by default gate/up on the two-CTA multicast
     kernel and down on the 2-SM pair kernel; BEAM_PREFILL_GEMM=pair or tm runs
-    both GEMMs on one of them."""
+    both GEMMs on one of them; tm2 runs gate/up on the 256-row token-major
+    kernel and down on the pair kernel."""
     if request.param == "mixed":
         monkeypatch.delenv("BEAM_PREFILL_GEMM", raising=False)
     else:

@@ -113,3 +113,37 @@ def test_nvfp4_checkpoint_size():
     assert 2 * u8 == experts
     total = u8 + 2 * bf16 + 4 * f32 + experts // 16
     assert abs(total - 293.63e9) < 0.02e9
+
+
+def test_expert_hand_case_closed_form():
+    """One token through one NVFP4 expert (H = I = 16, one block per row),
+    with operands chosen so that every quantisation is exact: each row's
+    block holds E2M1 grid values times a power of two, and each weight row's
+    block maximum is the matrix maximum over a power of two (block scale 448,
+    224, 112, 56). Only gate/up row 0 and down column 0 are non-zero, so the
+    activation row has one non-zero element, which its own quantisation keeps.
+    Closed form: y_h = bf16(silu(x . Wg[0]) * (x . Wu[0])) * Wd[h, 0]. Swapping
+    gate and up, dropping the BF16 step or transposing W_d changes the value."""
+    import torch
+    H = I = 16
+    x = np.zeros((1, H))
+    x[0, :9] = np.array([6, -4, 3, 0, 2, -1.5, 1, 0.5, -2]) * 0.25
+    wg = np.zeros((I, H))
+    wg[0, :6] = np.array([6, 2, -3, 1, 0.5, -1]) / 16
+    wu = np.zeros((I, H))
+    wu[0, :6] = np.array([1, -1, 0.5, 4, 6, 1.5]) / 8
+    wd = np.zeros((H, I))
+    wd[:6, 0] = np.array([6, -3, 1.5, -6, 0.75, 3]) / 4
+    gq = O.quantize_nvfp4(wg, I)
+    uq = O.quantize_nvfp4(wu, I)
+    dq = O.quantize_nvfp4(wd, H)
+    assert list(O.e4m3_decode(dq[1][:6, 0])) == [448, 224, 112, 448, 56, 224]
+    y = O.swiglu_expert_nvfp4(x, gq, uq, dq)
+    g0 = float(x[0] @ wg[0])
+    u0 = float(x[0] @ wu[0])
+    a0 = g0 / (1.0 + np.exp(-g0)) * u0
+    a0 = float(torch.tensor(a0, dtype=torch.float64).to(torch.bfloat16).to(torch.float64))
+    want = a0 * wd[:, 0]
+    assert np.allclose(y[0], want, rtol=1e-6, atol=1e-12)
+    # the BF16 step is visible at this size
+    assert abs(a0 - g0 / (1.0 + np.exp(-g0)) * u0) > 1e-6 * abs(a0)

@@ -133,3 +133,29 @@ def test_forward_query_row_subset_equals_full():
                                   head_dim=d, window=window, residual_k=5, query_rows=rows)
         assert np.allclose(sub["out"], full["out"][rows], rtol=1e-12, atol=1e-12)
         assert np.allclose(sub["h"], full["h"][rows], rtol=1e-12, atol=1e-12)
+
+
+def test_forward_single_token_closed_form():
+    """T = 1: the softmax has one key, so every head's output is its KV
+    head's value row, whatever q and k are. Closed form:
+    out = bf16(v[kv(h)] * sigmoid(x W_g^T)) W_o^T with x = bf16(RMSNorm(h_in)),
+    v = bf16(x W_v^T) -- it fixes the third block of the fused weight as W_v,
+    the fourth as the gate, the gate's per-channel product with the head
+    outputs, the query-head to KV-head grouping and W_o's orientation."""
+    import torch
+    rng = np.random.default_rng(6)
+    H, nq, nkv, d = 32, 4, 2, 8
+    h_in = rng.standard_normal((1, H))
+    wq, wk, wv, wg = (rng.standard_normal((n * d, H)) * 0.3 for n in (nq, nkv, nkv, nq))
+    wo = rng.standard_normal((H, nq * d)) * 0.3
+    w = np.concatenate([wq, wk, wv, wg])
+    for window in (0, 16):
+        r = O.attention_forward(h_in, w, wo, np.ones(d) * 1.5, np.ones(d) * 0.5, n_q=nq,
+                                n_kv=nkv, head_dim=d, window=window)
+        bf = lambda a: torch.tensor(a, dtype=torch.float64).to(torch.bfloat16).to(torch.float64).numpy()
+        x = bf(h_in / np.sqrt(np.mean(h_in ** 2) + 1e-6))
+        v = bf(x @ wv.T).reshape(nkv, d)
+        heads = np.concatenate([v[hd // (nq // nkv)] for hd in range(nq)])
+        gate = 1.0 / (1.0 + np.exp(-(x @ wg.T)[0]))
+        want = bf(heads * gate) @ wo.T
+        assert np.allclose(r["out"][0], want, rtol=1e-12, atol=1e-12)

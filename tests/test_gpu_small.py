@@ -395,3 +395,32 @@ def test_misaligned_pointer_is_rejected(B):
     with pytest.raises(B.BeamError) as ei:
         B.route(p, xs, d["w_router"])
     assert ei.value.code == 1
+
+
+def test_empty_batch_every_entry_point(B):
+    """T = 0 returns BEAM_OK without launching work for the quantised-expert
+    layers, the dense MLP and the attention sublayer, with a workspace of a
+    few bytes."""
+    base, d = S.make_custom(T=1, H=256, E=256, I=256, n_group=8, topk_group=4, top_k=8,
+                            seed=5, device="cuda")
+    dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    fp8 = tuple(B.quantize_e4m3_rows(d[k]) for k in ("w_gate", "w_up", "w_down"))
+    f4 = tuple(B.quantize_nvfp4(d[k]) for k in ("w_gate", "w_up", "w_down"))
+    assert B.status() == 0, B.last_error()
+    for flag, q, fwd in ((B.FLAG_FP8_EXPERTS, fp8, B.forward_fp8),
+                         (B.FLAG_NVFP4_EXPERTS, f4, B.forward_nvfp4)):
+        p = B.make_params(0, base.H, base.E, base.I, base.n_group, base.topk_group, base.top_k,
+                          base.routed_scale, base.rms_eps, 0, flag)
+        out = torch.empty((0, base.H), dtype=torch.bfloat16, device="cuda")
+        fwd(p, d["x"], d["w_router"], *q, out=out, workspace=dummy)
+        assert B.status() == 0, B.last_error()
+    out = torch.empty((0, base.H), dtype=torch.bfloat16, device="cuda")
+    B.dense_forward(0, base.H, base.I, d["x"], d["w_gate"][0], d["w_up"][0], d["w_down"][0],
+                    out=out, workspace=dummy)
+    assert B.status() == 0, B.last_error()
+    a = S.attn_inputs(1, 256, 4, 2, 3, "cuda", head_dim=128)
+    pa = B.make_attn_params(0, 256, 4, 2, 128, 512, 10000.0, 1e-6, 0, 0)
+    out = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    B.attention_forward(pa, a["x"], a["w_qkvg"], a["w_o"], a["q_gain"], a["k_gain"], out=out,
+                        workspace=dummy)
+    assert B.status() == 0, B.last_error()

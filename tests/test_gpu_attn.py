@@ -97,3 +97,13 @@ def test_attention_full_width(B, window):
     query rows (all keys) against the oracle."""
     rows = np.array([0, 1, 127, 128, 511, 512, 513, 1000, 1500, 2047])
     _check(B, 2048, 5120, 48, 8, window, seed=11 + window, pre_norm=True, residual_k=8, rows=rows)
+
+
+@pytest.mark.parametrize("name,window,k,seed", [("swa", 512, 10, 12), ("global", 0, 12, 13)])
+def test_attention_bench_configuration(B, name, window, k, seed):
+    """The benchmark's attention workloads exactly (T = 8192, hidden 5120,
+    48/8 heads, pre-norm, residual k, the bench's seed and input recipe):
+    sampled query rows -- the first rows, both sides of the window edge and
+    of key tiles, the last row -- against the oracle with every key."""
+    rows = np.array([0, 1, 127, 128, 511, 512, 513, 2047, 4096, 6143, 8000, 8191])
+    _check(B, 8192, 5120, 48, 8, window, seed=seed, pre_norm=True, residual_k=k, rows=rows)

@@ -40,8 +40,11 @@ def B():
     return B
 
 
-def _check(B, T, H, nq, nkv, window, seed, pre_norm=False, residual_k=0, rows=None):
+def _check(B, T, H, nq, nkv, window, seed, pre_norm=False, residual_k=0, rows=None, gain=None):
     d = S.attn_inputs(T, H, nq, nkv, seed, "cuda")
+    if gain is not None:   # constant q and k gains (sets the layer's logit bound)
+        d["q_gain"] = torch.full((128,), gain, dtype=torch.float32, device="cuda")
+        d["k_gain"] = torch.full((128,), gain, dtype=torch.float32, device="cuda")
     flags = (B.FLAG_PRE_NORM if pre_norm else 0) | (0 if residual_k else B.FLAG_FP32_OUT)
     p = B.make_attn_params(T, H, nq, nkv, 128, window, 10000.0, 1e-6, residual_k, flags)
     out = B.attention_forward(p, d["x"], d["w_qkvg"], d["w_o"], d["q_gain"], d["k_gain"])
@@ -107,3 +110,12 @@ def test_attention_bench_configuration(B, name, window, k, seed):
     of key tiles, the last row -- against the oracle with every key."""
     rows = np.array([0, 1, 127, 128, 511, 512, 513, 2047, 4096, 6143, 8000, 8191])
     _check(B, 8192, 5120, 48, 8, window, seed=seed, pre_norm=True, residual_k=k, rows=rows)
+
+
+@pytest.mark.parametrize("gain", [1.68, 3.0])
+@pytest.mark.parametrize("window", [512, 0])
+def test_attention_large_gains(B, gain, window):
+    """Constant q/k gains well above 1 make the logits large and the softmax
+    peaked (|s| up to sqrt(128) * gain^2), so the online reference moves and
+    the O rows are rescaled on many tiles."""
+    _check(B, 700, 256, 4, 2, window, seed=17, gain=gain)

@@ -186,3 +186,41 @@ def test_attn_workspace_and_empty_sequence():
     assert B.attention_workspace_size(B.make_attn_params(T=8192)) > 8192 * 14336 * 4
     p = B.make_attn_params(T=0)
     assert B.lib().beam_attention_forward(ctypes.byref(p), *([None] * 9), 0, None) == 0
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/beam_moe.h compiles as pedantic C99, and a C program links
+    against the library and runs a host-only entry point (argument checks;
+    no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    import sparse_moe_transformer_limited_b300 as pkg
+    from sparse_moe_transformer_limited_b300 import _native
+    lib = _native.LIB_PATH
+    if not os.path.exists(lib):
+        pytest.skip("library not built")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include "beam_moe.h"\n'
+        '#include <stdio.h>\n'
+        'int main(void) {\n'
+        '  beam_moe_params p = {0};\n'
+        '  /* T = 64 but H = 0: rejected on the host */\n'
+        '  p.T = 64; p.E = 256; p.I = 2560;\n'
+        '  beam_status_t s = beam_moe_route(&p, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0);\n'
+        '  printf("%d %s\\n", (int)s, beam_last_error_string());\n'
+        '  return s == BEAM_ERR_INVALID_ARG ? 0 : 1;\n'
+        '}\n')
+    exe = tmp_path / "abi"
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+           "-I", os.path.join(root, "include"), str(src), "-o", str(exe),
+           lib, "-Wl,-rpath," + os.path.dirname(lib)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("1 ")

@@ -339,9 +339,10 @@ size_t beam_attention_workspace_size(const beam_attn_params* p);
 /* Byte offsets of the attention workspace buffers (diagnostic): 0 pre-normed
  * x [T,H] bf16, 1 fused projection [T,(2nq+2nkv)*128] fp32, 2 Q [nq][Tp][128]
  * bf16, 3 K [nkv][Tp][128] bf16, 4 V transposed [nkv][128][Tp] bf16, 5 gate
- * [T][nq*128] fp32, 6 gated attention output [T][nq*128] bf16, 7 output
- * projection [T,H] fp32, 8-10 GEMM work lists and counts; Tp = T rounded up
- * to 128. Writes min(n, 11) entries and returns how many it wrote. */
+ * (empty: the gate logits are read from the fused projection), 6 gated
+ * attention output [T][nq*128] bf16, 7 output projection [T,H] fp32, 8-10
+ * GEMM work lists and counts; Tp = T rounded up to 128. Writes min(n, 11)
+ * entries and returns how many it wrote. */
 int beam_attention_workspace_layout(const beam_attn_params* p, size_t* offsets, int n);
 
 /* Arguments (device pointers, 16-byte aligned):

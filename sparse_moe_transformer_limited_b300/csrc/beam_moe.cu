@@ -1362,7 +1362,7 @@ AttnLayout attn_layout(const beam_attn_params& p) {
   sz[A_Q] = static_cast<size_t>(p.n_q) * L.Tp * beam::ATT_D * 2;
   sz[A_K] = static_cast<size_t>(p.n_kv) * L.Tp * beam::ATT_D * 2;
   sz[A_VT] = static_cast<size_t>(p.n_kv) * beam::ATT_D * L.Tp * 2;
-  sz[A_GATE] = T * dq * 4;
+  sz[A_GATE] = 0;   // (unused: the flash epilogue reads the gate logits from A_PROJ)
   sz[A_ATT] = T * dq * 2;
   sz[A_Y] = T * p.H * 4;
   sz[A_U1] = static_cast<size_t>(L.MT1) * L.groups * 16;
@@ -1464,17 +1464,16 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
   __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_Q]);
   __nv_bfloat16* k = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_K]);
   __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(ws + L.off[A_VT]);
-  float* gate = reinterpret_cast<float*>(ws + L.off[A_GATE]);
+  const float* gate = proj + static_cast<size_t>(nq + 2 * nkv) * beam::ATT_D;  // gate logits
   if (L.Tp > T)
     BEAM_CUDA_TRY(cudaMemset2DAsync(vt + T, static_cast<size_t>(L.Tp) * 2, 0,
                                     static_cast<size_t>(L.Tp - T) * 2,
                                     static_cast<size_t>(nkv) * beam::ATT_D, st));
   {
     ProfScope ps("attn_prep", st);
-    dim3 grid(T, (2 * nq + 2 * nkv + 7) / 8);
+    dim3 grid(T, (nq + nkv + 7) / 8);   // query and key heads
     beam::attn_prep_kernel<<<grid, 256, 0, st>>>(proj, T, L.Tp, nq, nkv, q_gain, k_gain,
-                                                 p->rms_eps, p->window, p->rope_theta, q, k, vt,
-                                                 gate);
+                                                 p->rms_eps, p->window, p->rope_theta, q, k, vt);
     beam::attn_vt_kernel<<<dim3((T + 31) / 32, (nkv + 3) / 4), 128, 0, st>>>(proj, T, L.Tp, nq,
                                                                              nkv, vt);
   }
@@ -1494,6 +1493,7 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
     aa.window = p->window;
     aa.scale = 1.0f / std::sqrt(static_cast<float>(beam::ATT_D));
     aa.gate = gate;
+    aa.gate_ld = (2 * nq + 2 * nkv) * beam::ATT_D;
     aa.out = att;
     aa.timeout_ns = kWaitTimeoutNs;
     if ((s = ensure_smem(reinterpret_cast<const void*>(beam::flash_attn_kernel),

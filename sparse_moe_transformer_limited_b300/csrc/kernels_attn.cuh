@@ -7,8 +7,8 @@
 // projection; section 残差流: RoPE and the query scaling in FP32). Head
 // dimension 128 ("config.json" of the release, head_dim).
 //
-//   attn_prep_kernel       QK-RMSNorm, RoPE or query scale, gate sigmoid,
-//                          from the FP32 fused projection
+//   attn_prep_kernel       QK-RMSNorm, RoPE or query scale, from the FP32
+//                          fused projection
 //   attn_vt_kernel         V transposed (keys contiguous)
 //   linear_units_kernel    work list of a dense GEMM on the 2-SM pair kernel
 //   flash_attn_kernel      softmax(Q K^T / sqrt(128) + mask) V per head on
@@ -36,15 +36,15 @@ constexpr int ATT_BK = 128;      // keys per tile (S's N, P V's K)
 // weight [W_q; W_k; W_v; W_g]).
 //   q[h][t][:] = bf16(rope_or_scale(RMSNorm(q) * q_gain))   [nq][Tp][128]
 //   k[g][t][:] = bf16(rope(RMSNorm(k) * k_gain))            [nkv][Tp][128]
-//   gate[t][h*128 + c] = sigmoid(.)  (FP32)                 [T][nq*128]
-// (value slots are written by attn_vt_kernel)
+// (value slots are written by attn_vt_kernel; the gate's sigmoid is taken
+// by flash_attn_kernel's epilogue straight from the projection)
 // window > 0: RoPE (theta) on q and k; window == 0: q *= (1 + (t+1)/2048)^0.1.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) attn_prep_kernel(
     const float* __restrict__ proj, int T, int Tp, int nq, int nkv,
     const float* __restrict__ q_gain, const float* __restrict__ k_gain, float eps, int window,
     float rope_theta, __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
-    __nv_bfloat16* __restrict__ vt, float* __restrict__ gate) {
+    __nv_bfloat16* __restrict__ vt) {
   const int t = blockIdx.x;
   const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -54,12 +54,6 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(
   float v[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = src[lane + 32 * i];
-  if (slot >= nq + 2 * nkv) {  // gate
-    float* dst = gate + static_cast<size_t>(t) * nq * ATT_D + static_cast<size_t>(slot - nq - 2 * nkv) * ATT_D;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = 1.0f / (1.0f + expf(-v[i]));
-    return;
-  }
   if (slot >= nq + nkv) return;  // values: attn_vt_kernel
   const bool is_q = slot < nq;
   // RMSNorm over the head's 128 channels (FP32), gain per channel
@@ -169,7 +163,8 @@ constexpr int ATT_THREADS = 32 * (3 + ATT_SOFTMAX_WARPS);
 struct AttnArgs {
   int T, Tp, nq, nkv, window;
   float scale;                 // 1 / sqrt(head_dim)
-  const float* gate;           // [T][nq * 128]
+  const float* gate;           // gate logits: row t at gate + t * gate_ld, head h at + h * 128
+  int gate_ld;                 // floats per row of the fused projection
   __nv_bfloat16* out;          // [T][nq * 128]
   unsigned long long timeout_ns;
 };
@@ -534,7 +529,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
     }
-    // final: O / l times the gate, BF16; l summed over all parts. Every
+    // final: O / l times the gate sigmoid(gate logit) (FP32), BF16; l summed
+    // over all parts. Every
     // MMA has completed once mma_done (committed after the last one) has.
     if (ok && ntiles > 0) {
       bool od = false;
@@ -556,7 +552,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
       const bool valid = qi < args.T;
       const size_t ld = static_cast<size_t>(args.nq) * ATT_D;
-      const float* gr = args.gate + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
+      const float* gr = args.gate + static_cast<size_t>(qi) * args.gate_ld + static_cast<size_t>(h) * ATT_D + col0;
       __nv_bfloat16* orow = args.out + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
 #pragma unroll 1
       for (int c = 0; c < ATT_KW; c += 16) {
@@ -570,6 +566,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             const float4 t4 = g4[i];
             gt[4 * i] = t4.x; gt[4 * i + 1] = t4.y; gt[4 * i + 2] = t4.z; gt[4 * i + 3] = t4.w;
           }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) gt[i] = __fdividef(1.0f, 1.0f + __expf(-gt[i]));
           uint4 pk[2];
           __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll

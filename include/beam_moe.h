@@ -338,8 +338,9 @@ size_t beam_attention_workspace_size(const beam_attn_params* p);
 
 /* Byte offsets of the attention workspace buffers (diagnostic): 0 pre-normed
  * x [T,H] bf16, 1 fused projection [T,(2nq+2nkv)*128] fp32, 2 Q [nq][Tp][128]
- * bf16, 3 K [nkv][Tp][128] bf16, 4 V transposed [nkv][128][Tp] bf16, 5 gate
- * (empty: the gate logits are read from the fused projection), 6 gated
+ * bf16, 3 K [nkv][Tp][128] bf16, 4 V transposed [nkv][128][Tp] bf16, 5 RoPE
+ * (cos, sin) table [T][64] fp32 pairs (sliding-window layers; empty for
+ * global ones; the gate logits are read from the fused projection), 6 gated
  * attention output [T][nq*128] bf16, 7 output projection [T,H] fp32, 8-10
  * GEMM work lists and counts; Tp = T rounded up to 128. Writes min(n, 11)
  * entries and returns how many it wrote. */

@@ -381,7 +381,7 @@ def attention_workspace_size(p: AttnParams) -> int:
     return int(n)
 
 
-ATTN_LAYOUT_NAMES = ("x", "proj", "q", "k", "vt", "gate", "attn", "y", "units_qkvg", "units_o",
+ATTN_LAYOUT_NAMES = ("x", "proj", "q", "k", "vt", "rope", "attn", "y", "units_qkvg", "units_o",
                      "n_units")
 
 

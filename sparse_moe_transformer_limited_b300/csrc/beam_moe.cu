@@ -1362,7 +1362,9 @@ AttnLayout attn_layout(const beam_attn_params& p) {
   sz[A_Q] = static_cast<size_t>(p.n_q) * L.Tp * beam::ATT_D * 2;
   sz[A_K] = static_cast<size_t>(p.n_kv) * L.Tp * beam::ATT_D * 2;
   sz[A_VT] = static_cast<size_t>(p.n_kv) * beam::ATT_D * L.Tp * 2;
-  sz[A_GATE] = 0;   // (unused: the flash epilogue reads the gate logits from A_PROJ)
+  // RoPE (cos, sin) table of the sliding-window layers (the gate logits are
+  // read from A_PROJ by the flash epilogue)
+  sz[A_GATE] = p.window > 0 ? T * (beam::ATT_D / 2) * sizeof(float2) : 0;
   sz[A_ATT] = T * dq * 2;
   sz[A_Y] = T * p.H * 4;
   sz[A_U1] = static_cast<size_t>(L.MT1) * L.groups * 16;
@@ -1471,9 +1473,14 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
                                     static_cast<size_t>(nkv) * beam::ATT_D, st));
   {
     ProfScope ps("attn_prep", st);
+    float2* rope_cs = reinterpret_cast<float2*>(ws + L.off[A_GATE]);
+    if (p->window > 0) {
+      const int n = T * (beam::ATT_D / 2);
+      beam::rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(T, p->rope_theta, rope_cs);
+    }
     dim3 grid(T, (nq + nkv + 7) / 8);   // query and key heads
     beam::attn_prep_kernel<<<grid, 256, 0, st>>>(proj, T, L.Tp, nq, nkv, q_gain, k_gain,
-                                                 p->rms_eps, p->window, p->rope_theta, q, k, vt);
+                                                 p->rms_eps, p->window, rope_cs, q, k, vt);
     beam::attn_vt_kernel<<<dim3((T + 31) / 32, (nkv + 3) / 4), 128, 0, st>>>(proj, T, L.Tp, nq,
                                                                              nkv, vt);
   }

@@ -43,8 +43,8 @@ constexpr int ATT_BK = 128;      // keys per tile (S's N, P V's K)
 __global__ void __launch_bounds__(256) attn_prep_kernel(
     const float* __restrict__ proj, int T, int Tp, int nq, int nkv,
     const float* __restrict__ q_gain, const float* __restrict__ k_gain, float eps, int window,
-    float rope_theta, __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
-    __nv_bfloat16* __restrict__ vt) {
+    const float2* __restrict__ rope_cs, __nv_bfloat16* __restrict__ q,
+    __nv_bfloat16* __restrict__ k, __nv_bfloat16* __restrict__ vt) {
   const int t = blockIdx.x;
   const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -67,16 +67,15 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] *= r * (gn ? gn[lane + 32 * i] : 1.f);
   if (window > 0) {
-    // rotate-half RoPE: pairs (c, c + 64) for c = lane and lane + 32
+    // rotate-half RoPE: pairs (c, c + 64) for c = lane and lane + 32, the
+    // (cos, sin) of token t and pair c from rope_table_kernel
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int c = lane + 32 * i;
-      const float inv_freq = powf(rope_theta, -2.0f * static_cast<float>(c) / static_cast<float>(ATT_D));
-      float sn, cs;
-      sincosf(static_cast<float>(t) * inv_freq, &sn, &cs);
+      const float2 r = rope_cs[static_cast<size_t>(t) * (ATT_D / 2) + c];
       const float x1 = v[i], x2 = v[i + 2];
-      v[i] = x1 * cs - x2 * sn;
-      v[i + 2] = x2 * cs + x1 * sn;
+      v[i] = x1 * r.x - x2 * r.y;
+      v[i + 2] = x2 * r.x + x1 * r.y;
     }
   } else if (is_q) {
     const float s = powf(1.0f + (static_cast<float>(t) + 1.0f) / 2048.0f, 0.1f);
@@ -87,6 +86,18 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(
                             : k + (static_cast<size_t>(slot - nq) * Tp + t) * ATT_D;
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = __float2bfloat16_rn(v[i]);
+}
+
+// RoPE (cos, sin) of every token t and channel pair c (0..63): angle
+// t * theta^(-2c/128) in FP32, shared by all query and key heads.
+__global__ void rope_table_kernel(int T, float rope_theta, float2* __restrict__ cs) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * (ATT_D / 2)) return;
+  const int t = i / (ATT_D / 2), c = i % (ATT_D / 2);
+  const float inv_freq = powf(rope_theta, -2.0f * static_cast<float>(c) / static_cast<float>(ATT_D));
+  float sn, co;
+  sincosf(static_cast<float>(t) * inv_freq, &sn, &co);
+  cs[i] = make_float2(co, sn);
 }
 
 // V transposed, keys contiguous: vt[g][c][t] = bf16(v[t][g][c]). One lane

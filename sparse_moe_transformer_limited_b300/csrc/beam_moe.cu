@@ -532,7 +532,8 @@ struct QuantBufs {
 // Steps 3-4: gate/up GEMM + SwiGLU into act (bf16), then the down GEMM into
 // the per-pair FP32 outputs y. E4M3 / NVFP4: the expert-ordered x (xop) and
 // the weights are quantised; act is quantised per row (into q.aq) before
-// the down GEMM. NVFP4 runs on the weight-major kernels only.
+// the down GEMM. NVFP4 runs on the weight-major kernel at decode and on the
+// token-major kernel (both GEMMs) for many tokens.
 template <int KIND>
 beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
                                   const ExpertWeights& w, const void* xop, const QuantBufs& q,

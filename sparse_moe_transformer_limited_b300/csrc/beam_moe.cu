@@ -763,7 +763,15 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   const long long Rl = f4 ? L.rows : R;
 
   const int NB = dense ? 1 : L.NB;
-  if (dense) {
+  // one permutation block and a token-tile work list (decode): histogram,
+  // scan and scatter in one launch
+  const bool small = !dense && L.NB == 1 && (L.path == PATH_W32 || L.path == PATH_W128);
+  if (small) {
+    ProfScope ps("expert_permute", st);
+    beam::expert_permute_small_kernel<<<1, 256, 0, st>>>(
+        idx, wts, T, K, E, counts, offs, ugu, nunits, L.NT, I / 128, path_mt_down(L.path, H),
+        L.pad, pair_row, row_tok, row_w);
+  } else if (dense) {
     ProfScope ps("dense_setup", st);
     beam::dense_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, blk_hist, pair_row, row_tok,
                                                               row_w, wts);
@@ -772,7 +780,7 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     beam::expert_block_hist_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(idx, T, K, E, blk_hist);
   }
   BEAM_LAUNCH_CHECK("expert_block_hist_kernel");
-  {
+  if (!small) {
     ProfScope ps("expert_scan_units", st);
     if (L.path == PATH_PAIR)
       beam::expert_scan_units_prefill_kernel<beam::LIST_PAIR, beam::LIST_PAIR>
@@ -798,7 +806,7 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
   if (quant) {
     // quantise x per token, gathered into expert order (identity when dense)
-    if (!dense) {
+    if (!dense && !small) {
       ProfScope ps("expert_scatter", st);
       beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(
           idx, wts, T, K, E, blk_off, pair_row, row_tok, row_w);
@@ -818,7 +826,7 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   } else if (dense) {
     xperm = const_cast<__nv_bfloat16*>(x);  // identity permutation: read x in place
   } else {
-    {
+    if (!small) {
       ProfScope ps("expert_scatter", st);
       beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(
           idx, wts, T, K, E, blk_off, pair_row, row_tok, row_w);

@@ -322,6 +322,74 @@ __global__ void __launch_bounds__(256) expert_scan_units_prefill_kernel(
   }
 }
 
+// At most PERM_TPB tokens (one permutation block): the histogram, the scan
+// with the token-tile work list and the scatter of expert_block_hist_kernel,
+// expert_scan_units_kernel and expert_scatter_kernel in one launch of one
+// block of 256 threads, with the same outputs (blk_hist / blk_off are not
+// needed and not written).
+__global__ void __launch_bounds__(256) expert_permute_small_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ wts, int T, int top_k, int E,
+    int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ tiles,
+    int* __restrict__ n_units, int NT, int MT_gu, int MT_dn, int pad,
+    int* __restrict__ pair_row, int* __restrict__ row_token, float* __restrict__ row_weight) {
+  __shared__ int s_e[PERM_TPB * 32];
+  __shared__ int s_cnt[256];
+  __shared__ int s_off[256];
+  __shared__ int s_order[256];
+  __shared__ int s_warp[8];
+  const int e = threadIdx.x;
+  const int np = T * top_k;
+  s_cnt[e] = 0;
+  __syncthreads();
+  for (int p = e; p < np; p += blockDim.x) {
+    const int x = idx[p];
+    s_e[p] = x;
+    atomicAdd(&s_cnt[x], 1);
+  }
+  __syncthreads();
+  const int c = s_cnt[e];                 // 0 for e >= E
+  int total = 0;
+  const int cpad = (c + pad - 1) / pad * pad;
+  const int off = block_exclusive_scan256(e < E ? cpad : 0, s_warp, &total);
+  s_off[e] = off;
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = off;
+    if (e == 0) offsets[E] = total;
+    for (int r = off + c; r < off + cpad; ++r) row_token[r] = -1;
+    int rank = 0;
+    for (int j = 0; j < E; ++j) rank += (s_cnt[j] > c) || (s_cnt[j] == c && j < e);
+    s_order[rank] = e;
+  }
+  __syncthreads();
+  // token-tile work list, experts by token count (descending, ties to the
+  // lower index)
+  const int ex = e < E ? s_order[e] : 0;
+  const int n = e < E ? s_cnt[ex] : 0;
+  const int nt = (n + NT - 1) / NT;
+  int ntiles = 0;
+  const int tb = block_exclusive_scan256(nt, s_warp, &ntiles);
+  if (e == 0) {
+    n_units[0] = ntiles * MT_gu;
+    n_units[1] = ntiles * MT_dn;
+    n_units[2] = ntiles;
+    n_units[3] = 0;
+  }
+  const int r0 = s_off[ex];
+  for (int j = 0; j < nt; ++j) tiles[tb + j] = make_int4(ex, r0 + j * NT, min(NT, n - j * NT), 0);
+  // pair p's row: its expert's first row plus its stable rank among the
+  // expert's pairs
+  for (int p = e; p < np; p += blockDim.x) {
+    const int x = s_e[p];
+    int r = 0;
+    for (int q = 0; q < p; ++q) r += (s_e[q] == x);
+    const int row = s_off[x] + r;
+    pair_row[p] = row;
+    row_token[row] = p / top_k;
+    row_weight[row] = wts[p];
+  }
+}
+
 // Row of every pair of this block in the expert-ordered layout: pair_row[p],
 // and the inverse maps row_token / row_weight.
 __global__ void __launch_bounds__(PERM_THREADS) expert_scatter_kernel(

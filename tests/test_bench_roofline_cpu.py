@@ -1,0 +1,54 @@
+"""The algorithmic work behind bench.py's roofline figures, against closed
+forms: expert FLOPs = T * top_k * 6 * H * I (T * 629,145,600 at the Beam
+shapes), weight bytes = touched experts * 3 * H * I * bytes per weight
+(78,643,200 per BF16 expert), plus the layer's BF16 input and output. No GPU
+needed."""
+import numpy as np
+import pytest
+
+import beam_synth as S
+
+
+@pytest.fixture(scope="module")
+def bench():
+    import bench as b
+    return b
+
+
+def _counts(E, touched):
+    c = np.zeros(E, dtype=np.int64)
+    c[:touched] = 3
+    return c
+
+
+def test_decode_bf16_closed_forms(bench):
+    wl = S.WORKLOADS["decode"]
+    a = bench._algorithmic(wl, _counts(wl.E, 220), "bf16")
+    assert a["touched"] == 220
+    # gate and up of 220 experts once, plus x: the bench's decode figure
+    assert a["gu_bytes"] == 220 * 2 * 2560 * 5120 * 2 + 64 * 5120 * 2 == 11_534_991_360
+    assert a["dn_bytes"] == 220 * 5120 * 2560 * 2 + 64 * 5120 * 2
+    assert a["gu_flops"] + a["dn_flops"] == 64 * 629_145_600
+    # the whole layer: 78.64 MB per touched expert, x in and h out, the FP32 router
+    assert a["layer_bytes"] == 220 * 78_643_200 + 2 * 64 * 5120 * 2 + 256 * 5120 * 4
+    assert a["layer_flops"] == 64 * 629_145_600 + 2 * 64 * 5120 * 256
+
+
+def test_prefill_flops_scale_with_tokens(bench):
+    wl = S.WORKLOADS["prefill"]
+    a = bench._algorithmic(wl, _counts(wl.E, wl.E), "bf16")
+    assert a["gu_flops"] == 2 * (8192 * 8) * 2 * 2560 * 5120 == 3_435_973_836_800
+    assert a["gu_flops"] + a["dn_flops"] == 8192 * 629_145_600
+
+
+@pytest.mark.parametrize("kind,per_weight,per_row", [("fp8", 1.0, 4), ("nvfp4", 0.5 + 1 / 16, 0)])
+def test_quantised_weight_bytes(bench, kind, per_weight, per_row):
+    """E4M3: one byte per weight and an FP32 scale per output row; NVFP4: half
+    a byte per weight and one E4M3 block scale per 16 weights."""
+    wl = S.WORKLOADS["decode"]
+    a = bench._algorithmic(wl, _counts(wl.E, 100), kind)
+    want_gu = int(100 * 2 * 2560 * (5120 * per_weight + per_row)) + 64 * 5120 * 2
+    assert a["gu_bytes"] == want_gu
+    # FLOPs do not depend on the weight format
+    b = bench._algorithmic(wl, _counts(wl.E, 100), "bf16")
+    assert a["gu_flops"] == b["gu_flops"] and a["dn_flops"] == b["dn_flops"]

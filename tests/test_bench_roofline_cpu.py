@@ -52,3 +52,20 @@ def test_quantised_weight_bytes(bench, kind, per_weight, per_row):
     # FLOPs do not depend on the weight format
     b = bench._algorithmic(wl, _counts(wl.E, 100), "bf16")
     assert a["gu_flops"] == b["gu_flops"] and a["dn_flops"] == b["dn_flops"]
+
+
+def test_peaks_come_from_the_measured_file(bench, tmp_path, monkeypatch):
+    """The roofline denominators are MEASURED_PEAKS.json's figures when the
+    file is there (source "measured") and the stated fallback otherwise."""
+    import json
+    import os
+    path = os.path.join(bench.ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            want = json.load(f)
+        p = bench._peaks()
+        assert p["source"] == "measured"
+        assert p["hbm"] == float(want["hbm_gbs"]) and p["bf16"] == float(want["bf16_tflops"])
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    p = bench._peaks()
+    assert p["source"] == "fallback" and p["hbm"] == 6400.0 and p["bf16"] == 1800.0

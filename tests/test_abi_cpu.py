@@ -224,3 +224,40 @@ def test_header_is_plain_c_and_links(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("1 ")
+
+
+def _list_bytes(lay):
+    """Sizes of the gate/up and down work lists (entries are 1 KB aligned)."""
+    return lay["units_dn"] - lay["units_gu"], lay["pair_row"] - lay["units_dn"]
+
+
+def _kb(nbytes):
+    return (nbytes + 1023) // 1024 * 1024
+
+
+@pytest.mark.parametrize("env,flags,T,want_gu,want_dn", [
+    # decode, 512 pairs <= 24 per expert: weight-major token tiles of 32;
+    # one list of (512/32 + E) tiles, expanded by the I/128 gate/up and H/128
+    # down weight tiles
+    (None, 0, 64, 16 * (16 + 256) * 20, 16 * (16 + 256) * 40),
+    # prefill BF16: two-CTA cluster units for gate/up (two int4 each), 2-SM
+    # pair units for down; groups = 65536/256 + E
+    (None, 0, 8192, 16 * 2 * (512 * 20 + 256 * 11), 16 * 512 * 20),
+    ("pair", 0, 8192, 16 * 512 * 20, 16 * 512 * 20),
+    ("tm2", 0, 8192, 16 * 512 * 20, 16 * 512 * 20),
+    # prefill NVFP4: both GEMMs on the cluster kernel
+    (None, "nvfp4", 8192, 16 * 2 * (512 * 20 + 256 * 11), 16 * 2 * (512 * 20 + 256 * 11)),
+    # NVFP4 on the weight-major kernel: 128-token tiles
+    ("w128", "nvfp4", 8192, 16 * (512 + 256) * 20, 16 * (512 + 256) * 40),
+])
+def test_gemm_regime_follows_tokens_and_switch(monkeypatch, env, flags, T, want_gu, want_dn):
+    """The expert-GEMM regime is chosen on the host from tokens per expert and
+    the BEAM_PREFILL_GEMM switch; each regime's work-list format fixes the
+    size of its workspace entries (read here without a GPU)."""
+    if env is None:
+        monkeypatch.delenv("BEAM_PREFILL_GEMM", raising=False)
+    else:
+        monkeypatch.setenv("BEAM_PREFILL_GEMM", env)
+    f = B.FLAG_NVFP4_EXPERTS if flags == "nvfp4" else 0
+    gu, dn = _list_bytes(B.workspace_layout(_p(T=T, flags=f)))
+    assert (gu, dn) == (_kb(want_gu), _kb(want_dn))

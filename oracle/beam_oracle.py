@@ -16,8 +16,8 @@ Sources (release pages about the model, cited by title and section):
        section "config.json 里还有六处能直接抄的细节" (n_group 8,
        topk_group 4, norm_topk_prob true, routed_scaling_factor 2.5).
 
-Readings where the pages leave a step open (each is also listed in the
-design notes):
+Readings where the pages leave a step open (the E4M3, NVFP4 and attention
+sections below list their own):
   * scaling: the combine weights are multiplied by 2.5 ([P1] 专家混合模型,
     [P5] routed_scaling_factor); [P3] "缩小为 2.5" is a garbled translation.
   * normalisation divides by the sum of the 8 selected sigmoid scores, with
@@ -38,9 +38,10 @@ design notes):
 Everything is FP64 except the FP32 rounding of the router scores (above) and
 the BF16 rounding of the pre-norm output.
 
-Every function has a pin in tests/test_oracle_pins.py that checks it against
-something other than itself (closed forms, hand-worked examples, brute force
-and library routines).
+Every function has a pin -- tests/test_oracle_pins.py, test_oracle_fp8_pins.py,
+test_oracle_nvfp4_pins.py and test_oracle_attn_pins.py -- that checks it
+against something other than itself (closed forms, hand-worked examples,
+brute force, exactly representable cases and library routines).
 """
 from __future__ import annotations
 

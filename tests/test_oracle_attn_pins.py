@@ -159,3 +159,67 @@ def test_forward_single_token_closed_form():
         gate = 1.0 / (1.0 + np.exp(-(x @ wg.T)[0]))
         want = bf(heads * gate) @ wo.T
         assert np.allclose(r["out"][0], want, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_global_query_scale_follows_the_norms():
+    """Global layer: q = (1 + (pos+1)/2048)^0.1 * RMSNorm(x W_q^T) * q_gain
+    and k = RMSNorm(x W_k^T) * k_gain, per head. With q_gain = 2 and
+    k_gain = 1/2 the RMS over a head's channels is 2 * scale(pos) for
+    queries and 1/2 for keys, up to BF16 rounding (relative 2^-9): at
+    position 2047 the scale is 2^0.1, so a scale applied before the norm,
+    or the key gain used for queries, is far off."""
+    rng = np.random.default_rng(16)
+    T, H, nq, nkv, d = 2048, 32, 2, 1, 16
+    w = rng.standard_normal(((nq + 2 * nkv + nq) * d, H)) * 0.3
+    wo = rng.standard_normal((H, nq * d)) * 0.3
+    rows = np.array([0, 1023, 2047])
+    r = O.attention_forward(rng.standard_normal((T, H)), w, wo, np.full(d, 2.0), np.full(d, 0.5),
+                            n_q=nq, n_kv=nkv, head_dim=d, window=0, query_rows=rows)
+    rms_q = np.sqrt(np.mean(r["q"] ** 2, axis=-1))               # [nq, rows]
+    want = 2.0 * (1.0 + (rows + 1.0) / 2048.0) ** 0.1
+    assert np.allclose(rms_q, want[None, :], rtol=2.0 ** -8, atol=0)
+    assert np.allclose(np.sqrt(np.mean(r["k"] ** 2, axis=-1)), 0.5, rtol=2.0 ** -8, atol=0)
+
+
+def test_forward_rope_acts_after_the_norm_gains():
+    """Sliding layer, every token the same input row: before RoPE the
+    normalised, gained q and k are the same at every position, and RoPE only
+    turns each (i, i + d/2) pair, so each pair's length is the same at every
+    position (up to BF16 rounding). The gains differ between the two halves
+    (1 and 2), so a norm or gain applied after the rotation would change the
+    pair lengths with the position."""
+    rng = np.random.default_rng(17)
+    T, H, nq, nkv, d = 12, 32, 2, 1, 16
+    w = rng.standard_normal(((nq + 2 * nkv + nq) * d, H)) * 0.3
+    wo = rng.standard_normal((H, nq * d)) * 0.3
+    h_in = np.tile(rng.standard_normal((1, H)), (T, 1))
+    g_q = np.concatenate([np.ones(d // 2), np.full(d // 2, 2.0)])
+    r = O.attention_forward(h_in, w, wo, g_q, g_q[::-1].copy(), n_q=nq, n_kv=nkv, head_dim=d,
+                            window=8)
+    for a in (r["q"], r["k"]):
+        pair = np.sqrt(a[..., : d // 2] ** 2 + a[..., d // 2:] ** 2)   # [heads, T, d/2]
+        assert np.allclose(pair, pair[:, :1, :], rtol=2.0 ** -7, atol=0)
+
+
+def test_forward_gains_and_residual_branch():
+    """The pre-norm gain scales each channel of the BF16 input x exactly
+    (powers of two); the post-norm gain scales the branch
+    h_k - sqrt((k-1)/k) h_{k-1}; and with W_o = 0 the output is 0, so
+    h_k = sqrt((k-1)/k) h_{k-1} with h_{k-1} the layer input itself (RMS 4
+    here, so not its normalised copy)."""
+    rng = np.random.default_rng(19)
+    T, H, nq, nkv, d, k = 10, 32, 2, 1, 16, 7
+    w = rng.standard_normal(((nq + 2 * nkv + nq) * d, H)) * 0.3
+    wo = rng.standard_normal((H, nq * d)) * 0.3
+    h = rng.standard_normal((T, H)) * 4.0
+    g = np.tile([0.5, 1.0, 2.0, 4.0], H // 4)
+    run = lambda wo_, pg, qg: O.attention_forward(h, w, wo_, np.ones(d), np.ones(d), n_q=nq,
+                                                  n_kv=nkv, head_dim=d, window=4, pre_gain=pg,
+                                                  residual_k=k, post_gain=qg)
+    base, pre, post = run(wo, None, None), run(wo, g, None), run(wo, None, g)
+    assert np.array_equal(pre["x"], base["x"] * g[None, :])
+    keep = math.sqrt((k - 1) / k) * h
+    assert np.allclose(post["h"] - keep, (base["h"] - keep) * g[None, :], rtol=1e-13, atol=1e-13)
+    zero = run(np.zeros_like(wo), None, None)
+    assert np.array_equal(zero["out"], np.zeros((T, H)))
+    assert np.allclose(zero["h"], keep, rtol=1e-15, atol=0)

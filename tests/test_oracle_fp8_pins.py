@@ -124,6 +124,53 @@ def test_fp8_expert_hand_case():
     assert not np.allclose(y[0], a * np.array([0.875, 1.75]), rtol=1e-4, atol=0)   # BF16 step matters
 
 
+def test_fp8_activation_is_quantised_per_row():
+    """x is quantised per row before the gate/up products. Row 1: amax 448,
+    scale 1, and 1.03125 (= 1 + 2^-5, between E4M3 grid points 1 and 1.125)
+    rounds to 1. Row 2 is row 1 halved: scale 1/2, the same codes, values
+    224 and 0.5. Gate and up weights read element 1 with code 0x38 (= 1.0)
+    and scale 1, so g = u = the quantised element: 1 and 0.5."""
+    x = np.array([[448.0, 1.03125], [224.0, 0.515625]])
+    one = (np.array([[0x00, 0x38]], dtype=np.uint8), np.array([1.0], dtype=np.float32))
+    a = O.swiglu_act_fp8(x, one, one)
+    silu = lambda z: z / (1.0 + math.exp(-z))
+    assert np.allclose(a[:, 0], [silu(1.0) * 1.0, silu(0.5) * 0.5], rtol=1e-15, atol=0)
+
+
+def test_fp8_forward_residual_keeps_the_layer_input():
+    """All-zero FP8 experts (codes 0, scale 1) give out = 0 and
+    h_k = sqrt((k-1)/k) * h_{k-1} exactly, with h_{k-1} the layer input
+    rather than its pre-normed copy."""
+    rng = np.random.default_rng(15)
+    T, H, E, I, k = 4, 32, 8, 4, 9
+    h = rng.normal(size=(T, H)) * 5.0
+    zq = tuple(O.quantize_rows_e4m3(np.zeros(shape)) for shape in ((I, H), (I, H), (H, I)))
+    r = O.moe_forward_fp8(h, rng.normal(size=(E, H)), None, lambda e: zq, n_group=2,
+                          topk_group=1, top_k=2, pre_norm=True, residual_k=k)
+    assert np.array_equal(r["out"], np.zeros((T, H)))
+    assert np.allclose(r["h"], math.sqrt((k - 1) / k) * h, rtol=1e-15, atol=0)
+
+
+def test_fp8_forward_gains():
+    """Pre- and post-norm gains of powers of two in the FP8 sublayer: the
+    BF16 pre-norm output scales exactly per channel and the post-norm branch
+    h_k - sqrt((k-1)/k) h_{k-1} scales by the post-norm gain."""
+    rng = np.random.default_rng(20)
+    T, H, E, I, k = 4, 32, 8, 8, 5
+    h = rng.normal(size=(T, H)) * 2.0
+    wr = rng.normal(size=(E, H))
+    Q = [tuple(O.quantize_rows_e4m3(rng.normal(size=s) * 0.2) for s in ((I, H), (I, H), (H, I)))
+         for _ in range(E)]
+    g = np.tile([0.5, 1.0, 2.0, 4.0], H // 4)
+    run = lambda pg, qg: O.moe_forward_fp8(h, wr, None, lambda e: Q[e], n_group=2, topk_group=1,
+                                           top_k=2, pre_norm=True, pre_gain=pg, residual_k=k,
+                                           post_gain=qg)
+    base, pre, post = run(None, None), run(g, None), run(None, g)
+    assert np.array_equal(pre["x"], base["x"] * g[None, :])
+    keep = math.sqrt((k - 1) / k) * h
+    assert np.allclose(post["h"] - keep, (base["h"] - keep) * g[None, :], rtol=1e-13, atol=1e-13)
+
+
 def test_fp8_forward_close_to_bf16_forward():
     # FP8 weights and activations stay within E4M3's relative precision of
     # the unquantised sublayer (a wrong scale or operand would be far off)

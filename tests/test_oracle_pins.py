@@ -335,6 +335,74 @@ def test_prenorm_rounds_to_bf16():
     assert np.array_equal(r["x"], want)
 
 
+def test_forward_residual_keeps_the_layer_input():
+    """With every expert weight zero the MoE output is exactly 0, RMSNorm(0)
+    is 0, and the step leaves h_k = sqrt((k-1)/k) * h_{k-1}: the residual
+    branch carries the layer input itself, not its pre-normed copy (the
+    input's RMS is 7 here, so the two differ)."""
+    rng = np.random.default_rng(13)
+    T, H, E, I, k = 5, 32, 8, 4, 11
+    h = rng.normal(size=(T, H)) * 7.0
+    zero = (np.zeros((I, H)), np.zeros((I, H)), np.zeros((H, I)))
+    r = O.moe_forward(h, rng.normal(size=(E, H)), None, lambda e: zero, n_group=2,
+                      topk_group=1, top_k=2, pre_norm=True, residual_k=k)
+    assert np.array_equal(r["out"], np.zeros((T, H)))
+    assert np.allclose(r["h"], math.sqrt((k - 1) / k) * h, rtol=1e-15, atol=0)
+
+
+def test_prenorm_gain_scales_each_channel():
+    """A pre-norm gain of powers of two scales each channel of the BF16
+    pre-norm output exactly (BF16 rounding commutes with a power-of-two
+    factor), and the router then sees the scaled x."""
+    rng = np.random.default_rng(14)
+    T, H, E = 6, 32, 8
+    h = rng.normal(size=(T, H)) * 3.0
+    g = np.tile([0.5, 1.0, 2.0, 4.0], H // 4)
+    zero = (np.zeros((2, H)), np.zeros((2, H)), np.zeros((H, 2)))
+    kw = dict(n_group=1, topk_group=1, top_k=2, pre_norm=True)
+    wr = rng.normal(size=(E, H))
+    plain = O.moe_forward(h, wr, None, lambda e: zero, **kw)
+    gained = O.moe_forward(h, wr, None, lambda e: zero, pre_gain=g, **kw)
+    assert np.array_equal(gained["x"], plain["x"] * g[None, :])
+    assert np.allclose(gained["sel"]["s64"], 1.0 / (1.0 + np.exp(-(plain["x"] * g) @ wr.T)),
+                       rtol=1e-14, atol=0)
+
+
+def test_residual_step_post_gain_hand_case():
+    """h_{k-1} = 0, sub-layer output 3 in every channel: RMSNorm gives
+    3 / sqrt(9 + eps) per channel, times the gain, times 1/sqrt(4)."""
+    g = np.array([1.0, 2.0, 0.5, -1.0])
+    h = O.residual_step(np.zeros((1, 4)), np.full((1, 4), 3.0), 4, gain=g)
+    assert np.allclose(h[0], 0.5 * 3.0 / math.sqrt(9.0 + 1e-6) * g, rtol=1e-15, atol=0)
+
+
+def _check_gains(run, h, k):
+    """run(pre_gain, post_gain) -> result dict with x and h. With per-channel
+    powers of two as gains, the BF16 pre-norm output scales exactly, channel
+    by channel, and the post-norm branch h_k - sqrt((k-1)/k) h_{k-1} scales
+    by the post-norm gain."""
+    g = np.tile([0.5, 1.0, 2.0, 4.0], h.shape[1] // 4)
+    base, pre, post = run(None, None), run(g, None), run(None, g)
+    assert np.array_equal(pre["x"], base["x"] * g[None, :])
+    keep = math.sqrt((k - 1) / k) * h
+    assert np.allclose(post["h"] - keep, (base["h"] - keep) * g[None, :], rtol=1e-13, atol=1e-13)
+    assert not np.allclose(post["h"], base["h"])
+
+
+def test_gains_reach_the_moe_and_dense_sublayers():
+    rng = np.random.default_rng(18)
+    T, H, E, I = 5, 32, 8, 8
+    h = rng.normal(size=(T, H)) * 2.0
+    wr = rng.normal(size=(E, H))
+    W = [tuple(rng.normal(size=s) * 0.2 for s in ((I, H), (I, H), (H, I))) for _ in range(E)]
+    k = 6
+    _check_gains(lambda pg, qg: O.moe_forward(
+        h, wr, None, lambda e: W[e], n_group=2, topk_group=1, top_k=2, pre_norm=True,
+        pre_gain=pg, residual_k=k, post_gain=qg), h, k)
+    _check_gains(lambda pg, qg: O.dense_mlp_forward(
+        h, *W[0], pre_norm=True, pre_gain=pg, residual_k=k, post_gain=qg), h, k)
+
+
 # --------------------------------------------------------------------------
 # page facts
 # --------------------------------------------------------------------------

@@ -160,6 +160,25 @@ MUTANTS = {
                                   "rms_norm(h_in, None, eps)"),
     "attn_post_gain_dropped": ("attention_forward", "residual_k, post_gain, eps",
                                "residual_k, None, eps"),
+    "bf16_mask_drops_bit": ('bf16_round', 'np.uint64(0xFFFF0000)', 'np.uint64(0xFFFE0000)'),
+    "group_margin_wrong_rank": ('group_limited_topk', 'gorder[topk_group - 1]', 'gorder[topk_group - 2]'),
+    "topk_margin_wrong_rank": ('group_limited_topk', 'corder[top_k - 1]', 'corder[top_k - 2]'),
+    "e4m3_sign_dropped": ('e4m3_round', 'return np.copysign(r, v)', 'return r'),
+    "e4m3_encode_subnormal_step": ('e4m3_encode', 'm_sub = a / 2.0 ** -9', 'm_sub = a / 2.0 ** -10'),
+    "e4m3_top_binade_is_nan": ('_e4m3_value', '(e == 15) & (m == 7)', '(e == 15)'),
+    "nvfp4_group_scales_tiled": ('quantize_nvfp4', 'np.repeat(g, rows_per_group)', 'np.tile(g, rows_per_group)'),
+    "nvfp4_multiplies_by_scale": ('quantize_nvfp4', 'F32(1.0) / np.where(sb_val > 0, denom, F32(1.0))', 'np.where(sb_val > 0, denom, F32(1.0))'),
+    "nvfp4_dequant_group_tiled": ('dequantize_nvfp4', 'np.repeat(np.asarray(group_scales, dtype=F64), rows_per_group)', 'np.tile(np.asarray(group_scales, dtype=F64), rows_per_group)'),
+    "nvfp4_x_not_quantised": ('swiglu_act_nvfp4', 'xd = dequantize_nvfp4(*quantize_nvfp4(x_rows, 1), 1)', 'xd = np.asarray(x_rows, dtype=F64)'),
+    "nvfp4_act_not_quantised": ('swiglu_expert_nvfp4', 'ad = dequantize_nvfp4(*quantize_nvfp4(a, 1), 1)', 'ad = np.asarray(a, dtype=F64)'),
+    "fp8_act_not_quantised": ('swiglu_expert_fp8', 'return dequantize_rows_e4m3(qa, sa) @', 'return np.asarray(a, dtype=F64) @'),
+    "softmax_normalised_over_queries": ('attention_core', 'p / p.sum(axis=1, keepdims=True)', 'p / p.sum(axis=0, keepdims=True)'),
+    "query_scale_relative_rows": ('attention_forward', 'global_query_scale(rows)', 'global_query_scale(np.arange(len(rows)))'),
+    "gate_after_rounding": ('attention_forward', 'bf16_round(o.transpose(1, 0, 2).reshape(len(rows), dq) * gate)', 'bf16_round(o.transpose(1, 0, 2).reshape(len(rows), dq)) * gate'),
+    "forward_ignores_window": ('attention_forward', 'attention_core(q, k, v, window, q_pos=rows)', 'attention_core(q, k, v, 0, q_pos=rows)'),
+    "v_not_rounded": ("attention_forward", "q, k, v = (bf16_round(a).astype(F64) for a in (q, k, v))",
+                      "q, k = (bf16_round(a).astype(F64) for a in (q, k))"),
+    "residual_allows_k1": ('residual_coeffs', 'if k < 2:', 'if k < 1:'),
 }
 
 

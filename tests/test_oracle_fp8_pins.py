@@ -137,6 +137,21 @@ def test_fp8_activation_is_quantised_per_row():
     assert np.allclose(a[:, 0], [silu(1.0) * 1.0, silu(0.5) * 0.5], rtol=1e-15, atol=0)
 
 
+def test_fp8_activation_row_quantised_before_down_projection():
+    """x = [4, 1]: scale 1/112, codes 448 and 112 (both on the grid), so the
+    expert sees x exactly. Identity gate/up rows (code 0x38 = 1, scale 1)
+    give g = u = [4, 1]; A = bf16(silu(g) * u) = [3.921875, 0.73046875].
+    A's row is quantised with inv = fp32(448 / 3.921875): element 1 becomes
+    83.44..., whose nearest E4M3 values are 80 and 88, so it is coded 80
+    and comes back as 80 * 3.921875 / 448. A down row that reads element 1
+    returns exactly that."""
+    x = np.array([[4.0, 1.0]])
+    eye = (np.array([[0x38, 0x00], [0x00, 0x38]], dtype=np.uint8), np.ones(2, dtype=np.float32))
+    down = (np.array([[0x00, 0x38]], dtype=np.uint8), np.ones(1, dtype=np.float32))
+    y = O.swiglu_expert_fp8(x, eye, eye, down)
+    assert np.allclose(y[0, 0], 80.0 * 3.921875 / 448.0, rtol=1e-6, atol=0)
+
+
 def test_fp8_forward_residual_keeps_the_layer_input():
     """All-zero FP8 experts (codes 0, scale 1) give out = 0 and
     h_k = sqrt((k-1)/k) * h_{k-1} exactly, with h_{k-1} the layer input

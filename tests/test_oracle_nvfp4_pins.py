@@ -115,6 +115,30 @@ def test_nvfp4_checkpoint_size():
     assert abs(total - 293.63e9) < 0.02e9
 
 
+def test_expert_quantises_x_and_the_activation_row():
+    """H = I = 16, one token. x = [1.5, 1.1875, 0, ...]: per-row group scale
+    1.5/2688, block scale 448, so x is coded at scale 1/4: 1.5 -> 6 and
+    1.1875 -> 4.75, whose nearest E2M1 value is 4, i.e. back to 1. Gate and
+    up weights are the identity on the first two channels (coded exactly):
+    g = u = [1.5, 1], A = bf16(silu(g) * u) = [1.8359375, 0.73046875]
+    (silu(1.5) * 1.5 = 1.83954..., silu(1) = 0.73106...). A's row is coded
+    at scale 1.8359375/6: 0.73046875 -> 2.387..., nearest E2M1 value 2, i.e.
+    back to 2 * 1.8359375 / 6. A down matrix that swaps the two channels
+    returns [2 * 1.8359375 / 6, 1.8359375] in its first two rows."""
+    H = I = 16
+    x = np.zeros((1, H))
+    x[0, :2] = [1.5, 1.1875]
+    eye2 = np.zeros((I, H))
+    eye2[0, 0] = eye2[1, 1] = 1.0
+    swap = np.zeros((H, I))
+    swap[0, 1] = swap[1, 0] = 1.0
+    gq = O.quantize_nvfp4(eye2, I)
+    dq = O.quantize_nvfp4(swap, H)
+    y = O.swiglu_expert_nvfp4(x, gq, gq, dq)
+    assert np.allclose(y[0, :2], [2.0 * 1.8359375 / 6.0, 1.8359375], rtol=1e-6, atol=0)
+    assert np.array_equal(y[0, 2:], np.zeros(H - 2))
+
+
 def test_expert_hand_case_closed_form():
     """One token through one NVFP4 expert (H = I = 16, one block per row),
     with operands chosen so that every quantisation is exact: each row's

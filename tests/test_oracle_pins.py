@@ -201,6 +201,8 @@ def test_near_tie_margins():
     assert sel["idx"][0].tolist() == [0, 1, 4, 2]
     assert 0 < sel["topk_margin"][0] < 1e-5
     assert O.near_ties(sel)[0]
+    # group scores 1.7, 1.3, 0.2, 0.2: the kept pair ends at 1.3, the next is 0.2
+    assert abs(sel["group_margin"][0] - 1.1) < 1e-6
 
 
 # --------------------------------------------------------------------------

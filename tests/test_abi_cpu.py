@@ -97,6 +97,28 @@ def test_null_pointers_rejected():
     assert r == 1
 
 
+def test_route_static_host_checks():
+    """The allocation-free router checks its arguments and its scratch size
+    on the host and returns before any CUDA call: bad sizes, NULL pointers,
+    misaligned x, and a batch whose scratch exceeds the fixed array
+    (T = 16384 with pre-norm needs far more than 8 MiB). Addresses here are
+    never dereferenced: every call fails before it would launch."""
+    lib = B.lib()
+    fake = ctypes.c_void_p(1 << 20)                 # 16-byte aligned, never read
+    args = lambda x: (x, fake, None, None, fake, fake, None, None)
+    assert lib.beam_moe_route_static(ctypes.byref(_p(top_k=0)), *args(fake)) == 1
+    assert lib.beam_moe_route_static(ctypes.byref(_p(H=5000)), *args(fake)) == 2
+    assert lib.beam_moe_route_static(ctypes.byref(_p()), *args(None)) == 1
+    assert lib.beam_moe_route_static(ctypes.byref(_p()), *args(ctypes.c_void_p((1 << 20) + 8))) == 1
+    assert "16-byte aligned" in B.last_error()
+    p = _p(flags=B.FLAG_RETURN_SCORES)
+    assert lib.beam_moe_route_static(ctypes.byref(p), *args(fake)) == 1     # no scores buffer
+    big = _p(T=16384, flags=B.FLAG_PRE_NORM)
+    assert lib.beam_moe_route_static(ctypes.byref(big), *args(fake)) == 2
+    assert "static scratch holds 8388608 bytes" in B.last_error()
+    assert lib.beam_moe_route_static(ctypes.byref(_p(T=0)), *args(None)) == 0
+
+
 def test_residual_step_args_rejected():
     lib = B.lib()
     assert lib.beam_residual_step(None, None, 4, 5120, 1, None, 1e-6, 1, 0, None, None) == 1

@@ -69,3 +69,18 @@ def test_peaks_come_from_the_measured_file(bench, tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     p = bench._peaks()
     assert p["source"] == "fallback" and p["hbm"] == 6400.0 and p["bf16"] == 1800.0
+
+
+def test_cpu_baseline_runs_for_its_minimum_time(bench):
+    """The oracle sample is repeated until it has taken the minimum time (at
+    least once, at most max_runs times), and the rate counts every run."""
+    import time
+    calls = []
+    run = lambda: (calls.append(1), time.sleep(0.02))
+    v, runs, dt = bench.time_oracle(run, 4, min_s=0.1, max_runs=50)
+    assert runs == len(calls) and 4 <= runs <= 7 and dt >= 0.1
+    assert abs(v - 4 * runs / dt) < 1e-9
+    v, runs, dt = bench.time_oracle(run, 4, min_s=10.0, max_runs=3)
+    assert runs == 3
+    v, runs, dt = bench.time_oracle(run, 4, min_s=0.0)
+    assert runs == 1

@@ -61,6 +61,12 @@ typedef enum {
 #define BEAM_FLAG_NVFP4_EXPERTS 16 /* workspace laid out for the NVFP4 expert path
                                       (beam_*_forward_nvfp4 require this bit; it
                                       excludes BEAM_FLAG_FP8_EXPERTS) */
+#define BEAM_FLAG_PREFILL_WEIGHT_MAJOR 32 /* many tokens per expert: run the expert
+                                      GEMMs on the weight-major kernel with token
+                                      tiles of 128 instead of the 2-SM (BF16/E4M3) or
+                                      token-major (NVFP4) kernels; same results within
+                                      FP32 rounding, for cross-checks (part of the
+                                      workspace layout: size it with the same flags) */
 
 /* Shape and hyper-parameters of one MoE sublayer call.
  *   T           tokens in the batch (0 is allowed: nothing is enqueued)
@@ -119,8 +125,9 @@ beam_status_t beam_moe_route(const beam_moe_params* p, const void* x,
  *   y_e = (silu(x W_gate[e]^T) * (x W_up[e]^T)) W_down[e]^T for each selected
  *         expert, BF16 operands, FP32 accumulation, SwiGLU product in FP32,
  *         the intermediate rounded to BF16 before the down projection
- *   o   = sum_j topk_w[t,j] * y_{topk_idx[t,j]}   (FP32 expert outputs, FP32 sum
- *         in slot order)
+ *   o   = sum_j topk_w[t,j] * y_{topk_idx[t,j]}   (FP32 expert outputs summed in
+ *         FP32 by the down projection's epilogue with L2 reductions, in an order
+ *         that varies from run to run)
  *   out = residual_k >= 2 ? bf16(sqrt((k-1)/k) x_in + RMSNorm(o) * post_gain / sqrt(k))
  *                         : o (bf16, or fp32 with BEAM_FLAG_FP32_OUT)
  * Arguments:
@@ -132,7 +139,9 @@ beam_status_t beam_moe_route(const beam_moe_params* p, const void* x,
  *   topk_idx, topk_w  optional outputs as in beam_moe_route (NULL: kept in the
  *              workspace)
  * Token-to-expert order inside the workspace is stable (by token, then slot).
- * Results are deterministic: the same inputs give bit-identical outputs. */
+ * Routing (topk_idx, topk_w) is bit-reproducible; o is reproducible to FP32
+ * rounding (the order of the 8 additions varies), so an output element can
+ * differ by one BF16 rounding step between runs. */
 beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in,
                                const float* w_router, const float* logit_bias,
                                const void* w_gate, const void* w_up, const void* w_down,
@@ -147,7 +156,7 @@ beam_status_t beam_moe_forward(const beam_moe_params* p, const void* x_in,
  *   T, H, I     tokens, hidden (multiple of 128, at most 8192), intermediate
  *               (multiple of 128)
  *   rms_eps, residual_k, flags  as in beam_moe_params (flags: PRE_NORM,
- *               FP32_OUT, FP8_EXPERTS)
+ *               FP32_OUT, FP8_EXPERTS, NVFP4_EXPERTS, PREFILL_WEIGHT_MAJOR)
  */
 typedef struct {
   int T, H, I;
@@ -161,7 +170,7 @@ size_t beam_dense_workspace_size(const beam_dense_params* p);
 
 /* Byte offsets of the dense MLP's workspace buffers, in the order and with
  * the meaning of beam_moe_workspace_layout (one expert, top_k = 1). Writes
- * min(n, 24) entries and returns how many it wrote (0 on invalid
+ * min(n, 25) entries and returns how many it wrote (0 on invalid
  * parameters). Diagnostic. */
 int beam_dense_workspace_layout(const beam_dense_params* p, size_t* offsets, int n);
 
@@ -405,8 +414,11 @@ const char* beam_last_error_string(void);
  * T <= 409 with pre-norm and T <= 511 without.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture. All calls on a device share the one
+ * (cudaGetSymbolAddress, with that device current) and caches it with the
+ * ID of the device's context; a call that finds a different context current
+ * (after a cudaDeviceReset, for instance) looks the address up again. Make
+ * the first call on a device, and the first after a reset, before any stream
+ * capture. All calls on a device share the one
  * array and it keeps the last call's contents; every call writes each scratch
  * byte it later reads, so nothing needs clearing between calls. Calls whose
  * work overlaps on the GPU (other streams, other host threads) race on the
@@ -423,8 +435,9 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
  * order: 0 normalised x [T,H] bf16, 1 router partial logits, 2 topk_idx,
  * 3 topk_w, 4 expert counts [E] int32, 5 expert offsets [E+1] int32,
  * 6 row_token [T*top_k] int32, 7 row_weight [T*top_k] fp32, 8 permuted x
- * [T*top_k,H] bf16, 9 SwiGLU activations [T*top_k,I] bf16, 10 per-pair
- * expert outputs [T*top_k,H] fp32, 11 unit counts [4] int32, 12 per-block
+ * [T*top_k,H] bf16, 9 SwiGLU activations [T*top_k,I] bf16, 10 the combined
+ * expert output o [T,H] fp32 (the down projection's epilogue adds into it),
+ * 11 unit counts [4] int32, 12 per-block
  * expert histograms, 13 per-block expert offsets, 14 gate/up work list,
  * 15 down work list, 16 pair -> row map [T*top_k] int32, 17 the router
  * weight split into three BF16 pieces [E, 3H], 18 the router GEMM's work
@@ -435,10 +448,12 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
  * block scales of x and 23 those of the activations (the SF-group layout
  * with token tiles of 32 or 128 rows -- the GEMM's token tile -- in place
  * of 128-row weight tiles: group (r / tile) * (K / 64) + k / 64, byte
- * (r % 32) * 16 + ((r % tile) / 32) * 4 + (k % 64) / 16).
- * Row-indexed buffers (6-10, 19-23) hold rows = T*top_k rows, or with NVFP4
+ * (r % 32) * 16 + ((r % tile) / 32) * 4 + (k % 64) / 16); 24 the combine's
+ * per-token arrival counters [T] int32, followed by its completion list [T]
+ * int32 and two int32 cursors.
+ * Row-indexed buffers (6-9, 19-23) hold rows = T*top_k rows, or with NVFP4
  * every expert's rows padded to the token tile (32 or 128). Writes
- * min(n, 24) entries and returns how many it wrote (0 on invalid
+ * min(n, 25) entries and returns how many it wrote (0 on invalid
  * parameters). */
 int beam_moe_workspace_layout(const beam_moe_params* p, size_t* offsets, int n);
 

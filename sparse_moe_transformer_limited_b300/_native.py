@@ -29,12 +29,13 @@ FLAG_FP32_OUT = 2
 FLAG_RETURN_SCORES = 4
 FLAG_FP8_EXPERTS = 8
 FLAG_NVFP4_EXPERTS = 16
+FLAG_PREFILL_WEIGHT_MAJOR = 32
 
 # names of the workspace buffers, in beam_moe_workspace_layout() order
 LAYOUT_NAMES = ("xn", "part", "topk_idx", "topk_w", "counts", "offsets", "row_token",
-                "row_weight", "xperm", "act", "y", "n_units", "blk_hist", "blk_off",
+                "row_weight", "xperm", "act", "oacc", "n_units", "blk_hist", "blk_off",
                 "units_gu", "units_dn", "pair_row", "router_w3", "router_units",
-                "x_scale", "act_q", "act_scale", "x_sf", "act_sf")
+                "x_scale", "act_q", "act_scale", "x_sf", "act_sf", "arrive")
 
 # every symbol include/beam_moe.h declares
 EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static",

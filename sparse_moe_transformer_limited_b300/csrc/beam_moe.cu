@@ -18,9 +18,10 @@
 
 #include "beam_moe.h"
 #include "kernels_attn.cuh"
+#include "kernels_combine.cuh"
 #include "kernels_gemm.cuh"
 #include "kernels_gemm_tm.cuh"
-#include "kernels_gemm_tm2.cuh"
+#include "kernels_gemm_wide.cuh"
 #include "kernels_gemm_2sm.cuh"
 #include "kernels_permute.cuh"
 #include "kernels_quant.cuh"
@@ -109,40 +110,36 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Expert-GEMM path, chosen from the mean tokens per expert:
 //  few tokens per expert (decode): weights as the M=128 operand, token tiles
 //    of 32 (expert_gemm_kernel);
-//  many tokens (prefill, H % 256 == 0): PATH_MIXED -- gate/up on the
-//    token-major two-CTA multicast kernel (expert_gemm_tm_kernel, whose
-//    token-major epilogue writes the SwiGLU output in 32-byte vectors), down
-//    on the 2-SM pair kernel (expert_gemm_pair_kernel); PATH_TM and
-//    PATH_PAIR run both GEMMs on one kernel (BEAM_PREFILL_GEMM=tm|pair);
-//    PATH_TM2 runs gate/up on the 256-row token-major kernel
-//    (expert_gemm_tm2_kernel) and down on the pair kernel
-//    (BEAM_PREFILL_GEMM=tm2);
-//  otherwise weights as M with token tiles of 128.
-enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2, PATH_PAIR = 3, PATH_MIXED = 4,
-                PATH_TM2 = 5 };
+//  many tokens, BF16 / E4M3 experts with H and I multiples of 256: both
+//    GEMMs on the wide 2-SM kernel (expert_gemm_wide_kernel);
+//  many tokens, NVFP4 experts with H, I % 256 == 0: both GEMMs on the
+//    token-major two-CTA kernel (expert_gemm_tm_kernel);
+//  otherwise, or with BEAM_FLAG_PREFILL_WEIGHT_MAJOR: weights as M with token
+//    tiles of 128 (expert_gemm_kernel).
+enum GemmPath { PATH_W32 = 0, PATH_W128 = 1, PATH_TM = 2, PATH_WIDE = 3 };
 
 GemmPath choose_path(const beam_moe_params& p) {
   const long long pairs = static_cast<long long>(p.T) * p.top_k;
   if (pairs <= 24LL * p.E) return PATH_W32;
-  // NVFP4 with many tokens: both GEMMs on the token-major kernel
-  if (p.flags & BEAM_FLAG_NVFP4_EXPERTS) {
-    const char* v = std::getenv("BEAM_PREFILL_GEMM");
-    if (p.H % 256 == 0 && !(v != nullptr && std::strcmp(v, "w128") == 0)) return PATH_TM;
-    return PATH_W128;
-  }
-  if (p.H % 256 == 0) {
-    const char* v = std::getenv("BEAM_PREFILL_GEMM");
-    if (v != nullptr && std::strcmp(v, "tm") == 0) return PATH_TM;
-    if (v != nullptr && std::strcmp(v, "pair") == 0) return PATH_PAIR;
-    if (v != nullptr && std::strcmp(v, "tm2") == 0) return PATH_TM2;
-    return PATH_MIXED;
-  }
-  return PATH_W128;
+  if (p.flags & BEAM_FLAG_PREFILL_WEIGHT_MAJOR) return PATH_W128;
+  if (p.flags & BEAM_FLAG_NVFP4_EXPERTS)
+    return (p.H % 256 == 0 && p.I % 256 == 0) ? PATH_TM : PATH_W128;
+  return (p.H % 256 == 0 && p.I % 256 == 0) ? PATH_WIDE : PATH_W128;
 }
 
 int path_nt(GemmPath g) { return g == PATH_W32 ? 32 : (g == PATH_W128 ? 128 : 256); }
 int path_mt_down(GemmPath g, int H) {
-  return (g == PATH_TM || g == PATH_PAIR || g == PATH_MIXED || g == PATH_TM2) ? H / 256 : H / 128;
+  return g == PATH_WIDE ? (H + 511) / 512 : (g == PATH_TM ? H / 256 : H / 128);
+}
+// Arrivals that complete one token in the fused combine of the down GEMM:
+// every (expert of the token, hidden slice, epilogue warp or lane group) adds
+// its share once. Weight-major: four warps of 32 hidden rows per 128-row tile;
+// wide: eight warps (64 hidden rows each, 32 in a last half slice) per slice
+// of 512 rows; token-major: two warps of 128 hidden columns per 256-column
+// tile.
+int combine_expected(GemmPath g, int H, int top_k) {
+  const int per_expert = g == PATH_WIDE ? 8 * ((H + 511) / 512) : (g == PATH_TM ? H / 128 : H / 32);
+  return top_k * per_expert;
 }
 
 // Router logits path: the tensor cores (exact three-way BF16 split of the
@@ -164,7 +161,7 @@ int choose_router_ks(const beam_moe_params& p, int num_sms) {
   return best;
 }
 
-constexpr int kLayoutEntries = 24;
+constexpr int kLayoutEntries = 25;
 
 struct Layout {
   size_t off[kLayoutEntries];
@@ -180,9 +177,9 @@ struct Layout {
 };
 
 enum {
-  L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_Y,
+  L_XN = 0, L_PART, L_IDX, L_W, L_COUNTS, L_OFFS, L_ROWTOK, L_ROWW, L_XPERM, L_ACT, L_OACC,
   L_NUNITS, L_BLKHIST, L_BLKOFF, L_UGU, L_UDN, L_PAIRROW, L_WR3, L_RUNITS,
-  L_XSCALE, L_ACTQ, L_ASCALE, L_XSF, L_ASF
+  L_XSCALE, L_ACTQ, L_ASCALE, L_XSF, L_ASF, L_ARRIVE
 };
 
 // Bytes of the router's unit list and count (tensor-core router only).
@@ -245,7 +242,8 @@ beam_status_t check_params(const beam_moe_params* p) {
   if (p->residual_k == 1 || p->residual_k < 0)
     return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", p->residual_k);
   if (p->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_RETURN_SCORES |
-                   BEAM_FLAG_FP8_EXPERTS | BEAM_FLAG_NVFP4_EXPERTS))
+                   BEAM_FLAG_FP8_EXPERTS | BEAM_FLAG_NVFP4_EXPERTS |
+                   BEAM_FLAG_PREFILL_WEIGHT_MAJOR))
     return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
   if ((p->flags & BEAM_FLAG_FP8_EXPERTS) && (p->flags & BEAM_FLAG_NVFP4_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP8_EXPERTS and BEAM_FLAG_NVFP4_EXPERTS exclude each other");
@@ -272,13 +270,12 @@ Layout make_layout(const beam_moe_params& p) {
   L.rows = f4 ? (R + (L.pad - 1) * std::min<long long>(p.E, R) + 127) / 128 * 128 : R;
   const long long Rr = L.rows;
   const long long tiles = (R + L.NT - 1) / L.NT + p.E;
-  if (L.path == PATH_PAIR || L.path == PATH_MIXED || L.path == PATH_TM2) {
+  if (L.path == PATH_WIDE) {
+    // at most ceil(n / 256) token groups per expert, one unit per group and
+    // weight slice
     const long long groups = (R + 255) / 256 + p.E;
-    // (the mixed path's gate/up list holds tm cluster units: two int4 each)
-    L.units_gu_max = L.path == PATH_MIXED
-                         ? 2 * (groups * (p.I / 128) + static_cast<long long>(p.E) * (p.I / 256 + 1))
-                         : groups * (p.I / 128);
-    L.units_dn_max = groups * (p.H / 256);
+    L.units_gu_max = groups * (p.I / 256);
+    L.units_dn_max = groups * ((p.H + 511) / 512);
   } else if (L.path == PATH_TM) {
     // cluster units (two int4 each): at most MT per 256-row group plus MT/2+1
     // tail units per expert
@@ -300,7 +297,7 @@ Layout make_layout(const beam_moe_params& p) {
   sz[L_ROWW] = static_cast<size_t>(Rr) * 4;
   sz[L_XPERM] = static_cast<size_t>(Rr) * p.H * 2;
   sz[L_ACT] = static_cast<size_t>(Rr) * p.I * 2;
-  sz[L_Y] = static_cast<size_t>(Rr) * p.H * 4;
+  sz[L_OACC] = static_cast<size_t>(p.T) * p.H * 4;
   sz[L_NUNITS] = 16;
   sz[L_BLKHIST] = static_cast<size_t>(L.NB) * p.E * 4;
   sz[L_BLKOFF] = static_cast<size_t>(L.NB) * p.E * 4;
@@ -316,6 +313,7 @@ Layout make_layout(const beam_moe_params& p) {
   // token block scales: 512-byte groups per (token tile of L.pad rows, K = 64 step)
   sz[L_XSF] = f4 ? static_cast<size_t>(Rr / L.pad) * (p.H / 64) * 512 : 0;
   sz[L_ASF] = f4 ? static_cast<size_t>(Rr / L.pad) * (p.I / 64) * 512 : 0;
+  sz[L_ARRIVE] = static_cast<size_t>(p.T) * 8 + 8;   // counters, completion list, cursors
   size_t cur = 0;
   for (int i = 0; i < kLayoutEntries; ++i) {
     L.off[i] = cur;
@@ -384,19 +382,17 @@ beam_status_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   return BEAM_OK;
 }
 
-template <int MODE, bool F8>
-beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& tok,
-                               const CUtensorMap& tok64, const beam::PairArgs& args,
-                               cudaStream_t st, const char* prof_name = nullptr) {
+template <bool F8>
+beam_status_t launch_gemm_pair(const CUtensorMap& a0, const CUtensorMap& tok, const CUtensorMap& tok64,
+                               const beam::PairArgs& args, cudaStream_t st, const char* prof_name) {
   using C = beam::PairCfg;
-  auto kern = beam::expert_gemm_pair_kernel<MODE, F8>;
+  auto kern = beam::expert_gemm_pair_kernel<F8>;
   beam_status_t sa = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (sa != BEAM_OK) return sa;
   const int grid = (sm_count() / 2) * 2;
-  ProfScope ps(prof_name ? prof_name : (MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down"),
-               st);
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(a0, a1, tok, tok64, args);
-  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_pair_kernel<gate/up>" : "expert_gemm_pair_kernel<down>");
+  ProfScope ps(prof_name, st);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(a0, tok, tok64, args);
+  BEAM_LAUNCH_CHECK("expert_gemm_pair_kernel");
   return BEAM_OK;
 }
 
@@ -414,16 +410,17 @@ beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const
   return BEAM_OK;
 }
 
-template <int KIND>
-beam_status_t launch_gemm_tm2(const CUtensorMap& wg, const CUtensorMap& wu, const CUtensorMap& tok,
-                              const beam::Tm2Args& args, cudaStream_t st) {
-  using C = beam::Tm2Cfg<KIND>;
-  auto kern = beam::expert_gemm_tm2_kernel<KIND>;
+template <int MODE, bool F8>
+beam_status_t launch_gemm_wide(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap (&tok)[4],
+                               const beam::WideArgs& args, cudaStream_t st) {
+  using C = beam::WideCfg;
+  auto kern = beam::expert_gemm_wide_kernel<MODE, F8>;
   beam_status_t sa = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (sa != BEAM_OK) return sa;
-  ProfScope ps("expert_gemm_gateup_swiglu", st);
-  kern<<<sm_count(), beam::TM2_THREADS, C::SMEM_BYTES, st>>>(wg, wu, tok, args);
-  BEAM_LAUNCH_CHECK("expert_gemm_tm2_kernel<gate/up>");
+  const int grid = (sm_count() / 2) * 2;
+  ProfScope ps(MODE == 0 ? "expert_gemm_gateup_swiglu" : "expert_gemm_down", st);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(w0, w1, tok[0], tok[1], tok[2], tok[3], args);
+  BEAM_LAUNCH_CHECK(MODE == 0 ? "expert_gemm_wide_kernel<gate/up>" : "expert_gemm_wide_kernel<down>");
   return BEAM_OK;
 }
 
@@ -471,7 +468,7 @@ beam_status_t launch_router(const beam_moe_params& p, const Layout& L, const voi
     ra.b_k_wrap = p.H / 64;
     ra.y_split = static_cast<size_t>(p.T) * p.E;
     ra.timeout_ns = kWaitTimeoutNs;
-    if ((s = launch_gemm_pair<1, false>(m_w, m_w, m_x, m_x64, ra, st, "router_logits_tc")) != BEAM_OK)
+    if ((s = launch_gemm_pair<false>(m_w, m_x, m_x64, ra, st, "router_logits_tc")) != BEAM_OK)
       return s;
   } else {
     dim3 g1((p.T + beam::RL_BT - 1) / beam::RL_BT, (p.E + beam::RL_BE - 1) / beam::RL_BE, L.KS);
@@ -529,36 +526,28 @@ struct QuantBufs {
   const int* rows_dev;   // NVFP4: device count of rows (offsets[E])
 };
 
-// Steps 3-4: gate/up GEMM + SwiGLU into act (bf16), then the down GEMM into
-// the per-pair FP32 outputs y. E4M3 / NVFP4: the expert-ordered x (xop) and
-// the weights are quantised; act is quantised per row (into q.aq) before
-// the down GEMM. NVFP4 runs on the weight-major kernel at decode and on the
-// token-major kernel (both GEMMs) for many tokens.
+// Steps 3-5: gate/up GEMM + SwiGLU into act (bf16), then the down GEMM whose
+// epilogue adds the router-weighted expert outputs into each token's FP32
+// accumulator and finalises every completed token (post-norm and residual,
+// or the output). E4M3 / NVFP4: the expert-ordered x (xop) and the weights
+// are quantised; act is quantised per row (into q.aq) before the down GEMM.
 template <int KIND>
 beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
                                   const ExpertWeights& w, const void* xop, const QuantBufs& q,
-                                  __nv_bfloat16* act, float* y, int4* ugu, int4* udn, int* nunits,
-                                  long long R, cudaStream_t st) {
+                                  __nv_bfloat16* act, const beam::CombineArgs& comb, int4* ugu,
+                                  int4* udn, int* nunits, long long R, cudaStream_t st) {
   constexpr bool F8 = KIND == beam::KIND_E4M3;
   constexpr bool F4 = KIND == beam::KIND_NVFP4;
   beam_status_t s = BEAM_OK;
   const int H = prm.H, E = prm.E, I = prm.I;
   const int KB = beam::KBlock<KIND>::ELEMS;
-  if (F4 && L.path != PATH_W32 && L.path != PATH_W128 && L.path != PATH_TM)
+  if (F4 && L.path == PATH_WIDE)
     return fail(BEAM_ERR_UNSUPPORTED, "NVFP4 experts run on the weight-major or token-major kernels");
   const bool bytes = F8 || F4;     // TMA maps over one-byte elements (codes)
   const int hc = F4 ? H / 2 : H;   // row length of the code matrices, in map elements
   const int ic = F4 ? I / 2 : I;
   // operand of the down GEMM: the bf16 act, or its codes
   const void* aop = (F8 || F4) ? static_cast<const void*>(q.aq) : static_cast<const void*>(act);
-  const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
-  const uint32_t gu_box = L.path == PATH_PAIR ? 64 : 128;
-  CUtensorMap m_g, m_u, m_d, m_x, m_a;
-  if ((s = make_map(&m_g, w.gate, static_cast<uint64_t>(E) * I, hc, gu_box, bytes)) != BEAM_OK) return s;
-  if ((s = make_map(&m_u, w.up, static_cast<uint64_t>(E) * I, hc, gu_box, bytes)) != BEAM_OK) return s;
-  if ((s = make_map(&m_d, w.down, static_cast<uint64_t>(E) * H, ic, 128, bytes)) != BEAM_OK) return s;
-  if ((s = make_map(&m_x, xop, R, hc, tok_box, bytes)) != BEAM_OK) return s;
-  if ((s = make_map(&m_a, aop, R, ic, tok_box, bytes)) != BEAM_OK) return s;
 
   // SwiGLU output -> per-row codes and scales (between the two GEMMs)
   auto quant_act = [&]() -> beam_status_t {
@@ -574,76 +563,53 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     return BEAM_OK;
   };
 
-  if (L.path == PATH_PAIR || L.path == PATH_MIXED || L.path == PATH_TM2) {
-    beam::PairArgs pa{};
-    pa.units = ugu;
-    pa.n_units = nunits + 0;
-    pa.k_blocks = H / KB;
-    pa.w_rows_per_expert = I;
-    pa.act = act;
-    pa.out_ld = I;
-    pa.timeout_ns = kWaitTimeoutNs;
-    pa.row_scale = q.xscale;
-    pa.w_scale0 = w.s_gate;
-    pa.w_scale1 = w.s_up;
-    beam::PairArgs pd = pa;
-    pd.units = udn;
-    pd.n_units = nunits + 1;
-    pd.k_blocks = I / KB;
-    pd.w_rows_per_expert = H;
-    pd.act = nullptr;
-    pd.y = y;
-    pd.out_ld = H;
-    pd.row_scale = nullptr;  // the activation row scales are applied by the combine
-    pd.w_scale0 = w.s_down;
-    pd.w_scale1 = nullptr;
-    CUtensorMap m_x64, m_a64;
-    if ((s = make_map(&m_x64, xop, R, H, 64, F8)) != BEAM_OK) return s;
-    if ((s = make_map(&m_a64, aop, R, I, 64, F8)) != BEAM_OK) return s;
-    if (L.path == PATH_TM2) {
-      // gate/up on the 256-row token-major kernel (128-row boxes)
-      CUtensorMap m_g128, m_u128, m_x128;
-      if ((s = make_map(&m_g128, w.gate, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
-      if ((s = make_map(&m_u128, w.up, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
-      if ((s = make_map(&m_x128, xop, R, H, 128, F8)) != BEAM_OK) return s;
-      beam::Tm2Args ta{};
-      ta.units = ugu;
-      ta.n_units = nunits + 0;
-      ta.k_blocks = H / KB;
-      ta.w_rows_per_expert = I;
-      ta.out = act;
-      ta.out_ld = I;
-      ta.timeout_ns = kWaitTimeoutNs;
-      ta.row_scale = q.xscale;
-      ta.w_scale0 = w.s_gate;
-      ta.w_scale1 = w.s_up;
-      if ((s = launch_gemm_tm2<F8 ? beam::KIND_E4M3 : beam::KIND_BF16>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK)
-        return s;
-    } else if (L.path == PATH_MIXED) {
-      // gate/up on the token-major multicast kernel (128-row boxes)
-      CUtensorMap m_g128, m_u128, m_x128;
-      if ((s = make_map(&m_g128, w.gate, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
-      if ((s = make_map(&m_u128, w.up, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
-      if ((s = make_map(&m_x128, xop, R, H, 128, F8)) != BEAM_OK) return s;
-      beam::TmArgs ta{};
-      ta.units = ugu;
-      ta.n_units = nunits + 0;
-      ta.k_blocks = H / KB;
-      ta.w_rows_per_expert = I;
-      ta.out = act;
-      ta.out_ld = I;
-      ta.timeout_ns = kWaitTimeoutNs;
-      ta.row_scale = q.xscale;
-      ta.w_scale0 = w.s_gate;
-      ta.w_scale1 = w.s_up;
-      if ((s = launch_gemm_tm<0, F8 ? beam::KIND_E4M3 : beam::KIND_BF16>(m_g128, m_u128, m_x128, ta, st)) != BEAM_OK)
-        return s;
-    } else {
-      if ((s = launch_gemm_pair<0, F8>(m_g, m_u, m_x, m_x64, pa, st)) != BEAM_OK) return s;
+  if (L.path == PATH_WIDE) {
+    // weights: 128-row boxes; tokens: 64/32/16/8-row boxes
+    CUtensorMap m_g, m_u, m_d, m_x[4], m_a[4];
+    if ((s = make_map(&m_g, w.gate, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
+    if ((s = make_map(&m_u, w.up, static_cast<uint64_t>(E) * I, H, 128, F8)) != BEAM_OK) return s;
+    if ((s = make_map(&m_d, w.down, static_cast<uint64_t>(E) * H, I, 128, F8)) != BEAM_OK) return s;
+    const uint32_t boxes[4] = {64, 32, 16, 8};
+    for (int j = 0; j < 4; ++j) {
+      if ((s = make_map(&m_x[j], xop, R, H, boxes[j], F8)) != BEAM_OK) return s;
+      if ((s = make_map(&m_a[j], aop, R, I, boxes[j], F8)) != BEAM_OK) return s;
     }
+    beam::WideArgs wa{};
+    wa.units = ugu;
+    wa.n_units = nunits + 0;
+    wa.k_blocks = H / KB;
+    wa.w_rows_per_expert = I;
+    wa.act = act;
+    wa.act_ld = I;
+    wa.timeout_ns = kWaitTimeoutNs;
+    wa.row_scale = q.xscale;
+    wa.w_scale0 = w.s_gate;
+    wa.w_scale1 = w.s_up;
+    beam::WideArgs wd = wa;
+    wd.units = udn;
+    wd.n_units = nunits + 1;
+    wd.k_blocks = I / KB;
+    wd.w_rows_per_expert = H;
+    wd.act = nullptr;
+    wd.row_scale = nullptr;  // the activation row scales are in the combine coefficient
+    wd.w_scale0 = w.s_down;
+    wd.w_scale1 = nullptr;
+    wd.comb = comb;
+    if ((s = launch_gemm_wide<0, F8>(m_g, m_u, m_x, wa, st)) != BEAM_OK) return s;
     if ((s = quant_act()) != BEAM_OK) return s;
-    if ((s = launch_gemm_pair<1, F8>(m_d, m_d, m_a, m_a64, pd, st)) != BEAM_OK) return s;
-  } else if (L.path == PATH_TM) {
+    if ((s = launch_gemm_wide<1, F8>(m_d, m_d, m_a, wd, st)) != BEAM_OK) return s;
+    return BEAM_OK;
+  }
+
+  const uint32_t tok_box = L.path == PATH_TM ? 128 : 16;
+  CUtensorMap m_g, m_u, m_d, m_x, m_a;
+  if ((s = make_map(&m_g, w.gate, static_cast<uint64_t>(E) * I, hc, 128, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_u, w.up, static_cast<uint64_t>(E) * I, hc, 128, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_d, w.down, static_cast<uint64_t>(E) * H, ic, 128, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_x, xop, R, hc, tok_box, bytes)) != BEAM_OK) return s;
+  if ((s = make_map(&m_a, aop, R, ic, tok_box, bytes)) != BEAM_OK) return s;
+
+  if (L.path == PATH_TM) {
     beam::TmArgs ta{};
     ta.units = ugu;
     ta.n_units = nunits + 0;
@@ -664,58 +630,59 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
     td.k_blocks = I / KB;
     td.w_rows_per_expert = H;
     td.out = nullptr;
-    td.y = y;
     td.out_ld = H;
-    td.row_scale = nullptr;  // the activation row scales are applied by the combine
+    td.row_scale = nullptr;  // the activation row scales are in the combine coefficient
     td.w_scale0 = w.s_down;
     td.w_scale1 = nullptr;
     td.a_sf = q.asf;
     td.w_sf0 = static_cast<const uint8_t*>(w.sf_down);
     td.w_sf1 = nullptr;
+    td.comb = comb;
     if ((s = launch_gemm_tm<0, KIND>(m_g, m_u, m_x, ta, st)) != BEAM_OK) return s;
     if ((s = quant_act()) != BEAM_OK) return s;
     if ((s = launch_gemm_tm<1, KIND>(m_d, m_d, m_a, td, st)) != BEAM_OK) return s;
+    return BEAM_OK;
+  }
+
+  beam::GemmArgs ga{};
+  ga.units = ugu;  // token tiles, shared by both GEMMs
+  ga.n_units = nunits + 0;
+  ga.m_tiles = I / 128;
+  ga.k_blocks = H / KB;
+  ga.a_rows_per_expert = I;
+  ga.out = act;
+  ga.out_ld = I;
+  ga.timeout_ns = kWaitTimeoutNs;
+  ga.row_scale = q.xscale;
+  ga.w_scale0 = w.s_gate;
+  ga.w_scale1 = w.s_up;
+  ga.a_sf0 = static_cast<const uint8_t*>(w.sf_gate);
+  ga.a_sf1 = static_cast<const uint8_t*>(w.sf_up);
+  ga.b_sf = q.xsf;
+  beam::GemmArgs gd = ga;
+  gd.n_units = nunits + 1;
+  gd.m_tiles = H / 128;
+  gd.k_blocks = I / KB;
+  gd.a_rows_per_expert = H;
+  gd.out = nullptr;
+  gd.out_ld = H;
+  gd.row_scale = nullptr;  // the activation row scales are in the combine coefficient
+  gd.w_scale0 = w.s_down;
+  gd.w_scale1 = nullptr;
+  gd.a_sf0 = static_cast<const uint8_t*>(w.sf_down);
+  gd.a_sf1 = nullptr;
+  gd.b_sf = q.asf;
+  gd.comb = comb;
+  // stage counts: NVFP4 stages also carry the K-block's block scales
+  constexpr int S_GU32 = F4 ? 5 : 6, S_DN32 = F4 ? 9 : 10;
+  if (L.path == PATH_W32) {
+    if ((s = launch_gemm<0, 32, S_GU32, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+    if ((s = quant_act()) != BEAM_OK) return s;
+    if ((s = launch_gemm<1, 32, S_DN32, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
   } else {
-    beam::GemmArgs ga{};
-    ga.units = ugu;  // token tiles, shared by both GEMMs
-    ga.n_units = nunits + 0;
-    ga.m_tiles = I / 128;
-    ga.k_blocks = H / KB;
-    ga.a_rows_per_expert = I;
-    ga.out = act;
-    ga.out_ld = I;
-    ga.timeout_ns = kWaitTimeoutNs;
-    ga.row_scale = q.xscale;
-    ga.w_scale0 = w.s_gate;
-    ga.w_scale1 = w.s_up;
-    ga.a_sf0 = static_cast<const uint8_t*>(w.sf_gate);
-    ga.a_sf1 = static_cast<const uint8_t*>(w.sf_up);
-    ga.b_sf = q.xsf;
-    beam::GemmArgs gd = ga;
-    gd.n_units = nunits + 1;
-    gd.m_tiles = H / 128;
-    gd.k_blocks = I / KB;
-    gd.a_rows_per_expert = H;
-    gd.out = nullptr;
-    gd.y = y;
-    gd.out_ld = H;
-    gd.row_scale = nullptr;  // the activation row scales are applied by the combine
-    gd.w_scale0 = w.s_down;
-    gd.w_scale1 = nullptr;
-    gd.a_sf0 = static_cast<const uint8_t*>(w.sf_down);
-    gd.a_sf1 = nullptr;
-    gd.b_sf = q.asf;
-    // stage counts: NVFP4 stages also carry the K-block's block scales
-    constexpr int S_GU32 = F4 ? 5 : 6, S_DN32 = F4 ? 9 : 10;
-    if (L.path == PATH_W32) {
-      if ((s = launch_gemm<0, 32, S_GU32, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
-      if ((s = quant_act()) != BEAM_OK) return s;
-      if ((s = launch_gemm<1, 32, S_DN32, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
-    } else {
-      if ((s = launch_gemm<0, 128, 4, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
-      if ((s = quant_act()) != BEAM_OK) return s;
-      if ((s = launch_gemm<1, 128, 6, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
-    }
+    if ((s = launch_gemm<0, 128, 4, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
+    if ((s = quant_act()) != BEAM_OK) return s;
+    if ((s = launch_gemm<1, 128, 6, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
   }
   return BEAM_OK;
 }
@@ -743,7 +710,8 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   int* pair_row = reinterpret_cast<int*>(ws + L.off[L_PAIRROW]);
   __nv_bfloat16* xperm = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_XPERM]);
   __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_ACT]);
-  float* y = reinterpret_cast<float*>(ws + L.off[L_Y]);
+  float* oacc = reinterpret_cast<float*>(ws + L.off[L_OACC]);
+  int* arrive = reinterpret_cast<int*>(ws + L.off[L_ARRIVE]);
   int4* ugu = reinterpret_cast<int4*>(ws + L.off[L_UGU]);
   int4* udn = reinterpret_cast<int4*>(ws + L.off[L_UDN]);
   int* nunits = reinterpret_cast<int*>(ws + L.off[L_NUNITS]);
@@ -782,18 +750,10 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   BEAM_LAUNCH_CHECK("expert_block_hist_kernel");
   if (!small) {
     ProfScope ps("expert_scan_units", st);
-    if (L.path == PATH_PAIR)
+    if (L.path == PATH_WIDE)
       beam::expert_scan_units_prefill_kernel<beam::LIST_PAIR, beam::LIST_PAIR>
-          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
-                              H / 256);
-    else if (L.path == PATH_TM2)
-      beam::expert_scan_units_prefill_kernel<beam::LIST_TM2, beam::LIST_PAIR>
-          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
-                              H / 256);
-    else if (L.path == PATH_MIXED)
-      beam::expert_scan_units_prefill_kernel<beam::LIST_TM, beam::LIST_PAIR>
-          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
-                              H / 256);
+          <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 256,
+                              (H + 511) / 512);
     else if (L.path == PATH_TM)
       beam::expert_scan_units_prefill_kernel<beam::LIST_TM, beam::LIST_TM>
           <<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs, ugu, udn, nunits, I / 128,
@@ -840,32 +800,45 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     BEAM_LAUNCH_CHECK("gather_rows_kernel");
   }
 
-  // 3. gate/up GEMM + SwiGLU -> act, 4. down GEMM -> per-pair y
-  if (w.kind == beam::KIND_NVFP4)
-    s = launch_expert_gemms<beam::KIND_NVFP4>(*p, L, w, xperm, qb, act, y, ugu, udn, nunits, Rl, st);
-  else if (w.kind == beam::KIND_E4M3)
-    s = launch_expert_gemms<beam::KIND_E4M3>(*p, L, w, xperm, qb, act, y, ugu, udn, nunits, R, st);
-  else
-    s = launch_expert_gemms<beam::KIND_BF16>(*p, L, w, xperm, qb, act, y, ugu, udn, nunits, R, st);
-  if (s != BEAM_OK) return s;
-
-  // 5. weighted combine, then post-norm + scaled residual (or the output)
+  // 3. gate/up GEMM + SwiGLU -> act, 4. down GEMM with the fused combine,
+  // 5. post-norm + scaled residual (or the output) of every completed token
   const int resid = p->residual_k >= 2;
   const float kf = static_cast<float>(resid ? p->residual_k : 2);
-  const float a = resid ? std::sqrt((kf - 1.f) / kf) : 0.f;
-  const float b = resid ? 1.f / std::sqrt(kf) : 1.f;
+  beam::CombineArgs cb{};
+  cb.acc = oacc;
+  cb.count = arrive;
+  cb.done = arrive + T;
+  cb.cursor = arrive + 2 * static_cast<size_t>(T);
+  cb.T = T;
+  cb.expected = combine_expected(L.path, H, K);
+  cb.row_token = row_tok;
+  cb.row_weight = row_w;
+  cb.row_scale = quant ? qb.ascale : nullptr;
+  cb.h_prev = static_cast<const __nv_bfloat16*>(x_in);
+  cb.gain = post_gain;
+  cb.out = out;
+  cb.H = H;
+  cb.eps = p->rms_eps;
+  cb.a = resid ? std::sqrt((kf - 1.f) / kf) : 0.f;
+  cb.b = resid ? 1.f / std::sqrt(kf) : 1.f;
+  cb.resid = resid;
+  cb.out_f32 = (p->flags & BEAM_FLAG_FP32_OUT) != 0;
   {
-    ProfScope ps("combine_rows", st);
-    if (p->flags & BEAM_FLAG_FP32_OUT)
-      beam::combine_rows_kernel<true><<<T, beam::COMBINE_THREADS, 0, st>>>(
-          y, qb.ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
-          p->rms_eps, a, b, resid);
-    else
-      beam::combine_rows_kernel<false><<<T, beam::COMBINE_THREADS, 0, st>>>(
-          y, qb.ascale, pair_row, wts, K, static_cast<const __nv_bfloat16*>(x_in), post_gain, out, H,
-          p->rms_eps, a, b, resid);
+    ProfScope ps("clear_acc", st);
+    const size_t n4 = static_cast<size_t>(T) * H / 4;
+    const unsigned blocks = static_cast<unsigned>(
+        std::min<size_t>((n4 + 255) / 256, static_cast<size_t>(2 * sm_count())));
+    beam::clear_acc_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<float4*>(oacc), n4, cb.count,
+                                                   cb.done, cb.cursor, T);
   }
-  BEAM_LAUNCH_CHECK("combine_rows_kernel");
+  BEAM_LAUNCH_CHECK("clear_acc_kernel");
+  if (w.kind == beam::KIND_NVFP4)
+    s = launch_expert_gemms<beam::KIND_NVFP4>(*p, L, w, xperm, qb, act, cb, ugu, udn, nunits, Rl, st);
+  else if (w.kind == beam::KIND_E4M3)
+    s = launch_expert_gemms<beam::KIND_E4M3>(*p, L, w, xperm, qb, act, cb, ugu, udn, nunits, R, st);
+  else
+    s = launch_expert_gemms<beam::KIND_BF16>(*p, L, w, xperm, qb, act, cb, ugu, udn, nunits, R, st);
+  if (s != BEAM_OK) return s;
   return BEAM_OK;
 }
 
@@ -1079,7 +1052,7 @@ beam_status_t check_dense(const beam_dense_params* d) {
   if (d->residual_k == 1 || d->residual_k < 0)
     return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", d->residual_k);
   if (d->flags & ~(BEAM_FLAG_PRE_NORM | BEAM_FLAG_FP32_OUT | BEAM_FLAG_FP8_EXPERTS |
-                   BEAM_FLAG_NVFP4_EXPERTS))
+                   BEAM_FLAG_NVFP4_EXPERTS | BEAM_FLAG_PREFILL_WEIGHT_MAJOR))
     return fail(BEAM_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
   if ((d->flags & BEAM_FLAG_FP8_EXPERTS) && (d->flags & BEAM_FLAG_NVFP4_EXPERTS))
     return fail(BEAM_ERR_INVALID_ARG, "BEAM_FLAG_FP8_EXPERTS and BEAM_FLAG_NVFP4_EXPERTS exclude each other");
@@ -1405,7 +1378,7 @@ beam_status_t dense_linear(const void* x, const void* w, int n, int N, int K, fl
   a.y = y;
   a.out_ld = N;
   a.timeout_ns = kWaitTimeoutNs;
-  return launch_gemm_pair<1, false>(m_w, m_w, m_x, m_x64, a, st, prof_name);
+  return launch_gemm_pair<false>(m_w, m_x, m_x64, a, st, prof_name);
 }
 
 }  // namespace
@@ -1558,23 +1531,63 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_route_static_mu;
 void* g_route_static_addr[kMaxDevices] = {};
+unsigned long long g_route_static_ctx[kMaxDevices] = {};
 
-// Device address of the static scratch on the current device (looked up on
-// the first call for that device, then cached).
+// Unique ID of the context current on this thread (driver entry points found
+// at run time, as for the tensor-map encoder); false when none is current or
+// the driver lacks the calls.
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*PFN_ctxGetCurrent_t)(CUcontext*);
+  typedef CUresult (*PFN_ctxGetId_t)(CUcontext, unsigned long long*);
+  static PFN_ctxGetCurrent_t get_current = nullptr;
+  static PFN_ctxGetId_t get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p1 = nullptr;
+    void* p2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<PFN_ctxGetCurrent_t>(p1);
+      get_id = reinterpret_cast<PFN_ctxGetId_t>(p2);
+    } else {
+      cudaGetLastError();
+    }
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the static scratch on the current device. It is looked
+// up with cudaGetSymbolAddress (with the device current) on the first call
+// for the device and again whenever the device's context has changed since
+// (a cudaDeviceReset destroys the context the cached address belonged to);
+// otherwise the cached address is used.
 beam_status_t route_static_scratch(void** addr) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(BEAM_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
     return fail(BEAM_ERR_UNSUPPORTED, "device ordinal %d is beyond %d", dev, kMaxDevices);
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
   std::lock_guard<std::mutex> g(g_route_static_mu);
-  if (g_route_static_addr[dev] == nullptr) {
+  if (!have_id || g_route_static_addr[dev] == nullptr || g_route_static_ctx[dev] != id) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_route_static_scratch);
     if (e != cudaSuccess || ptr == nullptr)
       return fail(BEAM_ERR_CUDA, "cudaGetSymbolAddress of the router scratch failed: %s",
                   cudaGetErrorString(e));
+    // the lookup made the device's primary context current if none was
+    unsigned long long id2 = 0;
     g_route_static_addr[dev] = ptr;
+    g_route_static_ctx[dev] = current_context_id(&id2) ? id2 : 0;
   }
   *addr = g_route_static_addr[dev];
   return BEAM_OK;

@@ -15,8 +15,9 @@
 //            epilogue: act[t, m*128+i] = bf16(silu(D_g) * D_u)   (FP32 math)
 //   down     (MODE 1): unit = (expert e, 128 hidden rows m, token tile)
 //            D[h,t] = sum_i Wd[e, m*128+h, i] * act[t, i]
-//            epilogue: y[t, m*128+h] = D[h,t] (FP32), the per-pair expert output
-//            (the row kernel combines the pairs of a token with its weights)
+//            epilogue: o[token(t), m*128+h] += w_t * D[h,t] (FP32), the
+//            router-weighted combine, then the post-norm and residual of
+//            every completed token (kernels_combine.cuh)
 //
 // Warp roles (192 threads, persistent, one CTA per SM):
 //   warp 0      TMA producer (one elected lane): fills a STAGES-deep smem ring
@@ -33,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "kernels_combine.cuh"
 #include "ptx.cuh"
 
 namespace beam {
@@ -47,7 +49,6 @@ struct GemmArgs {
   int k_blocks;               // K / 64 (BF16) or K / 128 (E4M3): 128-byte K-blocks
   int a_rows_per_expert;      // I (gate/up) or H (down)
   __nv_bfloat16* out;         // MODE 0: act [R, I] bf16
-  float* y;                   // MODE 1: y [R, H] fp32
   int out_ld;
   int m_tiles;                // weight row-tiles per token tile (I/128 or H/128)
   unsigned long long timeout_ns;
@@ -65,6 +66,7 @@ struct GemmArgs {
   const uint8_t* a_sf0;
   const uint8_t* a_sf1;
   const uint8_t* b_sf;
+  CombineArgs comb;           // MODE 1
 };
 
 // Unit u of a GEMM: token tile u / m_tiles of the tile list and weight
@@ -362,20 +364,42 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         } else {
+          // fused combine: o[token, col] += w * D (lanes 0..15 fetch the
+          // token and coefficient of the chunk's columns)
+          const CombineArgs& cb = args.comb;
           float d[16];
           tmem_ld16(tb + c * 16, d);
+          int tk = -1;
+          float cf = 0.f;
+          if (lane < 16 && c * 16 + lane < un.z) {
+            const int r = un.y + c * 16 + lane;
+            tk = cb.row_token[r];
+            if (tk >= 0) cf = combine_coef(cb, r);
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int tok = c * 16 + j;
-            if (tok < un.z)
-              args.y[static_cast<size_t>(un.y + tok) * args.out_ld + col] = (F8 || F4) ? d[j] * ws0 : d[j];
+            const int t = __shfl_sync(0xffffffffu, tk, j);
+            const float w = __shfl_sync(0xffffffffu, cf, j);
+            if (t >= 0) red_add_f32(args.comb.acc + static_cast<size_t>(t) * cb.H + col, w * (ws0 * d[j]));
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (MODE == 1) {
+        // one arrival per token of the unit (32 columns per call)
+#pragma unroll 1
+        for (int c = 0; c < un.z; c += 32) {
+          const int col_t = c + lane;
+          const int tk = col_t < un.z ? args.comb.row_token[un.y + col_t] : -1;
+          combine_arrive_warp(args.comb, tk, lane);
+        }
+      }
     }
+    // finalise completed tokens (rows) once this warp's own units are done
+    if (MODE == 1 && !combine_drain_warp(args.comb, lane, tmo, abort_flag) && lane == 0)
+      gemm_fail(abort_flag);
   }
 
   tc_fence_before();

@@ -1,26 +1,16 @@
-// Pair (2-SM) grouped expert GEMMs for prefill: tcgen05.mma.cta_group::2 on a
-// two-CTA cluster, weights as the MMA's M = 256 operand (128 rows in each
-// CTA), the tokens of one expert as N (32..256, N/2 rows in each CTA).
-//
-// The layer's experts ("Reflection 发布 Beam 501B 开源模型，支持 1M tokens 上下文",
-// section 专家混合模型): SwiGLU MLPs, hidden 5120, intermediate 2560, the
-// SwiGLU product in FP32 (section 残差流).
+// Pair (2-SM) GEMM with per-row FP32 outputs: tcgen05.mma.cta_group::2 on a
+// two-CTA cluster, the weights as the MMA's M = 256 operand (128 rows in each
+// CTA) and up to 256 rows of the activation as N (N/2 rows in each CTA). It
+// runs the router-logits GEMM of the tensor-core router (K-split, "Reflection
+// 发布 Beam 501B 开源模型，支持 1M tokens 上下文", section 专家混合模型: an FP32
+// router over all experts) and the attention sublayer's projections (section
+// 注意力), each as one "expert" whose rows are the tokens.
 //
 // Each CTA holds only its half of both operands, so one K-block is 32 KB of
-// shared memory per CTA (six stages fit) and each SM's shared memory serves
-// half of the MMA's operand reads. A unit is (expert e, weight tile m, a
-// group of at most 256 tokens of e); an expert's tokens are split into
-// balanced groups and N is the group size rounded up to 32, so a ragged group
-// costs MMA time in proportion to its tokens.
-//   gate/up (MODE 0): tile m = intermediate rows i0 = 128m .. +127. CTA r
-//            holds W_g rows i0+64r .. +63 (A rows 0..63) and W_u rows
-//            i0+64r .. +63 (A rows 64..127); TMEM lanes 0..63 = gate,
-//            64..127 = up. The warps holding up values pass them through
-//            shared memory to the warps holding the gate values of the same
-//            rows, which write act[t, i] = bf16(silu(g) * u) (FP32 math).
-//   down    (MODE 1): tile m = hidden rows h0 = 256m .. +255, CTA r holds
-//            rows h0+128r .. +127; y[t, h] = D (FP32), the per-pair expert
-//            output, combined per token by the row kernel.
+// shared memory per CTA (six stages fit). A unit is (expert or K-slice,
+// weight tile m, a group of at most 256 rows); N is the group size rounded
+// up to 32. Tile m = output columns h0 = 256m .. +255, CTA r holds weight
+// rows h0+128r .. +127 and writes y[t, h] = D (FP32) as coalesced rows.
 //
 // Roles per CTA (192 threads): warp 0 TMA producer; warp 1 TMEM allocation
 // (both CTAs) and, in the even CTA only, the MMA issuer; warps 2..5 epilogue.
@@ -40,12 +30,11 @@
 namespace beam {
 
 struct PairArgs {
-  const int4* units;        // {expert | K-split, first row, tokens (<= 256), weight tile}
+  const int4* units;        // {expert | K-split, first row, rows (<= 256), weight tile}
   const int* n_units;
   int k_blocks;             // 128-byte K-blocks per unit (64 BF16 or 128 E4M3 elements)
-  int w_rows_per_expert;    // I (gate/up) or H (down)
-  __nv_bfloat16* act;       // MODE 0: [R, I]
-  float* y;                 // MODE 1: [R, H]
+  int w_rows_per_expert;    // output columns per expert
+  float* y;                 // [rows, out_ld]
   int out_ld;
   // K-split (router logits): unit.x is the split index ks; the unit covers
   // K-blocks [ks*k_blocks, (ks+1)*k_blocks) of A, B's K-block is the A
@@ -54,12 +43,8 @@ struct PairArgs {
   int b_k_wrap;
   size_t y_split;
   unsigned long long timeout_ns;
-  // E4M3 operands only: per token-row scale (MODE 0; MODE 1 leaves the
-  // activation row scale to the combine) and per weight-row scales (gate and
-  // up for MODE 0, down for MODE 1), indexed expert * w_rows_per_expert + row
-  const float* row_scale;
+  // E4M3 operands only: per weight-row scales, indexed expert * w_rows_per_expert + row
   const float* w_scale0;
-  const float* w_scale1;
 };
 
 struct PairCfg {
@@ -70,40 +55,23 @@ struct PairCfg {
   static constexpr int ACC_COLS = 256;           // N <= 256
   static constexpr int NBUF = 2;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int XCHG_BYTES = 2 * 2 * 32 * 16 * 4;  // 2 warp pairs x 2 buffers
   static constexpr int BAR_BYTES = (2 * STAGES + 2 * NBUF + 1) * 8 + 16;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCHG_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// Named barrier that also ANDs a predicate over its participants.
-__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
-// F8: E4M3 operands (K-blocks of 128 elements, kind::f8f6f4) with the scales
-// applied in the epilogue; else BF16 (K-blocks of 64).
-template <int MODE, bool F8>
+// F8: E4M3 operands (K-blocks of 128 elements, kind::f8f6f4) with the weight
+// scales applied in the epilogue; else BF16 (K-blocks of 64).
+template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0,
-                            const __grid_constant__ CUtensorMap tm_a1,
                             const __grid_constant__ CUtensorMap tm_tok,
                             const __grid_constant__ CUtensorMap tm_tok64, const PairArgs args) {
   using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* xchg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::XCHG_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + C::NBUF;
@@ -132,7 +100,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     fence_mbar_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&tm_a0);
-    if (MODE == 0) tma_prefetch_desc(&tm_a1);
     tma_prefetch_desc(&tm_tok);
     tma_prefetch_desc(&tm_tok64);
   }
@@ -166,9 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const int tok0 = un.y + static_cast<int>(crank) * (N >> 1);
         const int expert = args.k_split ? 0 : un.x;
         const int kb0 = args.k_split ? un.x * args.k_blocks : 0;
-        const int wrow = (MODE == 0)
-                             ? expert * args.w_rows_per_expert + un.w * 128 + static_cast<int>(crank) * 64
-                             : expert * args.w_rows_per_expert + un.w * 256 + static_cast<int>(crank) * 128;
+        const int wrow = expert * args.w_rows_per_expert + un.w * 256 + static_cast<int>(crank) * 128;
         for (int kbl = 0; kbl < args.k_blocks; ++kbl) {
           const int kb = kb0 + kbl;
           const int kbb = args.b_k_wrap ? kb % args.b_k_wrap : kb;
@@ -181,12 +146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint32_t fbar = mapa_shared(&full[stage], 0);
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * cta_bytes);
           const int kx = kb * KBlock<F8>::ELEMS, kbx = kbb * KBlock<F8>::ELEMS;
-          if (MODE == 0) {
-            tma_load_2d_pair(sb, &tm_a0, fbar, kx, wrow, pol_w);
-            tma_load_2d_pair(sb + C::A_BYTES / 2, &tm_a1, fbar, kx, wrow, pol_w);
-          } else {
-            tma_load_2d_pair(sb, &tm_a0, fbar, kx, wrow, pol_w);
-          }
+          tma_load_2d_pair(sb, &tm_a0, fbar, kx, wrow, pol_w);
           for (int j = 0; j < n64; ++j)
             tma_load_2d_pair(sb + C::A_BYTES + j * 8192, &tm_tok64, fbar, kbx, tok0 + j * 64,
                              pol_x);
@@ -275,9 +235,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       bool ready = false;
       if (lane == 0) ready = mbar_wait_bounded(&tfull[buf], tpar, tmo, abort_flag);
       ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-      // gate/up: the two warps that exchange values through shared memory
-      // leave together, so neither waits alone at their named barrier
-      if (MODE == 0) ready = named_bar_and(1 + (q & 1), 64, ready);
       if (!ready) {
         if (lane == 0) gemm_fail(abort_flag);
         break;
@@ -286,60 +243,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint32_t tb = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS) +
                           (static_cast<uint32_t>(q * 32) << 16);
       const int nch = (un.z + 15) >> 4;
-      if (MODE == 0) {
-        // lanes 0..63 (q 0,1) gate, 64..127 (q 2,3) up of intermediate rows
-        // i = i0 + 64*crank + 32*(q & 1) + lane. Per chunk of 16 tokens the
-        // gate warp hands g of tokens 8..15 to its up partner and receives u
-        // of tokens 0..7, so each of the two computes and stores 8 tokens.
-        const int pairid = q & 1;
-        const bool is_gate = q < 2;
-        const int i = un.w * 128 + static_cast<int>(crank) * 64 + pairid * 32 + lane;
-        float* xb = xchg + pairid * (2 * 32 * 16);
-        const int tbase = is_gate ? 0 : 8;
-        float sg = 1.f, su = 1.f;
-        if (F8) {
-          const size_t wi = static_cast<size_t>(un.x) * args.w_rows_per_expert + i;
-          sg = args.w_scale0[wi];
-          su = args.w_scale1[wi];
-        }
-#pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
-          float v[16];
-          tmem_ld16(tb + c * 16, v);
-          // slot layout per lane: [0..7] u of tokens 0..7 (from up), [8..15] g of tokens 8..15
-          float* slot = xb + (c & 1) * (32 * 16) + lane * 16;
-          if (is_gate) {
-            *reinterpret_cast<float4*>(slot + 8) = make_float4(v[8], v[9], v[10], v[11]);
-            *reinterpret_cast<float4*>(slot + 12) = make_float4(v[12], v[13], v[14], v[15]);
-          } else {
-            *reinterpret_cast<float4*>(slot + 0) = make_float4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<float4*>(slot + 4) = make_float4(v[4], v[5], v[6], v[7]);
-          }
-          named_bar_sync(1 + pairid, 64);
-          const float4 o0 = *reinterpret_cast<const float4*>(slot + (is_gate ? 0 : 8));
-          const float4 o1 = *reinterpret_cast<const float4*>(slot + (is_gate ? 4 : 12));
-          const float other[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int tok = c * 16 + tbase + j;
-            if (tok < un.z) {
-              float g = is_gate ? v[j] : other[j];
-              float uu = is_gate ? other[j] : v[8 + j];
-              if (F8) {
-                const float sx = args.row_scale[un.y + tok];
-                g *= sg * sx;
-                uu *= su * sx;
-              }
-              const float a = __fdividef(g, 1.0f + __expf(-g)) * uu;
-              args.act[static_cast<size_t>(un.y + tok) * args.out_ld + i] = __float2bfloat16_rn(a);
-            }
-          }
-        }
-      } else {
+      {
         const int h = un.w * 256 + static_cast<int>(crank) * 128 + q * 32 + lane;
         float* ybase = args.k_split ? args.y + static_cast<size_t>(un.x) * args.y_split : args.y;
-        // E4M3: the weight-row scale here; the activation row scale is a
-        // factor of the whole output row and is applied by the combine
+        // E4M3: the weight-row scale
         const float sd = F8 ? args.w_scale0[static_cast<size_t>(un.x) * args.w_rows_per_expert + h] : 1.f;
         float* yrow = ybase + static_cast<size_t>(un.y) * args.out_ld + h;
         // 32 accumulator columns (tokens) per TMEM wait; the second half may
@@ -351,7 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = c * 16 + j;
-            // per-pair outputs are read once, by the row kernel: stream them past L2
+            // the rows are read once, by the next step: stream them past L2
             if (tok < un.z) __stcs(yrow + static_cast<size_t>(tok) * args.out_ld, F8 ? d[j] * sd : d[j]);
           }
 #pragma unroll

@@ -1,26 +1,26 @@
-// Token-major grouped expert GEMMs for many tokens per expert (prefill),
-// on tcgen05 + TMEM, with TMA multicast of the weight tiles inside a
-// two-CTA cluster.
+// Token-major grouped expert GEMMs for many tokens per expert with NVFP4
+// expert weights (prefill), on tcgen05 + TMEM.
 //
 // The layer's experts ("Reflection 发布 Beam 501B 开源模型，支持 1M tokens 上下文",
-// section 专家混合模型): SwiGLU MLPs, hidden 5120, intermediate 2560, the
-// SwiGLU product in FP32 (section 残差流).
+// section 专家混合模型): SwiGLU MLPs, hidden 5120, intermediate 2560, combined
+// with the normalised router weights; the SwiGLU product in FP32 and the
+// post-norm and residual in FP32 (section 残差流).
 //
-// A cluster unit is two sub-units, one per CTA, each (expert e, weight tile
-// n, up to 128 consecutive rows of the expert-ordered token layout = the
-// MMA's M). The weight tile has 256 rows (the MMA's N). In a PAIR unit both
-// CTAs work on the same tile (rows [0,128) and [128,256) of a 256-row group):
-// CTA r loads half r of the weight tile and multicasts it into both CTAs'
-// shared memory, so each weight byte leaves L2 once per 256 tokens. In a SOLO
-// unit (an expert's last <= 128 rows) each CTA works on its own tile and
-// loads both halves itself.
+// A cluster unit is two sub-units, one per CTA of a two-CTA cluster, each
+// (expert e, weight tile n, up to 128 consecutive rows of the expert-ordered
+// token layout = the MMA's M). The weight tile has 256 rows (the MMA's N) and
+// each CTA loads all of it into its own shared memory. In a PAIR unit both
+// CTAs work on the same tile (rows [0,128) and [128,256) of a 256-row group),
+// so the second read of the tile is served by L2 while the first is in
+// flight; in a SOLO unit (an expert's last <= 128 rows) each CTA works on its
+// own tile.
 //   gate/up (MODE 0): tile n = intermediate rows [128n, 128n+128) of W_g
 //            (half 0, TMEM columns 0..127) and of W_u (half 1, columns
 //            128..255); epilogue act[row, 128n + i] = bf16(silu(g_i) * u_i)
 //            with g_i and u_i read by the same thread (FP32 math).
-//   down    (MODE 1): tile n = hidden rows [256n, 256n+256) of W_d;
-//            epilogue y[row, 256n + j] = D[row, j] (FP32) -- the per-pair
-//            expert output, combined per token by the row kernel.
+//   down    (MODE 1): tile n = hidden rows [256n, 256n+256) of W_d; the
+//            epilogue adds w * y into the token's FP32 accumulator and
+//            finalises completed tokens (kernels_combine.cuh).
 //
 // NVFP4 (E2M1 codes with E4M3 scales per 16 elements, "NVFP4 版" section):
 // a K-block is 256 elements (128 bytes per row); each stage also carries the
@@ -29,21 +29,19 @@
 // into the stage's own TMEM columns (tcgen05.cp) before the block-scaled
 // MMAs. TMEM then holds one accumulator (256 columns) and the scale columns
 // of every stage (48 each), so the epilogue does not overlap the next unit.
+// BF16 and E4M3 operands are also supported (K-blocks of 64 / 128 elements).
 //
 // Warp roles as in the weight-major kernel: warp 0 TMA producer, warp 1 TMEM
 // owner and MMA issuer, warps 2..9 epilogue: two warps per TMEM lane quarter
-// (warp % 4), one per half of the accumulator's columns.
-// A shared-memory stage may be refilled only when the MMAs of BOTH CTAs have
-// consumed it (the peer's multicast writes into this CTA's stage too), so each
-// MMA commit arrives on the `empty` barrier of both CTAs (count 2). All waits
-// are bounded; the CTAs of a cluster meet at a cluster barrier before TMEM is
-// freed and before exit, so no CTA leaves while its peer may still write
-// into it.
+// (warp % 4), one per half of the accumulator's columns. All waits are
+// bounded; the CTAs of a cluster meet at a cluster barrier before TMEM is
+// freed and before exit.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "kernels_combine.cuh"
 #include "kernels_gemm.cuh"
 #include "kernels_permute.cuh"
 #include "ptx.cuh"
@@ -56,7 +54,6 @@ struct TmArgs {
   int k_blocks;             // 128-byte K-blocks: K / 64 (BF16), K / 128 (E4M3), K / 256 (NVFP4)
   int w_rows_per_expert;    // I (gate/up) or H (down)
   __nv_bfloat16* out;       // MODE 0: act [R, I] bf16
-  float* y;                 // MODE 1: y [R, H] fp32
   int out_ld;
   unsigned long long timeout_ns;
   // E4M3 operands only: per token-row scale (MODE 0; MODE 1 leaves the
@@ -73,6 +70,7 @@ struct TmArgs {
   const uint8_t* a_sf;
   const uint8_t* w_sf0;
   const uint8_t* w_sf1;
+  CombineArgs comb;         // MODE 1
 };
 
 template <int KIND>
@@ -133,7 +131,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < C::NBUF; ++b) {
       mbar_init(&tfull[b], 1);
@@ -152,7 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+  cluster_sync_all();  // barriers and TMEM ready in both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int n_units = *args.n_units;
@@ -169,7 +167,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
       bool ok = true;
       for (int u = cid; ok && u < n_units; u += ncl) {
         const int4 un = args.units[2 * u + crank];
-        const bool pair = (un.w & TM_PAIR) != 0;
         const int nt = un.w & 0xFFFF;
         // weight rows of half 0 and half 1 of the 256-row tile
         const int wr0 = (MODE == 0) ? un.x * args.w_rows_per_expert + nt * 128
@@ -187,17 +184,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
           // inner TMA coordinate in map elements: bf16 / e4m3 / bytes of e2m1 pairs
           const int kx = kb * (F4 ? 128 : KBlock<KIND>::ELEMS);
           tma_load_2d(sb, &tm_tok, &full[stage], kx, un.y, pol_x);
-          if (pair) {
-            if (crank == 0)
-              tma_load_2d_mc(sb + C::A_BYTES, &tm_w0, &full[stage], kx, wr0,
-                             static_cast<uint16_t>(0x3), pol_w);
-            else
-              tma_load_2d_mc(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kx, wr1,
-                             static_cast<uint16_t>(0x3), pol_w);
-          } else {
-            tma_load_2d(sb + C::A_BYTES, &tm_w0, &full[stage], kx, wr0, pol_w);
-            tma_load_2d(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kx, wr1, pol_w);
-          }
+          tma_load_2d(sb + C::A_BYTES, &tm_w0, &full[stage], kx, wr0, pol_w);
+          tma_load_2d(sb + C::A_BYTES + C::HALF_B, wm1, &full[stage], kx, wr1, pol_w);
           if (F4) {
             // this K-block's scale groups: token tile un.y / 128, weight tiles
             // of the two halves (each CTA loads all of them itself)
@@ -287,7 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
             for (int kk = 0; kk < 4; ++kk)
               mma_ss<F8>(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          mma_commit_mc(&empty[stage], static_cast<uint16_t>(0x3));
+          mma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -385,7 +373,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
           }
         }
       } else {
-        float* dst = args.y + row * args.out_ld + nt * 256 + 128 * half;
+        // fused combine: this thread's token row, 128 hidden columns
+        const CombineArgs& cb = args.comb;
+        const int tk = valid ? cb.row_token[row] : -1;
+        const float cf = tk >= 0 ? combine_coef(cb, static_cast<int>(row)) : 0.f;
+        float* dst = tk >= 0 ? cb.acc + static_cast<size_t>(tk) * cb.H + nt * 256 + 128 * half : nullptr;
         const size_t wi0 = static_cast<size_t>(un.x) * args.w_rows_per_expert + nt * 256 + 128 * half;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -402,19 +394,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) d[j] *= es0;
           }
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
+          if (tk >= 0) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              __stcs(d4 + j, make_float4(d[4 * j], d[4 * j + 1], d[4 * j + 2], d[4 * j + 3]));
+              red_add_v4_f32(dst + c * 16 + 4 * j, cf * d[4 * j], cf * d[4 * j + 1], cf * d[4 * j + 2],
+                             cf * d[4 * j + 3]);
           }
         }
+        combine_arrive_warp(cb, tk, lane);
       }
     }
+    // finalise completed tokens (rows) once this warp's own units are done
+    if (MODE == 1 && !combine_drain_warp(args.comb, lane, tmo, abort_flag) && lane == 0)
+      gemm_fail(abort_flag);
   }
 
   tc_fence_before();
-  cluster_sync_all();  // the peer no longer writes into this CTA
+  cluster_sync_all();  // both CTAs done before TMEM is freed
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);

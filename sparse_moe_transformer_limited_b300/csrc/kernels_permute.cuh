@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) expert_scan_units_kernel(
 // Work lists of the token-major two-CTA GEMMs. A cluster unit is two int4
 // sub-units, one per CTA: {expert, first row, rows (<= 128), weight tile |
 // TM_PAIR}. An expert's rows go in 256-row groups, each a PAIR unit (both
-// CTAs on the same weight tile, 128 rows each, the tile multicast); a last
+// CTAs on the same weight tile, 128 rows each); a last
 // remainder of at most 128 rows becomes SOLO sub-units -- one per weight
 // tile, two tiles per cluster unit, each CTA loading its own weights -- so a
 // tail costs one 128-row MMA tile instead of a 256-row group. Units of one
@@ -208,23 +208,12 @@ __device__ __forceinline__ int4 pair_unit_at(int l, int ex, int r0, int n, int M
   return make_int4(ex, r0 + start, q + (gi < extra ? 1 : 0), m);
 }
 
-// 256-row token-major lists: an expert's n rows go in groups of 256 from its
-// first row (the last group holds the remainder); a unit is {expert, first
-// row, group rows, weight tile}, weight-tile-major (the groups sharing a tile
-// are adjacent): unit l is tile l / g, group l % g, g = ceil(n / 256).
-__device__ __forceinline__ int4 tm2_unit_at(int l, int ex, int r0, int n, int MT) {
-  const int g = (n + 255) >> 8;
-  const int m = l / g, gi = l - m * g;
-  return make_int4(ex, r0 + 256 * gi, min(256, n - 256 * gi), m);
-}
-
 // Work lists for prefill: each GEMM's list in the format of the kernel that
-// runs it (LIST_TM: two-CTA multicast cluster units; LIST_PAIR: 2-SM pair
-// units; LIST_TM2: 256-row token-major units). Also writes counts, offsets
-// and the per-block row offsets.
+// runs it (LIST_TM: two-CTA token-major cluster units; LIST_PAIR: 2-SM pair
+// units of the wide kernel, MT weight slices per expert). Also writes
+// counts, offsets and the per-block row offsets.
 constexpr int LIST_TM = 0;
 constexpr int LIST_PAIR = 1;
-constexpr int LIST_TM2 = 2;
 
 template <int KIND>
 __device__ __forceinline__ int list_units_for(int n, int MT) {
@@ -238,8 +227,6 @@ __device__ __forceinline__ void list_unit(int4* units, int u, int l, int ex, int
     tm_unit_at(l, ex, r0, n, MT, two);
     units[2 * u] = two[0];
     units[2 * u + 1] = two[1];
-  } else if (KIND == LIST_TM2) {
-    units[u] = tm2_unit_at(l, ex, r0, n, MT);
   } else {
     units[u] = pair_unit_at(l, ex, r0, n, MT);
   }

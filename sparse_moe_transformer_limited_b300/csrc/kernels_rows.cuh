@@ -134,92 +134,4 @@ __global__ void __launch_bounds__(256) finalize_rows_kernel(
   }
 }
 
-// Weighted combine of a token's expert outputs, then either the output or the
-// post-norm + scaled residual ("Reflection 发布 Beam 501B 开源模型…", section
-// 专家混合模型: expert outputs combined with the normalised router weights;
-// section 残差流: normalise after the sublayer, then h_k = a*h_{k-1} + b*n):
-//   o[t,:] = sum_j w[t,j] * s[r] * y[r, :], r = pair_row[t,j]   (y FP32; FP32
-//            sum, slot order; s = the per-row scale of y, or 1 when y_scale
-//            is NULL -- the E4M3 path's activation row scales)
-//   resid:  out = bf16( a * h_prev + b * RMSNorm(o) * gain )
-//   else:   out = o  (bf16, or fp32 when OUT_F32)
-// One block of 128 threads per token; each thread keeps up to 8 chunks of 8
-// elements of o in registers (H <= 8192).
-constexpr int COMBINE_THREADS = 128;
-constexpr int COMBINE_MAX_CHUNKS = 8;
-
-template <bool OUT_F32>
-__global__ void __launch_bounds__(COMBINE_THREADS) combine_rows_kernel(
-    const float* __restrict__ y, const float* __restrict__ y_scale, const int* __restrict__ pair_row,
-    const float* __restrict__ topk_w, int top_k, const __nv_bfloat16* __restrict__ h_prev,
-    const float* __restrict__ gain, void* __restrict__ out, int H, float eps, float a, float b,
-    int resid) {
-  __shared__ int s_row[32];
-  __shared__ float s_w[32];
-  __shared__ float s_red[COMBINE_THREADS / 32];
-  const int t = blockIdx.x;
-  const int tid = threadIdx.x;
-  if (tid < top_k) {
-    const int r = pair_row[static_cast<size_t>(t) * top_k + tid];
-    s_row[tid] = r;
-    const float wt = topk_w[static_cast<size_t>(t) * top_k + tid];
-    s_w[tid] = y_scale != nullptr ? wt * y_scale[r] : wt;
-  }
-  __syncthreads();
-  const int nc = H >> 3;
-  float o[COMBINE_MAX_CHUNKS][8];
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < COMBINE_MAX_CHUNKS; ++i) {
-    const int c = tid + i * COMBINE_THREADS;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[i][e] = 0.f;
-    if (c < nc) {
-      for (int j = 0; j < top_k; ++j) {
-        float f[8];
-        load8(y + static_cast<size_t>(s_row[j]) * H, c, f);
-        const float wj = s_w[j];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[i][e] = fmaf(wj, f[e], o[i][e]);
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(o[i][e], o[i][e], ss);
-    }
-  }
-  float r = 1.f;
-  if (resid) {
-    ss = warp_sum(ss);
-    if ((tid & 31) == 0) s_red[tid >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < COMBINE_THREADS / 32; ++w) tot += s_red[w];
-    r = rsqrtf(tot / static_cast<float>(H) + eps);
-  }
-#pragma unroll
-  for (int i = 0; i < COMBINE_MAX_CHUNKS; ++i) {
-    const int c = tid + i * COMBINE_THREADS;
-    if (c >= nc) continue;
-    if (OUT_F32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<size_t>(t) * H) + 2 * c;
-      dst[0] = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
-      dst[1] = make_float4(o[i][4], o[i][5], o[i][6], o[i][7]);
-    } else {
-      float f[8];
-      if (resid) {
-        float hv[8], g[8];
-        load8(h_prev + static_cast<size_t>(t) * H, c, hv);
-        gain8(gain, c, g);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = fmaf(a, hv[e], b * (o[i][e] * r * g[e]));
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = o[i][e];
-      }
-      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + static_cast<size_t>(t) * H)[c] =
-          f32x8_to_bf16(f);
-    }
-  }
-}
-
 }  // namespace beam

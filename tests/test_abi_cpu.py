@@ -257,29 +257,43 @@ def _kb(nbytes):
     return (nbytes + 1023) // 1024 * 1024
 
 
-@pytest.mark.parametrize("env,flags,T,want_gu,want_dn", [
+@pytest.mark.parametrize("flags,T,want_gu,want_dn", [
     # decode, 512 pairs <= 24 per expert: weight-major token tiles of 32;
     # one list of (512/32 + E) tiles, expanded by the I/128 gate/up and H/128
     # down weight tiles
-    (None, 0, 64, 16 * (16 + 256) * 20, 16 * (16 + 256) * 40),
-    # prefill BF16: two-CTA cluster units for gate/up (two int4 each), 2-SM
-    # pair units for down; groups = 65536/256 + E
-    (None, 0, 8192, 16 * 2 * (512 * 20 + 256 * 11), 16 * 512 * 20),
-    ("pair", 0, 8192, 16 * 512 * 20, 16 * 512 * 20),
-    ("tm2", 0, 8192, 16 * 512 * 20, 16 * 512 * 20),
-    # prefill NVFP4: both GEMMs on the cluster kernel
-    (None, "nvfp4", 8192, 16 * 2 * (512 * 20 + 256 * 11), 16 * 2 * (512 * 20 + 256 * 11)),
-    # NVFP4 on the weight-major kernel: 128-token tiles
-    ("w128", "nvfp4", 8192, 16 * (512 + 256) * 20, 16 * (512 + 256) * 40),
+    (0, 64, 16 * (16 + 256) * 20, 16 * (16 + 256) * 40),
+    # prefill BF16: wide 2-SM units, at most 65536/256 + E token groups, one
+    # unit per group and weight slice (I/256 gate/up, H/512 down slices)
+    (0, 8192, 16 * 512 * 10, 16 * 512 * 10),
+    ("fp8", 8192, 16 * 512 * 10, 16 * 512 * 10),
+    # the weight-major flag: 128-token tiles for both GEMMs
+    ("wm", 8192, 16 * (512 + 256) * 20, 16 * (512 + 256) * 40),
+    # prefill NVFP4: both GEMMs on the token-major cluster kernel
+    ("nvfp4", 8192, 16 * 2 * (512 * 20 + 256 * 11), 16 * 2 * (512 * 20 + 256 * 11)),
+    # NVFP4 with the weight-major flag: 128-token tiles
+    ("nvfp4+wm", 8192, 16 * (512 + 256) * 20, 16 * (512 + 256) * 40),
 ])
-def test_gemm_regime_follows_tokens_and_switch(monkeypatch, env, flags, T, want_gu, want_dn):
-    """The expert-GEMM regime is chosen on the host from tokens per expert and
-    the BEAM_PREFILL_GEMM switch; each regime's work-list format fixes the
-    size of its workspace entries (read here without a GPU)."""
-    if env is None:
-        monkeypatch.delenv("BEAM_PREFILL_GEMM", raising=False)
-    else:
-        monkeypatch.setenv("BEAM_PREFILL_GEMM", env)
-    f = B.FLAG_NVFP4_EXPERTS if flags == "nvfp4" else 0
+def test_gemm_regime_follows_tokens_and_flag(flags, T, want_gu, want_dn):
+    """The expert-GEMM regime is chosen on the host from tokens per expert,
+    the expert weight type and BEAM_FLAG_PREFILL_WEIGHT_MAJOR; each regime's
+    work-list format fixes the size of its workspace entries (read here
+    without a GPU)."""
+    f = 0
+    if flags and "nvfp4" in flags:
+        f |= B.FLAG_NVFP4_EXPERTS
+    if flags and "fp8" in flags:
+        f |= B.FLAG_FP8_EXPERTS
+    if flags and "wm" in flags:
+        f |= B.FLAG_PREFILL_WEIGHT_MAJOR
     gu, dn = _list_bytes(B.workspace_layout(_p(T=T, flags=f)))
     assert (gu, dn) == (_kb(want_gu), _kb(want_dn))
+
+
+def test_combined_output_buffer_is_per_token():
+    """The down projection adds into one FP32 row per token (no per-pair
+    expert outputs), followed by one arrival counter per token."""
+    for T in (64, 8192):
+        lay = B.workspace_layout(_p(T=T))
+        assert lay["n_units"] - lay["oacc"] == _kb(T * 5120 * 4)
+        n = B.workspace_size(_p(T=T))
+        assert n - lay["arrive"] >= T * 4

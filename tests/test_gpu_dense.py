@@ -43,7 +43,7 @@ def _check(B, T, H, I, seed, pre_norm=False, residual_k=0, fp32_out=False, sampl
 
 @pytest.mark.parametrize("T,H,I", [(1, 256, 128), (7, 256, 384), (24, 512, 128),
                                    (64, 256, 256), (300, 512, 128), (1000, 256, 384),
-                                   (333, 384, 256)])
+                                   (333, 384, 256), (600, 512, 512), (1000, 768, 256)])
 def test_dense_shapes(B, T, H, I):
     _check(B, T, H, I, seed=T + I, fp32_out=True)
 

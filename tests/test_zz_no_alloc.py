@@ -69,6 +69,16 @@ def test_route_static_matches_route_on_two_calls(B, name, flags):
         _compare(B, p, d, gain)
 
 
+def test_route_static_tensor_core_router_on_two_calls(B):
+    """T >= 512 with E = 256: the router runs on the tensor cores, so the
+    static scratch also holds the three-way BF16 split of the router weight
+    and the router GEMM's work list. Small H keeps it inside the limit."""
+    wl = S.WORKLOADS["tiny"].replace(T=512)
+    for seed in (3, 29):                       # two calls in a row, different inputs
+        p, d, gain = _case(B, wl, seed, B.FLAG_RETURN_SCORES)
+        _compare(B, p, d, gain)
+
+
 def test_route_static_rejects_oversize_without_launching(B):
     wl = S.WORKLOADS["long_prefill"]
     p = B.make_params(wl.T, wl.H, wl.E, wl.I, flags=B.FLAG_PRE_NORM)

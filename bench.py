@@ -126,10 +126,50 @@ def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, seconds: fl
     return world * tokens_per_rank * steps / seconds
 
 
+def timed_steps(B, step, steps, stream, barrier, gpu_index, prof_steps=10):
+    """Time `steps` calls of step() with CUDA events on `stream` while the
+    clocks are sampled (the library's per-launch events off), then run up to
+    prof_steps more with the per-launch events on for the per-kernel split.
+    Returns (ms over the timed steps, per-kernel record, clocks, profiled steps)."""
+    clocks = ClockSampler(gpu_index)
+    barrier()
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    n_prof = max(1, min(steps, prof_steps))
+    B.profile_read()
+    B.profile_enable(True)
+    for _ in range(n_prof):
+        step()
+    barrier()
+    B.profile_enable(False)
+    prof = B.profile_read()
+    if B.status() != 0:
+        raise RuntimeError(B.last_error())
+    return ms, prof, clk, n_prof
+
+
 # ------------------------------------------------------------ workload
 def _workload(name):
     wl = S.WORKLOADS[name]
     return wl
+
+
+def _config(wl, world):
+    """The workload description both arms print."""
+    return {"workload": _describe(wl), "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I,
+            "top_k": wl.top_k, "seed": wl.seed,
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "no flush: 20.1 GB of expert weights per step exceed the 126 MB L2"}
 
 
 def _describe(wl):
@@ -239,25 +279,9 @@ def run_ours(args, rank, world, local_rank, kind="bf16"):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    # ---- device-timed region (inputs resident in HBM)
-    clocks = ClockSampler(local_rank)
-    barrier()
-    clocks.start()
-    B.profile_read()
-    B.profile_enable(True)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    barrier()
-    B.profile_enable(False)
-    clk = clocks.stop()
-    prof = B.profile_read()
-    ms_total = e0.elapsed_time(e1)
-    if B.status() != 0:
-        raise RuntimeError(B.last_error())
+    # ---- device-timed region (inputs resident in HBM), per-launch events off;
+    # then the per-kernel split in a second pass of the same steps
+    ms_total, prof, clk, prof_steps = timed_steps(B, step, args.steps, stream, barrier, local_rank)
 
     # ---- end-to-end through the public API with host buffers
     h_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
@@ -317,7 +341,9 @@ def run_ours(args, rank, world, local_rank, kind="bf16"):
              "tensor_frac": round(alg["layer_flops"] / (ms_step / 1e3) / 1e12 / peaks["bf16"], 4),
              "touched_experts": alg["touched"], "max_tokens_per_expert": int(counts.max())}
     kernels = {k: round(v[0] / v[1], 4) for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
-    launches = sum(v[1] for v in prof.values())   # the library's launches in the timed region
+    # the library's launches in the timed region: per step (from the profiled
+    # pass, which runs the same steps) times the timed steps
+    launches = sum(v[1] for v in prof.values()) // prof_steps * args.steps
     return dict(value=value, ms_step=ms_step, e2e=e2e_value, clocks=clk, roofline=roof,
                 layer=layer, kernels_ms=kernels, wl=wl, launches=launches,
                 h2d=wl.T * wl.H * 2, d2h=wl.T * wl.H * 2)
@@ -353,24 +379,9 @@ def run_dense(args, rank, world, local_rank, name):
         step()
     if B.status() != 0:
         raise RuntimeError(B.last_error())
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    B.profile_read()
-    B.profile_enable(True)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize(dev)
-    B.profile_enable(False)
-    clk = clocks.stop()
-    prof = B.profile_read()
-    if B.status() != 0:
-        raise RuntimeError(B.last_error())
-    ms = e0.elapsed_time(e1) / args.steps
+    ms, prof, clk, _ = timed_steps(B, step, args.steps, torch.cuda.current_stream(dev),
+                                   lambda: torch.cuda.synchronize(dev), local_rank)
+    ms /= args.steps
     peaks = _peaks()
     gu_ms = prof["expert_gemm_gateup_swiglu"][0] / prof["expert_gemm_gateup_swiglu"][1]
     flops = 2.0 * T * 3 * H * I
@@ -421,25 +432,10 @@ def run_attn(args, rank, world, local_rank, name):
         step()
     if B.status() != 0:
         raise RuntimeError(B.last_error())
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    B.profile_read()
-    B.profile_enable(True)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     steps = max(1, args.steps // 2)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize(dev)
-    B.profile_enable(False)
-    clk = clocks.stop()
-    prof = B.profile_read()
-    if B.status() != 0:
-        raise RuntimeError(B.last_error())
-    ms = e0.elapsed_time(e1) / steps
+    ms, prof, clk, _ = timed_steps(B, step, steps, torch.cuda.current_stream(dev),
+                                   lambda: torch.cuda.synchronize(dev), local_rank)
+    ms /= steps
     w = cfg["window"]
     pairs = sum(min(i + 1, w) for i in range(T)) if w else T * (T + 1) // 2
     attn_flops = 4.0 * nq * D * pairs                        # Q K^T and P V over visible pairs
@@ -612,7 +608,7 @@ def main():
                 "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic",
-                "config": {"workload": _describe(wl), "T": wl.T, "seed": wl.seed},
+                "config": _config(wl, world),
                 "cpu_baseline": {"value": round(r["value"], 4), "unit": "tokens/s",
                                  "cores": r["cores"], "kind": "oracle", "sample": r["sample"]},
                 "e2e": {"value": round(r["value"], 4), "unit": "tokens/s",
@@ -626,16 +622,28 @@ def main():
     if rank == 0 and world == 1 and args.config == "decode" and not args.no_prefill:
         a2 = argparse.Namespace(**vars(args))
         a2.config = "prefill"
-        torch.cuda.empty_cache()
-        r2 = run_ours(a2, rank, world, local_rank)
-        torch.cuda.empty_cache()
-        extra_dense = run_dense(a2, rank, world, local_rank, "dense_prefill")
+
         def summary(rr):
+            """A secondary workload's line: value, step time, e2e, roofline of
+            its dominant kernel, layer fractions and clocks (the per-kernel
+            split of the secondaries is left out to keep the line short)."""
+            ro = rr["roofline"]
+            keep = ("bound", "achieved", "peak", "unit", "frac", "frac_of_sustained", "traffic",
+                    "launch_ms", "dtype")
             return {"value": round(rr["value"], 1), "unit": "tokens/s",
                     "ms_per_step": round(rr["ms_step"], 4), "e2e": round(rr["e2e"], 1),
-                    "roofline": rr["roofline"], "layer": rr["layer"],
-                    "kernels_ms": rr["kernels_ms"], "clocks": rr["clocks"]}
-        extra = {"dense_mlp_T8192": extra_dense, "prefill_T8192": summary(r2)}
+                    "roofline": {k: ro[k] for k in keep if k in ro},
+                    "layer": {k: rr["layer"][k] for k in ("hbm_frac", "tensor_frac")},
+                    "clocks": None if rr["clocks"] is None else
+                    {k: rr["clocks"][k] for k in ("sm_mhz", "reasons")}}
+        # the BF16 T = 8192 line is measured right after the headline and
+        # printed last, where a reader keeping the end of the line sees it
+        torch.cuda.empty_cache()
+        rp = run_ours(a2, rank, world, local_rank)
+        prefill = summary(rp)
+        prefill["kernels_ms"] = dict(list(rp["kernels_ms"].items())[:4])
+        torch.cuda.empty_cache()
+        extra["dense_mlp_T8192"] = run_dense(a2, rank, world, local_rank, "dense_prefill")
         # the skewed-routing and long-prefill-with-residual workloads
         for cfg, key in (("skew", "skew_T4096"), ("long_prefill", "long_prefill_T16384")):
             a4 = argparse.Namespace(**vars(args))
@@ -654,6 +662,7 @@ def main():
                 torch.cuda.empty_cache()
                 extra[f"{k2}_experts_T8192"] = summary(run_ours(a2, rank, world, local_rank, k2))
             torch.cuda.empty_cache()
+        extra["prefill_T8192"] = prefill
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         torch.cuda.empty_cache()
@@ -673,10 +682,7 @@ def main():
             "scaling": "weak", "vs_baseline": None,
             "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[kind],
             "data": "synthetic",
-            "config": {"workload": _describe(wl), "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I,
-                       "top_k": wl.top_k, "seed": wl.seed,
-                       "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": "no flush: 20.1 GB of expert weights per step exceed the 126 MB L2"},
+            "config": _config(wl, world),
             "roofline": r["roofline"], "layer": r["layer"], "kernels_ms": r["kernels_ms"],
             "clocks": r["clocks"],
             "e2e": {"value": round(r["e2e"], 1), "unit": "tokens/s",

@@ -274,6 +274,62 @@ def prenorm_ambiguous(h64, gain, eps, rel=4e-7):
     return (v != lo) & (np.abs(v - mid) <= rel * np.abs(v))
 
 
+def bf16_neighbour_toward(lo, v):
+    """The BF16 value next to lo (a BF16 value) on the side of v."""
+    lo = np.asarray(lo, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    b = (lo.astype(np.float32).view(np.uint32) >> 16).astype(np.int64)
+    step = np.where(np.abs(v) > np.abs(lo), 1, -1)       # BF16 is sign-magnitude
+    nb = np.where(lo != 0, b + step, b)
+    return ((nb.astype(np.uint32) << 16).view(np.float32)).astype(np.float64)
+
+
+def validated_prenorm_x(x_gpu, h64, gain, eps, rel=4e-7):
+    """The GPU's BF16 pre-norm output, checked element by element: each
+    element must equal the oracle's BF16 rounding of the FP64 value, or --
+    where that value lies within `rel` of a rounding midpoint, so that FP32
+    arithmetic may round either way (prenorm_ambiguous) -- the BF16 neighbour
+    on the other side of the midpoint. Returns (the validated x as FP64, the
+    number of elements that took the other rounding); the oracle routes and
+    runs the experts on this x, so no token needs to be left out."""
+    v = O.rms_norm(np.asarray(h64, dtype=np.float64), gain, eps)
+    lo = O.bf16_round(v).astype(np.float64)
+    amb = prenorm_ambiguous(h64, gain, eps, rel)
+    other = bf16_neighbour_toward(lo, v)
+    xg = np.asarray(x_gpu, dtype=np.float64)
+    ok = (xg == lo) | (amb & (xg == other))
+    if not ok.all():
+        r, c = np.argwhere(~ok)[0]
+        raise AssertionError(f"{(~ok).sum()} pre-norm elements are neither rounding; first "
+                             f"[{r}, {c}]: gpu {xg[r, c]!r}, oracle {lo[r, c]!r}, exact {v[r, c]!r}")
+    return xg, int((ok & (xg != lo)).sum())
+
+
+def unit_cover_tokens(gpu_idx, E, tiling, size):
+    """Tokens whose outputs together pass through every expert-GEMM work unit
+    of a call: for every expert, the last token (in the expert's row order,
+    ascending token) of each of its row groups. tiling 'groups': the 2-SM
+    wide kernel's ceil(n / size) balanced groups (sizes differing by at most
+    one); 'tiles': consecutive tiles of `size` rows (token-major and
+    weight-major kernels). The last token of a group also lies in its last,
+    possibly partial, 16-row MMA block."""
+    gpu_idx = np.asarray(gpu_idx)
+    picks = set()
+    for e in range(E):
+        toks = np.nonzero((gpu_idx == e).any(axis=1))[0]
+        n = len(toks)
+        if n == 0:
+            continue
+        if tiling == "groups":
+            g = (n + size - 1) // size
+            q, extra = divmod(n, g)
+            ends = [i * q + min(i, extra) + q + (1 if i < extra else 0) - 1 for i in range(g)]
+        else:
+            ends = [min((j + 1) * size, n) - 1 for j in range((n + size - 1) // size)]
+        picks.update(int(toks[p]) for p in ends)
+    return np.array(sorted(picks), dtype=np.int64)
+
+
 # ---------------------------------------------------------------- NVFP4
 def sf_index(r, b, K, tile=128):
     """Byte of row r, 16-element block b in the library's SF-group layout

@@ -8,7 +8,7 @@ import torch
 
 import beam_synth as S
 import oracle as O
-from _helpers import OUT_REL_TOL, host, prenorm_ambiguous, rel_err
+from _helpers import OUT_REL_TOL, host, rel_err, validated_prenorm_x
 
 pytestmark = pytest.mark.gpu
 
@@ -25,17 +25,24 @@ def B():
 def _check(B, T, H, I, seed, pre_norm=False, residual_k=0, fp32_out=False, sample=None):
     x, wg, wu, wd = S.dense_inputs(T, H, I, seed, "cuda")
     flags = (B.FLAG_PRE_NORM if pre_norm else 0) | (B.FLAG_FP32_OUT if fp32_out else 0)
-    out = B.dense_forward(T, H, I, x, wg, wu, wd, residual_k=residual_k, flags=flags)
+    dp = B.DenseParams(T, H, I, 1e-6, residual_k, flags)
+    ws = torch.empty(B.dense_workspace_size(dp), dtype=torch.uint8, device="cuda")
+    out = B.dense_forward(T, H, I, x, wg, wu, wd, residual_k=residual_k, flags=flags, workspace=ws)
     assert B.status() == 0, B.last_error()
     toks = np.arange(T) if sample is None else sample
-    x64 = host(x).astype(np.float64)[toks]
+    h64 = host(x).astype(np.float64)[toks]
     if pre_norm:
-        amb = prenorm_ambiguous(x64, None, 1e-6)
-        toks = toks[~amb.any(axis=1)]
-        x64 = host(x).astype(np.float64)[toks]
-    r = O.dense_mlp_forward(x64, host(wg), host(wu), host(wd), pre_norm=pre_norm,
-                            residual_k=residual_k)
-    want = r["h"] if residual_k else r["out"]
+        # the GPU's BF16 x, each element the oracle's rounding or (on a
+        # midpoint) the other one; the oracle's MLP runs on it
+        lay = B.dense_workspace_layout(dp)
+        xg = ws[lay["xn"]:lay["xn"] + T * H * 2].view(torch.bfloat16).float().cpu().numpy()
+        xn, _ = validated_prenorm_x(xg.reshape(T, H)[toks], h64, None, 1e-6)
+        r = O.dense_mlp_forward(xn, host(wg), host(wu), host(wd), pre_norm=False)
+        want = O.residual_step(h64, r["out"], residual_k) if residual_k else r["out"]
+    else:
+        r = O.dense_mlp_forward(h64, host(wg), host(wu), host(wd), pre_norm=False,
+                                residual_k=residual_k)
+        want = r["h"] if residual_k else r["out"]
     err = rel_err(host(out)[toks], want)
     assert err <= OUT_REL_TOL, f"rel err {err}"
     return err

@@ -11,7 +11,7 @@ import torch
 import beam_synth as S
 import oracle as O
 from _helpers import (OUT_REL_TOL, act_rows_reader, check_act_codes_fp8, compare_routing,
-                      expert_getter_fp8, host, oracle_outputs_fp8_checked, prenorm_ambiguous,
+                      expert_getter_fp8, host, oracle_outputs_fp8_checked, validated_prenorm_x,
                       rel_err, weights_from_chosen)
 
 pytestmark = pytest.mark.gpu
@@ -185,25 +185,15 @@ def test_fp8_prenorm_residual(B):
     q = _quantize_experts(B, d)
     hk, idx, w, ws, p = _run(B, wl, d, q, B.FLAG_PRE_NORM, 50)
     h = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h, None, wl.rms_eps)
-    xo = O.bf16_round(O.rms_norm(h, None, wl.rms_eps)).astype(np.float64)
-    clean = np.nonzero(~amb.any(axis=1))[0]
-    assert len(clean) >= wl.T // 2
+    lay = B.workspace_layout(p)
+    xg = ws[lay["xn"]:lay["xn"] + wl.T * wl.H * 2].view(torch.bfloat16).float().cpu().numpy()
+    # the GPU's BF16 x, each element the oracle's rounding or (on a midpoint) the other one
+    xo, _ = validated_prenorm_x(xg.reshape(wl.T, wl.H), h, None, wl.rms_eps)
     sel = O.route(xo, host(d["w_router"]), None, 8, 4, 8, 2.5)
-    sub = {k: (v[clean] if isinstance(v, np.ndarray) and v.shape[:1] == (wl.T,) else v)
-           for k, v in sel.items()}
-    _, chosen_clean = compare_routing(sub, idx.cpu().numpy()[clean], w.cpu().numpy()[clean], wl)
-    # tokens with an ambiguous pre-norm element keep the GPU's routing for the
-    # row order only; they are not compared
-    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
-    chosen = [(gi[t], gw[t].astype(np.float64)) for t in range(wl.T)]
-    for j, t in enumerate(clean):
-        chosen[t] = chosen_clean[j]
-    o, ok = _expected(xo, idx, chosen, q, ws, B.workspace_layout(p), wl)
-    use = np.intersect1d(clean, np.nonzero(ok)[0])
-    assert len(use) >= wl.T // 2
-    want = O.residual_step(h[use], o[use], 50, None, wl.rms_eps, True)
-    assert rel_err(host(hk)[use], want) <= OUT_REL_TOL
+    _, chosen = compare_routing(sel, idx.cpu().numpy(), w.cpu().numpy(), wl)
+    o, _ = _expected(xo, idx, chosen, q, ws, lay, wl)
+    want = O.residual_step(h, o, 50, None, wl.rms_eps, True)
+    assert rel_err(host(hk), want) <= OUT_REL_TOL
 
 
 def test_fp8_rejects_missing_flag(B):

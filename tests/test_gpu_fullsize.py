@@ -1,8 +1,15 @@
 """GPU parity at the layer's full size (H=5120, E=256, I=2560, 20 GB of expert
-weights): routing of every token against the oracle, layer outputs on
-sampled tokens the oracle computes one by one, and the invariants that hold
-at any size. Includes the exact launch configuration the benchmark times
-(pre-norm, router, experts, post-norm, residual at k=50, T=64 and T=8192)."""
+weights): routing of every token against the oracle, layer outputs on tokens
+the oracle computes one by one, and the invariants that hold at any size.
+Includes the exact launch configuration the benchmark times (pre-norm,
+router, experts, post-norm, residual at k=50, T=64 and T=8192).
+
+With pre-norm, the GPU's BF16 x is read from the workspace and checked
+element by element (each element is the oracle's rounding, or the other one
+where the exact value sits on a rounding midpoint); the oracle then routes
+every token and runs the experts on that x. The output sample holds, for
+every expert, the last token of each of its row groups or tiles, so every
+work unit of both expert GEMMs (and every partial last block) is checked."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +19,8 @@ import oracle as O
 from _helpers import (OUT_REL_TOL, act_rows_reader, act_rows_reader_nvfp4, compare_routing,
                       expert_getter, expert_getter_fp8, expert_getter_nvfp4, host, nvfp4_pad,
                       oracle_outputs, oracle_outputs_fp8_checked, oracle_outputs_nvfp4_checked,
-                      prenorm_ambiguous, rel_err, sf_groups_to_plain, weights_from_chosen)
+                      rel_err, sf_groups_to_plain, unit_cover_tokens, validated_prenorm_x,
+                      weights_from_chosen)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +48,21 @@ def _forward(B, wl, d, flags=0, residual_k=0):
                     bias=d["bias"], topk_idx=idx, topk_w=w, workspace=ws)
     assert B.status() == 0, B.last_error()
     counts = ws[B.workspace_layout(p)["counts"]:][:wl.E * 4].view(torch.int32).cpu().numpy()
-    return out, idx.cpu().numpy(), w.cpu().numpy(), counts
+    return out, idx.cpu().numpy(), w.cpu().numpy(), counts, ws, p
+
+
+def _gpu_x(B, ws, p, wl):
+    """The GPU's BF16 pre-norm output, read from the workspace."""
+    lay = B.workspace_layout(p)
+    xn = ws[lay["xn"]:lay["xn"] + wl.T * wl.H * 2].view(torch.bfloat16)
+    return xn.float().cpu().numpy().reshape(wl.T, wl.H)
+
+
+def _prenorm(B, ws, p, wl, d):
+    """(h_prev, the validated pre-norm x, elements with the other rounding)."""
+    h64 = host(d["x"]).astype(np.float64)
+    x64, n_other = validated_prenorm_x(_gpu_x(B, ws, p, wl), h64, None, wl.rms_eps)
+    return h64, x64, n_other
 
 
 def _sample(T, n, seed):
@@ -48,23 +70,26 @@ def _sample(T, n, seed):
     return np.sort(rng.choice(T, size=min(n, T), replace=False))
 
 
-def _check(wl, d, out, gi, gw, sample, x64=None, h64=None, residual_k=0, clean=None):
-    """Routing of every (clean) token; outputs of the sampled tokens."""
+def _wide_cover(gi, wl, extra_seed=None):
+    """Last token of every token group of every expert (the wide 2-SM
+    kernel's units), plus a few random tokens."""
+    cover = unit_cover_tokens(gi, wl.E, "groups", 256)
+    if extra_seed is not None:
+        cover = np.union1d(cover, _sample(wl.T, 16, extra_seed))
+    return cover
+
+
+def _check(wl, d, out, gi, gw, sample, x64=None, h64=None, residual_k=0):
+    """Routing of every token; outputs of the sampled tokens."""
     if x64 is None:
         x64 = host(d["x"]).astype(np.float64)
-    toks = np.arange(wl.T) if clean is None else clean
-    sel = O.route(x64[toks], host(d["w_router"]), host(d["bias"]), wl.n_group,
-                  wl.topk_group, wl.top_k, wl.routed_scale)
-    ties, chosen = compare_routing(sel, gi[toks], gw[toks], wl)
-    pos = {int(t): i for i, t in enumerate(toks)}
-    samp = np.array([t for t in sample if int(t) in pos])
-    rows = [chosen[pos[int(t)]] for t in samp]
-    o = oracle_outputs(x64[samp], rows, np.arange(len(samp)), expert_getter(d))
-    if residual_k:
-        want = O.residual_step(h64[samp], o, residual_k, None, wl.rms_eps, True)
-    else:
-        want = o
-    err = rel_err(host(out)[samp], want)
+    sel = O.route(x64, host(d["w_router"]), host(d["bias"]), wl.n_group, wl.topk_group,
+                  wl.top_k, wl.routed_scale)
+    ties, chosen = compare_routing(sel, gi, gw, wl)
+    rows = [chosen[int(t)] for t in sample]
+    o = oracle_outputs(x64[sample], rows, np.arange(len(sample)), expert_getter(d))
+    want = O.residual_step(h64[sample], o, residual_k, None, wl.rms_eps, True) if residual_k else o
+    err = rel_err(host(out)[sample], want)
     assert err <= OUT_REL_TOL, f"rel err {err}"
     return int(ties.sum()), err
 
@@ -73,7 +98,7 @@ def test_decode_layer_T64(B):
     """Full Beam layer, decode regime: every token's output checked."""
     wl = S.WORKLOADS["decode"]
     d = S.make_inputs(wl, "cuda")
-    out, gi, gw, counts = _forward(B, wl, d, B.FLAG_FP32_OUT)
+    out, gi, gw, counts, *_ = _forward(B, wl, d, B.FLAG_FP32_OUT)
     n_ties, err = _check(wl, d, out, gi, gw, np.arange(wl.T))
     assert counts.sum() == wl.T * 8 and 180 <= (counts > 0).sum() <= 256
     print(f"decode: near ties {n_ties}, rel err {err:.2e}, touched {(counts > 0).sum()}")
@@ -82,72 +107,66 @@ def test_decode_layer_T64(B):
 @pytest.mark.parametrize("name", ["decode", "prefill"])
 def test_bench_configuration(B, name):
     """What the benchmark times: h_prev N(0,1) -> pre-norm -> MoE -> post-norm
-    -> residual k=50, at T=64 and T=8192."""
+    -> residual k=50, at T=64 (every token's output) and T=8192 (every work
+    unit's last token)."""
     wl = S.WORKLOADS[name]
     d = S.make_inputs(wl, "cuda")
-    hk, gi, gw, counts = _forward(B, wl, d, B.FLAG_PRE_NORM, 50)
-    h64 = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
-    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
-    clean = np.nonzero(~amb.any(axis=1))[0]
-    assert len(clean) >= 0.8 * wl.T
-    sample = _sample(wl.T, 64 if wl.T <= 64 else 16, 1)
-    n_ties, err = _check(wl, d, hk, gi, gw, sample, x64=x64, h64=h64, residual_k=50,
-                         clean=clean)
-    print(f"{name}: clean {len(clean)}/{wl.T}, near ties {n_ties}, rel err {err:.2e}")
+    hk, gi, gw, counts, ws, p = _forward(B, wl, d, B.FLAG_PRE_NORM, 50)
+    h64, x64, n_other = _prenorm(B, ws, p, wl, d)
+    sample = np.arange(wl.T) if wl.T <= 64 else _wide_cover(gi, wl, 1)
+    n_ties, err = _check(wl, d, hk, gi, gw, sample, x64=x64, h64=h64, residual_k=50)
+    print(f"{name}: other rounding {n_other} elements, near ties {n_ties}, "
+          f"outputs {len(sample)}, rel err {err:.2e}")
 
 
 def test_prefill_layer_T8192(B):
     wl = S.WORKLOADS["prefill"]
     d = S.make_inputs(wl, "cuda")
-    out, gi, gw, counts = _forward(B, wl, d, 0)
-    n_ties, err = _check(wl, d, out, gi, gw, _sample(wl.T, 16, 2))
+    out, gi, gw, counts, *_ = _forward(B, wl, d, 0)
+    sample = _wide_cover(gi, wl, 2)
+    n_ties, err = _check(wl, d, out, gi, gw, sample)
     assert counts.sum() == wl.T * 8 and (counts > 0).sum() == 256
     # any-size invariants: weights sum to 2.5, all experts distinct per token
     assert np.allclose(gw.sum(1), 2.5, atol=1e-5)
     assert all(len(set(r)) == 8 for r in gi.tolist())
-    print(f"prefill: near ties {n_ties}, rel err {err:.2e}, max/expert {counts.max()}")
+    print(f"prefill: near ties {n_ties}, outputs {len(sample)}, rel err {err:.2e}, "
+          f"max/expert {counts.max()}")
 
 
 def test_skewed_layer_T4096(B):
     wl = S.WORKLOADS["skew"]
     d = S.make_inputs(wl, "cuda")
-    out, gi, gw, counts = _forward(B, wl, d, 0)
-    hot = np.argsort(-counts)[:2]
-    # sample: a few tokens of the two hottest experts plus random tokens
-    hot_toks = np.nonzero(np.isin(gi, hot).any(axis=1))[0][:8]
-    sample = np.unique(np.concatenate([_sample(wl.T, 8, 3), hot_toks]))
+    out, gi, gw, counts, *_ = _forward(B, wl, d, 0)
+    # every group of every expert, the hottest (9 groups of about 244) included
+    sample = _wide_cover(gi, wl, 3)
     n_ties, err = _check(wl, d, out, gi, gw, sample)
     # Zipf-like load: hot experts take > 1000 tokens (about 9x the median);
     # with this recipe no expert ends up empty (empty experts are covered by
     # the small edge-case tests)
     assert counts.max() > 1000 and counts.max() > 8 * np.median(counts)
     print(f"skew: max {counts.max()}, median {np.median(counts)}, zero {(counts == 0).sum()}, "
-          f"near ties {n_ties}, rel err {err:.2e}")
+          f"near ties {n_ties}, outputs {len(sample)}, rel err {err:.2e}")
 
 
 def test_long_prefill_residual_T16384(B):
     wl = S.WORKLOADS["long_prefill"]
     d = S.make_inputs(wl, "cuda")
-    hk, gi, gw, counts = _forward(B, wl, d, B.FLAG_PRE_NORM, wl.residual_k)
-    h64 = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
-    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
-    clean = np.nonzero(~amb.any(axis=1))[0]
-    assert len(clean) >= 0.8 * wl.T
-    n_ties, err = _check(wl, d, hk, gi, gw, _sample(wl.T, 16, 4), x64=x64, h64=h64,
-                         residual_k=wl.residual_k, clean=clean)
+    hk, gi, gw, counts, ws, p = _forward(B, wl, d, B.FLAG_PRE_NORM, wl.residual_k)
+    h64, x64, n_other = _prenorm(B, ws, p, wl, d)
+    sample = _wide_cover(gi, wl, 4)
+    n_ties, err = _check(wl, d, hk, gi, gw, sample, x64=x64, h64=h64, residual_k=wl.residual_k)
     # the stream keeps unit scale: h = a*h_prev + b*n with |n| RMS 1
     rms = torch.sqrt(hk.float().pow(2).mean(1)).cpu().numpy()
     assert np.all(np.abs(rms - 1.0) < 0.05)
-    print(f"long prefill: clean {len(clean)}/{wl.T}, near ties {n_ties}, rel err {err:.2e}")
+    print(f"long prefill: other rounding {n_other}, near ties {n_ties}, outputs {len(sample)}, "
+          f"rel err {err:.2e}")
 
 
 @pytest.mark.parametrize("name", ["decode", "prefill"])
 def test_bench_configuration_fp8(B, name):
     """The E4M3 expert path as the benchmark times it (pre-norm, FP8
     experts, post-norm, residual k=50): the weight quantiser bit-exact on
-    sampled rows, routing of every clean token, and sampled tokens' outputs
+    sampled rows, routing of every token, and sampled tokens' outputs
     with each of their SwiGLU rows' codes validated."""
     wl = S.WORKLOADS[name]
     d = S.make_inputs(wl, "cuda")
@@ -171,29 +190,26 @@ def test_bench_configuration_fp8(B, name):
                        workspace=ws)
     assert B.status() == 0, B.last_error()
     gi, gw = idx.cpu().numpy(), w.cpu().numpy()
-    h64 = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
-    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
-    clean = np.nonzero(~amb.any(axis=1))[0]
-    assert len(clean) >= 0.8 * wl.T
-    sel = O.route(x64[clean], host(d["w_router"]), None, wl.n_group, wl.topk_group, wl.top_k,
+    h64, x64, n_other = _prenorm(B, ws, p, wl, d)
+    sel = O.route(x64, host(d["w_router"]), None, wl.n_group, wl.topk_group, wl.top_k,
                   wl.routed_scale)
-    ties, chosen = compare_routing(sel, gi[clean], gw[clean], wl)
-    sample = np.intersect1d(_sample(wl.T, 16, 5), clean)
-    o, _ = oracle_outputs_fp8_checked(x64, gi, weights_from_chosen(chosen, clean),
+    ties, chosen = compare_routing(sel, gi, gw, wl)
+    sample = np.arange(wl.T) if wl.T <= 64 else _wide_cover(gi, wl, 5)
+    o, _ = oracle_outputs_fp8_checked(x64, gi, weights_from_chosen(chosen),
                                       expert_getter_fp8(*q),
                                       act_rows_reader(ws, B.workspace_layout(p), wl.I), wl.E,
                                       tokens=sample)
     want = O.residual_step(h64[sample], o, 50, None, wl.rms_eps, True)
     err = rel_err(host(hk)[sample], want)
     assert err <= OUT_REL_TOL, f"rel err {err}"
-    print(f"{name} fp8: clean {len(clean)}/{wl.T}, near ties {int(ties.sum())}, rel err {err:.2e}")
+    print(f"{name} fp8: other rounding {n_other}, near ties {int(ties.sum())}, "
+          f"outputs {len(sample)}, rel err {err:.2e}")
 
 
 @pytest.mark.parametrize("name", ["decode", "prefill"])
 def test_bench_configuration_nvfp4(B, name):
     """The NVFP4 expert path as the benchmark times it: one expert matrix's
-    quantisation exact against the oracle, routing of every clean token,
+    quantisation exact against the oracle, routing of every token,
     sampled tokens' outputs with each SwiGLU row's quantisation validated."""
     wl = S.WORKLOADS[name]
     d = S.make_inputs(wl, "cuda")
@@ -217,21 +233,21 @@ def test_bench_configuration_nvfp4(B, name):
                          workspace=ws)
     assert B.status() == 0, B.last_error()
     gi, gw = idx.cpu().numpy(), w.cpu().numpy()
-    h64 = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h64, None, wl.rms_eps)
-    x64 = O.bf16_round(O.rms_norm(h64, None, wl.rms_eps)).astype(np.float64)
-    clean = np.nonzero(~amb.any(axis=1))[0]
-    assert len(clean) >= 0.8 * wl.T
-    sel = O.route(x64[clean], host(d["w_router"]), None, wl.n_group, wl.topk_group, wl.top_k,
+    h64, x64, n_other = _prenorm(B, ws, p, wl, d)
+    sel = O.route(x64, host(d["w_router"]), None, wl.n_group, wl.topk_group, wl.top_k,
                   wl.routed_scale)
-    ties, chosen = compare_routing(sel, gi[clean], gw[clean], wl)
-    sample = np.intersect1d(_sample(wl.T, 12, 6), clean)
+    ties, chosen = compare_routing(sel, gi, gw, wl)
     pad = nvfp4_pad(wl.T, wl.top_k, wl.E)
-    o = oracle_outputs_nvfp4_checked(x64, gi, weights_from_chosen(chosen, clean),
+    # decode: every token; prefill: the last token of every 128-row tile of
+    # every expert (the token-major kernel's sub-units)
+    sample = (np.arange(wl.T) if wl.T <= 64 else
+              np.union1d(unit_cover_tokens(gi, wl.E, "tiles", 128), _sample(wl.T, 12, 6)))
+    o = oracle_outputs_nvfp4_checked(x64, gi, weights_from_chosen(chosen),
                                      expert_getter_nvfp4(*q),
                                      act_rows_reader_nvfp4(ws, B.workspace_layout(p), wl.I, pad),
                                      wl.E, pad, tokens=sample)
     want = O.residual_step(h64[sample], o, 50, None, wl.rms_eps, True)
     err = rel_err(host(hk)[sample], want)
     assert err <= OUT_REL_TOL, f"rel err {err}"
-    print(f"{name} nvfp4: clean {len(clean)}/{wl.T}, near ties {int(ties.sum())}, rel err {err:.2e}")
+    print(f"{name} nvfp4: other rounding {n_other}, near ties {int(ties.sum())}, "
+          f"outputs {len(sample)}, rel err {err:.2e}")

@@ -13,7 +13,7 @@ import beam_synth as S
 import oracle as O
 from _helpers import (OUT_REL_TOL, act_rows_reader_nvfp4, check_act_codes_nvfp4,
                       compare_routing, expert_getter_nvfp4, host, nvfp4_pad,
-                      oracle_outputs_nvfp4_checked, prenorm_ambiguous, rel_err,
+                      oracle_outputs_nvfp4_checked, rel_err, validated_prenorm_x,
                       sf_groups_to_plain, weights_from_chosen)
 
 pytestmark = pytest.mark.gpu
@@ -189,18 +189,18 @@ def test_nvfp4_prenorm_residual(B):
     q = _quantize_experts(B, d)
     hk, idx, w, ws, p = _run(B, wl, d, q, B.FLAG_PRE_NORM, 50)
     h = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h, None, wl.rms_eps)
-    xo = O.bf16_round(O.rms_norm(h, None, wl.rms_eps)).astype(np.float64)
-    clean = np.nonzero(~amb.any(axis=1))[0]
-    assert len(clean) >= wl.T // 2
-    sel = O.route(xo[clean], host(d["w_router"]), None, 8, 4, 8, 2.5)
-    _, chosen = compare_routing(sel, idx.cpu().numpy()[clean], w.cpu().numpy()[clean], wl)
+    lay = B.workspace_layout(p)
+    xg = ws[lay["xn"]:lay["xn"] + wl.T * wl.H * 2].view(torch.bfloat16).float().cpu().numpy()
+    # the GPU's BF16 x, each element the oracle's rounding or (on a midpoint) the other one
+    xo, _ = validated_prenorm_x(xg.reshape(wl.T, wl.H), h, None, wl.rms_eps)
+    sel = O.route(xo, host(d["w_router"]), None, 8, 4, 8, 2.5)
+    _, chosen = compare_routing(sel, idx.cpu().numpy(), w.cpu().numpy(), wl)
     o = oracle_outputs_nvfp4_checked(
-        xo, idx.cpu().numpy(), weights_from_chosen(chosen, clean), expert_getter_nvfp4(*q),
-        act_rows_reader_nvfp4(ws, B.workspace_layout(p), wl.I, nvfp4_pad(wl.T, wl.top_k, wl.E)),
-        wl.E, nvfp4_pad(wl.T, wl.top_k, wl.E), tokens=clean)
-    want = O.residual_step(h[clean], o, 50, None, wl.rms_eps, True)
-    assert rel_err(host(hk)[clean], want) <= OUT_REL_TOL
+        xo, idx.cpu().numpy(), weights_from_chosen(chosen), expert_getter_nvfp4(*q),
+        act_rows_reader_nvfp4(ws, lay, wl.I, nvfp4_pad(wl.T, wl.top_k, wl.E)),
+        wl.E, nvfp4_pad(wl.T, wl.top_k, wl.E))
+    want = O.residual_step(h, o, 50, None, wl.rms_eps, True)
+    assert rel_err(host(hk), want) <= OUT_REL_TOL
 
 
 def test_nvfp4_rejects_wrong_flags(B):

@@ -11,7 +11,7 @@ import torch
 import beam_synth as S
 import oracle as O
 from _helpers import (OUT_REL_TOL, bf16_ulp, compare_routing, expert_getter, host,
-                      oracle_outputs, prenorm_ambiguous, rel_err)
+                      oracle_outputs, rel_err, validated_prenorm_x)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +39,15 @@ def _run_forward(B, wl, d, flags, residual_k=0):
                     bias=d["bias"], topk_idx=idx, topk_w=w, workspace=ws)
     assert B.status() == 0, B.last_error()
     return out, idx, w, ws, p
+
+
+def _workspace_x(B, ws, p, wl, h64, gain=None):
+    """The GPU's BF16 pre-norm x from the workspace, validated element by
+    element against the oracle (validated_prenorm_x)."""
+    lay = B.workspace_layout(p)
+    xg = ws[lay["xn"]:lay["xn"] + wl.T * wl.H * 2].view(torch.bfloat16).float().cpu().numpy()
+    x64, _ = validated_prenorm_x(xg.reshape(wl.T, wl.H), h64, gain, wl.rms_eps)
+    return x64
 
 
 def _oracle_sel(wl, d):
@@ -124,18 +133,14 @@ def test_route_bias_and_prenorm(B):
                           seed=4, device="cuda", skew_bias=True)
     gain = (1.0 + 0.1 * torch.randn(wl.H, generator=torch.Generator().manual_seed(1))).cuda()
     p = _params(B, wl, B.FLAG_PRE_NORM | B.FLAG_RETURN_SCORES)
-    idx, w, sc = B.route(p, d["x"], d["w_router"], bias=d["bias"], pre_gain=gain)
+    ws = B.alloc_workspace(p)
+    idx, w, sc = B.route(p, d["x"], d["w_router"], bias=d["bias"], pre_gain=gain, workspace=ws)
+    assert B.status() == 0
     h = host(d["x"]).astype(np.float64)
     g64 = gain.double().cpu().numpy()
-    amb = prenorm_ambiguous(h, g64, wl.rms_eps)
-    xo = O.bf16_round(O.rms_norm(h, g64, wl.rms_eps)).astype(np.float64)
+    xo = _workspace_x(B, ws, p, wl, h, g64)
     sel = O.route(xo, host(d["w_router"]), host(d["bias"]), 8, 4, 8, 2.5)
-    clean = ~amb.any(axis=1)
-    assert clean.sum() >= wl.T // 2
-    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
-    sub = {k: (v[clean] if isinstance(v, np.ndarray) and v.shape[:1] == (wl.T,) else v)
-           for k, v in sel.items()}
-    compare_routing(sub, gi[clean], gw[clean], wl)
+    compare_routing(sel, idx.cpu().numpy(), w.cpu().numpy(), wl)
 
 
 # ---------------------------------------------------------------- layer
@@ -302,20 +307,19 @@ def test_forward_token_major_residual(B):
                     wr_std=0.05, pre_norm=True, residual_k=9)
     d = S.make_inputs(wl, "cuda")
     p = _params(B, wl, B.FLAG_PRE_NORM, 9)
+    ws = B.alloc_workspace(p)
     idx = torch.empty((wl.T, 8), dtype=torch.int32, device="cuda")
     w = torch.empty((wl.T, 8), dtype=torch.float32, device="cuda")
     hk = B.forward(p, d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"],
-                   topk_idx=idx, topk_w=w)
+                   topk_idx=idx, topk_w=w, workspace=ws)
     assert B.status() == 0
     h = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h, None, wl.rms_eps)
-    xo = O.bf16_round(O.rms_norm(h, None, wl.rms_eps)).astype(np.float64)
-    clean = np.nonzero(~amb.any(axis=1))[0]
-    sel = O.route(xo[clean], host(d["w_router"]), None, 1, 1, 8, 2.5)
-    _, chosen = compare_routing(sel, idx.cpu().numpy()[clean], w.cpu().numpy()[clean], wl)
-    o = oracle_outputs(xo[clean], chosen, np.arange(len(clean)), expert_getter(d))
-    want = O.residual_step(h[clean], o, 9, None, wl.rms_eps, True)
-    assert rel_err(host(hk)[clean], want) <= OUT_REL_TOL
+    xo = _workspace_x(B, ws, p, wl, h)
+    sel = O.route(xo, host(d["w_router"]), None, 1, 1, 8, 2.5)
+    _, chosen = compare_routing(sel, idx.cpu().numpy(), w.cpu().numpy(), wl)
+    o = oracle_outputs(xo, chosen, np.arange(wl.T), expert_getter(d))
+    want = O.residual_step(h, o, 9, None, wl.rms_eps, True)
+    assert rel_err(host(hk), want) <= OUT_REL_TOL
 
 
 # ---------------------------------------------------------------- residual
@@ -355,22 +359,13 @@ def test_forward_prenorm_residual_small(B):
                    topk_idx=idx, topk_w=w, workspace=ws)
     assert B.status() == 0
     h = host(d["x"]).astype(np.float64)
-    amb = prenorm_ambiguous(h, None, wl.rms_eps)
-    xo = O.bf16_round(O.rms_norm(h, None, wl.rms_eps)).astype(np.float64)
     # the kernel's BF16 x equals the oracle's except where both roundings are valid
-    lay = B.workspace_layout(p)
-    xg = ws[lay["xn"]:lay["xn"] + wl.T * wl.H * 2].view(torch.bfloat16).float().cpu().numpy()
-    xg = xg.reshape(wl.T, wl.H)
-    bad = (xg != xo) & ~amb
-    assert not bad.any()
-    clean = np.nonzero(~amb.any(axis=1))[0]
+    xo = _workspace_x(B, ws, p, wl, h)
     sel = O.route(xo, host(d["w_router"]), None, 8, 4, 8, 2.5)
-    sub = {k: (v[clean] if isinstance(v, np.ndarray) and v.shape[:1] == (wl.T,) else v)
-           for k, v in sel.items()}
-    _, chosen = compare_routing(sub, idx.cpu().numpy()[clean], w.cpu().numpy()[clean], wl)
-    o = oracle_outputs(xo[clean], chosen, np.arange(len(clean)), expert_getter(d))
-    want = O.residual_step(h[clean], o, 50, None, wl.rms_eps, True)
-    assert rel_err(host(hk)[clean], want) <= OUT_REL_TOL
+    _, chosen = compare_routing(sel, idx.cpu().numpy(), w.cpu().numpy(), wl)
+    o = oracle_outputs(xo, chosen, np.arange(wl.T), expert_getter(d))
+    want = O.residual_step(h, o, 50, None, wl.rms_eps, True)
+    assert rel_err(host(hk), want) <= OUT_REL_TOL
 
 
 # ---------------------------------------------------------------- failures

@@ -172,3 +172,86 @@ def test_prenorm_ambiguity_flags_an_exact_midpoint():
     h = rng.normal(size=(64, 256))
     frac = Hp.prenorm_ambiguous(h, None, eps).mean()
     assert frac < 1e-3                                    # rare on random rows
+
+
+# ------------------------------------------------ pre-norm x and unit cover
+def test_bf16_neighbour_matches_torch_nextafter():
+    """The other rounding candidate is torch's BF16 nextafter toward v."""
+    import torch
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(4000) * np.exp2(rng.integers(-20, 20, 4000))
+    lo = O.bf16_round(v).astype(np.float64)
+    keep = lo != v
+    got = Hp.bf16_neighbour_toward(lo[keep], v[keep])
+    # torch's nextafter toward a target well beyond lo on the side of v (v
+    # itself would round to lo or to the neighbour in BF16)
+    away = np.sign(v[keep] - lo[keep]) * np.sign(lo[keep]) > 0
+    tgt = np.where(away, lo[keep] * 2.0, lo[keep] / 2.0)
+    want = torch.nextafter(torch.tensor(lo[keep]).to(torch.bfloat16),
+                           torch.tensor(tgt).to(torch.bfloat16)).double().numpy()
+    assert np.array_equal(got, want)
+
+
+def _prenorm_case(seed=11, T=40, H=256):
+    rng = np.random.default_rng(seed)
+    h = O.bf16_round(rng.standard_normal((T, H))).astype(np.float64)
+    x = O.bf16_round(O.rms_norm(h, None, 1e-6)).astype(np.float64)
+    return h, x
+
+
+def test_validated_prenorm_accepts_oracle_and_other_rounding_at_midpoints():
+    h, x = _prenorm_case()
+    got, n_other = Hp.validated_prenorm_x(x, h, None, 1e-6)
+    assert np.array_equal(got, x) and n_other == 0
+    # flip an element the checker calls ambiguous (make one by widening `rel`)
+    amb = Hp.prenorm_ambiguous(h, None, 1e-6, rel=1e-3)
+    r, c = np.argwhere(amb)[0]
+    v = O.rms_norm(h, None, 1e-6)
+    y = x.copy()
+    y[r, c] = Hp.bf16_neighbour_toward(x[r, c], v[r, c])
+    _, n_other = Hp.validated_prenorm_x(y, h, None, 1e-6, rel=1e-3)
+    assert n_other == 1
+
+
+def test_validated_prenorm_rejects_wrong_rounding():
+    h, x = _prenorm_case()
+    v = O.rms_norm(h, None, 1e-6)
+    amb = Hp.prenorm_ambiguous(h, None, 1e-6)
+    r, c = np.argwhere(~amb)[5]
+    for bad in (Hp.bf16_neighbour_toward(x[r, c], v[r, c]),          # the other rounding
+                Hp.bf16_neighbour_toward(x[r, c], -3 * v[r, c])):      # the far neighbour
+        y = x.copy()
+        y[r, c] = bad
+        with pytest.raises(AssertionError):
+            Hp.validated_prenorm_x(y, h, None, 1e-6)
+
+
+def _groups_brute(n, size):
+    """Balanced groups written out: ceil(n/size) groups, sizes differing by
+    at most one, the larger ones first."""
+    g = -(-n // size)
+    sizes = [n // g + (1 if i < n % g else 0) for i in range(g)]
+    out, s = [], 0
+    for z in sizes:
+        out.append(range(s, s + z))
+        s += z
+    return out
+
+
+@pytest.mark.parametrize("tiling,size", [("groups", 256), ("tiles", 128), ("tiles", 32)])
+def test_unit_cover_hits_every_group(tiling, size):
+    rng = np.random.default_rng(5)
+    T, E, K = 3000, 16, 8
+    gi = np.stack([rng.choice(E, K, replace=False) for _ in range(T)])
+    gi[:1200, 0] = 3                         # one hot expert: several groups
+    gi[:1200] = np.stack([np.concatenate([[3], rng.choice(np.delete(np.arange(E), 3), K - 1,
+                                                          replace=False)]) for _ in range(1200)])
+    picks = set(Hp.unit_cover_tokens(gi, E, tiling, size).tolist())
+    for e in range(E):
+        toks = np.nonzero((gi == e).any(axis=1))[0]
+        groups = (_groups_brute(len(toks), size) if tiling == "groups" else
+                  [range(j, min(j + size, len(toks))) for j in range(0, len(toks), size)])
+        for grp in groups:
+            assert any(int(toks[p]) in picks for p in grp), (e, grp)
+            assert int(toks[grp[-1]]) in picks          # the group's last row
+    assert len(picks) <= sum(-(-int((gi == e).any(1).sum()) // size) for e in range(E))

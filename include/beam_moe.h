@@ -429,6 +429,71 @@ beam_status_t beam_moe_route_static(const beam_moe_params* p, const void* x,
                                     const float* pre_gain, int32_t* topk_idx, float* topk_w,
                                     float* scores, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Expert parallelism ([P1] section 多 GPU 和多节点: each expert lives on one
+ * device and the device count divides the 256 experts; [P1] 专家混合模型 and
+ * 残差流 for what each step computes). P ranks, rank d owning experts
+ * [d E/P, (d+1) E/P). A rank routes its own tokens (beam_moe_route; the
+ * router weight is replicated), beam_ep_dispatch orders the token-expert
+ * pairs for sending, the caller exchanges them (an all-to-all of its own
+ * choosing), each owner runs beam_moe_forward_routed on the rows it
+ * received, the outputs travel back in the same order, and beam_ep_combine
+ * finishes the sublayer on the source rank.
+ * ------------------------------------------------------------------------ */
+
+/* The sublayer with the routing given instead of computed: the permutation,
+ * the expert GEMMs, the weighted combine and the output or post-norm +
+ * residual of beam_moe_forward, for BF16 experts.
+ *   p          T rows ("tokens"), E = the experts in w_gate/w_up/w_down,
+ *              top_k slots per row; flags PRE_NORM / FP32_OUT as in
+ *              beam_moe_forward (FP8_EXPERTS and NVFP4_EXPERTS are refused)
+ *   x_in       [T,H] bf16 (normalised first with BEAM_FLAG_PRE_NORM)
+ *   topk_idx   [T,top_k] int32 expert of each slot, in [0, E); an index
+ *              outside it sets the device error flag (BEAM_ERR_DEVICE_FLAG
+ *              from beam_status) and its slot is dropped
+ *   topk_w     [T,top_k] fp32 combine weight of each slot
+ *   the rest as in beam_moe_forward; workspace: beam_moe_workspace_size(p).
+ * An expert owner calls it with its received rows, their local expert ids,
+ * weights 1, top_k = 1, BEAM_FLAG_FP32_OUT and no residual: out[r] is then
+ * the FP32 output of row r's expert. */
+beam_status_t beam_moe_forward_routed(const beam_moe_params* p, const void* x_in,
+                                      const int32_t* topk_idx, const float* topk_w,
+                                      const void* w_gate, const void* w_up, const void* w_down,
+                                      const float* pre_gain, const float* post_gain, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Orders a rank's token-expert pairs for sending: by expert (so by owning
+ * rank), stable by pair p = t*top_k + j.
+ *   p          the layer (T, H, E, I, top_k as for beam_moe_route);
+ *              n_ranks divides E
+ *   x          [T,H] bf16 rows to send (the normalised x when the layer
+ *              pre-norms: beam_moe_route writes it to workspace entry 0)
+ *   topk_idx   [T,top_k] int32 global expert ids, in [0, E)
+ *   send_x     [T*top_k,H] bf16 out: x of each pair, in send order
+ *   send_expert [T*top_k] int32 out: global expert of each sent row
+ *   pair_row   [T*top_k] int32 out: send position of pair p
+ *   send_counts [n_ranks] int32 out: rows for each rank (contiguous blocks
+ *              in rank order)
+ *   workspace  beam_moe_workspace_size(p) bytes (may be the router's)
+ * Device pointers; asynchronous on `stream`. */
+beam_status_t beam_ep_dispatch(const beam_moe_params* p, int n_ranks, const void* x,
+                               const int32_t* topk_idx, void* send_x, int32_t* send_expert,
+                               int32_t* pair_row, int32_t* send_counts, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Finishes the sublayer on the source rank from the expert outputs returned
+ * in send order:
+ *   o[t]  = sum_j topk_w[t,j] * recv_y[pair_row[t*top_k+j]]   (FP32, slot order)
+ *   out[t] = residual_k >= 2 ? bf16(sqrt((k-1)/k) h_prev[t] + RMSNorm(o[t]) * post_gain / sqrt(k))
+ *                            : o[t] (bf16, or fp32 when out_f32)
+ *   recv_y [T*top_k,H] fp32; pair_row [T*top_k] int32 (from beam_ep_dispatch);
+ *   topk_w [T,top_k] fp32; h_prev [T,H] bf16 (the layer input, with the
+ *   residual); post_gain [H] fp32 or NULL; H a multiple of 128, at most 8192. */
+beam_status_t beam_ep_combine(int T, int top_k, int H, const float* recv_y,
+                              const int32_t* pair_row, const float* topk_w, const void* h_prev,
+                              const float* post_gain, float eps, int residual_k, int out_f32,
+                              void* out, void* stream);
+
 /* ---- diagnostics (tests and tooling) ---------------------------------- */
 
 /* Byte offsets of the internal buffers inside the forward workspace, in this

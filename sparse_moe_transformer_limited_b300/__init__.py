@@ -14,7 +14,8 @@ from ._native import (BeamError, Params, make_params, workspace_size, workspace_
                       dense_workspace_size, dense_workspace_layout, FLAG_NVFP4_EXPERTS,
                       quantize_nvfp4, forward_nvfp4, dense_forward_nvfp4, AttnParams,
                       make_attn_params, attention_workspace_size, attention_forward,
-                      attention_workspace_layout, FLAG_PREFILL_WEIGHT_MAJOR)
+                      attention_workspace_layout, FLAG_PREFILL_WEIGHT_MAJOR, forward_routed,
+                      ep_dispatch, ep_combine)
 
 __all__ = ["BeamError", "Params", "make_params", "workspace_size", "workspace_layout",
            "alloc_workspace", "route", "route_static", "forward", "dense_forward", "DenseParams", "residual_step", "status", "last_error",
@@ -24,4 +25,5 @@ __all__ = ["BeamError", "Params", "make_params", "workspace_size", "workspace_la
            "dense_workspace_size", "dense_workspace_layout", "FLAG_NVFP4_EXPERTS",
            "quantize_nvfp4", "forward_nvfp4", "dense_forward_nvfp4", "AttnParams",
            "make_attn_params", "attention_workspace_size", "attention_forward",
-           "attention_workspace_layout", "FLAG_PREFILL_WEIGHT_MAJOR"]
+           "attention_workspace_layout", "FLAG_PREFILL_WEIGHT_MAJOR", "forward_routed",
+           "ep_dispatch", "ep_combine"]

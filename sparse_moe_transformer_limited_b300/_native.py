@@ -46,7 +46,8 @@ EXPORTED = ("beam_moe_workspace_size", "beam_moe_route", "beam_moe_route_static"
             "beam_dense_mlp_forward_fp8", "beam_dense_workspace_layout",
             "beam_quantize_nvfp4", "beam_moe_forward_nvfp4", "beam_dense_mlp_forward_nvfp4",
             "beam_attention_workspace_size", "beam_attention_forward",
-            "beam_attention_workspace_layout")
+            "beam_attention_workspace_layout", "beam_moe_forward_routed", "beam_ep_dispatch",
+            "beam_ep_combine")
 
 
 class BeamError(RuntimeError):
@@ -125,6 +126,12 @@ def lib() -> ctypes.CDLL:
         L.beam_attention_workspace_layout.restype = i32
         L.beam_attention_forward.argtypes = [A] + [vp] * 9 + [sz, vp]
         L.beam_attention_forward.restype = i32
+        L.beam_moe_forward_routed.argtypes = [P] + [vp] * 10 + [sz, vp]
+        L.beam_moe_forward_routed.restype = i32
+        L.beam_ep_dispatch.argtypes = [P, i32] + [vp] * 7 + [sz, vp]
+        L.beam_ep_dispatch.restype = i32
+        L.beam_ep_combine.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp]
+        L.beam_ep_combine.restype = i32
         L.beam_residual_step.argtypes = [vp, vp, i32, i32, i32, vp, f32, i32, i32, vp, vp]
         L.beam_residual_step.restype = i32
         L.beam_status.argtypes = [vp]
@@ -248,6 +255,55 @@ def forward(p: Params, x, w_router, w_gate, w_up, w_down, bias=None, pre_gain=No
                                   _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(pre_gain),
                                   _ptr(post_gain), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
                                   _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def forward_routed(p: Params, x, topk_idx, topk_w, w_gate, w_up, w_down, pre_gain=None,
+                   post_gain=None, out=None, workspace=None, stream=None):
+    """beam_moe_forward_routed: the sublayer with the routing given."""
+    dev = x.device
+    if out is None:
+        dt = torch.float32 if (p.flags & FLAG_FP32_OUT) else torch.bfloat16
+        out = torch.empty((p.T, p.H), dtype=dt, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(p, dev)
+    _check(lib().beam_moe_forward_routed(ctypes.byref(p), _ptr(x), _ptr(topk_idx), _ptr(topk_w),
+                                         _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(pre_gain),
+                                         _ptr(post_gain), _ptr(out), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)))
+    return out
+
+
+def ep_dispatch(p: Params, n_ranks: int, x, topk_idx, workspace=None, stream=None):
+    """beam_ep_dispatch: (send_x [T*k,H] bf16, send_expert [T*k], pair_row
+    [T*k], send_counts [n_ranks]) for the pairs of this rank's tokens."""
+    dev = x.device
+    R = p.T * p.top_k
+    send_x = torch.empty((R, p.H), dtype=torch.bfloat16, device=dev)
+    send_expert = torch.empty(R, dtype=torch.int32, device=dev)
+    pair_row = torch.empty(R, dtype=torch.int32, device=dev)
+    send_counts = torch.zeros(n_ranks, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(p, dev)
+    _check(lib().beam_ep_dispatch(ctypes.byref(p), n_ranks, _ptr(x), _ptr(topk_idx),
+                                  _ptr(send_x), _ptr(send_expert), _ptr(pair_row),
+                                  _ptr(send_counts), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)))
+    return send_x, send_expert, pair_row, send_counts
+
+
+def ep_combine(recv_y, pair_row, topk_w, h_prev=None, post_gain=None, eps=1e-6, residual_k=0,
+               out_f32=False, out=None, stream=None):
+    """beam_ep_combine: the source rank's weighted combine of the returned
+    expert outputs, then the output or the post-norm + residual."""
+    T, K = topk_w.shape
+    H = recv_y.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32 if out_f32 else torch.bfloat16,
+                          device=recv_y.device)
+    _check(lib().beam_ep_combine(T, K, H, _ptr(recv_y), _ptr(pair_row), _ptr(topk_w),
+                                 _ptr(h_prev), _ptr(post_gain), eps, residual_k, int(out_f32),
+                                 _ptr(out), _stream(stream)))
     return out
 
 

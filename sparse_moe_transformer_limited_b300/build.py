@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libbeam_moe.so")
 SOURCES = ["beam_moe.cu"]
 HEADERS = ["ptx.cuh", "kernels_gemm.cuh", "kernels_gemm_tm.cuh", "kernels_gemm_wide.cuh", "kernels_gemm_2sm.cuh",
-           "kernels_combine.cuh",
+           "kernels_combine.cuh", "kernels_ep.cuh",
            "kernels_permute.cuh", "kernels_quant.cuh", "kernels_router.cuh", "kernels_rows.cuh",
            "kernels_attn.cuh"]
 

@@ -19,6 +19,7 @@
 #include "beam_moe.h"
 #include "kernels_attn.cuh"
 #include "kernels_combine.cuh"
+#include "kernels_ep.cuh"
 #include "kernels_gemm.cuh"
 #include "kernels_gemm_tm.cuh"
 #include "kernels_gemm_wide.cuh"
@@ -1233,6 +1234,9 @@ beam_status_t beam_status(void* stream) {
   if (v & beam::DEV_ERR_ALIGN)
     return fail(BEAM_ERR_DEVICE_FLAG, "a device-side copy address was misaligned and skipped (flag 0x%x)", v);
   if (v & beam::DEV_ERR_TIMEOUT) return fail(BEAM_ERR_TIMEOUT, "a device-side wait timed out (flag 0x%x)", v);
+  if (v & beam::DEV_ERR_INDEX)
+    return fail(BEAM_ERR_DEVICE_FLAG,
+                "a given expert index was outside [0, E); its pair was dropped (flag 0x%x)", v);
   return fail(BEAM_ERR_DEVICE_FLAG, "device error flag 0x%x", v);
 }
 
@@ -1631,4 +1635,168 @@ extern "C" beam_status_t beam_moe_route_static(const beam_moe_params* p, const v
   return launch_router(*p, L, x, w_router, logit_bias, pre_gain, topk_idx, topk_w,
                        (p->flags & BEAM_FLAG_RETURN_SCORES) ? scores : nullptr,
                        static_cast<uint8_t*>(base), static_cast<cudaStream_t>(stream));
+}
+
+// ===========================================================================
+// Expert parallelism: the sublayer split by expert across ranks (routed
+// forward on the expert owners, dispatch and combine on the token owners).
+// ===========================================================================
+extern "C" beam_status_t beam_moe_forward_routed(const beam_moe_params* p, const void* x_in,
+                                                 const int32_t* topk_idx, const float* topk_w,
+                                                 const void* w_gate, const void* w_up,
+                                                 const void* w_down, const float* pre_gain,
+                                                 const float* post_gain, void* out, void* workspace,
+                                                 size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_params(p);
+  if (s != BEAM_OK) return s;
+  if (p->flags & (BEAM_FLAG_FP8_EXPERTS | BEAM_FLAG_NVFP4_EXPERTS))
+    return fail(BEAM_ERR_UNSUPPORTED, "beam_moe_forward_routed takes BF16 experts");
+  if (p->T == 0) return BEAM_OK;
+  if (!x_in || !topk_idx || !topk_w || !w_gate || !w_up || !w_down || !out || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  const void* ptrs[] = {x_in, topk_idx, topk_w, w_gate, w_up, w_down, out, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(BEAM_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", q);
+  if ((pre_gain && !aligned16(pre_gain)) || (post_gain && !aligned16(post_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "gains must be 16-byte aligned");
+  if (out == x_in) return fail(BEAM_ERR_INVALID_ARG, "out must not alias x_in");
+  const Layout L = make_layout(*p);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* idx = reinterpret_cast<int32_t*>(ws + L.off[L_IDX]);
+  float* wts = reinterpret_cast<float*>(ws + L.off[L_W]);
+  const long long n = static_cast<long long>(p->T) * p->top_k;
+  {
+    ProfScope ps("routed_copy", st);
+    beam::routed_copy_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        topk_idx, topk_w, n, p->E, idx, wts);
+  }
+  BEAM_LAUNCH_CHECK("routed_copy_kernel");
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_in);
+  if (p->flags & BEAM_FLAG_PRE_NORM) {
+    __nv_bfloat16* xn = reinterpret_cast<__nv_bfloat16*>(ws + L.off[L_XN]);
+    {
+      ProfScope ps("prenorm", st);
+      beam::prenorm_kernel<<<(p->T + 7) / 8, 256, 0, st>>>(x, pre_gain, xn, p->T, p->H, p->rms_eps);
+    }
+    BEAM_LAUNCH_CHECK("prenorm_kernel");
+    x = xn;
+  }
+  ExpertWeights w{};
+  w.gate = w_gate;
+  w.up = w_up;
+  w.down = w_down;
+  w.kind = beam::KIND_BF16;
+  return run_experts(*p, L, x_in, x, idx, wts, w, post_gain, out, ws, st, false);
+}
+
+extern "C" beam_status_t beam_ep_dispatch(const beam_moe_params* p, int n_ranks, const void* x,
+                                          const int32_t* topk_idx, void* send_x,
+                                          int32_t* send_expert, int32_t* pair_row,
+                                          int32_t* send_counts, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  beam_status_t s = check_params(p);
+  if (s != BEAM_OK) return s;
+  if (n_ranks <= 0 || p->E % n_ranks)
+    return fail(BEAM_ERR_INVALID_ARG, "n_ranks=%d must divide E=%d", n_ranks, p->E);
+  if (p->T == 0) return BEAM_OK;
+  if (!x || !topk_idx || !send_x || !send_expert || !pair_row || !send_counts || !workspace)
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(x) || !aligned16(send_x) || !aligned16(workspace))
+    return fail(BEAM_ERR_INVALID_ARG, "x, send_x and the workspace must be 16-byte aligned");
+  const Layout L = make_layout(*p);
+  if (workspace_bytes < L.total)
+    return fail(BEAM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, L.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const long long R = static_cast<long long>(p->T) * p->top_k;
+  int32_t* idx = reinterpret_cast<int32_t*>(ws + L.off[L_IDX]);
+  float* wts = reinterpret_cast<float*>(ws + L.off[L_W]);
+  int* blk_hist = reinterpret_cast<int*>(ws + L.off[L_BLKHIST]);
+  int* blk_off = reinterpret_cast<int*>(ws + L.off[L_BLKOFF]);
+  int* counts = reinterpret_cast<int*>(ws + L.off[L_COUNTS]);
+  int* offs = reinterpret_cast<int*>(ws + L.off[L_OFFS]);
+  int* row_tok = reinterpret_cast<int*>(ws + L.off[L_ROWTOK]);
+  float* row_w = reinterpret_cast<float*>(ws + L.off[L_ROWW]);
+  int4* ugu = reinterpret_cast<int4*>(ws + L.off[L_UGU]);
+  int* nunits = reinterpret_cast<int*>(ws + L.off[L_NUNITS]);
+  // the caller's routing, range-checked (weights are not needed here)
+  {
+    ProfScope ps("routed_copy", st);
+    beam::routed_copy_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(
+        topk_idx, wts, R, p->E, idx, wts);
+  }
+  BEAM_LAUNCH_CHECK("routed_copy_kernel");
+  {
+    ProfScope ps("expert_hist", st);
+    beam::expert_block_hist_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(idx, p->T, p->top_k,
+                                                                        p->E, blk_hist);
+  }
+  BEAM_LAUNCH_CHECK("expert_block_hist_kernel");
+  {
+    ProfScope ps("expert_scan_units", st);
+    beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, p->E, blk_off, counts, offs,
+                                                      ugu, nunits, L.NT, p->I / 128,
+                                                      path_mt_down(L.path, p->H), 1, row_tok);
+  }
+  BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
+  {
+    ProfScope ps("expert_scatter", st);
+    beam::expert_scatter_kernel<<<L.NB, beam::PERM_THREADS, 0, st>>>(
+        idx, wts, p->T, p->top_k, p->E, blk_off, pair_row, row_tok, row_w);
+  }
+  BEAM_LAUNCH_CHECK("expert_scatter_kernel");
+  {
+    ProfScope ps("gather_rows", st);
+    beam::gather_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), row_tok, static_cast<int>(R), p->H,
+        static_cast<__nv_bfloat16*>(send_x));
+  }
+  BEAM_LAUNCH_CHECK("gather_rows_kernel");
+  {
+    ProfScope ps("ep_meta", st);
+    beam::ep_meta_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(
+        offs, p->E, n_ranks, R, send_expert, send_counts);
+  }
+  BEAM_LAUNCH_CHECK("ep_meta_kernel");
+  return BEAM_OK;
+}
+
+extern "C" beam_status_t beam_ep_combine(int T, int top_k, int H, const float* recv_y,
+                                         const int32_t* pair_row, const float* topk_w,
+                                         const void* h_prev, const float* post_gain, float eps,
+                                         int residual_k, int out_f32, void* out, void* stream) {
+  if (T < 0 || H <= 0 || top_k <= 0 || top_k > 32)
+    return fail(BEAM_ERR_INVALID_ARG, "T=%d H=%d top_k=%d out of range", T, H, top_k);
+  if (H % 128 || H > 8192) return fail(BEAM_ERR_UNSUPPORTED, "H=%d must be a multiple of 128, at most 8192", H);
+  if (residual_k == 1 || residual_k < 0)
+    return fail(BEAM_ERR_INVALID_ARG, "residual_k=%d: use 0 (none) or k >= 2", residual_k);
+  if (out_f32 && residual_k >= 2)
+    return fail(BEAM_ERR_INVALID_ARG, "an FP32 output applies only without the residual step");
+  if (T == 0) return BEAM_OK;
+  if (!recv_y || !pair_row || !topk_w || !out || (residual_k >= 2 && !h_prev))
+    return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(recv_y) || !aligned16(out) || (h_prev && !aligned16(h_prev)) ||
+      (post_gain && !aligned16(post_gain)))
+    return fail(BEAM_ERR_INVALID_ARG, "recv_y, out, h_prev and post_gain must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int resid = residual_k >= 2;
+  const float kf = static_cast<float>(resid ? residual_k : 2);
+  const float a = resid ? std::sqrt((kf - 1.f) / kf) : 0.f;
+  const float b = resid ? 1.f / std::sqrt(kf) : 1.f;
+  ProfScope ps("ep_combine", st);
+  if (out_f32)
+    beam::ep_combine_kernel<true><<<T, beam::EP_COMBINE_THREADS, 0, st>>>(
+        recv_y, pair_row, topk_w, top_k, static_cast<const __nv_bfloat16*>(h_prev), post_gain,
+        out, H, eps, a, b, resid);
+  else
+    beam::ep_combine_kernel<false><<<T, beam::EP_COMBINE_THREADS, 0, st>>>(
+        recv_y, pair_row, topk_w, top_k, static_cast<const __nv_bfloat16*>(h_prev), post_gain,
+        out, H, eps, a, b, resid);
+  BEAM_LAUNCH_CHECK("ep_combine_kernel");
+  return BEAM_OK;
 }

@@ -297,3 +297,31 @@ def test_combined_output_buffer_is_per_token():
         assert lay["n_units"] - lay["oacc"] == _kb(T * 5120 * 4)
         n = B.workspace_size(_p(T=T))
         assert n - lay["arrive"] >= T * 4
+
+
+def test_expert_parallel_entry_points_check_args_on_host():
+    """The expert-parallel entry points reject bad arguments before any CUDA
+    call (no GPU here): a rank count that does not divide E, NULL or
+    misaligned pointers, quantised-expert flags on the routed forward, a
+    residual step of 1 or an FP32 output with the residual in the combine.
+    Empty batches are no-ops."""
+    lib = B.lib()
+    fake = ctypes.c_void_p(1 << 20)                 # 16-byte aligned, never read
+    p = ctypes.byref(_p())
+    assert lib.beam_ep_dispatch(p, 3, *([fake] * 7), 1 << 30, None) == 1
+    assert "must divide" in B.last_error()
+    assert lib.beam_ep_dispatch(p, 8, None, *([fake] * 6), 1 << 30, None) == 1
+    assert lib.beam_ep_dispatch(p, 8, ctypes.c_void_p((1 << 20) + 4), *([fake] * 6), 1 << 30,
+                                None) == 1
+    assert lib.beam_ep_dispatch(ctypes.byref(_p(T=0)), 8, *([None] * 7), 0, None) == 0
+    routed = lambda q, x: lib.beam_moe_forward_routed(q, x, *([fake] * 9), 1 << 30, None)
+    assert routed(ctypes.byref(_p(flags=B.FLAG_FP8_EXPERTS)), fake) == 2
+    assert routed(p, None) == 1
+    assert routed(ctypes.byref(_p(T=0)), None) == 0
+    comb = lambda T, k, H, rk, f32: lib.beam_ep_combine(T, k, H, fake, fake, fake, fake, None,
+                                                        1e-6, rk, f32, fake, None)
+    assert comb(4, 8, 5120, 1, 0) == 1
+    assert comb(4, 8, 5120, 50, 1) == 1
+    assert comb(4, 33, 5120, 0, 0) == 1
+    assert comb(4, 8, 5000, 0, 0) == 2
+    assert comb(0, 8, 5120, 50, 0) == 0

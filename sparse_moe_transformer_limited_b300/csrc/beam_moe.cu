@@ -129,17 +129,24 @@ GemmPath choose_path(const beam_moe_params& p) {
 }
 
 int path_nt(GemmPath g) { return g == PATH_W32 ? 32 : (g == PATH_W128 ? 128 : 256); }
-int path_mt_down(GemmPath g, int H) {
-  return g == PATH_WIDE ? (H + 511) / 512 : (g == PATH_TM ? H / 256 : H / 128);
+// Weight rows per unit of the weight-major down GEMM on 32-token tiles.
+int w32_down_rows(bool f4) {
+  return f4 ? beam::UnitRows<1, 32, beam::KIND_NVFP4>::value : beam::UnitRows<1, 32, beam::KIND_BF16>::value;
+}
+int path_mt_down(GemmPath g, int H, bool f4) {
+  if (g == PATH_WIDE) return (H + 511) / 512;
+  if (g == PATH_TM) return H / 256;
+  return g == PATH_W32 ? H / w32_down_rows(f4) : H / 128;
 }
 // Arrivals that complete one token in the fused combine of the down GEMM:
 // every (expert of the token, hidden slice, epilogue warp or lane group) adds
-// its share once. Weight-major: four warps of 32 hidden rows per 128-row tile;
-// wide: eight warps (64 hidden rows each, 32 in a last half slice) per slice
-// of 512 rows; token-major: two warps of 128 hidden columns per 256-column
-// tile.
-int combine_expected(GemmPath g, int H, int top_k) {
-  const int per_expert = g == PATH_WIDE ? 8 * ((H + 511) / 512) : (g == PATH_TM ? H / 128 : H / 32);
+// its share once. Weight-major: four warps per unit (of 128 or 256 hidden
+// rows); wide: eight warps (64 hidden rows each, 32 in a last half slice) per
+// slice of 512 rows; token-major: two warps of 128 hidden columns per
+// 256-column tile.
+int combine_expected(GemmPath g, int H, int top_k, bool f4) {
+  const int per_expert = g == PATH_WIDE ? 8 * ((H + 511) / 512)
+                         : (g == PATH_TM ? H / 128 : 4 * path_mt_down(g, H, f4));
   return top_k * per_expert;
 }
 
@@ -174,6 +181,7 @@ struct Layout {
   size_t total;
   int KS, NB, NT;
   GemmPath path;
+  bool f4;          // NVFP4 experts
   long long units_gu_max, units_dn_max;
 };
 
@@ -267,6 +275,7 @@ Layout make_layout(const beam_moe_params& p) {
   L.NT = path_nt(L.path);
   const long long R = static_cast<long long>(p.T) * p.top_k;
   const bool f4 = (p.flags & BEAM_FLAG_NVFP4_EXPERTS) != 0;
+  L.f4 = f4;
   L.pad = f4 ? (L.path == PATH_W32 ? 32 : 128) : 1;
   L.rows = f4 ? (R + (L.pad - 1) * std::min<long long>(p.E, R) + 127) / 128 * 128 : R;
   const long long Rr = L.rows;
@@ -285,7 +294,7 @@ Layout make_layout(const beam_moe_params& p) {
     L.units_dn_max = 2 * (groups * (p.H / 256) + static_cast<long long>(p.E) * (p.H / 512 + 1));
   } else {
     L.units_gu_max = tiles * (p.I / 128);
-    L.units_dn_max = tiles * path_mt_down(L.path, p.H);
+    L.units_dn_max = tiles * path_mt_down(L.path, p.H, f4);
   }
   size_t sz[kLayoutEntries];
   sz[L_XN] = (p.flags & BEAM_FLAG_PRE_NORM) ? static_cast<size_t>(p.T) * p.H * 2 : 0;
@@ -414,7 +423,7 @@ beam_status_t launch_gemm_tm(const CUtensorMap& w0, const CUtensorMap& w1, const
 template <int MODE, bool F8>
 beam_status_t launch_gemm_wide(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap (&tok)[4],
                                const beam::WideArgs& args, cudaStream_t st) {
-  using C = beam::WideCfg;
+  using C = beam::WideCfg<MODE>;
   auto kern = beam::expert_gemm_wide_kernel<MODE, F8>;
   beam_status_t sa = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (sa != BEAM_OK) return sa;
@@ -662,7 +671,6 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
   ga.b_sf = q.xsf;
   beam::GemmArgs gd = ga;
   gd.n_units = nunits + 1;
-  gd.m_tiles = H / 128;
   gd.k_blocks = I / KB;
   gd.a_rows_per_expert = H;
   gd.out = nullptr;
@@ -675,12 +683,16 @@ beam_status_t launch_expert_gemms(const beam_moe_params& prm, const Layout& L,
   gd.b_sf = q.asf;
   gd.comb = comb;
   // stage counts: NVFP4 stages also carry the K-block's block scales
-  constexpr int S_GU32 = F4 ? 5 : 6, S_DN32 = F4 ? 9 : 10;
+  // (the NVFP4 down GEMM on 32-token tiles loads two 128-row weight tiles
+  // per stage)
+  constexpr int S_GU32 = F4 ? 5 : 6, S_DN32 = F4 ? 5 : 10;
   if (L.path == PATH_W32) {
+    gd.m_tiles = H / beam::UnitRows<1, 32, KIND>::value;
     if ((s = launch_gemm<0, 32, S_GU32, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
     if ((s = quant_act()) != BEAM_OK) return s;
     if ((s = launch_gemm<1, 32, S_DN32, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
   } else {
+    gd.m_tiles = H / beam::UnitRows<1, 128, KIND>::value;
     if ((s = launch_gemm<0, 128, 4, KIND>(m_g, m_u, m_x, ga, st)) != BEAM_OK) return s;
     if ((s = quant_act()) != BEAM_OK) return s;
     if ((s = launch_gemm<1, 128, 6, KIND>(m_d, m_d, m_a, gd, st)) != BEAM_OK) return s;
@@ -738,7 +750,7 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   if (small) {
     ProfScope ps("expert_permute", st);
     beam::expert_permute_small_kernel<<<1, 256, 0, st>>>(
-        idx, wts, T, K, E, counts, offs, ugu, nunits, L.NT, I / 128, path_mt_down(L.path, H),
+        idx, wts, T, K, E, counts, offs, ugu, nunits, L.NT, I / 128, path_mt_down(L.path, H, L.f4),
         L.pad, pair_row, row_tok, row_w);
   } else if (dense) {
     ProfScope ps("dense_setup", st);
@@ -762,7 +774,7 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
     else
       beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, NB, E, blk_off, counts, offs,
                                                         ugu, nunits, L.NT, I / 128,
-                                                        path_mt_down(L.path, H), L.pad, row_tok);
+                                                        path_mt_down(L.path, H, L.f4), L.pad, row_tok);
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
   if (quant) {
@@ -811,7 +823,7 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   cb.done = arrive + T;
   cb.cursor = arrive + 2 * static_cast<size_t>(T);
   cb.T = T;
-  cb.expected = combine_expected(L.path, H, K);
+  cb.expected = combine_expected(L.path, H, K, L.f4);
   cb.row_token = row_tok;
   cb.row_weight = row_w;
   cb.row_scale = quant ? qb.ascale : nullptr;
@@ -1741,7 +1753,7 @@ extern "C" beam_status_t beam_ep_dispatch(const beam_moe_params* p, int n_ranks,
     ProfScope ps("expert_scan_units", st);
     beam::expert_scan_units_kernel<<<1, 256, 0, st>>>(blk_hist, L.NB, p->E, blk_off, counts, offs,
                                                       ugu, nunits, L.NT, p->I / 128,
-                                                      path_mt_down(L.path, p->H), 1, row_tok);
+                                                      path_mt_down(L.path, p->H, L.f4), 1, row_tok);
   }
   BEAM_LAUNCH_CHECK("expert_scan_units_kernel");
   {

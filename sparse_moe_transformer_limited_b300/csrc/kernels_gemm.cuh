@@ -15,6 +15,10 @@
 //            epilogue: act[t, m*128+i] = bf16(silu(D_g) * D_u)   (FP32 math)
 //   down     (MODE 1): unit = (expert e, 128 hidden rows m, token tile)
 //            D[h,t] = sum_i Wd[e, m*128+h, i] * act[t, i]
+//            (NVFP4 with small token tiles: 256 hidden rows m*256.. as two
+//            128-row tiles into two accumulators, like gate/up: the block
+//            scales' TMEM copies and the MMAs of a K-block then move twice
+//            the weight bytes, and the two accumulators alternate)
 //            epilogue: o[token(t), m*128+h] += w_t * D[h,t] (FP32), the
 //            router-weighted combine, then the post-norm and residual of
 //            every completed token (kernels_combine.cuh)
@@ -69,6 +73,13 @@ struct GemmArgs {
   CombineArgs comb;           // MODE 1
 };
 
+// Weight rows of one unit: 128, or 256 for the NVFP4 down GEMM on token
+// tiles of at most 64 (two weight tiles per unit, see above).
+template <int MODE, int NT, int KIND>
+struct UnitRows {
+  static constexpr int value = (MODE == 1 && KIND == KIND_NVFP4 && NT <= 64) ? 256 : 128;
+};
+
 // Unit u of a GEMM: token tile u / m_tiles of the tile list and weight
 // row-tile u % m_tiles.
 template <int MODE, int NT>
@@ -76,6 +87,12 @@ __device__ __forceinline__ int4 gemm_unit(const GemmArgs& a, int u) {
   const int m = u % a.m_tiles, j = u / a.m_tiles;
   const int4 t = a.units[j];
   return make_int4(t.x, t.y, t.z, m);
+}
+
+// Unit u, or an empty unit past the end of the list.
+template <int MODE, int NT>
+__device__ __forceinline__ int4 gemm_unit_or_none(const GemmArgs& a, int u, int n_units) {
+  return u < n_units ? gemm_unit<MODE, NT>(a, u) : make_int4(0, 0, 0, 0);
 }
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
@@ -87,19 +104,21 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
 template <int MODE, int NT, int STAGES, int KIND = KIND_BF16>
 struct GemmCfg {
   static_assert(MODE == 0 || MODE == 1, "mode");
+  // two weight tiles per K-block: gate and up, or two down tiles (UnitRows)
+  static constexpr bool TWO_A = MODE == 0 || UnitRows<MODE, NT, KIND>::value == 256;
   static constexpr int A_TILE = 128 * 128;  // 128 rows x 128 bytes (64 bf16, 128 e4m3, 256 e2m1)
-  static constexpr int A_BYTES = (MODE == 0 ? 2 : 1) * A_TILE;
+  static constexpr int A_BYTES = (TWO_A ? 2 : 1) * A_TILE;
   static constexpr int B_BYTES = NT * 128;  // NT rows x 128 bytes
   // NVFP4: per stage the block scales of the K-block (four 512-byte groups
   // per operand matrix) follow the operand tiles
-  static constexpr int SF_A_BYTES = KIND == KIND_NVFP4 ? (MODE == 0 ? 2 : 1) * 2048 : 0;
+  static constexpr int SF_A_BYTES = KIND == KIND_NVFP4 ? (TWO_A ? 2 : 1) * 2048 : 0;
   static constexpr int SF_B_BYTES = KIND == KIND_NVFP4 ? 2048 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_A_BYTES + SF_B_BYTES;
-  static constexpr int ACC_COLS = (MODE == 0 ? 2 : 1) * NT;
+  static constexpr int ACC_COLS = (TWO_A ? 2 : 1) * NT;
   // NVFP4: each stage has its own TMEM columns for the scales it copies in
   // (four columns per group), after the accumulators
-  static constexpr int SF_COLS = KIND == KIND_NVFP4 ? 4 * 4 * (MODE == 0 ? 3 : 2) : 0;
-  static constexpr int SF_B_COL = KIND == KIND_NVFP4 ? 16 * (MODE == 0 ? 2 : 1) : 0;
+  static constexpr int SF_COLS = KIND == KIND_NVFP4 ? 4 * 4 * (TWO_A ? 3 : 2) : 0;
+  static constexpr int SF_B_COL = KIND == KIND_NVFP4 ? 16 * (TWO_A ? 2 : 1) : 0;
   static constexpr int NBUF = (2 * ACC_COLS + STAGES * SF_COLS <= 512) ? 2 : 1;
   static constexpr int SF_TMEM_BASE = NBUF * ACC_COLS;
   static constexpr int TMEM_COLS =
@@ -181,11 +200,15 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
+      // each unit's descriptor is fetched one unit ahead (here and in the
+      // other roles), so its global load overlaps the previous unit's work
+      int4 un_next = gemm_unit_or_none<MODE, NT>(args, blockIdx.x, n_units);
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const int4 un = gemm_unit<MODE, NT>(args, u);
+        const int4 un = un_next;
+        un_next = gemm_unit_or_none<MODE, NT>(args, u + gridDim.x, n_units);
         const int nb16 = (un.z + 15) >> 4;
         const uint32_t bytes = C::A_BYTES + nb16 * 2048 + C::SF_A_BYTES + C::SF_B_BYTES;
-        const int arow = un.x * args.a_rows_per_expert + un.w * 128;
+        const int arow = un.x * args.a_rows_per_expert + un.w * UnitRows<MODE, NT, KIND>::value;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, abort_flag)) {
             gemm_fail(abort_flag);
@@ -198,6 +221,7 @@ __global__ void __launch_bounds__(192, 1)
           const int kx = kb * (F4 ? 128 : KBlock<KIND>::ELEMS);
           tma_load_2d(sb, &tm_a0, &full[stage], kx, arow, pol_w);
           if (MODE == 0) tma_load_2d(sb + C::A_TILE, &tm_a1, &full[stage], kx, arow, pol_w);
+          else if (C::TWO_A) tma_load_2d(sb + C::A_TILE, &tm_a0, &full[stage], kx, arow + 128, pol_w);
           for (int j = 0; j < nb16; ++j)
             tma_load_2d(sb + C::A_BYTES + j * 2048, &tm_b, &full[stage], kx, un.y + j * 16,
                         pol_x);
@@ -209,7 +233,8 @@ __global__ void __launch_bounds__(192, 1)
             const size_t b_off = (static_cast<size_t>(un.y / NT) * ksteps + 4 * kb) * 512;
             uint8_t* sf = sb + C::A_BYTES + C::B_BYTES;
             const uint8_t* src0 = args.a_sf0 + a_off;
-            const uint8_t* src1 = MODE == 0 ? args.a_sf1 + a_off : src0;
+            // the second tile: gate/up -> up's scales; down -> the next 128-row tile's
+            const uint8_t* src1 = MODE == 0 ? args.a_sf1 + a_off : src0 + (C::TWO_A ? ksteps * 512 : 0);
             const uint8_t* srcb = args.b_sf + b_off;
             if (((reinterpret_cast<uintptr_t>(src0) | reinterpret_cast<uintptr_t>(src1) |
                   reinterpret_cast<uintptr_t>(srcb)) & 15) != 0) {
@@ -217,7 +242,7 @@ __global__ void __launch_bounds__(192, 1)
               atomicOr(&g_beam_err, DEV_ERR_ALIGN);
             } else {
               bulk_load(sf, src0, 2048, &full[stage], pol_w);
-              if (MODE == 0) bulk_load(sf + 2048, src1, 2048, &full[stage], pol_w);
+              if (C::TWO_A) bulk_load(sf + 2048, src1, 2048, &full[stage], pol_w);
               bulk_load(sf + C::SF_A_BYTES, srcb, 2048, &full[stage], pol_x);
             }
           }
@@ -249,8 +274,10 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      int4 un_next = gemm_unit_or_none<MODE, NT>(args, blockIdx.x, n_units);
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++it) {
-        const int4 un = gemm_unit<MODE, NT>(args, u);
+        const int4 un = un_next;
+        un_next = gemm_unit_or_none<MODE, NT>(args, u + gridDim.x, n_units);
         const int buf = (C::NBUF == 1) ? 0 : (it & 1);
         const uint32_t tpar = static_cast<uint32_t>((C::NBUF == 1) ? it : (it >> 1)) & 1u;
         if (!mbar_wait_bounded(&tempty[buf], tpar ^ 1u, tmo, abort_flag)) {
@@ -282,7 +309,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               tmem_cp_sf512(slot + 4 * kk, sdesc_sf512(sf + kk * 512));
-              if (MODE == 0) tmem_cp_sf512(slot + 16 + 4 * kk, sdesc_sf512(sf + 2048 + kk * 512));
+              if (C::TWO_A) tmem_cp_sf512(slot + 16 + 4 * kk, sdesc_sf512(sf + 2048 + kk * 512));
               tmem_cp_sf512(slot + C::SF_B_COL + 4 * kk, sdesc_sf512(sf + C::SF_A_BYTES + kk * 512));
             }
 #pragma unroll
@@ -290,7 +317,7 @@ __global__ void __launch_bounds__(192, 1)
               const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
               const uint32_t sfb = slot + C::SF_B_COL + 4 * kk;
               mma_nvf4_ss(d0, da0 + 2 * kk, db + 2 * kk, idesc, slot + 4 * kk, sfb, accum);
-              if (MODE == 0)
+              if (C::TWO_A)
                 mma_nvf4_ss(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, slot + 16 + 4 * kk, sfb, accum);
             }
           } else {
@@ -298,7 +325,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int kk = 0; kk < 4; ++kk) {
               const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
               mma_ss<F8>(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
-              if (MODE == 0) mma_ss<F8>(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+              if (C::TWO_A) mma_ss<F8>(d0 + NT, da1 + 2 * kk, db + 2 * kk, idesc, accum);
             }
           }
           mma_commit(&empty[stage]);
@@ -321,8 +348,10 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int rloc = q * 32 + lane;
     int it = 0;
+    int4 un_next = gemm_unit_or_none<MODE, NT>(args, blockIdx.x, n_units);
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-      const int4 un = gemm_unit<MODE, NT>(args, u);
+      const int4 un = un_next;
+      un_next = gemm_unit_or_none<MODE, NT>(args, u + gridDim.x, n_units);
       const int buf = (C::NBUF == 1) ? 0 : (it & 1);
       const uint32_t tpar = static_cast<uint32_t>((C::NBUF == 1) ? it : (it >> 1)) & 1u;
       bool ready = false;
@@ -336,7 +365,7 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t tb = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS) +
                           (static_cast<uint32_t>(q * 32) << 16);
       const int nch = (un.z + 15) >> 4;
-      const int col = un.w * 128 + rloc;
+      const int col = un.w * UnitRows<MODE, NT, KIND>::value + rloc;
       float ws0 = 1.f, ws1 = 1.f;
       if (F8 || F4) {
         const size_t wi = F8 ? static_cast<size_t>(un.x) * args.a_rows_per_expert + col
@@ -367,8 +396,11 @@ __global__ void __launch_bounds__(192, 1)
           // fused combine: o[token, col] += w * D (lanes 0..15 fetch the
           // token and coefficient of the chunk's columns)
           const CombineArgs& cb = args.comb;
-          float d[16];
-          tmem_ld16(tb + c * 16, d);
+          float d[16], d2[16];
+          if (C::TWO_A)
+            tmem_ld16x2(tb + c * 16, tb + NT + c * 16, d, d2);   // rows col and col + 128
+          else
+            tmem_ld16(tb + c * 16, d);
           int tk = -1;
           float cf = 0.f;
           if (lane < 16 && c * 16 + lane < un.z) {
@@ -380,7 +412,11 @@ __global__ void __launch_bounds__(192, 1)
           for (int j = 0; j < 16; ++j) {
             const int t = __shfl_sync(0xffffffffu, tk, j);
             const float w = __shfl_sync(0xffffffffu, cf, j);
-            if (t >= 0) red_add_f32(args.comb.acc + static_cast<size_t>(t) * cb.H + col, w * (ws0 * d[j]));
+            if (t >= 0) {
+              float* o = args.comb.acc + static_cast<size_t>(t) * cb.H + col;
+              red_add_f32(o, w * (ws0 * d[j]));
+              if (C::TWO_A) red_add_f32(o + 128, w * (ws0 * d2[j]));
+            }
           }
         }
       }

@@ -30,12 +30,13 @@
 // epilogue has read them (it releases TMEM before its stores complete and
 // before it finalises tokens).
 //
-// Roles per CTA (320 threads): warp 0 TMA producer; warp 1 TMEM allocation
-// (both CTAs) and, in the even CTA, the MMA issuer; warps 2..9 epilogue, two
-// per TMEM lane quarter (warp % 4), taking alternate 16-column chunks. Both
-// CTAs' TMA loads count their bytes on the even CTA's `full` barrier; the MMA
-// commits arrive on the `empty` and `tmem_full` barriers of both CTAs; the 16
-// epilogue warps release TMEM on the even CTA's `tmem_empty` barrier. All
+// Roles per CTA: warp 0 TMA producer; warp 1 TMEM allocation (both CTAs)
+// and, in the even CTA, the MMA issuer; then the epilogue warps, NSUB per
+// TMEM lane quarter (warp % 4), each taking every NSUB-th 16-column chunk
+// (NSUB = 2 for gate/up, 4 for down). Both CTAs' TMA loads count their bytes
+// on the even CTA's `full` barrier; the MMA commits arrive on the `empty` and
+// `tmem_full` barriers of both CTAs; all epilogue warps of both CTAs release
+// TMEM on the even CTA's `tmem_empty` barrier. All
 // waits are bounded; the CTAs meet at a cluster barrier before TMEM is freed
 // and before exit.
 #pragma once
@@ -66,19 +67,28 @@ struct WideArgs {
   CombineArgs comb;         // MODE 1
 };
 
-struct WideCfg {
+template <int EPI_WARPS_>
+struct WideCfgT {
   static constexpr int STAGES = 4;
   static constexpr int A_BYTES = 128 * 128;      // one 128-row weight tile x 128 bytes
   static constexpr int B_BYTES = 128 * 128;      // up to 128 token rows x 128 bytes
   static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
   static constexpr int D1_COL = 256;             // second accumulator
   static constexpr int TMEM_COLS = 512;
-  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_WARPS = EPI_WARPS_;
+  static constexpr int NSUB = EPI_WARPS / 4;     // epilogue warps per lane quarter
+  static constexpr int NCH = 16 / NSUB;          // 16-column chunks per warp and accumulator
+  static constexpr int NG = NCH / 2;             // per-lane registers for 32 columns each
+  static_assert(NSUB == 2 || NSUB == 4, "epilogue warps");
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int BAR_BYTES = (2 * STAGES + 3) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
+// Gate/up: two epilogue warps per lane quarter. Down: four, so that more of
+// the epilogue's global reductions are in flight while TMEM is held.
+template <int MODE>
+using WideCfg = WideCfgT<MODE == 0 ? 8 : 16>;
 
 // Token rows of one CTA for a unit of N tokens: N/2 rows, a multiple of 8,
 // loaded as 64-, 32-, 16- and 8-row boxes (the binary digits of N/2).
@@ -105,14 +115,14 @@ __device__ __forceinline__ void wide_load_tokens(uint8_t* dst, const CUtensorMap
 // F8: E4M3 operands (K-blocks of 128 elements, kind::f8f6f4) with the scales
 // applied in the epilogue; else BF16 (K-blocks of 64).
 template <int MODE, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg::THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg<MODE>::THREADS, 1)
     expert_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0,
                             const __grid_constant__ CUtensorMap tm_w1,
                             const __grid_constant__ CUtensorMap tm_t64,
                             const __grid_constant__ CUtensorMap tm_t32,
                             const __grid_constant__ CUtensorMap tm_t16,
                             const __grid_constant__ CUtensorMap tm_t8, const WideArgs args) {
-  using C = WideCfg;
+  using C = WideCfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -270,13 +280,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg::THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warp (q, half) owns TMEM lane quarter q and the chunks of 16 columns
-    // c = half + 2k, k = 0..7. Its local column l (0..127) is column
-    // (half + 2 * (l / 16)) * 16 + l % 16; lane j keeps the per-column values
-    // of local columns j, j + 32, j + 64 and j + 96, fetched from global
-    // memory before the accumulators are ready.
+    // Warp (q, sub) owns TMEM lane quarter q and the chunks of 16 columns
+    // c = sub + NSUB * k, k = 0..NCH-1. Its local column l is column
+    // (sub + NSUB * (l / 16)) * 16 + l % 16; lane j keeps the per-column
+    // values of local columns j, j + 32, ..., fetched from global memory
+    // before the accumulators are ready.
     const int q = warp & 3;                 // TMEM lane quarter
-    const int half = (warp - 2) >> 2;
+    const int sub = (warp - 2) >> 2;
     const int rloc = q * 32 + lane;         // TMEM lane = weight row of this CTA's tiles
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int it = 0;
@@ -286,12 +296,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg::THREADS, 1)
       const int nch = (n + 15) >> 4;
       // per-column values: MODE 0 the x row scale (E4M3), MODE 1 the token and
       // the combine coefficient
-      int tkr[4];
-      float cfr[4];
+      int tkr[C::NG];
+      float cfr[C::NG];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < C::NG; ++g) {
         const int l = g * 32 + lane;
-        const int col = (half + 2 * (l >> 4)) * 16 + (l & 15);
+        const int col = (sub + C::NSUB * (l >> 4)) * 16 + (l & 15);
         tkr[g] = -1;
         cfr[g] = 1.f;
         if (col < n) {
@@ -320,17 +330,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg::THREADS, 1)
           sg = args.w_scale0[wi];
           su = args.w_scale1[wi];
         }
-        // two chunks (k, k + 1) of both accumulators per TMEM wait
+        // two local chunks (k, k + 1) of both accumulators per TMEM wait
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-          const int c0 = half + 2 * k;
+        for (int k = 0; k < C::NCH; k += 2) {
+          const int c0 = sub + C::NSUB * k;
           if (c0 >= nch) break;
+          const int c1 = c0 + C::NSUB;
           float g0[16], u0[16], g1[16], u1[16];
-          tmem_ld16x4(tq + c0 * 16, tq + C::D1_COL + c0 * 16, tq + (c0 + 2) * 16,
-                      tq + C::D1_COL + (c0 + 2) * 16, g0, u0, g1, u1);
+          tmem_ld16x4(tq + c0 * 16, tq + C::D1_COL + c0 * 16, tq + c1 * 16,
+                      tq + C::D1_COL + c1 * 16, g0, u0, g1, u1);
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = c0 + 2 * h2;
+            const int c = h2 ? c1 : c0;
             const float* g = h2 ? g1 : g0;
             const float* v = h2 ? u1 : u0;
 #pragma unroll
@@ -364,12 +375,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg::THREADS, 1)
           if (two) s1 = args.w_scale0[wi + h1];
         }
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-          const int c0 = half + 2 * k;
+        for (int k = 0; k < C::NCH; k += 2) {
+          const int c0 = sub + C::NSUB * k;
           if (c0 >= nch) break;
+          const int c1 = c0 + C::NSUB;
           float d0[16], e0[16], d1[16], e1[16];
-          tmem_ld16x4(tq + c0 * 16, tq + C::D1_COL + c0 * 16, tq + (c0 + 2) * 16,
-                      tq + C::D1_COL + (c0 + 2) * 16, d0, e0, d1, e1);
+          tmem_ld16x4(tq + c0 * 16, tq + C::D1_COL + c0 * 16, tq + c1 * 16,
+                      tq + C::D1_COL + c1 * 16, d0, e0, d1, e1);
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             const float* d = h2 ? d1 : d0;
@@ -390,8 +402,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty, 0));
-        // one arrival per token of this warp's columns (32 per call)
-        combine_arrive_warp<4>(cb, tkr);
+        // one arrival per token of this warp's columns (32 per register)
+        combine_arrive_warp<C::NG>(cb, tkr);
       }
     }
     // finalise completed tokens (rows) once this warp's own units are done

@@ -1496,6 +1496,8 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
     aa.nq = nq;
     aa.nkv = nkv;
     aa.window = p->window;
+    aa.n_qt = L.Tp / beam::ATT_BQ;
+    aa.n_items = aa.n_qt * nq;
     aa.scale = 1.0f / std::sqrt(static_cast<float>(beam::ATT_D));
     aa.gate = gate;
     aa.gate_ld = (2 * nq + 2 * nkv) * beam::ATT_D;
@@ -1505,8 +1507,9 @@ extern "C" beam_status_t beam_attention_forward(const beam_attn_params* p, const
                          beam::AttnCfg::SMEM_BYTES)) != BEAM_OK)
       return s;
     ProfScope ps("flash_attn", st);
-    beam::flash_attn_kernel<<<dim3(L.Tp / beam::ATT_BQ, nq), beam::ATT_THREADS,
-                              beam::AttnCfg::SMEM_BYTES, st>>>(
+    // persistent: one CTA per SM over the (query tile, head) items
+    const int grid = std::min(aa.n_items, sm_count());
+    beam::flash_attn_kernel<<<grid, beam::ATT_THREADS, beam::AttnCfg::SMEM_BYTES, st>>>(
         m_q, m_k, m_vt, aa);
   }
   BEAM_LAUNCH_CHECK("flash_attn_kernel");

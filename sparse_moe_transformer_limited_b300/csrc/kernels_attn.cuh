@@ -135,16 +135,26 @@ __global__ void linear_units_kernel(int n, int MT, int4* __restrict__ units, int
 }
 
 // ---------------------------------------------------------------------------
-// Flash attention on tcgen05, one CTA per (query tile of 128 rows, query
-// head). Warp 0: TMA producer of Q (once) and of K tiles of 128 keys into a
-// three-stage ring (a stage is freed as soon as its S has been computed);
-// the last warp: TMA producer of V^T tiles into a two-stage ring (freed after
-// P V). Warp 1: TMEM owner and MMA issuer: S_0, S_1 and S_2 up front into
-// three TMEM S buffers; then per tile j: O += P_j V_j as soon as P_j is
-// written, with P_j read from TMEM (the MMA's A operand), then S_{j+3} into
-// the same buffer (one thread's MMAs execute in issue order, so S_{j+3}
-// overwrites P_j only after P_j V_j has read it); the S of the next two
-// tiles is thus computed while a tile's softmax runs. Warps 2..: ATT_PARTS warps
+// Flash attention on tcgen05, persistent: one CTA per SM walks a static
+// share of the (query tile of 128 rows, query head) work items, heaviest
+// first (a causal layer's last query tiles see the most keys). Tiles are
+// numbered across the CTA's items, so every ring, buffer and barrier below
+// runs on without a break from one item to the next: the next item's Q is
+// loaded and its first S computed while the previous item's last tiles and
+// output are still in progress.
+// Warp 0: TMA producer of Q (two buffers, one per item parity) and of K
+// tiles of 128 keys into a two-stage ring (a stage is freed as soon as its S
+// has been computed); the last warp: TMA producer of V^T tiles into a
+// two-stage ring (freed after P V). Warp 1: TMEM owner and MMA issuer: per
+// item S_0 and S_1 into two of three TMEM S buffers; then per tile j, as
+// soon as P_j is written: O += P_j V_j (P_j read from TMEM as the MMA's A
+// operand) with its K steps alternating with those of S_{j+2}, whose buffer
+// held the previous tile's P (one thread's MMAs execute in issue order, so
+// S_{j+2} overwrites it only after its P V has read it). The two
+// accumulators (O and an S buffer) take turns, so no MMA waits on the one
+// before it into the same TMEM, and S_{j+1} is ready while tile j+1's
+// softmax runs. An item's first P V (which overwrites O) waits until the
+// softmax warps have read the previous item's O. Warps 2..: ATT_PARTS warps
 // per 32-row TMEM lane quarter, each for ATT_KW consecutive keys of the tile
 // (and the matching columns of O); thread = (query row, part). Per tile: read
 // the part of the S row, mask (boundary tiles only), row maximum over all
@@ -152,8 +162,8 @@ __global__ void linear_units_kernel(int n, int MT, int4* __restrict__ units, int
 // lazy reference: m moves (and the O row is rescaled) only when a tile's
 // maximum exceeds it by more than ATT_TAU2, so P <= 2^TAU2; P goes as BF16
 // pairs over the first 64 columns of its own S buffer (every warp of a lane
-// quarter has read its part of S before any writes P). At the end O / l
-// times the gate, BF16, to `out`.
+// quarter has read its part of S before any writes P). At the end of an
+// item O / l times the gate, BF16, to `out`.
 // TMEM columns: S/P buffers [0,128), [128,256), [256,384); O [384,512).
 // All waits are bounded; on expiry the error word is set and every role
 // leaves after its in-flight copies and MMAs have completed. The two warps of
@@ -173,6 +183,8 @@ constexpr int ATT_THREADS = 32 * (3 + ATT_SOFTMAX_WARPS);
 
 struct AttnArgs {
   int T, Tp, nq, nkv, window;
+  int n_qt;                    // query tiles per head (Tp / 128)
+  int n_items;                 // n_qt * nq work items
   float scale;                 // 1 / sqrt(head_dim)
   const float* gate;           // gate logits: row t at gate + t * gate_ld, head h at + h * 128
   int gate_ld;                 // floats per row of the fused projection
@@ -184,13 +196,23 @@ struct AttnCfg {
   static constexpr int Q_BYTES = ATT_BQ * ATT_D * 2;     // 32 KB: two 64-channel blocks
   static constexpr int K_BYTES = ATT_BK * ATT_D * 2;     // 32 KB
   static constexpr int V_BYTES = ATT_D * ATT_BK * 2;     // 32 KB (V^T: 128 channels x 128 keys)
-  static constexpr int K_STAGES = 3, V_STAGES = 2;
-  static constexpr int XCH_BYTES = 2 * ATT_PARTS * ATT_BQ * 4;  // per (tile parity, part, row): one float
-  static constexpr int BAR_BYTES = 24 * 8;
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES +
-                                    XCH_BYTES + BAR_BYTES;
+  // two Q buffers (the next item's Q loads while this one's S MMAs run);
+  // K: S_{t+2} reads stage t % 2 once S_t has released it
+  static constexpr int Q_STAGES = 2, K_STAGES = 2, V_STAGES = 2;
+  static_assert(K_STAGES <= 3 && Q_STAGES <= 2, "barrier slots");
+  // row maxima: [tile parity][part][row]; row sums: [part][row]
+  static constexpr int XCH_BYTES = 3 * ATT_PARTS * ATT_BQ * 4;
+  static constexpr int BAR_BYTES = 32 * 8;
+  static constexpr int SMEM_BYTES = 1024 + Q_STAGES * Q_BYTES + K_STAGES * K_BYTES +
+                                    V_STAGES * V_BYTES + XCH_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
+
+// Work item it: query tile and head, the heaviest query tiles first.
+__device__ __forceinline__ void attn_item(const AttnArgs& a, int it, int* qt, int* h) {
+  *qt = a.n_qt - 1 - it / a.nq;
+  *h = it % a.nq;
+}
 
 // First and one-past-last key tile of query tile qt.
 __device__ __forceinline__ void attn_key_tiles(int qt, int T, int window, int* j0, int* j1) {
@@ -262,52 +284,52 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + C::Q_BYTES;
+  uint8_t* sQ = smem;                                   // [2] query tiles
+  uint8_t* sK = sQ + C::Q_STAGES * C::Q_BYTES;
   uint8_t* sV = sK + C::K_STAGES * C::K_BYTES;
-  float* xch = reinterpret_cast<float*>(sV + C::V_STAGES * C::V_BYTES);  // [parity][part][row]
+  float* xch = reinterpret_cast<float*>(sV + C::V_STAGES * C::V_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::V_STAGES * C::V_BYTES + C::XCH_BYTES);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;        // [3]
-  uint64_t* k_empty = bars + 4;       // [3]
-  uint64_t* v_full = bars + 7;        // [2]
-  uint64_t* v_empty = bars + 10;      // [2]
-  // Per S buffer b: s_full[b] / p_full[b] complete once per tile j with
-  // j % 3 == b. Neither can run two phases ahead of its waiter: S_{j+3} is
-  // issued only after P_j (whose softmax waited on S_j) has been consumed.
-  uint64_t* s_full = bars + 12;       // [3]
-  uint64_t* p_full = bars + 15;       // [3]
-  uint64_t* o_done = bars + 18;       // [2]: P_j V_j done, tiles of parity j & 1
-  uint64_t* mma_done = bars + 20;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  uint64_t* q_full = bars + 0;        // [Q_STAGES], by item
+  uint64_t* q_empty = bars + 2;       // [2]: the item's S MMAs are done with its Q
+  uint64_t* k_full = bars + 4;        // [K_STAGES <= 3]
+  uint64_t* k_empty = bars + 7;       // [K_STAGES]
+  uint64_t* v_full = bars + 10;       // [2]
+  uint64_t* v_empty = bars + 12;      // [2]
+  // Per S buffer b: s_full[b] / p_full[b] complete once per tile t (numbered
+  // across items) with t % 3 == b. Neither can run two phases ahead of its
+  // waiter: S_{t+3} is issued (with P_{t+1} V_{t+1}, or with the next item's
+  // first tiles) only after P_{t+1} or P_t exist, hence after the softmax has
+  // consumed S_t.
+  uint64_t* s_full = bars + 14;       // [3]
+  uint64_t* p_full = bars + 17;       // [3]
+  uint64_t* o_done = bars + 20;       // [2]: P_t V_t done, tiles of parity t & 1
+  uint64_t* o_free = bars + 22;       // the softmax warps have read an item's O
+  uint64_t* mma_done = bars + 23;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heavy tiles first: the last query tiles of a causal global layer see the most keys
-  const int qt = gridDim.x - 1 - blockIdx.x;
-  const int h = blockIdx.y;
-  const int g = h / (args.nq / args.nkv);
-  int j0, j1;
-  attn_key_tiles(qt, args.T, args.window, &j0, &j1);
-  const int ntiles = j1 - j0;
   const uint64_t tmo = args.timeout_ns;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int s = 0; s < C::Q_STAGES; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
     for (int s = 0; s < C::K_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
     }
-    for (int s = 0; s < C::V_STAGES; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
+      mbar_init(&o_done[s], 1);
     }
     for (int s = 0; s < ATT_SBUF; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], ATT_SOFTMAX_WARPS);
     }
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
+    mbar_init(o_free, ATT_SOFTMAX_WARPS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -332,40 +354,59 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
       const volatile int never = 0;
-      if (kp) {
-        const int qrow = h * args.Tp + qt * ATT_BQ;
-        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-        tma_load_2d(sQ, &tm_q, q_full, 0, qrow, pol);
-        tma_load_2d(sQ + C::Q_BYTES / 2, &tm_q, q_full, 64, qrow, pol);
-      }
-      // K tiles (three stages) or V^T tiles (two stages)
       const int NS = kp ? C::K_STAGES : C::V_STAGES;
       uint64_t* full = kp ? k_full : v_full;
       uint64_t* empty = kp ? k_empty : v_empty;
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int s = j % NS;
-        if (!mbar_wait_bounded(&empty[s], ((j / NS) & 1) ^ 1u, tmo, abort_flag)) {
-          gemm_fail(abort_flag);
-          break;
-        }
-        const int k0 = (j0 + j) * ATT_BK;
-        mbar_arrive_expect_tx(&full[s], C::K_BYTES);
+      int t = 0, n = 0;                     // tiles and items issued
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < args.n_items; it += gridDim.x) {
+        int qt, h, j0, j1;
+        attn_item(args, it, &qt, &h);
+        attn_key_tiles(qt, args.T, args.window, &j0, &j1);
+        const int g = h / (args.nq / args.nkv);
         if (kp) {
-          uint8_t* st = sK + s * C::K_BYTES;
-          tma_load_2d(st, &tm_k, &full[s], 0, g * args.Tp + k0, pol);
-          tma_load_2d(st + C::K_BYTES / 2, &tm_k, &full[s], 64, g * args.Tp + k0, pol);
-        } else {
-          uint8_t* st = sV + s * C::V_BYTES;
-          tma_load_2d(st, &tm_vt, &full[s], k0, g * ATT_D, pol);
-          tma_load_2d(st + C::V_BYTES / 2, &tm_vt, &full[s], k0 + 64, g * ATT_D, pol);
+          const int qb = n % C::Q_STAGES;
+          if (!mbar_wait_bounded(&q_empty[qb], ((n / C::Q_STAGES) & 1) ^ 1u, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            break;
+          }
+          const int qrow = h * args.Tp + qt * ATT_BQ;
+          uint8_t* sq = sQ + qb * C::Q_BYTES;
+          mbar_arrive_expect_tx(&q_full[qb], C::Q_BYTES);
+          tma_load_2d(sq, &tm_q, &q_full[qb], 0, qrow, pol);
+          tma_load_2d(sq + C::Q_BYTES / 2, &tm_q, &q_full[qb], 64, qrow, pol);
         }
-        ++issued;
+        ++n;
+        // K tiles or V^T tiles of this item, into the ring
+        for (int j = j0; j < j1; ++j) {
+          const int s = t % NS;
+          if (!mbar_wait_bounded(&empty[s], ((t / NS) & 1) ^ 1u, tmo, abort_flag)) {
+            gemm_fail(abort_flag);
+            ok = false;
+            break;
+          }
+          const int k0 = j * ATT_BK;
+          mbar_arrive_expect_tx(&full[s], C::K_BYTES);
+          if (kp) {
+            uint8_t* st = sK + s * C::K_BYTES;
+            tma_load_2d(st, &tm_k, &full[s], 0, g * args.Tp + k0, pol);
+            tma_load_2d(st + C::K_BYTES / 2, &tm_k, &full[s], 64, g * args.Tp + k0, pol);
+          } else {
+            uint8_t* st = sV + s * C::V_BYTES;
+            tma_load_2d(st, &tm_vt, &full[s], k0, g * ATT_D, pol);
+            tma_load_2d(st + C::V_BYTES / 2, &tm_vt, &full[s], k0 + 64, g * ATT_D, pol);
+          }
+          ++t;
+        }
       }
-      // every load must land before the CTA exits
-      if (kp && !mbar_wait_bounded(q_full, 0, tmo, &never)) gemm_fail(abort_flag);
-      for (int j = max(0, issued - NS); j < issued; ++j)
-        if (!mbar_wait_bounded(&full[j % NS], (j / NS) & 1, tmo, &never)) gemm_fail(abort_flag);
+      // every load must land before the CTA exits: the last phase of each
+      // ring stage and Q buffer that was filled
+      for (int u = max(0, t - NS); u < t; ++u)
+        if (!mbar_wait_bounded(&full[u % NS], (u / NS) & 1, tmo, &never)) gemm_fail(abort_flag);
+      if (kp)
+        for (int u = max(0, n - C::Q_STAGES); u < n; ++u)
+          if (!mbar_wait_bounded(&q_full[u % C::Q_STAGES], (u / C::Q_STAGES) & 1, tmo, &never))
+            gemm_fail(abort_flag);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -373,50 +414,90 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
       const uint32_t dO = tmem_base + ATT_O_COL;
-      bool ok = mbar_wait_bounded(q_full, 0, tmo, abort_flag);
-      tc_fence_after();
-      const uint64_t dq = sdesc_k128(smem_u32(sQ));
-      const uint64_t dq1 = sdesc_k128(smem_u32(sQ + C::Q_BYTES / 2));
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % C::K_STAGES;
-        if (!mbar_wait_bounded(&k_full[ks], (j / C::K_STAGES) & 1, tmo, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t base = smem_u32(sK + ks * C::K_BYTES);
-        const uint64_t dk = sdesc_k128(base), dk1 = sdesc_k128(base + C::K_BYTES / 2);
-        const uint32_t dS = tmem_base + static_cast<uint32_t>((j % ATT_SBUF) * 128);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dS, dq + 2 * kk, dk + 2 * kk, idesc, kk != 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dS, dq1 + 2 * kk, dk1 + 2 * kk, idesc, 1u);
-        mma_commit(&s_full[j % ATT_SBUF]);
-        mma_commit(&k_empty[ks]);
-        return true;
-      };
-      for (int j = 0; ok && j < ATT_SBUF && j < ntiles; ++j) ok = issue_s(j);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int vs = j % C::V_STAGES;
-        if (!mbar_wait_bounded(&p_full[j % ATT_SBUF], (j / ATT_SBUF) & 1, tmo, abort_flag) ||
-            !mbar_wait_bounded(&v_full[vs], (j / C::V_STAGES) & 1, tmo, abort_flag)) {
+      bool ok = true;
+      int t0 = 0, n = 0;                    // first tile of the item, items done
+      for (int it = blockIdx.x; ok && it < args.n_items; it += gridDim.x, ++n) {
+        int qt, h, j0, j1;
+        attn_item(args, it, &qt, &h);
+        attn_key_tiles(qt, args.T, args.window, &j0, &j1);
+        const int ntiles = j1 - j0;
+        const int qb = n % C::Q_STAGES;
+        if (!mbar_wait_bounded(&q_full[qb], (n / C::Q_STAGES) & 1, tmo, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // O += P_j V_j: P_j from TMEM (keys 16kk.. in columns 8kk..), V_j^T from
-        // shared memory (two 64-key blocks)
-        const uint32_t dP = tmem_base + static_cast<uint32_t>((j % ATT_SBUF) * 128);
-        const uint32_t base = smem_u32(sV + vs * C::V_BYTES);
-        const uint64_t dv = sdesc_k128(base), dv1 = sdesc_k128(base + C::V_BYTES / 2);
+        const uint64_t dq = sdesc_k128(smem_u32(sQ + qb * C::Q_BYTES));
+        const uint64_t dq1 = sdesc_k128(smem_u32(sQ + qb * C::Q_BYTES + C::Q_BYTES / 2));
+        // S_t = Q K_t^T into S buffer t % 3 (eight K = 16 steps; with pv set,
+        // each step alternates with one step of O += P V issued by pv(kk), so
+        // two independent accumulators share the tensor pipe)
+        auto issue_s = [&](int t, auto&& pv) -> bool {
+          const int ks = t % C::K_STAGES;
+          if (!mbar_wait_bounded(&k_full[ks], (t / C::K_STAGES) & 1, tmo, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t base = smem_u32(sK + ks * C::K_BYTES);
+          const uint64_t dk = sdesc_k128(base), dk1 = sdesc_k128(base + C::K_BYTES / 2);
+          const uint32_t dS = tmem_base + static_cast<uint32_t>((t % ATT_SBUF) * 128);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16_ts(dO, dP + 8 * kk, dv + 2 * kk, idesc, (j | kk) != 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16_ts(dO, dP + 32 + 8 * kk, dv1 + 2 * kk, idesc, 1u);
-        mma_commit(&o_done[j & 1]);
-        mma_commit(&v_empty[vs]);
-        // S_{j+3} into the buffer P_j occupies, after P_j V_j in issue order
-        if (j + ATT_SBUF < ntiles && !issue_s(j + ATT_SBUF)) {
-          ok = false;
-          break;
+          for (int kk = 0; kk < 8; ++kk) {
+            pv(kk);
+            const uint64_t a = (kk < 4 ? dq : dq1) + 2 * (kk & 3);
+            const uint64_t b = (kk < 4 ? dk : dk1) + 2 * (kk & 3);
+            mma_bf16_ss(dS, a, b, idesc, kk != 0);
+          }
+          return true;
+        };
+        auto no_pv = [](int) {};
+        // S of the item's first two tiles; their buffers held P of tiles
+        // t0 - 3 and t0 - 2, whose P V were issued before
+        for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
+          ok = issue_s(t0 + j, no_pv);
+          if (ok) {
+            mma_commit(&s_full[(t0 + j) % ATT_SBUF]);
+            mma_commit(&k_empty[(t0 + j) % C::K_STAGES]);
+          }
         }
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int t = t0 + j;
+          const int vs = t % C::V_STAGES;
+          if (!mbar_wait_bounded(&p_full[t % ATT_SBUF], (t / ATT_SBUF) & 1, tmo, abort_flag) ||
+              !mbar_wait_bounded(&v_full[vs], (t / C::V_STAGES) & 1, tmo, abort_flag) ||
+              (j == 0 && n > 0 && !mbar_wait_bounded(o_free, (n - 1) & 1, tmo, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O += P_t V_t: P_t from TMEM (keys 16kk.. in columns 8kk..), V_t^T
+          // from shared memory (two 64-key blocks); the item's first
+          // overwrites O (the previous item's O has been read: o_free)
+          const uint32_t dP = tmem_base + static_cast<uint32_t>((t % ATT_SBUF) * 128);
+          const uint32_t base = smem_u32(sV + vs * C::V_BYTES);
+          const uint64_t dv = sdesc_k128(base), dv1 = sdesc_k128(base + C::V_BYTES / 2);
+          auto pv = [&](int kk) {
+            const uint64_t b = (kk < 4 ? dv : dv1) + 2 * (kk & 3);
+            mma_bf16_ts(dO, dP + 8 * kk, b, idesc, (j | kk) != 0);
+          };
+          if (j + 2 < ntiles) {
+            if (!issue_s(t + 2, pv)) {
+              ok = false;
+              break;
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) pv(kk);
+          }
+          mma_commit(&o_done[t & 1]);
+          mma_commit(&v_empty[vs]);
+          if (j + 2 < ntiles) {
+            mma_commit(&s_full[(t + 2) % ATT_SBUF]);
+            mma_commit(&k_empty[(t + 2) % C::K_STAGES]);
+          }
+        }
+        // every S MMA of the item has been issued: its Q buffer is free once
+        // they complete
+        if (ok) mma_commit(&q_empty[qb]);
+        t0 += ntiles;
       }
       if (!ok) gemm_fail(abort_flag);
       mma_commit(mma_done);
@@ -429,167 +510,189 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const int q = warp & 3;                 // TMEM lane quarter
     const int part = (warp - 2) >> 2;       // keys / O columns [KW part, KW part + KW)
     const int row = q * 32 + lane;          // query row within the tile
-    const int qi = qt * ATT_BQ + row;       // query index
     const uint32_t lanebits = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t col0 = static_cast<uint32_t>(part * ATT_KW);
     const int bar_id = 1 + q;               // named barrier of this lane quarter's warps
     const float NEG = -1e30f;
-    float m = NEG, l = 0.f;                 // base-2 units; l over this part's keys
     // global layers' query scale is already in q; logits to base 2 in one FMA
     const float c2 = args.scale * ATT_LOG2E;
     const uint64_t cc = f2_pack(c2, c2);
-    const int hi = min(qi, args.T - 1);     // visible keys of row qi: [lo, hi]
-    const int lo = args.window > 0 ? qi - args.window + 1 : 0;
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;                  // exchange slots
-      const int sb = j % ATT_SBUF;          // S / P buffer
-      if (ok) {
-        bool ready = false;
-        if (lane == 0) ready = mbar_wait_bounded(&s_full[sb], (j / ATT_SBUF) & 1, tmo, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-      }
-      float sv[ATT_KW];
-      float mt = -INFINITY;
-      if (ok) {
-        tc_fence_after();
-        attn_ld_part(tmem_base + lanebits + sb * 128 + col0, sv);
-        const int k0 = (j0 + j) * ATT_BK + part * ATT_KW;
-        if (__any_sync(0xffffffffu, k0 < lo || k0 + ATT_KW - 1 > hi)) {
+    int t0 = 0;                             // first tile of the item
+    for (int it = blockIdx.x; it < args.n_items; it += gridDim.x) {
+      int qt, h, j0, j1;
+      attn_item(args, it, &qt, &h);
+      attn_key_tiles(qt, args.T, args.window, &j0, &j1);
+      const int ntiles = j1 - j0;
+      const int qi = qt * ATT_BQ + row;     // query index
+      const int hi = min(qi, args.T - 1);   // visible keys of row qi: [lo, hi]
+      const int lo = args.window > 0 ? qi - args.window + 1 : 0;
+      float m = NEG, l = 0.f;               // base-2 units; l over this part's keys
+      for (int j = 0; j < ntiles; ++j) {
+        const int t = t0 + j;
+        const int s = t & 1;                // exchange slots
+        const int sb = t % ATT_SBUF;        // S / P buffer
+        if (ok) {
+          bool ready = false;
+          if (lane == 0) ready = mbar_wait_bounded(&s_full[sb], (t / ATT_SBUF) & 1, tmo, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        }
+        float sv[ATT_KW];
+        float mt = -INFINITY;
+        if (ok) {
+          tc_fence_after();
+          attn_ld_part(tmem_base + lanebits + sb * 128 + col0, sv);
+          const int k0 = (j0 + j) * ATT_BK + part * ATT_KW;
+          if (__any_sync(0xffffffffu, k0 < lo || k0 + ATT_KW - 1 > hi)) {
 #pragma unroll
-          for (int c = 0; c < ATT_KW; ++c) {
-            const int kj = k0 + c;
-            sv[c] = (kj >= lo && kj <= hi) ? sv[c] : -INFINITY;
+            for (int c = 0; c < ATT_KW; ++c) {
+              const int kj = k0 + c;
+              sv[c] = (kj >= lo && kj <= hi) ? sv[c] : -INFINITY;
+            }
+          }
+          // raw maximum in eight independent partials (long dependency chains
+          // would stall the scheduler)
+          float mp[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mp[i] = fmaxf(sv[i], sv[8 + i]);
+#pragma unroll
+          for (int c = 16; c < ATT_KW; c += 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mp[i] = fmax3(mp[i], sv[c + i], sv[c + 8 + i]);
+          }
+          mt = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * c2;
+        }
+        // tile maximum over all parts of the row (-inf from a failed part),
+        // through slots of this tile's parity: a partner's next write to them
+        // (tile t + 2) comes after the barrier of tile t + 1 (or an item's
+        // end), which this warp reaches only after reading. The barrier also
+        // orders every warp's S reads before any P write.
+        float* xs = xch + s * ATT_PARTS * ATT_BQ;
+        xs[part * ATT_BQ + row] = mt;
+        tc_fence_before();
+        named_bar_sync(bar_id, 32 * ATT_PARTS);
+        tc_fence_after();
+#pragma unroll
+        for (int o = 1; o < ATT_PARTS; ++o) mt = fmaxf(mt, xs[((part + o) % ATT_PARTS) * ATT_BQ + row]);
+        if (!ok) continue;
+        // lazy reference: move m only when this tile exceeds it by more than TAU2
+        const float mn = mt > m + ATT_TAU2 ? mt : m;
+        const float alpha = ex2_approx(m - mn);
+        const uint64_t nm = f2_pack(-mn, -mn);
+        uint64_t sp[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < ATT_KW; c += 2) {
+          float a, b;
+          f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), cc, nm), a, b);
+          sv[c] = ex2_approx(a);
+          sv[c + 1] = ex2_approx(b);
+          sp[(c >> 1) & 3] = f2_add(sp[(c >> 1) & 3], f2_pack(sv[c], sv[c + 1]));
+        }
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float a, b;
+          f2_unpack(sp[i], a, b);
+          ps += a + b;
+        }
+        l = l * alpha + ps;
+        m = mn;
+        // the O row is rescaled only after the previous P V has completed.
+        // o_done[b] completes once per tile of parity b. At tile t every P V
+        // up to t - 2 has completed (S_t was issued with P_{t-2} V_{t-2}, or
+        // after it for an item's first two tiles, and its s_full commit
+        // covers every MMA issued before it) and P_{t+1} V_{t+1} cannot have,
+        // so the phase of P_{t-1} V_{t-1} is the current or the last one of
+        // o_done[(t-1)&1]: the parity wait is exact even when earlier tiles
+        // skipped it. (An item's first tile has no O to rescale.)
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          bool od = false;
+          if (lane == 0)
+            od = mbar_wait_bounded(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, tmo, abort_flag);
+          ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
+          if (!ok) continue;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < ATT_KW; c += 16) {
+            float o[16];
+            tmem_ld16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            tmem_st16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
           }
         }
-        // raw maximum in eight independent partials (long dependency chains
-        // would stall the scheduler)
-        float mp[8];
+        // this part of the P row as BF16 pairs (key 2i in the low half) into
+        // columns [KW/2 part, KW/2 part + KW/2) of this tile's S buffer
+        attn_st_p(tmem_base + lanebits + sb * 128 + part * (ATT_KW / 2), sv);
+        tmem_wait_st();
+        // P and the O rescale visible to the MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+      }
+      // end of the item: O / l times the gate sigmoid(gate logit) (FP32),
+      // BF16; l summed over all parts. The gate row part is fetched and its
+      // sigmoid taken before the wait for the item's last P V, so its global
+      // loads overlap it. o_done of the last tile t0 + ntiles - 1: its
+      // previous phase (tile t0 + ntiles - 3) completed before S of the last
+      // tile could, and the next item's first P V waits for o_free below.
+      const bool valid = qi < args.T;
+      float gt[ATT_KW];
+      if (valid) {
+        const float4* g4 = reinterpret_cast<const float4*>(
+            args.gate + static_cast<size_t>(qi) * args.gate_ld + static_cast<size_t>(h) * ATT_D + col0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = fmaxf(sv[i], sv[8 + i]);
-#pragma unroll
-        for (int c = 16; c < ATT_KW; c += 16) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mp[i] = fmax3(mp[i], sv[c + i], sv[c + 8 + i]);
+        for (int i = 0; i < ATT_KW / 4; ++i) {
+          const float4 t4 = g4[i];
+          gt[4 * i] = t4.x; gt[4 * i + 1] = t4.y; gt[4 * i + 2] = t4.z; gt[4 * i + 3] = t4.w;
         }
-        mt = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * c2;
-      }
-      // tile maximum over all parts of the row (-inf from a failed part),
-      // through slots of this tile's parity: a partner's next write to them
-      // (tile j + 2) comes after the barrier of tile j + 1, which this warp
-      // reaches only after reading. The barrier also orders every warp's S
-      // reads before any P write.
-      float* xs = xch + s * ATT_PARTS * ATT_BQ;
-      xs[part * ATT_BQ + row] = mt;
-      tc_fence_before();
-      named_bar_sync(bar_id, 32 * ATT_PARTS);
-      tc_fence_after();
 #pragma unroll
-      for (int o = 1; o < ATT_PARTS; ++o) mt = fmaxf(mt, xs[((part + o) % ATT_PARTS) * ATT_BQ + row]);
-      if (!ok) continue;
-      // lazy reference: move m only when this tile exceeds it by more than TAU2
-      const float mn = mt > m + ATT_TAU2 ? mt : m;
-      const float alpha = ex2_approx(m - mn);
-      const uint64_t nm = f2_pack(-mn, -mn);
-      uint64_t sp[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int c = 0; c < ATT_KW; c += 2) {
-        float a, b;
-        f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), cc, nm), a, b);
-        sv[c] = ex2_approx(a);
-        sv[c + 1] = ex2_approx(b);
-        sp[(c >> 1) & 3] = f2_add(sp[(c >> 1) & 3], f2_pack(sv[c], sv[c + 1]));
+        for (int i = 0; i < ATT_KW; ++i) gt[i] = __fdividef(1.0f, 1.0f + __expf(-gt[i]));
       }
-      float ps = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float a, b;
-        f2_unpack(sp[i], a, b);
-        ps += a + b;
-      }
-      l = l * alpha + ps;
-      m = mn;
-      // the O row is rescaled only after the previous P V has completed.
-      // o_done[b] completes once per tile of parity b. At tile j every P V
-      // up to j - 3 has completed (S_j was issued after P_{j-3} V_{j-3}) and
-      // P_{j+1} V_{j+1} cannot have, so the phase of P_{j-1} V_{j-1} is the
-      // current or the last one of o_done[(j-1)&1]: the parity wait is exact
-      // even when earlier tiles skipped it.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      const int tl = t0 + ntiles - 1;
+      if (ok) {
         bool od = false;
-        if (lane == 0)
-          od = mbar_wait_bounded(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, tmo, abort_flag);
+        if (lane == 0) od = mbar_wait_bounded(&o_done[tl & 1], (tl >> 1) & 1, tmo, abort_flag);
         ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
-        if (!ok) continue;
+      }
+      // row sums through their own slots: a partner rewrites its slot only
+      // at the next item's end, after the barriers of that item's tiles,
+      // which this warp reaches only after reading
+      float* xl = xch + 2 * ATT_PARTS * ATT_BQ;
+      xl[part * ATT_BQ + row] = l;
+      named_bar_sync(bar_id, 32 * ATT_PARTS);
+      float lt = l;
+#pragma unroll
+      for (int o = 1; o < ATT_PARTS; ++o) lt += xl[((part + o) % ATT_PARTS) * ATT_BQ + row];
+      if (ok) {
         tc_fence_after();
-#pragma unroll 1
+        const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+        const size_t ld = static_cast<size_t>(args.nq) * ATT_D;
+        __nv_bfloat16* orow = args.out + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
+#pragma unroll
         for (int c = 0; c < ATT_KW; c += 16) {
           float o[16];
           tmem_ld16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
+          if (valid) {
+            uint4 pk[2];
+            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= alpha;
-          tmem_st16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
+            for (int i = 0; i < 8; ++i)
+              p2[i] = __floats2bfloat162_rn(o[2 * i] * inv_l * gt[c + 2 * i],
+                                            o[2 * i + 1] * inv_l * gt[c + 2 * i + 1]);
+            uint4* d4 = reinterpret_cast<uint4*>(orow + c);
+            d4[0] = pk[0];
+            d4[1] = pk[1];
+          }
         }
       }
-      // this part of the P row as BF16 pairs (key 2i in the low half) into
-      // columns [KW/2 part, KW/2 part + KW/2) of this tile's S buffer
-      attn_st_p(tmem_base + lanebits + sb * 128 + part * (ATT_KW / 2), sv);
-      tmem_wait_st();
-      // P and the O rescale visible to the MMA
+      // this warp's O columns have been read: the next item may overwrite O
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
+      if (lane == 0) mbar_arrive(o_free);
+      t0 += ntiles;
     }
-    // final: O / l times the gate sigmoid(gate logit) (FP32), BF16; l summed
-    // over all parts. Every
-    // MMA has completed once mma_done (committed after the last one) has.
-    if (ok && ntiles > 0) {
-      bool od = false;
-      if (lane == 0) od = mbar_wait_bounded(mma_done, 0, tmo, abort_flag);
-      ok = __shfl_sync(0xffffffffu, od ? 1 : 0, 0) != 0;
-    }
-    // (the last tile's exchange used parity (ntiles - 1) & 1; these slots
-    // were last read at tile ntiles - 2, before that tile's barrier)
-    float* xl = xch + (ntiles & 1) * ATT_PARTS * ATT_BQ;
-    xl[part * ATT_BQ + row] = l;
-    named_bar_sync(bar_id, 32 * ATT_PARTS);
-    float lt = l;
-#pragma unroll
-    for (int o = 1; o < ATT_PARTS; ++o) lt += xl[((part + o) % ATT_PARTS) * ATT_BQ + row];
-    if (!ok) {
-      if (lane == 0) gemm_fail(abort_flag);
-    } else {
-      tc_fence_after();
-      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-      const bool valid = qi < args.T;
-      const size_t ld = static_cast<size_t>(args.nq) * ATT_D;
-      const float* gr = args.gate + static_cast<size_t>(qi) * args.gate_ld + static_cast<size_t>(h) * ATT_D + col0;
-      __nv_bfloat16* orow = args.out + static_cast<size_t>(qi) * ld + static_cast<size_t>(h) * ATT_D + col0;
-#pragma unroll 1
-      for (int c = 0; c < ATT_KW; c += 16) {
-        float o[16];
-        tmem_ld16(tmem_base + lanebits + ATT_O_COL + col0 + c, o);
-        if (valid) {
-          float gt[16];
-          const float4* g4 = reinterpret_cast<const float4*>(gr + c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 t4 = g4[i];
-            gt[4 * i] = t4.x; gt[4 * i + 1] = t4.y; gt[4 * i + 2] = t4.z; gt[4 * i + 3] = t4.w;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) gt[i] = __fdividef(1.0f, 1.0f + __expf(-gt[i]));
-          uint4 pk[2];
-          __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            p2[i] = __floats2bfloat162_rn(o[2 * i] * inv_l * gt[2 * i], o[2 * i + 1] * inv_l * gt[2 * i + 1]);
-          uint4* d4 = reinterpret_cast<uint4*>(orow + c);
-          d4[0] = pk[0];
-          d4[1] = pk[1];
-        }
-      }
-    }
+    if (!ok && lane == 0) gemm_fail(abort_flag);
   }
 
   tc_fence_before();

@@ -137,6 +137,17 @@ def test_nvfp4_forward_shape_sweep(B, T, H, I):
     _layer_check(B, wl, d)
 
 
+@pytest.mark.parametrize("T,H,I", [(90, 512, 512), (40, 768, 2560), (40, 512, 3840)])
+def test_nvfp4_down_two_tile_units(B, T, H, I):
+    """The decode-shaped NVFP4 down GEMM runs 256 hidden rows (two weight
+    tiles into two accumulators) per unit: about 22 tokens per expert (some
+    experts with two 32-token tiles), three units per expert (H = 768), and
+    long rows (I = 3840, 15 K-blocks of 256)."""
+    wl, d = S.make_custom(T=T, H=H, E=32, I=I, n_group=1, topk_group=1, top_k=8,
+                          seed=T + H + I + 5, device="cuda")
+    _layer_check(B, wl, d)
+
+
 @pytest.mark.parametrize("mode", ["hot_expert", "hot_group"])
 def test_nvfp4_forward_routing_edge_cases(B, mode):
     wl, d = S.make_custom(T=300, H=256, E=256, I=256, n_group=8, topk_group=4, top_k=8,

@@ -175,8 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg<MODE>::THREA
     if (lane == 0) {
       // weights at normal priority: an expert's second token group runs
       // the same weight slices in the adjacent units and re-reads them from
-      // L2 (as evict-first lines they were gone: 0.66 GB more DRAM reads
-      // per gate/up launch at T = 8192)
+      // L2 (as evict-first lines they were often gone already)
       const uint64_t pol_w = l2_policy_evict_normal();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;

@@ -277,11 +277,7 @@ __device__ __forceinline__ void attn_st_p(uint32_t taddr, const float (&p)[64]) 
   tmem_st32(taddr, pk);
 }
 
-// 184 registers a thread (352 x 184 = 64,768 of 65,536: one CTA per SM);
-// below that ptxas spilled the softmax's row state
-constexpr int ATT_MAXNREG = 184;
-static_assert(ATT_THREADS * ATT_MAXNREG <= 65536, "registers");
-__global__ void __maxnreg__(ATT_MAXNREG)
+__global__ void __launch_bounds__(ATT_THREADS, 1)
     flash_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_vt, const AttnArgs args) {
   using C = AttnCfg;

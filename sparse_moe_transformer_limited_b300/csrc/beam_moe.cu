@@ -824,6 +824,9 @@ beam_status_t run_experts(const beam_moe_params& prm, const Layout& L, const voi
   cb.cursor = arrive + 2 * static_cast<size_t>(T);
   cb.T = T;
   cb.expected = combine_expected(L.path, H, K, L.f4);
+  // weight-major kernels (few tokens): one grid-wide completion count
+  // instead of per-token arrivals
+  cb.grid_done = (L.path == PATH_W32 || L.path == PATH_W128) ? 1 : 0;
   cb.row_token = row_tok;
   cb.row_weight = row_w;
   cb.row_scale = quant ? qb.ascale : nullptr;

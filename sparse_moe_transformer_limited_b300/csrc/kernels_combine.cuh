@@ -54,6 +54,11 @@ struct CombineArgs {
   float eps, a, b;
   int resid;
   int out_f32;
+  // 0: per-token arrival counters and the completion list (above); else
+  // every epilogue warp of the grid counts itself done once after all its
+  // units, and once all have, the warps finalise the T tokens between them
+  // (combine_grid_finish; the weight-major kernel, where tokens are few)
+  int grid_done;
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
@@ -166,6 +171,34 @@ __device__ __forceinline__ bool combine_drain_warp(const CombineArgs& c, int lan
     __threadfence();
     combine_finalize_token(c, t, lane);
   }
+}
+
+// Grid-wide completion (grid_done): called by every epilogue warp of the
+// grid once its own units are done; warp wid of nwarps finalises tokens wid,
+// wid + nwarps, ... after all nwarps warps have counted themselves in
+// cursor[0] (each after a fence that covers its reductions). The wait is
+// bounded; returns false on a timeout. Every CTA of the grid is resident
+// (one per SM), as the completion list's waits also assume.
+__device__ __forceinline__ bool combine_grid_finish(const CombineArgs& c, int lane, int wid,
+                                                    int nwarps, unsigned long long timeout_ns,
+                                                    const volatile int* abort_flag) {
+  __threadfence();
+  __syncwarp();
+  int n = 0;
+  if (lane == 0) {
+    atomicAdd(c.cursor, 1);
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(n) : "l"(c.cursor) : "memory");
+      if (n >= nwarps || *abort_flag || globaltimer_ns() - t0 > timeout_ns) break;
+      __nanosleep(256);
+    }
+  }
+  n = __shfl_sync(0xffffffffu, n, 0);
+  if (n < nwarps) return false;
+  __threadfence();
+  for (int t = wid; t < c.T; t += nwarps) combine_finalize_token(c, t, lane);
+  return true;
 }
 
 // Before the down GEMM: o = 0 (n4 float4), counters = 0, list entries = -1,

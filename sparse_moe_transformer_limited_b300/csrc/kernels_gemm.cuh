@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
-      if (MODE == 1) {
+      if (MODE == 1 && !args.comb.grid_done) {
         // one arrival per token of the unit (32 columns per call)
 #pragma unroll 1
         for (int c = 0; c < un.z; c += 32) {
@@ -434,8 +434,13 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     // finalise completed tokens (rows) once this warp's own units are done
-    if (MODE == 1 && !combine_drain_warp(args.comb, lane, tmo, abort_flag) && lane == 0)
-      gemm_fail(abort_flag);
+    if (MODE == 1) {
+      const bool fin = args.comb.grid_done
+                           ? combine_grid_finish(args.comb, lane, static_cast<int>(blockIdx.x) * 4 + (warp - 2),
+                                                 static_cast<int>(gridDim.x) * 4, tmo, abort_flag)
+                           : combine_drain_warp(args.comb, lane, tmo, abort_flag);
+      if (!fin && lane == 0) gemm_fail(abort_flag);
+    }
   }
 
   tc_fence_before();

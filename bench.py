@@ -190,8 +190,8 @@ TENSOR_RATIO = {"bf16": 1, "fp8": 2, "nvfp4": 6}
 def _algorithmic(wl, counts, kind="bf16"):
     """Algorithmic bytes / FLOPs (what the method must move and compute): each
     touched expert's weights once (WEIGHT_BYTES) plus the layer's BF16 input
-    or output; the intermediates (permuted x, SwiGLU activations, per-pair
-    outputs) are not counted."""
+    or output; the intermediates (permuted x, SwiGLU activations, the FP32
+    combine rows) are not counted."""
     touched = int((counts > 0).sum())
     R = wl.T * wl.top_k
     eb, sc = WEIGHT_BYTES[kind]

@@ -210,16 +210,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ss_pair<F8>(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-          mma_commit_pair_mc(&empty[stage], static_cast<uint16_t>(0x3));
+          mma_commit_pair_both(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit_pair_mc(&tfull[buf], static_cast<uint16_t>(0x3));
+        mma_commit_pair_both(&tfull[buf]);
       }
-      mma_commit_pair_mc(mma_done, static_cast<uint16_t>(0x1));
+      mma_commit_pair_to(mma_done, 0);
       const volatile int never = 0;
       if (!mbar_wait_bounded(mma_done, 0, tmo, &never)) gemm_fail(abort_flag);
     }

@@ -267,16 +267,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg<MODE>::THREA
             mma_ss_pair<F8>(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
             if (two) mma_ss_pair<F8>(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
-          mma_commit_pair_mc(&empty[stage], static_cast<uint16_t>(0x3));
+          mma_commit_pair_both(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit_pair_mc(tfull, static_cast<uint16_t>(0x3));
+        mma_commit_pair_both(tfull);
       }
-      mma_commit_pair_mc(mma_done, static_cast<uint16_t>(0x1));
+      mma_commit_pair_to(mma_done, 0);
       const volatile int never = 0;
       if (!mbar_wait_bounded(mma_done, 0, tmo, &never)) gemm_fail(abort_flag);
     }

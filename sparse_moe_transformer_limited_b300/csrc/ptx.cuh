@@ -242,14 +242,18 @@ __device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Completion of the issuing thread's pair MMAs, arriving on the barrier at the
-// same offset in every CTA named in `mask`.
-__device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t mask) {
+// Completion of the issuing thread's pair MMAs, arriving on the barrier at
+// the same offset in CTA `rank` of the pair (one commit per CTA to signal).
+__device__ __forceinline__ void mma_commit_pair_to(uint64_t* bar, uint32_t rank) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          mapa_shared(bar, rank))
       : "memory");
+}
+// ... on the barrier of both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair_both(uint64_t* bar) {
+  mma_commit_pair_to(bar, 0);
+  mma_commit_pair_to(bar, 1);
 }
 
 // Arrive once on `bar` when all previously issued tcgen05.mma of this thread

@@ -30,13 +30,13 @@
 // epilogue has read them (it releases TMEM before its stores complete and
 // before it finalises tokens).
 //
-// Roles per CTA: warp 0 TMA producer; warp 1 TMEM allocation (both CTAs)
-// and, in the even CTA, the MMA issuer; then the epilogue warps, NSUB per
-// TMEM lane quarter (warp % 4), each taking every NSUB-th 16-column chunk
-// (NSUB = 2 for gate/up, 4 for down). Both CTAs' TMA loads count their bytes
-// on the even CTA's `full` barrier; the MMA commits arrive on the `empty` and
-// `tmem_full` barriers of both CTAs; all epilogue warps of both CTAs release
-// TMEM on the even CTA's `tmem_empty` barrier. All
+// Roles per CTA (576 threads): warp 0 TMA producer; warp 1 TMEM allocation
+// (both CTAs) and, in the even CTA, the MMA issuer; then sixteen epilogue
+// warps, four per TMEM lane quarter (warp % 4), each taking every fourth
+// 16-column chunk. Both CTAs' TMA loads count their bytes on the even CTA's
+// `full` barrier; the MMA commits arrive on the `empty` and `tmem_full`
+// barriers of both CTAs; all epilogue warps of both CTAs release TMEM on the
+// even CTA's `tmem_empty` barrier. All
 // waits are bounded; the CTAs meet at a cluster barrier before TMEM is freed
 // and before exit.
 #pragma once
@@ -85,10 +85,12 @@ struct WideCfgT {
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
-// Gate/up: two epilogue warps per lane quarter. Down: four, so that more of
-// the epilogue's global reductions are in flight while TMEM is held.
+// Four epilogue warps per lane quarter in both GEMMs: TMEM holds one unit,
+// so the epilogue (SwiGLU and the act stores; the combine's reductions)
+// stalls the next unit's MMAs, and more warps shorten it (E4M3 gate/up, whose
+// units are half as long, 2.14 -> 1.97 ms at T = 8192; BF16 unchanged).
 template <int MODE>
-using WideCfg = WideCfgT<MODE == 0 ? 8 : 16>;
+using WideCfg = WideCfgT<16>;
 
 // Token rows of one CTA for a unit of N tokens: N/2 rows, a multiple of 8,
 // loaded as 64-, 32-, 16- and 8-row boxes (the binary digits of N/2).

@@ -335,32 +335,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg<MODE>::THREA
           sg = args.w_scale0[wi];
           su = args.w_scale1[wi];
         }
-        // two local chunks (k, k + 1) of both accumulators per TMEM wait
+        // SwiGLU of this warp's chunks into registers (BF16 pairs; two local
+        // chunks of both accumulators per TMEM wait), then TMEM is released
+        // before the global stores, so the next unit's MMAs overlap them
+        uint32_t ap[C::NCH][8];
 #pragma unroll
         for (int k = 0; k < C::NCH; k += 2) {
           const int c0 = sub + C::NSUB * k;
-          if (c0 >= nch) break;
-          const int c1 = c0 + C::NSUB;
-          float g0[16], u0[16], g1[16], u1[16];
-          tmem_ld16x4(tq + c0 * 16, tq + C::D1_COL + c0 * 16, tq + c1 * 16,
-                      tq + C::D1_COL + c1 * 16, g0, u0, g1, u1);
+          if (c0 < nch) {
+            const int c1 = c0 + C::NSUB;
+            float g0[16], u0[16], g1[16], u1[16];
+            tmem_ld16x4(tq + c0 * 16, tq + C::D1_COL + c0 * 16, tq + c1 * 16,
+                        tq + C::D1_COL + c1 * 16, g0, u0, g1, u1);
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = h2 ? c1 : c0;
-            const float* g = h2 ? g1 : g0;
-            const float* v = h2 ? u1 : u0;
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const float* g = h2 ? g1 : g0;
+              const float* v = h2 ? u1 : u0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int tok = c * 16 + j;
-              float gj = g[j], uj = v[j];
-              if (F8) {
-                const float sx = __shfl_sync(0xffffffffu, cfr[(k + h2) >> 1], (((k + h2) & 1) << 4) + j);
-                gj *= sg * sx;
-                uj *= su * sx;
-              }
-              if (tok < n) {
-                const float a = __fdividef(gj, 1.0f + __expf(-gj)) * uj;
-                args.act[static_cast<size_t>(un.y + tok) * args.act_ld + i] = __float2bfloat16_rn(a);
+              for (int j = 0; j < 16; j += 2) {
+                float a2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  float gj = g[j + e], uj = v[j + e];
+                  if (F8) {
+                    const float sx = __shfl_sync(0xffffffffu, cfr[(k + h2) >> 1],
+                                                 (((k + h2) & 1) << 4) + j + e);
+                    gj *= sg * sx;
+                    uj *= su * sx;
+                  }
+                  a2[e] = __fdividef(gj, 1.0f + __expf(-gj)) * uj;
+                }
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(a2[0], a2[1]);
+                ap[k + h2][j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
               }
             }
           }
@@ -368,6 +374,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WideCfg<MODE>::THREA
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty, 0));
+        // act[t, i] for the chunks' tokens (a warp writes 64 contiguous bytes
+        // of a token row per store)
+#pragma unroll
+        for (int k = 0; k < C::NCH; ++k) {
+          const int c = sub + C::NSUB * k;
+          if (c >= nch) break;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c * 16 + j;
+            if (tok < n) {
+              const uint32_t w2 = ap[k][j >> 1];
+              const uint16_t h = static_cast<uint16_t>((j & 1) ? (w2 >> 16) : (w2 & 0xFFFFu));
+              reinterpret_cast<uint16_t*>(args.act)[static_cast<size_t>(un.y + tok) * args.act_ld + i] = h;
+            }
+          }
+        }
       } else {
         const CombineArgs& cb = args.comb;
         const int h0 = un.w * 512 + static_cast<int>(crank) * 128 + rloc;

@@ -206,6 +206,35 @@ def _algorithmic(wl, counts, kind="bf16"):
                 layer_flops=gu_flops + dn_flops + 2.0 * wl.T * wl.H * wl.E)
 
 
+def gemm_roofline(kname, nbytes, flops, launch_ms, peaks, dtype, traffic):
+    """Roofline of one GEMM launch against the bound that binds it: the larger
+    of the two least times, algorithmic bytes / measured copy rate and
+    algorithmic FLOPs / measured sustained tensor rate (the expert GEMMs run
+    inside loops of back-to-back steps, seconds under the board's power cap).
+    Decode-sized launches are bound by their weight bytes; prefill BF16 by
+    FLOPs; with few tokens per expert (skewed routing) or packed 4-bit
+    weights the bytes can bind at prefill sizes too. The other bound's
+    fraction is given beside it."""
+    s = launch_ms / 1e3
+    hbm = {"bound": "hbm", "achieved": round(nbytes / s / 1e9, 1), "peak": peaks["hbm"],
+           "unit": "GB/s", "frac": round(nbytes / s / 1e9 / peaks["hbm"], 4),
+           "peak_source": peaks["source"] + " hbm_gbs", "algorithmic_bytes_per_launch": nbytes}
+    tc = {"bound": "tensor", "achieved": round(flops / s / 1e12, 1),
+          "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+          "frac": round(flops / s / 1e12 / peaks["bf16_sustained"], 4),
+          "peak_source": (peaks["source"] + " bf16_tflops_sustained (timed inside a long step)"
+                          + peaks.get("tensor_note", "")),
+          "frac_of_burst": round(flops / s / 1e12 / peaks["bf16"], 4),
+          "algorithmic_flops_per_launch": flops}
+    t_bytes = nbytes / (peaks["hbm"] * 1e9)
+    t_flops = flops / (peaks["bf16_sustained"] * 1e12)
+    roof, other = (hbm, tc) if t_bytes >= t_flops else (tc, hbm)
+    roof = dict({"kernel": kname}, **roof)
+    roof.update(dtype=dtype, traffic=traffic, launch_ms=round(launch_ms, 4),
+                other_bound={"bound": other["bound"], "frac": other["frac"]})
+    return roof
+
+
 def _traffic_for(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -341,29 +370,10 @@ def run_ours(args, rank, world, local_rank, kind="bf16"):
                      tensor_note=f" x {rt} (nominal {kind}/BF16 dense ratio)")
     gu_ms = prof["expert_gemm_gateup_swiglu"][0] / prof["expert_gemm_gateup_swiglu"][1]
     dn_ms = prof["expert_gemm_down"][0] / prof["expert_gemm_down"][1]
-    decode_like = wl.T * wl.top_k <= 24 * wl.E
     kname = "expert_gemm_gateup_swiglu"
-    if decode_like:
-        achieved = alg["gu_bytes"] / (gu_ms / 1e3) / 1e9
-        roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
-                "peak_source": peaks["source"] + " hbm_gbs",
-                "traffic": _traffic_for(kname, wl.name if kind == "bf16" else f"{wl.name}_{kind}"),
-                "algorithmic_bytes_per_launch": alg["gu_bytes"], "launch_ms": round(gu_ms, 4)}
-    else:
-        # the kernel runs inside a loop of back-to-back steps (seconds under
-        # the board's power cap), so its peak is the sustained GEMM rate; the
-        # burst fraction is given beside it
-        achieved = alg["gu_flops"] / (gu_ms / 1e3) / 1e12
-        roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
-                "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_sustained"], 4),
-                "peak_source": (peaks["source"] + " bf16_tflops_sustained (timed inside a long step)"
-                                + peaks.get("tensor_note", "")),
-                "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[kind],
-                "frac_of_burst": round(achieved / peaks["bf16"], 4),
-                "traffic": _traffic_for(kname, wl.name if kind == "bf16" else f"{wl.name}_{kind}"),
-                "algorithmic_flops_per_launch": alg["gu_flops"], "launch_ms": round(gu_ms, 4)}
+    roof = gemm_roofline(kname, alg["gu_bytes"], alg["gu_flops"], gu_ms, peaks,
+                         {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[kind],
+                         _traffic_for(kname, wl.name if kind == "bf16" else f"{wl.name}_{kind}"))
     layer = {"hbm_frac": round(alg["layer_bytes"] / (ms_step / 1e3) / 1e9 / peaks["hbm"], 4),
              "tensor_frac": round(alg["layer_flops"] / (ms_step / 1e3) / 1e12
                                   / peaks["bf16_sustained"], 4),
@@ -664,7 +674,7 @@ def main():
             split of the secondaries is left out to keep the line short)."""
             ro = rr["roofline"]
             keep = ("bound", "achieved", "peak", "unit", "frac", "frac_of_burst", "traffic",
-                    "launch_ms", "dtype")
+                    "launch_ms", "dtype", "other_bound")
             return {"value": round(rr["value"], 1), "unit": "tokens/s",
                     "ms_per_step": round(rr["ms_step"], 4), "e2e": round(rr["e2e"], 1),
                     "roofline": {k: ro[k] for k in keep if k in ro},

@@ -84,3 +84,39 @@ def test_cpu_baseline_runs_for_its_minimum_time(bench):
     assert runs == 3
     v, runs, dt = bench.time_oracle(run, 4, min_s=0.0)
     assert runs == 1
+
+
+def _fake_peaks():
+    return {"hbm": 6500.0, "bf16": 1800.0, "bf16_sustained": 1355.0, "source": "measured"}
+
+
+@pytest.mark.parametrize("name,kind,touched,want", [
+    ("decode", "bf16", 220, "hbm"),        # 11.5 GB of weights, 0.04 TFLOP
+    ("prefill", "bf16", 256, "tensor"),    # 13.5 GB: 2.08 ms at the copy rate; 3.44 TFLOP: 2.54 ms
+    ("skew", "bf16", 256, "hbm"),          # T = 4096: 13.5 GB (2.07 ms) against 1.72 TFLOP (1.27 ms)
+    ("prefill", "fp8", 256, "tensor"),     # 6.7 GB (1.04 ms) against 3.44 TFLOP at 2 x 1355 (1.27 ms)
+    ("prefill", "nvfp4", 256, "hbm"),      # 3.8 GB (0.58 ms) against 3.44 TFLOP at 6 x 1355 (0.42 ms)
+])
+def test_roofline_takes_the_binding_bound(bench, name, kind, touched, want):
+    """The roofline of the gate/up launch is the bound with the larger least
+    time (algorithmic bytes / copy rate against FLOPs / sustained tensor
+    rate), whatever the launch takes; the other bound's fraction is kept."""
+    wl = S.WORKLOADS[name]
+    a = bench._algorithmic(wl, _counts(wl.E, touched), kind)
+    peaks = _fake_peaks()
+    if kind != "bf16":
+        rt = bench.TENSOR_RATIO[kind]
+        peaks = dict(peaks, bf16=rt * peaks["bf16"], bf16_sustained=rt * peaks["bf16_sustained"])
+    t_bytes = a["gu_bytes"] / (peaks["hbm"] * 1e9)
+    t_flops = a["gu_flops"] / (peaks["bf16_sustained"] * 1e12)
+    for launch_s in (1.05 * max(t_bytes, t_flops), 3.0 * max(t_bytes, t_flops)):
+        r = bench.gemm_roofline("k", a["gu_bytes"], a["gu_flops"], launch_s * 1e3, peaks, kind, None)
+        assert r["bound"] == want
+        assert r["other_bound"]["bound"] == ("tensor" if want == "hbm" else "hbm")
+        # the binding bound's fraction is the larger one, and both follow from the time
+        f_bytes = a["gu_bytes"] / launch_s / 1e9 / peaks["hbm"]
+        f_flops = a["gu_flops"] / launch_s / 1e12 / peaks["bf16_sustained"]
+        got = {r["bound"]: r["frac"], r["other_bound"]["bound"]: r["other_bound"]["frac"]}
+        assert got["hbm"] == pytest.approx(f_bytes, abs=1e-4)
+        assert got["tensor"] == pytest.approx(f_flops, abs=1e-4)
+        assert r["frac"] >= r["other_bound"]["frac"]

@@ -369,7 +369,6 @@ def run_ours(args, rank, world, local_rank, kind="bf16"):
         peaks = dict(peaks, bf16=rt * peaks["bf16"], bf16_sustained=rt * peaks["bf16_sustained"],
                      tensor_note=f" x {rt} (nominal {kind}/BF16 dense ratio)")
     gu_ms = prof["expert_gemm_gateup_swiglu"][0] / prof["expert_gemm_gateup_swiglu"][1]
-    dn_ms = prof["expert_gemm_down"][0] / prof["expert_gemm_down"][1]
     kname = "expert_gemm_gateup_swiglu"
     roof = gemm_roofline(kname, alg["gu_bytes"], alg["gu_flops"], gu_ms, peaks,
                          {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[kind],

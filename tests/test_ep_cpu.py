@@ -75,7 +75,7 @@ def _weights():
     return wr, wg, wu, wd
 
 
-def _rank(rank, world, port, results):
+def _rank(rank, world, port, results, Ts=None):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -87,7 +87,7 @@ def _rank(rank, world, port, results):
         per = E // world
         mine = slice(rank * per, (rank + 1) * per)
         local = LocalExperts(torch.tensor(wg[mine]), torch.tensor(wu[mine]), torch.tensor(wd[mine]))
-        T = 40 + 17 * rank                            # ranks hold different token counts
+        T = 40 + 17 * rank if Ts is None else Ts[rank]   # ranks hold different token counts
         h = O.bf16_round(np.random.default_rng(100 + rank).standard_normal((T, H))).astype(np.float64)
         worst = 0.0
         for flags, k in ((0, 0), (1, 9)):            # plain output; pre-norm + residual k = 9
@@ -97,7 +97,9 @@ def _rank(rank, world, port, results):
                                 topk_group=4, top_k=TOPK, scale=2.5, eps=1e-6,
                                 pre_norm=bool(flags), residual_k=k)
             want = ref["h"] if k else ref["out"]
-            worst = max(worst, float(np.max(np.abs(got.numpy() - want)) / np.sqrt(np.mean(want ** 2))))
+            assert got.shape == (T, H)
+            if T:
+                worst = max(worst, float(np.max(np.abs(got.numpy() - want)) / np.sqrt(np.mean(want ** 2))))
         results[rank] = worst
     finally:
         dist.destroy_process_group()
@@ -119,3 +121,35 @@ def test_expert_parallel_matches_single_process_oracle(world):
         worst = dict(results)
     assert sorted(worst) == list(range(world))
     assert max(worst.values()) < 1e-9, worst
+
+
+def test_expert_parallel_with_a_rank_without_tokens():
+    """A rank with no tokens still takes part in every exchange (zero-row
+    splits both ways) and its owners' experts serve the other ranks."""
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        mp.start_processes(_rank, args=(2, _free_port(), results, (0, 73)), nprocs=2, join=True,
+                           start_method="spawn")
+        worst = dict(results)
+    assert sorted(worst) == [0, 1]
+    assert max(worst.values()) < 1e-9, worst
+
+
+def test_expert_parallel_rejects_a_wrong_local_expert_count():
+    """A rank must hold exactly E / P experts: the call raises before any
+    exchange."""
+    from sparse_moe_transformer_limited_b300 import _native as N
+    from sparse_moe_transformer_limited_b300.expert_parallel import LocalExperts, moe_forward_ep
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(_free_port())
+    dist.init_process_group("gloo", rank=0, world_size=1)
+    try:
+        wr, wg, wu, wd = _weights()
+        local = LocalExperts(torch.tensor(wg[:3]), torch.tensor(wu[:3]), torch.tensor(wd[:3]))
+        p = N.make_params(4, H, E, I, 8, 4, TOPK, 2.5, 1e-6, 0, 0)
+        with pytest.raises(ValueError, match="holds 3 experts"):
+            moe_forward_ep(p, torch.zeros((4, H), dtype=torch.float64), torch.tensor(wr), local,
+                           ops=OracleOps())
+    finally:
+        dist.destroy_process_group()

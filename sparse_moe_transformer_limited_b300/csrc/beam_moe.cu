@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -160,7 +161,9 @@ constexpr int kRouterKSplit = 2;  // K-slices of the tensor-core router GEMM
 // is small. Must divide H / 32 and leave at least 64 columns per slice.
 int choose_router_ks(const beam_moe_params& p, int num_sms) {
   if (router_on_tensor_cores(p)) return kRouterKSplit;
-  const int tiles = ((p.T + beam::RL_BT - 1) / beam::RL_BT) * ((p.E + beam::RL_BE - 1) / beam::RL_BE);
+  // (an empty batch has no tiles; count one so the split is defined)
+  const int tiles = std::max(1, ((p.T + beam::RL_BT - 1) / beam::RL_BT) *
+                                    ((p.E + beam::RL_BE - 1) / beam::RL_BE));
   const int want = (2 * num_sms + tiles - 1) / tiles;
   const int nk = p.H / 32;
   int best = 1;

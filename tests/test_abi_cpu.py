@@ -131,6 +131,17 @@ def test_empty_batch_is_a_no_op():
     assert B.lib().beam_moe_forward(ctypes.byref(p), *([None] * 12), 0, None) == 0
 
 
+@pytest.mark.parametrize("flags", [0, B.FLAG_PRE_NORM, B.FLAG_FP8_EXPERTS, B.FLAG_NVFP4_EXPERTS,
+                                   B.FLAG_RETURN_SCORES])
+def test_empty_batch_workspace_queries(flags):
+    """Sizing a workspace for T = 0 (a rank without tokens, say) returns a
+    size and a layout; routing an empty batch is a no-op."""
+    p = _p(T=0, flags=flags)
+    assert B.workspace_size(p) > 0
+    assert len(B.workspace_layout(p)) > 0
+    assert B.lib().beam_moe_route(ctypes.byref(p), *([None] * 8), ctypes.c_size_t(0), None) == 0
+
+
 def test_fp8_workspace_holds_e4m3_buffers():
     plain = B.workspace_layout(_p())
     f8 = B.workspace_layout(_p(flags=B.FLAG_FP8_EXPERTS))

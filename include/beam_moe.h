@@ -475,7 +475,8 @@ beam_status_t beam_moe_forward_routed(const beam_moe_params* p, const void* x_in
  *   send_counts [n_ranks] int32 out: rows for each rank (contiguous blocks
  *              in rank order)
  *   workspace  beam_moe_workspace_size(p) bytes (may be the router's)
- * Device pointers; asynchronous on `stream`. */
+ * Device pointers; asynchronous on `stream`. With T = 0 the call only
+ * zeroes send_counts (when it is given). */
 beam_status_t beam_ep_dispatch(const beam_moe_params* p, int n_ranks, const void* x,
                                const int32_t* topk_idx, void* send_x, int32_t* send_expert,
                                int32_t* pair_row, int32_t* send_counts, void* workspace,

@@ -1723,7 +1723,13 @@ extern "C" beam_status_t beam_ep_dispatch(const beam_moe_params* p, int n_ranks,
   if (s != BEAM_OK) return s;
   if (n_ranks <= 0 || p->E % n_ranks)
     return fail(BEAM_ERR_INVALID_ARG, "n_ranks=%d must divide E=%d", n_ranks, p->E);
-  if (p->T == 0) return BEAM_OK;
+  if (p->T == 0) {
+    // a rank without tokens sends no rows to every rank
+    if (send_counts != nullptr)
+      BEAM_CUDA_TRY(cudaMemsetAsync(send_counts, 0, static_cast<size_t>(n_ranks) * sizeof(int32_t),
+                                    static_cast<cudaStream_t>(stream)));
+    return BEAM_OK;
+  }
   if (!x || !topk_idx || !send_x || !send_expert || !pair_row || !send_counts || !workspace)
     return fail(BEAM_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!aligned16(x) || !aligned16(send_x) || !aligned16(workspace))

@@ -32,8 +32,13 @@ def B():
 def _rank_inputs(P, H, I, E, seeds, Ts):
     wl, d = S.make_custom(T=Ts[0], H=H, E=E, I=I, n_group=8, topk_group=4, top_k=8, seed=seeds[0],
                           device="cuda")
-    xs = [d["x"]] + [S.make_custom(T=T, H=H, E=E, I=I, n_group=8, topk_group=4, top_k=8, seed=s,
-                                   device="cuda")[1]["x"] for T, s in zip(Ts[1:], seeds[1:])]
+
+    def x_of(T, s):
+        if T == 0:          # a rank without tokens
+            return torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+        return S.make_custom(T=T, H=H, E=E, I=I, n_group=8, topk_group=4, top_k=8, seed=s,
+                             device="cuda")[1]["x"]
+    xs = [d["x"]] + [x_of(T, s) for T, s in zip(Ts[1:], seeds[1:])]
     return wl, d, xs
 
 
@@ -84,13 +89,18 @@ def _ep_emulated(B, P, wl, d, xs, flags, k):
     return outs
 
 
-@pytest.mark.parametrize("P", [2, 4])
+@pytest.mark.parametrize("P,Ts", [(2, (300, 77)), (4, (300, 77, 512, 5)), (4, (300, 0, 512, 5))])
 @pytest.mark.parametrize("resid", [False, True])
-def test_ep_emulated_matches_single_device(B, P, resid):
-    wl, d, xs = _rank_inputs(P, 256, 256, 256, [11, 12, 13, 14][:P], [300, 77, 512, 5][:P])
+def test_ep_emulated_matches_single_device(B, P, Ts, resid):
+    """(the last case has a rank without tokens: it sends and receives zero
+    rows, and its experts still serve the others)"""
+    wl, d, xs = _rank_inputs(P, 256, 256, 256, [11, 12, 13, 14][:P], list(Ts))
     flags, k = (B.FLAG_PRE_NORM, 9) if resid else (B.FLAG_FP32_OUT, 0)
     outs = _ep_emulated(B, P, wl, d, xs, flags, k)
     for x, (out, idx, w) in zip(xs, outs):
+        if x.shape[0] == 0:
+            assert out.shape == (0, wl.H) and idx.shape[0] == 0
+            continue
         p = B.make_params(x.shape[0], wl.H, wl.E, wl.I, 8, 4, 8, 2.5, 1e-6, k, flags)
         i2 = torch.empty_like(idx)
         w2 = torch.empty_like(w)

@@ -336,3 +336,19 @@ def test_expert_parallel_entry_points_check_args_on_host():
     assert comb(4, 33, 5120, 0, 0) == 1
     assert comb(4, 8, 5000, 0, 0) == 2
     assert comb(0, 8, 5120, 50, 0) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every entry point raises; nothing falls back
+    to another implementation."""
+    from sparse_moe_transformer_limited_b300 import _native
+    monkeypatch.setattr(_native, "_lib", None)
+    monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libbeam_moe.so"))
+    with pytest.raises(ImportError, match="is missing"):
+        _native.lib()
+    with pytest.raises(ImportError):
+        _native.workspace_size(_p())
+    import torch
+    x = torch.zeros((4, 256), dtype=torch.bfloat16)
+    with pytest.raises(ImportError):
+        _native.route(_p(T=4, H=256), x, torch.zeros((256, 256)))

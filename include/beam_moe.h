@@ -30,6 +30,10 @@
  *     timed out) set a per-device flag read back by beam_status().
  *   - beam_last_error_string() describes the last failure of the calling
  *     host thread.
+ *   - An empty batch (T = 0) is valid everywhere: size and layout queries
+ *     answer, the calls check their other arguments and return BEAM_OK
+ *     without enqueuing work (pointers may then be NULL), except
+ *     beam_ep_dispatch, which zeroes its send counts.
  */
 #ifndef BEAM_MOE_H_
 #define BEAM_MOE_H_

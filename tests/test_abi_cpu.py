@@ -352,3 +352,35 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     x = torch.zeros((4, 256), dtype=torch.bfloat16)
     with pytest.raises(ImportError):
         _native.route(_p(T=4, H=256), x, torch.zeros((256, 256)))
+
+
+def test_empty_batch_every_entry_point():
+    """T = 0 (or zero rows) returns BEAM_OK from every compute entry point
+    with NULL buffers: nothing is enqueued."""
+    lib = B.lib()
+    n0 = ctypes.c_size_t(0)
+    L0 = ctypes.c_longlong(0)
+    f8 = _p(T=0, flags=B.FLAG_FP8_EXPERTS)
+    f4 = _p(T=0, flags=B.FLAG_NVFP4_EXPERTS)
+    dense = B.DenseParams(0, 5120, 12288, 1e-6, 3, 0)
+    dense8 = B.DenseParams(0, 5120, 12288, 1e-6, 3, B.FLAG_FP8_EXPERTS)
+    dense4 = B.DenseParams(0, 5120, 12288, 1e-6, 3, B.FLAG_NVFP4_EXPERTS)
+    attn = B.make_attn_params(T=0)
+    calls = {
+        "route": lib.beam_moe_route(ctypes.byref(_p(T=0)), *([None] * 8), n0, None),
+        "forward": lib.beam_moe_forward(ctypes.byref(_p(T=0)), *([None] * 12), n0, None),
+        "forward_fp8": lib.beam_moe_forward_fp8(ctypes.byref(f8), *([None] * 15), n0, None),
+        "forward_nvfp4": lib.beam_moe_forward_nvfp4(ctypes.byref(f4), *([None] * 18), n0, None),
+        "dense": lib.beam_dense_mlp_forward(ctypes.byref(dense), *([None] * 8), n0, None),
+        "dense_fp8": lib.beam_dense_mlp_forward_fp8(ctypes.byref(dense8), *([None] * 11), n0, None),
+        "dense_nvfp4": lib.beam_dense_mlp_forward_nvfp4(ctypes.byref(dense4), *([None] * 14), n0,
+                                                        None),
+        "attention": lib.beam_attention_forward(ctypes.byref(attn), *([None] * 9), n0, None),
+        "quantize_e4m3": lib.beam_quantize_e4m3_rows(None, L0, 5120, None, None, None),
+        "quantize_nvfp4": lib.beam_quantize_nvfp4(None, L0, 5120, 128, None, None, None, None),
+        "residual": lib.beam_residual_step(None, None, 0, 5120, 2, None, ctypes.c_float(1e-6), 1,
+                                           0, None, None),
+        "ep_combine": lib.beam_ep_combine(0, 8, 5120, None, None, None, None, None,
+                                          ctypes.c_float(1e-6), 9, 0, None, None),
+    }
+    assert all(v == 0 for v in calls.values()), calls
